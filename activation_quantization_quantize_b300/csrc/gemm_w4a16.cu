@@ -1,0 +1,384 @@
+// gemm_w4a16.cu -- group-wise INT4 weights x bf16 activations.
+//
+// Method ("第11章 模型量化与压缩" 11.1.6, INT4 per-group worked case): the weight
+// W [N x K] is stored as 4-bit codes in row-wise groups of g with a binary16
+// scale (and, for asymmetric codes, a 4-bit zero point) per group; at
+// inference each weight is dequantized to the 16-bit compute type,
+// w^ = bf16(fl(s * (q - z))), and multiplied with bf16 activations, summing in
+// binary32.
+//
+// Packed layout (version 1), built by k_pack_w4 from the canonical codes:
+//   codes  [N/16][K/64][32 lanes][4 words]: the 16 x 64 tile of one warp-wide
+//          chunk.  Lane l = 4*gq + t owns rows gq and gq+8 of the tile and the
+//          16 consecutive k = 16*t .. 16*t+15 of the chunk.  Word j of the lane
+//          holds k = 16*t + 4*j + {0..3} of both rows, nibble layout
+//            nib 0/4: row gq,   k+0/k+1     nib 1/5: row gq+8, k+0/k+1
+//            nib 2/6: row gq,   k+2/k+3     nib 3/7: row gq+8, k+2/k+3
+//          which is an m16n8k16 A fragment (a0..a7) of the k-permutation
+//          "logical k (2t+e) <-> real 16t+4j+e, (2t+8+e) <-> real 16t+4j+2+e".
+//          Nibble values are unsigned: q for UINT4, q+8 for symmetric INT4.
+//   scales [N/16][K/g][16] binary16, rows in the order 0,8,1,9,...,7,15 so a
+//          lane reads the (gq, gq+8) pair as one 32-bit word.
+//   zeros  [N/16][K/g][8] bytes: byte i = z(row i) | z(row i+8) << 4 (asym only).
+//
+// The dequantization w^ = bf16_rn(s*d), d = u - z, is formed with packed bf16
+// arithmetic: s = s_hi + s_lo with s_hi = bf16_rn(s); s_lo*d is exact in bf16
+// (at most 2 + 4 significant bits), so fma.rn.bf16x2(d, s_hi, s_lo*d) rounds
+// the exact product s*d once -- bit-identical to rounding fl(s*d).
+#include "qlin_common.cuh"
+#include "qlin_internal.h"
+
+namespace qlin {
+
+// ------------------------------------------------------------------ layout
+void w4_layout(int64_t N, int64_t K, int group, int asym, qlin_w4_header* h) {
+    auto up = [](uint64_t v) { return (v + 255) & ~(uint64_t)255; };
+    h->magic = QLIN_W4_MAGIC;
+    h->version = QLIN_W4_VERSION;
+    h->N = N;
+    h->K = K;
+    h->group = group;
+    h->asym = asym;
+    uint64_t off = up(sizeof(qlin_w4_header));
+    h->codes_off = off;
+    off = up(off + (uint64_t)N * K / 2);
+    h->scales_off = off;
+    off = up(off + (uint64_t)N * (K / group) * 2);
+    h->zeros_off = asym ? off : 0;
+    if (asym) off = up(off + (uint64_t)(N / 16) * (K / group) * 8);
+    h->total_bytes = off;
+}
+
+// ------------------------------------------------------------------ pack
+// One thread per (n_tile, chunk, lane): gathers the 32 nibbles of its word set
+// from the canonical row-major nibbles.
+__global__ void k_pack_codes(const uint8_t* __restrict__ q, uint32_t* __restrict__ out, int64_t N, int64_t K,
+                             int asym) {
+    int64_t nchunk = K / 64;
+    int64_t total = (N / 16) * nchunk * 32;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
+        int lane = (int)(i & 31);
+        int64_t tile = i >> 5;  // n_tile * nchunk + chunk
+        int64_t nt = tile / nchunk, kc = tile % nchunk;
+        int gq = lane >> 2, t = lane & 3;
+        int64_t r0 = nt * 16 + gq, r1 = r0 + 8;
+        uint32_t w[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            int64_t k = kc * 64 + 16 * t + 4 * j;
+            uint32_t nib[8];
+            // canonical: element c of row r at byte r*K/2 + c/2, low nibble for even c
+            auto get = [&](int64_t r, int64_t c) -> uint32_t {
+                uint8_t b = q[r * (K / 2) + c / 2];
+                uint32_t v = (c & 1) ? (b >> 4) : (b & 0xF);
+                return asym ? v : ((v + 8) & 0xF);  // two's complement -> offset binary
+            };
+            nib[0] = get(r0, k + 0);
+            nib[4] = get(r0, k + 1);
+            nib[1] = get(r1, k + 0);
+            nib[5] = get(r1, k + 1);
+            nib[2] = get(r0, k + 2);
+            nib[6] = get(r0, k + 3);
+            nib[3] = get(r1, k + 2);
+            nib[7] = get(r1, k + 3);
+            uint32_t v = 0;
+#pragma unroll
+            for (int p = 0; p < 8; ++p) v |= nib[p] << (4 * p);
+            w[j] = v;
+        }
+        reinterpret_cast<uint4*>(out)[i] = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+}
+
+__global__ void k_pack_meta(const __half* __restrict__ s, const int32_t* __restrict__ z, __half* __restrict__ s_out,
+                            uint8_t* __restrict__ z_out, int64_t N, int64_t ngr) {
+    int64_t total = (N / 16) * ngr;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
+        int64_t nt = i / ngr, gi = i % ngr;
+#pragma unroll
+        for (int r = 0; r < 8; ++r) {
+            s_out[i * 16 + 2 * r] = s[(nt * 16 + r) * ngr + gi];
+            s_out[i * 16 + 2 * r + 1] = s[(nt * 16 + r + 8) * ngr + gi];
+            if (z) {
+                uint32_t z0 = (uint32_t)z[(nt * 16 + r) * ngr + gi] & 0xF;
+                uint32_t z1 = (uint32_t)z[(nt * 16 + r + 8) * ngr + gi] & 0xF;
+                z_out[i * 8 + r] = (uint8_t)(z0 | (z1 << 4));
+            }
+        }
+    }
+}
+
+__global__ void k_write_header(qlin_w4_header h, qlin_w4_header* out) { *out = h; }
+
+cudaError_t run_pack_w4(const void* q, const void* s_f16, const int32_t* z, const qlin_w4_header* h, void* packed,
+                        cudaStream_t st) {
+    uint8_t* base = reinterpret_cast<uint8_t*>(packed);
+    int64_t N = h->N, K = h->K, ngr = K / h->group;
+    int blocks = num_sms() * 4;
+    k_write_header<<<1, 1, 0, st>>>(*h, reinterpret_cast<qlin_w4_header*>(base));
+    k_pack_codes<<<blocks, 256, 0, st>>>(reinterpret_cast<const uint8_t*>(q),
+                                         reinterpret_cast<uint32_t*>(base + h->codes_off), N, K, h->asym);
+    k_pack_meta<<<blocks, 256, 0, st>>>(reinterpret_cast<const __half*>(s_f16), h->asym ? z : nullptr,
+                                        reinterpret_cast<__half*>(base + h->scales_off),
+                                        h->asym ? base + h->zeros_off : nullptr, N, ngr);
+    return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------ dequant helpers
+__device__ __forceinline__ uint32_t bf16x2_sub(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("sub.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+__device__ __forceinline__ uint32_t bf16x2_mul(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+__device__ __forceinline__ uint32_t bf16x2_fma(uint32_t a, uint32_t b, uint32_t c) {
+    uint32_t d;
+    asm("fma.rn.bf16x2 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+__device__ __forceinline__ uint32_t f32x2_to_bf16x2(float lo, float hi) {
+    uint32_t d;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));
+    return d;
+}
+
+// Per-row dequantization constants: (s_hi, s_hi), (s_lo, s_lo), (128+z, 128+z).
+struct RowDq {
+    uint32_t shi2, slo2, c2;
+};
+
+__device__ __forceinline__ RowDq row_dq(float s, uint32_t z) {
+    RowDq r;
+    r.shi2 = f32x2_to_bf16x2(s, s);
+    float shi = __uint_as_float(r.shi2 << 16);
+    float slo = s - shi;  // exact
+    r.slo2 = f32x2_to_bf16x2(slo, slo);
+    r.c2 = 0x43004300u | z | (z << 16);  // bf16(128 + z) in both halves
+    return r;
+}
+
+// Dequantize one word of 8 nibbles into the A fragment (a0a1, a2a3, a4a5, a6a7):
+// pairs 0 and 2 use row gq (rg), pairs 1 and 3 row gq+8 (rh).
+__device__ __forceinline__ void dq_word(uint32_t w, const RowDq& rg, const RowDq& rh, uint32_t a[4]) {
+#pragma unroll
+    for (int p = 0; p < 4; ++p) {
+        uint32_t v = ((w >> (4 * p)) & 0x000F000Fu) | 0x43004300u;  // bf16x2(128+u)
+        const RowDq& R = (p & 1) ? rh : rg;
+        uint32_t d = bf16x2_sub(v, R.c2);                            // u - z, exact
+        uint32_t lo = bf16x2_mul(d, R.slo2);                         // exact
+        a[p] = bf16x2_fma(d, R.shi2, lo);                            // bf16_rn(s*d)
+    }
+}
+
+__device__ __forceinline__ void mma_bf16_16816(float c[4], const uint32_t a[4], uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};\n"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// Load the dequantization constants of lane (gq) for group gi of n-tile nt.
+__device__ __forceinline__ void load_rowdq(const uint8_t* __restrict__ blob, const qlin_w4_header& h, int64_t nt,
+                                           int64_t ngr, int64_t gi, int gq, RowDq& rg, RowDq& rh) {
+    const uint32_t* sp = reinterpret_cast<const uint32_t*>(blob + h.scales_off) + (nt * ngr + gi) * 8 + gq;
+    uint32_t sw = __ldg(sp);
+    __half2 s2 = *reinterpret_cast<__half2*>(&sw);
+    float2 sf = __half22float2(s2);
+    uint32_t z0 = 8, z1 = 8;
+    if (h.asym) {
+        uint8_t zb = __ldg(blob + h.zeros_off + (nt * ngr + gi) * 8 + gq);
+        z0 = zb & 0xF;
+        z1 = zb >> 4;
+    }
+    rg = row_dq(sf.x, z0);
+    rh = row_dq(sf.y, z1);
+}
+
+// ------------------------------------------------------------------ GEMV (M <= 16)
+// One CTA per 16-row n-tile; its 8 warps split the K chunks, each warp
+// accumulating m16n8k16 tiles (W as the A operand, X^T as B) in registers;
+// the partial tiles are summed in a fixed order in shared memory.
+template <int MT>  // number of n8 tiles of tokens: 1 (M <= 8) or 2 (M <= 16)
+__global__ void __launch_bounds__(256) k_w4_gemv(const __nv_bfloat16* __restrict__ x, const uint8_t* __restrict__ blob,
+                                                 qlin_w4_header h, int64_t M, __nv_bfloat16* __restrict__ y) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int gq = lane >> 2, t = lane & 3;
+    const int64_t nt = blockIdx.x;
+    const int64_t K = h.K, nchunk = K / 64, ngr = K / h.group;
+    const uint4* __restrict__ codes = reinterpret_cast<const uint4*>(blob + h.codes_off) + nt * nchunk * 32 + lane;
+
+    float acc[MT][4];
+#pragma unroll
+    for (int u = 0; u < MT; ++u)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) acc[u][e] = 0.0f;
+
+    int64_t last_g = -1;
+    RowDq rg, rh;
+    for (int64_t kc = warp; kc < nchunk; kc += 8) {
+        uint4 wv = __ldg(codes + kc * 32);
+        int64_t k0 = kc * 64 + 16 * t;
+        // activations: rows gq (and gq+8), k0..k0+15
+        uint4 xb[MT][2];
+#pragma unroll
+        for (int u = 0; u < MT; ++u) {
+            int64_t m = u * 8 + gq;
+            if (m < M) {
+                const uint4* xp = reinterpret_cast<const uint4*>(x + m * K + k0);
+                xb[u][0] = __ldg(xp);
+                xb[u][1] = __ldg(xp + 1);
+            } else {
+                xb[u][0] = make_uint4(0, 0, 0, 0);
+                xb[u][1] = make_uint4(0, 0, 0, 0);
+            }
+        }
+        int64_t gi = k0 / h.group;
+        if (gi != last_g) {
+            load_rowdq(blob, h, nt, ngr, gi, gq, rg, rh);
+            last_g = gi;
+        }
+        uint32_t wd[4] = {wv.x, wv.y, wv.z, wv.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            uint32_t a[4];
+            dq_word(wd[j], rg, rh, a);
+#pragma unroll
+            for (int u = 0; u < MT; ++u) {
+                const uint32_t* xw = reinterpret_cast<const uint32_t*>(&xb[u][0]);
+                mma_bf16_16816(acc[u], a, xw[2 * j], xw[2 * j + 1]);
+            }
+        }
+    }
+
+    // acc[u][e]: e=0,1 -> (row gq, tokens u*8 + 2t, +1); e=2,3 -> (row gq+8, same tokens)
+    __shared__ float part[8][16][16];  // [warp][n row][token]
+#pragma unroll
+    for (int u = 0; u < MT; ++u) {
+        part[warp][gq][u * 8 + 2 * t] = acc[u][0];
+        part[warp][gq][u * 8 + 2 * t + 1] = acc[u][1];
+        part[warp][gq + 8][u * 8 + 2 * t] = acc[u][2];
+        part[warp][gq + 8][u * 8 + 2 * t + 1] = acc[u][3];
+    }
+    __syncthreads();
+    int row = threadIdx.x >> 4, tok = threadIdx.x & 15;
+    if (tok < M && tok < MT * 8) {
+        float s = 0.0f;
+#pragma unroll
+        for (int w = 0; w < 8; ++w) s += part[w][row][tok];
+        y[(int64_t)tok * h.N + nt * 16 + row] = __float2bfloat16_rn(s);
+    }
+}
+
+// ------------------------------------------------------------------ GEMM (M > 16), mma.sync
+// CTA: 8 warps x 16 weight rows = 128 rows of W, BM tokens.  Each warp keeps
+// its 16 x 64 weight chunk in registers (dequantized once) and multiplies it
+// with all BM/8 token tiles of the chunk's X tile, staged in shared memory.
+constexpr int kW4BM = 64;
+constexpr int kXStride = 64 + 8;  // bf16 elements per smem row (padding against bank conflicts)
+
+__global__ void __launch_bounds__(256) k_w4_gemm_mma(const __nv_bfloat16* __restrict__ x, const uint8_t* __restrict__ blob,
+                                                     qlin_w4_header h, int64_t M, __nv_bfloat16* __restrict__ y) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int gq = lane >> 2, t = lane & 3;
+    const int64_t K = h.K, nchunk = K / 64, ngr = K / h.group;
+    const int64_t nt = (int64_t)blockIdx.x * 8 + warp;  // this warp's n-tile
+    const int64_t m0 = (int64_t)blockIdx.y * kW4BM;
+    const bool nt_ok = nt < h.N / 16;
+    const uint4* __restrict__ codes = reinterpret_cast<const uint4*>(blob + h.codes_off) + nt * nchunk * 32 + lane;
+
+    __shared__ __align__(16) __nv_bfloat16 xs[2][kW4BM * kXStride];
+
+    float acc[kW4BM / 8][4];
+#pragma unroll
+    for (int u = 0; u < kW4BM / 8; ++u)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) acc[u][e] = 0.0f;
+
+    // stage chunk kc of X (BM x 64 bf16 = 512 16-byte pieces; 2 per thread)
+    auto stage = [&](int buf, int64_t kc) {
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+            int piece = threadIdx.x + 256 * i;
+            int r = piece >> 3, c8 = piece & 7;
+            int64_t m = m0 + r;
+            uint4 v = make_uint4(0, 0, 0, 0);
+            if (m < M) v = __ldg(reinterpret_cast<const uint4*>(x + m * K + kc * 64 + c8 * 8));
+            *reinterpret_cast<uint4*>(&xs[buf][r * kXStride + c8 * 8]) = v;
+        }
+    };
+
+    stage(0, 0);
+    __syncthreads();
+    int64_t last_g = -1;
+    RowDq rg, rh;
+    for (int64_t kc = 0; kc < nchunk; ++kc) {
+        int buf = (int)(kc & 1);
+        uint4 wv = make_uint4(0x88888888u, 0x88888888u, 0x88888888u, 0x88888888u);
+        if (nt_ok) wv = __ldg(codes + kc * 32);
+        if (kc + 1 < nchunk) stage(buf ^ 1, kc + 1);
+        int64_t gi = (kc * 64 + 16 * t) / h.group;
+        if (nt_ok && gi != last_g) {
+            load_rowdq(blob, h, nt, ngr, gi, gq, rg, rh);
+            last_g = gi;
+        }
+        if (!nt_ok) {
+            rg = row_dq(0.0f, 8);
+            rh = rg;
+        }
+        uint32_t wd[4] = {wv.x, wv.y, wv.z, wv.w};
+        uint32_t a[4][4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) dq_word(wd[j], rg, rh, a[j]);
+#pragma unroll
+        for (int u = 0; u < kW4BM / 8; ++u) {
+            const __nv_bfloat16* xr = &xs[buf][(u * 8 + gq) * kXStride + 16 * t];
+            uint4 b01 = *reinterpret_cast<const uint4*>(xr);
+            uint4 b23 = *reinterpret_cast<const uint4*>(xr + 8);
+            mma_bf16_16816(acc[u], a[0], b01.x, b01.y);
+            mma_bf16_16816(acc[u], a[1], b01.z, b01.w);
+            mma_bf16_16816(acc[u], a[2], b23.x, b23.y);
+            mma_bf16_16816(acc[u], a[3], b23.z, b23.w);
+        }
+        __syncthreads();
+    }
+    if (!nt_ok) return;
+#pragma unroll
+    for (int u = 0; u < kW4BM / 8; ++u) {
+        int64_t mA = m0 + u * 8 + 2 * t, mB = mA + 1;
+        int64_t n0 = nt * 16 + gq, n1 = n0 + 8;
+        if (mA < M) {
+            y[mA * h.N + n0] = __float2bfloat16_rn(acc[u][0]);
+            y[mA * h.N + n1] = __float2bfloat16_rn(acc[u][2]);
+        }
+        if (mB < M) {
+            y[mB * h.N + n0] = __float2bfloat16_rn(acc[u][1]);
+            y[mB * h.N + n1] = __float2bfloat16_rn(acc[u][3]);
+        }
+    }
+}
+
+size_t w4a16_ws_bytes(int64_t, int64_t, int64_t) { return 0; }
+
+cudaError_t run_gemm_w4a16(const void* x, const void* packed, const qlin_w4_header* h, int64_t M, void* y, void*,
+                           cudaStream_t st) {
+    const __nv_bfloat16* xb = reinterpret_cast<const __nv_bfloat16*>(x);
+    const uint8_t* blob = reinterpret_cast<const uint8_t*>(packed);
+    __nv_bfloat16* yb = reinterpret_cast<__nv_bfloat16*>(y);
+    unsigned ntiles = (unsigned)(h->N / 16);
+    if (M <= 8) {
+        k_w4_gemv<1><<<ntiles, 256, 0, st>>>(xb, blob, *h, M, yb);
+    } else if (M <= 16) {
+        k_w4_gemv<2><<<ntiles, 256, 0, st>>>(xb, blob, *h, M, yb);
+    } else {
+        dim3 grid((unsigned)ceil_div(ntiles, 8), (unsigned)ceil_div(M, kW4BM));
+        k_w4_gemm_mma<<<grid, 256, 0, st>>>(xb, blob, *h, M, yb);
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace qlin

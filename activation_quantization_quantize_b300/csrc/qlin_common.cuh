@@ -1,0 +1,196 @@
+// qlin_common.cuh -- device helpers shared by the qlin kernels (sm_103a).
+//
+// The arithmetic here is the affine quantizer of the pages "量化、蒸馏与模型压缩"
+// (core formula) and "第11章 模型量化与压缩" 11.1.1-11.1.2: codes are
+// clip(rne(fl(x/s)) + z, qmin, qmax) with fl() the correctly rounded binary32
+// quotient.  The fast path below reaches exactly that result without a
+// division per element.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/qlin.h"
+
+namespace qlin {
+
+// ---------------------------------------------------------------- device error word
+// Set by kernels whose bounded waits give up; read and cleared by
+// qlin_device_error().
+__device__ int g_device_error = 0;
+
+__device__ __forceinline__ void raise_device_error(int code) { atomicExch(&g_device_error, code); }
+
+// ---------------------------------------------------------------- loads / stores
+template <typename T>
+__device__ __forceinline__ float to_f32(T v);
+template <>
+__device__ __forceinline__ float to_f32<float>(float v) { return v; }
+template <>
+__device__ __forceinline__ float to_f32<__nv_bfloat16>(__nv_bfloat16 v) { return __bfloat162float(v); }
+template <>
+__device__ __forceinline__ float to_f32<__half>(__half v) { return __half2float(v); }
+
+// Widen 8 consecutive elements starting at p (16-byte aligned for the 16-bit
+// types, 32-byte aligned for binary32) into v[0..7].
+template <typename T>
+__device__ __forceinline__ void load8(const T* p, float v[8]);
+
+template <>
+__device__ __forceinline__ void load8<__nv_bfloat16>(const __nv_bfloat16* p, float v[8]) {
+    uint4 u = __ldg(reinterpret_cast<const uint4*>(p));
+    uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        v[2 * i] = __uint_as_float(w[i] << 16);
+        v[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+    }
+}
+
+template <>
+__device__ __forceinline__ void load8<__half>(const __half* p, float v[8]) {
+    uint4 u = __ldg(reinterpret_cast<const uint4*>(p));
+    uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        __half2 h = *reinterpret_cast<__half2*>(&w[i]);
+        float2 f = __half22float2(h);
+        v[2 * i] = f.x;
+        v[2 * i + 1] = f.y;
+    }
+}
+
+template <>
+__device__ __forceinline__ void load8<float>(const float* p, float v[8]) {
+    float4 a = __ldg(reinterpret_cast<const float4*>(p));
+    float4 b = __ldg(reinterpret_cast<const float4*>(p) + 1);
+    v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+    v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+}
+
+template <typename T>
+__device__ __forceinline__ float load1(const T* p) { return to_f32<T>(p[0]); }
+
+// ---------------------------------------------------------------- scale / zero point
+struct ScopeParams {
+    float s;      // stored scale (binary32 value of the stored scale)
+    float r;      // approximate 1/s, only used to guess the code
+    float hs;     // s * (0.5 - 2^-11): half-step minus a safety margin
+    float cz;     // 1.5*2^23 + z
+};
+
+// Clamp bounds of code_bits() in the 1.5*2^23 + code domain.
+struct CodeRange {
+    float lo, hi;
+};
+__device__ __forceinline__ CodeRange make_range(int qmin, int qmax) {
+    CodeRange c;
+    c.lo = 12582912.0f + (float)qmin;
+    c.hi = 12582912.0f + (float)qmax;
+    return c;
+}
+
+// Round a scale to binary16 (nearest-even) saturating at 65504, as a binary32 value.
+__device__ __forceinline__ float round_f16_sat(float s) {
+    float r = __half2float(__float2half_rn(s));
+    if (isinf(r)) r = copysignf(65504.0f, s);
+    return r;
+}
+
+// Dynamic scale and zero point from the scope statistics
+// ([CH11] 11.1.1-11.1.2; [CSDN] symmetric / asymmetric sections).
+//   symmetric : hi = max|x|          -> s = fl(hi / qmax), z = 0
+//   asymmetric: lo = min(min x, 0), hi = max(max x, 0)
+//               -> s = fl(fl(hi - lo) / (qmax - qmin)), z = clip(qmin + rne(fl(-lo/s)))
+__device__ __forceinline__ void scale_zero(float lo, float hi, int qmin, int qmax, bool sym,
+                                           bool f16, float& s, int& z) {
+    if (sym) {
+        s = __fdiv_rn(hi, (float)qmax);
+    } else {
+        s = __fdiv_rn(__fsub_rn(hi, lo), (float)(qmax - qmin));
+    }
+    if (f16) s = round_f16_sat(s);
+    if (s == 0.0f) s = 1.0f;
+    if (sym) {
+        z = 0;
+    } else {
+        float t = rintf(__fdiv_rn(-lo, s));
+        float zz = fminf(fmaxf(t + (float)qmin, (float)qmin), (float)qmax);
+        z = (int)zz;
+    }
+}
+
+__device__ __forceinline__ ScopeParams make_scope(float s, int z) {
+    ScopeParams p;
+    p.s = s;
+    p.r = __frcp_rn(s);
+    p.hs = s * 0.49951171875f;
+    p.cz = 12582912.0f + (float)z;
+    return p;
+}
+
+// Code of one (already smoothed) value, returned as the bit pattern of the
+// binary32 number 1.5*2^23 + code, so that its low byte is the two's-complement
+// code byte and its low nibble the 4-bit code.
+//
+// Exactness: t = v*r is within a few ulp of v/s.  When |t| < 4096 the
+// candidate n = rne(t) (1.5*2^23 trick, exact round-half-even) gives an exact
+// remainder d = v - n*s (fma; n*s and v share the quantum of s).  If |d| stays
+// below (0.5 - 2^-11)*s the true quotient is more than 2^-11 away from a
+// half-integer, so fl(v/s) (within 2^-13 of v/s here) rounds to the same n and
+// rne(t) + z = rne(t + z).  Every other case -- a near-tie, a value far
+// outside the code range, an overflowing reciprocal -- takes the correctly
+// rounded division.
+__device__ __forceinline__ uint32_t code_bits(float v, const ScopeParams& p, const CodeRange& cr) {
+    float t = v * p.r;
+    float m;
+    if (fabsf(t) < 4096.0f) {
+        m = t + p.cz;                          // rne(t) + 1.5*2^23 + z
+        float n = m - p.cz;                    // rne(t), exact
+        float d = fmaf(-n, p.s, v);            // exact remainder
+        if (!(fabsf(d) < p.hs)) {
+            float q = rintf(__fdiv_rn(v, p.s));
+            m = fminf(fmaxf(q, -8388608.0f), 8388608.0f) + p.cz;
+        }
+    } else {
+        float q = rintf(__fdiv_rn(v, p.s));
+        m = fminf(fmaxf(q, -8388608.0f), 8388608.0f) + p.cz;
+    }
+    m = fminf(fmaxf(m, cr.lo), cr.hi);
+    return __float_as_uint(m);
+}
+
+// Pack the low bytes of four code_bits() words: byte i <- a[i].
+__device__ __forceinline__ uint32_t pack_bytes4(uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3) {
+    uint32_t lo = __byte_perm(a0, a1, 0x0040);
+    uint32_t hi = __byte_perm(a2, a3, 0x0040);
+    return __byte_perm(lo, hi, 0x5410);
+}
+
+// Pack eight codes into four bytes of nibbles: element 2i in the low nibble.
+__device__ __forceinline__ uint32_t pack_nibbles8(const uint32_t c[8]) {
+    uint32_t b0 = pack_bytes4(c[0], c[1], c[2], c[3]) & 0x0F0F0F0Fu;
+    uint32_t b1 = pack_bytes4(c[4], c[5], c[6], c[7]) & 0x0F0F0F0Fu;
+    b0 = b0 | (b0 >> 4);   // bytes 0 and 2 now hold (c0|c1<<4), (c2|c3<<4)
+    b1 = b1 | (b1 >> 4);
+    return __byte_perm(b0, b1, 0x6420);
+}
+
+// ---------------------------------------------------------------- reductions
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+__device__ __forceinline__ float warp_min(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fminf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+
+// ---------------------------------------------------------------- misc
+__host__ __device__ __forceinline__ int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+}  // namespace qlin

@@ -1,0 +1,39 @@
+// qlin_internal.h -- host-side launchers shared between the entry points
+// (api.cu) and the kernel files.  Not part of the public ABI.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/qlin.h"
+
+namespace qlin {
+
+int num_sms();
+int64_t percentile_rank(int64_t n, double p);
+
+size_t quantize_ws_bytes(int64_t rows, int64_t cols, const qlin_qparams* p);
+cudaError_t run_quantize(const void* x, int xt, int64_t rows, int64_t cols, int64_t ld, const float* smooth,
+                         const qlin_qparams* p, void* q, void* s, int32_t* z, void* ws, cudaStream_t st);
+cudaError_t run_absmax(const void* x, int xt, int64_t rows, int64_t cols, int64_t ld, int gran, int group,
+                       float* out, void* ws, cudaStream_t st);
+cudaError_t run_dequantize(const void* q, const void* s, const int32_t* z, const qlin_qparams* p, int64_t rows,
+                           int64_t cols, void* y, int yt, cudaStream_t st);
+cudaError_t run_smooth_factors(const float* xmax, const float* wmax, int64_t K, float alpha, float* s,
+                               cudaStream_t st);
+
+// W8A8 (gemm_w8a8.cu)
+size_t w8a8_ws_bytes(int64_t M, int64_t N, int64_t K);
+cudaError_t run_gemm_w8a8(const int8_t* qx, const float* sx, const int8_t* qw, const float* sw, int64_t M,
+                          int64_t N, int64_t K, void* y, int yt, int32_t* acc_out, void* ws, cudaStream_t st);
+
+// W4A16 (gemm_w4a16.cu)
+void w4_layout(int64_t N, int64_t K, int group, int asym, qlin_w4_header* h);
+cudaError_t run_pack_w4(const void* q, const void* s_f16, const int32_t* z, const qlin_w4_header* h, void* packed,
+                        cudaStream_t st);
+size_t w4a16_ws_bytes(int64_t M, int64_t N, int64_t K);
+cudaError_t run_gemm_w4a16(const void* x, const void* packed, const qlin_w4_header* h, int64_t M, void* y,
+                           void* ws, cudaStream_t st);
+
+}  // namespace qlin

@@ -1,0 +1,874 @@
+// quantize.cu -- quantize / dequantize / absmax / smoothing-factor kernels.
+//
+// Method: the affine quantizer q = clip(round(x/s) + z, qmin, qmax),
+// x^ = s(q - z) of "量化、蒸馏与模型压缩" (core formula) and
+// "第11章 模型量化与压缩" 11.1.1-11.1.5, at the granularities of
+// "十九：模型压缩：量化、ZeroQuant、LLM.int8() 与 SmoothQuant" section 4.
+//
+// Kernels (all HBM-bound; the design target is one read of x and one write of
+// the codes per element where the scope is row-local):
+//   k_quant_rows    per-row / per-group scopes: the row is held in registers,
+//                   reduced with warp shuffles, quantized and packed in one pass.
+//   k_stats_strip   per-tensor / per-column range statistics (atomic max of
+//                   non-negative binary32 bit patterns: order-independent, so
+//                   deterministic).
+//   k_finalize      statistics -> (s, z) per scope.
+//   k_quant_strip   per-tensor / per-column codes from stored (s, z).
+//   k_*_generic     scalar fallbacks for unaligned or odd shapes.
+//   k_hist*/k_select percentile clipping (exact radix select on |x| bits).
+//   k_dequant       x^ = fl(s (q - z)) rounded to the output type.
+#include "qlin_common.cuh"
+#include "qlin_internal.h"
+
+namespace qlin {
+
+// ------------------------------------------------------------------ parameters
+struct QuantArgs {
+    const void* x;
+    int64_t rows, cols, ld;
+    const float* smooth;
+    int smooth_mode;
+    int qmin, qmax;
+    int sym;
+    int gran;
+    int group;
+    int scale_f16;
+    int static_scale;
+    int code4;        // 1: two codes per byte
+    void* q;
+    void* s;
+    int32_t* z;
+    float* absmax_out;  // stats-only mode (qlin_absmax), else nullptr
+};
+
+__device__ __forceinline__ float load_scale(const void* s, int64_t i, int f16) {
+    return f16 ? __half2float(reinterpret_cast<const __half*>(s)[i]) : reinterpret_cast<const float*>(s)[i];
+}
+__device__ __forceinline__ void store_scale(void* s, int64_t i, int f16, float v) {
+    if (f16)
+        reinterpret_cast<__half*>(s)[i] = __float2half_rn(v);  // v is already a binary16 value
+    else
+        reinterpret_cast<float*>(s)[i] = v;
+}
+
+// Optional smoothing of 8 elements of columns c0..c0+7: x / s_c (correctly
+// rounded binary32 division) or x * s_c.
+__device__ __forceinline__ void smooth8(float v[8], int mode, const float* __restrict__ sm, int64_t c0) {
+    if (mode == QLIN_SMOOTH_NONE) return;
+    float4 a = __ldg(reinterpret_cast<const float4*>(sm + c0));
+    float4 b = __ldg(reinterpret_cast<const float4*>(sm + c0) + 1);
+    float f[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+#pragma unroll
+    for (int j = 0; j < 8; ++j) v[j] = (mode == QLIN_SMOOTH_DIVIDE) ? __fdiv_rn(v[j], f[j]) : v[j] * f[j];
+}
+
+// Store 8 codes of chunk `chunk` of row r (codes as code_bits words).
+__device__ __forceinline__ void store_codes8(void* q, int64_t r, int64_t cols, int64_t chunk, int code4,
+                                             const uint32_t c[8]) {
+    if (code4) {
+        uint32_t w = pack_nibbles8(c);
+        reinterpret_cast<uint32_t*>(reinterpret_cast<uint8_t*>(q) + r * (cols / 2))[chunk] = w;
+    } else {
+        uint2 w;
+        w.x = pack_bytes4(c[0], c[1], c[2], c[3]);
+        w.y = pack_bytes4(c[4], c[5], c[6], c[7]);
+        reinterpret_cast<uint2*>(reinterpret_cast<int8_t*>(q) + r * cols)[chunk] = w;
+    }
+}
+
+// ------------------------------------------------------------------ row-local scopes
+// One CTA walks rows r = blockIdx.x, blockIdx.x + gridDim.x, ...; thread t holds
+// chunks c = i*blockDim.x + t (8 elements each) of the row in registers.
+// PER_ROW reduces over the CTA; PER_GROUP over the g/8 adjacent lanes holding
+// one group.  CPT = max chunks per thread.
+template <typename T, int CPT>
+__global__ void __launch_bounds__(512) k_quant_rows(QuantArgs a) {
+    const int tid = threadIdx.x;
+    const int nt = blockDim.x;
+    const int64_t nchunks = a.cols / 8;
+    const bool per_row = (a.gran == QLIN_PER_ROW);
+    const int gl = per_row ? 0 : a.group / 8;  // lanes per group
+    const T* __restrict__ x = reinterpret_cast<const T*>(a.x);
+    const CodeRange cr = make_range(a.qmin, a.qmax);
+    __shared__ float red_hi[32], red_lo[32];
+    __shared__ float bc[2];
+
+    for (int64_t r = blockIdx.x; r < a.rows; r += gridDim.x) {
+        float v[CPT][8];
+#pragma unroll
+        for (int i = 0; i < CPT; ++i) {
+            int64_t c = (int64_t)i * nt + tid;
+            if (c < nchunks) {
+                load8<T>(x + r * a.ld + c * 8, v[i]);
+                smooth8(v[i], a.smooth_mode, a.smooth, c * 8);
+            } else {
+#pragma unroll
+                for (int j = 0; j < 8; ++j) v[i][j] = 0.0f;
+            }
+        }
+
+        if (per_row) {
+            float s;
+            int z;
+            if (a.static_scale) {
+                s = load_scale(a.s, r, a.scale_f16);
+                z = a.z ? a.z[r] : 0;
+            } else {
+                float hi = 0.0f, lo = 0.0f;
+#pragma unroll
+                for (int i = 0; i < CPT; ++i)
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        if (a.sym) {
+                            hi = fmaxf(hi, fabsf(v[i][j]));
+                        } else {
+                            hi = fmaxf(hi, v[i][j]);
+                            lo = fminf(lo, v[i][j]);
+                        }
+                    }
+                hi = warp_max(hi);
+                lo = warp_min(lo);
+                if ((tid & 31) == 0) {
+                    red_hi[tid >> 5] = hi;
+                    red_lo[tid >> 5] = lo;
+                }
+                __syncthreads();
+                if (tid < 32) {
+                    int nw = nt >> 5;
+                    float h = (tid < nw) ? red_hi[tid] : 0.0f;
+                    float l = (tid < nw) ? red_lo[tid] : 0.0f;
+                    h = warp_max(h);
+                    l = warp_min(l);
+                    if (tid == 0) {
+                        bc[0] = h;
+                        bc[1] = l;
+                    }
+                }
+                __syncthreads();
+                hi = bc[0];
+                lo = bc[1];
+                __syncthreads();  // bc / red_* are reused by the next row
+                if (a.absmax_out) {
+                    if (tid == 0) a.absmax_out[r] = hi;
+                    continue;
+                }
+                scale_zero(lo, hi, a.qmin, a.qmax, a.sym, a.scale_f16, s, z);
+                if (tid == 0) {
+                    store_scale(a.s, r, a.scale_f16, s);
+                    if (a.z) a.z[r] = z;
+                }
+            }
+            const ScopeParams p = make_scope(s, z);
+#pragma unroll
+            for (int i = 0; i < CPT; ++i) {
+                int64_t c = (int64_t)i * nt + tid;
+                if (c < nchunks) {
+                    uint32_t cb[8];
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) cb[j] = code_bits(v[i][j], p, cr);
+                    store_codes8(a.q, r, a.cols, c, a.code4, cb);
+                }
+            }
+        } else {
+            const int64_t ngr = a.cols / a.group;
+#pragma unroll
+            for (int i = 0; i < CPT; ++i) {
+                int64_t c = (int64_t)i * nt + tid;
+                int64_t grp = (c * 8) / a.group;  // group index within the row
+                float s;
+                int z;
+                if (a.static_scale) {
+                    s = (c < nchunks) ? load_scale(a.s, r * ngr + grp, a.scale_f16) : 1.0f;
+                    z = (c < nchunks && a.z) ? a.z[r * ngr + grp] : 0;
+                } else {
+                    float hi = 0.0f, lo = 0.0f;
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        if (a.sym) {
+                            hi = fmaxf(hi, fabsf(v[i][j]));
+                        } else {
+                            hi = fmaxf(hi, v[i][j]);
+                            lo = fminf(lo, v[i][j]);
+                        }
+                    }
+                    for (int o = 1; o < gl; o <<= 1) {
+                        hi = fmaxf(hi, __shfl_xor_sync(0xffffffffu, hi, o));
+                        lo = fminf(lo, __shfl_xor_sync(0xffffffffu, lo, o));
+                    }
+                    const bool leader = (c < nchunks) && ((c % gl) == 0);
+                    if (a.absmax_out) {
+                        if (leader) a.absmax_out[r * ngr + grp] = hi;
+                        continue;
+                    }
+                    scale_zero(lo, hi, a.qmin, a.qmax, a.sym, a.scale_f16, s, z);
+                    if (leader) {
+                        store_scale(a.s, r * ngr + grp, a.scale_f16, s);
+                        if (a.z) a.z[r * ngr + grp] = z;
+                    }
+                }
+                if (c < nchunks) {
+                    const ScopeParams p = make_scope(s, z);
+                    uint32_t cb[8];
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) cb[j] = code_bits(v[i][j], p, cr);
+                    store_codes8(a.q, r, a.cols, c, a.code4, cb);
+                }
+            }
+        }
+    }
+}
+
+// ------------------------------------------------------------------ column-strip kernels
+// Thread layout shared by the per-tensor / per-column kernels: the block's
+// threads cover `cpb` chunk columns x `rpi` rows per iteration; the block
+// walks rows [r0, r1) of its row slab.
+struct Strip {
+    int64_t chunk;   // chunk column of this thread (-1 when idle)
+    int64_t r_begin, r_end, r_step;
+};
+
+__device__ __forceinline__ Strip strip_of(int64_t nchunks, int64_t rows, int rows_per_block) {
+    Strip st;
+    const int nt = blockDim.x, t = threadIdx.x;
+    int64_t cpb = nchunks < nt ? nchunks : nt;        // chunk columns per block
+    int64_t rpi = nt / cpb;                           // rows per iteration
+    int64_t cl = t % cpb, rl = t / cpb;
+    st.chunk = (rl < rpi) ? (int64_t)blockIdx.x * cpb + cl : -1;
+    if (st.chunk >= nchunks) st.chunk = -1;
+    int64_t r0 = (int64_t)blockIdx.y * rows_per_block;
+    int64_t r1 = r0 + rows_per_block;
+    if (r1 > rows) r1 = rows;
+    st.r_begin = r0 + rl;
+    st.r_end = r1;
+    st.r_step = rpi;
+    return st;
+}
+
+// Range statistics into ws words (binary32 bit patterns of non-negative values,
+// atomicMax): stat[2*scope] = max(max x, 0) (or max|x|), stat[2*scope+1] =
+// -min(min x, 0).  The words start at 0 (memset by the host).
+template <typename T>
+__global__ void __launch_bounds__(256) k_stats_strip(QuantArgs a, uint32_t* stat, int rows_per_block) {
+    const int64_t nchunks = a.cols / 8;
+    const T* __restrict__ x = reinterpret_cast<const T*>(a.x);
+    Strip st = strip_of(nchunks, a.rows, rows_per_block);
+    float hi[8], lo[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        hi[j] = 0.0f;
+        lo[j] = 0.0f;
+    }
+    if (st.chunk >= 0) {
+        for (int64_t r = st.r_begin; r < st.r_end; r += st.r_step) {
+            float v[8];
+            load8<T>(x + r * a.ld + st.chunk * 8, v);
+            smooth8(v, a.smooth_mode, a.smooth, st.chunk * 8);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                float u = v[j];
+                if (a.sym) {
+                    hi[j] = fmaxf(hi[j], fabsf(u));
+                } else {
+                    hi[j] = fmaxf(hi[j], u);
+                    lo[j] = fminf(lo[j], u);
+                }
+            }
+        }
+    }
+    if (a.gran == QLIN_PER_COL) {
+        if (st.chunk >= 0) {
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                int64_t c = st.chunk * 8 + j;
+                if (hi[j] > 0.0f) atomicMax(&stat[2 * c], __float_as_uint(hi[j]));
+                if (lo[j] < 0.0f) atomicMax(&stat[2 * c + 1], __float_as_uint(-lo[j]));
+            }
+        }
+    } else {
+        float h = 0.0f, l = 0.0f;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            h = fmaxf(h, hi[j]);
+            l = fminf(l, lo[j]);
+        }
+        h = warp_max(h);
+        l = warp_min(l);
+        if ((threadIdx.x & 31) == 0) {
+            if (h > 0.0f) atomicMax(&stat[0], __float_as_uint(h));
+            if (l < 0.0f) atomicMax(&stat[1], __float_as_uint(-l));
+        }
+    }
+}
+
+// Statistics -> stored scale and zero point of every scope.
+__global__ void k_finalize(QuantArgs a, const uint32_t* stat, int64_t nscopes) {
+    int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= nscopes) return;
+    float hi = __uint_as_float(stat[2 * i]);
+    float lo = -__uint_as_float(stat[2 * i + 1]);
+    if (a.absmax_out) {
+        a.absmax_out[i] = hi;
+        return;
+    }
+    float s;
+    int z;
+    scale_zero(lo, hi, a.qmin, a.qmax, a.sym, a.scale_f16, s, z);
+    store_scale(a.s, i, a.scale_f16, s);
+    if (a.z) a.z[i] = z;
+}
+
+// Codes for per-tensor / per-column scopes from the stored (s, z).
+template <typename T>
+__global__ void __launch_bounds__(256) k_quant_strip(QuantArgs a, int rows_per_block) {
+    const int64_t nchunks = a.cols / 8;
+    const T* __restrict__ x = reinterpret_cast<const T*>(a.x);
+    Strip st = strip_of(nchunks, a.rows, rows_per_block);
+    if (st.chunk < 0) return;
+    const CodeRange cr = make_range(a.qmin, a.qmax);
+    ScopeParams sp[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        int64_t sc = (a.gran == QLIN_PER_COL) ? st.chunk * 8 + j : 0;
+        float s = load_scale(a.s, sc, a.scale_f16);
+        int z = a.z ? a.z[sc] : 0;
+        sp[j] = make_scope(s, z);
+    }
+    for (int64_t r = st.r_begin; r < st.r_end; r += st.r_step) {
+        float v[8];
+        load8<T>(x + r * a.ld + st.chunk * 8, v);
+        smooth8(v, a.smooth_mode, a.smooth, st.chunk * 8);
+        uint32_t cb[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) cb[j] = code_bits(v[j], sp[j], cr);
+        store_codes8(a.q, r, a.cols, st.chunk, a.code4, cb);
+    }
+}
+
+// ------------------------------------------------------------------ generic (scalar) path
+__device__ __forceinline__ int64_t scope_index(int gran, int64_t r, int64_t c, int64_t cols, int group) {
+    switch (gran) {
+    case QLIN_PER_TENSOR: return 0;
+    case QLIN_PER_ROW: return r;
+    case QLIN_PER_COL: return c;
+    default: return r * (cols / group) + c / group;
+    }
+}
+
+template <typename T>
+__device__ __forceinline__ float load_smoothed(const QuantArgs& a, int64_t r, int64_t c) {
+    float v = load1<T>(reinterpret_cast<const T*>(a.x) + r * a.ld + c);
+    if (a.smooth_mode == QLIN_SMOOTH_DIVIDE) return __fdiv_rn(v, a.smooth[c]);
+    if (a.smooth_mode == QLIN_SMOOTH_MULTIPLY) return v * a.smooth[c];
+    return v;
+}
+
+template <typename T>
+__global__ void k_stats_generic(QuantArgs a, uint32_t* stat) {
+    int64_t n = a.rows * a.cols;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
+        int64_t r = i / a.cols, c = i % a.cols;
+        float v = load_smoothed<T>(a, r, c);
+        int64_t sc = scope_index(a.gran, r, c, a.cols, a.group);
+        if (a.sym) {
+            float h = fabsf(v);
+            if (h > 0.0f) atomicMax(&stat[2 * sc], __float_as_uint(h));
+        } else {
+            if (v > 0.0f) atomicMax(&stat[2 * sc], __float_as_uint(v));
+            if (v < 0.0f) atomicMax(&stat[2 * sc + 1], __float_as_uint(-v));
+        }
+    }
+}
+
+// One thread per code byte (one or two elements).
+template <typename T>
+__global__ void k_quant_generic(QuantArgs a) {
+    int64_t per_row = a.code4 ? a.cols / 2 : a.cols;
+    int64_t n = a.rows * per_row;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
+        int64_t r = i / per_row, b = i % per_row;
+        int ne = a.code4 ? 2 : 1;
+        uint32_t byte = 0;
+        for (int e = 0; e < ne; ++e) {
+            int64_t c = b * ne + e;
+            int64_t sc = scope_index(a.gran, r, c, a.cols, a.group);
+            float s = load_scale(a.s, sc, a.scale_f16);
+            int z = a.z ? a.z[sc] : 0;
+            ScopeParams p = make_scope(s, z);
+            uint32_t cbits = code_bits(load_smoothed<T>(a, r, c), p, make_range(a.qmin, a.qmax));
+            byte |= a.code4 ? ((cbits & 0xFu) << (4 * e)) : (cbits & 0xFFu);
+        }
+        reinterpret_cast<uint8_t*>(a.q)[r * per_row + b] = (uint8_t)byte;
+    }
+}
+
+// ------------------------------------------------------------------ percentile clipping
+// Exact nearest-rank selection of |x| by its binary32 bit pattern (for
+// non-negative floats the pattern order is the value order): a 32768-bin
+// histogram of the top 16 bits, a selection, then (when the low 16 bits can be
+// non-zero) a 65536-bin histogram of the low bits inside the selected bin.
+// ws words: hist1[32768] | hist2[65536] | sel[4].
+constexpr int kHist1 = 32768, kHist2 = 65536;
+
+template <typename T>
+__global__ void __launch_bounds__(1024) k_hist1(QuantArgs a, uint32_t* hist1) {
+    extern __shared__ uint32_t sh[];
+    for (int i = threadIdx.x; i < kHist1; i += blockDim.x) sh[i] = 0;
+    __syncthreads();
+    for (int64_t r = blockIdx.x; r < a.rows; r += gridDim.x)
+        for (int64_t c = threadIdx.x; c < a.cols; c += blockDim.x) {
+            float v = fabsf(load_smoothed<T>(a, r, c));
+            atomicAdd(&sh[__float_as_uint(v) >> 16], 1u);
+        }
+    __syncthreads();
+    for (int i = threadIdx.x; i < kHist1; i += blockDim.x)
+        if (sh[i]) atomicAdd(&hist1[i], sh[i]);
+}
+
+template <typename T>
+__global__ void k_hist2(QuantArgs a, const uint32_t* sel, uint32_t* hist2) {
+    uint32_t bin = sel[0];
+    for (int64_t r = blockIdx.x; r < a.rows; r += gridDim.x)
+        for (int64_t c = threadIdx.x; c < a.cols; c += blockDim.x) {
+            uint32_t u = __float_as_uint(fabsf(load_smoothed<T>(a, r, c)));
+            if ((u >> 16) == bin) atomicAdd(&hist2[u & 0xFFFFu], 1u);
+        }
+}
+
+// Single CTA of 1024 threads: find the bin holding rank k (1-based) of `hist`
+// (nbins = 1024 * per), write {bin, rank inside bin}.
+__device__ void select_rank(const uint32_t* hist, int per, uint64_t k, uint32_t* out_bin, uint64_t* out_rank) {
+    __shared__ unsigned long long part[1024];
+    const int t = threadIdx.x;
+    unsigned long long sum = 0;
+    for (int j = 0; j < per; ++j) sum += hist[t * per + j];
+    part[t] = sum;
+    __syncthreads();
+    if (t == 0) {
+        unsigned long long acc = 0;
+        int tsel = 1023;
+        for (int i = 0; i < 1024; ++i) {
+            if (acc + part[i] >= k) {
+                tsel = i;
+                break;
+            }
+            acc += part[i];
+        }
+        uint32_t bin = (uint32_t)(tsel * per + per - 1);
+        for (int j = 0; j < per; ++j) {
+            uint32_t h = hist[tsel * per + j];
+            if (acc + h >= k) {
+                bin = (uint32_t)(tsel * per + j);
+                break;
+            }
+            acc += h;
+        }
+        *out_bin = bin;
+        *out_rank = k - acc;
+    }
+    __syncthreads();
+}
+
+// Level 1: select the top-16-bit bin; when `final_` the low bits are known to
+// be zero and the scale is written directly.
+__global__ void __launch_bounds__(1024) k_select1(QuantArgs a, const uint32_t* hist1, uint32_t* sel, uint64_t k, int final_) {
+    __shared__ uint32_t bin;
+    __shared__ uint64_t rk;
+    select_rank(hist1, kHist1 / 1024, k, &bin, &rk);
+    if (threadIdx.x == 0) {
+        sel[0] = bin;
+        sel[1] = (uint32_t)rk;
+        if (final_) {
+            float T_ = __uint_as_float(bin << 16);
+            float s;
+            int z;
+            scale_zero(0.0f, T_, a.qmin, a.qmax, true, a.scale_f16, s, z);
+            store_scale(a.s, 0, a.scale_f16, s);
+            if (a.z) a.z[0] = 0;
+        }
+    }
+}
+
+__global__ void __launch_bounds__(1024) k_select2(QuantArgs a, const uint32_t* hist2, const uint32_t* sel) {
+    __shared__ uint32_t bin;
+    __shared__ uint64_t rk;
+    select_rank(hist2, kHist2 / 1024, sel[1], &bin, &rk);
+    if (threadIdx.x == 0) {
+        float T_ = __uint_as_float((sel[0] << 16) | bin);
+        float s;
+        int z;
+        scale_zero(0.0f, T_, a.qmin, a.qmax, true, a.scale_f16, s, z);
+        store_scale(a.s, 0, a.scale_f16, s);
+        if (a.z) a.z[0] = 0;
+    }
+}
+
+// ------------------------------------------------------------------ dequantize
+struct DequantArgs {
+    const void* q;
+    const void* s;
+    const int32_t* z;
+    int64_t rows, cols;
+    int gran, group, scale_f16, code4, code_signed;
+    void* y;
+    int yt;
+};
+
+__device__ __forceinline__ int code_at(const DequantArgs& d, int64_t r, int64_t c) {
+    if (d.code4) {
+        uint8_t b = reinterpret_cast<const uint8_t*>(d.q)[r * (d.cols / 2) + c / 2];
+        int v = (c & 1) ? (b >> 4) : (b & 0xF);
+        if (d.code_signed && v >= 8) v -= 16;
+        return v;
+    }
+    if (d.code_signed) return reinterpret_cast<const int8_t*>(d.q)[r * d.cols + c];
+    return reinterpret_cast<const uint8_t*>(d.q)[r * d.cols + c];
+}
+
+__device__ __forceinline__ void store_y(const DequantArgs& d, int64_t i, float v) {
+    if (d.yt == QLIN_BF16)
+        reinterpret_cast<__nv_bfloat16*>(d.y)[i] = __float2bfloat16_rn(v);
+    else if (d.yt == QLIN_F16)
+        reinterpret_cast<__half*>(d.y)[i] = __float2half_rn(v);
+    else
+        reinterpret_cast<float*>(d.y)[i] = v;
+}
+
+// Vector path: 8 elements per thread (cols % 8 == 0, group % 8 == 0).
+__global__ void k_dequant_vec(DequantArgs d) {
+    int64_t nchunks = d.rows * (d.cols / 8);
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < nchunks; i += (int64_t)gridDim.x * blockDim.x) {
+        int64_t r = i / (d.cols / 8), c0 = (i % (d.cols / 8)) * 8;
+        int code[8];
+        if (d.code4) {
+            uint32_t w = reinterpret_cast<const uint32_t*>(reinterpret_cast<const uint8_t*>(d.q) + r * (d.cols / 2))[c0 / 8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                int v = (w >> (4 * j)) & 0xF;
+                code[j] = (d.code_signed && v >= 8) ? v - 16 : v;
+            }
+        } else {
+            uint2 w = reinterpret_cast<const uint2*>(reinterpret_cast<const uint8_t*>(d.q) + r * d.cols)[c0 / 8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                uint32_t b = ((j < 4 ? w.x : w.y) >> (8 * (j & 3))) & 0xFFu;
+                code[j] = d.code_signed ? (int)(int8_t)b : (int)b;
+            }
+        }
+        float out[8];
+        if (d.gran == QLIN_PER_COL) {
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                float s = load_scale(d.s, c0 + j, d.scale_f16);
+                int z = d.z ? d.z[c0 + j] : 0;
+                out[j] = s * (float)(code[j] - z);
+            }
+        } else {
+            // one scope for the whole chunk (groups are whole chunks)
+            int64_t sc = (d.gran == QLIN_PER_TENSOR) ? 0
+                       : (d.gran == QLIN_PER_ROW) ? r
+                       : r * (d.cols / d.group) + c0 / d.group;
+            float s = load_scale(d.s, sc, d.scale_f16);
+            int z = d.z ? d.z[sc] : 0;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) out[j] = s * (float)(code[j] - z);
+        }
+        int64_t base = r * d.cols + c0;
+        if (d.yt == QLIN_BF16) {
+            uint4 u;
+            __nv_bfloat162 p0 = __floats2bfloat162_rn(out[0], out[1]);
+            __nv_bfloat162 p1 = __floats2bfloat162_rn(out[2], out[3]);
+            __nv_bfloat162 p2 = __floats2bfloat162_rn(out[4], out[5]);
+            __nv_bfloat162 p3 = __floats2bfloat162_rn(out[6], out[7]);
+            u.x = *reinterpret_cast<uint32_t*>(&p0);
+            u.y = *reinterpret_cast<uint32_t*>(&p1);
+            u.z = *reinterpret_cast<uint32_t*>(&p2);
+            u.w = *reinterpret_cast<uint32_t*>(&p3);
+            reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(d.y) + base)[0] = u;
+        } else if (d.yt == QLIN_F32) {
+            float4* yp = reinterpret_cast<float4*>(reinterpret_cast<float*>(d.y) + base);
+            yp[0] = make_float4(out[0], out[1], out[2], out[3]);
+            yp[1] = make_float4(out[4], out[5], out[6], out[7]);
+        } else {
+#pragma unroll
+            for (int j = 0; j < 8; ++j) store_y(d, base + j, out[j]);
+        }
+    }
+}
+
+__global__ void k_dequant_generic(DequantArgs d) {
+    int64_t n = d.rows * d.cols;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
+        int64_t r = i / d.cols, c = i % d.cols;
+        int64_t sc = scope_index(d.gran, r, c, d.cols, d.group);
+        float s = load_scale(d.s, sc, d.scale_f16);
+        int z = d.z ? d.z[sc] : 0;
+        store_y(d, i, s * (float)(code_at(d, r, c) - z));
+    }
+}
+
+// ------------------------------------------------------------------ smoothing factors
+// s_j = max|X_j|^alpha / max|W_j|^(1-alpha) ("量化、蒸馏与模型压缩" 2.3 eq. 1).
+__global__ void k_smooth_factors(const float* xmax, const float* wmax, int64_t K, float alpha, float* s) {
+    int64_t j = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (j >= K) return;
+    float mx = xmax[j], mw = wmax[j];
+    float v;
+    if (mx == 0.0f || mw == 0.0f)
+        v = 1.0f;
+    else if (alpha == 0.5f)
+        v = __fdiv_rn(__fsqrt_rn(mx), __fsqrt_rn(mw));
+    else
+        v = __fdiv_rn(powf(mx, alpha), powf(mw, 1.0f - alpha));
+    s[j] = v;
+}
+
+// ------------------------------------------------------------------ host launchers
+static int g_num_sms = 0;
+int num_sms() {
+    if (g_num_sms == 0) {
+        int dev = 0;
+        cudaGetDevice(&dev);
+        cudaDeviceGetAttribute(&g_num_sms, cudaDevAttrMultiProcessorCount, dev);
+        if (g_num_sms <= 0) g_num_sms = 148;
+    }
+    return g_num_sms;
+}
+
+static inline int elem_size(int xt) { return xt == QLIN_F32 ? 4 : 2; }
+
+// Whether the row kernel applies: 8-element chunks, 16-byte aligned rows,
+// groups that are whole chunks and fit a warp.
+static bool rows_kernel_ok(const QuantArgs& a, int xt) {
+    int es = elem_size(xt);
+    if (a.cols % 8 != 0) return false;
+    if (((uintptr_t)a.x) % 16 != 0 || (a.ld * es) % 16 != 0) return false;
+    if (a.code4 && ((uintptr_t)a.q) % 4 != 0) return false;
+    if (!a.code4 && ((uintptr_t)a.q) % 8 != 0) return false;
+    if (a.gran == QLIN_PER_GROUP) {
+        if (a.group % 8 != 0 || a.group > 256) return false;
+        int gl = a.group / 8;
+        if (gl & (gl - 1)) return false;  // power of two lanes
+    }
+    if (a.cols / 8 > 8 * 512) return false;
+    if (a.smooth_mode != QLIN_SMOOTH_NONE && ((uintptr_t)a.smooth) % 16 != 0) return false;
+    return true;
+}
+
+template <typename T>
+static cudaError_t launch_rows(const QuantArgs& a, cudaStream_t st) {
+    int64_t nchunks = a.cols / 8;
+    int cpt = (nchunks <= 512) ? 1 : (nchunks <= 1024) ? 2 : (nchunks <= 2048) ? 4 : 8;
+    int64_t nt = ceil_div(nchunks, cpt);
+    nt = ceil_div(nt, 32) * 32;
+    if (a.gran == QLIN_PER_GROUP) {
+        int gl = a.group / 8;
+        if (nt % gl) nt = ceil_div(nt, gl) * gl;
+    }
+    if (nt < 32) nt = 32;
+    int per_sm = (int)(2048 / nt);
+    if (per_sm < 1) per_sm = 1;
+    int64_t grid = (int64_t)num_sms() * per_sm;
+    if (grid > a.rows) grid = a.rows;
+    if (grid < 1) grid = 1;
+    switch (cpt) {
+    case 1: k_quant_rows<T, 1><<<(unsigned)grid, (unsigned)nt, 0, st>>>(a); break;
+    case 2: k_quant_rows<T, 2><<<(unsigned)grid, (unsigned)nt, 0, st>>>(a); break;
+    case 4: k_quant_rows<T, 4><<<(unsigned)grid, (unsigned)nt, 0, st>>>(a); break;
+    default: k_quant_rows<T, 8><<<(unsigned)grid, (unsigned)nt, 0, st>>>(a); break;
+    }
+    return cudaGetLastError();
+}
+
+static void strip_grid(int64_t nchunks, int64_t rows, dim3& grid, int& rows_per_block) {
+    int64_t cpb = nchunks < 256 ? nchunks : 256;
+    int64_t gx = ceil_div(nchunks, cpb);
+    int64_t target = (int64_t)num_sms() * 8;  // blocks in flight
+    int64_t gy = ceil_div(target, gx);
+    if (gy > rows) gy = rows;
+    if (gy < 1) gy = 1;
+    rows_per_block = (int)ceil_div(rows, gy);
+    gy = ceil_div(rows, rows_per_block);
+    grid = dim3((unsigned)gx, (unsigned)gy);
+}
+
+static bool strip_ok(const QuantArgs& a, int xt) {
+    int es = elem_size(xt);
+    if (a.cols % 8 != 0 || a.rows == 0) return false;
+    if (a.smooth_mode != QLIN_SMOOTH_NONE && ((uintptr_t)a.smooth) % 16 != 0) return false;
+    if (((uintptr_t)a.x) % 16 != 0 || (a.ld * es) % 16 != 0) return false;
+    if (a.code4 && ((uintptr_t)a.q) % 4 != 0) return false;
+    if (!a.code4 && ((uintptr_t)a.q) % 8 != 0) return false;
+    return true;
+}
+
+static int64_t nscopes_of(const QuantArgs& a) {
+    switch (a.gran) {
+    case QLIN_PER_TENSOR: return 1;
+    case QLIN_PER_ROW: return a.rows;
+    case QLIN_PER_COL: return a.cols;
+    default: return a.rows * (a.cols / a.group);
+    }
+}
+
+size_t quantize_ws_bytes(int64_t rows, int64_t cols, const qlin_qparams* p) {
+    if (p->static_scale) return 0;
+    if (p->clip_percentile > 0.0) return (size_t)(kHist1 + kHist2 + 4) * 4;
+    if (p->gran == QLIN_PER_TENSOR) return 2 * 4;
+    if (p->gran == QLIN_PER_COL) return (size_t)cols * 2 * 4;
+    // per-row / per-group: the fused row kernel needs nothing; the generic
+    // fallback needs one pair of words per scope.
+    int64_t ns = (p->gran == QLIN_PER_ROW) ? rows : (p->group > 0 ? rows * (cols / p->group) : 0);
+    return (size_t)ns * 2 * 4;
+}
+
+template <typename T>
+static cudaError_t run_quantize_t(QuantArgs a, int xt, const qlin_qparams* p, void* ws, cudaStream_t st) {
+    cudaError_t e = cudaSuccess;
+    const int64_t n = a.rows * a.cols;
+    const int gblocks = num_sms() * 4;
+    const bool row_local = (a.gran == QLIN_PER_ROW || a.gran == QLIN_PER_GROUP);
+    if (row_local && rows_kernel_ok(a, xt) && p->clip_percentile <= 0.0) return launch_rows<T>(a, st);
+
+    // Stats (dynamic) -> finalize -> codes.
+    if (!a.static_scale) {
+        uint32_t* stat = reinterpret_cast<uint32_t*>(ws);
+        if (p->clip_percentile > 0.0) {
+            uint32_t* hist1 = stat;
+            uint32_t* hist2 = stat + kHist1;
+            uint32_t* sel = hist2 + kHist2;
+            uint64_t k = (uint64_t)percentile_rank(n, p->clip_percentile);
+            if ((e = cudaMemsetAsync(ws, 0, (size_t)(kHist1 + kHist2 + 4) * 4, st)) != cudaSuccess) return e;
+            cudaFuncSetAttribute(k_hist1<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, kHist1 * 4);
+            k_hist1<T><<<num_sms(), 1024, kHist1 * 4, st>>>(a, hist1);
+            // Low 16 bits of |x| are zero for unsmoothed bf16 input.
+            bool need2 = !(xt == QLIN_BF16 && a.smooth_mode == QLIN_SMOOTH_NONE);
+            k_select1<<<1, 1024, 0, st>>>(a, hist1, sel, k, need2 ? 0 : 1);
+            if (need2) {
+                k_hist2<T><<<gblocks, 256, 0, st>>>(a, sel, hist2);
+                k_select2<<<1, 1024, 0, st>>>(a, hist2, sel);
+            }
+        } else {
+            int64_t ns = nscopes_of(a);
+            if ((e = cudaMemsetAsync(ws, 0, (size_t)ns * 8, st)) != cudaSuccess) return e;
+            if (!row_local && strip_ok(a, xt)) {
+                dim3 grid;
+                int rpb;
+                strip_grid(a.cols / 8, a.rows, grid, rpb);
+                k_stats_strip<T><<<grid, 256, 0, st>>>(a, stat, rpb);
+            } else {
+                k_stats_generic<T><<<gblocks, 256, 0, st>>>(a, stat);
+            }
+            k_finalize<<<(unsigned)ceil_div(ns, 256), 256, 0, st>>>(a, stat, ns);
+        }
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    }
+    if (a.absmax_out) return cudaGetLastError();
+    if (!row_local && strip_ok(a, xt)) {
+        dim3 grid;
+        int rpb;
+        strip_grid(a.cols / 8, a.rows, grid, rpb);
+        k_quant_strip<T><<<grid, 256, 0, st>>>(a, rpb);
+    } else {
+        k_quant_generic<T><<<gblocks, 256, 0, st>>>(a);
+    }
+    return cudaGetLastError();
+}
+
+cudaError_t run_quantize(const void* x, int xt, int64_t rows, int64_t cols, int64_t ld, const float* smooth,
+                         const qlin_qparams* p, void* q, void* s, int32_t* z, void* ws, cudaStream_t st) {
+    QuantArgs a;
+    a.x = x;
+    a.rows = rows;
+    a.cols = cols;
+    a.ld = ld;
+    a.smooth = smooth;
+    a.smooth_mode = p->smooth_mode;
+    a.qmin = p->qmin;
+    a.qmax = p->qmax;
+    a.sym = p->symmetric;
+    a.gran = p->gran;
+    a.group = p->group;
+    a.scale_f16 = (p->scale_dtype == QLIN_F16);
+    a.static_scale = p->static_scale;
+    a.code4 = (p->code == QLIN_S4 || p->code == QLIN_U4);
+    a.q = q;
+    a.s = s;
+    a.z = z;
+    a.absmax_out = nullptr;
+    switch (xt) {
+    case QLIN_BF16: return run_quantize_t<__nv_bfloat16>(a, xt, p, ws, st);
+    case QLIN_F16: return run_quantize_t<__half>(a, xt, p, ws, st);
+    default: return run_quantize_t<float>(a, xt, p, ws, st);
+    }
+}
+
+cudaError_t run_absmax(const void* x, int xt, int64_t rows, int64_t cols, int64_t ld, int gran, int group,
+                       float* out, void* ws, cudaStream_t st) {
+    qlin_qparams p{};
+    p.code = QLIN_S8;
+    p.qmin = -127;
+    p.qmax = 127;
+    p.symmetric = 1;
+    p.gran = (qlin_gran)gran;
+    p.group = group;
+    p.scale_dtype = QLIN_F32;
+    QuantArgs a{};
+    a.x = x;
+    a.rows = rows;
+    a.cols = cols;
+    a.ld = ld;
+    a.smooth_mode = QLIN_SMOOTH_NONE;
+    a.qmin = -127;
+    a.qmax = 127;
+    a.sym = 1;
+    a.gran = gran;
+    a.group = group;
+    a.absmax_out = out;
+    a.q = nullptr;
+    switch (xt) {
+    case QLIN_BF16: return run_quantize_t<__nv_bfloat16>(a, xt, &p, ws, st);
+    case QLIN_F16: return run_quantize_t<__half>(a, xt, &p, ws, st);
+    default: return run_quantize_t<float>(a, xt, &p, ws, st);
+    }
+}
+
+cudaError_t run_dequantize(const void* q, const void* s, const int32_t* z, const qlin_qparams* p, int64_t rows,
+                           int64_t cols, void* y, int yt, cudaStream_t st) {
+    DequantArgs d;
+    d.q = q;
+    d.s = s;
+    d.z = z;
+    d.rows = rows;
+    d.cols = cols;
+    d.gran = p->gran;
+    d.group = p->group;
+    d.scale_f16 = (p->scale_dtype == QLIN_F16);
+    d.code4 = (p->code == QLIN_S4 || p->code == QLIN_U4);
+    d.code_signed = (p->code == QLIN_S8 || p->code == QLIN_S4);
+    d.y = y;
+    d.yt = yt;
+    int blocks = num_sms() * 8;
+    int ys = (yt == QLIN_F32) ? 4 : 2;
+    bool vec = (cols % 8 == 0) && (p->gran != QLIN_PER_GROUP || p->group % 8 == 0) &&
+               ((uintptr_t)q % (d.code4 ? 4 : 8) == 0) && ((uintptr_t)y % (8 * ys) == 0);
+    if (vec)
+        k_dequant_vec<<<blocks, 256, 0, st>>>(d);
+    else
+        k_dequant_generic<<<blocks, 256, 0, st>>>(d);
+    return cudaGetLastError();
+}
+
+cudaError_t run_smooth_factors(const float* xmax, const float* wmax, int64_t K, float alpha, float* s,
+                               cudaStream_t st) {
+    k_smooth_factors<<<(unsigned)ceil_div(K, 256), 256, 0, st>>>(xmax, wmax, K, alpha, s);
+    return cudaGetLastError();
+}
+
+int64_t percentile_rank(int64_t n, double p) {
+    double k = ceil((double)n * p / 100.0);
+    if (k < 1.0) k = 1.0;
+    if (k > (double)n) k = (double)n;
+    return (int64_t)k;
+}
+
+}  // namespace qlin

@@ -1,0 +1,479 @@
+#!/usr/bin/env python3
+"""Benchmark of the quantized linear layer on B300.
+
+One step = one pass of the whole hot path over one batch of the 70B-shaped
+down-projection workload (W [8192 x 28672]):
+  1. qlin_quantize   X bf16 [4096 x 28672] -> per-token INT8, after dividing by
+                     the folded SmoothQuant factors (alpha = 0.5)
+  2. qlin_gemm_w8a8  4096 x 8192 x 28672, INT32 sums, bf16 out
+  3. qlin_gemm_w4a16 UINT4 asymmetric g=128 fp16 scales, M = 1, 8, 64, 256
+  4. qlin_dequantize the INT8 activations back to bf16
+The reported value is the step's fraction of the B300 roofline: the sum over
+kernels of max(bytes / HBM peak, ops / tensor peak) divided by the measured
+step time, summed over ranks (so N replicas report up to N x 100).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+"""
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import threading
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from activation_quantization_quantize_b300 import inputs, qlin  # noqa: E402
+
+METRIC = "W8A8 GEMM TOPS and W4A16 decode weight-GB/s, as % of B300 roofline"
+UNIT = "% of one B300 roofline (whole job)"
+M8, N, K = 4096, 8192, 28672
+W4_MS = (1, 8, 64, 256)
+GROUP = 128
+L2_BYTES = 126 * 1024 * 1024
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return {"hbm_gbs": float(d["hbm_gbs"]), "bf16_tflops": float(d["bf16_tflops"]),
+                "bf16_tflops_sustained": float(d.get("bf16_tflops_sustained", d["bf16_tflops"])),
+                "source": "measured"}
+    return {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0, "source": "fallback"}
+
+
+# ------------------------------------------------------------------ roofline model
+def kernel_bytes_flops():
+    """Algorithmic bytes / ops of each kernel of one step."""
+    d = {}
+    # quantize: read X bf16 + smoothing factors, write int8 codes + fp32 scales
+    d["quantize"] = (M8 * K * 2 + K * 4 + M8 * K + M8 * 4, 0.0)
+    # W8A8: read both operands once, write bf16 Y; 2*M*N*K integer ops
+    d["gemm_w8a8"] = (M8 * K + N * K + M8 * 4 + N * 4 + M8 * N * 2, 2.0 * M8 * N * K)
+    w4_bytes = N * K // 2 + N * (K // GROUP) * 2 + N * (K // GROUP) // 2
+    for m in W4_MS:
+        d["gemm_w4a16_m%d" % m] = (w4_bytes + m * K * 2 + m * N * 2, 2.0 * m * N * K)
+    # dequantize: read int8 codes + scales, write bf16
+    d["dequantize"] = (M8 * K + M8 * 4 + M8 * K * 2, 0.0)
+    return d
+
+
+def roofline_seconds(nbytes, ops, peaks, int8_peak_tflops):
+    t_mem = nbytes / (peaks["hbm_gbs"] * 1e9)
+    t_ops = ops / (int8_peak_tflops * 1e12) if ops else 0.0
+    return max(t_mem, t_ops)
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    """nvidia-smi samples (200 ms) during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index):
+        self.dev = device_index
+        self.proc = None
+        self.t0 = self.t1 = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.dev), "--query-gpu=timestamp," + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.reader = threading.Thread(target=self._read, daemon=True)
+            self.reader.start()
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def mark(self, begin):
+        if begin:
+            self.t0 = time.time()
+        else:
+            self.t1 = time.time()
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = [l for (t, l) in self.lines if self.t0 is not None and self.t0 - 0.1 <= t <= (self.t1 or t) + 0.1]
+        if not rows:
+            rows = [l for (_, l) in self.lines]
+        sm, smax, reasons = [], [], set()
+        for l in rows:
+            f = [x.strip() for x in l.split(",")]
+            if len(f) < 10:
+                continue
+            try:
+                sm.append(float(f[2]))
+                smax.append(float(f[3]))
+            except ValueError:
+                continue
+            names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+            for name, v in zip(names, f[6:10]):
+                if v.lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ workload
+class Step:
+    """Device-resident inputs and the launch sequence of one step."""
+
+    def __init__(self, dev, n_w4_copies=len(W4_MS)):
+        torch.cuda.set_device(dev)
+        self.dev = dev
+        # activations and weights (seeded synthetic)
+        x = inputs.downproj_activation(M8, outliers=True)
+        w = inputs.downproj_weight()
+        self.x = x.to(dev)
+        wd = w.to(dev)
+        del x, w
+        # SmoothQuant factors (alpha = 0.5) from the channel maxima; weights smoothed offline
+        xmax = qlin.absmax(self.x, qlin.QLIN_PER_COL)
+        wmax = qlin.absmax(wd, qlin.QLIN_PER_COL)
+        self.smooth = qlin.smooth_factors(xmax, wmax, 0.5)
+        pw = qlin.make_params("s8", "row", smooth_mode=qlin.QLIN_SMOOTH_MULTIPLY)
+        self.qw, self.sw, _ = qlin.quantize(wd, pw, smooth=self.smooth)
+        # W4A16 weights (unsmoothed W), one packed copy per call so no call finds
+        # its weights in L2
+        p4 = qlin.make_params("u4", "group", group=GROUP, scale_f16=True)
+        q4, s4, z4 = qlin.quantize(wd, p4)
+        self.w4 = []
+        for _ in range(n_w4_copies):
+            self.w4.append(qlin.pack_w4(q4, s4, z4, N, K, GROUP))
+        del q4, s4, z4, wd
+        self.xs = [inputs.downproj_activation(m).to(dev) for m in W4_MS]
+        # outputs / scratch
+        self.px = qlin.make_params("s8", "row", smooth_mode=qlin.QLIN_SMOOTH_DIVIDE)
+        self.qx = torch.empty((M8, K), dtype=torch.int8, device=dev)
+        self.sx = torch.empty(M8, dtype=torch.float32, device=dev)
+        nb = qlin.qlin_workspace_size(qlin.QLIN_OP_QUANTIZE, M8, K, 0, self.px)
+        self.ws_q = torch.empty(max(nb, 16), dtype=torch.uint8, device=dev)
+        self.ws_q_bytes = nb
+        self.y8 = torch.empty((M8, N), dtype=torch.bfloat16, device=dev)
+        self.y4 = [torch.empty((m, N), dtype=torch.bfloat16, device=dev) for m in W4_MS]
+        self.xhat = torch.empty((M8, K), dtype=torch.bfloat16, device=dev)
+        nb8 = qlin.qlin_workspace_size(qlin.QLIN_OP_GEMM_W8A8, M8, N, K)
+        self.ws8 = torch.empty(max(nb8, 16), dtype=torch.uint8, device=dev)
+        self.ws8_bytes = nb8
+        torch.cuda.synchronize()
+
+    names = ["quantize", "gemm_w8a8"] + ["gemm_w4a16_m%d" % m for m in W4_MS] + ["dequantize"]
+    launches_per_step = 7
+
+    def run(self, stream, events=None):
+        """Enqueue one step; events (len 8) bracket each kernel if given."""
+        def ev(i):
+            if events is not None:
+                events[i].record(stream)
+        ev(0)
+        qlin.qlin_quantize(self.x, qlin.QLIN_BF16, M8, K, K, self.smooth, self.px, self.qx, self.sx, None,
+                           self.ws_q, self.ws_q_bytes, stream)
+        ev(1)
+        qlin.qlin_gemm_w8a8(self.qx, self.sx, self.qw, self.sw, M8, N, K, self.y8, qlin.QLIN_BF16, None,
+                            self.ws8, self.ws8_bytes, stream)
+        ev(2)
+        for i, m in enumerate(W4_MS):
+            packed, hdr = self.w4[i % len(self.w4)]
+            qlin.qlin_gemm_w4a16(self.xs[i], packed, hdr, m, self.y4[i], None, 0, stream)
+            ev(3 + i)
+        qlin.qlin_dequantize(self.qx, self.sx, None, self.px, M8, K, self.xhat, qlin.QLIN_BF16, stream)
+        ev(7)
+
+
+def measure_int8_reference_peak(dev):
+    """Best torch._int_mm (cuBLASLt INT8) throughput on 8192^3, TFLOP/s."""
+    try:
+        a = torch.randint(-127, 128, (8192, 8192), dtype=torch.int8, device=dev)
+        b = torch.randint(-127, 128, (8192, 8192), dtype=torch.int8, device=dev).t()
+        for _ in range(3):
+            torch._int_mm(a, b)
+        torch.cuda.synchronize()
+        best = float("inf")
+        for _ in range(10):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            torch._int_mm(a, b)
+            e1.record()
+            e1.synchronize()
+            best = min(best, e0.elapsed_time(e1) / 1e3)
+        del a, b
+        return 2.0 * 8192 ** 3 / best / 1e12
+    except Exception:  # noqa: BLE001 -- a missing INT8 library path is recorded as absent
+        return None
+
+
+# ------------------------------------------------------------------ CPU baseline (oracle)
+def oracle_step_seconds(rows_w8, threads):
+    """Time the CPU oracle on a bounded sample of one step; return
+    (extrapolated seconds of a full step, sample description)."""
+    import oracle
+    from activation_quantization_quantize_b300.inputs import normal
+
+    oracle.set_threads(threads)
+    rng_rows = rows_w8
+    x = normal((rng_rows, K), 1.0, 101)
+    sm = np.random.default_rng(102).uniform(0.2, 5, K).astype(np.float32)
+    wq = np.random.default_rng(103).integers(-127, 128, (N, K)).astype(np.int8)
+    sw = np.random.default_rng(104).uniform(1e-4, 1e-3, N).astype(np.float32)
+    w4q = np.random.default_rng(105).integers(0, 16, (N, K)).astype(np.int32)
+    w4s = np.random.default_rng(106).uniform(1e-4, 1e-3, N * (K // GROUP)).astype(np.float32)
+    w4z = np.random.default_rng(107).integers(0, 16, N * (K // GROUP)).astype(np.int32)
+    t = {}
+    t0 = time.perf_counter()
+    qx, sx, _ = oracle.quantize(x, -127, 127, True, oracle.PER_ROW, smooth=sm, smooth_mode=oracle.SMOOTH_DIVIDE)
+    t["quantize"] = time.perf_counter() - t0
+    t0 = time.perf_counter()
+    acc = oracle.w8a8_acc(qx.astype(np.int8), wq)
+    oracle.w8a8_out(acc, sx, sw)
+    t["gemm_w8a8"] = time.perf_counter() - t0
+    t0 = time.perf_counter()
+    what = oracle.w4_dequant(w4q, w4s, w4z, GROUP)
+    t["w4_dequant"] = time.perf_counter() - t0
+    x1 = normal((1, K), 1.0, 108)
+    t0 = time.perf_counter()
+    oracle.matmul_f64(x1, what)
+    t["gemm_w4a16_m1"] = time.perf_counter() - t0
+    t0 = time.perf_counter()
+    oracle.dequantize(qx, sx, None, oracle.PER_ROW)
+    t["dequantize"] = time.perf_counter() - t0
+    scale = M8 / rows_w8
+    full = (t["quantize"] + t["gemm_w8a8"] + t["dequantize"]) * scale
+    full += len(W4_MS) * t["w4_dequant"] + sum(m * t["gemm_w4a16_m1"] for m in W4_MS)
+    sample = ("oracle on %d of %d activation rows (quantize, W8A8 int64 sums, dequantize), "
+              "full W4 dequant + an M=1 fp64 GEMV; extrapolated linearly to one step" % (rows_w8, M8))
+    return full, sample
+
+
+def cpu_threads():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+# ------------------------------------------------------------------ main
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        torch.distributed.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        torch.distributed.barrier()
+
+
+def max_over_ranks(v, world, dev):
+    if world == 1:
+        return v
+    t = torch.tensor([v], dtype=torch.float64, device=dev)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def run_reference(args, world, rank):
+    """The oracle as it stands on the host cores, on bounded samples of the step."""
+    if rank != 0:
+        return
+    peaks = load_peaks()
+    bf = kernel_bytes_flops()
+    int8_peak = peaks["bf16_tflops"]
+    t_roof = sum(roofline_seconds(b, f, peaks, int8_peak) for b, f in bf.values())
+    threads = cpu_threads()
+    per_step_budget = 150.0 / max(1, args.steps + args.warmup)
+    rows = 1 if per_step_budget < 4.0 else 2
+    for _ in range(args.warmup):
+        oracle_step_seconds(rows, threads)
+    times = []
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        full, sample = oracle_step_seconds(rows, threads)
+        times.append(full)
+    wall = time.perf_counter() - t0
+    step = statistics.mean(times)
+    value = 100.0 * t_roof / step
+    out = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+           "steps": args.steps, "warmup": args.warmup, "ms_per_step": step * 1e3, "higher_is_better": True,
+           "scaling": "weak", "vs_baseline": None, "dtype": "int64+f64", "data": "synthetic",
+           "config": {"workload": "70B down-projection W[8192x28672]: quantize+W8A8 M=4096, W4A16 M=1/8/64/256",
+                      "note": "CPU oracle on bounded samples per step, extrapolated", "sample_wall_s": wall},
+           "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle", "sample": sample},
+           "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(out))
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=10)
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+
+    world, rank, local = dist_setup()
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+        if world > 1:
+            torch.distributed.destroy_process_group()
+        return
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    qlin.load()
+    peaks = load_peaks()
+    step = Step(dev)
+    stream = torch.cuda.Stream(device=dev)
+    int8_ref = measure_int8_reference_peak(dev)
+    int8_peak = max(peaks["bf16_tflops"], int8_ref or 0.0)
+
+    # warm-up
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            step.run(stream)
+    stream.synchronize()
+    if qlin.qlin_device_error(stream) != 0:
+        raise RuntimeError("device-side error during warm-up")
+
+    # timed region: per-kernel events inside, whole-region events around
+    uuid = str(getattr(torch.cuda.get_device_properties(dev), "uuid", "") or "")
+    clocks = ClockSampler(("GPU-" + uuid) if uuid and not uuid.startswith("GPU-") else (uuid or local))
+    clocks.start()
+    time.sleep(0.4)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(8)] for _ in range(args.steps)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    clocks.mark(True)
+    start.record(stream)
+    for i in range(args.steps):
+        step.run(stream, evs[i])
+    end.record(stream)
+    torch.cuda.synchronize()
+    clocks.mark(False)
+    barrier(world)
+    clock_info = clocks.stop()
+    elapsed = start.elapsed_time(end) / 1e3
+    elapsed = max_over_ranks(elapsed, world, dev)
+    err = qlin.qlin_device_error(stream)
+    if err != 0:
+        raise RuntimeError("device-side error in timed region: %d" % err)
+
+    per_kernel = {}
+    for k, name in enumerate(Step.names):
+        per_kernel[name] = statistics.mean(evs[i][k].elapsed_time(evs[i][k + 1]) for i in range(args.steps)) / 1e3
+    bf = kernel_bytes_flops()
+    t_roof = sum(roofline_seconds(bf[n][0], bf[n][1], peaks, int8_peak) for n in Step.names)
+    ms_per_step = elapsed / args.steps * 1e3
+    value = world * 100.0 * t_roof / (elapsed / args.steps)
+
+    t8 = per_kernel["gemm_w8a8"]
+    w8_tops = bf["gemm_w8a8"][1] / t8 / 1e12
+    roofline = {"bound": "tensor", "achieved": w8_tops, "peak": int8_peak, "unit": "TFLOP/s",
+                "frac": w8_tops / int8_peak, "traffic": None,
+                "kernel": "gemm_w8a8 (4096x8192x28672 int8 ops)",
+                "peak_source": "max(bf16 dense %s %.1f, torch._int_mm %s)" % (
+                    peaks["source"], peaks["bf16_tflops"], "%.1f" % int8_ref if int8_ref else "n/a")}
+    detail = {}
+    for name in Step.names:
+        b, f = bf[name]
+        t = per_kernel[name]
+        d = {"us": t * 1e6, "gbs": b / t / 1e9, "roofline_frac": roofline_seconds(b, f, peaks, int8_peak) / t}
+        if f:
+            d["tops"] = f / t / 1e12
+        detail[name] = d
+    w4_weight_bytes = N * K // 2 + N * (K // GROUP) * 2 + N * (K // GROUP) // 2
+    detail["w4a16_decode_weight_gbs_m1"] = w4_weight_bytes / per_kernel["gemm_w4a16_m1"] / 1e9
+    detail["w4a16_decode_frac_m1"] = detail["w4a16_decode_weight_gbs_m1"] / peaks["hbm_gbs"]
+
+    # end to end through the C ABI with host buffers: H2D of the step's
+    # activations, the step, D2H of its outputs
+    x_host = step.x.cpu().pin_memory()
+    xs_host = [t.cpu().pin_memory() for t in step.xs]
+    y8_host = torch.empty(step.y8.shape, dtype=step.y8.dtype).pin_memory()
+    y4_host = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in step.y4]
+    h2d = x_host.numel() * 2 + sum(t.numel() * 2 for t in xs_host)
+    d2h = y8_host.numel() * 2 + sum(t.numel() * 2 for t in y4_host)
+
+    def e2e_step():
+        step.x.copy_(x_host, non_blocking=True)
+        for d_, h_ in zip(step.xs, xs_host):
+            d_.copy_(h_, non_blocking=True)
+        step.run(stream)
+        y8_host.copy_(step.y8, non_blocking=True)
+        for h_, d_ in zip(y4_host, step.y4):
+            h_.copy_(d_, non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for _ in range(2):
+            e2e_step()
+        stream.synchronize()
+        barrier(world)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.e2e_steps):
+            e2e_step()
+        e1.record(stream)
+        stream.synchronize()
+    e2e_t = max_over_ranks(e0.elapsed_time(e1) / 1e3 / args.e2e_steps, world, dev)
+    e2e_value = world * 100.0 * t_roof / e2e_t
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        threads = cpu_threads()
+        full, sample = oracle_step_seconds(4, threads)
+        cpu = {"value": 100.0 * t_roof / full, "unit": UNIT, "cores": threads, "kind": "oracle",
+               "sample": sample, "seconds_per_step": full}
+
+    if rank == 0:
+        out = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+               "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+               "scaling": "weak", "vs_baseline": None, "dtype": "int8xint8->int32, bf16 (w4a16)",
+               "data": "synthetic",
+               "config": {"workload": "70B down-projection W[8192x28672]: smoothed per-token quantize + "
+                                      "W8A8 M=4096 + W4A16 UINT4 g128 M=1/8/64/256 + dequantize",
+                          "M_w8a8": M8, "N": N, "K": K, "w4_group": GROUP, "w4_M": list(W4_MS),
+                          "l2": "every operand > L2 or read from a distinct copy (one packed W4 copy per call)",
+                          "parallelism": "replicas" if world > 1 else "single GPU"},
+               "roofline": roofline, "cpu_baseline": cpu,
+               "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                       "ms_per_step": e2e_t * 1e3},
+               "gpu_launches": Step.launches_per_step * args.steps,
+               "clocks": clock_info, "peaks": peaks, "int8_ref_tflops": int8_ref, "detail": detail}
+        print(json.dumps(out))
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,241 @@
+/*
+ * qlin.h -- C ABI of libqlin.so, a quantized linear layer for NVIDIA B300
+ * (sm_103a).
+ *
+ * The method (affine quantizer, its granularities, and the two quantized
+ * linear-layer paths) is the one stated on these pages:
+ *   [QDC]  "量化、蒸馏与模型压缩" (Quantization, distillation and model
+ *          compression), llm-knowledge-atlas notes 03-05: core formula,
+ *          section 1 (error of y = Wx), 1.1 (groups), 2.3 (SmoothQuant).
+ *   [L19]  "十九：模型压缩：量化、ZeroQuant、LLM.int8() 与 SmoothQuant":
+ *          section 3 (basic formula), 4 (granularity), 6 (W8A8).
+ *   [CH11] "第11章 模型量化与压缩" (ai-infra-guide chapter 11): 11.1.1-11.1.6
+ *          (affine quantization, symmetric/asymmetric, granularity, dynamic vs
+ *          static, calibration, INT4 worked case), 11.4.2-11.4.5 (SmoothQuant).
+ *   [CSDN] "大模型压缩：从研究到生产的完整攻略（1）": symmetric and
+ *          asymmetric quantization sections, outliers.
+ *
+ * Conventions for every entry point:
+ *   - Pointers named as device pointers must be CUDA device (or managed)
+ *     memory on the current device; the caller owns every buffer.  The library
+ *     allocates no memory except where an entry point says so.
+ *   - Work is enqueued on `stream` (a cudaStream_t; NULL = legacy default
+ *     stream) and returns without synchronizing.
+ *   - Arguments are validated on the host before any launch.  On a bad
+ *     argument the call returns a negative qlin_status and launches nothing.
+ *     A failed launch returns QLIN_ERR_CUDA.  No C++ exception crosses the ABI.
+ *   - Inputs must be finite; results for NaN/Inf inputs are unspecified (but
+ *     never out-of-bounds accesses).
+ *   - Rounding: codes are round-half-to-even of the correctly rounded binary32
+ *     quotient fl(x/s), and the zero point is added after rounding.
+ */
+#ifndef QLIN_H
+#define QLIN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    QLIN_OK = 0,
+    QLIN_ERR_ARG = -1,          /* invalid argument (shape, pointer, range) */
+    QLIN_ERR_UNSUPPORTED = -2,  /* valid for the method, not implemented    */
+    QLIN_ERR_CUDA = -3,         /* a CUDA runtime call or launch failed      */
+    QLIN_ERR_TIMEOUT = -4,      /* a bounded device-side wait gave up        */
+    QLIN_ERR_WORKSPACE = -5,    /* workspace missing or too small            */
+    QLIN_ERR_LAYOUT = -6        /* packed-weight header does not match       */
+} qlin_status;
+
+/* Granularity: which elements share one scale / zero point
+ * ([L19] section 4; [CH11] 11.1.3 table 11-1; [QDC] 1.1). */
+typedef enum {
+    QLIN_PER_TENSOR = 0,  /* one scope                                          */
+    QLIN_PER_ROW = 1,     /* one per row: per-token (activations) or per-output-
+                             channel (weights stored [out x in])                */
+    QLIN_PER_COL = 2,     /* one per column: per-input-channel                  */
+    QLIN_PER_GROUP = 3    /* one per g contiguous elements of a row             */
+} qlin_gran;
+
+typedef enum {
+    QLIN_F32 = 0, QLIN_BF16 = 1, QLIN_F16 = 2,
+    QLIN_S8 = 3, QLIN_U8 = 4, QLIN_S4 = 5, QLIN_U4 = 6, QLIN_S32 = 7
+} qlin_dtype;
+
+typedef enum {
+    QLIN_SMOOTH_NONE = 0,
+    QLIN_SMOOTH_DIVIDE = 1,   /* x' = fl(x / smooth[c])  -- X diag(s)^-1 ([QDC] 2.3) */
+    QLIN_SMOOTH_MULTIPLY = 2  /* x' = fl(x * smooth[c])  -- diag(s) W (weights)      */
+} qlin_smooth;
+
+/* Quantization parameters: the pages' (s, z, qmin/qmax, g, granularity)
+ * statement of the problem ([QDC] symbol table; [CH11] 11.1.1-11.1.5). */
+typedef struct {
+    qlin_dtype code;         /* code storage: QLIN_S8, QLIN_U8, QLIN_S4, QLIN_U4      */
+    int qmin, qmax;          /* integer range, must fit `code`; e.g. [-127,127]      */
+    int symmetric;           /* 1: z = 0, s = absmax/qmax, needs qmin == -qmax        */
+    qlin_gran gran;
+    int group;               /* g for QLIN_PER_GROUP (must divide cols), else ignored */
+    double clip_percentile;  /* 0: min-max; else p in (0,100]: symmetric per-tensor
+                                nearest-rank percentile of |x| replaces max|x|        */
+    qlin_dtype scale_dtype;  /* QLIN_F32 or QLIN_F16 (stored scale is what quantizes) */
+    int static_scale;        /* 1: read caller's s (and z); 0: compute them (dynamic) */
+    int smooth_mode;         /* qlin_smooth                                           */
+} qlin_qparams;
+
+/* Operation ids for qlin_workspace_size. */
+enum { QLIN_OP_QUANTIZE = 0, QLIN_OP_ABSMAX = 1, QLIN_OP_GEMM_W8A8 = 2, QLIN_OP_GEMM_W4A16 = 3 };
+
+/* Library version (major*10000 + minor*100 + patch). */
+int qlin_version(void);
+
+/* Human-readable text of a qlin_status (static string, never NULL). */
+const char *qlin_status_string(int status);
+
+/*
+ * Bytes of device workspace an operation needs (0 = none; pass ws = NULL).
+ * For QLIN_OP_QUANTIZE and QLIN_OP_ABSMAX, M = rows, N = cols, K ignored
+ * (for ABSMAX, p->gran selects the granularity).  The workspace is scratch
+ * owned by the caller; it may be reused once the call's work on `stream`
+ * has completed.
+ */
+size_t qlin_workspace_size(int op, int64_t M, int64_t N, int64_t K, const qlin_qparams *p);
+
+/*
+ * qlin_quantize -- affine quantizer q = clip(round(x/s) + z, qmin, qmax)
+ * ([QDC] core formula; [L19] section 3; [CH11] 11.1.1-11.1.5; [CSDN] linear
+ * quantization), with optional per-column smoothing first ([QDC] 2.3;
+ * [CH11] 11.4.2).
+ *
+ *   x      device, rows x cols elements of type xt (F32, BF16 or F16), row
+ *          stride ld elements (ld >= cols).
+ *   smooth device, cols binary32 factors, or NULL when p->smooth_mode is NONE.
+ *   q      device output codes, dense row-major: S8/U8 one byte per code
+ *          (rows*cols bytes); S4/U4 two codes per byte, element 2i in the low
+ *          nibble, S4 in two's complement (rows*cols/2 bytes; cols even).
+ *   s      device scales, one per scope (1, rows, cols or rows*cols/g), binary32
+ *          or binary16 as p->scale_dtype says; written (dynamic) or read
+ *          (p->static_scale).
+ *   z      device int32 zero points, one per scope; written or read like s.
+ *          May be NULL for symmetric parameters.
+ *   ws     device workspace of qlin_workspace_size(QLIN_OP_QUANTIZE, rows,
+ *          cols, 0, p) bytes (NULL when that is 0).
+ * Dynamic scales: symmetric s = fl(max|x| / qmax); asymmetric
+ * s = fl(fl(rmax - rmin) / (qmax - qmin)) with rmin = min(min x, 0),
+ * rmax = max(max x, 0), z = clip(qmin + rne(fl(-rmin / s)), qmin, qmax).
+ * A scale that comes out as 0 is stored as 1; an F16 scale is rounded to
+ * nearest-even binary16, saturating at 65504.
+ * Percentile clipping (p->clip_percentile > 0) is supported for symmetric
+ * QLIN_PER_TENSOR only (else QLIN_ERR_UNSUPPORTED); its rank is
+ * k = ceil(n * p / 100) computed in binary64, clamped to [1, n].
+ */
+int qlin_quantize(const void *x, qlin_dtype xt, int64_t rows, int64_t cols, int64_t ld,
+                  const float *smooth, const qlin_qparams *p,
+                  void *q, void *s, int32_t *z, void *ws, size_t ws_bytes, void *stream);
+
+/*
+ * qlin_dequantize -- x^ = s * (q - z) ([QDC] core formula; [CSDN] asymmetric
+ * dequantization), evaluated as one binary32 product and then rounded to yt
+ * (F32, BF16 or F16, nearest-even).
+ *   q, s, z  device, in the layouts qlin_quantize writes for p (z may be NULL
+ *            for symmetric parameters).
+ *   y        device output, rows x cols dense row-major of type yt.
+ */
+int qlin_dequantize(const void *q, const void *s, const int32_t *z, const qlin_qparams *p,
+                    int64_t rows, int64_t cols, void *y, qlin_dtype yt, void *stream);
+
+/*
+ * qlin_absmax -- max|x| of every scope of the given granularity (the
+ * symmetric-scale statistic; with QLIN_PER_COL on X and on W it gives the
+ * channel maxima SmoothQuant's factors are built from, [CH11] 11.4.5 step 1).
+ *   x    device, rows x cols of type xt, row stride ld.
+ *   out  device binary32, one value per scope.
+ *   ws   device workspace of qlin_workspace_size(QLIN_OP_ABSMAX, rows, cols,
+ *        0, p) bytes where p->gran = gran.
+ */
+int qlin_absmax(const void *x, qlin_dtype xt, int64_t rows, int64_t cols, int64_t ld,
+                qlin_gran gran, int group, float *out, void *ws, size_t ws_bytes, void *stream);
+
+/*
+ * qlin_smooth_factors -- s_j = max|X_j|^alpha / max|W_j|^(1-alpha)
+ * ([QDC] 2.3 eq. 1; [CH11] 11.4.3), j < K.  alpha = 0.5 is evaluated as
+ * fl(sqrt(mx) / sqrt(mw)) with correctly rounded binary32 operations; other
+ * alphas with binary32 pow (a few ulp).  A channel with a zero maximum gets
+ * s_j = 1.  xmax, wmax, s: device binary32 arrays of K values.
+ */
+int qlin_smooth_factors(const float *xmax, const float *wmax, int64_t K, float alpha,
+                        float *s, void *stream);
+
+/* Header at the start of a packed INT4 weight blob (layout version 1). */
+#define QLIN_W4_MAGIC 0x34574C51u  /* "QLW4" */
+#define QLIN_W4_VERSION 1u
+typedef struct {
+    uint32_t magic, version;
+    int64_t N, K;            /* weight is N (output channels) x K (input)     */
+    int32_t group, asym;     /* g in {32, 64, 128}; asym: per-group zero point */
+    uint64_t codes_off, scales_off, zeros_off, total_bytes;  /* byte offsets  */
+} qlin_w4_header;
+
+/* Bytes of the packed blob qlin_pack_w4 writes for these sizes. */
+size_t qlin_pack_w4_size(int64_t N, int64_t K, int group, int asym);
+
+/*
+ * qlin_pack_w4 -- rearrange group-wise INT4 weights ([CH11] 11.1.6: W [N x K]
+ * in row-wise groups of g, 4-bit codes, fp16 per-group scales) into the
+ * layout qlin_gemm_w4a16 streams.
+ *   q      device canonical codes from qlin_quantize: N x K nibbles, two per
+ *          byte (S4 two's complement when z == NULL, else U4).
+ *   s_f16  device binary16 scales, N x K/g, row-major.
+ *   z      device int32 zero points in [0, 15], N x K/g, or NULL (symmetric).
+ *   packed device output of capacity packed_cap >= qlin_pack_w4_size(...).
+ *   hdr    host output (may be NULL): a copy of the blob's header, which
+ *          qlin_gemm_w4a16 takes to describe the blob.
+ * Requirements: K % g == 0, g in {32, 64, 128}, N % 16 == 0, K % 64 == 0.
+ */
+int qlin_pack_w4(const void *q, const void *s_f16, const int32_t *z, int64_t N, int64_t K,
+                 int group, void *packed, size_t packed_cap, qlin_w4_header *hdr, void *stream);
+
+/*
+ * qlin_gemm_w8a8 -- W8A8 linear layer ([L19] section 6; [CH11] 11.1.4,
+ * 11.4.5 step 6): acc[m,n] = sum_k qx[m,k] * qw[n,k] exactly in int32, then
+ * y[m,n] = (float(acc) * sx[m]) * sw[n] in binary32, rounded once to yt.
+ *   qx     device int8 [M x K], row-major (per-token codes).
+ *   sx     device binary32 [M] per-token scales.
+ *   qw     device int8 [N x K], row-major (per-output-channel codes).
+ *   sw     device binary32 [N] per-channel scales.
+ *   y      device output [M x N] of type yt (F32 or BF16), row-major.
+ *   acc_out device int32 [M x N] exact sums, or NULL.
+ * Requirements: K % 16 == 0; qx, qw 16-byte aligned.  The exact sums must fit
+ * int32 (always true for codes in [-127,127] when K < 133,144).
+ */
+int qlin_gemm_w8a8(const int8_t *qx, const float *sx, const int8_t *qw, const float *sw,
+                   int64_t M, int64_t N, int64_t K, void *y, qlin_dtype yt,
+                   int32_t *acc_out, void *ws, size_t ws_bytes, void *stream);
+
+/*
+ * qlin_gemm_w4a16 -- W4A16 linear layer ([CH11] 11.1.6 step 5: dequantize,
+ * then a 16-bit matmul): w^[n,k] = bf16(fl(s[n,k/g] * (q[n,k] - z[n,k/g]))),
+ * y[m,n] = sum_k x[m,k] * w^[n,k] accumulated in binary32, rounded once to
+ * bf16.
+ *   x      device bf16 [M x K], row-major.
+ *   packed device blob written by qlin_pack_w4; hdr its header (host copy).
+ *   y      device bf16 [M x N], row-major.
+ */
+int qlin_gemm_w4a16(const void *x, const void *packed, const qlin_w4_header *hdr, int64_t M,
+                    void *y, void *ws, size_t ws_bytes, void *stream);
+
+/*
+ * qlin_device_error -- synchronizes `stream`, then returns and clears the
+ * library's device-side error word: QLIN_OK, or QLIN_ERR_TIMEOUT when a
+ * bounded wait inside a kernel gave up (that kernel's outputs are then
+ * unspecified).  Returns QLIN_ERR_CUDA if the synchronization itself fails.
+ */
+int qlin_device_error(void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* QLIN_H */

@@ -1,0 +1,197 @@
+"""GPU parity of the two quantized linear-layer paths against the oracle.
+
+W8A8: INT32 sums bit-exact (acc_out), outputs within GEMM_REL_TOL of the
+binary64 oracle sx*sw*acc.  W4A16: the packed blob dequantizes to the
+oracle's w^ = bf16(fl(s (q - z))) and outputs are within GEMM_REL_TOL of the
+binary64 product with that w^."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from activation_quantization_quantize_b300 import inputs, qlin
+from helpers import GEMM_REL_TOL, codes_to_int, host_f32, oracle_quantize, rel_err, scales_f32
+
+pytestmark = pytest.mark.gpu
+
+
+# ------------------------------------------------------------------ W8A8
+def w8a8_run(x_dev, w_dev, out_dtype=torch.float32, smooth=None):
+    """Quantize X per token (optionally smoothed) and W per output channel on
+    the GPU, run the GEMM with acc_out; return device results."""
+    M, K = x_dev.shape
+    N = w_dev.shape[0]
+    px = qlin.make_params("s8", "row", smooth_mode=qlin.QLIN_SMOOTH_DIVIDE if smooth is not None else 0)
+    pw = qlin.make_params("s8", "row", smooth_mode=qlin.QLIN_SMOOTH_MULTIPLY if smooth is not None else 0)
+    qx, sx, _ = qlin.quantize(x_dev, px, smooth=smooth)
+    qw, sw, _ = qlin.quantize(w_dev, pw, smooth=smooth)
+    acc = torch.empty((M, N), dtype=torch.int32, device="cuda")
+    y = qlin.gemm_w8a8(qx, sx, qw, sw, out_dtype=out_dtype, acc_out=acc)
+    torch.cuda.synchronize()
+    return qx, sx, qw, sw, acc, y
+
+
+def test_w8a8_tiny_config():
+    """8x128x256 fp32 with outlier channels 3 and 77, fp32 epilogue."""
+    cfg = inputs.w8a8_tiny()
+    xd = torch.from_numpy(cfg.x).cuda()
+    wd = torch.from_numpy(cfg.w).cuda()
+    qx, sx, qw, sw, acc, y = w8a8_run(xd, wd, torch.float32)
+    p = qlin.make_params("s8", "row")
+    qxo, sxo, _ = oracle_quantize(cfg.x, p)
+    qwo, swo, _ = oracle_quantize(cfg.w, p)
+    np.testing.assert_array_equal(codes_to_int(qx, p, 8, 256), qxo)
+    np.testing.assert_array_equal(codes_to_int(qw, p, 128, 256), qwo)
+    np.testing.assert_array_equal(sx.cpu().numpy().view(np.uint32), sxo.view(np.uint32))
+    acco = oracle.w8a8_acc(qxo, qwo)
+    np.testing.assert_array_equal(acc.cpu().numpy(), acco)
+    yo = oracle.w8a8_out(acco, sxo, swo)
+    assert rel_err(y.cpu().numpy(), yo) < 1e-6            # binary32 epilogue, no bf16 rounding
+    # the five-element page-5 vector through the GPU quantizer, per tensor
+    v = torch.from_numpy(cfg.vec5.reshape(1, 5).repeat(8, 0)[:1, :].copy())
+    v8 = torch.zeros((1, 8), dtype=torch.float32)
+    v8[0, :5] = v[0]
+    q, s, _ = qlin.quantize(v8.cuda(), qlin.make_params("s8", "tensor"))
+    assert list(q.cpu().numpy()[0, :5]) == [30, -73, 127, -48, 103]
+    assert int(s.cpu().numpy().view(np.uint32)[0]) == 0x3C877551
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 1, 16), (3, 5, 32), (17, 33, 80), (130, 129, 208), (64, 256, 1040),
+                                   (255, 384, 4096), (128, 128, 2048 + 16)])
+def test_w8a8_ragged_exact(M, N, K):
+    rng = np.random.default_rng(M * 1000 + N + K)
+    qx = torch.from_numpy(rng.integers(-127, 128, (M, K)).astype(np.int8)).cuda()
+    qw = torch.from_numpy(rng.integers(-127, 128, (N, K)).astype(np.int8)).cuda()
+    sx = torch.from_numpy(rng.uniform(0.001, 0.1, M).astype(np.float32)).cuda()
+    sw = torch.from_numpy(rng.uniform(0.001, 0.1, N).astype(np.float32)).cuda()
+    acc = torch.empty((M, N), dtype=torch.int32, device="cuda")
+    y = qlin.gemm_w8a8(qx, sx, qw, sw, out_dtype=torch.bfloat16, acc_out=acc)
+    acco = oracle.w8a8_acc(qx.cpu().numpy(), qw.cpu().numpy())
+    np.testing.assert_array_equal(acc.cpu().numpy(), acco)
+    yo = oracle.w8a8_out(acco, sx.cpu().numpy(), sw.cpu().numpy())
+    assert rel_err(host_f32(y), yo) < GEMM_REL_TOL
+
+
+@pytest.mark.parametrize("K", [1024, 1040, 4096, 28672])
+def test_w8a8_extreme_sums(K):
+    """All codes +-127: partial sums reach 16129*K (beyond 2^24 for K > 1040)."""
+    M, N = 128, 256
+    qx = torch.full((M, K), 127, dtype=torch.int8, device="cuda")
+    qx[1::2] = -127
+    qw = torch.full((N, K), 127, dtype=torch.int8, device="cuda")
+    qw[:, ::3] = -127
+    sx = torch.ones(M, device="cuda")
+    sw = torch.ones(N, device="cuda")
+    acc = torch.empty((M, N), dtype=torch.int32, device="cuda")
+    qlin.gemm_w8a8(qx, sx, qw, sw, out_dtype=torch.float32, acc_out=acc)
+    acco = oracle.w8a8_acc(qx[:2].cpu().numpy(), qw.cpu().numpy())
+    np.testing.assert_array_equal(acc[:2].cpu().numpy(), acco)
+    np.testing.assert_array_equal(acc[2:4].cpu().numpy(), acco)
+
+
+@pytest.mark.parametrize("smooth", [False, True])
+def test_w8a8_prefill_config_sampled(smooth):
+    """2048 x 11008 x 4096 SmoothQuant-style prefill; oracle on 64 sampled rows."""
+    x, w, _ = inputs.w8a8_prefill()
+    xd, wd = x.cuda(), w.cuda()
+    sm = None
+    if smooth:
+        sm = qlin.smooth_factors(qlin.absmax(xd, qlin.QLIN_PER_COL), qlin.absmax(wd, qlin.QLIN_PER_COL), 0.5)
+    qx, sx, qw, sw, acc, y = w8a8_run(xd, wd, torch.bfloat16, smooth=sm)
+    rows = np.sort(np.random.default_rng(5).choice(2048, 64, replace=False))
+    xh = host_f32(x)[rows]
+    wh = host_f32(w)
+    smh = None if sm is None else sm.cpu().numpy()
+    px = qlin.make_params("s8", "row", smooth_mode=qlin.QLIN_SMOOTH_DIVIDE if smooth else 0)
+    pw = qlin.make_params("s8", "row", smooth_mode=qlin.QLIN_SMOOTH_MULTIPLY if smooth else 0)
+    qxo, sxo, _ = oracle_quantize(xh, px, smooth=smh)
+    qwo, swo, _ = oracle_quantize(wh, pw, smooth=smh)
+    np.testing.assert_array_equal(codes_to_int(qx, px, 2048, 4096)[rows], qxo)
+    np.testing.assert_array_equal(codes_to_int(qw, pw, 11008, 4096), qwo)
+    acco = oracle.w8a8_acc(qxo, qwo)
+    np.testing.assert_array_equal(acc.cpu().numpy()[rows], acco)
+    yo = oracle.w8a8_out(acco, sxo, swo)
+    assert rel_err(host_f32(y)[rows], yo) < GEMM_REL_TOL
+
+
+def test_w8a8_downproj_sampled():
+    """4096 x 8192 x 28672 with outlier channels: 16 sampled rows x all N."""
+    torch.manual_seed(0)
+    x = inputs.downproj_activation(4096, outliers=True)
+    w = inputs.downproj_weight()
+    xd, wd = x.cuda(), w.cuda()
+    del x
+    qx, sx, qw, sw, acc, y = w8a8_run(xd, wd, torch.bfloat16)
+    rows = np.sort(np.random.default_rng(6).choice(4096, 16, replace=False))
+    acco = oracle.w8a8_acc(qx[rows].cpu().numpy(), qw.cpu().numpy())
+    np.testing.assert_array_equal(acc.cpu().numpy()[rows], acco)
+    yo = oracle.w8a8_out(acco, sx.cpu().numpy()[rows], sw.cpu().numpy())
+    assert rel_err(host_f32(y)[rows], yo) < GEMM_REL_TOL
+
+
+# ------------------------------------------------------------------ W4A16
+def w4_prepare(w_dev, group, asym):
+    """Quantize W [N x K] group-wise to INT4 with fp16 scales and pack it."""
+    N, K = w_dev.shape
+    p = qlin.make_params("u4" if asym else "s4", "group", group=group, scale_f16=True)
+    q, s, z = qlin.quantize(w_dev, p)
+    packed, hdr = qlin.pack_w4(q, s, z, N, K, group)
+    return p, q, s, z, packed, hdr
+
+
+def w4_oracle_weight(q, s, z, p, N, K, group, rows=None):
+    """Oracle dequantized weight w^ of the (optionally sampled) rows, from the
+    device codes / scales / zero points."""
+    if rows is not None:
+        idx = torch.from_numpy(np.asarray(rows)).cuda()
+        q = q[idx]
+        s = s.reshape(N, K // group)[idx]
+        z = None if z is None else z.reshape(N, K // group)[idx]
+        N = len(rows)
+    qi = codes_to_int(q, p, N, K)
+    sf = scales_f32(s).reshape(-1)
+    zi = None if z is None else z.cpu().numpy().reshape(-1)
+    return oracle.w4_dequant(qi, sf, zi, group)
+
+
+@pytest.mark.parametrize("asym", [False, True])
+@pytest.mark.parametrize("group", [32, 64, 128])
+@pytest.mark.parametrize("M", [1, 3, 8, 16, 17, 64, 100])
+def test_w4a16_small(asym, group, M):
+    N, K = 256, 1024
+    w = torch.from_numpy(inputs.normal((N, K), 0.02, 7)).to(torch.bfloat16).cuda()
+    x = torch.from_numpy(inputs.normal((M, K), 1.0, 8)).to(torch.bfloat16).cuda()
+    p, q, s, z, packed, hdr = w4_prepare(w, group, asym)
+    y = qlin.gemm_w4a16(x, packed, hdr)
+    # the quantized codes themselves match the oracle quantizer
+    qo, so, zo = oracle_quantize(host_f32(w), p)
+    np.testing.assert_array_equal(codes_to_int(q, p, N, K), qo)
+    np.testing.assert_array_equal(scales_f32(s), so)
+    what = w4_oracle_weight(q, s, z, p, N, K, group)
+    yo = oracle.matmul_f64(host_f32(x), what)
+    assert rel_err(host_f32(y), yo) < GEMM_REL_TOL
+
+
+@pytest.mark.parametrize("M", [1, 4, 16])
+def test_w4a16_decode_config(M):
+    """4096 x 4096 symmetric INT4, g = 128, fp16 scales (131,072 groups)."""
+    x, w = inputs.w4a16_decode(M)
+    p, q, s, z, packed, hdr = w4_prepare(w.cuda(), 128, False)
+    assert s.numel() == 131072
+    y = qlin.gemm_w4a16(x.cuda(), packed, hdr)
+    what = w4_oracle_weight(q, s, z, p, 4096, 4096, 128)
+    yo = oracle.matmul_f64(host_f32(x), what)
+    assert rel_err(host_f32(y), yo) < GEMM_REL_TOL
+
+
+@pytest.mark.parametrize("M", [1, 8, 64, 256])
+def test_w4a16_downproj_sampled(M):
+    """8192 x 28672 asymmetric UINT4, g = 128: all tokens x 256 sampled output channels."""
+    w = inputs.downproj_weight()
+    x = inputs.downproj_activation(M)
+    p, q, s, z, packed, hdr = w4_prepare(w.cuda(), 128, True)
+    y = qlin.gemm_w4a16(x.cuda(), packed, hdr)
+    rows = np.sort(np.random.default_rng(9).choice(8192, 256, replace=False))
+    what = w4_oracle_weight(q, s, z, p, 8192, 28672, 128, rows=rows)
+    yo = oracle.matmul_f64(host_f32(x), what)
+    assert rel_err(host_f32(y)[:, rows], yo) < GEMM_REL_TOL

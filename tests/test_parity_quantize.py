@@ -1,0 +1,248 @@
+"""GPU parity of qlin_quantize / qlin_dequantize / qlin_absmax /
+qlin_smooth_factors against the CPU oracle: codes, scales (binary32 bits or
+binary16 values), zero points and dequantized values must be bit-exact."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from activation_quantization_quantize_b300 import inputs, qlin
+from helpers import codes_to_int, host_f32, oracle_quantize, scales_f32
+
+pytestmark = pytest.mark.gpu
+
+DT = {"bf16": torch.bfloat16, "f16": torch.float16, "f32": torch.float32}
+
+
+def make_x(rows, cols, seed, dtype, special=True):
+    x = inputs.normal((rows, cols), 1.0, seed)
+    if special and rows * cols > 0:
+        rng = np.random.default_rng(seed + 100)
+        x[:, rng.integers(0, cols)] *= 40.0                       # an outlier channel
+        x.reshape(-1)[rng.integers(0, rows * cols, max(1, rows * cols // 500))] = 100.0
+        x[rows // 2] = 0.0                                        # an all-zero row
+        if rows > 2:
+            x[1] = -np.abs(x[1])                                  # a negative-only row
+    t = torch.from_numpy(x).to(DT[dtype])
+    return t.cuda(), host_f32(t)
+
+
+def run_case(xd, xh, p, smooth=None):
+    rows, cols = xh.shape
+    sm_d = None if smooth is None else torch.from_numpy(smooth).cuda()
+    q, s, z = qlin.quantize(xd, p, smooth=sm_d)
+    torch.cuda.synchronize()
+    qo, so, zo = oracle_quantize(xh, p, smooth=smooth)
+    np.testing.assert_array_equal(codes_to_int(q, p, rows, cols), qo)
+    sg = scales_f32(s)
+    if p.scale_dtype == qlin.QLIN_F32:
+        np.testing.assert_array_equal(sg.view(np.uint32), so.view(np.uint32))
+    else:
+        np.testing.assert_array_equal(sg, so)
+    if not p.symmetric:
+        np.testing.assert_array_equal(z.cpu().numpy(), zo)
+    return q, s, z, qo, so, zo
+
+
+CODES = ["s8", "s4", "u8", "u4"]
+SHAPES = [(1, 8), (3, 40), (17, 264), (64, 4096), (5, 1024), (33, 384)]
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f16", "f32"])
+@pytest.mark.parametrize("code", CODES)
+@pytest.mark.parametrize("gran", ["tensor", "row", "col"])
+@pytest.mark.parametrize("shape", SHAPES)
+def test_quantize_dynamic(dtype, code, gran, shape):
+    rows, cols = shape
+    xd, xh = make_x(rows, cols, seed=rows * 7 + cols, dtype=dtype)
+    run_case(xd, xh, qlin.make_params(code, gran))
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("code", CODES)
+@pytest.mark.parametrize("group", [8, 32, 64, 128])
+@pytest.mark.parametrize("shape", [(3, 128), (17, 384), (64, 4096), (2, 28672)])
+def test_quantize_groups(dtype, code, group, shape):
+    rows, cols = shape
+    if cols % group:
+        pytest.skip("group does not divide cols")
+    xd, xh = make_x(rows, cols, seed=cols + group, dtype=dtype)
+    run_case(xd, xh, qlin.make_params(code, "group", group=group))
+
+
+@pytest.mark.parametrize("code", CODES)
+@pytest.mark.parametrize("gran,group", [("row", 0), ("group", 128), ("group", 32), ("tensor", 0)])
+def test_quantize_f16_scales(code, gran, group):
+    xd, xh = make_x(24, 512, seed=3, dtype="bf16")
+    xd = (xd.float() * 0.02).to(torch.bfloat16)
+    xh = host_f32(xd)
+    run_case(xd, xh, qlin.make_params(code, gran, group=group, scale_f16=True))
+
+
+@pytest.mark.parametrize("mode", [qlin.QLIN_SMOOTH_DIVIDE, qlin.QLIN_SMOOTH_MULTIPLY])
+@pytest.mark.parametrize("gran", ["row", "tensor", "col", "group"])
+def test_quantize_smoothing(mode, gran):
+    rows, cols = 32, 1024
+    xd, xh = make_x(rows, cols, seed=11, dtype="bf16")
+    rng = np.random.default_rng(12)
+    sm = rng.uniform(0.05, 30.0, cols).astype(np.float32)
+    run_case(xd, xh, qlin.make_params("s8", gran, group=64 if gran == "group" else 0, smooth_mode=mode),
+             smooth=sm)
+
+
+@pytest.mark.parametrize("code", CODES)
+@pytest.mark.parametrize("gran", ["tensor", "row", "col", "group"])
+def test_quantize_static_scales(code, gran):
+    rows, cols = 16, 256
+    xd, xh = make_x(rows, cols, seed=21, dtype="bf16")
+    group = 64 if gran == "group" else 0
+    p = qlin.make_params(code, gran, group=group)
+    _, so, zo = oracle_quantize(xh * 0.7, p)               # scales from other data -> clipping
+    ps = qlin.make_params(code, gran, group=group, static_scale=True)
+    s = torch.from_numpy(so).cuda()
+    z = torch.from_numpy(zo).cuda()
+    q, _, _ = qlin.quantize(xd, ps, s=s, z=z)
+    qo, _, _ = oracle_quantize(xh, ps, static_s=so, static_z=zo)
+    np.testing.assert_array_equal(codes_to_int(q, ps, rows, cols), qo)
+
+
+def test_quantize_unaligned_rows_generic_path():
+    base = torch.from_numpy(inputs.normal((9, 100), 1.0, 5)).to(torch.bfloat16).cuda()
+    xd = base[:, 3:3 + 90]                                   # ld = 100, odd offset
+    xh = host_f32(xd)
+    for code, gran, group in [("s8", "row", 0), ("u8", "tensor", 0), ("s4", "group", 10), ("u4", "col", 0)]:
+        p = qlin.make_params(code, gran, group=group)
+        q, s, z = qlin.quantize(xd, p)
+        qo, so, zo = oracle_quantize(np.ascontiguousarray(xh), p)
+        np.testing.assert_array_equal(codes_to_int(q, p, 9, 90), qo)
+        np.testing.assert_array_equal(scales_f32(s).view(np.uint32), so.view(np.uint32))
+
+
+def test_exhaustive_bf16_static_scales():
+    """Every finite bf16 value against the oracle at a set of scales and zero
+    points (the code decision near half-integers)."""
+    bits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    v = oracle.bf16_bits_to_f32(bits)
+    v = v[np.isfinite(v)]
+    v = v[: (v.size // 8) * 8]
+    cols = 8
+    rows = v.size // cols
+    xt = torch.from_numpy(v.reshape(rows, cols)).to(torch.bfloat16).cuda()
+    rng = np.random.default_rng(31)
+    scales = [0.016535433, 1.0, 2.0 ** -10, 3.7e-3, 0.787401, 1e-30, 3e5] + list(rng.uniform(1e-3, 2, 20))
+    for sc in scales:
+        for code, z in [("s8", 0), ("u8", 93), ("s4", 0), ("u4", 8), ("u8", 0)]:
+            p = qlin.make_params(code, "tensor", static_scale=True)
+            s = torch.tensor([sc], dtype=torch.float32).cuda()
+            zt = torch.tensor([z], dtype=torch.int32).cuda()
+            q, _, _ = qlin.quantize(xt, p, s=s, z=zt)
+            qo, _, _ = oracle_quantize(v.reshape(rows, cols), p, static_s=np.array([sc], np.float32),
+                                       static_z=np.array([z], np.int32))
+            np.testing.assert_array_equal(codes_to_int(q, p, rows, cols), qo)
+
+
+def test_near_ties_binary32():
+    """Values whose binary32 quotient lands on (or next to) a half-integer."""
+    rng = np.random.default_rng(41)
+    s = np.float32(0.0123)
+    n = rng.integers(-120, 120, 4096)
+    base = ((n + 0.5) * np.float64(s)).astype(np.float32)
+    neigh = np.stack([np.nextafter(base, np.float32(-np.inf)), base, np.nextafter(base, np.float32(np.inf))], 1)
+    x = neigh.reshape(-1, 8)
+    xt = torch.from_numpy(x).cuda()
+    for code, z in [("s8", 0), ("u8", 3), ("u8", 128)]:
+        p = qlin.make_params(code, "tensor", static_scale=True)
+        q, _, _ = qlin.quantize(xt, p, s=torch.tensor([s]).cuda(), z=torch.tensor([z], dtype=torch.int32).cuda())
+        qo, _, _ = oracle_quantize(x, p, static_s=np.array([s]), static_z=np.array([z], np.int32))
+        np.testing.assert_array_equal(codes_to_int(q, p, *x.shape), qo)
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_percentile_per_tensor(dtype):
+    xd, xh = make_x(200, 1024, seed=51, dtype=dtype)
+    run_case(xd, xh, qlin.make_params("s8", "tensor", percentile=99.9))
+    run_case(xd, xh, qlin.make_params("s4", "tensor", percentile=99.0))
+    sm = np.random.default_rng(52).uniform(0.5, 4, 1024).astype(np.float32)
+    run_case(xd, xh, qlin.make_params("s8", "tensor", percentile=99.9, smooth_mode=qlin.QLIN_SMOOTH_DIVIDE),
+             smooth=sm)
+
+
+@pytest.mark.parametrize("code", CODES)
+@pytest.mark.parametrize("gran,group", [("tensor", 0), ("row", 0), ("col", 0), ("group", 32), ("group", 128)])
+@pytest.mark.parametrize("out", [torch.bfloat16, torch.float32, torch.float16])
+def test_dequantize(code, gran, group, out):
+    rows, cols = 19, 256
+    xd, xh = make_x(rows, cols, seed=61, dtype="bf16")
+    p = qlin.make_params(code, gran, group=group, scale_f16=(gran == "group"))
+    q, s, z = qlin.quantize(xd, p)
+    y = qlin.dequantize(q, s, z, p, rows, cols, out_dtype=out)
+    qo, so, zo = oracle_quantize(xh, p)
+    yo = oracle.dequantize(qo, so, zo if not p.symmetric else None, {0: 0, 1: 1, 2: 2, 3: 3}[p.gran], group)
+    if out == torch.bfloat16:
+        yo = oracle.round_bf16(yo)
+    elif out == torch.float16:
+        yo = yo.astype(np.float16).astype(np.float32)
+    np.testing.assert_array_equal(host_f32(y), yo)
+
+
+@pytest.mark.parametrize("gran,group", [("tensor", 0), ("row", 0), ("col", 0), ("group", 64)])
+def test_absmax(gran, group):
+    xd, xh = make_x(37, 512, seed=71, dtype="bf16")
+    a = qlin.absmax(xd, qlin.GRANS[gran], group)
+    ao = oracle.absmax(xh, {"tensor": 0, "row": 1, "col": 2, "group": 3}[gran], group)
+    np.testing.assert_array_equal(a.cpu().numpy(), ao)
+
+
+@pytest.mark.parametrize("alpha", [0.5, 0.0, 1.0, 0.7])
+def test_smooth_factors(alpha):
+    rng = np.random.default_rng(81)
+    mx = rng.uniform(0.1, 60, 4099).astype(np.float32)
+    mw = rng.uniform(1e-3, 0.1, 4099).astype(np.float32)
+    mx[5] = 0.0
+    s = qlin.smooth_factors(torch.from_numpy(mx).cuda(), torch.from_numpy(mw).cuda(), alpha).cpu().numpy()
+    so = oracle.smooth_factors(mx, mw, alpha)
+    if alpha in (0.5, 1.0):
+        np.testing.assert_array_equal(s, so)
+    else:
+        np.testing.assert_allclose(s, so, rtol=4 * 2 ** -23)
+
+
+def test_empty_input_is_noop():
+    x = torch.empty((0, 64), dtype=torch.bfloat16, device="cuda")
+    q, s, z = qlin.quantize(x, qlin.make_params("s8", "row"))
+    assert q.numel() == 0
+
+
+# ------------------------------------------------------------- full-size sweep (16384 x 4096)
+@pytest.fixture(scope="module")
+def sweep():
+    t = inputs.sweep_tensor()
+    return t.cuda(), host_f32(t)
+
+
+@pytest.mark.parametrize("code", ["s8", "s4", "u8"])
+@pytest.mark.parametrize("gran,group", [("row", 0), ("group", 32), ("group", 64), ("group", 128)])
+def test_sweep_rowlocal_sampled(sweep, code, gran, group):
+    xd, xh = sweep
+    p = qlin.make_params(code, gran, group=group)
+    q, s, z = qlin.quantize(xd, p)
+    rows = np.random.default_rng(91).choice(xh.shape[0], 64, replace=False)
+    rows.sort()
+    qo, so, zo = oracle_quantize(xh[rows], p)
+    qg = codes_to_int(q, p, *xh.shape)[rows]
+    np.testing.assert_array_equal(qg, qo)
+    ngr = 1 if gran == "row" else xh.shape[1] // group
+    sg = scales_f32(s).reshape(xh.shape[0], ngr)[rows].reshape(-1)
+    np.testing.assert_array_equal(sg.view(np.uint32), so.view(np.uint32))
+
+
+@pytest.mark.parametrize("code,gran", [("s8", "tensor"), ("u8", "tensor"), ("s8", "col"), ("u8", "col"),
+                                       ("s4", "col")])
+def test_sweep_global_scopes(sweep, code, gran):
+    xd, xh = sweep
+    run_case(xd, xh, qlin.make_params(code, gran))
+
+
+def test_sweep_percentile(sweep):
+    xd, xh = sweep
+    run_case(xd, xh, qlin.make_params("s8", "tensor", percentile=99.9))
