@@ -6,8 +6,9 @@ import torch
 import oracle
 from activation_quantization_quantize_b300 import qlin
 
-# Max relative error allowed for binary32-accumulated GEMM outputs rounded to
-# bf16 (one bf16 rounding is <= 2^-9 = 1.953e-3 of |y|).
+# Max relative error of a GEMM output before its final rounding to the output
+# type.  A bf16 output also carries that one rounding (up to half a bf16 ulp,
+# 2^-8 of |y| at the bottom of a binade), which rel_err_out() allows on top.
 GEMM_REL_TOL = 2e-3
 
 _ORC_GRAN = {qlin.QLIN_PER_TENSOR: oracle.PER_TENSOR, qlin.QLIN_PER_ROW: oracle.PER_ROW,
@@ -22,6 +23,28 @@ def rel_err(y, r):
     den = np.maximum(np.abs(r), 0.01 * rms)
     den = np.where(den == 0, 1.0, den)
     return float(np.max(np.abs(y - r) / den)) if r.size else 0.0
+
+
+def half_ulp(r, mant_bits):
+    """Half an ulp of |r| in a binary format with mant_bits fraction bits."""
+    r = np.abs(np.asarray(r, dtype=np.float64))
+    _, e = np.frexp(np.where(r == 0, 1.0, r))        # r = f * 2^e, f in [0.5, 1)
+    return np.ldexp(1.0, e - 2 - mant_bits) * (r != 0)
+
+
+def rel_err_out(y, r, out="bf16"):
+    """rel_err after removing the final rounding of the exact result r to the
+    output type: max_i max(|y_i - r_i| - halfulp(r_i), 0) / max(|r_i|, 0.01 rms(r))."""
+    y = np.asarray(y, dtype=np.float64)
+    r = np.asarray(r, dtype=np.float64)
+    if r.size == 0:
+        return 0.0
+    bits = {"bf16": 7, "f16": 10, "f32": 23}[out]
+    rms = np.sqrt(np.mean(r * r))
+    den = np.maximum(np.abs(r), 0.01 * rms)
+    den = np.where(den == 0, 1.0, den)
+    ex = np.maximum(np.abs(y - r) - half_ulp(r, bits) * (1 + 2.0 ** -20), 0.0)
+    return float(np.max(ex / den))
 
 
 def host_f32(t):
