@@ -200,6 +200,7 @@ __device__ __forceinline__ void load_rowdq(const uint8_t* __restrict__ blob, con
 }
 
 // ------------------------------------------------------------------ GEMV (M <= 16)
+constexpr int kPromoteGemv = 8;  // chunks per promoted accumulation chain
 // One CTA per 16-row n-tile; its 8 warps split the K chunks, each warp
 // accumulating m16n8k16 tiles (W as the A operand, X^T as B) in registers;
 // the partial tiles are summed in a fixed order in shared memory.
@@ -218,7 +219,13 @@ __global__ void __launch_bounds__(256) k_w4_gemv(const __nv_bfloat16* __restrict
 #pragma unroll
         for (int e = 0; e < 4; ++e) acc[u][e] = 0.0f;
 
+    float tot[MT][4];
+#pragma unroll
+    for (int u = 0; u < MT; ++u)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) tot[u][e] = 0.0f;
     int64_t last_g = -1;
+    int since = 0;
     RowDq rg, rh;
     for (int64_t kc = warp; kc < nchunk; kc += 8) {
         uint4 wv = __ldg(codes + kc * 32);
@@ -253,7 +260,21 @@ __global__ void __launch_bounds__(256) k_w4_gemv(const __nv_bfloat16* __restrict
                 mma_bf16_16816(acc[u], a, xw[2 * j], xw[2 * j + 1]);
             }
         }
+        if (++since == kPromoteGemv) {
+            since = 0;
+#pragma unroll
+            for (int u = 0; u < MT; ++u)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    tot[u][e] += acc[u][e];
+                    acc[u][e] = 0.0f;
+                }
+        }
     }
+#pragma unroll
+    for (int u = 0; u < MT; ++u)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) acc[u][e] += tot[u][e];
 
     // acc[u][e]: e=0,1 -> (row gq, tokens u*8 + 2t, +1); e=2,3 -> (row gq+8, same tokens)
     __shared__ float part[8][16][16];  // [warp][n row][token]
@@ -279,6 +300,7 @@ __global__ void __launch_bounds__(256) k_w4_gemv(const __nv_bfloat16* __restrict
 // its 16 x 64 weight chunk in registers (dequantized once) and multiplies it
 // with all BM/8 token tiles of the chunk's X tile, staged in shared memory.
 constexpr int kW4BM = 64;
+constexpr int kPromote = 8;  // chunks (of 64 k) per promoted accumulation chain
 constexpr int kXStride = 64 + 8;  // bf16 elements per smem row (padding against bank conflicts)
 
 __global__ void __launch_bounds__(256) k_w4_gemm_mma(const __nv_bfloat16* __restrict__ x, const uint8_t* __restrict__ blob,
@@ -293,11 +315,13 @@ __global__ void __launch_bounds__(256) k_w4_gemm_mma(const __nv_bfloat16* __rest
 
     __shared__ __align__(16) __nv_bfloat16 xs[2][kW4BM * kXStride];
 
-    float acc[kW4BM / 8][4];
+    // The tensor-core accumulator is promoted into `tot` every kPromote chunks
+    // so that no single accumulation chain runs over the whole of K.
+    float acc[kW4BM / 8][4], tot[kW4BM / 8][4];
 #pragma unroll
     for (int u = 0; u < kW4BM / 8; ++u)
 #pragma unroll
-        for (int e = 0; e < 4; ++e) acc[u][e] = 0.0f;
+        for (int e = 0; e < 4; ++e) acc[u][e] = tot[u][e] = 0.0f;
 
     // stage chunk kc of X (BM x 64 bf16 = 512 16-byte pieces; 2 per thread)
     auto stage = [&](int buf, int64_t kc) {
@@ -344,6 +368,15 @@ __global__ void __launch_bounds__(256) k_w4_gemm_mma(const __nv_bfloat16* __rest
             mma_bf16_16816(acc[u], a[2], b23.x, b23.y);
             mma_bf16_16816(acc[u], a[3], b23.z, b23.w);
         }
+        if ((kc & (kPromote - 1)) == kPromote - 1 || kc + 1 == nchunk) {
+#pragma unroll
+            for (int u = 0; u < kW4BM / 8; ++u)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    tot[u][e] += acc[u][e];
+                    acc[u][e] = 0.0f;
+                }
+        }
         __syncthreads();
     }
     if (!nt_ok) return;
@@ -352,12 +385,12 @@ __global__ void __launch_bounds__(256) k_w4_gemm_mma(const __nv_bfloat16* __rest
         int64_t mA = m0 + u * 8 + 2 * t, mB = mA + 1;
         int64_t n0 = nt * 16 + gq, n1 = n0 + 8;
         if (mA < M) {
-            y[mA * h.N + n0] = __float2bfloat16_rn(acc[u][0]);
-            y[mA * h.N + n1] = __float2bfloat16_rn(acc[u][2]);
+            y[mA * h.N + n0] = __float2bfloat16_rn(tot[u][0]);
+            y[mA * h.N + n1] = __float2bfloat16_rn(tot[u][2]);
         }
         if (mB < M) {
-            y[mB * h.N + n0] = __float2bfloat16_rn(acc[u][1]);
-            y[mB * h.N + n1] = __float2bfloat16_rn(acc[u][3]);
+            y[mB * h.N + n0] = __float2bfloat16_rn(tot[u][1]);
+            y[mB * h.N + n1] = __float2bfloat16_rn(tot[u][3]);
         }
     }
 }

@@ -6,11 +6,25 @@
 // per token, weights per output channel, the contraction runs on integers with
 // INT32 accumulation, and y[m,n] = acc[m,n] * sx[m] * sw[n].
 //
-// Kernel here: the legacy warp-level tensor path (mma.sync m16n8k32 s8,
-// native INT32 accumulation).  CTA tile 128 x 128 x 64, 8 warps (2 x 4), a
-// 4-stage cp.async pipeline, XOR-swizzled 64-byte smem rows read by ldmatrix.
+// sm_103a has no INT8 tcgen05 MMA, and its legacy INT8 path (mma.sync s8,
+// cuBLASLt INT8) runs at roughly a tenth of the 16-bit tensor rate.  The main
+// kernel (k_w8a8_tc) therefore computes the exact integer contraction on the
+// fp16 tensor cores: codes in [-128, 127] are exact in fp16, every product
+// (<= 2^14) is exact in fp32, and a sum of integers stays exact while its
+// magnitude is below 2^24.  The converter warps track, per activation row, the
+// sum of |code| since the accumulator was last emptied; before a k-block could
+// push any partial sum to 2^24 (sum|qx| * 128 >= 2^24), the accumulator is
+// drained into an INT32 region of tensor memory and restarted.  The INT32
+// result is therefore bit-exact for every input.
+//
+// k_w8a8_mma (warp-level mma.sync s8, native INT32 accumulation) is the
+// legacy-path kernel, kept for comparison (QLIN_W8A8_KERNEL=mma).
+#include <stdlib.h>
+#include <string.h>
+
 #include "qlin_common.cuh"
 #include "qlin_internal.h"
+#include "tc_ptx.cuh"
 
 namespace qlin {
 
@@ -168,16 +182,354 @@ __global__ void __launch_bounds__(w8::THREADS) k_w8a8_mma(const int8_t* __restri
     }
 }
 
+// ====================================================================== tcgen05 kernel
+namespace w8tc {
+constexpr int BM = 128;                   // rows of qx per CTA (TMEM lanes)
+constexpr int BN = 256;                   // rows of qw per CTA (TMEM columns)
+constexpr int BK = 64;                    // k per stage (one 128-byte fp16 row)
+constexpr int STAGES = 4;
+constexpr int A_BYTES = BM * BK * 2;      // 16 KB fp16 tile
+constexpr int B_BYTES = BN * BK * 2;      // 32 KB fp16 tile
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr int NCONV_WARPS = 8;            // warps 0-7: int8 -> fp16 converters
+constexpr int NCONV = NCONV_WARPS * 32;
+constexpr int EPI_WARP0 = 8;              // warps 8-11: drains + epilogue (one per TMEM lane quarter)
+constexpr int MMA_WARP = 12;              // warp 12: TMEM owner, MMA issuer
+constexpr int THREADS = 13 * 32;
+constexpr int PIECES = (BM + BN) * BK / 16;   // 16-byte int8 pieces per k-block (1536)
+constexpr int PPT = PIECES / NCONV;           // pieces per converter thread (6)
+constexpr int A_PIECES = BM * BK / 16;        // 512
+constexpr uint32_t ROWSUM_LIMIT = 131071;     // sum|qx| * 128 < 2^24
+constexpr uint32_t TMEM_COLS = 512;           // [0,256): fp32 accumulator, [256,512): int32 sums
+constexpr uint32_t EV_DRAIN = 1, EV_FINAL = 2;
+constexpr size_t SMEM_BYTES = 1024 + (size_t)STAGES * STAGE_BYTES + 4096;
+}  // namespace w8tc
+
+// int8 x4 -> two fp16x2 words, exact: bias to unsigned, place each byte in the
+// low mantissa of fp16 1024 (0x64xx = 1024 + u), subtract 1152.
+__device__ __forceinline__ void s8x4_to_f16(uint32_t w, uint32_t& lo, uint32_t& hi) {
+    uint32_t u = w ^ 0x80808080u;
+    uint32_t a = __byte_perm(u, 0x64646464u, 0x4140);
+    uint32_t b = __byte_perm(u, 0x64646464u, 0x4342);
+    asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(lo) : "r"(a), "r"(0x64806480u));
+    asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(hi) : "r"(b), "r"(0x64806480u));
+}
+
+__device__ __forceinline__ uint32_t abs_sum4(uint32_t w, uint32_t acc) {
+    return __dp4a(__vabs4(w), 0x01010101u, acc);  // bytes as unsigned |b|, -128 -> 128
+}
+
+// Epilogue of 32 consecutive outputs of row m starting at column nb:
+// acc_out (exact sums) and y = (float(acc) * sx[m]) * sw[n], one rounding.
+__device__ __forceinline__ void store_row32(const int (&tot)[32], int64_t m, int64_t nb, int64_t N, float sxm,
+                                            const float* __restrict__ sw, void* __restrict__ y, int yt,
+                                            int32_t* __restrict__ acc_out) {
+    const bool full = (nb + 32 <= N) && (N % 8 == 0);
+    if (acc_out) {
+        int32_t* ap = acc_out + m * N + nb;
+        if (full) {
+#pragma unroll
+            for (int j = 0; j < 32; j += 4) *reinterpret_cast<int4*>(ap + j) = make_int4(tot[j], tot[j + 1], tot[j + 2], tot[j + 3]);
+        } else {
+            for (int j = 0; j < 32; ++j)
+                if (nb + j < N) ap[j] = tot[j];
+        }
+    }
+    float f[32];
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+        float swn = (nb + j < N) ? __ldg(sw + nb + j) : 0.0f;
+        f[j] = ((float)tot[j] * sxm) * swn;
+    }
+    if (yt == QLIN_BF16) {
+        __nv_bfloat16* yp = reinterpret_cast<__nv_bfloat16*>(y) + m * N + nb;
+        if (full) {
+#pragma unroll
+            for (int j = 0; j < 32; j += 8) {
+                __nv_bfloat162 p0 = __floats2bfloat162_rn(f[j], f[j + 1]);
+                __nv_bfloat162 p1 = __floats2bfloat162_rn(f[j + 2], f[j + 3]);
+                __nv_bfloat162 p2 = __floats2bfloat162_rn(f[j + 4], f[j + 5]);
+                __nv_bfloat162 p3 = __floats2bfloat162_rn(f[j + 6], f[j + 7]);
+                uint4 u;
+                u.x = *reinterpret_cast<uint32_t*>(&p0);
+                u.y = *reinterpret_cast<uint32_t*>(&p1);
+                u.z = *reinterpret_cast<uint32_t*>(&p2);
+                u.w = *reinterpret_cast<uint32_t*>(&p3);
+                *reinterpret_cast<uint4*>(yp + j) = u;
+            }
+        } else {
+            for (int j = 0; j < 32; ++j)
+                if (nb + j < N) yp[j] = __float2bfloat16_rn(f[j]);
+        }
+    } else {
+        float* yp = reinterpret_cast<float*>(y) + m * N + nb;
+        if (full) {
+#pragma unroll
+            for (int j = 0; j < 32; j += 4) *reinterpret_cast<float4*>(yp + j) = make_float4(f[j], f[j + 1], f[j + 2], f[j + 3]);
+        } else {
+            for (int j = 0; j < 32; ++j)
+                if (nb + j < N) yp[j] = f[j];
+        }
+    }
+}
+
+__global__ void __launch_bounds__(w8tc::THREADS, 1)
+    k_w8a8_tc(const int8_t* __restrict__ qx, const float* __restrict__ sx, const int8_t* __restrict__ qw,
+              const float* __restrict__ sw, int64_t M, int64_t N, int64_t K, void* __restrict__ y, int yt,
+              int32_t* __restrict__ acc_out, int num_m_tiles) {
+    using namespace w8tc;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+    uint8_t* tiles = smem;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
+    // bars: full[STAGES], empty[STAGES], acc_full, acc_empty, ev, done
+    uint32_t* rowsum = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 4);  // [STAGES][BM]
+    volatile uint32_t* misc = rowsum + STAGES * BM;  // [0] tmem base, [1] event type, [2] abort
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 2);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t m0 = (int64_t)(blockIdx.x % num_m_tiles) * BM;
+    const int64_t n0 = (int64_t)(blockIdx.x / num_m_tiles) * BN;
+    const int nkb = (int)ceil_div(K, BK);
+
+    const uint32_t bar0 = tc::smem_addr(bars);
+    auto full_bar = [&](int s) { return bar0 + 8u * s; };
+    auto empty_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };
+    const uint32_t acc_full = bar0 + 8u * (2 * STAGES);
+    const uint32_t acc_empty = acc_full + 8u;
+    const uint32_t ev_bar = acc_full + 16u;
+    const uint32_t done_bar = acc_full + 24u;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            tc::mbar_init(full_bar(s), NCONV);
+            tc::mbar_init(empty_bar(s), 1);
+        }
+        tc::mbar_init(acc_full, 1);
+        tc::mbar_init(acc_empty, 128);
+        tc::mbar_init(ev_bar, 1);
+        tc::mbar_init(done_bar, 1);
+        misc[2] = 0;
+        tc::mbar_init_fence();
+    }
+    if (warp == MMA_WARP) {
+        tc::tmem_alloc(tc::smem_addr((const void*)&misc[0]), TMEM_COLS);
+        tc::tmem_relinquish();
+    }
+    tc::tc_fence_before();
+    __syncthreads();
+    tc::tc_fence_after();
+    const uint32_t tmem = misc[0];
+
+    if (warp < NCONV_WARPS) {
+        // ---------------------------------------------------------- converters
+        const int tid = threadIdx.x;
+        uint4 buf[PPT];
+        auto load_kb = [&](int kb) {
+            const int64_t k0 = (int64_t)kb * BK;
+#pragma unroll
+            for (int j = 0; j < PPT; ++j) {
+                int piece = tid + NCONV * j;
+                bool is_a = piece < A_PIECES;
+                int pr = is_a ? piece : piece - A_PIECES;
+                int row = pr >> 2, ch = pr & 3;
+                int64_t kk = k0 + ch * 16;
+                int64_t grow = (is_a ? m0 : n0) + row;
+                bool ok = kk < K && grow < (is_a ? M : N);
+                const int8_t* src = is_a ? qx : qw;
+                buf[j] = ok ? __ldg(reinterpret_cast<const uint4*>(src + grow * K + kk)) : make_uint4(0, 0, 0, 0);
+            }
+        };
+        load_kb(0);
+        for (int kb = 0; kb < nkb; ++kb) {
+            const int s = kb % STAGES;
+            const uint32_t ph = (uint32_t)(kb / STAGES) & 1u;
+            uint4 cur[PPT];
+#pragma unroll
+            for (int j = 0; j < PPT; ++j) cur[j] = buf[j];
+            if (kb + 1 < nkb) load_kb(kb + 1);
+            if (!tc::mbar_wait(empty_bar(s), ph ^ 1u, abort_flag)) break;
+            uint8_t* tA = tiles + (size_t)s * STAGE_BYTES;
+            uint8_t* tB = tA + A_BYTES;
+#pragma unroll
+            for (int j = 0; j < PPT; ++j) {
+                int piece = tid + NCONV * j;
+                bool is_a = piece < A_PIECES;
+                int pr = is_a ? piece : piece - A_PIECES;
+                uint32_t row = (uint32_t)(pr >> 2), ch = (uint32_t)(pr & 3);
+                uint32_t h[8];
+                s8x4_to_f16(cur[j].x, h[0], h[1]);
+                s8x4_to_f16(cur[j].y, h[2], h[3]);
+                s8x4_to_f16(cur[j].z, h[4], h[5]);
+                s8x4_to_f16(cur[j].w, h[6], h[7]);
+                uint8_t* t = is_a ? tA : tB;
+                *reinterpret_cast<uint4*>(t + tc::sw128_off(row, 2 * ch)) = make_uint4(h[0], h[1], h[2], h[3]);
+                *reinterpret_cast<uint4*>(t + tc::sw128_off(row, 2 * ch + 1)) = make_uint4(h[4], h[5], h[6], h[7]);
+                if (j < A_PIECES / NCONV) {  // compile-time: the first pieces are all A pieces
+                    uint32_t a = abs_sum4(cur[j].x, 0);
+                    a = abs_sum4(cur[j].y, a);
+                    a = abs_sum4(cur[j].z, a);
+                    a = abs_sum4(cur[j].w, a);
+                    a += __shfl_xor_sync(0xffffffffu, a, 1);
+                    a += __shfl_xor_sync(0xffffffffu, a, 2);
+                    if (ch == 0) rowsum[s * BM + row] = a;
+                }
+            }
+            tc::fence_proxy_async_smem();
+            tc::mbar_arrive(full_bar(s));
+        }
+    } else if (warp == MMA_WARP) {
+        // ---------------------------------------------------------- MMA issuer
+        constexpr uint32_t IDESC = tc::idesc_f16(BM, BN, false);
+        const uint32_t tiles_addr = tc::smem_addr(tiles);
+        uint32_t S[4] = {0, 0, 0, 0};
+        bool started = false;
+        uint32_t ndrain = 0, nev = 0;
+        bool ok = true;
+        for (int kb = 0; kb < nkb && ok; ++kb) {
+            const int s = kb % STAGES;
+            const uint32_t ph = (uint32_t)(kb / STAGES) & 1u;
+            if (!tc::mbar_wait(full_bar(s), ph, abort_flag)) {
+                ok = false;
+                break;
+            }
+            uint32_t T[4], mx = 0;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                T[i] = S[i] + rowsum[s * BM + lane * 4 + i];
+                mx = max(mx, T[i]);
+            }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+            if (started && mx > ROWSUM_LIMIT) {
+                // drain the accumulator into the INT32 sums before adding this k-block
+                if (lane == 0) {
+                    misc[1] = EV_DRAIN;
+                    tc::mbar_arrive(ev_bar);
+                    tc::mma_commit(acc_full);
+                }
+                ++nev;
+                __syncwarp();
+                if (!tc::mbar_wait(acc_empty, ndrain & 1u, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                ++ndrain;
+                started = false;
+#pragma unroll
+                for (int i = 0; i < 4; ++i) S[i] = rowsum[s * BM + lane * 4 + i];
+            } else {
+#pragma unroll
+                for (int i = 0; i < 4; ++i) S[i] = T[i];
+            }
+            tc::tc_fence_after();
+            if (lane == 0) {
+                const uint32_t a_addr = tiles_addr + (uint32_t)s * STAGE_BYTES;
+                const uint64_t ad = tc::desc_sw128(a_addr);
+                const uint64_t bd = tc::desc_sw128(a_addr + A_BYTES);
+#pragma unroll
+                for (int j = 0; j < BK / 16; ++j)  // 32 bytes of K per MMA
+                    tc::mma_f16(tmem, ad + 2 * j, bd + 2 * j, IDESC, (started || j > 0) ? 1u : 0u);
+                tc::mma_commit(empty_bar(s));
+            }
+            started = true;
+            __syncwarp();
+        }
+        if (lane == 0) {
+            misc[1] = ok ? EV_FINAL : 0u;
+            tc::mbar_arrive(ev_bar);
+            tc::mma_commit(acc_full);
+            tc::mma_commit(done_bar);
+        }
+        __syncwarp();
+        tc::mbar_wait(done_bar, 0, abort_flag);
+    } else {
+        // ---------------------------------------------------------- drains + epilogue
+        const int q = warp & 3;  // TMEM lane quarter of this warp
+        const uint32_t lane_base = (uint32_t)(32 * q) << 16;
+        const int64_t m = m0 + 32 * q + lane;
+        const uint32_t t_acc = tmem + lane_base;
+        const uint32_t t_int = tmem + lane_base + 256;
+        uint32_t ndrain = 0;
+        for (uint32_t ev = 0;; ++ev) {
+            if (!tc::mbar_wait(ev_bar, ev & 1u, abort_flag)) break;
+            const uint32_t type = misc[1];
+            if (!tc::mbar_wait(acc_full, ev & 1u, abort_flag)) break;
+            tc::tc_fence_after();
+            if (type == EV_DRAIN) {
+                for (int c = 0; c < BN; c += 32) {
+                    uint32_t a[32], r[32];
+                    tc::tmem_ld32(t_acc + c, a);
+                    if (ndrain) tc::tmem_ld32(t_int + c, r);
+                    tc::tmem_wait_ld();
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) {
+                        int v = __float2int_rn(__uint_as_float(a[j]));
+                        r[j] = ndrain ? (uint32_t)((int)r[j] + v) : (uint32_t)v;
+                    }
+                    tc::tmem_st32(t_int + c, r);
+                }
+                tc::tmem_wait_st();
+                ++ndrain;
+                tc::tc_fence_before();
+                tc::mbar_arrive(acc_empty);
+                continue;
+            }
+            if (type != EV_FINAL) break;
+            // final: y[m, n] = (float(total) * sx[m]) * sw[n]
+            const float sxm = (m < M) ? sx[m] : 0.0f;
+            for (int c = 0; c < BN; c += 32) {
+                __syncwarp();
+                uint32_t a[32], r[32];
+                tc::tmem_ld32(t_acc + c, a);
+                if (ndrain) tc::tmem_ld32(t_int + c, r);
+                tc::tmem_wait_ld();
+                int tot[32];
+#pragma unroll
+                for (int j = 0; j < 32; ++j) {
+                    int v = __float2int_rn(__uint_as_float(a[j]));
+                    tot[j] = ndrain ? (int)r[j] + v : v;
+                }
+                if (m < M) store_row32(tot, m, n0 + c, N, sxm, sw, y, yt, acc_out);
+            }
+            break;
+        }
+    }
+
+    tc::tc_fence_before();
+    __syncthreads();
+    if (warp == MMA_WARP) {
+        tc::tc_fence_after();
+        tc::tmem_dealloc(tmem, TMEM_COLS);
+    }
+}
+
 size_t w8a8_ws_bytes(int64_t, int64_t, int64_t) { return 0; }
+
+// 1 selects the legacy mma.sync kernel (read on every call, so a process can
+// compare both kernels).
+static int w8a8_kernel_choice() {
+    const char* e = getenv("QLIN_W8A8_KERNEL");
+    return (e && strcmp(e, "mma") == 0) ? 1 : 0;
+}
 
 cudaError_t run_gemm_w8a8(const int8_t* qx, const float* sx, const int8_t* qw, const float* sw, int64_t M, int64_t N,
                           int64_t K, void* y, int yt, int32_t* acc_out, void*, cudaStream_t st) {
-    using namespace w8;
-    size_t smem = (size_t)2 * STAGES * TILE_BYTES;
-    cudaError_t e = cudaFuncSetAttribute(k_w8a8_mma, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (w8a8_kernel_choice() == 1) {
+        using namespace w8;
+        size_t smem = (size_t)2 * STAGES * TILE_BYTES;
+        cudaError_t e = cudaFuncSetAttribute(k_w8a8_mma, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        dim3 grid((unsigned)ceil_div(N, BN), (unsigned)ceil_div(M, BM));
+        k_w8a8_mma<<<grid, THREADS, smem, st>>>(qx, sx, qw, sw, M, N, K, y, yt, acc_out);
+        return cudaGetLastError();
+    }
+    using namespace w8tc;
+    cudaError_t e = cudaFuncSetAttribute(k_w8a8_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
     if (e != cudaSuccess) return e;
-    dim3 grid((unsigned)ceil_div(N, BN), (unsigned)ceil_div(M, BM));
-    k_w8a8_mma<<<grid, THREADS, smem, st>>>(qx, sx, qw, sw, M, N, K, y, yt, acc_out);
+    int num_m = (int)ceil_div(M, BM);
+    int64_t tiles = (int64_t)num_m * ceil_div(N, BN);
+    k_w8a8_tc<<<(unsigned)tiles, THREADS, SMEM_BYTES, st>>>(qx, sx, qw, sw, M, N, K, y, yt, acc_out, num_m);
     return cudaGetLastError();
 }
 

@@ -197,3 +197,39 @@ def test_w4a16_downproj_sampled(M):
     what = w4_oracle_weight(q, s, z, p, 8192, 28672, 128, rows=rows)
     yo = oracle.matmul_f64(host_f32(x), what)
     assert rel_err_out(host_f32(y)[:, rows], yo) < GEMM_REL_TOL
+
+
+@pytest.mark.parametrize("M,N,K", [(128, 256, 64), (200, 300, 1056), (64, 512, 28672)])
+def test_w8a8_tensor_core_matches_legacy_kernel(M, N, K, monkeypatch):
+    """The fp16-tensor-core kernel and the legacy mma.sync s8 kernel give the
+    same INT32 sums and the same outputs."""
+    rng = np.random.default_rng(M + N + K)
+    qx = torch.from_numpy(rng.integers(-128, 128, (M, K)).astype(np.int8)).cuda()
+    qw = torch.from_numpy(rng.integers(-127, 128, (N, K)).astype(np.int8)).cuda()
+    sx = torch.from_numpy(rng.uniform(0.001, 0.1, M).astype(np.float32)).cuda()
+    sw = torch.from_numpy(rng.uniform(0.001, 0.1, N).astype(np.float32)).cuda()
+    a1 = torch.empty((M, N), dtype=torch.int32, device="cuda")
+    a2 = torch.empty((M, N), dtype=torch.int32, device="cuda")
+    y1 = qlin.gemm_w8a8(qx, sx, qw, sw, out_dtype=torch.float32, acc_out=a1)
+    monkeypatch.setenv("QLIN_W8A8_KERNEL", "mma")
+    y2 = qlin.gemm_w8a8(qx, sx, qw, sw, out_dtype=torch.float32, acc_out=a2)
+    torch.cuda.synchronize()
+    assert torch.equal(a1, a2)
+    assert torch.equal(y1, y2)
+    assert qlin.qlin_device_error() == 0
+
+
+def test_w8a8_drain_boundary():
+    """Rows whose |code| sums cross the 2^24 / 128 drain threshold at different
+    k-blocks: every row's sum stays exact."""
+    M, N, K = 128, 256, 8192
+    qx = torch.zeros((M, K), dtype=torch.int8, device="cuda")
+    for r in range(M):
+        qx[r, : 64 * (r + 1)] = 127 if r % 2 == 0 else -128
+    qw = torch.full((N, K), -127, dtype=torch.int8, device="cuda")
+    qw[::2] = 127
+    acc = torch.empty((M, N), dtype=torch.int32, device="cuda")
+    qlin.gemm_w8a8(qx, torch.ones(M, device="cuda"), qw, torch.ones(N, device="cuda"), out_dtype=torch.float32,
+                   acc_out=acc)
+    acco = oracle.w8a8_acc(qx.cpu().numpy(), qw.cpu().numpy())
+    np.testing.assert_array_equal(acc.cpu().numpy(), acco)
