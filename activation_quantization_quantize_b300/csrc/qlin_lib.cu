@@ -4,3 +4,4 @@
 #include "gemm_w8a8.cu"
 #include "gemm_w4a16.cu"
 #include "api.cu"
+#include "noalloc.cu"

@@ -74,6 +74,9 @@ def load():
         L.qlin_gemm_w8a8.argtypes = [_P, _P, _P, _P, _I64, _I64, _I64, _P, C.c_int, _P, _P, C.c_size_t, _P]
         L.qlin_gemm_w4a16.argtypes = [_P, _P, C.POINTER(qlin_w4_header), _I64, _P, _P, C.c_size_t, _P]
         L.qlin_device_error.argtypes = [_P]
+        L.qlin_quantize_noalloc.argtypes = [_P, C.c_int, _I64, _I64, _I64, _P, C.POINTER(qlin_qparams),
+                                            _P, _P, _P, _P]
+        L.qlin_quantize_noalloc.restype = C.c_int
         for name in ("qlin_quantize", "qlin_dequantize", "qlin_absmax", "qlin_smooth_factors",
                      "qlin_pack_w4", "qlin_gemm_w8a8", "qlin_gemm_w4a16", "qlin_device_error"):
             getattr(L, name).restype = C.c_int
@@ -161,6 +164,11 @@ def qlin_gemm_w8a8(qx, sx, qw, sw, M, N, K, y, yt, acc_out, ws, ws_bytes, stream
 def qlin_gemm_w4a16(x, packed, hdr, M, y, ws, ws_bytes, stream=None):
     return _check("qlin_gemm_w4a16", load().qlin_gemm_w4a16(
         _ptr(x), _ptr(packed), C.byref(hdr), M, _ptr(y), _ptr(ws), ws_bytes, _stream(stream)))
+
+
+def qlin_quantize_noalloc(x, xt, rows, cols, ld, smooth, p, q, s, z, stream=None):
+    return _check("qlin_quantize_noalloc", load().qlin_quantize_noalloc(
+        _ptr(x), xt, rows, cols, ld, _ptr(smooth), C.byref(p), _ptr(q), _ptr(s), _ptr(z), _stream(stream)))
 
 
 def qlin_device_error(stream=None):

@@ -227,6 +227,37 @@ int qlin_gemm_w4a16(const void *x, const void *packed, const qlin_w4_header *hdr
                     void *y, void *ws, size_t ws_bytes, void *stream);
 
 /*
+ * qlin_quantize_noalloc -- qlin_quantize for callers that cannot allocate
+ * device memory.  The pages have no counterpart: this is a deployment
+ * convenience, not part of the method.
+ *
+ * Some callers cannot call cudaMalloc or any allocating routine (a plug-in
+ * whose host owns all device memory, code running under an allocator's lock,
+ * a loop with a fixed memory plan), so they cannot provide the workspace that
+ * the per-tensor, per-column and percentile scopes of qlin_quantize need.
+ * This entry point takes qlin_quantize's arguments without ws / ws_bytes and
+ * uses a fixed scratch array of QLIN_NOALLOC_SCRATCH_BYTES in the library's
+ * own device memory instead, held on every GPU that loads the library until
+ * the process exits.  It allocates nothing.
+ *   - Limit: an operation whose workspace (qlin_workspace_size with
+ *     QLIN_OP_QUANTIZE) exceeds QLIN_NOALLOC_SCRATCH_BYTES returns
+ *     QLIN_ERR_WORKSPACE and launches nothing (e.g. per-column statistics of
+ *     more than 65,536 columns).
+ *   - The first call on a device looks up the array's device address with
+ *     cudaGetSymbolAddress (once per device, with that device current); make
+ *     that first call before any stream capture.
+ *   - Every call on a device shares the one array, and the array keeps the
+ *     last call's contents; each call clears what it needs zeroed on its own
+ *     stream.  Calls whose work overlaps on the GPU (other streams, other host
+ *     threads) race on the array and must be serialized by the caller.
+ * All other arguments, results and errors are those of qlin_quantize.
+ */
+#define QLIN_NOALLOC_SCRATCH_BYTES (512u * 1024u)
+int qlin_quantize_noalloc(const void *x, qlin_dtype xt, int64_t rows, int64_t cols, int64_t ld,
+                          const float *smooth, const qlin_qparams *p,
+                          void *q, void *s, int32_t *z, void *stream);
+
+/*
  * qlin_device_error -- synchronizes `stream`, then returns and clears the
  * library's device-side error word: QLIN_OK, or QLIN_ERR_TIMEOUT when a
  * bounded wait inside a kernel gave up (that kernel's outputs are then
