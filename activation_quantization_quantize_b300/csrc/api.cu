@@ -199,9 +199,9 @@ int qlin_gemm_w4a16(const void* x, const void* packed, const qlin_w4_header* hdr
         return QLIN_ERR_LAYOUT;
     if (M == 0) return QLIN_OK;
     if (!x || !packed || !y) return QLIN_ERR_ARG;
-    if (!aligned(x, 16) || !aligned(packed, 256) || !aligned(y, 4)) return QLIN_ERR_ARG;
+    if (!aligned(x, 16) || !aligned(packed, 256) || !aligned(y, 16)) return QLIN_ERR_ARG;
     size_t need = w4a16_ws_bytes(M, hdr->N, hdr->K);
-    if (need > 0 && (!ws || ws_bytes < need)) return QLIN_ERR_WORKSPACE;
+    if (need > 0 && (!ws || ws_bytes < need || !aligned(ws, 16))) return QLIN_ERR_WORKSPACE;
     return cuda_status(run_gemm_w4a16(x, packed, hdr, M, y, ws, (cudaStream_t)stream));
 }
 

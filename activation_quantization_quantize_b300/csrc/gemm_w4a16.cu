@@ -25,8 +25,13 @@
 // arithmetic: s = s_hi + s_lo with s_hi = bf16_rn(s); s_lo*d is exact in bf16
 // (at most 2 + 4 significant bits), so fma.rn.bf16x2(d, s_hi, s_lo*d) rounds
 // the exact product s*d once -- bit-identical to rounding fl(s*d).
+#include <cuda.h>
+
+#include <mutex>
+
 #include "qlin_common.cuh"
 #include "qlin_internal.h"
+#include "tc_ptx.cuh"
 
 namespace qlin {
 
@@ -395,9 +400,379 @@ __global__ void __launch_bounds__(256) k_w4_gemm_mma(const __nv_bfloat16* __rest
     }
 }
 
-size_t w4a16_ws_bytes(int64_t, int64_t, int64_t) { return 0; }
+// ====================================================================== tcgen05 GEMM (M > 16)
+// D[n, m] = sum_k w^[n, k] x[m, k] on the bf16 tensor cores, fp32 in TMEM.
+//   A operand: 128 weight rows, dequantized by 8 converter warps from the
+//              packed blob into a 128B-swizzled bf16 tile (one 16x64 packed
+//              tile per warp per k-block: the lane's 32 nibbles -> rows gq and
+//              gq+8, k = 16t..16t+15 of the chunk).
+//   B operand: up to 256 tokens of x, loaded by TMA (128B swizzle, rows past M
+//              zero-filled).
+// K is split across gridDim.y CTAs; each writes fp32 partial sums, which
+// k_w4_reduce adds in a fixed order (deterministic) and rounds once to bf16.
+// Every `promote` k-blocks the TMEM accumulator is folded into a second fp32
+// TMEM region so that no tensor-core accumulation chain spans more than
+// promote*64 k.
+namespace w4tc {
+constexpr int BMW = 128;                  // weight rows per CTA (TMEM lanes)
+constexpr int BK = 64;
+constexpr int STAGES = 4;
+constexpr int A_BYTES = BMW * BK * 2;     // 16 KB
+constexpr int B_BYTES = 256 * BK * 2;     // 32 KB (up to 256 tokens)
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr int NCONV = 256;                // warps 0-7
+constexpr int EPI_WARP0 = 8;              // warps 8-11
+constexpr int MMA_WARP = 12;
+constexpr int TMA_WARP = 13;
+constexpr int THREADS = 14 * 32;
+constexpr uint32_t TMEM_COLS = 512;       // [0,256) accumulator, [256,512) promoted sums
+constexpr uint32_t EV_DRAIN = 1, EV_FINAL = 2;
+constexpr int RING = 4;                   // register prefetch depth of the packed codes
+constexpr size_t SMEM_BYTES = 1024 + (size_t)STAGES * STAGE_BYTES + 1024;
+}  // namespace w4tc
 
-cudaError_t run_gemm_w4a16(const void* x, const void* packed, const qlin_w4_header* h, int64_t M, void* y, void*,
+struct W4TcArgs {
+    const uint8_t* blob;
+    qlin_w4_header h;
+    int64_t M;
+    int ntok;         // MMA N: tokens per CTA (multiple of 16, <= 256) = TMA box rows
+    int nchunk;       // K / 64
+    int nsplit;
+    int promote;      // k-blocks per accumulation chain (0: no promotion)
+    uint32_t idesc;
+    float* part;            // [nsplit][M][N] fp32 partials, or nullptr when nsplit == 1
+    __nv_bfloat16* y;       // [M][N] output when nsplit == 1
+};
+
+__global__ void __launch_bounds__(w4tc::THREADS, 1) k_w4_gemm_tc(const __grid_constant__ CUtensorMap tmx, W4TcArgs a) {
+    using namespace w4tc;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+    uint8_t* tiles = smem;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
+    volatile uint32_t* misc = reinterpret_cast<volatile uint32_t*>(bars + 2 * STAGES + 4);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 2);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t N = a.h.N;
+    const int64_t nblk = blockIdx.x;              // 128-row block of W
+    const int split = blockIdx.y;
+    const int64_t m0 = (int64_t)blockIdx.z * a.ntok;
+    // k-chunk range of this split
+    const int c_begin = (int)((int64_t)a.nchunk * split / a.nsplit);
+    const int c_end = (int)((int64_t)a.nchunk * (split + 1) / a.nsplit);
+    const int nkb = c_end - c_begin;
+
+    const uint32_t bar0 = tc::smem_addr(bars);
+    auto full_bar = [&](int s) { return bar0 + 8u * s; };
+    auto empty_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };
+    const uint32_t acc_full = bar0 + 8u * (2 * STAGES);
+    const uint32_t acc_empty = acc_full + 8u;
+    const uint32_t ev_bar = acc_full + 16u;
+    const uint32_t done_bar = acc_full + 24u;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            tc::mbar_init(full_bar(s), NCONV + 1);  // converters + the TMA issuer's expect_tx
+            tc::mbar_init(empty_bar(s), 1);
+        }
+        tc::mbar_init(acc_full, 1);
+        tc::mbar_init(acc_empty, 128);
+        tc::mbar_init(ev_bar, 1);
+        tc::mbar_init(done_bar, 1);
+        misc[2] = 0;
+        tc::mbar_init_fence();
+    }
+    if (warp == MMA_WARP) {
+        tc::tmem_alloc(tc::smem_addr((const void*)&misc[0]), TMEM_COLS);
+        tc::tmem_relinquish();
+    }
+    tc::tc_fence_before();
+    __syncthreads();
+    tc::tc_fence_after();
+    const uint32_t tmem = misc[0];
+
+    if (warp < 8) {
+        // ---------------------------------------------------------- weight dequantization
+        const int ntl = warp;                 // 16-row packed tile within the 128-row block
+        const int gq = lane >> 2, t = lane & 3;
+        const int64_t nt = nblk * 8 + ntl;
+        const int64_t ngr = a.h.K / a.h.group;
+        const uint4* __restrict__ codes =
+            reinterpret_cast<const uint4*>(a.blob + a.h.codes_off) + nt * a.nchunk * 32 + lane;
+        uint4 ring[RING];
+#pragma unroll
+        for (int i = 0; i < RING; ++i) ring[i] = (i < nkb) ? __ldg(codes + (int64_t)(c_begin + i) * 32) : make_uint4(0, 0, 0, 0);
+        int64_t last_g = -1;
+        RowDq rg, rh;
+        const uint32_t r_g = (uint32_t)(ntl * 16 + gq), r_h = r_g + 8;
+        for (int kb = 0; kb < nkb; ++kb) {
+            const int s = kb % STAGES;
+            const uint32_t ph = (uint32_t)(kb / STAGES) & 1u;
+            uint4 wv = ring[0];
+#pragma unroll
+            for (int i = 0; i < RING - 1; ++i) ring[i] = ring[i + 1];
+            ring[RING - 1] = (kb + RING < nkb) ? __ldg(codes + (int64_t)(c_begin + kb + RING) * 32) : make_uint4(0, 0, 0, 0);
+            const int64_t kc = c_begin + kb;
+            const int64_t gi = (kc * 64 + 16 * t) / a.h.group;
+            if (gi != last_g) {
+                load_rowdq(a.blob, a.h, nt, ngr, gi, gq, rg, rh);
+                last_g = gi;
+            }
+            uint32_t wd[4] = {wv.x, wv.y, wv.z, wv.w};
+            uint32_t og[8], oh[8];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                uint32_t f[4];
+                dq_word(wd[j], rg, rh, f);
+                og[2 * j] = f[0];      // row gq,   k 4j, 4j+1
+                og[2 * j + 1] = f[2];  // row gq,   k 4j+2, 4j+3
+                oh[2 * j] = f[1];      // row gq+8
+                oh[2 * j + 1] = f[3];
+            }
+            if (!tc::mbar_wait(empty_bar(s), ph ^ 1u, abort_flag)) break;
+            uint8_t* tA = tiles + (size_t)s * STAGE_BYTES;
+            *reinterpret_cast<uint4*>(tA + tc::sw128_off(r_g, 2 * t)) = make_uint4(og[0], og[1], og[2], og[3]);
+            *reinterpret_cast<uint4*>(tA + tc::sw128_off(r_g, 2 * t + 1)) = make_uint4(og[4], og[5], og[6], og[7]);
+            *reinterpret_cast<uint4*>(tA + tc::sw128_off(r_h, 2 * t)) = make_uint4(oh[0], oh[1], oh[2], oh[3]);
+            *reinterpret_cast<uint4*>(tA + tc::sw128_off(r_h, 2 * t + 1)) = make_uint4(oh[4], oh[5], oh[6], oh[7]);
+            tc::fence_proxy_async_smem();
+            tc::mbar_arrive(full_bar(s));
+        }
+    } else if (warp == TMA_WARP) {
+        // ---------------------------------------------------------- activation tiles (TMA)
+        if (lane == 0) {
+            const uint32_t tx = (uint32_t)a.ntok * BK * 2;
+            for (int kb = 0; kb < nkb; ++kb) {
+                const int s = kb % STAGES;
+                const uint32_t ph = (uint32_t)(kb / STAGES) & 1u;
+                if (!tc::mbar_wait(empty_bar(s), ph ^ 1u, abort_flag)) break;
+                tc::mbar_arrive_expect_tx(full_bar(s), tx);
+                const uint32_t dstB = tc::smem_addr(tiles + (size_t)s * STAGE_BYTES + A_BYTES);
+                tc::tma_load_2d(dstB, &tmx, (c_begin + kb) * BK, (int)m0, full_bar(s));
+            }
+        }
+        __syncwarp();
+    } else if (warp == MMA_WARP) {
+        // ---------------------------------------------------------- MMA issuer
+        const uint32_t tiles_addr = tc::smem_addr(tiles);
+        bool started = false, ok = true;
+        uint32_t ndrain = 0;
+        int chain = 0;
+        for (int kb = 0; kb < nkb; ++kb) {
+            const int s = kb % STAGES;
+            const uint32_t ph = (uint32_t)(kb / STAGES) & 1u;
+            if (!tc::mbar_wait(full_bar(s), ph, abort_flag)) {
+                ok = false;
+                break;
+            }
+            if (started && a.promote > 0 && chain == a.promote) {
+                if (lane == 0) {
+                    misc[1] = EV_DRAIN;
+                    tc::mbar_arrive(ev_bar);
+                    tc::mma_commit(acc_full);
+                }
+                __syncwarp();
+                if (!tc::mbar_wait(acc_empty, ndrain & 1u, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                ++ndrain;
+                started = false;
+                chain = 0;
+            }
+            tc::tc_fence_after();
+            if (lane == 0) {
+                const uint32_t a_addr = tiles_addr + (uint32_t)s * STAGE_BYTES;
+                const uint64_t ad = tc::desc_sw128(a_addr);
+                const uint64_t bd = tc::desc_sw128(a_addr + A_BYTES);
+#pragma unroll
+                for (int j = 0; j < BK / 16; ++j)
+                    tc::mma_f16(tmem, ad + 2 * j, bd + 2 * j, a.idesc, (started || j > 0) ? 1u : 0u);
+                tc::mma_commit(empty_bar(s));
+            }
+            started = true;
+            ++chain;
+            __syncwarp();
+        }
+        if (lane == 0) {
+            misc[1] = (ok && nkb > 0) ? EV_FINAL : 0u;
+            tc::mbar_arrive(ev_bar);
+            tc::mma_commit(acc_full);
+            tc::mma_commit(done_bar);
+        }
+        __syncwarp();
+        tc::mbar_wait(done_bar, 0, abort_flag);
+    } else {
+        // ---------------------------------------------------------- promotions + epilogue
+        const int q = warp & 3;
+        const uint32_t lane_base = (uint32_t)(32 * q) << 16;
+        const int64_t n = nblk * BMW + 32 * q + lane;  // output channel of this thread
+        const uint32_t t_acc = tmem + lane_base;
+        const uint32_t t_sum = tmem + lane_base + 256;
+        uint32_t ndrain = 0;
+        for (uint32_t ev = 0;; ++ev) {
+            if (!tc::mbar_wait(ev_bar, ev & 1u, abort_flag)) break;
+            const uint32_t type = misc[1];
+            if (!tc::mbar_wait(acc_full, ev & 1u, abort_flag)) break;
+            tc::tc_fence_after();
+            if (type == EV_DRAIN) {
+                for (int c = 0; c < a.ntok; c += 32) {
+                    uint32_t v[32], r[32];
+                    tc::tmem_ld32(t_acc + c, v);
+                    if (ndrain) tc::tmem_ld32(t_sum + c, r);
+                    tc::tmem_wait_ld();
+#pragma unroll
+                    for (int j = 0; j < 32; ++j)
+                        r[j] = ndrain ? __float_as_uint(__uint_as_float(r[j]) + __uint_as_float(v[j])) : v[j];
+                    tc::tmem_st32(t_sum + c, r);
+                }
+                tc::tmem_wait_st();
+                ++ndrain;
+                tc::tc_fence_before();
+                tc::mbar_arrive(acc_empty);
+                continue;
+            }
+            if (type != EV_FINAL) break;
+            for (int c = 0; c < a.ntok; c += 32) {
+                __syncwarp();
+                uint32_t v[32], r[32];
+                tc::tmem_ld32(t_acc + c, v);
+                if (ndrain) tc::tmem_ld32(t_sum + c, r);
+                tc::tmem_wait_ld();
+#pragma unroll
+                for (int j = 0; j < 32; ++j) {
+                    float f = __uint_as_float(v[j]);
+                    if (ndrain) f += __uint_as_float(r[j]);
+                    const int64_t m = m0 + c + j;
+                    if (c + j < a.ntok && m < a.M) {
+                        if (a.part)
+                            a.part[((int64_t)split * a.M + m) * N + n] = f;
+                        else
+                            a.y[m * N + n] = __float2bfloat16_rn(f);
+                    }
+                }
+            }
+            break;
+        }
+        if (nkb == 0 && !*abort_flag) {
+            // an empty split contributes zeros
+            for (int64_t j = 0; j < a.ntok; ++j) {
+                const int64_t m = m0 + j;
+                if (m < a.M) {
+                    if (a.part)
+                        a.part[((int64_t)split * a.M + m) * N + n] = 0.0f;
+                    else
+                        a.y[m * N + n] = __float2bfloat16_rn(0.0f);
+                }
+            }
+        }
+    }
+
+    tc::tc_fence_before();
+    __syncthreads();
+    if (warp == MMA_WARP) {
+        tc::tc_fence_after();
+        tc::tmem_dealloc(tmem, TMEM_COLS);
+    }
+}
+
+// y[m, n] = bf16( sum_s part[s, m, n] ), summed in split order.
+__global__ void k_w4_reduce(const float* __restrict__ part, int nsplit, int64_t MN, __nv_bfloat16* __restrict__ y) {
+    for (int64_t i = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) * 4; i < MN; i += (int64_t)gridDim.x * blockDim.x * 4) {
+        float4 acc = *reinterpret_cast<const float4*>(part + i);
+        for (int s = 1; s < nsplit; ++s) {
+            float4 v = *reinterpret_cast<const float4*>(part + (int64_t)s * MN + i);
+            acc.x += v.x;
+            acc.y += v.y;
+            acc.z += v.z;
+            acc.w += v.w;
+        }
+        __nv_bfloat162 p0 = __floats2bfloat162_rn(acc.x, acc.y);
+        __nv_bfloat162 p1 = __floats2bfloat162_rn(acc.z, acc.w);
+        uint2 u;
+        u.x = *reinterpret_cast<uint32_t*>(&p0);
+        u.y = *reinterpret_cast<uint32_t*>(&p1);
+        *reinterpret_cast<uint2*>(y + i) = u;
+    }
+}
+
+// ------------------------------------------------------------------ planning
+struct W4Plan {
+    bool tc;          // tensor-core path
+    int ntok;         // tokens per CTA (TMA box rows, MMA N)
+    int64_t mtiles;
+    int nsplit;
+};
+
+static W4Plan w4_plan(int64_t M, int64_t N, int64_t K) {
+    W4Plan p{};
+    p.tc = (M > 16) && (N % w4tc::BMW == 0) && (K % 64 == 0);
+    if (!p.tc) return p;
+    p.ntok = (int)((M >= 256) ? 256 : ((M + 15) / 16) * 16);
+    p.mtiles = ceil_div(M, p.ntok);
+    const int64_t tiles = (N / w4tc::BMW) * p.mtiles;
+    const int64_t nchunk = K / 64;
+    const int sms = num_sms();
+    // pick the split that minimizes (wave-quantized compute) + (partial-sum traffic)
+    double best = 1e30;
+    int best_s = 1;
+    for (int s = 1; s <= 16; ++s) {
+        if (nchunk / s < 8 && s > 1) break;  // at least 512 k per split
+        int64_t ctas = tiles * s;
+        double waves = (double)ceil_div(ctas, sms);
+        double compute = waves / s;                  // in units of one full-K tile per SM
+        double traffic = (s > 1) ? (double)s * M * N * 8.0 : 0.0;  // partial write + read bytes
+        // convert traffic to the compute unit: one full-K 128 x ntok tile on one SM
+        double tile_flops = 2.0 * w4tc::BMW * p.ntok * (double)K;
+        double per_sm_flops = 8.0e12;                // ~ one SM's bf16 rate
+        double traffic_units = traffic / 6.0e12 / (tile_flops / per_sm_flops);
+        double cost = compute + traffic_units;
+        if (cost < best - 1e-9) {
+            best = cost;
+            best_s = s;
+        }
+    }
+    p.nsplit = best_s;
+    return p;
+}
+
+size_t w4a16_ws_bytes(int64_t M, int64_t N, int64_t K) {
+    W4Plan p = w4_plan(M, N, K);
+    if (!p.tc || p.nsplit <= 1) return 0;
+    return (size_t)p.nsplit * M * N * sizeof(float);
+}
+
+typedef CUresult (*PFN_encodeTiled)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                    const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                    CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static PFN_encodeTiled encode_tiled_fn() {
+    static PFN_encodeTiled fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_encodeTiled>(p);
+    });
+    return fn;
+}
+
+// 1: force the mma.sync GEMM for M > 16 (comparison); read on every call.
+static bool w4_force_mma() {
+    const char* e = getenv("QLIN_W4A16_KERNEL");
+    return e && strcmp(e, "mma") == 0;
+}
+
+static int w4_promote() {
+    const char* e = getenv("QLIN_W4A16_PROMOTE");
+    return e ? atoi(e) : 8;
+}
+
+cudaError_t run_gemm_w4a16(const void* x, const void* packed, const qlin_w4_header* h, int64_t M, void* y, void* ws,
                            cudaStream_t st) {
     const __nv_bfloat16* xb = reinterpret_cast<const __nv_bfloat16*>(x);
     const uint8_t* blob = reinterpret_cast<const uint8_t*>(packed);
@@ -405,13 +780,51 @@ cudaError_t run_gemm_w4a16(const void* x, const void* packed, const qlin_w4_head
     unsigned ntiles = (unsigned)(h->N / 16);
     if (M <= 8) {
         k_w4_gemv<1><<<ntiles, 256, 0, st>>>(xb, blob, *h, M, yb);
-    } else if (M <= 16) {
+        return cudaGetLastError();
+    }
+    if (M <= 16) {
         k_w4_gemv<2><<<ntiles, 256, 0, st>>>(xb, blob, *h, M, yb);
-    } else {
+        return cudaGetLastError();
+    }
+    W4Plan plan = w4_plan(M, h->N, h->K);
+    PFN_encodeTiled enc = plan.tc ? encode_tiled_fn() : nullptr;
+    if (!plan.tc || !enc || w4_force_mma()) {
         dim3 grid((unsigned)ceil_div(ntiles, 8), (unsigned)ceil_div(M, kW4BM));
         k_w4_gemm_mma<<<grid, 256, 0, st>>>(xb, blob, *h, M, yb);
+        return cudaGetLastError();
     }
-    return cudaGetLastError();
+    CUtensorMap tmap;
+    cuuint64_t gdim[2] = {(cuuint64_t)h->K, (cuuint64_t)M};
+    cuuint64_t gstride[1] = {(cuuint64_t)h->K * 2};
+    cuuint32_t box[2] = {64, (cuuint32_t)plan.ntok};
+    cuuint32_t estride[2] = {1, 1};
+    if (enc(&tmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(x), gdim, gstride, box, estride,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return cudaErrorInvalidValue;
+    W4TcArgs a;
+    a.blob = blob;
+    a.h = *h;
+    a.M = M;
+    a.ntok = plan.ntok;
+    a.nchunk = (int)(h->K / 64);
+    a.nsplit = plan.nsplit;
+    a.promote = w4_promote();
+    a.idesc = tc::idesc_f16(w4tc::BMW, plan.ntok, true);
+    a.part = (plan.nsplit > 1) ? reinterpret_cast<float*>(ws) : nullptr;
+    a.y = yb;
+    cudaError_t e = cudaFuncSetAttribute(k_w4_gemm_tc, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)w4tc::SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    dim3 grid((unsigned)(h->N / w4tc::BMW), (unsigned)plan.nsplit, (unsigned)plan.mtiles);
+    k_w4_gemm_tc<<<grid, w4tc::THREADS, w4tc::SMEM_BYTES, st>>>(tmap, a);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    if (plan.nsplit > 1) {
+        int64_t MN = M * h->N;
+        k_w4_reduce<<<num_sms() * 4, 256, 0, st>>>(a.part, plan.nsplit, MN, yb);
+        e = cudaGetLastError();
+    }
+    return e;
 }
 
 }  // namespace qlin

@@ -177,6 +177,10 @@ class Step:
         self.y8 = torch.empty((M8, N), dtype=torch.bfloat16, device=dev)
         self.y4 = [torch.empty((m, N), dtype=torch.bfloat16, device=dev) for m in W4_MS]
         self.xhat = torch.empty((M8, K), dtype=torch.bfloat16, device=dev)
+        self.ws4 = []
+        for m in W4_MS:
+            nb4 = qlin.qlin_workspace_size(qlin.QLIN_OP_GEMM_W4A16, m, N, K)
+            self.ws4.append((torch.empty(max(nb4, 16), dtype=torch.uint8, device=dev), nb4))
         nb8 = qlin.qlin_workspace_size(qlin.QLIN_OP_GEMM_W8A8, M8, N, K)
         self.ws8 = torch.empty(max(nb8, 16), dtype=torch.uint8, device=dev)
         self.ws8_bytes = nb8
@@ -199,7 +203,8 @@ class Step:
         ev(2)
         for i, m in enumerate(W4_MS):
             packed, hdr = self.w4[i % len(self.w4)]
-            qlin.qlin_gemm_w4a16(self.xs[i], packed, hdr, m, self.y4[i], None, 0, stream)
+            ws4, nb4 = self.ws4[i]
+            qlin.qlin_gemm_w4a16(self.xs[i], packed, hdr, m, self.y4[i], ws4, nb4, stream)
             ev(3 + i)
         qlin.qlin_dequantize(self.qx, self.sx, None, self.px, M8, K, self.xhat, qlin.QLIN_BF16, stream)
         ev(7)

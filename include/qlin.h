@@ -219,9 +219,14 @@ int qlin_gemm_w8a8(const int8_t *qx, const float *sx, const int8_t *qw, const fl
  * then a 16-bit matmul): w^[n,k] = bf16(fl(s[n,k/g] * (q[n,k] - z[n,k/g]))),
  * y[m,n] = sum_k x[m,k] * w^[n,k] accumulated in binary32, rounded once to
  * bf16.
- *   x      device bf16 [M x K], row-major.
+ *   x      device bf16 [M x K], row-major, 16-byte aligned.
  *   packed device blob written by qlin_pack_w4; hdr its header (host copy).
- *   y      device bf16 [M x N], row-major.
+ *   y      device bf16 [M x N], row-major, 16-byte aligned.
+ *   ws     device workspace of qlin_workspace_size(QLIN_OP_GEMM_W4A16, M, N, K)
+ *          bytes, 16-byte aligned (fp32 partial sums of the K split used for
+ *          M > 16; none for M <= 16).
+ * M <= 16 runs a split-K GEMV; larger M runs the tensor-core GEMM, whose
+ * split-K partial sums are added in a fixed order (results are reproducible).
  */
 int qlin_gemm_w4a16(const void *x, const void *packed, const qlin_w4_header *hdr, int64_t M,
                     void *y, void *ws, size_t ws_bytes, void *stream);

@@ -233,3 +233,32 @@ def test_w8a8_drain_boundary():
                    acc_out=acc)
     acco = oracle.w8a8_acc(qx.cpu().numpy(), qw.cpu().numpy())
     np.testing.assert_array_equal(acc.cpu().numpy(), acco)
+
+
+@pytest.mark.parametrize("M", [17, 64, 256])
+def test_w4a16_tensor_core_vs_legacy_kernel(M, monkeypatch):
+    """The tcgen05 GEMM and the mma.sync GEMM agree with the oracle on the
+    same packed weights (K = 4096, asymmetric UINT4, g = 128)."""
+    N, K = 512, 4096
+    w = torch.from_numpy(inputs.normal((N, K), 0.02, 21)).to(torch.bfloat16).cuda()
+    x = torch.from_numpy(inputs.normal((M, K), 1.0, 22)).to(torch.bfloat16).cuda()
+    p, q, s, z, packed, hdr = w4_prepare(w, 128, True)
+    y_tc = qlin.gemm_w4a16(x, packed, hdr)
+    monkeypatch.setenv("QLIN_W4A16_KERNEL", "mma")
+    y_mma = qlin.gemm_w4a16(x, packed, hdr)
+    torch.cuda.synchronize()
+    yo = oracle.matmul_f64(host_f32(x), w4_oracle_weight(q, s, z, p, N, K, 128))
+    assert rel_err_out(host_f32(y_tc), yo) < GEMM_REL_TOL
+    assert rel_err_out(host_f32(y_mma), yo) < GEMM_REL_TOL
+    assert qlin.qlin_device_error() == 0
+
+
+def test_w4a16_reproducible():
+    """Split-K partial sums are added in a fixed order: two calls agree bit for bit."""
+    w = torch.from_numpy(inputs.normal((1024, 8192), 0.02, 23)).to(torch.bfloat16).cuda()
+    x = torch.from_numpy(inputs.normal((256, 8192), 1.0, 24)).to(torch.bfloat16).cuda()
+    _, _, _, _, packed, hdr = w4_prepare(w, 128, False)
+    a = qlin.gemm_w4a16(x, packed, hdr)
+    b = qlin.gemm_w4a16(x, packed, hdr)
+    torch.cuda.synchronize()
+    assert torch.equal(a, b)
