@@ -1,6 +1,8 @@
 // api.cu -- the extern "C" entry points of libqlin.so: argument validation on
 // the host, then a launch on the caller's stream.  Nothing here allocates.
 #include <math.h>
+#include <stdio.h>
+#include <stdlib.h>
 #include <string.h>
 
 #include "qlin_common.cuh"
@@ -12,7 +14,13 @@ namespace {
 
 inline bool aligned(const void* p, size_t a) { return ((uintptr_t)p % a) == 0; }
 
-inline int cuda_status(cudaError_t e) { return e == cudaSuccess ? QLIN_OK : QLIN_ERR_CUDA; }
+// QLIN_ERR_CUDA for a failed runtime call; with QLIN_DEBUG set in the
+// environment the CUDA error text is also printed to stderr.
+inline int cuda_status(cudaError_t e) {
+    if (e == cudaSuccess) return QLIN_OK;
+    if (getenv("QLIN_DEBUG")) fprintf(stderr, "qlin: CUDA error %d: %s\n", (int)e, cudaGetErrorString(e));
+    return QLIN_ERR_CUDA;
+}
 
 inline bool is_float_type(int t) { return t == QLIN_F32 || t == QLIN_BF16 || t == QLIN_F16; }
 

@@ -273,7 +273,7 @@ __device__ __forceinline__ void store_row32(const int (&tot)[32], int64_t m, int
     }
 }
 
-__global__ void __maxnreg__(152)
+__global__ void __launch_bounds__(w8tc::THREADS, 1)
     k_w8a8_tc(const int8_t* __restrict__ qx, const float* __restrict__ sx, const int8_t* __restrict__ qw,
               const float* __restrict__ sw, int64_t M, int64_t N, int64_t K, void* __restrict__ y, int yt,
               int32_t* __restrict__ acc_out, int num_m_tiles) {
@@ -324,10 +324,8 @@ __global__ void __maxnreg__(152)
     if (warp < NCONV_WARPS) {
         // ---------------------------------------------------------- converters
         const int tid = threadIdx.x;
-        // Register prefetch ring: k-blocks kb+1 and kb+2 are in flight while kb
-        // is converted (global-load latency is the converters' main stall).
-        uint4 b0[PPT], b1[PPT], b2[PPT];
-        auto load_kb = [&](uint4 (&buf)[PPT], int kb) {
+        uint4 buf[PPT];
+        auto load_kb = [&](int kb) {
             const int64_t k0 = (int64_t)kb * BK;
 #pragma unroll
             for (int j = 0; j < PPT; ++j) {
@@ -337,25 +335,19 @@ __global__ void __maxnreg__(152)
                 int row = pr >> 2, ch = pr & 3;
                 int64_t kk = k0 + ch * 16;
                 int64_t grow = (is_a ? m0 : n0) + row;
-                bool ok = kb < nkb && kk < K && grow < (is_a ? M : N);
+                bool ok = kk < K && grow < (is_a ? M : N);
                 const int8_t* src = is_a ? qx : qw;
                 buf[j] = ok ? __ldg(reinterpret_cast<const uint4*>(src + grow * K + kk)) : make_uint4(0, 0, 0, 0);
             }
         };
-        load_kb(b0, 0);
-        load_kb(b1, 1);
-        load_kb(b2, 2);
+        load_kb(0);
         for (int kb = 0; kb < nkb; ++kb) {
             const int s = kb % STAGES;
             const uint32_t ph = (uint32_t)(kb / STAGES) & 1u;
             uint4 cur[PPT];
 #pragma unroll
-            for (int j = 0; j < PPT; ++j) {
-                cur[j] = b0[j];
-                b0[j] = b1[j];
-                b1[j] = b2[j];
-            }
-            load_kb(b2, kb + 3);
+            for (int j = 0; j < PPT; ++j) cur[j] = buf[j];
+            if (kb + 1 < nkb) load_kb(kb + 1);
             if (!tc::mbar_wait(empty_bar(s), ph ^ 1u, abort_flag)) break;
             uint8_t* tA = tiles + (size_t)s * STAGE_BYTES;
             uint8_t* tB = tA + A_BYTES;
