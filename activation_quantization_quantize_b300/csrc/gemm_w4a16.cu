@@ -32,6 +32,7 @@
 #include "qlin_common.cuh"
 #include "qlin_internal.h"
 #include "tc_ptx.cuh"
+#include "tma_map.h"
 
 namespace qlin {
 
@@ -741,24 +742,6 @@ size_t w4a16_ws_bytes(int64_t M, int64_t N, int64_t K) {
     W4Plan p = w4_plan(M, N, K);
     if (!p.tc || p.nsplit <= 1) return 0;
     return (size_t)p.nsplit * M * N * sizeof(float);
-}
-
-typedef CUresult (*PFN_encodeTiled)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
-                                    const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
-                                    CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-static PFN_encodeTiled encode_tiled_fn() {
-    static PFN_encodeTiled fn = nullptr;
-    static std::once_flag once;
-    std::call_once(once, [] {
-        void* p = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_encodeTiled>(p);
-    });
-    return fn;
 }
 
 // 1: force the mma.sync GEMM for M > 16 (comparison); read on every call.

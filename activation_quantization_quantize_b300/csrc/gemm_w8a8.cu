@@ -25,6 +25,7 @@
 #include "qlin_common.cuh"
 #include "qlin_internal.h"
 #include "tc_ptx.cuh"
+#include "tma_map.h"
 
 namespace qlin {
 
@@ -187,22 +188,28 @@ namespace w8tc {
 constexpr int BM = 128;                   // rows of qx per CTA (TMEM lanes)
 constexpr int BN = 256;                   // rows of qw per CTA (TMEM columns)
 constexpr int BK = 64;                    // k per stage (one 128-byte fp16 row)
-constexpr int STAGES = 4;
+constexpr int S16 = 3;                    // fp16 operand stages (converter -> MMA)
+constexpr int S8 = 3;                     // int8 staging stages (TMA -> converter)
 constexpr int A_BYTES = BM * BK * 2;      // 16 KB fp16 tile
 constexpr int B_BYTES = BN * BK * 2;      // 32 KB fp16 tile
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr int A8_BYTES = BM * BK;         // 8 KB int8 tile (rows of 64 bytes)
+constexpr int B8_BYTES = BN * BK;         // 16 KB
+constexpr int STAGE8_BYTES = A8_BYTES + B8_BYTES;
 constexpr int NCONV_WARPS = 8;            // warps 0-7: int8 -> fp16 converters
 constexpr int NCONV = NCONV_WARPS * 32;
 constexpr int EPI_WARP0 = 8;              // warps 8-11: drains + epilogue (one per TMEM lane quarter)
 constexpr int MMA_WARP = 12;              // warp 12: TMEM owner, MMA issuer
-constexpr int THREADS = 13 * 32;
+constexpr int TMA_WARP = 13;              // warp 13: int8 tile loads
+constexpr int THREADS = 14 * 32;
 constexpr int PIECES = (BM + BN) * BK / 16;   // 16-byte int8 pieces per k-block (1536)
 constexpr int PPT = PIECES / NCONV;           // pieces per converter thread (6)
 constexpr int A_PIECES = BM * BK / 16;        // 512
 constexpr uint32_t ROWSUM_LIMIT = 131071;     // sum|qx| * 128 < 2^24
 constexpr uint32_t TMEM_COLS = 512;           // [0,256): fp32 accumulator, [256,512): int32 sums
 constexpr uint32_t EV_DRAIN = 1, EV_FINAL = 2;
-constexpr size_t SMEM_BYTES = 1024 + (size_t)STAGES * STAGE_BYTES + 4096;
+constexpr size_t CTRL_BYTES = 4096;
+constexpr size_t SMEM_BYTES = 1024 + (size_t)S16 * STAGE_BYTES + (size_t)S8 * STAGE8_BYTES + CTRL_BYTES;
 }  // namespace w8tc
 
 // int8 x4 -> two fp16x2 words, exact: bias to unsigned, place each byte in the
@@ -273,37 +280,55 @@ __device__ __forceinline__ void store_row32(const int (&tot)[32], int64_t m, int
     }
 }
 
+struct W8TcArgs {
+    const float* sx;
+    const float* sw;
+    int64_t M, N, K;
+    void* y;
+    int yt;
+    int32_t* acc_out;
+    int num_m_tiles;
+};
+
+// int8 tiles arrive by TMA (zero-filled past M, N and K) into a staging ring;
+// converter warps widen them to fp16 in the 128B-swizzled layout the MMA
+// reads; one thread issues tcgen05.mma (kind::f16, fp32 in TMEM).
 __global__ void __launch_bounds__(w8tc::THREADS, 1)
-    k_w8a8_tc(const int8_t* __restrict__ qx, const float* __restrict__ sx, const int8_t* __restrict__ qw,
-              const float* __restrict__ sw, int64_t M, int64_t N, int64_t K, void* __restrict__ y, int yt,
-              int32_t* __restrict__ acc_out, int num_m_tiles) {
+    k_w8a8_tc(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b, W8TcArgs p) {
     using namespace w8tc;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
-    uint8_t* tiles = smem;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
-    // bars: full[STAGES], empty[STAGES], acc_full, acc_empty, ev, done
-    uint32_t* rowsum = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 4);  // [STAGES][BM]
-    volatile uint32_t* misc = rowsum + STAGES * BM;  // [0] tmem base, [1] event type, [2] abort
+    uint8_t* tiles = smem;                                   // S16 x (A fp16 | B fp16)
+    uint8_t* stage8 = smem + S16 * STAGE_BYTES;              // S8 x (A int8 | B int8)
+    uint64_t* bars = reinterpret_cast<uint64_t*>(stage8 + S8 * STAGE8_BYTES);
+    // bars: full16[S16], empty16[S16], full8[S8], empty8[S8], acc_full, acc_empty, ev, done
+    uint32_t* rowsum = reinterpret_cast<uint32_t*>(bars + 2 * S16 + 2 * S8 + 4);  // [S16][BM]
+    volatile uint32_t* misc = rowsum + S16 * BM;  // [0] tmem base, [1] event type, [2] abort
     volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 2);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int64_t m0 = (int64_t)(blockIdx.x % num_m_tiles) * BM;
-    const int64_t n0 = (int64_t)(blockIdx.x / num_m_tiles) * BN;
-    const int nkb = (int)ceil_div(K, BK);
+    const int64_t m0 = (int64_t)(blockIdx.x % p.num_m_tiles) * BM;
+    const int64_t n0 = (int64_t)(blockIdx.x / p.num_m_tiles) * BN;
+    const int nkb = (int)ceil_div(p.K, BK);
 
     const uint32_t bar0 = tc::smem_addr(bars);
     auto full_bar = [&](int s) { return bar0 + 8u * s; };
-    auto empty_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };
-    const uint32_t acc_full = bar0 + 8u * (2 * STAGES);
+    auto empty_bar = [&](int s) { return bar0 + 8u * (S16 + s); };
+    auto full8_bar = [&](int s) { return bar0 + 8u * (2 * S16 + s); };
+    auto empty8_bar = [&](int s) { return bar0 + 8u * (2 * S16 + S8 + s); };
+    const uint32_t acc_full = bar0 + 8u * (2 * S16 + 2 * S8);
     const uint32_t acc_empty = acc_full + 8u;
     const uint32_t ev_bar = acc_full + 16u;
     const uint32_t done_bar = acc_full + 24u;
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < STAGES; ++s) {
+        for (int s = 0; s < S16; ++s) {
             tc::mbar_init(full_bar(s), NCONV);
             tc::mbar_init(empty_bar(s), 1);
+        }
+        for (int s = 0; s < S8; ++s) {
+            tc::mbar_init(full8_bar(s), 1);
+            tc::mbar_init(empty8_bar(s), NCONV);
         }
         tc::mbar_init(acc_full, 1);
         tc::mbar_init(acc_empty, 128);
@@ -324,30 +349,37 @@ __global__ void __launch_bounds__(w8tc::THREADS, 1)
     if (warp < NCONV_WARPS) {
         // ---------------------------------------------------------- converters
         const int tid = threadIdx.x;
-        uint4 buf[PPT];
-        auto load_kb = [&](int kb) {
-            const int64_t k0 = (int64_t)kb * BK;
-#pragma unroll
-            for (int j = 0; j < PPT; ++j) {
-                int piece = tid + NCONV * j;
-                bool is_a = piece < A_PIECES;
-                int pr = is_a ? piece : piece - A_PIECES;
-                int row = pr >> 2, ch = pr & 3;
-                int64_t kk = k0 + ch * 16;
-                int64_t grow = (is_a ? m0 : n0) + row;
-                bool ok = kk < K && grow < (is_a ? M : N);
-                const int8_t* src = is_a ? qx : qw;
-                buf[j] = ok ? __ldg(reinterpret_cast<const uint4*>(src + grow * K + kk)) : make_uint4(0, 0, 0, 0);
-            }
-        };
-        load_kb(0);
         for (int kb = 0; kb < nkb; ++kb) {
-            const int s = kb % STAGES;
-            const uint32_t ph = (uint32_t)(kb / STAGES) & 1u;
+            const int s = kb % S16, s8 = kb % S8;
+            const uint32_t ph = (uint32_t)(kb / S16) & 1u, ph8 = (uint32_t)(kb / S8) & 1u;
+            if (!tc::mbar_wait(full8_bar(s8), ph8, abort_flag)) break;
+            const uint8_t* a8 = stage8 + (size_t)s8 * STAGE8_BYTES;
             uint4 cur[PPT];
 #pragma unroll
-            for (int j = 0; j < PPT; ++j) cur[j] = buf[j];
-            if (kb + 1 < nkb) load_kb(kb + 1);
+            for (int j = 0; j < PPT; ++j) {
+                // piece = tid + 256 j: pieces 0..511 are A (row = piece/4), the rest B
+                cur[j] = *reinterpret_cast<const uint4*>(a8 + (size_t)(tid + NCONV * j) * 16);
+            }
+            uint32_t hbuf[PPT][8];
+#pragma unroll
+            for (int j = 0; j < PPT; ++j) {
+                s8x4_to_f16(cur[j].x, hbuf[j][0], hbuf[j][1]);
+                s8x4_to_f16(cur[j].y, hbuf[j][2], hbuf[j][3]);
+                s8x4_to_f16(cur[j].z, hbuf[j][4], hbuf[j][5]);
+                s8x4_to_f16(cur[j].w, hbuf[j][6], hbuf[j][7]);
+            }
+            uint32_t rs[A_PIECES / NCONV];
+#pragma unroll
+            for (int j = 0; j < A_PIECES / NCONV; ++j) {
+                uint32_t a = abs_sum4(cur[j].x, 0);
+                a = abs_sum4(cur[j].y, a);
+                a = abs_sum4(cur[j].z, a);
+                a = abs_sum4(cur[j].w, a);
+                a += __shfl_xor_sync(0xffffffffu, a, 1);
+                a += __shfl_xor_sync(0xffffffffu, a, 2);
+                rs[j] = a;
+            }
+            tc::mbar_arrive(empty8_bar(s8));  // the staging slot may be refilled
             if (!tc::mbar_wait(empty_bar(s), ph ^ 1u, abort_flag)) break;
             uint8_t* tA = tiles + (size_t)s * STAGE_BYTES;
             uint8_t* tB = tA + A_BYTES;
@@ -357,38 +389,41 @@ __global__ void __launch_bounds__(w8tc::THREADS, 1)
                 bool is_a = piece < A_PIECES;
                 int pr = is_a ? piece : piece - A_PIECES;
                 uint32_t row = (uint32_t)(pr >> 2), ch = (uint32_t)(pr & 3);
-                uint32_t h[8];
-                s8x4_to_f16(cur[j].x, h[0], h[1]);
-                s8x4_to_f16(cur[j].y, h[2], h[3]);
-                s8x4_to_f16(cur[j].z, h[4], h[5]);
-                s8x4_to_f16(cur[j].w, h[6], h[7]);
                 uint8_t* t = is_a ? tA : tB;
-                *reinterpret_cast<uint4*>(t + tc::sw128_off(row, 2 * ch)) = make_uint4(h[0], h[1], h[2], h[3]);
-                *reinterpret_cast<uint4*>(t + tc::sw128_off(row, 2 * ch + 1)) = make_uint4(h[4], h[5], h[6], h[7]);
-                if (j < A_PIECES / NCONV) {  // compile-time: the first pieces are all A pieces
-                    uint32_t a = abs_sum4(cur[j].x, 0);
-                    a = abs_sum4(cur[j].y, a);
-                    a = abs_sum4(cur[j].z, a);
-                    a = abs_sum4(cur[j].w, a);
-                    a += __shfl_xor_sync(0xffffffffu, a, 1);
-                    a += __shfl_xor_sync(0xffffffffu, a, 2);
-                    if (ch == 0) rowsum[s * BM + row] = a;
-                }
+                *reinterpret_cast<uint4*>(t + tc::sw128_off(row, 2 * ch)) =
+                    make_uint4(hbuf[j][0], hbuf[j][1], hbuf[j][2], hbuf[j][3]);
+                *reinterpret_cast<uint4*>(t + tc::sw128_off(row, 2 * ch + 1)) =
+                    make_uint4(hbuf[j][4], hbuf[j][5], hbuf[j][6], hbuf[j][7]);
+                if (j < A_PIECES / NCONV && ch == 0) rowsum[s * BM + row] = rs[j];
             }
             tc::fence_proxy_async_smem();
             tc::mbar_arrive(full_bar(s));
         }
+    } else if (warp == TMA_WARP) {
+        // ---------------------------------------------------------- int8 tile loads
+        if (lane == 0) {
+            for (int kb = 0; kb < nkb; ++kb) {
+                const int s8 = kb % S8;
+                const uint32_t ph8 = (uint32_t)(kb / S8) & 1u;
+                if (!tc::mbar_wait(empty8_bar(s8), ph8 ^ 1u, abort_flag)) break;
+                tc::mbar_arrive_expect_tx(full8_bar(s8), STAGE8_BYTES);
+                const uint32_t dst = tc::smem_addr(stage8 + (size_t)s8 * STAGE8_BYTES);
+                tc::tma_load_2d(dst, &tm_a, kb * BK, (int)m0, full8_bar(s8));
+                tc::tma_load_2d(dst + A8_BYTES, &tm_b, kb * BK, (int)n0, full8_bar(s8));
+            }
+        }
+        __syncwarp();
     } else if (warp == MMA_WARP) {
         // ---------------------------------------------------------- MMA issuer
         constexpr uint32_t IDESC = tc::idesc_f16(BM, BN, false);
         const uint32_t tiles_addr = tc::smem_addr(tiles);
         uint32_t S[4] = {0, 0, 0, 0};
         bool started = false;
-        uint32_t ndrain = 0, nev = 0;
+        uint32_t ndrain = 0;
         bool ok = true;
         for (int kb = 0; kb < nkb && ok; ++kb) {
-            const int s = kb % STAGES;
-            const uint32_t ph = (uint32_t)(kb / STAGES) & 1u;
+            const int s = kb % S16;
+            const uint32_t ph = (uint32_t)(kb / S16) & 1u;
             if (!tc::mbar_wait(full_bar(s), ph, abort_flag)) {
                 ok = false;
                 break;
@@ -408,7 +443,6 @@ __global__ void __launch_bounds__(w8tc::THREADS, 1)
                     tc::mbar_arrive(ev_bar);
                     tc::mma_commit(acc_full);
                 }
-                ++nev;
                 __syncwarp();
                 if (!tc::mbar_wait(acc_empty, ndrain & 1u, abort_flag)) {
                     ok = false;
@@ -477,7 +511,7 @@ __global__ void __launch_bounds__(w8tc::THREADS, 1)
             }
             if (type != EV_FINAL) break;
             // final: y[m, n] = (float(total) * sx[m]) * sw[n]
-            const float sxm = (m < M) ? sx[m] : 0.0f;
+            const float sxm = (m < p.M) ? p.sx[m] : 0.0f;
             for (int c = 0; c < BN; c += 32) {
                 __syncwarp();
                 uint32_t a[32], r[32];
@@ -490,7 +524,7 @@ __global__ void __launch_bounds__(w8tc::THREADS, 1)
                     int v = __float2int_rn(__uint_as_float(a[j]));
                     tot[j] = ndrain ? (int)r[j] + v : v;
                 }
-                if (m < M) store_row32(tot, m, n0 + c, N, sxm, sw, y, yt, acc_out);
+                if (m < p.M) store_row32(tot, m, n0 + c, p.N, sxm, p.sw, p.y, p.yt, p.acc_out);
             }
             break;
         }
@@ -525,11 +559,36 @@ cudaError_t run_gemm_w8a8(const int8_t* qx, const float* sx, const int8_t* qw, c
         return cudaGetLastError();
     }
     using namespace w8tc;
+    PFN_encodeTiled enc = encode_tiled_fn();
+    if (!enc) return cudaErrorNotSupported;
+    CUtensorMap ta, tb;
+    cuuint64_t gda[2] = {(cuuint64_t)K, (cuuint64_t)M};
+    cuuint64_t gdb[2] = {(cuuint64_t)K, (cuuint64_t)N};
+    cuuint64_t gstride[1] = {(cuuint64_t)K};
+    cuuint32_t boxa[2] = {BK, BM}, boxb[2] = {BK, BN};
+    cuuint32_t estride[2] = {1, 1};
+    if (enc(&ta, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<int8_t*>(qx), gda, gstride, boxa, estride,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return cudaErrorInvalidValue;
+    if (enc(&tb, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<int8_t*>(qw), gdb, gstride, boxb, estride,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return cudaErrorInvalidValue;
     cudaError_t e = cudaFuncSetAttribute(k_w8a8_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
     if (e != cudaSuccess) return e;
-    int num_m = (int)ceil_div(M, BM);
-    int64_t tiles = (int64_t)num_m * ceil_div(N, BN);
-    k_w8a8_tc<<<(unsigned)tiles, THREADS, SMEM_BYTES, st>>>(qx, sx, qw, sw, M, N, K, y, yt, acc_out, num_m);
+    W8TcArgs a;
+    a.sx = sx;
+    a.sw = sw;
+    a.M = M;
+    a.N = N;
+    a.K = K;
+    a.y = y;
+    a.yt = yt;
+    a.acc_out = acc_out;
+    a.num_m_tiles = (int)ceil_div(M, BM);
+    int64_t tiles = (int64_t)a.num_m_tiles * ceil_div(N, BN);
+    k_w8a8_tc<<<(unsigned)tiles, THREADS, SMEM_BYTES, st>>>(ta, tb, a);
     return cudaGetLastError();
 }
 
