@@ -344,12 +344,12 @@ def run_profile_case(name, dev):
     warm-up calls and one measured call, then exit."""
     torch.cuda.set_device(dev)
     if name == "w8a8":
-        Mp, Np = 2048, 4096                       # 56 MiB + 112 MiB of int8 operands
-        rng = np.random.default_rng(7)
-        qx = torch.from_numpy(rng.integers(-127, 128, (Mp, K), dtype=np.int8)).to(dev)
-        qw = torch.from_numpy(rng.integers(-127, 128, (Np, K), dtype=np.int8)).to(dev)
-        sx = torch.full((Mp,), 1e-3, device=dev)
-        sw = torch.full((Np,), 1e-3, device=dev)
+        # 2048 x 4096 x 28672: 56 MiB + 112 MiB of int8 codes, quantized from
+        # the down-projection activations (with outlier channels) and weights
+        Mp, Np = 2048, 4096
+        p8 = qlin.make_params("s8", "row")
+        qx, sx, _ = qlin.quantize(inputs.downproj_activation(Mp, outliers=True).to(dev), p8)
+        qw, sw, _ = qlin.quantize(inputs.downproj_weight(N=Np).to(dev), p8)
         fn = lambda: qlin.gemm_w8a8(qx, sx, qw, sw)  # noqa: E731
     elif name.startswith("w4a16"):
         m = int(name.split("_m")[1])
@@ -365,7 +365,10 @@ def run_profile_case(name, dev):
         px = qlin.make_params("s8", "row")
         qx, sx, _ = qlin.quantize(x, px)
         if name == "quantize":
-            fn = lambda: qlin.quantize(x, px)  # noqa: E731
+            # as in the step: per-token INT8 after dividing by smoothing factors
+            pd = qlin.make_params("s8", "row", smooth_mode=qlin.QLIN_SMOOTH_DIVIDE)
+            sm = torch.rand(K, device=dev) + 0.5
+            fn = lambda: qlin.quantize(x, pd, smooth=sm)  # noqa: E731
         else:
             fn = lambda: qlin.dequantize(qx, sx, None, px, M8, K)  # noqa: E731
     for _ in range(3):
