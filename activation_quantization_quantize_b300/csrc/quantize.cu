@@ -218,6 +218,87 @@ __global__ void __launch_bounds__(512) k_quant_rows(QuantArgs a) {
     }
 }
 
+// ------------------------------------------------------------------ long rows, per-row scopes
+// For rows longer than 4096 elements: one CTA of 512 threads per row at a
+// time, the smoothed binary32 row staged in shared memory (so registers stay
+// few and two CTAs fit on an SM): pass 1 loads (four chunks in flight per
+// thread), smooths, stores and reduces; pass 2 reads the staged values back
+// and writes the codes.
+template <typename T>
+__global__ void __launch_bounds__(512, 2) k_quant_longrows(QuantArgs a) {
+    extern __shared__ float xs[];  // [cols]
+    __shared__ float red_hi[32], red_lo[32];
+    const int tid = threadIdx.x, nt = blockDim.x;
+    const int64_t nchunks = a.cols / 8;
+    const T* __restrict__ x = reinterpret_cast<const T*>(a.x);
+    const CodeRange cr = make_range(a.qmin, a.qmax);
+    for (int64_t r = blockIdx.x; r < a.rows; r += gridDim.x) {
+        float hi = 0.0f, lo = 0.0f;
+        for (int64_t c0 = tid; c0 < nchunks; c0 += 4 * (int64_t)nt) {
+            float v[4][8];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                int64_t c = c0 + (int64_t)u * nt;
+                if (c < nchunks) load8<T>(x + r * a.ld + c * 8, v[u]);
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                int64_t c = c0 + (int64_t)u * nt;
+                if (c >= nchunks) break;
+                smooth8(v[u], a.smooth_mode, a.smooth, c * 8);
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    if (a.sym) {
+                        hi = fmaxf(hi, fabsf(v[u][j]));
+                    } else {
+                        hi = fmaxf(hi, v[u][j]);
+                        lo = fminf(lo, v[u][j]);
+                    }
+                }
+                float4* d = reinterpret_cast<float4*>(xs + c * 8);
+                d[0] = make_float4(v[u][0], v[u][1], v[u][2], v[u][3]);
+                d[1] = make_float4(v[u][4], v[u][5], v[u][6], v[u][7]);
+            }
+        }
+        hi = warp_max(hi);
+        lo = warp_min(lo);
+        if ((tid & 31) == 0) {
+            red_hi[tid >> 5] = hi;
+            red_lo[tid >> 5] = lo;
+        }
+        __syncthreads();
+        hi = 0.0f;
+        lo = 0.0f;
+        for (int w = 0; w < (nt >> 5); ++w) {
+            hi = fmaxf(hi, red_hi[w]);
+            lo = fminf(lo, red_lo[w]);
+        }
+        float s;
+        int z;
+        if (a.static_scale) {
+            s = load_scale(a.s, r, a.scale_f16);
+            z = a.z ? a.z[r] : 0;
+        } else {
+            scale_zero(lo, hi, a.qmin, a.qmax, a.sym, a.scale_f16, s, z);
+            if (tid == 0) {
+                store_scale(a.s, r, a.scale_f16, s);
+                if (a.z) a.z[r] = z;
+            }
+        }
+        const ScopeParams p = make_scope(s, z);
+        for (int64_t c = tid; c < nchunks; c += nt) {
+            const float4* d = reinterpret_cast<const float4*>(xs + c * 8);
+            float4 u0 = d[0], u1 = d[1];
+            float v[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
+            uint32_t cb[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) cb[j] = code_bits(v[j], p, cr);
+            store_codes8(a.q, r, a.cols, c, a.code4, cb);
+        }
+        __syncthreads();  // xs and red_* are reused by the next row
+    }
+}
+
 // ------------------------------------------------------------------ column-strip kernels
 // Thread layout shared by the per-tensor / per-column kernels: the block's
 // threads cover `cpb` chunk columns x `rpi` rows per iteration; the block
@@ -533,64 +614,80 @@ __device__ __forceinline__ void store_y(const DequantArgs& d, int64_t i, float v
         reinterpret_cast<float*>(d.y)[i] = v;
 }
 
-// Vector path: 8 elements per thread (cols % 8 == 0, group % 8 == 0).
-__global__ void k_dequant_vec(DequantArgs d) {
-    int64_t nchunks = d.rows * (d.cols / 8);
-    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < nchunks; i += (int64_t)gridDim.x * blockDim.x) {
-        int64_t r = i / (d.cols / 8), c0 = (i % (d.cols / 8)) * 8;
-        int code[8];
-        if (d.code4) {
-            uint32_t w = reinterpret_cast<const uint32_t*>(reinterpret_cast<const uint8_t*>(d.q) + r * (d.cols / 2))[c0 / 8];
+// Vector path (cols % 8 == 0, group % 8 == 0): blockIdx.y walks rows, each
+// thread handles DQ_U chunks of 8 elements spaced blockDim.x apart.
+constexpr int DQ_U = 4;
+
+__device__ __forceinline__ void dequant_chunk(const DequantArgs& d, int64_t r, int64_t c0, float out[8]) {
+    int code[8];
+    if (d.code4) {
+        uint32_t w = reinterpret_cast<const uint32_t*>(reinterpret_cast<const uint8_t*>(d.q) + r * (d.cols / 2))[c0 / 8];
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                int v = (w >> (4 * j)) & 0xF;
-                code[j] = (d.code_signed && v >= 8) ? v - 16 : v;
-            }
-        } else {
-            uint2 w = reinterpret_cast<const uint2*>(reinterpret_cast<const uint8_t*>(d.q) + r * d.cols)[c0 / 8];
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                uint32_t b = ((j < 4 ? w.x : w.y) >> (8 * (j & 3))) & 0xFFu;
-                code[j] = d.code_signed ? (int)(int8_t)b : (int)b;
-            }
+        for (int j = 0; j < 8; ++j) {
+            int v = (w >> (4 * j)) & 0xF;
+            code[j] = (d.code_signed && v >= 8) ? v - 16 : v;
         }
-        float out[8];
-        if (d.gran == QLIN_PER_COL) {
+    } else {
+        uint2 w = reinterpret_cast<const uint2*>(reinterpret_cast<const uint8_t*>(d.q) + r * d.cols)[c0 / 8];
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                float s = load_scale(d.s, c0 + j, d.scale_f16);
-                int z = d.z ? d.z[c0 + j] : 0;
-                out[j] = s * (float)(code[j] - z);
-            }
-        } else {
-            // one scope for the whole chunk (groups are whole chunks)
-            int64_t sc = (d.gran == QLIN_PER_TENSOR) ? 0
-                       : (d.gran == QLIN_PER_ROW) ? r
-                       : r * (d.cols / d.group) + c0 / d.group;
-            float s = load_scale(d.s, sc, d.scale_f16);
-            int z = d.z ? d.z[sc] : 0;
-#pragma unroll
-            for (int j = 0; j < 8; ++j) out[j] = s * (float)(code[j] - z);
+        for (int j = 0; j < 8; ++j) {
+            uint32_t b = ((j < 4 ? w.x : w.y) >> (8 * (j & 3))) & 0xFFu;
+            code[j] = d.code_signed ? (int)(int8_t)b : (int)b;
         }
-        int64_t base = r * d.cols + c0;
-        if (d.yt == QLIN_BF16) {
-            uint4 u;
-            __nv_bfloat162 p0 = __floats2bfloat162_rn(out[0], out[1]);
-            __nv_bfloat162 p1 = __floats2bfloat162_rn(out[2], out[3]);
-            __nv_bfloat162 p2 = __floats2bfloat162_rn(out[4], out[5]);
-            __nv_bfloat162 p3 = __floats2bfloat162_rn(out[6], out[7]);
-            u.x = *reinterpret_cast<uint32_t*>(&p0);
-            u.y = *reinterpret_cast<uint32_t*>(&p1);
-            u.z = *reinterpret_cast<uint32_t*>(&p2);
-            u.w = *reinterpret_cast<uint32_t*>(&p3);
-            reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(d.y) + base)[0] = u;
-        } else if (d.yt == QLIN_F32) {
-            float4* yp = reinterpret_cast<float4*>(reinterpret_cast<float*>(d.y) + base);
-            yp[0] = make_float4(out[0], out[1], out[2], out[3]);
-            yp[1] = make_float4(out[4], out[5], out[6], out[7]);
-        } else {
+    }
+    if (d.gran == QLIN_PER_COL) {
 #pragma unroll
-            for (int j = 0; j < 8; ++j) store_y(d, base + j, out[j]);
+        for (int j = 0; j < 8; ++j) {
+            float s = load_scale(d.s, c0 + j, d.scale_f16);
+            int z = d.z ? d.z[c0 + j] : 0;
+            out[j] = s * (float)(code[j] - z);
+        }
+    } else {
+        // one scope for the whole chunk (groups are whole chunks)
+        int64_t sc = (d.gran == QLIN_PER_TENSOR) ? 0 : (d.gran == QLIN_PER_ROW) ? r : r * (d.cols / d.group) + c0 / d.group;
+        float s = load_scale(d.s, sc, d.scale_f16);
+        int z = d.z ? d.z[sc] : 0;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) out[j] = s * (float)(code[j] - z);
+    }
+}
+
+__global__ void __launch_bounds__(256) k_dequant_vec(DequantArgs d) {
+    const int64_t nchunks = d.cols / 8;
+    for (int64_t r = blockIdx.y; r < d.rows; r += gridDim.y) {
+        for (int64_t cb = (int64_t)blockIdx.x * blockDim.x * DQ_U + threadIdx.x; cb < nchunks;
+             cb += (int64_t)gridDim.x * blockDim.x * DQ_U) {
+            float out[DQ_U][8];
+#pragma unroll
+            for (int u = 0; u < DQ_U; ++u) {
+                int64_t c = cb + (int64_t)u * blockDim.x;
+                if (c < nchunks) dequant_chunk(d, r, c * 8, out[u]);
+            }
+#pragma unroll
+            for (int u = 0; u < DQ_U; ++u) {
+                int64_t c = cb + (int64_t)u * blockDim.x;
+                if (c >= nchunks) break;
+                int64_t base = r * d.cols + c * 8;
+                if (d.yt == QLIN_BF16) {
+                    uint4 v;
+                    __nv_bfloat162 p0 = __floats2bfloat162_rn(out[u][0], out[u][1]);
+                    __nv_bfloat162 p1 = __floats2bfloat162_rn(out[u][2], out[u][3]);
+                    __nv_bfloat162 p2 = __floats2bfloat162_rn(out[u][4], out[u][5]);
+                    __nv_bfloat162 p3 = __floats2bfloat162_rn(out[u][6], out[u][7]);
+                    v.x = *reinterpret_cast<uint32_t*>(&p0);
+                    v.y = *reinterpret_cast<uint32_t*>(&p1);
+                    v.z = *reinterpret_cast<uint32_t*>(&p2);
+                    v.w = *reinterpret_cast<uint32_t*>(&p3);
+                    reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(d.y) + base)[0] = v;
+                } else if (d.yt == QLIN_F32) {
+                    float4* yp = reinterpret_cast<float4*>(reinterpret_cast<float*>(d.y) + base);
+                    yp[0] = make_float4(out[u][0], out[u][1], out[u][2], out[u][3]);
+                    yp[1] = make_float4(out[u][4], out[u][5], out[u][6], out[u][7]);
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) store_y(d, base + j, out[u][j]);
+                }
+            }
         }
     }
 }
@@ -654,10 +751,13 @@ static bool rows_kernel_ok(const QuantArgs& a, int xt) {
     return true;
 }
 
+// Rows of up to 8192 elements: 4 chunks per thread and small CTAs (<= 256
+// threads), so that many rows are in flight per SM.  Longer rows (group
+// scopes) use 8 chunks per thread and up to 512 threads.
 template <typename T>
 static cudaError_t launch_rows(const QuantArgs& a, cudaStream_t st) {
     int64_t nchunks = a.cols / 8;
-    int cpt = (nchunks <= 512) ? 1 : (nchunks <= 1024) ? 2 : (nchunks <= 2048) ? 4 : 8;
+    int cpt = (nchunks <= 128) ? 1 : (nchunks <= 256) ? 2 : (nchunks <= 1024) ? 4 : 8;
     int64_t nt = ceil_div(nchunks, cpt);
     nt = ceil_div(nt, 32) * 32;
     if (a.gran == QLIN_PER_GROUP) {
@@ -666,6 +766,7 @@ static cudaError_t launch_rows(const QuantArgs& a, cudaStream_t st) {
     }
     if (nt < 32) nt = 32;
     int per_sm = (int)(2048 / nt);
+    if (per_sm > 16) per_sm = 16;
     if (per_sm < 1) per_sm = 1;
     int64_t grid = (int64_t)num_sms() * per_sm;
     if (grid > a.rows) grid = a.rows;
@@ -727,7 +828,20 @@ static cudaError_t run_quantize_t(QuantArgs a, int xt, const qlin_qparams* p, vo
     const int64_t n = a.rows * a.cols;
     const int gblocks = num_sms() * 4;
     const bool row_local = (a.gran == QLIN_PER_ROW || a.gran == QLIN_PER_GROUP);
-    if (row_local && rows_kernel_ok(a, xt) && p->clip_percentile <= 0.0) return launch_rows<T>(a, st);
+    if (row_local && rows_kernel_ok(a, xt) && p->clip_percentile <= 0.0) {
+        const int64_t nchunks = a.cols / 8;
+        const size_t row_bytes = (size_t)a.cols * sizeof(float);
+        if (a.gran == QLIN_PER_ROW && !a.absmax_out && nchunks > 1024 && row_bytes <= 113 * 1024) {
+            cudaError_t e = cudaFuncSetAttribute(k_quant_longrows<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                 (int)row_bytes);
+            if (e != cudaSuccess) return e;
+            int64_t grid = (int64_t)num_sms() * 2;
+            if (grid > a.rows) grid = a.rows;
+            k_quant_longrows<T><<<(unsigned)grid, 512, row_bytes, st>>>(a);
+            return cudaGetLastError();
+        }
+        return launch_rows<T>(a, st);
+    }
 
     // Stats (dynamic) -> finalize -> codes.
     if (!a.static_scale) {
@@ -851,9 +965,16 @@ cudaError_t run_dequantize(const void* q, const void* s, const int32_t* z, const
     int ys = (yt == QLIN_F32) ? 4 : 2;
     bool vec = (cols % 8 == 0) && (p->gran != QLIN_PER_GROUP || p->group % 8 == 0) &&
                ((uintptr_t)q % (d.code4 ? 4 : 8) == 0) && ((uintptr_t)y % (8 * ys) == 0);
-    if (vec)
-        k_dequant_vec<<<blocks, 256, 0, st>>>(d);
-    else
+    if (vec) {
+        int64_t nchunks = cols / 8;
+        int threads = nchunks >= 256 * DQ_U ? 256 : (int)ceil_div(ceil_div(nchunks, DQ_U), 32) * 32;
+        int64_t gx = ceil_div(nchunks, (int64_t)threads * DQ_U);
+        int64_t gy = ceil_div((int64_t)num_sms() * 2048 / threads, gx);
+        if (gy > rows) gy = rows;
+        if (gy > 65535) gy = 65535;
+        if (gy < 1) gy = 1;
+        k_dequant_vec<<<dim3((unsigned)gx, (unsigned)gy), threads, 0, st>>>(d);
+    } else
         k_dequant_generic<<<blocks, 256, 0, st>>>(d);
     return cudaGetLastError();
 }
