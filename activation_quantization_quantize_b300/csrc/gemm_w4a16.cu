@@ -188,30 +188,43 @@ __device__ __forceinline__ void mma_bf16_16816(float c[4], const uint32_t a[4], 
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
+// Raw dequantization words of lane (gq) for group gi of n-tile nt: the
+// (row gq, row gq+8) binary16 scale pair and their packed zero points.
+struct DqRaw {
+    uint32_t s2;  // two binary16 scales
+    uint32_t zb;  // z(row gq) | z(row gq+8) << 4, or 0x88 for symmetric codes
+};
+
+__device__ __forceinline__ DqRaw fetch_dq(const uint8_t* __restrict__ blob, const qlin_w4_header& h, int64_t nt,
+                                          int64_t ngr, int64_t gi, int gq) {
+    DqRaw d;
+    d.s2 = __ldg(reinterpret_cast<const uint32_t*>(blob + h.scales_off) + (nt * ngr + gi) * 8 + gq);
+    d.zb = h.asym ? (uint32_t)__ldg(blob + h.zeros_off + (nt * ngr + gi) * 8 + gq) : 0x88u;
+    return d;
+}
+
+__device__ __forceinline__ void build_dq(const DqRaw& d, RowDq& rg, RowDq& rh) {
+    uint32_t sw = d.s2;
+    __half2 s2 = *reinterpret_cast<__half2*>(&sw);
+    float2 sf = __half22float2(s2);
+    rg = row_dq(sf.x, d.zb & 0xF);
+    rh = row_dq(sf.y, (d.zb >> 4) & 0xF);
+}
+
 // Load the dequantization constants of lane (gq) for group gi of n-tile nt.
 __device__ __forceinline__ void load_rowdq(const uint8_t* __restrict__ blob, const qlin_w4_header& h, int64_t nt,
                                            int64_t ngr, int64_t gi, int gq, RowDq& rg, RowDq& rh) {
-    const uint32_t* sp = reinterpret_cast<const uint32_t*>(blob + h.scales_off) + (nt * ngr + gi) * 8 + gq;
-    uint32_t sw = __ldg(sp);
-    __half2 s2 = *reinterpret_cast<__half2*>(&sw);
-    float2 sf = __half22float2(s2);
-    uint32_t z0 = 8, z1 = 8;
-    if (h.asym) {
-        uint8_t zb = __ldg(blob + h.zeros_off + (nt * ngr + gi) * 8 + gq);
-        z0 = zb & 0xF;
-        z1 = zb >> 4;
-    }
-    rg = row_dq(sf.x, z0);
-    rh = row_dq(sf.y, z1);
+    build_dq(fetch_dq(blob, h, nt, ngr, gi, gq), rg, rh);
 }
 
 // ------------------------------------------------------------------ GEMV (M <= 16)
 constexpr int kPromoteGemv = 8;  // chunks per promoted accumulation chain
+constexpr int GV_U = 4;          // chunks in flight per warp
 // One CTA per 16-row n-tile; its 8 warps split the K chunks, each warp
 // accumulating m16n8k16 tiles (W as the A operand, X^T as B) in registers;
 // the partial tiles are summed in a fixed order in shared memory.
 template <int MT>  // number of n8 tiles of tokens: 1 (M <= 8) or 2 (M <= 16)
-__global__ void __launch_bounds__(256) k_w4_gemv(const __nv_bfloat16* __restrict__ x, const uint8_t* __restrict__ blob,
+__global__ void __launch_bounds__(256, 2) k_w4_gemv(const __nv_bfloat16* __restrict__ x, const uint8_t* __restrict__ blob,
                                                  qlin_w4_header h, int64_t M, __nv_bfloat16* __restrict__ y) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int gq = lane >> 2, t = lane & 3;
@@ -230,51 +243,61 @@ __global__ void __launch_bounds__(256) k_w4_gemv(const __nv_bfloat16* __restrict
     for (int u = 0; u < MT; ++u)
 #pragma unroll
         for (int e = 0; e < 4; ++e) tot[u][e] = 0.0f;
-    int64_t last_g = -1;
+    const int gshift = __ffs(h.group) - 1;  // group is a power of two
+    // Each warp takes chunks warp, warp+8, ...; GV_U chunks per iteration
+    // with every load (codes, scales, activations) issued before any use.
     int since = 0;
-    RowDq rg, rh;
-    for (int64_t kc = warp; kc < nchunk; kc += 8) {
-        uint4 wv = __ldg(codes + kc * 32);
-        int64_t k0 = kc * 64 + 16 * t;
-        // activations: rows gq (and gq+8), k0..k0+15
-        uint4 xb[MT][2];
+    for (int64_t kc0 = warp; kc0 < nchunk; kc0 += 8 * GV_U) {
+        uint4 wv[GV_U];
+        DqRaw dr[GV_U];
+        uint4 xb[GV_U][MT][2];
 #pragma unroll
-        for (int u = 0; u < MT; ++u) {
-            int64_t m = u * 8 + gq;
-            if (m < M) {
-                const uint4* xp = reinterpret_cast<const uint4*>(x + m * K + k0);
-                xb[u][0] = __ldg(xp);
-                xb[u][1] = __ldg(xp + 1);
-            } else {
-                xb[u][0] = make_uint4(0, 0, 0, 0);
-                xb[u][1] = make_uint4(0, 0, 0, 0);
-            }
-        }
-        int64_t gi = k0 / h.group;
-        if (gi != last_g) {
-            load_rowdq(blob, h, nt, ngr, gi, gq, rg, rh);
-            last_g = gi;
-        }
-        uint32_t wd[4] = {wv.x, wv.y, wv.z, wv.w};
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            uint32_t a[4];
-            dq_word(wd[j], rg, rh, a);
+        for (int i = 0; i < GV_U; ++i) {
+            const int64_t kc = kc0 + 8 * i;
+            const bool ok = kc < nchunk;
+            const int64_t kcc = ok ? kc : kc0;
+            wv[i] = __ldg(codes + kcc * 32);
+            const int64_t k0 = kcc * 64 + 16 * t;
+            dr[i] = fetch_dq(blob, h, nt, ngr, k0 >> gshift, gq);
 #pragma unroll
             for (int u = 0; u < MT; ++u) {
-                const uint32_t* xw = reinterpret_cast<const uint32_t*>(&xb[u][0]);
-                mma_bf16_16816(acc[u], a, xw[2 * j], xw[2 * j + 1]);
+                const int64_t m = u * 8 + gq;
+                if (m < M && ok) {
+                    const uint4* xp = reinterpret_cast<const uint4*>(x + m * K + k0);
+                    xb[i][u][0] = __ldg(xp);
+                    xb[i][u][1] = __ldg(xp + 1);
+                } else {
+                    xb[i][u][0] = make_uint4(0, 0, 0, 0);
+                    xb[i][u][1] = make_uint4(0, 0, 0, 0);
+                }
             }
         }
-        if (++since == kPromoteGemv) {
-            since = 0;
 #pragma unroll
-            for (int u = 0; u < MT; ++u)
+        for (int i = 0; i < GV_U; ++i) {
+            if (kc0 + 8 * i >= nchunk) break;
+            RowDq rg, rh;
+            build_dq(dr[i], rg, rh);
+            uint32_t wd[4] = {wv[i].x, wv[i].y, wv[i].z, wv[i].w};
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    tot[u][e] += acc[u][e];
-                    acc[u][e] = 0.0f;
+            for (int j = 0; j < 4; ++j) {
+                uint32_t a[4];
+                dq_word(wd[j], rg, rh, a);
+#pragma unroll
+                for (int u = 0; u < MT; ++u) {
+                    const uint32_t* xw = reinterpret_cast<const uint32_t*>(&xb[i][u][0]);
+                    mma_bf16_16816(acc[u], a, xw[2 * j], xw[2 * j + 1]);
                 }
+            }
+            if (++since == kPromoteGemv) {
+                since = 0;
+#pragma unroll
+                for (int u = 0; u < MT; ++u)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        tot[u][e] += acc[u][e];
+                        acc[u][e] = 0.0f;
+                    }
+            }
         }
     }
 #pragma unroll
@@ -501,25 +524,31 @@ __global__ void __launch_bounds__(w4tc::THREADS, 1) k_w4_gemm_tc(const __grid_co
         const int64_t ngr = a.h.K / a.h.group;
         const uint4* __restrict__ codes =
             reinterpret_cast<const uint4*>(a.blob + a.h.codes_off) + nt * a.nchunk * 32 + lane;
+        const int gshift = __ffs(a.h.group) - 1;  // group is a power of two
+        // register ring: codes and group constants of the next RING k-blocks
         uint4 ring[RING];
+        DqRaw rdq[RING];
+        auto fetch = [&](int kb, uint4& w, DqRaw& d) {
+            const int64_t kc = c_begin + (kb < nkb ? kb : 0);
+            w = __ldg(codes + kc * 32);
+            d = fetch_dq(a.blob, a.h, nt, ngr, (kc * 64 + 16 * t) >> gshift, gq);
+        };
 #pragma unroll
-        for (int i = 0; i < RING; ++i) ring[i] = (i < nkb) ? __ldg(codes + (int64_t)(c_begin + i) * 32) : make_uint4(0, 0, 0, 0);
-        int64_t last_g = -1;
-        RowDq rg, rh;
+        for (int i = 0; i < RING; ++i) fetch(i, ring[i], rdq[i]);
         const uint32_t r_g = (uint32_t)(ntl * 16 + gq), r_h = r_g + 8;
         for (int kb = 0; kb < nkb; ++kb) {
             const int s = kb % STAGES;
             const uint32_t ph = (uint32_t)(kb / STAGES) & 1u;
             uint4 wv = ring[0];
+            DqRaw dq = rdq[0];
 #pragma unroll
-            for (int i = 0; i < RING - 1; ++i) ring[i] = ring[i + 1];
-            ring[RING - 1] = (kb + RING < nkb) ? __ldg(codes + (int64_t)(c_begin + kb + RING) * 32) : make_uint4(0, 0, 0, 0);
-            const int64_t kc = c_begin + kb;
-            const int64_t gi = (kc * 64 + 16 * t) / a.h.group;
-            if (gi != last_g) {
-                load_rowdq(a.blob, a.h, nt, ngr, gi, gq, rg, rh);
-                last_g = gi;
+            for (int i = 0; i < RING - 1; ++i) {
+                ring[i] = ring[i + 1];
+                rdq[i] = rdq[i + 1];
             }
+            fetch(kb + RING, ring[RING - 1], rdq[RING - 1]);
+            RowDq rg, rh;
+            build_dq(dq, rg, rh);
             uint32_t wd[4] = {wv.x, wv.y, wv.z, wv.w};
             uint32_t og[8], oh[8];
 #pragma unroll

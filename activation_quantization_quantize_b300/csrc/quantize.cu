@@ -614,80 +614,64 @@ __device__ __forceinline__ void store_y(const DequantArgs& d, int64_t i, float v
         reinterpret_cast<float*>(d.y)[i] = v;
 }
 
-// Vector path (cols % 8 == 0, group % 8 == 0): blockIdx.y walks rows, each
-// thread handles DQ_U chunks of 8 elements spaced blockDim.x apart.
-constexpr int DQ_U = 4;
-
-__device__ __forceinline__ void dequant_chunk(const DequantArgs& d, int64_t r, int64_t c0, float out[8]) {
-    int code[8];
-    if (d.code4) {
-        uint32_t w = reinterpret_cast<const uint32_t*>(reinterpret_cast<const uint8_t*>(d.q) + r * (d.cols / 2))[c0 / 8];
+// Vector path: 8 elements per thread (cols % 8 == 0, group % 8 == 0).
+__global__ void k_dequant_vec(DequantArgs d) {
+    int64_t nchunks = d.rows * (d.cols / 8);
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < nchunks; i += (int64_t)gridDim.x * blockDim.x) {
+        int64_t r = i / (d.cols / 8), c0 = (i % (d.cols / 8)) * 8;
+        int code[8];
+        if (d.code4) {
+            uint32_t w = reinterpret_cast<const uint32_t*>(reinterpret_cast<const uint8_t*>(d.q) + r * (d.cols / 2))[c0 / 8];
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            int v = (w >> (4 * j)) & 0xF;
-            code[j] = (d.code_signed && v >= 8) ? v - 16 : v;
-        }
-    } else {
-        uint2 w = reinterpret_cast<const uint2*>(reinterpret_cast<const uint8_t*>(d.q) + r * d.cols)[c0 / 8];
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            uint32_t b = ((j < 4 ? w.x : w.y) >> (8 * (j & 3))) & 0xFFu;
-            code[j] = d.code_signed ? (int)(int8_t)b : (int)b;
-        }
-    }
-    if (d.gran == QLIN_PER_COL) {
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            float s = load_scale(d.s, c0 + j, d.scale_f16);
-            int z = d.z ? d.z[c0 + j] : 0;
-            out[j] = s * (float)(code[j] - z);
-        }
-    } else {
-        // one scope for the whole chunk (groups are whole chunks)
-        int64_t sc = (d.gran == QLIN_PER_TENSOR) ? 0 : (d.gran == QLIN_PER_ROW) ? r : r * (d.cols / d.group) + c0 / d.group;
-        float s = load_scale(d.s, sc, d.scale_f16);
-        int z = d.z ? d.z[sc] : 0;
-#pragma unroll
-        for (int j = 0; j < 8; ++j) out[j] = s * (float)(code[j] - z);
-    }
-}
-
-__global__ void __launch_bounds__(256) k_dequant_vec(DequantArgs d) {
-    const int64_t nchunks = d.cols / 8;
-    for (int64_t r = blockIdx.y; r < d.rows; r += gridDim.y) {
-        for (int64_t cb = (int64_t)blockIdx.x * blockDim.x * DQ_U + threadIdx.x; cb < nchunks;
-             cb += (int64_t)gridDim.x * blockDim.x * DQ_U) {
-            float out[DQ_U][8];
-#pragma unroll
-            for (int u = 0; u < DQ_U; ++u) {
-                int64_t c = cb + (int64_t)u * blockDim.x;
-                if (c < nchunks) dequant_chunk(d, r, c * 8, out[u]);
+            for (int j = 0; j < 8; ++j) {
+                int v = (w >> (4 * j)) & 0xF;
+                code[j] = (d.code_signed && v >= 8) ? v - 16 : v;
             }
+        } else {
+            uint2 w = reinterpret_cast<const uint2*>(reinterpret_cast<const uint8_t*>(d.q) + r * d.cols)[c0 / 8];
 #pragma unroll
-            for (int u = 0; u < DQ_U; ++u) {
-                int64_t c = cb + (int64_t)u * blockDim.x;
-                if (c >= nchunks) break;
-                int64_t base = r * d.cols + c * 8;
-                if (d.yt == QLIN_BF16) {
-                    uint4 v;
-                    __nv_bfloat162 p0 = __floats2bfloat162_rn(out[u][0], out[u][1]);
-                    __nv_bfloat162 p1 = __floats2bfloat162_rn(out[u][2], out[u][3]);
-                    __nv_bfloat162 p2 = __floats2bfloat162_rn(out[u][4], out[u][5]);
-                    __nv_bfloat162 p3 = __floats2bfloat162_rn(out[u][6], out[u][7]);
-                    v.x = *reinterpret_cast<uint32_t*>(&p0);
-                    v.y = *reinterpret_cast<uint32_t*>(&p1);
-                    v.z = *reinterpret_cast<uint32_t*>(&p2);
-                    v.w = *reinterpret_cast<uint32_t*>(&p3);
-                    reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(d.y) + base)[0] = v;
-                } else if (d.yt == QLIN_F32) {
-                    float4* yp = reinterpret_cast<float4*>(reinterpret_cast<float*>(d.y) + base);
-                    yp[0] = make_float4(out[u][0], out[u][1], out[u][2], out[u][3]);
-                    yp[1] = make_float4(out[u][4], out[u][5], out[u][6], out[u][7]);
-                } else {
-#pragma unroll
-                    for (int j = 0; j < 8; ++j) store_y(d, base + j, out[u][j]);
-                }
+            for (int j = 0; j < 8; ++j) {
+                uint32_t b = ((j < 4 ? w.x : w.y) >> (8 * (j & 3))) & 0xFFu;
+                code[j] = d.code_signed ? (int)(int8_t)b : (int)b;
             }
+        }
+        float out[8];
+        if (d.gran == QLIN_PER_COL) {
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                float s = load_scale(d.s, c0 + j, d.scale_f16);
+                int z = d.z ? d.z[c0 + j] : 0;
+                out[j] = s * (float)(code[j] - z);
+            }
+        } else {
+            // one scope for the whole chunk (groups are whole chunks)
+            int64_t sc = (d.gran == QLIN_PER_TENSOR) ? 0
+                       : (d.gran == QLIN_PER_ROW) ? r
+                       : r * (d.cols / d.group) + c0 / d.group;
+            float s = load_scale(d.s, sc, d.scale_f16);
+            int z = d.z ? d.z[sc] : 0;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) out[j] = s * (float)(code[j] - z);
+        }
+        int64_t base = r * d.cols + c0;
+        if (d.yt == QLIN_BF16) {
+            uint4 u;
+            __nv_bfloat162 p0 = __floats2bfloat162_rn(out[0], out[1]);
+            __nv_bfloat162 p1 = __floats2bfloat162_rn(out[2], out[3]);
+            __nv_bfloat162 p2 = __floats2bfloat162_rn(out[4], out[5]);
+            __nv_bfloat162 p3 = __floats2bfloat162_rn(out[6], out[7]);
+            u.x = *reinterpret_cast<uint32_t*>(&p0);
+            u.y = *reinterpret_cast<uint32_t*>(&p1);
+            u.z = *reinterpret_cast<uint32_t*>(&p2);
+            u.w = *reinterpret_cast<uint32_t*>(&p3);
+            reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(d.y) + base)[0] = u;
+        } else if (d.yt == QLIN_F32) {
+            float4* yp = reinterpret_cast<float4*>(reinterpret_cast<float*>(d.y) + base);
+            yp[0] = make_float4(out[0], out[1], out[2], out[3]);
+            yp[1] = make_float4(out[4], out[5], out[6], out[7]);
+        } else {
+#pragma unroll
+            for (int j = 0; j < 8; ++j) store_y(d, base + j, out[j]);
         }
     }
 }
@@ -751,13 +735,10 @@ static bool rows_kernel_ok(const QuantArgs& a, int xt) {
     return true;
 }
 
-// Rows of up to 8192 elements: 4 chunks per thread and small CTAs (<= 256
-// threads), so that many rows are in flight per SM.  Longer rows (group
-// scopes) use 8 chunks per thread and up to 512 threads.
 template <typename T>
 static cudaError_t launch_rows(const QuantArgs& a, cudaStream_t st) {
     int64_t nchunks = a.cols / 8;
-    int cpt = (nchunks <= 128) ? 1 : (nchunks <= 256) ? 2 : (nchunks <= 1024) ? 4 : 8;
+    int cpt = (nchunks <= 512) ? 1 : (nchunks <= 1024) ? 2 : (nchunks <= 2048) ? 4 : 8;
     int64_t nt = ceil_div(nchunks, cpt);
     nt = ceil_div(nt, 32) * 32;
     if (a.gran == QLIN_PER_GROUP) {
@@ -766,7 +747,6 @@ static cudaError_t launch_rows(const QuantArgs& a, cudaStream_t st) {
     }
     if (nt < 32) nt = 32;
     int per_sm = (int)(2048 / nt);
-    if (per_sm > 16) per_sm = 16;
     if (per_sm < 1) per_sm = 1;
     int64_t grid = (int64_t)num_sms() * per_sm;
     if (grid > a.rows) grid = a.rows;
@@ -965,16 +945,9 @@ cudaError_t run_dequantize(const void* q, const void* s, const int32_t* z, const
     int ys = (yt == QLIN_F32) ? 4 : 2;
     bool vec = (cols % 8 == 0) && (p->gran != QLIN_PER_GROUP || p->group % 8 == 0) &&
                ((uintptr_t)q % (d.code4 ? 4 : 8) == 0) && ((uintptr_t)y % (8 * ys) == 0);
-    if (vec) {
-        int64_t nchunks = cols / 8;
-        int threads = nchunks >= 256 * DQ_U ? 256 : (int)ceil_div(ceil_div(nchunks, DQ_U), 32) * 32;
-        int64_t gx = ceil_div(nchunks, (int64_t)threads * DQ_U);
-        int64_t gy = ceil_div((int64_t)num_sms() * 2048 / threads, gx);
-        if (gy > rows) gy = rows;
-        if (gy > 65535) gy = 65535;
-        if (gy < 1) gy = 1;
-        k_dequant_vec<<<dim3((unsigned)gx, (unsigned)gy), threads, 0, st>>>(d);
-    } else
+    if (vec)
+        k_dequant_vec<<<blocks, 256, 0, st>>>(d);
+    else
         k_dequant_generic<<<blocks, 256, 0, st>>>(d);
     return cudaGetLastError();
 }
