@@ -497,11 +497,11 @@ __global__ void __launch_bounds__(w4tc::THREADS, 1) k_w4_gemm_tc(const __grid_co
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
-            tc::mbar_init(full_bar(s), NCONV + 1);  // converters + the TMA issuer's expect_tx
+            tc::mbar_init(full_bar(s), 8 + 1);  // one arrival per converter warp + the TMA issuer's expect_tx
             tc::mbar_init(empty_bar(s), 1);
         }
         tc::mbar_init(acc_full, 1);
-        tc::mbar_init(acc_empty, 128);
+        tc::mbar_init(acc_empty, 4);  // one arrival per epilogue warp
         tc::mbar_init(ev_bar, 1);
         tc::mbar_init(done_bar, 1);
         misc[2] = 0;
@@ -560,14 +560,15 @@ __global__ void __launch_bounds__(w4tc::THREADS, 1) k_w4_gemm_tc(const __grid_co
                 oh[2 * j] = f[1];      // row gq+8
                 oh[2 * j + 1] = f[3];
             }
-            if (!tc::mbar_wait(empty_bar(s), ph ^ 1u, abort_flag)) break;
+            if (!tc::mbar_wait_warp(empty_bar(s), ph ^ 1u, abort_flag)) break;
             uint8_t* tA = tiles + (size_t)s * STAGE_BYTES;
             *reinterpret_cast<uint4*>(tA + tc::sw128_off(r_g, 2 * t)) = make_uint4(og[0], og[1], og[2], og[3]);
             *reinterpret_cast<uint4*>(tA + tc::sw128_off(r_g, 2 * t + 1)) = make_uint4(og[4], og[5], og[6], og[7]);
             *reinterpret_cast<uint4*>(tA + tc::sw128_off(r_h, 2 * t)) = make_uint4(oh[0], oh[1], oh[2], oh[3]);
             *reinterpret_cast<uint4*>(tA + tc::sw128_off(r_h, 2 * t + 1)) = make_uint4(oh[4], oh[5], oh[6], oh[7]);
             tc::fence_proxy_async_smem();
-            tc::mbar_arrive(full_bar(s));
+            __syncwarp();
+            if (lane == 0) tc::mbar_arrive(full_bar(s));
         }
     } else if (warp == TMA_WARP) {
         // ---------------------------------------------------------- activation tiles (TMA)
@@ -592,7 +593,7 @@ __global__ void __launch_bounds__(w4tc::THREADS, 1) k_w4_gemm_tc(const __grid_co
         for (int kb = 0; kb < nkb; ++kb) {
             const int s = kb % STAGES;
             const uint32_t ph = (uint32_t)(kb / STAGES) & 1u;
-            if (!tc::mbar_wait(full_bar(s), ph, abort_flag)) {
+            if (!tc::mbar_wait_warp(full_bar(s), ph, abort_flag)) {
                 ok = false;
                 break;
             }
@@ -603,7 +604,7 @@ __global__ void __launch_bounds__(w4tc::THREADS, 1) k_w4_gemm_tc(const __grid_co
                     tc::mma_commit(acc_full);
                 }
                 __syncwarp();
-                if (!tc::mbar_wait(acc_empty, ndrain & 1u, abort_flag)) {
+                if (!tc::mbar_wait_warp(acc_empty, ndrain & 1u, abort_flag)) {
                     ok = false;
                     break;
                 }
@@ -632,7 +633,7 @@ __global__ void __launch_bounds__(w4tc::THREADS, 1) k_w4_gemm_tc(const __grid_co
             tc::mma_commit(done_bar);
         }
         __syncwarp();
-        tc::mbar_wait(done_bar, 0, abort_flag);
+        tc::mbar_wait_warp(done_bar, 0, abort_flag);
     } else {
         // ---------------------------------------------------------- promotions + epilogue
         const int q = warp & 3;
@@ -642,9 +643,9 @@ __global__ void __launch_bounds__(w4tc::THREADS, 1) k_w4_gemm_tc(const __grid_co
         const uint32_t t_sum = tmem + lane_base + 256;
         uint32_t ndrain = 0;
         for (uint32_t ev = 0;; ++ev) {
-            if (!tc::mbar_wait(ev_bar, ev & 1u, abort_flag)) break;
+            if (!tc::mbar_wait_warp(ev_bar, ev & 1u, abort_flag)) break;
             const uint32_t type = misc[1];
-            if (!tc::mbar_wait(acc_full, ev & 1u, abort_flag)) break;
+            if (!tc::mbar_wait_warp(acc_full, ev & 1u, abort_flag)) break;
             tc::tc_fence_after();
             if (type == EV_DRAIN) {
                 for (int c = 0; c < a.ntok; c += 32) {
@@ -660,7 +661,8 @@ __global__ void __launch_bounds__(w4tc::THREADS, 1) k_w4_gemm_tc(const __grid_co
                 tc::tmem_wait_st();
                 ++ndrain;
                 tc::tc_fence_before();
-                tc::mbar_arrive(acc_empty);
+                __syncwarp();
+                if (lane == 0) tc::mbar_arrive(acc_empty);
                 continue;
             }
             if (type != EV_FINAL) break;

@@ -322,16 +322,18 @@ __global__ void __launch_bounds__(w8tc::THREADS, 1)
     const uint32_t done_bar = acc_full + 24u;
 
     if (threadIdx.x == 0) {
+        // converter warps arrive once per warp (an elected lane after __syncwarp):
+        // one arrival per thread would serialize 256 arrivals per k-block
         for (int s = 0; s < S16; ++s) {
-            tc::mbar_init(full_bar(s), NCONV);
+            tc::mbar_init(full_bar(s), NCONV_WARPS);
             tc::mbar_init(empty_bar(s), 1);
         }
         for (int s = 0; s < S8; ++s) {
             tc::mbar_init(full8_bar(s), 1);
-            tc::mbar_init(empty8_bar(s), NCONV);
+            tc::mbar_init(empty8_bar(s), NCONV_WARPS);
         }
         tc::mbar_init(acc_full, 1);
-        tc::mbar_init(acc_empty, 128);
+        tc::mbar_init(acc_empty, 4);  // one arrival per epilogue warp
         tc::mbar_init(ev_bar, 1);
         tc::mbar_init(done_bar, 1);
         misc[2] = 0;
@@ -352,7 +354,7 @@ __global__ void __launch_bounds__(w8tc::THREADS, 1)
         for (int kb = 0; kb < nkb; ++kb) {
             const int s = kb % S16, s8 = kb % S8;
             const uint32_t ph = (uint32_t)(kb / S16) & 1u, ph8 = (uint32_t)(kb / S8) & 1u;
-            if (!tc::mbar_wait(full8_bar(s8), ph8, abort_flag)) break;
+            if (!tc::mbar_wait_warp(full8_bar(s8), ph8, abort_flag)) break;
             const uint8_t* a8 = stage8 + (size_t)s8 * STAGE8_BYTES;
             uint4 cur[PPT];
 #pragma unroll
@@ -379,8 +381,9 @@ __global__ void __launch_bounds__(w8tc::THREADS, 1)
                 a += __shfl_xor_sync(0xffffffffu, a, 2);
                 rs[j] = a;
             }
-            tc::mbar_arrive(empty8_bar(s8));  // the staging slot may be refilled
-            if (!tc::mbar_wait(empty_bar(s), ph ^ 1u, abort_flag)) break;
+            __syncwarp();
+            if (lane == 0) tc::mbar_arrive(empty8_bar(s8));  // the staging slot may be refilled
+            if (!tc::mbar_wait_warp(empty_bar(s), ph ^ 1u, abort_flag)) break;
             uint8_t* tA = tiles + (size_t)s * STAGE_BYTES;
             uint8_t* tB = tA + A_BYTES;
 #pragma unroll
@@ -397,7 +400,8 @@ __global__ void __launch_bounds__(w8tc::THREADS, 1)
                 if (j < A_PIECES / NCONV && ch == 0) rowsum[s * BM + row] = rs[j];
             }
             tc::fence_proxy_async_smem();
-            tc::mbar_arrive(full_bar(s));
+            __syncwarp();
+            if (lane == 0) tc::mbar_arrive(full_bar(s));
         }
     } else if (warp == TMA_WARP) {
         // ---------------------------------------------------------- int8 tile loads
@@ -424,7 +428,7 @@ __global__ void __launch_bounds__(w8tc::THREADS, 1)
         for (int kb = 0; kb < nkb && ok; ++kb) {
             const int s = kb % S16;
             const uint32_t ph = (uint32_t)(kb / S16) & 1u;
-            if (!tc::mbar_wait(full_bar(s), ph, abort_flag)) {
+            if (!tc::mbar_wait_warp(full_bar(s), ph, abort_flag)) {
                 ok = false;
                 break;
             }
@@ -444,7 +448,7 @@ __global__ void __launch_bounds__(w8tc::THREADS, 1)
                     tc::mma_commit(acc_full);
                 }
                 __syncwarp();
-                if (!tc::mbar_wait(acc_empty, ndrain & 1u, abort_flag)) {
+                if (!tc::mbar_wait_warp(acc_empty, ndrain & 1u, abort_flag)) {
                     ok = false;
                     break;
                 }
@@ -476,7 +480,7 @@ __global__ void __launch_bounds__(w8tc::THREADS, 1)
             tc::mma_commit(done_bar);
         }
         __syncwarp();
-        tc::mbar_wait(done_bar, 0, abort_flag);
+        tc::mbar_wait_warp(done_bar, 0, abort_flag);
     } else {
         // ---------------------------------------------------------- drains + epilogue
         const int q = warp & 3;  // TMEM lane quarter of this warp
@@ -486,9 +490,9 @@ __global__ void __launch_bounds__(w8tc::THREADS, 1)
         const uint32_t t_int = tmem + lane_base + 256;
         uint32_t ndrain = 0;
         for (uint32_t ev = 0;; ++ev) {
-            if (!tc::mbar_wait(ev_bar, ev & 1u, abort_flag)) break;
+            if (!tc::mbar_wait_warp(ev_bar, ev & 1u, abort_flag)) break;
             const uint32_t type = misc[1];
-            if (!tc::mbar_wait(acc_full, ev & 1u, abort_flag)) break;
+            if (!tc::mbar_wait_warp(acc_full, ev & 1u, abort_flag)) break;
             tc::tc_fence_after();
             if (type == EV_DRAIN) {
                 for (int c = 0; c < BN; c += 32) {
@@ -506,7 +510,8 @@ __global__ void __launch_bounds__(w8tc::THREADS, 1)
                 tc::tmem_wait_st();
                 ++ndrain;
                 tc::tc_fence_before();
-                tc::mbar_arrive(acc_empty);
+                __syncwarp();
+                if (lane == 0) tc::mbar_arrive(acc_empty);
                 continue;
             }
             if (type != EV_FINAL) break;
