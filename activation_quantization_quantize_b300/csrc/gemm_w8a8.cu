@@ -11,11 +11,12 @@
 // kernel (k_w8a8_tc) therefore computes the exact integer contraction on the
 // fp16 tensor cores: codes in [-128, 127] are exact in fp16, every product
 // (<= 2^14) is exact in fp32, and a sum of integers stays exact while its
-// magnitude is below 2^24.  The converter warps track, per activation row, the
-// sum of |code| since the accumulator was last emptied; before a k-block could
-// push any partial sum to 2^24 (sum|qx| * 128 >= 2^24), the accumulator is
-// drained into an INT32 region of tensor memory and restarted.  The INT32
-// result is therefore bit-exact for every input.
+// magnitude is below 2^24.  The converter warps report, per activation row and
+// k-block of 64, the sum of |code|; the MMA warp accumulates it since the
+// accumulator was last emptied.  Before a k-block could push any partial sum
+// to 2^24 (sum|qx| * 128 >= 2^24), the accumulator is drained into an INT32
+// region of tensor memory and restarted.  The INT32 result is therefore
+// bit-exact for every input.
 //
 // k_w8a8_mma (warp-level mma.sync s8, native INT32 accumulation) is the
 // legacy-path kernel, kept for comparison (QLIN_W8A8_KERNEL=mma).
@@ -222,8 +223,13 @@ __device__ __forceinline__ void s8x4_to_f16(uint32_t w, uint32_t& lo, uint32_t& 
     asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(hi) : "r"(b), "r"(0x64806480u));
 }
 
-__device__ __forceinline__ uint32_t abs_sum4(uint32_t w, uint32_t acc) {
-    return __dp4a(__vabs4(w), 0x01010101u, acc);  // bytes as unsigned |b|, -128 -> 128
+// acc + sum of |b| over the four int8 codes b of w, exactly: a negative byte b
+// becomes ~b = |b| - 1 (non-negative as a signed byte), and the count of
+// negative bytes is added back.
+__device__ __forceinline__ int abs_sum4(uint32_t w, int acc) {
+    const uint32_t neg = (w >> 7) & 0x01010101u;  // 1 in every negative byte
+    acc = __dp4a((int)(w ^ (neg * 0xFFu)), 0x01010101, acc);
+    return __dp4a((int)neg, 0x01010101, acc);
 }
 
 // Epilogue of 32 consecutive outputs of row m starting at column nb:
@@ -351,6 +357,18 @@ __global__ void __launch_bounds__(w8tc::THREADS, 1)
     if (warp < NCONV_WARPS) {
         // ---------------------------------------------------------- converters
         const int tid = threadIdx.x;
+        // swizzled byte offsets (within a stage) of each piece's first 16-byte
+        // chunk; the second chunk is at offset ^ 16
+        uint32_t soff[PPT];
+#pragma unroll
+        for (int j = 0; j < PPT; ++j) {
+            const int piece = tid + NCONV * j;
+            const bool is_a = j < A_PIECES / NCONV;
+            const int pr = is_a ? piece : piece - A_PIECES;
+            soff[j] = (is_a ? 0u : (uint32_t)A_BYTES) + tc::sw128_off((uint32_t)(pr >> 2), 2u * (uint32_t)(pr & 3));
+        }
+        const uint32_t rs_row = (uint32_t)(tid >> 2);  // A row of the first piece (j = 0); j = 1 adds 64
+        const bool rs_leader = (tid & 3) == 0;
         for (int kb = 0; kb < nkb; ++kb) {
             const int s = kb % S16, s8 = kb % S8;
             const uint32_t ph = (uint32_t)(kb / S16) & 1u, ph8 = (uint32_t)(kb / S8) & 1u;
@@ -370,34 +388,30 @@ __global__ void __launch_bounds__(w8tc::THREADS, 1)
                 s8x4_to_f16(cur[j].z, hbuf[j][4], hbuf[j][5]);
                 s8x4_to_f16(cur[j].w, hbuf[j][6], hbuf[j][7]);
             }
-            uint32_t rs[A_PIECES / NCONV];
+            int rs[A_PIECES / NCONV];
 #pragma unroll
             for (int j = 0; j < A_PIECES / NCONV; ++j) {
-                uint32_t a = abs_sum4(cur[j].x, 0);
+                int a = abs_sum4(cur[j].x, 0);
                 a = abs_sum4(cur[j].y, a);
                 a = abs_sum4(cur[j].z, a);
                 a = abs_sum4(cur[j].w, a);
                 a += __shfl_xor_sync(0xffffffffu, a, 1);
                 a += __shfl_xor_sync(0xffffffffu, a, 2);
-                rs[j] = a;
+                rs[j] = a;  // sum |q| of the row's 64 codes of this k-block
             }
             __syncwarp();
             if (lane == 0) tc::mbar_arrive(empty8_bar(s8));  // the staging slot may be refilled
             if (!tc::mbar_wait_warp(empty_bar(s), ph ^ 1u, abort_flag)) break;
-            uint8_t* tA = tiles + (size_t)s * STAGE_BYTES;
-            uint8_t* tB = tA + A_BYTES;
+            uint8_t* tS = tiles + (size_t)s * STAGE_BYTES;
 #pragma unroll
             for (int j = 0; j < PPT; ++j) {
-                int piece = tid + NCONV * j;
-                bool is_a = piece < A_PIECES;
-                int pr = is_a ? piece : piece - A_PIECES;
-                uint32_t row = (uint32_t)(pr >> 2), ch = (uint32_t)(pr & 3);
-                uint8_t* t = is_a ? tA : tB;
-                *reinterpret_cast<uint4*>(t + tc::sw128_off(row, 2 * ch)) =
-                    make_uint4(hbuf[j][0], hbuf[j][1], hbuf[j][2], hbuf[j][3]);
-                *reinterpret_cast<uint4*>(t + tc::sw128_off(row, 2 * ch + 1)) =
+                *reinterpret_cast<uint4*>(tS + soff[j]) = make_uint4(hbuf[j][0], hbuf[j][1], hbuf[j][2], hbuf[j][3]);
+                *reinterpret_cast<uint4*>(tS + (soff[j] ^ 16u)) =
                     make_uint4(hbuf[j][4], hbuf[j][5], hbuf[j][6], hbuf[j][7]);
-                if (j < A_PIECES / NCONV && ch == 0) rowsum[s * BM + row] = rs[j];
+            }
+            if (rs_leader) {
+                rowsum[s * BM + rs_row] = (uint32_t)rs[0];
+                rowsum[s * BM + rs_row + 64] = (uint32_t)rs[1];
             }
             tc::fence_proxy_async_smem();
             __syncwarp();
@@ -432,10 +446,11 @@ __global__ void __launch_bounds__(w8tc::THREADS, 1)
                 ok = false;
                 break;
             }
-            uint32_t T[4], mx = 0;
+            uint32_t T[4], B[4], mx = 0;
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
-                T[i] = S[i] + rowsum[s * BM + lane * 4 + i];
+                B[i] = rowsum[s * BM + lane * 4 + i];
+                T[i] = S[i] + B[i];
                 mx = max(mx, T[i]);
             }
 #pragma unroll
@@ -455,7 +470,7 @@ __global__ void __launch_bounds__(w8tc::THREADS, 1)
                 ++ndrain;
                 started = false;
 #pragma unroll
-                for (int i = 0; i < 4; ++i) S[i] = rowsum[s * BM + lane * 4 + i];
+                for (int i = 0; i < 4; ++i) S[i] = B[i];
             } else {
 #pragma unroll
                 for (int i = 0; i < 4; ++i) S[i] = T[i];
