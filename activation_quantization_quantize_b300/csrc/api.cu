@@ -188,7 +188,7 @@ int qlin_gemm_w8a8(const int8_t* qx, const float* sx, const int8_t* qw, const fl
         (acc_out && !aligned(acc_out, 4)))
         return QLIN_ERR_ARG;
     size_t need = w8a8_ws_bytes(M, N, K);
-    if (need > 0 && (!ws || ws_bytes < need)) return QLIN_ERR_WORKSPACE;
+    if (need > 0 && (!ws || ws_bytes < need || !aligned(ws, 16))) return QLIN_ERR_WORKSPACE;
     if (K == 0) return QLIN_ERR_UNSUPPORTED;
     return cuda_status(run_gemm_w8a8(qx, sx, qw, sw, M, N, K, y, yt, acc_out, ws, (cudaStream_t)stream));
 }

@@ -186,15 +186,16 @@ __global__ void __launch_bounds__(w8::THREADS) k_w8a8_mma(const int8_t* __restri
 
 // ====================================================================== tcgen05 kernel
 namespace w8tc {
-constexpr int BM = 128;                   // rows of qx per CTA (TMEM lanes)
+constexpr int BM = 256;                   // rows of qx per CTA: two M=128 MMAs (TMEM lanes)
 constexpr int BN = 256;                   // rows of qw per CTA (TMEM columns)
 constexpr int BK = 64;                    // k per stage (one 128-byte fp16 row)
-constexpr int S16 = 3;                    // fp16 operand stages (converter -> MMA)
+constexpr int S16 = 2;                    // fp16 operand stages (converter -> MMA)
 constexpr int S8 = 3;                     // int8 staging stages (TMA -> converter)
-constexpr int A_BYTES = BM * BK * 2;      // 16 KB fp16 tile
+constexpr int A_BYTES = BM * BK * 2;      // 32 KB fp16 tile (two 16 KB halves)
+constexpr int A_HALF = A_BYTES / 2;
 constexpr int B_BYTES = BN * BK * 2;      // 32 KB fp16 tile
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-constexpr int A8_BYTES = BM * BK;         // 8 KB int8 tile (rows of 64 bytes)
+constexpr int A8_BYTES = BM * BK;         // 16 KB int8 tile (rows of 64 bytes)
 constexpr int B8_BYTES = BN * BK;         // 16 KB
 constexpr int STAGE8_BYTES = A8_BYTES + B8_BYTES;
 constexpr int NCONV_WARPS = 8;            // warps 0-7: int8 -> fp16 converters
@@ -203,13 +204,13 @@ constexpr int EPI_WARP0 = 8;              // warps 8-11: drains + epilogue (one 
 constexpr int MMA_WARP = 12;              // warp 12: TMEM owner, MMA issuer
 constexpr int TMA_WARP = 13;              // warp 13: int8 tile loads
 constexpr int THREADS = 14 * 32;
-constexpr int PIECES = (BM + BN) * BK / 16;   // 16-byte int8 pieces per k-block (1536)
-constexpr int PPT = PIECES / NCONV;           // pieces per converter thread (6)
-constexpr int A_PIECES = BM * BK / 16;        // 512
+constexpr int PIECES = (BM + BN) * BK / 16;   // 16-byte int8 pieces per k-block (2048)
+constexpr int PPT = PIECES / NCONV;           // pieces per converter thread (8)
+constexpr int A_PIECES = BM * BK / 16;        // 1024
 constexpr uint32_t ROWSUM_LIMIT = 131071;     // sum|qx| * 128 < 2^24
-constexpr uint32_t TMEM_COLS = 512;           // [0,256): fp32 accumulator, [256,512): int32 sums
+constexpr uint32_t TMEM_COLS = 512;           // [0,256): rows 0-127, [256,512): rows 128-255 (fp32)
 constexpr uint32_t EV_DRAIN = 1, EV_FINAL = 2;
-constexpr size_t CTRL_BYTES = 4096;
+constexpr size_t CTRL_BYTES = 2048;
 constexpr size_t SMEM_BYTES = 1024 + (size_t)S16 * STAGE_BYTES + (size_t)S8 * STAGE8_BYTES + CTRL_BYTES;
 }  // namespace w8tc
 
@@ -293,12 +294,17 @@ struct W8TcArgs {
     void* y;
     int yt;
     int32_t* acc_out;
+    int32_t* drain;   // [M][N] INT32 partial sums, written only when a drain occurs
     int num_m_tiles;
 };
 
-// int8 tiles arrive by TMA (zero-filled past M, N and K) into a staging ring;
-// converter warps widen them to fp16 in the 128B-swizzled layout the MMA
-// reads; one thread issues tcgen05.mma (kind::f16, fp32 in TMEM).
+// A CTA owns a 256 x 256 output tile: two M=128 MMAs per k-step share the
+// converted weight tile, so widening (and shared-memory traffic) per FLOP is a
+// third lower than with a 128-row tile.  int8 tiles arrive by TMA (zero-filled
+// past M, N and K) into a staging ring; converter warps widen them to fp16 in
+// the 128B-swizzled layout the MMA reads; one thread issues tcgen05.mma
+// (kind::f16, fp32 in TMEM).  Drains (rare) add the accumulators into an INT32
+// tile in global memory.
 __global__ void __launch_bounds__(w8tc::THREADS, 1)
     k_w8a8_tc(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b, W8TcArgs p) {
     using namespace w8tc;
@@ -308,8 +314,8 @@ __global__ void __launch_bounds__(w8tc::THREADS, 1)
     uint8_t* stage8 = smem + S16 * STAGE_BYTES;              // S8 x (A int8 | B int8)
     uint64_t* bars = reinterpret_cast<uint64_t*>(stage8 + S8 * STAGE8_BYTES);
     // bars: full16[S16], empty16[S16], full8[S8], empty8[S8], acc_full, acc_empty, ev, done
-    uint32_t* rowsum = reinterpret_cast<uint32_t*>(bars + 2 * S16 + 2 * S8 + 4);  // [S16][BM]
-    volatile uint32_t* misc = rowsum + S16 * BM;  // [0] tmem base, [1] event type, [2] abort
+    uint16_t* rowsum = reinterpret_cast<uint16_t*>(bars + 2 * S16 + 2 * S8 + 4);  // [S16][BM]
+    volatile uint32_t* misc = reinterpret_cast<volatile uint32_t*>(rowsum + S16 * BM);  // tmem, event, abort
     volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 2);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -328,8 +334,7 @@ __global__ void __launch_bounds__(w8tc::THREADS, 1)
     const uint32_t done_bar = acc_full + 24u;
 
     if (threadIdx.x == 0) {
-        // converter warps arrive once per warp (an elected lane after __syncwarp):
-        // one arrival per thread would serialize 256 arrivals per k-block
+        // converter warps arrive once per warp (an elected lane after __syncwarp)
         for (int s = 0; s < S16; ++s) {
             tc::mbar_init(full_bar(s), NCONV_WARPS);
             tc::mbar_init(empty_bar(s), 1);
@@ -358,7 +363,8 @@ __global__ void __launch_bounds__(w8tc::THREADS, 1)
         // ---------------------------------------------------------- converters
         const int tid = threadIdx.x;
         // swizzled byte offsets (within a stage) of each piece's first 16-byte
-        // chunk; the second chunk is at offset ^ 16
+        // chunk; the second chunk is at offset ^ 16.  Pieces j < 4 are
+        // activation rows tid/4 + 64 j, the rest weight rows.
         uint32_t soff[PPT];
 #pragma unroll
         for (int j = 0; j < PPT; ++j) {
@@ -367,7 +373,7 @@ __global__ void __launch_bounds__(w8tc::THREADS, 1)
             const int pr = is_a ? piece : piece - A_PIECES;
             soff[j] = (is_a ? 0u : (uint32_t)A_BYTES) + tc::sw128_off((uint32_t)(pr >> 2), 2u * (uint32_t)(pr & 3));
         }
-        const uint32_t rs_row = (uint32_t)(tid >> 2);  // A row of the first piece (j = 0); j = 1 adds 64
+        const uint32_t rs_row = (uint32_t)(tid >> 2);
         const bool rs_leader = (tid & 3) == 0;
         for (int kb = 0; kb < nkb; ++kb) {
             const int s = kb % S16, s8 = kb % S8;
@@ -376,18 +382,7 @@ __global__ void __launch_bounds__(w8tc::THREADS, 1)
             const uint8_t* a8 = stage8 + (size_t)s8 * STAGE8_BYTES;
             uint4 cur[PPT];
 #pragma unroll
-            for (int j = 0; j < PPT; ++j) {
-                // piece = tid + 256 j: pieces 0..511 are A (row = piece/4), the rest B
-                cur[j] = *reinterpret_cast<const uint4*>(a8 + (size_t)(tid + NCONV * j) * 16);
-            }
-            uint32_t hbuf[PPT][8];
-#pragma unroll
-            for (int j = 0; j < PPT; ++j) {
-                s8x4_to_f16(cur[j].x, hbuf[j][0], hbuf[j][1]);
-                s8x4_to_f16(cur[j].y, hbuf[j][2], hbuf[j][3]);
-                s8x4_to_f16(cur[j].z, hbuf[j][4], hbuf[j][5]);
-                s8x4_to_f16(cur[j].w, hbuf[j][6], hbuf[j][7]);
-            }
+            for (int j = 0; j < PPT; ++j) cur[j] = *reinterpret_cast<const uint4*>(a8 + (size_t)(tid + NCONV * j) * 16);
             int rs[A_PIECES / NCONV];
 #pragma unroll
             for (int j = 0; j < A_PIECES / NCONV; ++j) {
@@ -397,7 +392,15 @@ __global__ void __launch_bounds__(w8tc::THREADS, 1)
                 a = abs_sum4(cur[j].w, a);
                 a += __shfl_xor_sync(0xffffffffu, a, 1);
                 a += __shfl_xor_sync(0xffffffffu, a, 2);
-                rs[j] = a;  // sum |q| of the row's 64 codes of this k-block
+                rs[j] = a;  // sum |q| of the row's 64 codes of this k-block (<= 8192)
+            }
+            uint32_t hbuf[PPT][8];
+#pragma unroll
+            for (int j = 0; j < PPT; ++j) {
+                s8x4_to_f16(cur[j].x, hbuf[j][0], hbuf[j][1]);
+                s8x4_to_f16(cur[j].y, hbuf[j][2], hbuf[j][3]);
+                s8x4_to_f16(cur[j].z, hbuf[j][4], hbuf[j][5]);
+                s8x4_to_f16(cur[j].w, hbuf[j][6], hbuf[j][7]);
             }
             __syncwarp();
             if (lane == 0) tc::mbar_arrive(empty8_bar(s8));  // the staging slot may be refilled
@@ -410,8 +413,8 @@ __global__ void __launch_bounds__(w8tc::THREADS, 1)
                     make_uint4(hbuf[j][4], hbuf[j][5], hbuf[j][6], hbuf[j][7]);
             }
             if (rs_leader) {
-                rowsum[s * BM + rs_row] = (uint32_t)rs[0];
-                rowsum[s * BM + rs_row + 64] = (uint32_t)rs[1];
+#pragma unroll
+                for (int j = 0; j < A_PIECES / NCONV; ++j) rowsum[s * BM + rs_row + 64 * j] = (uint16_t)rs[j];
             }
             tc::fence_proxy_async_smem();
             __syncwarp();
@@ -433,9 +436,9 @@ __global__ void __launch_bounds__(w8tc::THREADS, 1)
         __syncwarp();
     } else if (warp == MMA_WARP) {
         // ---------------------------------------------------------- MMA issuer
-        constexpr uint32_t IDESC = tc::idesc_f16(BM, BN, false);
+        constexpr uint32_t IDESC = tc::idesc_f16(128, BN, false);
         const uint32_t tiles_addr = tc::smem_addr(tiles);
-        uint32_t S[4] = {0, 0, 0, 0};
+        uint32_t S[8] = {0, 0, 0, 0, 0, 0, 0, 0};  // running sum|qx| of rows 8 lane .. 8 lane + 7
         bool started = false;
         uint32_t ndrain = 0;
         bool ok = true;
@@ -446,17 +449,16 @@ __global__ void __launch_bounds__(w8tc::THREADS, 1)
                 ok = false;
                 break;
             }
-            uint32_t T[4], B[4], mx = 0;
+            uint32_t B[8], mx = 0;
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                B[i] = rowsum[s * BM + lane * 4 + i];
-                T[i] = S[i] + B[i];
-                mx = max(mx, T[i]);
+            for (int i = 0; i < 8; ++i) {
+                B[i] = rowsum[s * BM + lane * 8 + i];
+                mx = max(mx, S[i] + B[i]);
             }
 #pragma unroll
             for (int o = 16; o > 0; o >>= 1) mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
             if (started && mx > ROWSUM_LIMIT) {
-                // drain the accumulator into the INT32 sums before adding this k-block
+                // drain the accumulators into the INT32 tile before adding this k-block
                 if (lane == 0) {
                     misc[1] = EV_DRAIN;
                     tc::mbar_arrive(ev_bar);
@@ -470,19 +472,23 @@ __global__ void __launch_bounds__(w8tc::THREADS, 1)
                 ++ndrain;
                 started = false;
 #pragma unroll
-                for (int i = 0; i < 4; ++i) S[i] = B[i];
+                for (int i = 0; i < 8; ++i) S[i] = B[i];
             } else {
 #pragma unroll
-                for (int i = 0; i < 4; ++i) S[i] = T[i];
+                for (int i = 0; i < 8; ++i) S[i] += B[i];
             }
             tc::tc_fence_after();
             if (lane == 0) {
                 const uint32_t a_addr = tiles_addr + (uint32_t)s * STAGE_BYTES;
-                const uint64_t ad = tc::desc_sw128(a_addr);
+                const uint64_t ad0 = tc::desc_sw128(a_addr);
+                const uint64_t ad1 = tc::desc_sw128(a_addr + A_HALF);
                 const uint64_t bd = tc::desc_sw128(a_addr + A_BYTES);
 #pragma unroll
-                for (int j = 0; j < BK / 16; ++j)  // 32 bytes of K per MMA
-                    tc::mma_f16(tmem, ad + 2 * j, bd + 2 * j, IDESC, (started || j > 0) ? 1u : 0u);
+                for (int j = 0; j < BK / 16; ++j) {  // 32 bytes of K per MMA
+                    const uint32_t acc = (started || j > 0) ? 1u : 0u;
+                    tc::mma_f16(tmem, ad0 + 2 * j, bd + 2 * j, IDESC, acc);
+                    tc::mma_f16(tmem + 256, ad1 + 2 * j, bd + 2 * j, IDESC, acc);
+                }
                 tc::mma_commit(empty_bar(s));
             }
             started = true;
@@ -500,53 +506,64 @@ __global__ void __launch_bounds__(w8tc::THREADS, 1)
         // ---------------------------------------------------------- drains + epilogue
         const int q = warp & 3;  // TMEM lane quarter of this warp
         const uint32_t lane_base = (uint32_t)(32 * q) << 16;
-        const int64_t m = m0 + 32 * q + lane;
-        const uint32_t t_acc = tmem + lane_base;
-        const uint32_t t_int = tmem + lane_base + 256;
         uint32_t ndrain = 0;
         for (uint32_t ev = 0;; ++ev) {
             if (!tc::mbar_wait_warp(ev_bar, ev & 1u, abort_flag)) break;
             const uint32_t type = misc[1];
             if (!tc::mbar_wait_warp(acc_full, ev & 1u, abort_flag)) break;
             tc::tc_fence_after();
-            if (type == EV_DRAIN) {
+            if (type != EV_DRAIN && type != EV_FINAL) break;
+            const float swz = 0.0f;
+            (void)swz;
+            for (int h = 0; h < 2; ++h) {
+                const int64_t m = m0 + 128 * h + 32 * q + lane;
+                const float sxm = (type == EV_FINAL && m < p.M) ? p.sx[m] : 0.0f;
                 for (int c = 0; c < BN; c += 32) {
-                    uint32_t a[32], r[32];
-                    tc::tmem_ld32(t_acc + c, a);
-                    if (ndrain) tc::tmem_ld32(t_int + c, r);
+                    __syncwarp();
+                    uint32_t a[32];
+                    tc::tmem_ld32(tmem + lane_base + 256 * h + c, a);
                     tc::tmem_wait_ld();
+                    int tot[32];
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) {
-                        int v = __float2int_rn(__uint_as_float(a[j]));
-                        r[j] = ndrain ? (uint32_t)((int)r[j] + v) : (uint32_t)v;
+                    for (int j = 0; j < 32; ++j) tot[j] = __float2int_rn(__uint_as_float(a[j]));
+                    if (m >= p.M) continue;
+                    const int64_t nb = n0 + c;
+                    int32_t* dp = p.drain + m * p.N + nb;
+                    const bool full = (nb + 32 <= p.N) && (p.N % 4 == 0);
+                    if (ndrain) {  // add the INT32 sums of earlier drains
+                        if (full) {
+#pragma unroll
+                            for (int j = 0; j < 32; j += 4) {
+                                int4 v = *reinterpret_cast<const int4*>(dp + j);
+                                tot[j] += v.x;
+                                tot[j + 1] += v.y;
+                                tot[j + 2] += v.z;
+                                tot[j + 3] += v.w;
+                            }
+                        } else {
+                            for (int j = 0; j < 32; ++j)
+                                if (nb + j < p.N) tot[j] += dp[j];
+                        }
                     }
-                    tc::tmem_st32(t_int + c, r);
-                }
-                tc::tmem_wait_st();
-                ++ndrain;
-                tc::tc_fence_before();
-                __syncwarp();
-                if (lane == 0) tc::mbar_arrive(acc_empty);
-                continue;
-            }
-            if (type != EV_FINAL) break;
-            // final: y[m, n] = (float(total) * sx[m]) * sw[n]
-            const float sxm = (m < p.M) ? p.sx[m] : 0.0f;
-            for (int c = 0; c < BN; c += 32) {
-                __syncwarp();
-                uint32_t a[32], r[32];
-                tc::tmem_ld32(t_acc + c, a);
-                if (ndrain) tc::tmem_ld32(t_int + c, r);
-                tc::tmem_wait_ld();
-                int tot[32];
+                    if (type == EV_DRAIN) {
+                        if (full) {
 #pragma unroll
-                for (int j = 0; j < 32; ++j) {
-                    int v = __float2int_rn(__uint_as_float(a[j]));
-                    tot[j] = ndrain ? (int)r[j] + v : v;
+                            for (int j = 0; j < 32; j += 4)
+                                *reinterpret_cast<int4*>(dp + j) = make_int4(tot[j], tot[j + 1], tot[j + 2], tot[j + 3]);
+                        } else {
+                            for (int j = 0; j < 32; ++j)
+                                if (nb + j < p.N) dp[j] = tot[j];
+                        }
+                    } else {
+                        store_row32(tot, m, nb, p.N, sxm, p.sw, p.y, p.yt, p.acc_out);
+                    }
                 }
-                if (m < p.M) store_row32(tot, m, n0 + c, p.N, sxm, p.sw, p.y, p.yt, p.acc_out);
             }
-            break;
+            if (type == EV_FINAL) break;
+            ++ndrain;
+            tc::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) tc::mbar_arrive(acc_empty);
         }
     }
 
@@ -558,7 +575,9 @@ __global__ void __launch_bounds__(w8tc::THREADS, 1)
     }
 }
 
-size_t w8a8_ws_bytes(int64_t, int64_t, int64_t) { return 0; }
+// INT32 tile that drains of the exact accumulation add into (touched only
+// when a drain occurs).
+size_t w8a8_ws_bytes(int64_t M, int64_t N, int64_t) { return (size_t)M * N * sizeof(int32_t); }
 
 // 1 selects the legacy mma.sync kernel (read on every call, so a process can
 // compare both kernels).
@@ -568,7 +587,7 @@ static int w8a8_kernel_choice() {
 }
 
 cudaError_t run_gemm_w8a8(const int8_t* qx, const float* sx, const int8_t* qw, const float* sw, int64_t M, int64_t N,
-                          int64_t K, void* y, int yt, int32_t* acc_out, void*, cudaStream_t st) {
+                          int64_t K, void* y, int yt, int32_t* acc_out, void* ws, cudaStream_t st) {
     if (w8a8_kernel_choice() == 1) {
         using namespace w8;
         size_t smem = (size_t)2 * STAGES * TILE_BYTES;
@@ -606,6 +625,7 @@ cudaError_t run_gemm_w8a8(const int8_t* qx, const float* sx, const int8_t* qw, c
     a.y = y;
     a.yt = yt;
     a.acc_out = acc_out;
+    a.drain = reinterpret_cast<int32_t*>(ws);
     a.num_m_tiles = (int)ceil_div(M, BM);
     int64_t tiles = (int64_t)a.num_m_tiles * ceil_div(N, BN);
     k_w8a8_tc<<<(unsigned)tiles, THREADS, SMEM_BYTES, st>>>(ta, tb, a);

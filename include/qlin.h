@@ -207,6 +207,10 @@ int qlin_pack_w4(const void *q, const void *s_f16, const int32_t *z, int64_t N, 
  *   sw     device binary32 [N] per-channel scales.
  *   y      device output [M x N] of type yt (F32 or BF16), row-major.
  *   acc_out device int32 [M x N] exact sums, or NULL.
+ *   ws     device workspace of qlin_workspace_size(QLIN_OP_GEMM_W8A8, M, N, K)
+ *          bytes, 16-byte aligned: an INT32 [M x N] tile that the kernel only
+ *          touches when the exact accumulation must be drained (rows whose
+ *          sum of |code| over a run of K would reach 2^24 / 128).
  * Requirements: K % 16 == 0; qx, qw 16-byte aligned.  The exact sums must fit
  * int32 (always true for codes in [-127,127] when K < 133,144).
  */
