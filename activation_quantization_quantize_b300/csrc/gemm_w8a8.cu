@@ -187,7 +187,7 @@ __global__ void __launch_bounds__(w8::THREADS) k_w8a8_mma(const int8_t* __restri
 // ====================================================================== tcgen05 kernel
 namespace w8tc {
 constexpr int BM = 256;                   // rows of qx per CTA: two M=128 MMAs (TMEM lanes)
-constexpr int BN = 256;                   // rows of qw per CTA (TMEM columns)
+constexpr int BN = 256;                   // max rows of qw per CTA (TMEM columns); the launch picks bn <= BN
 constexpr int BK = 64;                    // k per stage (one 128-byte fp16 row)
 constexpr int S16 = 2;                    // fp16 operand stages (converter -> MMA)
 constexpr int S8 = 3;                     // int8 staging stages (TMA -> converter)
@@ -204,8 +204,8 @@ constexpr int EPI_WARP0 = 8;              // warps 8-11: drains + epilogue (one 
 constexpr int MMA_WARP = 12;              // warp 12: TMEM owner, MMA issuer
 constexpr int TMA_WARP = 13;              // warp 13: int8 tile loads
 constexpr int THREADS = 14 * 32;
-constexpr int PIECES = (BM + BN) * BK / 16;   // 16-byte int8 pieces per k-block (2048)
-constexpr int PPT = PIECES / NCONV;           // pieces per converter thread (8)
+constexpr int PIECES = (BM + BN) * BK / 16;   // max 16-byte int8 pieces per k-block (2048)
+constexpr int PPT = PIECES / NCONV;           // max pieces per converter thread (8)
 constexpr int A_PIECES = BM * BK / 16;        // 1024
 constexpr uint32_t ROWSUM_LIMIT = 131071;     // sum|qx| * 128 < 2^24
 constexpr uint32_t TMEM_COLS = 512;           // [0,256): rows 0-127, [256,512): rows 128-255 (fp32)
@@ -296,6 +296,8 @@ struct W8TcArgs {
     int32_t* acc_out;
     int32_t* drain;   // [M][N] INT32 partial sums, written only when a drain occurs
     int num_m_tiles;
+    int bn;           // weight rows per CTA (multiple of 32, <= 256)
+    uint32_t idesc;   // MMA instruction descriptor (M = 128, N = bn)
 };
 
 // A CTA owns a 256 x 256 output tile: two M=128 MMAs per k-step share the
@@ -319,9 +321,11 @@ __global__ void __launch_bounds__(w8tc::THREADS, 1)
     volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 2);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int bn = p.bn;
     const int64_t m0 = (int64_t)(blockIdx.x % p.num_m_tiles) * BM;
-    const int64_t n0 = (int64_t)(blockIdx.x / p.num_m_tiles) * BN;
+    const int64_t n0 = (int64_t)(blockIdx.x / p.num_m_tiles) * bn;
     const int nkb = (int)ceil_div(p.K, BK);
+    const int npieces = (BM + bn) * BK / 16;
 
     const uint32_t bar0 = tc::smem_addr(bars);
     auto full_bar = [&](int s) { return bar0 + 8u * s; };
@@ -382,7 +386,9 @@ __global__ void __launch_bounds__(w8tc::THREADS, 1)
             const uint8_t* a8 = stage8 + (size_t)s8 * STAGE8_BYTES;
             uint4 cur[PPT];
 #pragma unroll
-            for (int j = 0; j < PPT; ++j) cur[j] = *reinterpret_cast<const uint4*>(a8 + (size_t)(tid + NCONV * j) * 16);
+            for (int j = 0; j < PPT; ++j)
+                cur[j] = (tid + NCONV * j < npieces) ? *reinterpret_cast<const uint4*>(a8 + (size_t)(tid + NCONV * j) * 16)
+                                                    : make_uint4(0, 0, 0, 0);
             int rs[A_PIECES / NCONV];
 #pragma unroll
             for (int j = 0; j < A_PIECES / NCONV; ++j) {
@@ -408,6 +414,7 @@ __global__ void __launch_bounds__(w8tc::THREADS, 1)
             uint8_t* tS = tiles + (size_t)s * STAGE_BYTES;
 #pragma unroll
             for (int j = 0; j < PPT; ++j) {
+                if (tid + NCONV * j >= npieces) continue;
                 *reinterpret_cast<uint4*>(tS + soff[j]) = make_uint4(hbuf[j][0], hbuf[j][1], hbuf[j][2], hbuf[j][3]);
                 *reinterpret_cast<uint4*>(tS + (soff[j] ^ 16u)) =
                     make_uint4(hbuf[j][4], hbuf[j][5], hbuf[j][6], hbuf[j][7]);
@@ -427,7 +434,7 @@ __global__ void __launch_bounds__(w8tc::THREADS, 1)
                 const int s8 = kb % S8;
                 const uint32_t ph8 = (uint32_t)(kb / S8) & 1u;
                 if (!tc::mbar_wait(empty8_bar(s8), ph8 ^ 1u, abort_flag)) break;
-                tc::mbar_arrive_expect_tx(full8_bar(s8), STAGE8_BYTES);
+                tc::mbar_arrive_expect_tx(full8_bar(s8), (uint32_t)(BM + bn) * BK);
                 const uint32_t dst = tc::smem_addr(stage8 + (size_t)s8 * STAGE8_BYTES);
                 tc::tma_load_2d(dst, &tm_a, kb * BK, (int)m0, full8_bar(s8));
                 tc::tma_load_2d(dst + A8_BYTES, &tm_b, kb * BK, (int)n0, full8_bar(s8));
@@ -436,7 +443,7 @@ __global__ void __launch_bounds__(w8tc::THREADS, 1)
         __syncwarp();
     } else if (warp == MMA_WARP) {
         // ---------------------------------------------------------- MMA issuer
-        constexpr uint32_t IDESC = tc::idesc_f16(128, BN, false);
+        const uint32_t IDESC = p.idesc;
         const uint32_t tiles_addr = tc::smem_addr(tiles);
         uint32_t S[8] = {0, 0, 0, 0, 0, 0, 0, 0};  // running sum|qx| of rows 8 lane .. 8 lane + 7
         bool started = false;
@@ -518,7 +525,7 @@ __global__ void __launch_bounds__(w8tc::THREADS, 1)
             for (int h = 0; h < 2; ++h) {
                 const int64_t m = m0 + 128 * h + 32 * q + lane;
                 const float sxm = (type == EV_FINAL && m < p.M) ? p.sx[m] : 0.0f;
-                for (int c = 0; c < BN; c += 32) {
+                for (int c = 0; c < bn; c += 32) {
                     __syncwarp();
                     uint32_t a[32];
                     tc::tmem_ld32(tmem + lane_base + 256 * h + c, a);
@@ -604,7 +611,21 @@ cudaError_t run_gemm_w8a8(const int8_t* qx, const float* sx, const int8_t* qw, c
     cuuint64_t gda[2] = {(cuuint64_t)K, (cuuint64_t)M};
     cuuint64_t gdb[2] = {(cuuint64_t)K, (cuuint64_t)N};
     cuuint64_t gstride[1] = {(cuuint64_t)K};
-    cuuint32_t boxa[2] = {BK, BM}, boxb[2] = {BK, BN};
+    // Weight rows per CTA: the fewest waves of tiles over bn in {256, 224,
+    // ..., 128}, larger bn on ties (measured: a CTA's time per k-block does not
+    // shrink with bn, so only the wave count matters).
+    const int sms = num_sms();
+    const int64_t mt = ceil_div(M, BM);
+    int bn = BN;
+    int64_t best = INT64_MAX;
+    for (int cand = BN; cand >= 128; cand -= 32) {
+        const int64_t waves = ceil_div(mt * ceil_div(N, cand), sms);
+        if (waves < best) {
+            best = waves;
+            bn = cand;
+        }
+    }
+    cuuint32_t boxa[2] = {BK, BM}, boxb[2] = {BK, (cuuint32_t)bn};
     cuuint32_t estride[2] = {1, 1};
     if (enc(&ta, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<int8_t*>(qx), gda, gstride, boxa, estride,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -627,7 +648,9 @@ cudaError_t run_gemm_w8a8(const int8_t* qx, const float* sx, const int8_t* qw, c
     a.acc_out = acc_out;
     a.drain = reinterpret_cast<int32_t*>(ws);
     a.num_m_tiles = (int)ceil_div(M, BM);
-    int64_t tiles = (int64_t)a.num_m_tiles * ceil_div(N, BN);
+    a.bn = bn;
+    a.idesc = tc::idesc_f16(128, bn, false);
+    int64_t tiles = (int64_t)a.num_m_tiles * ceil_div(N, bn);
     k_w8a8_tc<<<(unsigned)tiles, THREADS, SMEM_BYTES, st>>>(ta, tb, a);
     return cudaGetLastError();
 }

@@ -73,6 +73,34 @@ __device__ __forceinline__ void load8<float>(const float* p, float v[8]) {
 template <typename T>
 __device__ __forceinline__ float load1(const T* p) { return to_f32<T>(p[0]); }
 
+// Widen 8 packed 16-bit values (one 16-byte chunk) to binary32.
+template <typename T>
+__device__ __forceinline__ void unpack8(const uint4 u, float v[8]);
+template <>
+__device__ __forceinline__ void unpack8<__nv_bfloat16>(const uint4 u, float v[8]) {
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        v[2 * i] = __uint_as_float(w[i] << 16);
+        v[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+    }
+}
+template <>
+__device__ __forceinline__ void unpack8<__half>(const uint4 u, float v[8]) {
+    uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        float2 f = __half22float2(*reinterpret_cast<__half2*>(&w[i]));
+        v[2 * i] = f.x;
+        v[2 * i + 1] = f.y;
+    }
+}
+template <>
+__device__ __forceinline__ void unpack8<float>(const uint4, float v[8]) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) v[i] = 0.0f;  // not used: binary32 rows take another kernel
+}
+
 // ---------------------------------------------------------------- scale / zero point
 struct ScopeParams {
     float s;      // stored scale (binary32 value of the stored scale)
@@ -156,6 +184,22 @@ __device__ __forceinline__ uint32_t code_bits(float v, const ScopeParams& p, con
         }
     } else {
         float q = rintf(__fdiv_rn(v, p.s));
+        m = fminf(fmaxf(q, -8388608.0f), 8388608.0f) + p.cz;
+    }
+    m = fminf(fmaxf(m, cr.lo), cr.hi);
+    return __float_as_uint(m);
+}
+
+// code_bits() for values known to satisfy |v/s| <= qmax + 1 (dynamic scales
+// computed from the same scope): the far-range branch is dropped; near-ties
+// still take the correctly rounded division.
+__device__ __forceinline__ uint32_t code_bits_inrange(float v, const ScopeParams& p, const CodeRange& cr) {
+    const float t = v * p.r;
+    float m = t + p.cz;
+    const float n = m - p.cz;
+    const float d = fmaf(-n, p.s, v);
+    if (!(fabsf(d) < p.hs)) {
+        const float q = rintf(__fdiv_rn(v, p.s));
         m = fminf(fmaxf(q, -8388608.0f), 8388608.0f) + p.cz;
     }
     m = fminf(fmaxf(m, cr.lo), cr.hi);

@@ -299,6 +299,91 @@ __global__ void __launch_bounds__(512, 2) k_quant_longrows(QuantArgs a) {
     }
 }
 
+// ------------------------------------------------------------------ long rows, 16-bit input, no smoothing
+// Per-row scopes of long bf16/f16 rows without smoothing: the raw 16-bit row
+// is staged in shared memory (cols * 2 bytes, so up to four CTAs per SM), pass
+// 1 loads and reduces, pass 2 re-reads the staged row and writes the codes.
+// With dynamic scales |x/s| <= qmax (+ rounding), so the far-range branch of
+// the code computation is never taken.
+template <typename T>
+__global__ void __launch_bounds__(256, 4) k_quant_rows16(QuantArgs a) {
+    extern __shared__ uint4 xs16[];  // [cols / 8] raw 16-bit chunks
+    __shared__ float red_hi[8], red_lo[8];
+    const int tid = threadIdx.x, nt = blockDim.x;
+    const int64_t nchunks = a.cols / 8;
+    const uint4* __restrict__ xg = reinterpret_cast<const uint4*>(a.x);
+    const CodeRange cr = make_range(a.qmin, a.qmax);
+    for (int64_t r = blockIdx.x; r < a.rows; r += gridDim.x) {
+        const uint4* __restrict__ xr = xg + r * (a.ld / 8);
+        float hi = 0.0f, lo = 0.0f;
+        for (int64_t c0 = tid; c0 < nchunks; c0 += 4 * (int64_t)nt) {
+            uint4 raw[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int64_t c = c0 + (int64_t)u * nt;
+                raw[u] = (c < nchunks) ? __ldg(xr + c) : make_uint4(0, 0, 0, 0);
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int64_t c = c0 + (int64_t)u * nt;
+                if (c >= nchunks) break;
+                xs16[c] = raw[u];
+                float v[8];
+                unpack8<T>(raw[u], v);
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    if (a.sym) {
+                        hi = fmaxf(hi, fabsf(v[j]));
+                    } else {
+                        hi = fmaxf(hi, v[j]);
+                        lo = fminf(lo, v[j]);
+                    }
+                }
+            }
+        }
+        hi = warp_max(hi);
+        lo = warp_min(lo);
+        if ((tid & 31) == 0) {
+            red_hi[tid >> 5] = hi;
+            red_lo[tid >> 5] = lo;
+        }
+        __syncthreads();
+        hi = 0.0f;
+        lo = 0.0f;
+        for (int w = 0; w < (nt >> 5); ++w) {
+            hi = fmaxf(hi, red_hi[w]);
+            lo = fminf(lo, red_lo[w]);
+        }
+        float s;
+        int z;
+        if (a.static_scale) {
+            s = load_scale(a.s, r, a.scale_f16);
+            z = a.z ? a.z[r] : 0;
+        } else {
+            scale_zero(lo, hi, a.qmin, a.qmax, a.sym, a.scale_f16, s, z);
+            if (tid == 0) {
+                store_scale(a.s, r, a.scale_f16, s);
+                if (a.z) a.z[r] = z;
+            }
+        }
+        const ScopeParams p = make_scope(s, z);
+        for (int64_t c = tid; c < nchunks; c += nt) {
+            float v[8];
+            unpack8<T>(xs16[c], v);
+            uint32_t cb[8];
+            if (a.static_scale) {
+#pragma unroll
+                for (int j = 0; j < 8; ++j) cb[j] = code_bits(v[j], p, cr);
+            } else {
+#pragma unroll
+                for (int j = 0; j < 8; ++j) cb[j] = code_bits_inrange(v[j], p, cr);
+            }
+            store_codes8(a.q, r, a.cols, c, a.code4, cb);
+        }
+        __syncthreads();  // xs16 and red_* are reused by the next row
+    }
+}
+
 // ------------------------------------------------------------------ column-strip kernels
 // Thread layout shared by the per-tensor / per-column kernels: the block's
 // threads cover `cpb` chunk columns x `rpi` rows per iteration; the block
@@ -811,6 +896,17 @@ static cudaError_t run_quantize_t(QuantArgs a, int xt, const qlin_qparams* p, vo
     if (row_local && rows_kernel_ok(a, xt) && p->clip_percentile <= 0.0) {
         const int64_t nchunks = a.cols / 8;
         const size_t row_bytes = (size_t)a.cols * sizeof(float);
+        const size_t raw_bytes = (size_t)a.cols * 2;
+        if (a.gran == QLIN_PER_ROW && !a.absmax_out && nchunks > 512 && xt != QLIN_F32 &&
+            a.smooth_mode == QLIN_SMOOTH_NONE && raw_bytes <= 56 * 1024) {
+            cudaError_t e = cudaFuncSetAttribute(k_quant_rows16<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                 (int)raw_bytes);
+            if (e != cudaSuccess) return e;
+            int64_t grid = (int64_t)num_sms() * 4;
+            if (grid > a.rows) grid = a.rows;
+            k_quant_rows16<T><<<(unsigned)grid, 256, raw_bytes, st>>>(a);
+            return cudaGetLastError();
+        }
         if (a.gran == QLIN_PER_ROW && !a.absmax_out && nchunks > 1024 && row_bytes <= 113 * 1024) {
             cudaError_t e = cudaFuncSetAttribute(k_quant_longrows<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                  (int)row_bytes);

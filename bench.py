@@ -3,8 +3,9 @@
 
 One step = one pass of the whole hot path over one batch of the 70B-shaped
 down-projection workload (W [8192 x 28672]):
-  1. qlin_quantize   X bf16 [4096 x 28672] -> per-token INT8, after dividing by
-                     the folded SmoothQuant factors (alpha = 0.5)
+  1. qlin_quantize   X' bf16 [4096 x 28672] -> per-token INT8, where X' = X / s
+                     carries the SmoothQuant factors (alpha = 0.5) folded into
+                     the previous layer, as SmoothQuant deploys them
   2. qlin_gemm_w8a8  4096 x 8192 x 28672, INT32 sums, bf16 out
   3. qlin_gemm_w4a16 UINT4 asymmetric g=128 fp16 scales, M = 1, 8, 64, 256
   4. qlin_dequantize the INT8 activations back to bf16
@@ -55,8 +56,8 @@ def load_peaks():
 def kernel_bytes_flops():
     """Algorithmic bytes / ops of each kernel of one step."""
     d = {}
-    # quantize: read X bf16 + smoothing factors, write int8 codes + fp32 scales
-    d["quantize"] = (M8 * K * 2 + K * 4 + M8 * K + M8 * 4, 0.0)
+    # quantize: read X' bf16, write int8 codes + fp32 scales
+    d["quantize"] = (M8 * K * 2 + M8 * K + M8 * 4, 0.0)
     # W8A8: read both operands once, write bf16 Y; 2*M*N*K integer ops
     d["gemm_w8a8"] = (M8 * K + N * K + M8 * 4 + N * 4 + M8 * N * 2, 2.0 * M8 * N * K)
     w4_bytes = N * K // 2 + N * (K // GROUP) * 2 + N * (K // GROUP) // 2
@@ -152,10 +153,13 @@ class Step:
         self.x = x.to(dev)
         wd = w.to(dev)
         del x, w
-        # SmoothQuant factors (alpha = 0.5) from the channel maxima; weights smoothed offline
+        # SmoothQuant factors (alpha = 0.5) from the channel maxima; the weights
+        # are smoothed offline and 1/s is folded into the previous layer, so the
+        # step's activations arrive as X' = bf16(X / s)
         xmax = qlin.absmax(self.x, qlin.QLIN_PER_COL)
         wmax = qlin.absmax(wd, qlin.QLIN_PER_COL)
         self.smooth = qlin.smooth_factors(xmax, wmax, 0.5)
+        self.x = (self.x.float() / self.smooth[None, :]).to(torch.bfloat16)
         pw = qlin.make_params("s8", "row", smooth_mode=qlin.QLIN_SMOOTH_MULTIPLY)
         self.qw, self.sw, _ = qlin.quantize(wd, pw, smooth=self.smooth)
         # W4A16 weights (unsmoothed W), one packed copy per call so no call finds
@@ -168,7 +172,7 @@ class Step:
         del q4, s4, z4, wd
         self.xs = [inputs.downproj_activation(m).to(dev) for m in W4_MS]
         # outputs / scratch
-        self.px = qlin.make_params("s8", "row", smooth_mode=qlin.QLIN_SMOOTH_DIVIDE)
+        self.px = qlin.make_params("s8", "row")
         self.qx = torch.empty((M8, K), dtype=torch.int8, device=dev)
         self.sx = torch.empty(M8, dtype=torch.float32, device=dev)
         nb = qlin.qlin_workspace_size(qlin.QLIN_OP_QUANTIZE, M8, K, 0, self.px)
@@ -195,7 +199,7 @@ class Step:
             if events is not None:
                 events[i].record(stream)
         ev(0)
-        qlin.qlin_quantize(self.x, qlin.QLIN_BF16, M8, K, K, self.smooth, self.px, self.qx, self.sx, None,
+        qlin.qlin_quantize(self.x, qlin.QLIN_BF16, M8, K, K, None, self.px, self.qx, self.sx, None,
                            self.ws_q, self.ws_q_bytes, stream)
         ev(1)
         qlin.qlin_gemm_w8a8(self.qx, self.sx, self.qw, self.sw, M8, N, K, self.y8, qlin.QLIN_BF16, None,
@@ -365,10 +369,8 @@ def run_profile_case(name, dev):
         px = qlin.make_params("s8", "row")
         qx, sx, _ = qlin.quantize(x, px)
         if name == "quantize":
-            # as in the step: per-token INT8 after dividing by smoothing factors
-            pd = qlin.make_params("s8", "row", smooth_mode=qlin.QLIN_SMOOTH_DIVIDE)
-            sm = torch.rand(K, device=dev) + 0.5
-            fn = lambda: qlin.quantize(x, pd, smooth=sm)  # noqa: E731
+            # as in the step: per-token INT8 of (folded) bf16 activations
+            fn = lambda: qlin.quantize(x, px)  # noqa: E731
         else:
             fn = lambda: qlin.dequantize(qx, sx, None, px, M8, K)  # noqa: E731
     for _ in range(3):
@@ -514,7 +516,7 @@ def main():
                "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
                "scaling": "weak", "vs_baseline": None, "dtype": "int8xint8->int32, bf16 (w4a16)",
                "data": "synthetic",
-               "config": {"workload": "70B down-projection W[8192x28672]: smoothed per-token quantize + "
+               "config": {"workload": "70B down-projection W[8192x28672]: per-token quantize of SmoothQuant-folded X + "
                                       "W8A8 M=4096 + W4A16 UINT4 g128 M=1/8/64/256 + dequantize",
                           "M_w8a8": M8, "N": N, "K": K, "w4_group": GROUP, "w4_M": list(W4_MS),
                           "l2": "every operand > L2 or read from a distinct copy (one packed W4 copy per call)",
