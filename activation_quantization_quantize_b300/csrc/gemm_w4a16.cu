@@ -180,8 +180,10 @@ __device__ __forceinline__ void dq_word(uint32_t w, const RowDq& rg, const RowDq
     }
 }
 
+// A pure register-to-register operation (no volatile): the compiler may
+// interleave independent MMAs with the surrounding dequantization.
 __device__ __forceinline__ void mma_bf16_16816(float c[4], const uint32_t a[4], uint32_t b0, uint32_t b1) {
-    asm volatile(
+    asm(
         "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
         "{%0,%1,%2,%3};\n"
         : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
@@ -218,110 +220,364 @@ __device__ __forceinline__ void load_rowdq(const uint8_t* __restrict__ blob, con
 }
 
 // ------------------------------------------------------------------ GEMV (M <= 16)
-constexpr int kPromoteGemv = 8;  // chunks per promoted accumulation chain
-constexpr int GV_U = 4;          // chunks in flight per warp
-// One CTA per 16-row n-tile; its 8 warps split the K chunks, each warp
-// accumulating m16n8k16 tiles (W as the A operand, X^T as B) in registers;
-// the partial tiles are summed in a fixed order in shared memory.
-template <int MT>  // number of n8 tiles of tokens: 1 (M <= 8) or 2 (M <= 16)
+// Two decode kernels share one structure: a CTA covers NT 16-row packed tiles;
+// warp w covers a contiguous 1/8 of the k range for all NT tiles, so each
+// activation load serves NT tiles.  Codes and group constants stream into a
+// per-warp ring in shared memory with cp.async (each lane reads back only what
+// it copied, so no barrier is needed).  m16n8k16 with W as A and X^T as B.  The
+// 8 partial tiles are summed in a fixed order through shared memory, so the
+// result does not depend on timing.  Each accumulation chain covers at most K/8.
+//
+// k_w4_gemv steps one 64-wide chunk at a time and serves any K % 64 == 0;
+// k_w4_gemv2 (below) steps two chunks at a time and serves K % 128 == 0.
+constexpr int GV_D = 6;  // ring depth in chunks
+
+template <int NT>
+constexpr int gemv_smem_bytes() {
+    return 8 * GV_D * NT * (512 + 256);
+}
+
+template <int MT, int NT>  // MT: n8 token tiles (1: M <= 8, 2: M <= 16); NT: 16-row tiles per CTA
 __global__ void __launch_bounds__(256, 2) k_w4_gemv(const __nv_bfloat16* __restrict__ x, const uint8_t* __restrict__ blob,
-                                                 qlin_w4_header h, int64_t M, __nv_bfloat16* __restrict__ y) {
+                                                    qlin_w4_header h, int64_t M, __nv_bfloat16* __restrict__ y) {
+    extern __shared__ __align__(16) uint8_t gv_smem[];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int gq = lane >> 2, t = lane & 3;
-    const int64_t nt = blockIdx.x;
     const int64_t K = h.K, nchunk = K / 64, ngr = K / h.group;
-    const uint4* __restrict__ codes = reinterpret_cast<const uint4*>(blob + h.codes_off) + nt * nchunk * 32 + lane;
-
-    float acc[MT][4];
-#pragma unroll
-    for (int u = 0; u < MT; ++u)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) acc[u][e] = 0.0f;
-
-    float tot[MT][4];
-#pragma unroll
-    for (int u = 0; u < MT; ++u)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) tot[u][e] = 0.0f;
     const int gshift = __ffs(h.group) - 1;  // group is a power of two
-    // Each warp takes chunks warp, warp+8, ...; GV_U chunks per iteration
-    // with every load (codes, scales, activations) issued before any use.
-    int since = 0;
-    for (int64_t kc0 = warp; kc0 < nchunk; kc0 += 8 * GV_U) {
-        uint4 wv[GV_U];
-        DqRaw dr[GV_U];
-        uint4 xb[GV_U][MT][2];
+    const int64_t nt0 = (int64_t)blockIdx.x * NT;
+    const int64_t c_begin = nchunk * warp / 8, c_end = nchunk * (warp + 1) / 8;
+    const bool asym = h.asym != 0;
+
+    // per-lane ring slots: codes [GV_D][NT][32][16 B], group words [GV_D][NT][32][8 B]
+    const uint32_t cring = tc::smem_addr(gv_smem + warp * (GV_D * NT * 512) + lane * 16);
+    const uint32_t mring = tc::smem_addr(gv_smem + 8 * GV_D * NT * 512 + warp * (GV_D * NT * 256) + lane * 8);
+    const uint8_t* gcodes = blob + h.codes_off + lane * 16;
+    const uint8_t* gscales = blob + h.scales_off + gq * 4;
+    const uint8_t* gzeros = blob + h.zeros_off + (gq & 4);
+    const int zshift = 8 * (gq & 3);
+
+    auto issue = [&](int slot, int64_t kc) {
+        if (kc < c_end) {
+            const int64_t gi = (kc * 64 + 16 * t) >> gshift;
 #pragma unroll
-        for (int i = 0; i < GV_U; ++i) {
-            const int64_t kc = kc0 + 8 * i;
-            const bool ok = kc < nchunk;
-            const int64_t kcc = ok ? kc : kc0;
-            wv[i] = __ldg(codes + kcc * 32);
-            const int64_t k0 = kcc * 64 + 16 * t;
-            dr[i] = fetch_dq(blob, h, nt, ngr, k0 >> gshift, gq);
-#pragma unroll
-            for (int u = 0; u < MT; ++u) {
-                const int64_t m = u * 8 + gq;
-                if (m < M && ok) {
-                    const uint4* xp = reinterpret_cast<const uint4*>(x + m * K + k0);
-                    xb[i][u][0] = __ldg(xp);
-                    xb[i][u][1] = __ldg(xp + 1);
-                } else {
-                    xb[i][u][0] = make_uint4(0, 0, 0, 0);
-                    xb[i][u][1] = make_uint4(0, 0, 0, 0);
-                }
+            for (int n = 0; n < NT; ++n) {
+                const int sl = slot * NT + n;
+                cp_async16(cring + sl * 512, gcodes + ((nt0 + n) * nchunk + kc) * 512);
+                cp_async4(mring + sl * 256, gscales + ((nt0 + n) * ngr + gi) * 32);
+                if (asym) cp_async4(mring + sl * 256 + 4, gzeros + ((nt0 + n) * ngr + gi) * 8);
             }
         }
+        cp_async_commit();
+    };
+    auto load_x = [&](uint4 (&xb)[MT][2], int64_t kc) {
+        const int64_t k0 = kc * 64 + 16 * t;
 #pragma unroll
-        for (int i = 0; i < GV_U; ++i) {
-            if (kc0 + 8 * i >= nchunk) break;
+        for (int u = 0; u < MT; ++u) {
+            const int64_t m = u * 8 + gq;
+            if (m < M) {
+                const uint4* xp = reinterpret_cast<const uint4*>(x + m * K + k0);
+                xb[u][0] = __ldg(xp);
+                xb[u][1] = __ldg(xp + 1);
+            } else {
+                xb[u][0] = make_uint4(0, 0, 0, 0);
+                xb[u][1] = make_uint4(0, 0, 0, 0);
+            }
+        }
+    };
+
+    float acc[NT][MT][4];
+#pragma unroll
+    for (int n = 0; n < NT; ++n)
+#pragma unroll
+        for (int u = 0; u < MT; ++u)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) acc[n][u][e] = 0.0f;
+
+#pragma unroll
+    for (int i = 0; i < GV_D - 1; ++i) issue(i, c_begin + i);
+    uint4 xn[MT][2];
+    if (c_begin < c_end) load_x(xn, c_begin);
+
+    int slot = 0;
+    for (int64_t kc = c_begin; kc < c_end; ++kc) {
+        issue(slot == 0 ? GV_D - 1 : slot - 1, kc + GV_D - 1);
+        uint4 xb[MT][2];
+#pragma unroll
+        for (int u = 0; u < MT; ++u) {
+            xb[u][0] = xn[u][0];
+            xb[u][1] = xn[u][1];
+        }
+        if (kc + 1 < c_end) load_x(xn, kc + 1);
+        cp_async_wait<GV_D - 1>();
+#pragma unroll
+        for (int n = 0; n < NT; ++n) {
+            const int sl = slot * NT + n;
+            uint4 cw;
+            uint32_t s2, zw = 0x88u;
+            asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+                         : "=r"(cw.x), "=r"(cw.y), "=r"(cw.z), "=r"(cw.w)
+                         : "r"(cring + sl * 512));
+            if (asym) {
+                asm volatile("ld.shared.v2.u32 {%0,%1}, [%2];" : "=r"(s2), "=r"(zw) : "r"(mring + sl * 256));
+                zw = (zw >> zshift) & 0xFFu;
+            } else {
+                asm volatile("ld.shared.u32 %0, [%1];" : "=r"(s2) : "r"(mring + sl * 256));
+            }
+            DqRaw d;
+            d.s2 = s2;
+            d.zb = zw;
             RowDq rg, rh;
-            build_dq(dr[i], rg, rh);
-            uint32_t wd[4] = {wv[i].x, wv[i].y, wv[i].z, wv[i].w};
+            build_dq(d, rg, rh);
+            const uint32_t wd[4] = {cw.x, cw.y, cw.z, cw.w};
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
                 uint32_t a[4];
                 dq_word(wd[j], rg, rh, a);
 #pragma unroll
                 for (int u = 0; u < MT; ++u) {
-                    const uint32_t* xw = reinterpret_cast<const uint32_t*>(&xb[i][u][0]);
-                    mma_bf16_16816(acc[u], a, xw[2 * j], xw[2 * j + 1]);
+                    const uint32_t* xw = reinterpret_cast<const uint32_t*>(&xb[u][0]);
+                    mma_bf16_16816(acc[n][u], a, xw[2 * j], xw[2 * j + 1]);
                 }
             }
-            if (++since == kPromoteGemv) {
-                since = 0;
+        }
+        slot = slot + 1 == GV_D ? 0 : slot + 1;
+    }
+    cp_async_wait<0>();
+    __syncthreads();
+
+    // acc[n][u][e]: e=0,1 -> (row gq of tile n, tokens u*8 + 2t, +1); e=2,3 -> row gq+8
+    float(*part)[NT * 16][16] = reinterpret_cast<float(*)[NT * 16][16]>(gv_smem);  // [warp][row][token]
 #pragma unroll
-                for (int u = 0; u < MT; ++u)
+    for (int n = 0; n < NT; ++n)
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        tot[u][e] += acc[u][e];
-                        acc[u][e] = 0.0f;
-                    }
-            }
+        for (int u = 0; u < MT; ++u) {
+            part[warp][n * 16 + gq][u * 8 + 2 * t] = acc[n][u][0];
+            part[warp][n * 16 + gq][u * 8 + 2 * t + 1] = acc[n][u][1];
+            part[warp][n * 16 + gq + 8][u * 8 + 2 * t] = acc[n][u][2];
+            part[warp][n * 16 + gq + 8][u * 8 + 2 * t + 1] = acc[n][u][3];
+        }
+    __syncthreads();
+    for (int i = threadIdx.x; i < NT * 16 * 16; i += blockDim.x) {
+        const int row = i >> 4, tok = i & 15;
+        if (tok < M && tok < MT * 8) {
+            float s = 0.0f;
+#pragma unroll
+            for (int w = 0; w < 8; ++w) s += part[w][row][tok];
+            y[(int64_t)tok * h.N + nt0 * 16 + row] = __float2bfloat16_rn(s);
         }
     }
-#pragma unroll
-    for (int u = 0; u < MT; ++u)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) acc[u][e] += tot[u][e];
+}
 
-    // acc[u][e]: e=0,1 -> (row gq, tokens u*8 + 2t, +1); e=2,3 -> (row gq+8, same tokens)
-    __shared__ float part[8][16][16];  // [warp][n row][token]
+// Pair-chunk variant for K % 128 == 0: one loop step covers the chunks
+// (2p, 2p+1) of each of the NT tiles, so groups of >= 128 build their
+// dequantization constants once per step (G128).  Codes and group words stream
+// through a per-warp ring of GV_P steps; activations are read from L2 at the
+// top of the step (rows >= M read row M-1: those token columns are dropped).
+constexpr int GV_P = 3;  // ring depth in chunk pairs
+
+template <int NT>
+constexpr int gemv2_stage_bytes() {
+    return NT * (1024 + 512);
+}
+
+template <int MT, int NT, bool G128>
+__global__ void __launch_bounds__(256, 2) k_w4_gemv2(const __nv_bfloat16* __restrict__ x,
+                                                     const uint8_t* __restrict__ blob, qlin_w4_header h, int64_t M,
+                                                     __nv_bfloat16* __restrict__ y) {
+    extern __shared__ __align__(16) uint8_t gv_smem[];
+    constexpr int SB = gemv2_stage_bytes<NT>();
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int gq = lane >> 2, t = lane & 3;
+    const int64_t K = h.K, npair = K / 128, ngr = K / h.group;
+    const int64_t nt0 = (int64_t)blockIdx.x * NT;
+    const int64_t p_begin = npair * warp / 8, p_end = npair * (warp + 1) / 8;
+    const bool asym = h.asym != 0;
+
+    const uint32_t ring = tc::smem_addr(gv_smem) + warp * (GV_P * SB) + lane * 16;
+    const uint8_t* ringp = gv_smem + warp * (GV_P * SB) + lane * 16;
+    // Global streams of this lane, positioned at pair p_begin.  The group of
+    // lane t in chunk 2p is (128 p + 16 t) / g; in chunk 2p+1 it is 64 / g
+    // groups later (g = 32, 64).  Scale words are 32 B and zero words 8 B per
+    // group of a tile.
+    const int gpp = 128 / h.group;  // groups per pair: 1, 2 or 4
+    const int64_t g0 = (p_begin * 128 + 16 * t) / h.group;
+    const int sb_off = 32 * (gpp >> 1), zb_off = 8 * (gpp >> 1);
+    const uint8_t* gc[NT];
+    const uint8_t* gs[NT];
+    const uint8_t* gz[NT];
+#pragma unroll
+    for (int n = 0; n < NT; ++n) {
+        gc[n] = blob + h.codes_off + ((nt0 + n) * (K / 64) + 2 * p_begin) * 512 + lane * 16;
+        gs[n] = blob + h.scales_off + ((nt0 + n) * ngr + g0) * 32 + gq * 4;
+        gz[n] = blob + h.zeros_off + ((nt0 + n) * ngr + g0) * 8 + (gq & 4);
+    }
+    const int zshift = 8 * (gq & 3);
+    const __nv_bfloat16* xr[MT];
 #pragma unroll
     for (int u = 0; u < MT; ++u) {
-        part[warp][gq][u * 8 + 2 * t] = acc[u][0];
-        part[warp][gq][u * 8 + 2 * t + 1] = acc[u][1];
-        part[warp][gq + 8][u * 8 + 2 * t] = acc[u][2];
-        part[warp][gq + 8][u * 8 + 2 * t + 1] = acc[u][3];
+        const int64_t m = (u * 8 + gq) < M ? (u * 8 + gq) : M - 1;
+        xr[u] = x + m * K + p_begin * 128 + 16 * t;
     }
-    __syncthreads();
-    int row = threadIdx.x >> 4, tok = threadIdx.x & 15;
-    if (tok < M && tok < MT * 8) {
-        float s = 0.0f;
+
+    int64_t p_issue = p_begin;
+    uint32_t s_issue = 0;
+    auto issue = [&]() {
+        if (p_issue < p_end) {
 #pragma unroll
-        for (int w = 0; w < 8; ++w) s += part[w][row][tok];
-        y[(int64_t)tok * h.N + nt * 16 + row] = __float2bfloat16_rn(s);
+            for (int n = 0; n < NT; ++n) {
+                const uint32_t cs = ring + s_issue + n * 1024;
+                const uint32_t ms = ring + s_issue + NT * 1024 + n * 512;
+                cp_async16(cs, gc[n]);
+                cp_async16(cs + 512, gc[n] + 512);
+                gc[n] += 1024;
+                cp_async4(ms, gs[n]);
+                if (asym) cp_async4(ms + 4, gz[n]);
+                if (!G128) {
+                    cp_async4(ms + 8, gs[n] + sb_off);
+                    if (asym) cp_async4(ms + 12, gz[n] + zb_off);
+                }
+                gs[n] += 32 * gpp;
+                gz[n] += 8 * gpp;
+            }
+        }
+        cp_async_commit();
+        ++p_issue;
+        s_issue = (s_issue + SB == GV_P * SB) ? 0 : s_issue + SB;
+    };
+    auto load_x = [&](uint4 (&xb)[MT][2][2]) {
+#pragma unroll
+        for (int u = 0; u < MT; ++u) {
+            const uint4* xp = reinterpret_cast<const uint4*>(xr[u]);
+            xb[u][0][0] = __ldg(xp);
+            xb[u][0][1] = __ldg(xp + 1);
+            xb[u][1][0] = __ldg(xp + 8);
+            xb[u][1][1] = __ldg(xp + 9);
+            xr[u] += 128;
+        }
+    };
+
+    float acc[NT][MT][4];
+#pragma unroll
+    for (int n = 0; n < NT; ++n)
+#pragma unroll
+        for (int u = 0; u < MT; ++u)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) acc[n][u][e] = 0.0f;
+
+    uint32_t s_use = 0;
+    auto step = [&](const uint4 (&xb)[MT][2][2]) {
+        issue();
+        cp_async_wait<GV_P - 1>();
+#pragma unroll
+        for (int n = 0; n < NT; ++n) {
+            const uint8_t* cs = ringp + s_use + n * 1024;
+            const uint4 meta = *reinterpret_cast<const uint4*>(ringp + s_use + NT * 1024 + n * 512);
+            RowDq rg, rh;
+            {
+                DqRaw d;
+                d.s2 = meta.x;
+                d.zb = asym ? (meta.y >> zshift) & 0xFFu : 0x88u;
+                build_dq(d, rg, rh);
+            }
+#pragma unroll
+            for (int c = 0; c < 2; ++c) {
+                if (!G128 && c == 1) {
+                    DqRaw d;
+                    d.s2 = meta.z;
+                    d.zb = asym ? (meta.w >> zshift) & 0xFFu : 0x88u;
+                    build_dq(d, rg, rh);
+                }
+                const uint4 cw = *reinterpret_cast<const uint4*>(cs + c * 512);
+                const uint32_t wd[4] = {cw.x, cw.y, cw.z, cw.w};
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    uint32_t a[4];
+                    dq_word(wd[j], rg, rh, a);
+#pragma unroll
+                    for (int u = 0; u < MT; ++u) {
+                        const uint32_t* xw = reinterpret_cast<const uint32_t*>(&xb[u][c][0]);
+                        mma_bf16_16816(acc[n][u], a, xw[2 * j], xw[2 * j + 1]);
+                    }
+                }
+            }
+        }
+        s_use = (s_use + SB == GV_P * SB) ? 0 : s_use + SB;
+    };
+
+#pragma unroll
+    for (int i = 0; i < GV_P - 1; ++i) issue();
+
+    if (MT == 1) {
+        // activations one step ahead, double-buffered by a 2x unrolled loop
+        uint4 xa[MT][2][2], xc[MT][2][2];
+        if (p_begin < p_end) load_x(xa);
+        for (int64_t p = p_begin; p < p_end; p += 2) {
+            if (p + 1 < p_end) load_x(xc);
+            step(xa);
+            if (p + 1 < p_end) {
+                if (p + 2 < p_end) load_x(xa);
+                step(xc);
+            }
+        }
+    } else {
+        for (int64_t p = p_begin; p < p_end; ++p) {
+            uint4 xb[MT][2][2];
+            load_x(xb);
+            step(xb);
+        }
     }
+    cp_async_wait<0>();
+    __syncthreads();
+
+    float(*part)[NT * 16][16] = reinterpret_cast<float(*)[NT * 16][16]>(gv_smem);  // [warp][row][token]
+#pragma unroll
+    for (int n = 0; n < NT; ++n)
+#pragma unroll
+        for (int u = 0; u < MT; ++u) {
+            part[warp][n * 16 + gq][u * 8 + 2 * t] = acc[n][u][0];
+            part[warp][n * 16 + gq][u * 8 + 2 * t + 1] = acc[n][u][1];
+            part[warp][n * 16 + gq + 8][u * 8 + 2 * t] = acc[n][u][2];
+            part[warp][n * 16 + gq + 8][u * 8 + 2 * t + 1] = acc[n][u][3];
+        }
+    __syncthreads();
+    for (int i = threadIdx.x; i < NT * 16 * 16; i += blockDim.x) {
+        const int row = i >> 4, tok = i & 15;
+        if (tok < M && tok < MT * 8) {
+            float s = 0.0f;
+#pragma unroll
+            for (int w = 0; w < 8; ++w) s += part[w][row][tok];
+            y[(int64_t)tok * h.N + nt0 * 16 + row] = __float2bfloat16_rn(s);
+        }
+    }
+}
+
+template <int MT, int NT, bool G128>
+static cudaError_t launch_gemv2(const __nv_bfloat16* x, const uint8_t* blob, const qlin_w4_header& h, int64_t M,
+                                __nv_bfloat16* y, cudaStream_t st) {
+    constexpr int smem = 8 * GV_P * gemv2_stage_bytes<NT>();
+    static_assert(smem >= 8 * NT * 16 * 16 * 4, "reduction tile must fit in the ring");
+    cudaError_t e = cudaFuncSetAttribute(k_w4_gemv2<MT, NT, G128>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    k_w4_gemv2<MT, NT, G128><<<(unsigned)(h.N / (16 * NT)), 256, smem, st>>>(x, blob, h, M, y);
+    return cudaGetLastError();
+}
+
+template <int MT, int NT>
+static cudaError_t launch_gemv2g(const __nv_bfloat16* x, const uint8_t* blob, const qlin_w4_header& h, int64_t M,
+                                 __nv_bfloat16* y, cudaStream_t st) {
+    return h.group >= 128 ? launch_gemv2<MT, NT, true>(x, blob, h, M, y, st)
+                          : launch_gemv2<MT, NT, false>(x, blob, h, M, y, st);
+}
+
+template <int MT, int NT>
+static cudaError_t launch_gemv(const __nv_bfloat16* x, const uint8_t* blob, const qlin_w4_header& h, int64_t M,
+                               __nv_bfloat16* y, cudaStream_t st) {
+    constexpr int smem = gemv_smem_bytes<NT>();
+    cudaError_t e = cudaFuncSetAttribute(k_w4_gemv<MT, NT>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    k_w4_gemv<MT, NT><<<(unsigned)(h.N / (16 * NT)), 256, smem, st>>>(x, blob, h, M, y);
+    return cudaGetLastError();
 }
 
 // ------------------------------------------------------------------ GEMM (M > 16), mma.sync
@@ -791,15 +1047,19 @@ cudaError_t run_gemm_w4a16(const void* x, const void* packed, const qlin_w4_head
     const __nv_bfloat16* xb = reinterpret_cast<const __nv_bfloat16*>(x);
     const uint8_t* blob = reinterpret_cast<const uint8_t*>(packed);
     __nv_bfloat16* yb = reinterpret_cast<__nv_bfloat16*>(y);
-    unsigned ntiles = (unsigned)(h->N / 16);
-    if (M <= 8) {
-        k_w4_gemv<1><<<ntiles, 256, 0, st>>>(xb, blob, *h, M, yb);
-        return cudaGetLastError();
-    }
     if (M <= 16) {
-        k_w4_gemv<2><<<ntiles, 256, 0, st>>>(xb, blob, *h, M, yb);
-        return cudaGetLastError();
+        // Two 16-row tiles per CTA (one activation load serves both) when that
+        // still leaves at least one CTA per SM.
+        const bool two = (h->N % 32 == 0) && (h->N / 32 >= num_sms());
+        if (h->K % 128 == 0) {
+            if (M <= 8)
+                return two ? launch_gemv2g<1, 2>(xb, blob, *h, M, yb, st) : launch_gemv2g<1, 1>(xb, blob, *h, M, yb, st);
+            return two ? launch_gemv2g<2, 2>(xb, blob, *h, M, yb, st) : launch_gemv2g<2, 1>(xb, blob, *h, M, yb, st);
+        }
+        if (M <= 8) return two ? launch_gemv<1, 2>(xb, blob, *h, M, yb, st) : launch_gemv<1, 1>(xb, blob, *h, M, yb, st);
+        return two ? launch_gemv<2, 2>(xb, blob, *h, M, yb, st) : launch_gemv<2, 1>(xb, blob, *h, M, yb, st);
     }
+    unsigned ntiles = (unsigned)(h->N / 16);
     W4Plan plan = w4_plan(M, h->N, h->K);
     PFN_encodeTiled enc = plan.tc ? encode_tiled_fn() : nullptr;
     if (!plan.tc || !enc || w4_force_mma()) {

@@ -39,14 +39,6 @@ __device__ __forceinline__ uint32_t smem_u32(const void* p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
-// 16-byte cp.async with zero fill when !pred.
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, bool pred) {
-    int n = pred ? 16 : 0;
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(dst), "l"(src), "r"(n));
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;\n" ::"n"(N)); }
 
 // byte offset of (row, 16-byte chunk) inside a [rows x 64 B] tile
 __device__ __forceinline__ uint32_t sw_off(int row, int chunk) {
@@ -91,8 +83,8 @@ __global__ void __launch_bounds__(w8::THREADS) k_w8a8_mma(const int8_t* __restri
             bool pa = kin && ma < M, pb = kin && nb < N;
             const int8_t* ga = qx + (pa ? ma * K + kk : 0);
             const int8_t* gb = qw + (pb ? nb * K + kk : 0);
-            cp_async16(smem_u32(sA + stage * TILE_BYTES + sw_off(row, ch)), ga, pa);
-            cp_async16(smem_u32(sB + stage * TILE_BYTES + sw_off(row, ch)), gb, pb);
+            cp_async16_zfill(smem_u32(sA + stage * TILE_BYTES + sw_off(row, ch)), ga, pa);
+            cp_async16_zfill(smem_u32(sB + stage * TILE_BYTES + sw_off(row, ch)), gb, pb);
         }
     };
 

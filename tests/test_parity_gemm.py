@@ -262,3 +262,36 @@ def test_w4a16_reproducible():
     b = qlin.gemm_w4a16(x, packed, hdr)
     torch.cuda.synchronize()
     assert torch.equal(a, b)
+
+
+@pytest.mark.parametrize("N", [96, 4736])
+@pytest.mark.parametrize("group", [32, 64])
+@pytest.mark.parametrize("M", [1, 5, 16])
+def test_w4a16_gemv_odd_chunk_count(N, group, M):
+    """K = 1088 (17 chunks of 64): the single-chunk decode kernel, with one
+    (N = 96) and two (N = 4736 = 148 x 32) 16-row tiles per CTA."""
+    K = 1088
+    w = torch.from_numpy(inputs.normal((N, K), 0.02, 11)).to(torch.bfloat16).cuda()
+    x = torch.from_numpy(inputs.normal((M, K), 1.0, 12)).to(torch.bfloat16).cuda()
+    p, q, s, z, packed, hdr = w4_prepare(w, group, True)
+    y = qlin.gemm_w4a16(x, packed, hdr)
+    what = w4_oracle_weight(q, s, z, p, N, K, group)
+    yo = oracle.matmul_f64(host_f32(x), what)
+    assert rel_err_out(host_f32(y), yo) < GEMM_REL_TOL
+
+
+@pytest.mark.parametrize("group", [32, 64, 128])
+@pytest.mark.parametrize("M", [1, 8, 9, 16])
+@pytest.mark.parametrize("asym", [False, True])
+def test_w4a16_gemv_two_tiles_per_cta(group, M, asym):
+    """N = 9472 (296 CTAs of two 16-row tiles), K = 2048: decode kernel with
+    both tiles of a CTA in one loop."""
+    N, K = 9472, 2048
+    w = torch.from_numpy(inputs.normal((N, K), 0.02, 13)).to(torch.bfloat16).cuda()
+    x = torch.from_numpy(inputs.normal((M, K), 1.0, 14)).to(torch.bfloat16).cuda()
+    p, q, s, z, packed, hdr = w4_prepare(w, group, asym)
+    y = qlin.gemm_w4a16(x, packed, hdr)
+    rows = np.sort(np.random.default_rng(15).choice(N, 512, replace=False))
+    what = w4_oracle_weight(q, s, z, p, N, K, group, rows=rows)
+    yo = oracle.matmul_f64(host_f32(x), what)
+    assert rel_err_out(host_f32(y)[:, rows], yo) < GEMM_REL_TOL
