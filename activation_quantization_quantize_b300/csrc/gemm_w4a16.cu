@@ -696,19 +696,31 @@ __global__ void __launch_bounds__(256) k_w4_gemm_mma(const __nv_bfloat16* __rest
 namespace w4tc {
 constexpr int BMW = 128;                  // weight rows per CTA (TMEM lanes)
 constexpr int BK = 64;
-constexpr int STAGES = 4;
+constexpr int A_STAGES_MAX = 6;           // converted-weight stages (A operand)
+constexpr int B_STAGES_MAX = 16;          // activation stages (B operand, TMA)
 constexpr int A_BYTES = BMW * BK * 2;     // 16 KB
-constexpr int B_BYTES = 256 * BK * 2;     // 32 KB (up to 256 tokens)
-constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-constexpr int NCONV = 256;                // warps 0-7
-constexpr int EPI_WARP0 = 8;              // warps 8-11
-constexpr int MMA_WARP = 12;
-constexpr int TMA_WARP = 13;
-constexpr int THREADS = 14 * 32;
-constexpr uint32_t TMEM_COLS = 512;       // [0,256) accumulator, [256,512) promoted sums
-constexpr uint32_t EV_DRAIN = 1, EV_FINAL = 2;
-constexpr int RING = 4;                   // register prefetch depth of the packed codes
-constexpr size_t SMEM_BYTES = 1024 + (size_t)STAGES * STAGE_BYTES + 1024;
+constexpr int NCONV_WARPS = 16;           // warps 0-15: warp w converts tile w % 8 of k-blocks of parity w / 8
+constexpr int EPI_WARP0 = 16;             // warps 16-19
+constexpr int MMA_WARP = 20;
+constexpr int TMA_WARP = 21;
+constexpr int THREADS = 22 * 32;
+constexpr uint32_t TMEM_COLS = 512;       // accumulators in [0,256) (two of 128 for ntok <= 128), promoted sums in [256,512)
+constexpr int CRING = 6;                  // cp.async ring depth (own k-blocks) of each converter warp
+constexpr int CR_WARP_BYTES = CRING * (512 + 256);  // codes [CRING][32][16 B] + group words [CRING][32][8 B]
+constexpr int RING_BYTES = NCONV_WARPS * CR_WARP_BYTES;
+constexpr int BAR_BYTES = 512;
+constexpr size_t SMEM_LIMIT = 232448;     // dynamic shared memory per CTA
+// The activation tiles have their own, deeper ring: their TMA latency (L2
+// under the weight stream) would otherwise bound the k-block rate.
+__host__ __device__ constexpr int b_bytes(int ntok) { return ntok * BK * 2; }  // ntok rows of 128 B
+inline int a_stages(int ntok) { return ntok > 128 ? 3 : A_STAGES_MAX; }  // EXP
+inline int b_stages(int ntok) {
+    int s = (int)((SMEM_LIMIT - 1024 - RING_BYTES - BAR_BYTES - (size_t)a_stages(ntok) * A_BYTES) / b_bytes(ntok));
+    return s < B_STAGES_MAX ? s : B_STAGES_MAX;
+}
+inline size_t smem_bytes(int ntok) {
+    return 1024 + (size_t)a_stages(ntok) * A_BYTES + (size_t)b_stages(ntok) * b_bytes(ntok) + RING_BYTES + BAR_BYTES;
+}
 }  // namespace w4tc
 
 struct W4TcArgs {
@@ -718,6 +730,8 @@ struct W4TcArgs {
     int ntok;         // MMA N: tokens per CTA (multiple of 16, <= 256) = TMA box rows
     int nchunk;       // K / 64
     int nsplit;
+    int a_stages;     // converted-weight stages
+    int b_stages;     // activation stages
     int promote;      // k-blocks per accumulation chain (0: no promotion)
     uint32_t idesc;
     float* part;            // [nsplit][M][N] fp32 partials, or nullptr when nsplit == 1
@@ -728,9 +742,13 @@ __global__ void __launch_bounds__(w4tc::THREADS, 1) k_w4_gemm_tc(const __grid_co
     using namespace w4tc;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
-    uint8_t* tiles = smem;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
-    volatile uint32_t* misc = reinterpret_cast<volatile uint32_t*>(bars + 2 * STAGES + 4);
+    const int SA = a.a_stages, SB = a.b_stages;
+    const uint32_t B_BYTES = (uint32_t)b_bytes(a.ntok);
+    uint8_t* tilesA = smem;                                  // [SA][16 KB], 1024-aligned
+    uint8_t* tilesB = smem + (size_t)SA * A_BYTES;           // [SB][ntok * 128 B], 1024-aligned
+    uint8_t* cring = tilesB + (size_t)SB * B_BYTES;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(cring + RING_BYTES);
+    volatile uint32_t* misc = reinterpret_cast<volatile uint32_t*>(bars + 2 * SA + 2 * SB + 5);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 2);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -744,21 +762,38 @@ __global__ void __launch_bounds__(w4tc::THREADS, 1) k_w4_gemm_tc(const __grid_co
     const int nkb = c_end - c_begin;
 
     const uint32_t bar0 = tc::smem_addr(bars);
-    auto full_bar = [&](int s) { return bar0 + 8u * s; };
-    auto empty_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };
-    const uint32_t acc_full = bar0 + 8u * (2 * STAGES);
-    const uint32_t acc_empty = acc_full + 8u;
-    const uint32_t ev_bar = acc_full + 16u;
-    const uint32_t done_bar = acc_full + 24u;
+    auto fullA = [&](int s) { return bar0 + 8u * s; };
+    auto emptyA = [&](int s) { return bar0 + 8u * (SA + s); };
+    auto fullB = [&](int s) { return bar0 + 8u * (2 * SA + s); };
+    auto emptyB = [&](int s) { return bar0 + 8u * (2 * SA + SB + s); };
+    // Accumulation chains: chain c (a.promote k-blocks, the last one shorter)
+    // accumulates into TMEM buffer c % nbuf; the epilogue adds every chain but
+    // the last into the promoted sums and then frees the buffer.  Each buffer
+    // has its own full / empty barrier, so no barrier ever runs two phases
+    // ahead of its waiter.
+    const uint32_t acc_full0 = bar0 + 8u * (2 * SA + 2 * SB);
+    auto acc_full = [&](int b) { return acc_full0 + 8u * b; };
+    auto acc_empty = [&](int b) { return acc_full0 + 16u + 8u * b; };
+    const uint32_t done_bar = acc_full0 + 32u;
+    const bool two_buf = a.ntok <= 128;
+    auto buf_of = [&](int c) { return two_buf ? (c & 1) : 0; };        // c % nbuf
+    auto use_of = [&](int c) { return (uint32_t)(two_buf ? (c >> 1) : c); };  // c / nbuf
+    const int chain_len = a.promote > 0 ? a.promote : (nkb > 0 ? nkb : 1);
+    const int nchains = nkb > 0 ? (nkb + chain_len - 1) / chain_len : 0;
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < STAGES; ++s) {
-            tc::mbar_init(full_bar(s), 8 + 1);  // one arrival per converter warp + the TMA issuer's expect_tx
-            tc::mbar_init(empty_bar(s), 1);
+        for (int s = 0; s < SA; ++s) {
+            tc::mbar_init(fullA(s), 8);  // the 8 warps converting this k-block
+            tc::mbar_init(emptyA(s), 1);
         }
-        tc::mbar_init(acc_full, 1);
-        tc::mbar_init(acc_empty, 4);  // one arrival per epilogue warp
-        tc::mbar_init(ev_bar, 1);
+        for (int s = 0; s < SB; ++s) {
+            tc::mbar_init(fullB(s), 1);  // the TMA issuer's expect_tx
+            tc::mbar_init(emptyB(s), 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            tc::mbar_init(acc_full(b), 1);
+            tc::mbar_init(acc_empty(b), 4);  // one arrival per epilogue warp
+        }
         tc::mbar_init(done_bar, 1);
         misc[2] = 0;
         tc::mbar_init_fence();
@@ -772,40 +807,55 @@ __global__ void __launch_bounds__(w4tc::THREADS, 1) k_w4_gemm_tc(const __grid_co
     tc::tc_fence_after();
     const uint32_t tmem = misc[0];
 
-    if (warp < 8) {
+    if (warp < NCONV_WARPS) {
         // ---------------------------------------------------------- weight dequantization
-        const int ntl = warp;                 // 16-row packed tile within the 128-row block
+        // Warp w converts 16-row tile w % 8 for the k-blocks of parity w / 8, so
+        // two warps share each tile.  Codes and group words of the warp's next
+        // CRING-1 k-blocks stream into its cp.async ring (each lane reads back
+        // only what it copied).
+        const int ntl = warp & 7;             // 16-row packed tile within the 128-row block
+        const int par = warp >> 3;
         const int gq = lane >> 2, t = lane & 3;
         const int64_t nt = nblk * 8 + ntl;
         const int64_t ngr = a.h.K / a.h.group;
-        const uint4* __restrict__ codes =
-            reinterpret_cast<const uint4*>(a.blob + a.h.codes_off) + nt * a.nchunk * 32 + lane;
         const int gshift = __ffs(a.h.group) - 1;  // group is a power of two
-        // register ring: codes and group constants of the next RING k-blocks
-        uint4 ring[RING];
-        DqRaw rdq[RING];
-        auto fetch = [&](int kb, uint4& w, DqRaw& d) {
-            const int64_t kc = c_begin + (kb < nkb ? kb : 0);
-            w = __ldg(codes + kc * 32);
-            d = fetch_dq(a.blob, a.h, nt, ngr, (kc * 64 + 16 * t) >> gshift, gq);
-        };
-#pragma unroll
-        for (int i = 0; i < RING; ++i) fetch(i, ring[i], rdq[i]);
-        const uint32_t r_g = (uint32_t)(ntl * 16 + gq), r_h = r_g + 8;
-        for (int kb = 0; kb < nkb; ++kb) {
-            const int s = kb % STAGES;
-            const uint32_t ph = (uint32_t)(kb / STAGES) & 1u;
-            uint4 wv = ring[0];
-            DqRaw dq = rdq[0];
-#pragma unroll
-            for (int i = 0; i < RING - 1; ++i) {
-                ring[i] = ring[i + 1];
-                rdq[i] = rdq[i + 1];
+        const bool asym = a.h.asym != 0;
+        const int zshift = 8 * (gq & 3);
+        const uint8_t* gcodes = a.blob + a.h.codes_off + (nt * a.nchunk + c_begin) * 512 + lane * 16;
+        const uint8_t* gsc = a.blob + a.h.scales_off + nt * ngr * 32 + gq * 4;
+        const uint8_t* gze = a.blob + a.h.zeros_off + nt * ngr * 8 + (gq & 4);
+        uint8_t* rp = cring + warp * CR_WARP_BYTES;
+        const uint32_t rc = tc::smem_addr(rp) + lane * 16;               // codes [CRING][32][16 B]
+        const uint32_t rm = tc::smem_addr(rp + CRING * 512) + lane * 8;  // words [CRING][32][8 B]
+        int kb_issue = par, slot_issue = 0;
+        auto issue = [&]() {
+            if (kb_issue < nkb) {
+                const int64_t gi = ((int64_t)(c_begin + kb_issue) * 64 + 16 * t) >> gshift;
+                cp_async16(rc + slot_issue * 512, gcodes + (int64_t)kb_issue * 512);
+                cp_async4(rm + slot_issue * 256, gsc + gi * 32);
+                if (asym) cp_async4(rm + slot_issue * 256 + 4, gze + gi * 8);
             }
-            fetch(kb + RING, ring[RING - 1], rdq[RING - 1]);
+            cp_async_commit();
+            kb_issue += 2;
+            slot_issue = slot_issue + 1 == CRING ? 0 : slot_issue + 1;
+        };
+#pragma unroll 1
+        for (int i = 0; i < CRING - 1; ++i) issue();
+        const uint32_t r_g = (uint32_t)(ntl * 16 + gq), r_h = r_g + 8;
+        int s = par < SA ? par : par - SA, slot = 0;
+        uint32_t ph = par < SA ? 0u : 1u;
+        for (int kb = par; kb < nkb; kb += 2) {
+            issue();
+            cp_async_wait<CRING - 1>();
+            const uint4 wv = *reinterpret_cast<const uint4*>(rp + slot * 512 + lane * 16);
+            const uint2 mw = *reinterpret_cast<const uint2*>(rp + CRING * 512 + slot * 256 + lane * 8);
+            slot = slot + 1 == CRING ? 0 : slot + 1;
+            DqRaw dq;
+            dq.s2 = mw.x;
+            dq.zb = asym ? (mw.y >> zshift) & 0xFFu : 0x88u;
             RowDq rg, rh;
             build_dq(dq, rg, rh);
-            uint32_t wd[4] = {wv.x, wv.y, wv.z, wv.w};
+            const uint32_t wd[4] = {wv.x, wv.y, wv.z, wv.w};
             uint32_t og[8], oh[8];
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
@@ -816,76 +866,86 @@ __global__ void __launch_bounds__(w4tc::THREADS, 1) k_w4_gemm_tc(const __grid_co
                 oh[2 * j] = f[1];      // row gq+8
                 oh[2 * j + 1] = f[3];
             }
-            if (!tc::mbar_wait_warp(empty_bar(s), ph ^ 1u, abort_flag)) break;
-            uint8_t* tA = tiles + (size_t)s * STAGE_BYTES;
+            if (!tc::mbar_wait_warp(emptyA(s), ph ^ 1u, abort_flag)) break;
+            uint8_t* tA = tilesA + (size_t)s * A_BYTES;
             *reinterpret_cast<uint4*>(tA + tc::sw128_off(r_g, 2 * t)) = make_uint4(og[0], og[1], og[2], og[3]);
             *reinterpret_cast<uint4*>(tA + tc::sw128_off(r_g, 2 * t + 1)) = make_uint4(og[4], og[5], og[6], og[7]);
             *reinterpret_cast<uint4*>(tA + tc::sw128_off(r_h, 2 * t)) = make_uint4(oh[0], oh[1], oh[2], oh[3]);
             *reinterpret_cast<uint4*>(tA + tc::sw128_off(r_h, 2 * t + 1)) = make_uint4(oh[4], oh[5], oh[6], oh[7]);
             tc::fence_proxy_async_smem();
             __syncwarp();
-            if (lane == 0) tc::mbar_arrive(full_bar(s));
+            if (lane == 0) tc::mbar_arrive(fullA(s));
+            s += 2;
+            if (s >= SA) {
+                s -= SA;
+                ph ^= 1u;
+            }
         }
+        cp_async_wait<0>();
     } else if (warp == TMA_WARP) {
         // ---------------------------------------------------------- activation tiles (TMA)
         if (lane == 0) {
             const uint32_t tx = (uint32_t)a.ntok * BK * 2;
+            int s = 0;
+            uint32_t ph = 0;
             for (int kb = 0; kb < nkb; ++kb) {
-                const int s = kb % STAGES;
-                const uint32_t ph = (uint32_t)(kb / STAGES) & 1u;
-                if (!tc::mbar_wait(empty_bar(s), ph ^ 1u, abort_flag)) break;
-                tc::mbar_arrive_expect_tx(full_bar(s), tx);
-                const uint32_t dstB = tc::smem_addr(tiles + (size_t)s * STAGE_BYTES + A_BYTES);
-                tc::tma_load_2d(dstB, &tmx, (c_begin + kb) * BK, (int)m0, full_bar(s));
+                if (!tc::mbar_wait(emptyB(s), ph ^ 1u, abort_flag)) break;
+                tc::mbar_arrive_expect_tx(fullB(s), tx);
+                const uint32_t dstB = tc::smem_addr(tilesB + (size_t)s * B_BYTES);
+                tc::tma_load_2d(dstB, &tmx, (c_begin + kb) * BK, (int)m0, fullB(s));
+                if (++s == SB) {
+                    s = 0;
+                    ph ^= 1u;
+                }
             }
         }
         __syncwarp();
     } else if (warp == MMA_WARP) {
         // ---------------------------------------------------------- MMA issuer
-        const uint32_t tiles_addr = tc::smem_addr(tiles);
-        bool started = false, ok = true;
-        uint32_t ndrain = 0;
-        int chain = 0;
+        // The warp runs the loop together, so that descriptors and addresses
+        // are warp-uniform values; one elected lane issues the MMAs and
+        // commits (single-thread operations).
+        const uint32_t tA_addr = tc::smem_addr(tilesA), tB_addr = tc::smem_addr(tilesB);
+        int c = 0, in_chain = 0;
+        int s = 0, sb = 0;
+        uint32_t ph = 0, phb = 0;
         for (int kb = 0; kb < nkb; ++kb) {
-            const int s = kb % STAGES;
-            const uint32_t ph = (uint32_t)(kb / STAGES) & 1u;
-            if (!tc::mbar_wait_warp(full_bar(s), ph, abort_flag)) {
-                ok = false;
-                break;
-            }
-            if (started && a.promote > 0 && chain == a.promote) {
-                if (lane == 0) {
-                    misc[1] = EV_DRAIN;
-                    tc::mbar_arrive(ev_bar);
-                    tc::mma_commit(acc_full);
-                }
+            if (!tc::mbar_wait_warp(fullB(sb), phb, abort_flag)) break;
+            if (!tc::mbar_wait_warp(fullA(s), ph, abort_flag)) break;
+            if (in_chain == chain_len) {
+                // chain c is complete: hand its buffer to the epilogue and start
+                // chain c + 1 once that chain's buffer has been drained
+                if (tc::elect_one()) tc::mma_commit(acc_full(buf_of(c)));
                 __syncwarp();
-                if (!tc::mbar_wait_warp(acc_empty, ndrain & 1u, abort_flag)) {
-                    ok = false;
+                ++c;
+                in_chain = 0;
+                if (use_of(c) >= 1 && !tc::mbar_wait_warp(acc_empty(buf_of(c)), (use_of(c) - 1) & 1u, abort_flag))
                     break;
-                }
-                ++ndrain;
-                started = false;
-                chain = 0;
             }
             tc::tc_fence_after();
-            if (lane == 0) {
-                const uint32_t a_addr = tiles_addr + (uint32_t)s * STAGE_BYTES;
-                const uint64_t ad = tc::desc_sw128(a_addr);
-                const uint64_t bd = tc::desc_sw128(a_addr + A_BYTES);
+            const uint64_t ad = tc::desc_sw128(tA_addr + (uint32_t)s * A_BYTES);
+            const uint64_t bd = tc::desc_sw128(tB_addr + (uint32_t)sb * B_BYTES);
+            const uint32_t dacc = tmem + 128u * (uint32_t)buf_of(c);
+            if (tc::elect_one()) {
 #pragma unroll
                 for (int j = 0; j < BK / 16; ++j)
-                    tc::mma_f16(tmem, ad + 2 * j, bd + 2 * j, a.idesc, (started || j > 0) ? 1u : 0u);
-                tc::mma_commit(empty_bar(s));
+                    tc::mma_f16(dacc, ad + 2 * j, bd + 2 * j, a.idesc, (in_chain > 0 || j > 0) ? 1u : 0u);
+                tc::mma_commit(emptyA(s));
+                tc::mma_commit(emptyB(sb));
             }
-            started = true;
-            ++chain;
             __syncwarp();
+            ++in_chain;
+            if (++s == SA) {
+                s = 0;
+                ph ^= 1u;
+            }
+            if (++sb == SB) {
+                sb = 0;
+                phb ^= 1u;
+            }
         }
-        if (lane == 0) {
-            misc[1] = (ok && nkb > 0) ? EV_FINAL : 0u;
-            tc::mbar_arrive(ev_bar);
-            tc::mma_commit(acc_full);
+        if (tc::elect_one()) {
+            if (nkb > 0) tc::mma_commit(acc_full(buf_of(c)));  // the last chain
             tc::mma_commit(done_bar);
         }
         __syncwarp();
@@ -895,45 +955,42 @@ __global__ void __launch_bounds__(w4tc::THREADS, 1) k_w4_gemm_tc(const __grid_co
         const int q = warp & 3;
         const uint32_t lane_base = (uint32_t)(32 * q) << 16;
         const int64_t n = nblk * BMW + 32 * q + lane;  // output channel of this thread
-        const uint32_t t_acc = tmem + lane_base;
         const uint32_t t_sum = tmem + lane_base + 256;
-        uint32_t ndrain = 0;
-        for (uint32_t ev = 0;; ++ev) {
-            if (!tc::mbar_wait_warp(ev_bar, ev & 1u, abort_flag)) break;
-            const uint32_t type = misc[1];
-            if (!tc::mbar_wait_warp(acc_full, ev & 1u, abort_flag)) break;
+        for (int c = 0; c < nchains; ++c) {
+            const int b = buf_of(c);
+            const uint32_t t_acc = tmem + lane_base + 128u * (uint32_t)b;
+            if (!tc::mbar_wait_warp(acc_full(b), use_of(c) & 1u, abort_flag)) break;
             tc::tc_fence_after();
-            if (type == EV_DRAIN) {
-                for (int c = 0; c < a.ntok; c += 32) {
-                    uint32_t v[32], r[32];
-                    tc::tmem_ld32(t_acc + c, v);
-                    if (ndrain) tc::tmem_ld32(t_sum + c, r);
+            if (c + 1 < nchains) {
+                // promote: sums (+)= chain c
+                for (int col = 0; col < a.ntok; col += 16) {
+                    uint32_t v[16], r[16];
+                    tc::tmem_ld16(t_acc + col, v);
+                    if (c > 0) tc::tmem_ld16(t_sum + col, r);
                     tc::tmem_wait_ld();
 #pragma unroll
-                    for (int j = 0; j < 32; ++j)
-                        r[j] = ndrain ? __float_as_uint(__uint_as_float(r[j]) + __uint_as_float(v[j])) : v[j];
-                    tc::tmem_st32(t_sum + c, r);
+                    for (int j = 0; j < 16; ++j)
+                        r[j] = c > 0 ? __float_as_uint(__uint_as_float(r[j]) + __uint_as_float(v[j])) : v[j];
+                    tc::tmem_st16(t_sum + col, r);
                 }
                 tc::tmem_wait_st();
-                ++ndrain;
                 tc::tc_fence_before();
                 __syncwarp();
-                if (lane == 0) tc::mbar_arrive(acc_empty);
+                if (lane == 0) tc::mbar_arrive(acc_empty(b));
                 continue;
             }
-            if (type != EV_FINAL) break;
-            for (int c = 0; c < a.ntok; c += 32) {
+            for (int col = 0; col < a.ntok; col += 16) {
                 __syncwarp();
-                uint32_t v[32], r[32];
-                tc::tmem_ld32(t_acc + c, v);
-                if (ndrain) tc::tmem_ld32(t_sum + c, r);
+                uint32_t v[16], r[16];
+                tc::tmem_ld16(t_acc + col, v);
+                if (c > 0) tc::tmem_ld16(t_sum + col, r);
                 tc::tmem_wait_ld();
 #pragma unroll
-                for (int j = 0; j < 32; ++j) {
+                for (int j = 0; j < 16; ++j) {
                     float f = __uint_as_float(v[j]);
-                    if (ndrain) f += __uint_as_float(r[j]);
-                    const int64_t m = m0 + c + j;
-                    if (c + j < a.ntok && m < a.M) {
+                    if (c > 0) f += __uint_as_float(r[j]);
+                    const int64_t m = m0 + col + j;
+                    if (col + j < a.ntok && m < a.M) {
                         if (a.part)
                             a.part[((int64_t)split * a.M + m) * N + n] = f;
                         else
@@ -941,7 +998,6 @@ __global__ void __launch_bounds__(w4tc::THREADS, 1) k_w4_gemm_tc(const __grid_co
                     }
                 }
             }
-            break;
         }
         if (nkb == 0 && !*abort_flag) {
             // an empty split contributes zeros
@@ -1037,9 +1093,17 @@ static bool w4_force_mma() {
     return e && strcmp(e, "mma") == 0;
 }
 
-static int w4_promote() {
+// k-blocks per accumulation chain.  The tensor cores' fp32 accumulation loses
+// accuracy over long chains; promoting every 8 k-blocks (512 k) keeps the
+// error near 2e-5 of the output scale, every 32 near 2e-4 (8192 x 28672 UINT4).
+// With ntok <= 128 two TMEM accumulators alternate and promotion does not
+// stall the MMAs; above that one accumulator must be drained in place, so the
+// chains are longer.  QLIN_W4A16_PROMOTE overrides (0: one chain); read on
+// every call.
+static int w4_promote(int ntok) {
     const char* e = getenv("QLIN_W4A16_PROMOTE");
-    return e ? atoi(e) : 8;
+    if (e) return atoi(e);
+    return ntok <= 128 ? 8 : 32;
 }
 
 cudaError_t run_gemm_w4a16(const void* x, const void* packed, const qlin_w4_header* h, int64_t M, void* y, void* ws,
@@ -1083,15 +1147,17 @@ cudaError_t run_gemm_w4a16(const void* x, const void* packed, const qlin_w4_head
     a.ntok = plan.ntok;
     a.nchunk = (int)(h->K / 64);
     a.nsplit = plan.nsplit;
-    a.promote = w4_promote();
+    a.a_stages = w4tc::a_stages(plan.ntok);
+    a.b_stages = w4tc::b_stages(plan.ntok);
+    a.promote = w4_promote(plan.ntok);
     a.idesc = tc::idesc_f16(w4tc::BMW, plan.ntok, true);
     a.part = (plan.nsplit > 1) ? reinterpret_cast<float*>(ws) : nullptr;
     a.y = yb;
-    cudaError_t e = cudaFuncSetAttribute(k_w4_gemm_tc, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)w4tc::SMEM_BYTES);
+    const size_t smem = w4tc::smem_bytes(plan.ntok);
+    cudaError_t e = cudaFuncSetAttribute(k_w4_gemm_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     dim3 grid((unsigned)(h->N / w4tc::BMW), (unsigned)plan.nsplit, (unsigned)plan.mtiles);
-    k_w4_gemm_tc<<<grid, w4tc::THREADS, w4tc::SMEM_BYTES, st>>>(tmap, a);
+    k_w4_gemm_tc<<<grid, w4tc::THREADS, smem, st>>>(tmap, a);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     if (plan.nsplit > 1) {
         int64_t MN = M * h->N;

@@ -458,7 +458,7 @@ __global__ void __launch_bounds__(w8tc::THREADS, 1)
             for (int o = 16; o > 0; o >>= 1) mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
             if (started && mx > ROWSUM_LIMIT) {
                 // drain the accumulators into the INT32 tile before adding this k-block
-                if (lane == 0) {
+                if (tc::elect_one()) {
                     misc[1] = EV_DRAIN;
                     tc::mbar_arrive(ev_bar);
                     tc::mma_commit(acc_full);
@@ -477,11 +477,13 @@ __global__ void __launch_bounds__(w8tc::THREADS, 1)
                 for (int i = 0; i < 8; ++i) S[i] += B[i];
             }
             tc::tc_fence_after();
-            if (lane == 0) {
-                const uint32_t a_addr = tiles_addr + (uint32_t)s * STAGE_BYTES;
-                const uint64_t ad0 = tc::desc_sw128(a_addr);
-                const uint64_t ad1 = tc::desc_sw128(a_addr + A_HALF);
-                const uint64_t bd = tc::desc_sw128(a_addr + A_BYTES);
+            // descriptors are computed by the whole warp (warp-uniform values);
+            // one elected lane issues
+            const uint32_t a_addr = tiles_addr + (uint32_t)s * STAGE_BYTES;
+            const uint64_t ad0 = tc::desc_sw128(a_addr);
+            const uint64_t ad1 = tc::desc_sw128(a_addr + A_HALF);
+            const uint64_t bd = tc::desc_sw128(a_addr + A_BYTES);
+            if (tc::elect_one()) {
 #pragma unroll
                 for (int j = 0; j < BK / 16; ++j) {  // 32 bytes of K per MMA
                     const uint32_t acc = (started || j > 0) ? 1u : 0u;
@@ -493,7 +495,7 @@ __global__ void __launch_bounds__(w8tc::THREADS, 1)
             started = true;
             __syncwarp();
         }
-        if (lane == 0) {
+        if (tc::elect_one()) {
             misc[1] = ok ? EV_FINAL : 0u;
             tc::mbar_arrive(ev_bar);
             tc::mma_commit(acc_full);
