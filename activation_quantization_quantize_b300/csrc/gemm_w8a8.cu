@@ -14,9 +14,9 @@
 // magnitude is below 2^24.  The converter warps report, per activation row and
 // k-block of 64, the sum of |code|; the MMA warp accumulates it since the
 // accumulator was last emptied.  Before a k-block could push any partial sum
-// to 2^24 (sum|qx| * 128 >= 2^24), the accumulator is drained into an INT32
-// region of tensor memory and restarted.  The INT32 result is therefore
-// bit-exact for every input.
+// to 2^24 (sum|qx| * 128 >= 2^24), the accumulators are drained into an INT32
+// workspace tile and restarted.  The INT32 result is therefore bit-exact for
+// every input.
 //
 // k_w8a8_mma (warp-level mma.sync s8, native INT32 accumulation) is the
 // legacy-path kernel, kept for comparison (QLIN_W8A8_KERNEL=mma).

@@ -68,6 +68,26 @@ def kernel_bytes_flops():
     return d
 
 
+# DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one W8A8 launch
+# at 4096 x 8192 x 28672, from a one-pass ncu capture, and a digest of the
+# sources that kernel was built from: a changed kernel reports no traffic until
+# it is captured again.
+W8A8_TRAFFIC_BYTES = 726.7e6 + 61.1e6
+W8A8_TRAFFIC_SOURCES = ("activation_quantization_quantize_b300/csrc/gemm_w8a8.cu",
+                        "activation_quantization_quantize_b300/csrc/tc_ptx.cuh",
+                        "activation_quantization_quantize_b300/csrc/qlin_common.cuh")
+W8A8_TRAFFIC_DIGEST = "e92707844e0ba493"
+
+
+def w8a8_traffic_bytes():
+    import hashlib
+    h = hashlib.sha256()
+    for f in W8A8_TRAFFIC_SOURCES:
+        with open(os.path.join(ROOT, f), "rb") as fh:
+            h.update(fh.read())
+    return W8A8_TRAFFIC_BYTES if h.hexdigest()[:16] == W8A8_TRAFFIC_DIGEST else None
+
+
 def roofline_seconds(nbytes, ops, peaks, int8_peak_tflops):
     t_mem = nbytes / (peaks["hbm_gbs"] * 1e9)
     t_ops = ops / (int8_peak_tflops * 1e12) if ops else 0.0
@@ -191,7 +211,11 @@ class Step:
         torch.cuda.synchronize()
 
     names = ["quantize", "gemm_w8a8"] + ["gemm_w4a16_m%d" % m for m in W4_MS] + ["dequantize"]
-    launches_per_step = 7
+    def launches_per_step(self):
+        """Kernels one step launches: quantize (one per-token kernel), W8A8,
+        each W4A16 call (plus the split-K reduction when it needs a
+        workspace), dequantize."""
+        return 1 + 1 + sum(1 + (1 if nb4 > 0 else 0) for _, nb4 in self.ws4) + 1
 
     def run(self, stream, events=None):
         """Enqueue one step; events (len 8) bracket each kernel if given."""
@@ -340,17 +364,18 @@ def run_reference(args, world, rank):
 
 
 # ------------------------------------------------------------------ profiling cases
-PROFILE_CASES = ("w8a8", "w4a16_m1", "w4a16_m256", "quantize", "dequantize")
+PROFILE_CASES = ("w8a8", "w8a8_full", "w4a16_m1", "w4a16_m64", "w4a16_m256", "quantize", "dequantize")
 
 
 def run_profile_case(name, dev):
     """One kernel on a bounded case larger than L2 (for ncu captures): two
     warm-up calls and one measured call, then exit."""
     torch.cuda.set_device(dev)
-    if name == "w8a8":
+    if name.startswith("w8a8"):
         # 2048 x 4096 x 28672: 56 MiB + 112 MiB of int8 codes, quantized from
-        # the down-projection activations (with outlier channels) and weights
-        Mp, Np = 2048, 4096
+        # the down-projection activations (with outlier channels) and weights;
+        # w8a8_full: the step's 4096 x 8192 x 28672 (for one-pass counters)
+        Mp, Np = (M8, N) if name == "w8a8_full" else (2048, 4096)
         p8 = qlin.make_params("s8", "row")
         qx, sx, _ = qlin.quantize(inputs.downproj_activation(Mp, outliers=True).to(dev), p8)
         qw, sw, _ = qlin.quantize(inputs.downproj_weight(N=Np).to(dev), p8)
@@ -456,7 +481,8 @@ def main():
     t8 = per_kernel["gemm_w8a8"]
     w8_tops = bf["gemm_w8a8"][1] / t8 / 1e12
     roofline = {"bound": "tensor", "achieved": w8_tops, "peak": int8_peak, "unit": "TFLOP/s",
-                "frac": w8_tops / int8_peak, "traffic": None,
+                "frac": w8_tops / int8_peak, "traffic": w8a8_traffic_bytes(),
+                "traffic_unit": "bytes per launch (DRAM read + write)",
                 "kernel": "gemm_w8a8 (4096x8192x28672 int8 ops)",
                 "peak_source": "max(bf16 dense %s %.1f, torch._int_mm %s)" % (
                     peaks["source"], peaks["bf16_tflops"], "%.1f" % int8_ref if int8_ref else "n/a")}
@@ -524,7 +550,7 @@ def main():
                "roofline": roofline, "cpu_baseline": cpu,
                "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                        "ms_per_step": e2e_t * 1e3},
-               "gpu_launches": Step.launches_per_step * args.steps,
+               "gpu_launches": step.launches_per_step() * args.steps,
                "clocks": clock_info, "peaks": peaks, "int8_ref_tflops": int8_ref, "detail": detail}
         print(json.dumps(out))
     if world > 1:
