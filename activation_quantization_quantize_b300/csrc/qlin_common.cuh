@@ -206,6 +206,39 @@ __device__ __forceinline__ uint32_t code_bits_inrange(float v, const ScopeParams
     return __float_as_uint(m);
 }
 
+// code_bits() of eight values with one branch.  The fast candidates of all
+// eight are formed in one basic block (so their dependency chains interleave)
+// and the near-tie test is folded into the sign bits of |d| - hs (floating
+// point work instead of eight compares; a NaN result has a clear sign bit and
+// so fails the test).  A chunk holding a near-tie (or, unless kInRange, a value
+// with |v/s| >= 4096) re-derives every element through the scalar function.
+// kClamp = false drops the clamp to [qmin, qmax]; callers use it only for
+// symmetric scopes whose scale came from the scope's own absmax, where
+// |rne(v/s)| <= qmax always holds.  Same results as code_bits() /
+// code_bits_inrange() per element.
+template <bool kInRange, bool kClamp = true>
+__device__ __forceinline__ void code_bits8(const float v[8], const ScopeParams& p, const CodeRange& cr,
+                                           uint32_t cb[8]) {
+    float m[8];
+    uint32_t neg = 0xFFFFFFFFu;  // AND of the sign bits of |d| - hs (and of |t| - 4096)
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        const float t = v[j] * p.r;
+        m[j] = t + p.cz;
+        const float n = m[j] - p.cz;
+        const float d = fmaf(-n, p.s, v[j]);
+        neg &= __float_as_uint(fabsf(d) - p.hs);
+        if (!kInRange) neg &= __float_as_uint(fabsf(t) - 4096.0f);
+    }
+    if (neg & 0x80000000u) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) cb[j] = __float_as_uint(kClamp ? fminf(fmaxf(m[j], cr.lo), cr.hi) : m[j]);
+    } else {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) cb[j] = kInRange ? code_bits_inrange(v[j], p, cr) : code_bits(v[j], p, cr);
+    }
+}
+
 // Pack the low bytes of four code_bits() words: byte i <- a[i].
 __device__ __forceinline__ uint32_t pack_bytes4(uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3) {
     uint32_t lo = __byte_perm(a0, a1, 0x0040);

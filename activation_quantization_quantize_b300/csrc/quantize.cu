@@ -19,6 +19,7 @@
 //   k_dequant       x^ = fl(s (q - z)) rounded to the output type.
 #include "qlin_common.cuh"
 #include "qlin_internal.h"
+#include "tc_ptx.cuh"
 
 namespace qlin {
 
@@ -164,8 +165,7 @@ __global__ void __launch_bounds__(512) k_quant_rows(QuantArgs a) {
                 int64_t c = (int64_t)i * nt + tid;
                 if (c < nchunks) {
                     uint32_t cb[8];
-#pragma unroll
-                    for (int j = 0; j < 8; ++j) cb[j] = code_bits(v[i][j], p, cr);
+                    code_bits8<false>(v[i], p, cr, cb);
                     store_codes8(a.q, r, a.cols, c, a.code4, cb);
                 }
             }
@@ -209,8 +209,7 @@ __global__ void __launch_bounds__(512) k_quant_rows(QuantArgs a) {
                 if (c < nchunks) {
                     const ScopeParams p = make_scope(s, z);
                     uint32_t cb[8];
-#pragma unroll
-                    for (int j = 0; j < 8; ++j) cb[j] = code_bits(v[i][j], p, cr);
+                    code_bits8<false>(v[i], p, cr, cb);
                     store_codes8(a.q, r, a.cols, c, a.code4, cb);
                 }
             }
@@ -291,8 +290,7 @@ __global__ void __launch_bounds__(512, 2) k_quant_longrows(QuantArgs a) {
             float4 u0 = d[0], u1 = d[1];
             float v[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
             uint32_t cb[8];
-#pragma unroll
-            for (int j = 0; j < 8; ++j) cb[j] = code_bits(v[j], p, cr);
+            code_bits8<false>(v, p, cr, cb);
             store_codes8(a.q, r, a.cols, c, a.code4, cb);
         }
         __syncthreads();  // xs and red_* are reused by the next row
@@ -372,15 +370,182 @@ __global__ void __launch_bounds__(256, 4) k_quant_rows16(QuantArgs a) {
             unpack8<T>(xs16[c], v);
             uint32_t cb[8];
             if (a.static_scale) {
-#pragma unroll
-                for (int j = 0; j < 8; ++j) cb[j] = code_bits(v[j], p, cr);
+                code_bits8<false>(v, p, cr, cb);
             } else {
-#pragma unroll
-                for (int j = 0; j < 8; ++j) cb[j] = code_bits_inrange(v[j], p, cr);
+                code_bits8<true>(v, p, cr, cb);
             }
             store_codes8(a.q, r, a.cols, c, a.code4, cb);
         }
         __syncthreads();  // xs16 and red_* are reused by the next row
+    }
+}
+
+// Per-token quantize of 16-bit rows streamed through shared memory by bulk
+// copies.  One persistent CTA per SM keeps `nbuf` (2 or 3) row buffers: while
+// it reduces and quantizes row i from one, the copies of its next rows land in
+// the others, so every SM keeps nbuf - 1 rows in flight.  Same arithmetic as
+// k_quant_rows16.
+constexpr int kBulkThreads = 512;
+
+// Running range of packed 16-bit pairs: |x| max (symmetric) or max and min.
+template <typename T>
+struct PairRange;
+template <>
+struct PairRange<__nv_bfloat16> {
+    __nv_bfloat162 hi = __floats2bfloat162_rn(0.0f, 0.0f), lo = __floats2bfloat162_rn(0.0f, 0.0f);
+    __device__ __forceinline__ void add(const uint4 u, int sym) {
+        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const __nv_bfloat162 v = *reinterpret_cast<const __nv_bfloat162*>(&w[i]);
+            if (sym) {
+                hi = __hmax2(hi, __habs2(v));
+            } else {
+                hi = __hmax2(hi, v);
+                lo = __hmin2(lo, v);
+            }
+        }
+    }
+    __device__ __forceinline__ void result(int sym, float& h, float& l) const {
+        h = fmaxf(__low2float(hi), __high2float(hi));
+        l = sym ? 0.0f : fminf(__low2float(lo), __high2float(lo));
+    }
+};
+template <>
+struct PairRange<__half> {
+    __half2 hi = __floats2half2_rn(0.0f, 0.0f), lo = __floats2half2_rn(0.0f, 0.0f);
+    __device__ __forceinline__ void add(const uint4 u, int sym) {
+        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const __half2 v = *reinterpret_cast<const __half2*>(&w[i]);
+            if (sym) {
+                hi = __hmax2(hi, __habs2(v));
+            } else {
+                hi = __hmax2(hi, v);
+                lo = __hmin2(lo, v);
+            }
+        }
+    }
+    __device__ __forceinline__ void result(int sym, float& h, float& l) const {
+        h = fmaxf(__low2float(hi), __high2float(hi));
+        l = sym ? 0.0f : fminf(__low2float(lo), __high2float(lo));
+    }
+};
+template <>
+struct PairRange<float> {  // not used: binary32 rows take another kernel
+    __device__ __forceinline__ void add(const uint4, int) {}
+    __device__ __forceinline__ void result(int, float& h, float& l) const { h = l = 0.0f; }
+};
+
+template <typename T>
+__global__ void __launch_bounds__(kBulkThreads, 1) k_quant_rows_bulk(QuantArgs a, uint32_t buf_stride, int nbuf) {
+    extern __shared__ __align__(128) uint8_t qb_smem[];
+    __shared__ float red_hi[kBulkThreads / 32], red_lo[kBulkThreads / 32];
+    __shared__ __align__(8) uint64_t bar[3];
+    __shared__ int abort_flag;
+    const int tid = threadIdx.x, nt = blockDim.x;
+    const int64_t nchunks = a.cols / 8;
+    const uint32_t row_bytes = (uint32_t)(a.cols * 2);
+    const CodeRange cr = make_range(a.qmin, a.qmax);
+    const uint32_t bar0 = tc::smem_addr(&bar[0]);
+    const uint32_t buf0 = tc::smem_addr(qb_smem);
+    const uint8_t* xg = reinterpret_cast<const uint8_t*>(a.x);
+    if (tid == 0) {
+        for (int b = 0; b < nbuf; ++b) tc::mbar_init(bar0 + 8u * b, 1);
+        abort_flag = 0;
+        tc::mbar_init_fence();
+    }
+    __syncthreads();
+    // thread 0: start the copy of row r into buffer b (whose earlier readers
+    // have all passed a __syncthreads)
+    auto issue = [&](int64_t r, int b) {
+        tc::fence_proxy_async_smem();
+        tc::mbar_arrive_expect_tx(bar0 + 8u * b, row_bytes);
+        tc::bulk_load(buf0 + (uint32_t)b * buf_stride, xg + r * a.ld * 2, row_bytes, bar0 + 8u * b);
+    };
+    if (tid == 0) {
+        for (int b = 0; b < nbuf; ++b)
+            if (blockIdx.x + (int64_t)b * gridDim.x < a.rows) issue(blockIdx.x + (int64_t)b * gridDim.x, b);
+    }
+    int b = 0;
+    uint32_t ph = 0;
+    for (int64_t r = blockIdx.x; r < a.rows; r += gridDim.x) {
+        const bool ok = tc::mbar_wait(bar0 + 8u * b, ph, &abort_flag);
+        if (!__syncthreads_and(ok)) break;
+        const uint4* xs16 = reinterpret_cast<const uint4*>(qb_smem + (size_t)b * buf_stride);
+        // pass 1: range of the row on packed 16-bit pairs (exact; NaN-ignoring
+        // like fmaxf), four chunks in flight per thread
+        PairRange<T> pr;
+        for (int64_t c0 = tid; c0 < nchunks; c0 += 4 * (int64_t)nt) {
+            uint4 raw[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int64_t c = c0 + (int64_t)u * nt;
+                raw[u] = c < nchunks ? xs16[c] : make_uint4(0, 0, 0, 0);
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u) pr.add(raw[u], a.sym);
+        }
+        float hi, lo;
+        pr.result(a.sym, hi, lo);
+        hi = warp_max(hi);
+        lo = warp_min(lo);
+        if ((tid & 31) == 0) {
+            red_hi[tid >> 5] = hi;
+            red_lo[tid >> 5] = lo;
+        }
+        __syncthreads();
+        hi = 0.0f;
+        lo = 0.0f;
+        for (int w = 0; w < (nt >> 5); ++w) {
+            hi = fmaxf(hi, red_hi[w]);
+            lo = fminf(lo, red_lo[w]);
+        }
+        float s;
+        int z;
+        if (a.static_scale) {
+            s = load_scale(a.s, r, a.scale_f16);
+            z = a.z ? a.z[r] : 0;
+        } else {
+            scale_zero(lo, hi, a.qmin, a.qmax, a.sym, a.scale_f16, s, z);
+            if (tid == 0) {
+                store_scale(a.s, r, a.scale_f16, s);
+                if (a.z) a.z[r] = z;
+            }
+        }
+        const ScopeParams p = make_scope(s, z);
+        // pass 2: codes, four chunks in flight per thread
+        for (int64_t c0 = tid; c0 < nchunks; c0 += 4 * (int64_t)nt) {
+            uint4 raw[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int64_t c = c0 + (int64_t)u * nt;
+                if (c < nchunks) raw[u] = xs16[c];
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int64_t c = c0 + (int64_t)u * nt;
+                if (c >= nchunks) break;
+                float v[8];
+                unpack8<T>(raw[u], v);
+                uint32_t cb[8];
+                if (a.static_scale) {
+                    code_bits8<false>(v, p, cr, cb);
+                } else if (a.sym) {
+                    code_bits8<true, false>(v, p, cr, cb);
+                } else {
+                    code_bits8<true>(v, p, cr, cb);
+                }
+                store_codes8(a.q, r, a.cols, c, a.code4, cb);
+            }
+        }
+        __syncthreads();  // buffer b and red_* are free
+        if (tid == 0 && r + (int64_t)nbuf * gridDim.x < a.rows) issue(r + (int64_t)nbuf * gridDim.x, b);
+        if (++b == nbuf) {
+            b = 0;
+            ph ^= 1u;
+        }
     }
 }
 
@@ -761,6 +926,102 @@ __global__ void k_dequant_vec(DequantArgs d) {
     }
 }
 
+// Row-segment path (per-tensor / per-row / per-group with g % 16 == 0,
+// cols % 16 == 0): a CTA takes one segment of kDqUnroll * 256 chunks of 16
+// codes of one row and issues all of its loads before converting, so each
+// thread keeps kDqUnroll loads in flight; the row and segment come from one
+// division per CTA iteration.  Same arithmetic as k_dequant_vec.
+constexpr int kDqUnroll = 4;
+
+__device__ __forceinline__ void store16_y(const DequantArgs& d, int64_t base, const float (&o)[16]) {
+    if (d.yt == QLIN_F32) {
+        float4* yp = reinterpret_cast<float4*>(reinterpret_cast<float*>(d.y) + base);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) yp[j] = make_float4(o[4 * j], o[4 * j + 1], o[4 * j + 2], o[4 * j + 3]);
+        return;
+    }
+    uint32_t w[8];
+    if (d.yt == QLIN_BF16) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            __nv_bfloat162 p2 = __floats2bfloat162_rn(o[2 * j], o[2 * j + 1]);
+            w[j] = *reinterpret_cast<uint32_t*>(&p2);
+        }
+    } else {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            __half2 p2 = __floats2half2_rn(o[2 * j], o[2 * j + 1]);
+            w[j] = *reinterpret_cast<uint32_t*>(&p2);
+        }
+    }
+    uint4* yp = reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(d.y) + base);
+    yp[0] = make_uint4(w[0], w[1], w[2], w[3]);
+    yp[1] = make_uint4(w[4], w[5], w[6], w[7]);
+}
+
+__global__ void __launch_bounds__(256) k_dequant_rows(DequantArgs d) {
+    const int tid = threadIdx.x, nt = blockDim.x;
+    const int64_t nch = d.cols / 16;
+    const int64_t seg_len = (int64_t)kDqUnroll * nt;
+    const int64_t nseg = (nch + seg_len - 1) / seg_len;
+    const int64_t units = d.rows * nseg;
+    for (int64_t unit = blockIdx.x; unit < units; unit += gridDim.x) {
+        const int64_t r = unit / nseg, c0 = (unit - r * nseg) * seg_len + tid;
+        uint4 raw[kDqUnroll];
+#pragma unroll
+        for (int u = 0; u < kDqUnroll; ++u) {
+            const int64_t c = c0 + (int64_t)u * nt;
+            if (c < nch) {
+                if (d.code4) {
+                    const uint2 w = reinterpret_cast<const uint2*>(reinterpret_cast<const uint8_t*>(d.q) + r * (d.cols / 2))[c];
+                    raw[u] = make_uint4(w.x, w.y, 0, 0);
+                } else {
+                    raw[u] = reinterpret_cast<const uint4*>(reinterpret_cast<const uint8_t*>(d.q) + r * d.cols)[c];
+                }
+            }
+        }
+        const bool row_scope = d.gran != QLIN_PER_GROUP;
+        float s_row = 0.0f;
+        int z_row = 0;
+        if (row_scope) {
+            const int64_t sc = (d.gran == QLIN_PER_TENSOR) ? 0 : r;
+            s_row = load_scale(d.s, sc, d.scale_f16);
+            z_row = d.z ? d.z[sc] : 0;
+        }
+#pragma unroll
+        for (int u = 0; u < kDqUnroll; ++u) {
+            const int64_t c = c0 + (int64_t)u * nt;
+            if (c >= nch) break;
+            float s = s_row;
+            int z = z_row;
+            if (!row_scope) {
+                const int64_t sc = r * (d.cols / d.group) + (c * 16) / d.group;
+                s = load_scale(d.s, sc, d.scale_f16);
+                z = d.z ? d.z[sc] : 0;
+            }
+            int code[16];
+            if (d.code4) {
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    const int v = (((j < 8) ? raw[u].x : raw[u].y) >> (4 * (j & 7))) & 0xF;
+                    code[j] = (d.code_signed && v >= 8) ? v - 16 : v;
+                }
+            } else {
+                const uint32_t wv[4] = {raw[u].x, raw[u].y, raw[u].z, raw[u].w};
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    const uint32_t b = (wv[j >> 2] >> (8 * (j & 3))) & 0xFFu;
+                    code[j] = d.code_signed ? (int)(int8_t)b : (int)b;
+                }
+            }
+            float o[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) o[j] = s * (float)(code[j] - z);
+            store16_y(d, r * d.cols + c * 16, o);
+        }
+    }
+}
+
 __global__ void k_dequant_generic(DequantArgs d) {
     int64_t n = d.rows * d.cols;
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
@@ -897,6 +1158,19 @@ static cudaError_t run_quantize_t(QuantArgs a, int xt, const qlin_qparams* p, vo
         const int64_t nchunks = a.cols / 8;
         const size_t row_bytes = (size_t)a.cols * sizeof(float);
         const size_t raw_bytes = (size_t)a.cols * 2;
+        const uint32_t buf_stride = (uint32_t)((raw_bytes + 127) & ~(size_t)127);
+        if (a.gran == QLIN_PER_ROW && !a.absmax_out && nchunks > 512 && xt != QLIN_F32 &&
+            a.smooth_mode == QLIN_SMOOTH_NONE && 2 * (size_t)buf_stride <= 200 * 1024) {
+            const int nbuf = 3 * (size_t)buf_stride <= 200 * 1024 ? 3 : 2;
+            const int smem = nbuf * (int)buf_stride;
+            cudaError_t e = cudaFuncSetAttribute(k_quant_rows_bulk<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                 smem);
+            if (e != cudaSuccess) return e;
+            int64_t grid = num_sms();
+            if (grid > a.rows) grid = a.rows;
+            k_quant_rows_bulk<T><<<(unsigned)grid, kBulkThreads, smem, st>>>(a, buf_stride, nbuf);
+            return cudaGetLastError();
+        }
         if (a.gran == QLIN_PER_ROW && !a.absmax_out && nchunks > 512 && xt != QLIN_F32 &&
             a.smooth_mode == QLIN_SMOOTH_NONE && raw_bytes <= 56 * 1024) {
             cudaError_t e = cudaFuncSetAttribute(k_quant_rows16<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -1041,7 +1315,12 @@ cudaError_t run_dequantize(const void* q, const void* s, const int32_t* z, const
     int ys = (yt == QLIN_F32) ? 4 : 2;
     bool vec = (cols % 8 == 0) && (p->gran != QLIN_PER_GROUP || p->group % 8 == 0) &&
                ((uintptr_t)q % (d.code4 ? 4 : 8) == 0) && ((uintptr_t)y % (8 * ys) == 0);
-    if (vec)
+    const bool rows16 = (cols % 16 == 0) && (p->gran != QLIN_PER_COL) &&
+                        (p->gran != QLIN_PER_GROUP || p->group % 16 == 0) &&
+                        ((uintptr_t)q % (d.code4 ? 8 : 16) == 0) && ((uintptr_t)y % 16 == 0);
+    if (rows16)
+        k_dequant_rows<<<blocks, 256, 0, st>>>(d);
+    else if (vec)
         k_dequant_vec<<<blocks, 256, 0, st>>>(d);
     else
         k_dequant_generic<<<blocks, 256, 0, st>>>(d);
