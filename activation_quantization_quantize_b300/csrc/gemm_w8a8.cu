@@ -287,6 +287,9 @@ struct W8TcArgs {
     int yt;
     int32_t* acc_out;
     int32_t* drain;   // [M][N] INT32 partial sums, written only when a drain occurs
+    int32_t* part;    // [tail tiles][tail_split][BM][BN] INT32 sums of the split tail tiles
+    int64_t full_tiles;  // CTAs [0, full_tiles) own whole tiles
+    int tail_split;      // K parts of each later tile (one CTA per part)
     int num_m_tiles;
     int bn;           // weight rows per CTA (multiple of 32, <= 256)
     uint32_t idesc;   // MMA instruction descriptor (M = 128, N = bn)
@@ -314,9 +317,27 @@ __global__ void __launch_bounds__(w8tc::THREADS, 1)
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int bn = p.bn;
-    const int64_t m0 = (int64_t)(blockIdx.x % p.num_m_tiles) * BM;
-    const int64_t n0 = (int64_t)(blockIdx.x / p.num_m_tiles) * bn;
-    const int nkb = (int)ceil_div(p.K, BK);
+    // Tile and k-block range of this CTA: whole tiles first; each tile of the
+    // last, partial wave is cut into tail_split K parts whose exact INT32 sums
+    // go to their own slice of `part` (summed by k_w8a8_tail).
+    int64_t tile = blockIdx.x;
+    int kpart = 0, nparts = 1;
+    if (tile >= p.full_tiles) {
+        const int64_t u = tile - p.full_tiles;
+        tile = p.full_tiles + u / p.tail_split;
+        kpart = (int)(u % p.tail_split);
+        nparts = p.tail_split;
+    }
+    const int64_t m0 = (tile % p.num_m_tiles) * BM;
+    const int64_t n0 = (tile / p.num_m_tiles) * bn;
+    const int nkb_all = (int)ceil_div(p.K, BK);
+    const int kb0 = (int)((int64_t)nkb_all * kpart / nparts);
+    const int nkb = (int)((int64_t)nkb_all * (kpart + 1) / nparts) - kb0;
+    const bool split = nparts > 1;
+    // INT32 target of drains (and, for split tiles, of the final sums)
+    int32_t* const dtile = split ? p.part + ((tile - p.full_tiles) * nparts + kpart) * (int64_t)BM * BN
+                                 : p.drain + m0 * p.N + n0;
+    const int64_t dld = split ? BN : p.N;
     const int npieces = (BM + bn) * BK / 16;
 
     const uint32_t bar0 = tc::smem_addr(bars);
@@ -428,8 +449,8 @@ __global__ void __launch_bounds__(w8tc::THREADS, 1)
                 if (!tc::mbar_wait(empty8_bar(s8), ph8 ^ 1u, abort_flag)) break;
                 tc::mbar_arrive_expect_tx(full8_bar(s8), (uint32_t)(BM + bn) * BK);
                 const uint32_t dst = tc::smem_addr(stage8 + (size_t)s8 * STAGE8_BYTES);
-                tc::tma_load_2d(dst, &tm_a, kb * BK, (int)m0, full8_bar(s8));
-                tc::tma_load_2d(dst + A8_BYTES, &tm_b, kb * BK, (int)n0, full8_bar(s8));
+                tc::tma_load_2d(dst, &tm_a, (kb0 + kb) * BK, (int)m0, full8_bar(s8));
+                tc::tma_load_2d(dst + A8_BYTES, &tm_b, (kb0 + kb) * BK, (int)n0, full8_bar(s8));
             }
         }
         __syncwarp();
@@ -529,7 +550,7 @@ __global__ void __launch_bounds__(w8tc::THREADS, 1)
                     for (int j = 0; j < 32; ++j) tot[j] = __float2int_rn(__uint_as_float(a[j]));
                     if (m >= p.M) continue;
                     const int64_t nb = n0 + c;
-                    int32_t* dp = p.drain + m * p.N + nb;
+                    int32_t* dp = dtile + (m - m0) * dld + c;
                     const bool full = (nb + 32 <= p.N) && (p.N % 4 == 0);
                     if (ndrain) {  // add the INT32 sums of earlier drains
                         if (full) {
@@ -546,7 +567,7 @@ __global__ void __launch_bounds__(w8tc::THREADS, 1)
                                 if (nb + j < p.N) tot[j] += dp[j];
                         }
                     }
-                    if (type == EV_DRAIN) {
+                    if (type == EV_DRAIN || split) {  // a split tile's final sums go to its slice
                         if (full) {
 #pragma unroll
                             for (int j = 0; j < 32; j += 4)
@@ -576,9 +597,88 @@ __global__ void __launch_bounds__(w8tc::THREADS, 1)
     }
 }
 
+// y / acc_out of the split tail tiles: the tail_split exact INT32 partial sums
+// of each output are added and go through the same epilogue as whole tiles.
+__global__ void __launch_bounds__(256) k_w8a8_tail(W8TcArgs p, int64_t tail_tiles) {
+    using namespace w8tc;
+    const int64_t nch = p.bn / 32;  // 32-column chunks of a tile row
+    const int64_t total = tail_tiles * BM * nch;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t t = i / (BM * nch), rem = i - t * (BM * nch);
+        const int64_t row = rem / nch, ch = rem - row * nch;
+        const int64_t tile = p.full_tiles + t;
+        const int64_t m = (tile % p.num_m_tiles) * BM + row;
+        const int64_t nb = (tile / p.num_m_tiles) * p.bn + ch * 32;
+        if (m >= p.M || nb >= p.N) continue;
+        int tot[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) tot[j] = 0;
+        for (int k = 0; k < p.tail_split; ++k) {
+            const int4* src = reinterpret_cast<const int4*>(p.part + (t * p.tail_split + k) * (int64_t)BM * BN + row * BN +
+                                                            ch * 32);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const int4 v = src[j];
+                tot[4 * j] += v.x;
+                tot[4 * j + 1] += v.y;
+                tot[4 * j + 2] += v.z;
+                tot[4 * j + 3] += v.w;
+            }
+        }
+        store_row32(tot, m, nb, p.N, p.sx[m], p.sw, p.y, p.yt, p.acc_out);
+    }
+}
+
+// Launch plan of k_w8a8_tc: weight rows per CTA and the split of the last,
+// partial wave of tiles.
+struct W8Plan {
+    int bn;
+    int64_t tiles, full_tiles, tail_tiles;
+    int split;
+};
+
+static W8Plan w8_plan(int64_t M, int64_t N, int64_t K) {
+    using namespace w8tc;
+    W8Plan pl{};
+    // Weight rows per CTA: the fewest waves of tiles over bn in {256, 224,
+    // ..., 128}, larger bn on ties (measured: a CTA's time per k-block does not
+    // shrink with bn, so only the wave count matters).
+    const int sms = num_sms();
+    const int64_t mt = ceil_div(M, BM);
+    pl.bn = BN;
+    int64_t best = INT64_MAX;
+    for (int cand = BN; cand >= 128; cand -= 32) {
+        const int64_t waves = ceil_div(mt * ceil_div(N, cand), sms);
+        if (waves < best) {
+            best = waves;
+            pl.bn = cand;
+        }
+    }
+    pl.tiles = mt * ceil_div(N, pl.bn);
+    // The tiles of the last wave would leave SMs idle: cut each into `split`
+    // K parts (2..4, at least 4 k-blocks each) when that still fits one wave.
+    const int64_t tail = pl.tiles % sms;
+    const int64_t nkb = ceil_div(K, BK);
+    pl.split = 1;
+    if (tail > 0) {
+        int64_t sp = sms / tail;
+        if (sp > 4) sp = 4;
+        while (sp > 1 && nkb < 4 * sp) --sp;
+        pl.split = (int)sp;
+    }
+    pl.tail_tiles = pl.split > 1 ? tail : 0;
+    pl.full_tiles = pl.tiles - pl.tail_tiles;
+    return pl;
+}
+
 // INT32 tile that drains of the exact accumulation add into (touched only
-// when a drain occurs).
-size_t w8a8_ws_bytes(int64_t M, int64_t N, int64_t) { return (size_t)M * N * sizeof(int32_t); }
+// when a drain occurs), then the partial-sum slices of the split tail tiles.
+static size_t w8a8_drain_bytes(int64_t M, int64_t N) { return ((size_t)M * N * sizeof(int32_t) + 15) & ~(size_t)15; }
+
+size_t w8a8_ws_bytes(int64_t M, int64_t N, int64_t K) {
+    const W8Plan pl = w8_plan(M, N, K);
+    return w8a8_drain_bytes(M, N) + (size_t)pl.tail_tiles * pl.split * w8tc::BM * w8tc::BN * sizeof(int32_t);
+}
 
 // 1 selects the legacy mma.sync kernel (read on every call, so a process can
 // compare both kernels).
@@ -605,20 +705,8 @@ cudaError_t run_gemm_w8a8(const int8_t* qx, const float* sx, const int8_t* qw, c
     cuuint64_t gda[2] = {(cuuint64_t)K, (cuuint64_t)M};
     cuuint64_t gdb[2] = {(cuuint64_t)K, (cuuint64_t)N};
     cuuint64_t gstride[1] = {(cuuint64_t)K};
-    // Weight rows per CTA: the fewest waves of tiles over bn in {256, 224,
-    // ..., 128}, larger bn on ties (measured: a CTA's time per k-block does not
-    // shrink with bn, so only the wave count matters).
-    const int sms = num_sms();
-    const int64_t mt = ceil_div(M, BM);
-    int bn = BN;
-    int64_t best = INT64_MAX;
-    for (int cand = BN; cand >= 128; cand -= 32) {
-        const int64_t waves = ceil_div(mt * ceil_div(N, cand), sms);
-        if (waves < best) {
-            best = waves;
-            bn = cand;
-        }
-    }
+    const W8Plan pl = w8_plan(M, N, K);
+    const int bn = pl.bn;
     cuuint32_t boxa[2] = {BK, BM}, boxb[2] = {BK, (cuuint32_t)bn};
     cuuint32_t estride[2] = {1, 1};
     if (enc(&ta, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<int8_t*>(qx), gda, gstride, boxa, estride,
@@ -641,11 +729,18 @@ cudaError_t run_gemm_w8a8(const int8_t* qx, const float* sx, const int8_t* qw, c
     a.yt = yt;
     a.acc_out = acc_out;
     a.drain = reinterpret_cast<int32_t*>(ws);
+    a.part = reinterpret_cast<int32_t*>(reinterpret_cast<uint8_t*>(ws) + w8a8_drain_bytes(M, N));  // 16-byte aligned
+    a.full_tiles = pl.full_tiles;
+    a.tail_split = pl.split;
     a.num_m_tiles = (int)ceil_div(M, BM);
     a.bn = bn;
     a.idesc = tc::idesc_f16(128, bn, false);
-    int64_t tiles = (int64_t)a.num_m_tiles * ceil_div(N, bn);
-    k_w8a8_tc<<<(unsigned)tiles, THREADS, SMEM_BYTES, st>>>(ta, tb, a);
+    const int64_t ctas = pl.full_tiles + pl.tail_tiles * pl.split;
+    k_w8a8_tc<<<(unsigned)ctas, THREADS, SMEM_BYTES, st>>>(ta, tb, a);
+    if ((e = cudaGetLastError()) != cudaSuccess || pl.tail_tiles == 0) return e;
+    const int64_t work = pl.tail_tiles * BM * (bn / 32);
+    const int64_t blocks = ceil_div(work, 256) < (int64_t)num_sms() * 8 ? ceil_div(work, 256) : (int64_t)num_sms() * 8;
+    k_w8a8_tail<<<(unsigned)blocks, 256, 0, st>>>(a, pl.tail_tiles);
     return cudaGetLastError();
 }
 

@@ -212,10 +212,13 @@ class Step:
 
     names = ["quantize", "gemm_w8a8"] + ["gemm_w4a16_m%d" % m for m in W4_MS] + ["dequantize"]
     def launches_per_step(self):
-        """Kernels one step launches: quantize (one per-token kernel), W8A8,
-        each W4A16 call (plus the split-K reduction when it needs a
-        workspace), dequantize."""
-        return 1 + 1 + sum(1 + (1 if nb4 > 0 else 0) for _, nb4 in self.ws4) + 1
+        """Kernels one step launches: quantize (one per-token kernel), W8A8
+        (plus the kernel that finishes K-split tail tiles, present when the
+        workspace holds more than the INT32 drain tile), each W4A16 call (plus
+        the split-K reduction when it needs a workspace), dequantize."""
+        drain_bytes = (M8 * N * 4 + 15) // 16 * 16
+        w8 = 1 + (1 if self.ws8_bytes > drain_bytes else 0)
+        return 1 + w8 + sum(1 + (1 if nb4 > 0 else 0) for _, nb4 in self.ws4) + 1
 
     def run(self, stream, events=None):
         """Enqueue one step; events (len 8) bracket each kernel if given."""

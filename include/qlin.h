@@ -210,7 +210,11 @@ int qlin_pack_w4(const void *q, const void *s_f16, const int32_t *z, int64_t N, 
  *   ws     device workspace of qlin_workspace_size(QLIN_OP_GEMM_W8A8, M, N, K)
  *          bytes, 16-byte aligned: an INT32 [M x N] tile that the kernel only
  *          touches when the exact accumulation must be drained (rows whose
- *          sum of |code| over a run of K would reach 2^24 / 128).
+ *          sum of |code| over a run of K would reach 2^24 / 128), followed by
+ *          the INT32 partial sums of the output tiles whose K range is split
+ *          across CTAs (the tiles of a last, partial wave over the device's
+ *          SMs).  No initialisation is needed.  The size depends on the SM
+ *          count of the current device.
  * Requirements: K % 16 == 0; qx, qw 16-byte aligned.  The exact sums must fit
  * int32 (always true for codes in [-127,127] when K < 133,144).
  */

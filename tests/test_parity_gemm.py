@@ -235,6 +235,27 @@ def test_w8a8_drain_boundary():
     np.testing.assert_array_equal(acc.cpu().numpy(), acco)
 
 
+def test_w8a8_split_tail_tiles():
+    """2560 x 4096 x 1024: 160 tiles of 256 x 256, so the 12 tiles after the
+    first 148 are cut into K parts whose INT32 sums are added by a second
+    kernel; sampled rows of those tiles and of whole tiles stay exact."""
+    M, N, K = 2560, 4096, 1024
+    rng = np.random.default_rng(31)
+    qx = torch.from_numpy(rng.integers(-127, 128, (M, K)).astype(np.int8)).cuda()
+    qw = torch.from_numpy(rng.integers(-127, 128, (N, K)).astype(np.int8)).cuda()
+    sx = torch.from_numpy(rng.uniform(0.001, 0.1, M).astype(np.float32)).cuda()
+    sw = torch.from_numpy(rng.uniform(0.001, 0.1, N).astype(np.float32)).cuda()
+    acc = torch.empty((M, N), dtype=torch.int32, device="cuda")
+    y = qlin.gemm_w8a8(qx, sx, qw, sw, out_dtype=torch.bfloat16, acc_out=acc)
+    rows = np.sort(np.concatenate([rng.choice(np.arange(2048, 2560), 32, replace=False),
+                                   rng.choice(2048, 32, replace=False)]))
+    acco = oracle.w8a8_acc(qx.cpu().numpy()[rows], qw.cpu().numpy())
+    np.testing.assert_array_equal(acc.cpu().numpy()[rows], acco)
+    yo = oracle.w8a8_out(acco, sx.cpu().numpy()[rows], sw.cpu().numpy())
+    assert rel_err_out(host_f32(y)[rows], yo) < GEMM_REL_TOL
+    assert qlin.qlin_device_error() == 0
+
+
 @pytest.mark.parametrize("M", [17, 64, 256])
 def test_w4a16_tensor_core_vs_legacy_kernel(M, monkeypatch):
     """The tcgen05 GEMM and the mma.sync GEMM agree with the oracle on the
