@@ -190,14 +190,14 @@ constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int A8_BYTES = BM * BK;         // 16 KB int8 tile (rows of 64 bytes)
 constexpr int B8_BYTES = BN * BK;         // 16 KB
 constexpr int STAGE8_BYTES = A8_BYTES + B8_BYTES;
-constexpr int NCONV_WARPS = 8;            // warps 0-7: int8 -> fp16 converters
+constexpr int NCONV_WARPS = 16;           // warps 0-15: int8 -> fp16 converters
 constexpr int NCONV = NCONV_WARPS * 32;
-constexpr int EPI_WARP0 = 8;              // warps 8-11: drains + epilogue (one per TMEM lane quarter)
-constexpr int MMA_WARP = 12;              // warp 12: TMEM owner, MMA issuer
-constexpr int TMA_WARP = 13;              // warp 13: int8 tile loads
-constexpr int THREADS = 14 * 32;
+constexpr int EPI_WARP0 = 16;             // warps 16-19: drains + epilogue (one per TMEM lane quarter)
+constexpr int MMA_WARP = 20;              // warp 20: TMEM owner, MMA issuer
+constexpr int TMA_WARP = 21;              // warp 21: int8 tile loads
+constexpr int THREADS = 22 * 32;
 constexpr int PIECES = (BM + BN) * BK / 16;   // max 16-byte int8 pieces per k-block (2048)
-constexpr int PPT = PIECES / NCONV;           // max pieces per converter thread (8)
+constexpr int PPT = PIECES / NCONV;           // max pieces per converter thread (4)
 constexpr int A_PIECES = BM * BK / 16;        // 1024
 constexpr uint32_t ROWSUM_LIMIT = 131071;     // sum|qx| * 128 < 2^24
 constexpr uint32_t TMEM_COLS = 512;           // [0,256): rows 0-127, [256,512): rows 128-255 (fp32)
@@ -225,25 +225,26 @@ __device__ __forceinline__ int abs_sum4(uint32_t w, int acc) {
     return __dp4a((int)neg, 0x01010101, acc);
 }
 
-// Epilogue of 32 consecutive outputs of row m starting at column nb:
+// Epilogue of W (16 or 32) consecutive outputs of row m starting at column nb:
 // acc_out (exact sums) and y = (float(acc) * sx[m]) * sw[n], one rounding.
-__device__ __forceinline__ void store_row32(const int (&tot)[32], int64_t m, int64_t nb, int64_t N, float sxm,
+template <int W>
+__device__ __forceinline__ void store_row(const int (&tot)[W], int64_t m, int64_t nb, int64_t N, float sxm,
                                             const float* __restrict__ sw, void* __restrict__ y, int yt,
                                             int32_t* __restrict__ acc_out) {
-    const bool full = (nb + 32 <= N) && (N % 8 == 0);
+    const bool full = (nb + W <= N) && (N % 8 == 0);
     if (acc_out) {
         int32_t* ap = acc_out + m * N + nb;
         if (full) {
 #pragma unroll
-            for (int j = 0; j < 32; j += 4) *reinterpret_cast<int4*>(ap + j) = make_int4(tot[j], tot[j + 1], tot[j + 2], tot[j + 3]);
+            for (int j = 0; j < W; j += 4) *reinterpret_cast<int4*>(ap + j) = make_int4(tot[j], tot[j + 1], tot[j + 2], tot[j + 3]);
         } else {
-            for (int j = 0; j < 32; ++j)
+            for (int j = 0; j < W; ++j)
                 if (nb + j < N) ap[j] = tot[j];
         }
     }
-    float f[32];
+    float f[W];
 #pragma unroll
-    for (int j = 0; j < 32; ++j) {
+    for (int j = 0; j < W; ++j) {
         float swn = (nb + j < N) ? __ldg(sw + nb + j) : 0.0f;
         f[j] = ((float)tot[j] * sxm) * swn;
     }
@@ -251,7 +252,7 @@ __device__ __forceinline__ void store_row32(const int (&tot)[32], int64_t m, int
         __nv_bfloat16* yp = reinterpret_cast<__nv_bfloat16*>(y) + m * N + nb;
         if (full) {
 #pragma unroll
-            for (int j = 0; j < 32; j += 8) {
+            for (int j = 0; j < W; j += 8) {
                 __nv_bfloat162 p0 = __floats2bfloat162_rn(f[j], f[j + 1]);
                 __nv_bfloat162 p1 = __floats2bfloat162_rn(f[j + 2], f[j + 3]);
                 __nv_bfloat162 p2 = __floats2bfloat162_rn(f[j + 4], f[j + 5]);
@@ -264,16 +265,16 @@ __device__ __forceinline__ void store_row32(const int (&tot)[32], int64_t m, int
                 *reinterpret_cast<uint4*>(yp + j) = u;
             }
         } else {
-            for (int j = 0; j < 32; ++j)
+            for (int j = 0; j < W; ++j)
                 if (nb + j < N) yp[j] = __float2bfloat16_rn(f[j]);
         }
     } else {
         float* yp = reinterpret_cast<float*>(y) + m * N + nb;
         if (full) {
 #pragma unroll
-            for (int j = 0; j < 32; j += 4) *reinterpret_cast<float4*>(yp + j) = make_float4(f[j], f[j + 1], f[j + 2], f[j + 3]);
+            for (int j = 0; j < W; j += 4) *reinterpret_cast<float4*>(yp + j) = make_float4(f[j], f[j + 1], f[j + 2], f[j + 3]);
         } else {
-            for (int j = 0; j < 32; ++j)
+            for (int j = 0; j < W; ++j)
                 if (nb + j < N) yp[j] = f[j];
         }
     }
@@ -434,7 +435,7 @@ __global__ void __launch_bounds__(w8tc::THREADS, 1)
             }
             if (rs_leader) {
 #pragma unroll
-                for (int j = 0; j < A_PIECES / NCONV; ++j) rowsum[s * BM + rs_row + 64 * j] = (uint16_t)rs[j];
+                for (int j = 0; j < A_PIECES / NCONV; ++j) rowsum[s * BM + rs_row + (NCONV / 4) * j] = (uint16_t)rs[j];
             }
             tc::fence_proxy_async_smem();
             __syncwarp();
@@ -540,22 +541,22 @@ __global__ void __launch_bounds__(w8tc::THREADS, 1)
             for (int h = 0; h < 2; ++h) {
                 const int64_t m = m0 + 128 * h + 32 * q + lane;
                 const float sxm = (type == EV_FINAL && m < p.M) ? p.sx[m] : 0.0f;
-                for (int c = 0; c < bn; c += 32) {
+                for (int c = 0; c < bn; c += 16) {
                     __syncwarp();
-                    uint32_t a[32];
-                    tc::tmem_ld32(tmem + lane_base + 256 * h + c, a);
+                    uint32_t a[16];
+                    tc::tmem_ld16(tmem + lane_base + 256 * h + c, a);
                     tc::tmem_wait_ld();
-                    int tot[32];
+                    int tot[16];
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) tot[j] = __float2int_rn(__uint_as_float(a[j]));
+                    for (int j = 0; j < 16; ++j) tot[j] = __float2int_rn(__uint_as_float(a[j]));
                     if (m >= p.M) continue;
                     const int64_t nb = n0 + c;
                     int32_t* dp = dtile + (m - m0) * dld + c;
-                    const bool full = (nb + 32 <= p.N) && (p.N % 4 == 0);
+                    const bool full = (nb + 16 <= p.N) && (p.N % 4 == 0);
                     if (ndrain) {  // add the INT32 sums of earlier drains
                         if (full) {
 #pragma unroll
-                            for (int j = 0; j < 32; j += 4) {
+                            for (int j = 0; j < 16; j += 4) {
                                 int4 v = *reinterpret_cast<const int4*>(dp + j);
                                 tot[j] += v.x;
                                 tot[j + 1] += v.y;
@@ -563,21 +564,21 @@ __global__ void __launch_bounds__(w8tc::THREADS, 1)
                                 tot[j + 3] += v.w;
                             }
                         } else {
-                            for (int j = 0; j < 32; ++j)
+                            for (int j = 0; j < 16; ++j)
                                 if (nb + j < p.N) tot[j] += dp[j];
                         }
                     }
                     if (type == EV_DRAIN || split) {  // a split tile's final sums go to its slice
                         if (full) {
 #pragma unroll
-                            for (int j = 0; j < 32; j += 4)
+                            for (int j = 0; j < 16; j += 4)
                                 *reinterpret_cast<int4*>(dp + j) = make_int4(tot[j], tot[j + 1], tot[j + 2], tot[j + 3]);
                         } else {
-                            for (int j = 0; j < 32; ++j)
+                            for (int j = 0; j < 16; ++j)
                                 if (nb + j < p.N) dp[j] = tot[j];
                         }
                     } else {
-                        store_row32(tot, m, nb, p.N, sxm, p.sw, p.y, p.yt, p.acc_out);
+                        store_row<16>(tot, m, nb, p.N, sxm, p.sw, p.y, p.yt, p.acc_out);
                     }
                 }
             }
@@ -625,7 +626,7 @@ __global__ void __launch_bounds__(256) k_w8a8_tail(W8TcArgs p, int64_t tail_tile
                 tot[4 * j + 3] += v.w;
             }
         }
-        store_row32(tot, m, nb, p.N, p.sx[m], p.sw, p.y, p.yt, p.acc_out);
+        store_row<32>(tot, m, nb, p.N, p.sx[m], p.sw, p.y, p.yt, p.acc_out);
     }
 }
 
