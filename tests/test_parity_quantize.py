@@ -167,6 +167,32 @@ def test_percentile_per_tensor(dtype):
              smooth=sm)
 
 
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+@pytest.mark.parametrize("code", CODES)
+@pytest.mark.parametrize("shape", [(1, 4104), (300, 28672), (517, 8200)])
+def test_quantize_per_token_long_rows(dtype, code, shape):
+    """Per-token scopes of rows longer than 4096 16-bit values: the rows are
+    streamed through shared memory (several rows per CTA when rows > SMs)."""
+    rows, cols = shape
+    xd, xh = make_x(rows, cols, seed=rows + cols, dtype=dtype)
+    run_case(xd, xh, qlin.make_params(code, "row"))
+
+
+@pytest.mark.parametrize("code", ["s8", "u4"])
+def test_quantize_per_token_long_rows_static(code):
+    """Static per-token scales taken from other data (so codes clip) on rows
+    streamed through shared memory."""
+    rows, cols = 200, 12288
+    xd, xh = make_x(rows, cols, seed=91, dtype="bf16")
+    p = qlin.make_params(code, "row")
+    _, so, zo = oracle_quantize(xh * 0.7, p)
+    ps = qlin.make_params(code, "row", static_scale=True)
+    q, _, _ = qlin.quantize(xd, ps, s=torch.from_numpy(so).cuda(),
+                            z=None if zo is None else torch.from_numpy(zo).cuda())
+    qo, _, _ = oracle_quantize(xh, ps, static_s=so, static_z=zo)
+    np.testing.assert_array_equal(codes_to_int(q, ps, rows, cols), qo)
+
+
 @pytest.mark.parametrize("code", CODES)
 @pytest.mark.parametrize("gran,group", [("tensor", 0), ("row", 0), ("col", 0), ("group", 32), ("group", 128)])
 @pytest.mark.parametrize("out", [torch.bfloat16, torch.float32, torch.float16])
