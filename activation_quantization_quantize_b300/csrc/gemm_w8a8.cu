@@ -600,25 +600,26 @@ __global__ void __launch_bounds__(w8tc::THREADS, 1)
 
 // y / acc_out of the split tail tiles: the tail_split exact INT32 partial sums
 // of each output are added and go through the same epilogue as whole tiles.
-__global__ void __launch_bounds__(256) k_w8a8_tail(W8TcArgs p, int64_t tail_tiles) {
+__global__ void __launch_bounds__(256) k_w8a8_tail(W8TcArgs p, int tail_tiles) {
     using namespace w8tc;
-    const int64_t nch = p.bn / 32;  // 32-column chunks of a tile row
-    const int64_t total = tail_tiles * BM * nch;
-    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
-        const int64_t t = i / (BM * nch), rem = i - t * (BM * nch);
-        const int64_t row = rem / nch, ch = rem - row * nch;
+    const int nch = p.bn / 16;  // 16-column chunks of a tile row
+    const int per_tile = BM * nch;
+    const int total = tail_tiles * per_tile;
+    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < total; i += gridDim.x * blockDim.x) {
+        const int t = i / per_tile, rem = i - t * per_tile;
+        const int row = rem / nch, ch = rem - row * nch;
         const int64_t tile = p.full_tiles + t;
         const int64_t m = (tile % p.num_m_tiles) * BM + row;
-        const int64_t nb = (tile / p.num_m_tiles) * p.bn + ch * 32;
+        const int64_t nb = (tile / p.num_m_tiles) * p.bn + ch * 16;
         if (m >= p.M || nb >= p.N) continue;
-        int tot[32];
+        int tot[16];
 #pragma unroll
-        for (int j = 0; j < 32; ++j) tot[j] = 0;
+        for (int j = 0; j < 16; ++j) tot[j] = 0;
         for (int k = 0; k < p.tail_split; ++k) {
-            const int4* src = reinterpret_cast<const int4*>(p.part + (t * p.tail_split + k) * (int64_t)BM * BN + row * BN +
-                                                            ch * 32);
+            const int4* src = reinterpret_cast<const int4*>(p.part + ((int64_t)t * p.tail_split + k) * (int64_t)BM * BN +
+                                                            row * BN + ch * 16);
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
+            for (int j = 0; j < 4; ++j) {
                 const int4 v = src[j];
                 tot[4 * j] += v.x;
                 tot[4 * j + 1] += v.y;
@@ -626,7 +627,7 @@ __global__ void __launch_bounds__(256) k_w8a8_tail(W8TcArgs p, int64_t tail_tile
                 tot[4 * j + 3] += v.w;
             }
         }
-        store_row<32>(tot, m, nb, p.N, p.sx[m], p.sw, p.y, p.yt, p.acc_out);
+        store_row<16>(tot, m, nb, p.N, p.sx[m], p.sw, p.y, p.yt, p.acc_out);
     }
 }
 
@@ -739,9 +740,8 @@ cudaError_t run_gemm_w8a8(const int8_t* qx, const float* sx, const int8_t* qw, c
     const int64_t ctas = pl.full_tiles + pl.tail_tiles * pl.split;
     k_w8a8_tc<<<(unsigned)ctas, THREADS, SMEM_BYTES, st>>>(ta, tb, a);
     if ((e = cudaGetLastError()) != cudaSuccess || pl.tail_tiles == 0) return e;
-    const int64_t work = pl.tail_tiles * BM * (bn / 32);
-    const int64_t blocks = ceil_div(work, 256) < (int64_t)num_sms() * 8 ? ceil_div(work, 256) : (int64_t)num_sms() * 8;
-    k_w8a8_tail<<<(unsigned)blocks, 256, 0, st>>>(a, pl.tail_tiles);
+    const int64_t work = pl.tail_tiles * BM * (bn / 16);  // < 2^31: tail tiles < SMs
+    k_w8a8_tail<<<(unsigned)ceil_div(work, 256), 256, 0, st>>>(a, (int)pl.tail_tiles);
     return cudaGetLastError();
 }
 
