@@ -216,13 +216,14 @@ __device__ __forceinline__ void s8x4_to_f16(uint32_t w, uint32_t& lo, uint32_t& 
     asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(hi) : "r"(b), "r"(0x64806480u));
 }
 
-// acc + sum of |b| over the four int8 codes b of w, exactly: a negative byte b
-// becomes ~b = |b| - 1 (non-negative as a signed byte), and the count of
-// negative bytes is added back.
+// acc + sum of |b| over the four signed int8 codes b of w, exactly: prmt in
+// sign-replicate mode makes 0xFF in every negative byte and 0x00 elsewhere;
+// with 0x01 or-ed in, each byte is the sign (+1 / -1) of its code, and the
+// signed dot product of codes and signs is the sum of |b| (|-128| = 128).
 __device__ __forceinline__ int abs_sum4(uint32_t w, int acc) {
-    const uint32_t neg = (w >> 7) & 0x01010101u;  // 1 in every negative byte
-    acc = __dp4a((int)(w ^ (neg * 0xFFu)), 0x01010101, acc);
-    return __dp4a((int)neg, 0x01010101, acc);
+    uint32_t m;
+    asm("prmt.b32 %0, %1, 0, 0xBA98;" : "=r"(m) : "r"(w));
+    return __dp4a((int)w, (int)(m | 0x01010101u), acc);
 }
 
 // Epilogue of W (16 or 32) consecutive outputs of row m starting at column nb:
