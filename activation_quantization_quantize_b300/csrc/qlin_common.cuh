@@ -206,29 +206,75 @@ __device__ __forceinline__ uint32_t code_bits_inrange(float v, const ScopeParams
     return __float_as_uint(m);
 }
 
+// Packed binary32 pairs (sm_100 family): each lane of the pair is an IEEE
+// operation rounded to nearest, exactly as its scalar counterpart.
+__device__ __forceinline__ float2 f2_fma(float2 a, float2 b, float2 c) {
+    float2 d;
+    asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\t"
+        "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\tmov.b64 rc, {%6, %7};\n\t"
+        "fma.rn.f32x2 rd, ra, rb, rc;\n\t"
+        "mov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+    return d;
+}
+__device__ __forceinline__ float2 f2_add(float2 a, float2 b) {
+    float2 d;
+    asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
+        "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+        "add.rn.f32x2 rd, ra, rb;\n\t"
+        "mov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+    return d;
+}
+__device__ __forceinline__ float2 f2_mul(float2 a, float2 b) {
+    float2 d;
+    asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
+        "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+        "mul.rn.f32x2 rd, ra, rb;\n\t"
+        "mov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+    return d;
+}
+
 // code_bits() of eight values with one branch.  The fast candidates of all
-// eight are formed in one basic block (so their dependency chains interleave)
-// and the near-tie test is folded into the sign bits of |d| - hs (floating
-// point work instead of eight compares; a NaN result has a clear sign bit and
-// so fails the test).  A chunk holding a near-tie (or, unless kInRange, a value
-// with |v/s| >= 4096) re-derives every element through the scalar function.
-// kClamp = false drops the clamp to [qmin, qmax]; callers use it only for
-// symmetric scopes whose scale came from the scope's own absmax, where
-// |rne(v/s)| <= qmax always holds.  Same results as code_bits() /
-// code_bits_inrange() per element.
+// eight are formed in one basic block on packed pairs, and the near-tie test
+// |d| < hs becomes the sign of d*d - hs*hs (one fused multiply-add per pair;
+// its rounding can only move the outcome for |d| within an ulp of hs, where
+// either path gives the right code, since hs keeps a 2^-11 * s margin from
+// the tie; a NaN has a clear sign bit and fails the test).  Likewise
+// |t| < 4096 is tested as t*t - 2^24 < 0 unless kInRange.  A chunk that fails
+// re-derives every element through the scalar function.  kClamp = false drops
+// the clamp to [qmin, qmax]; callers use it only for symmetric scopes whose
+// scale came from the scope's own absmax, where |rne(v/s)| <= qmax always
+// holds.  Same results as code_bits() / code_bits_inrange() per element.
 template <bool kInRange, bool kClamp = true>
 __device__ __forceinline__ void code_bits8(const float v[8], const ScopeParams& p, const CodeRange& cr,
                                            uint32_t cb[8]) {
     float m[8];
-    uint32_t neg = 0xFFFFFFFFu;  // AND of the sign bits of |d| - hs (and of |t| - 4096)
+    uint32_t neg = 0xFFFFFFFFu;  // AND of the sign bits of the tests
+    const float2 r2 = make_float2(p.r, p.r), cz2 = make_float2(p.cz, p.cz), ncz2 = make_float2(-p.cz, -p.cz);
+    const float2 ns2 = make_float2(-p.s, -p.s);
+    const float hs_sq = p.hs * p.hs;
+    const float2 nhs2 = make_float2(-hs_sq, -hs_sq);
+    const float2 nlim2 = make_float2(-16777216.0f, -16777216.0f);
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-        const float t = v[j] * p.r;
-        m[j] = t + p.cz;
-        const float n = m[j] - p.cz;
-        const float d = fmaf(-n, p.s, v[j]);
-        neg &= __float_as_uint(fabsf(d) - p.hs);
-        if (!kInRange) neg &= __float_as_uint(fabsf(t) - 4096.0f);
+    for (int j = 0; j < 4; ++j) {
+        const float2 v2 = make_float2(v[2 * j], v[2 * j + 1]);
+        const float2 t2 = f2_mul(v2, r2);
+        const float2 m2 = f2_add(t2, cz2);      // rne(t) + 1.5*2^23 + z
+        const float2 n2 = f2_add(m2, ncz2);     // rne(t), exact
+        const float2 d2 = f2_fma(n2, ns2, v2);  // v - n*s, exact
+        const float2 e2 = f2_fma(d2, d2, nhs2);
+        neg &= __float_as_uint(e2.x) & __float_as_uint(e2.y);
+        if (!kInRange) {
+            const float2 g2 = f2_fma(t2, t2, nlim2);
+            neg &= __float_as_uint(g2.x) & __float_as_uint(g2.y);
+        }
+        m[2 * j] = m2.x;
+        m[2 * j + 1] = m2.y;
     }
     if (neg & 0x80000000u) {
 #pragma unroll

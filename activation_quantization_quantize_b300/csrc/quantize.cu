@@ -445,7 +445,7 @@ __global__ void __launch_bounds__(kBulkThreads, 1) k_quant_rows_bulk(QuantArgs a
     __shared__ __align__(8) uint64_t bar[3];
     __shared__ int abort_flag;
     const int tid = threadIdx.x, nt = blockDim.x;
-    const int64_t nchunks = a.cols / 8;
+    const int nchunks = (int)(a.cols / 8);  // <= 4096
     const uint32_t row_bytes = (uint32_t)(a.cols * 2);
     const CodeRange cr = make_range(a.qmin, a.qmax);
     const uint32_t bar0 = tc::smem_addr(&bar[0]);
@@ -477,11 +477,11 @@ __global__ void __launch_bounds__(kBulkThreads, 1) k_quant_rows_bulk(QuantArgs a
         // pass 1: range of the row on packed 16-bit pairs (exact; NaN-ignoring
         // like fmaxf), four chunks in flight per thread
         PairRange<T> pr;
-        for (int64_t c0 = tid; c0 < nchunks; c0 += 4 * (int64_t)nt) {
+        for (int c0 = tid; c0 < nchunks; c0 += 4 * nt) {
             uint4 raw[4];
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
-                const int64_t c = c0 + (int64_t)u * nt;
+                const int c = c0 + u * nt;
                 raw[u] = c < nchunks ? xs16[c] : make_uint4(0, 0, 0, 0);
             }
 #pragma unroll
@@ -516,16 +516,16 @@ __global__ void __launch_bounds__(kBulkThreads, 1) k_quant_rows_bulk(QuantArgs a
         }
         const ScopeParams p = make_scope(s, z);
         // pass 2: codes, four chunks in flight per thread
-        for (int64_t c0 = tid; c0 < nchunks; c0 += 4 * (int64_t)nt) {
+        for (int c0 = tid; c0 < nchunks; c0 += 4 * nt) {
             uint4 raw[4];
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
-                const int64_t c = c0 + (int64_t)u * nt;
+                const int c = c0 + u * nt;
                 if (c < nchunks) raw[u] = xs16[c];
             }
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
-                const int64_t c = c0 + (int64_t)u * nt;
+                const int c = c0 + u * nt;
                 if (c >= nchunks) break;
                 float v[8];
                 unpack8<T>(raw[u], v);
@@ -545,6 +545,100 @@ __global__ void __launch_bounds__(kBulkThreads, 1) k_quant_rows_bulk(QuantArgs a
         if (++b == nbuf) {
             b = 0;
             ph ^= 1u;
+        }
+    }
+}
+
+// Row-local scopes (per-row, or per-group with g/8 a power of two <= 32) of
+// 16-bit rows of at most 32 * NC eight-value chunks: one warp per row, the row
+// held in registers (lane l holds chunks l, l + 32, ...), every reduction a
+// register shuffle.  Many warps per SM keep many rows in flight.  Same
+// arithmetic as k_quant_rows16 / k_quant_rows_bulk.
+template <typename T, int NC>
+__global__ void __launch_bounds__(256) k_quant_warprows(QuantArgs a) {
+    const int lane = threadIdx.x & 31;
+    const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+    const int64_t nchunks = a.cols / 8;
+    const bool per_row = a.gran == QLIN_PER_ROW;
+    const int gl = per_row ? 32 : a.group / 8;  // lanes (chunks) per scope within one i
+    const int64_t ngr = per_row ? 1 : a.cols / a.group;
+    const CodeRange cr = make_range(a.qmin, a.qmax);
+    const uint4* __restrict__ xg = reinterpret_cast<const uint4*>(a.x);
+    for (int64_t r = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; r < a.rows; r += nwarps) {
+        const uint4* __restrict__ xr = xg + r * (a.ld / 8);
+        uint4 raw[NC];
+#pragma unroll
+        for (int i = 0; i < NC; ++i) {
+            const int64_t c = lane + 32 * i;
+            raw[i] = c < nchunks ? __ldg(xr + c) : make_uint4(0, 0, 0, 0);
+        }
+        auto quant_chunk = [&](const uint4& u, int64_t c, const ScopeParams& sp) {
+            float v[8];
+            unpack8<T>(u, v);
+            uint32_t cb[8];
+            if (a.static_scale) {
+                code_bits8<false>(v, sp, cr, cb);
+            } else if (a.sym) {
+                code_bits8<true, false>(v, sp, cr, cb);
+            } else {
+                code_bits8<true>(v, sp, cr, cb);
+            }
+            store_codes8(a.q, r, a.cols, c, a.code4, cb);
+        };
+        if (per_row) {
+            float s;
+            int z;
+            if (a.static_scale) {
+                s = load_scale(a.s, r, a.scale_f16);
+                z = a.z ? a.z[r] : 0;
+            } else {
+                PairRange<T> pr;
+#pragma unroll
+                for (int i = 0; i < NC; ++i) pr.add(raw[i], a.sym);  // zero padding: the range includes 0
+                float hi, lo;
+                pr.result(a.sym, hi, lo);
+                hi = warp_max(hi);
+                lo = warp_min(lo);
+                scale_zero(lo, hi, a.qmin, a.qmax, a.sym, a.scale_f16, s, z);
+                if (lane == 0) {
+                    store_scale(a.s, r, a.scale_f16, s);
+                    if (a.z) a.z[r] = z;
+                }
+            }
+            const ScopeParams sp = make_scope(s, z);
+#pragma unroll
+            for (int i = 0; i < NC; ++i) {
+                const int64_t c = lane + 32 * i;
+                if (c < nchunks) quant_chunk(raw[i], c, sp);
+            }
+        } else {
+#pragma unroll
+            for (int i = 0; i < NC; ++i) {
+                const int64_t c = lane + 32 * i;
+                if (32 * i >= nchunks) break;  // warp-uniform
+                const int64_t sc = r * ngr + c / gl;
+                float s;
+                int z;
+                if (a.static_scale) {
+                    s = c < nchunks ? load_scale(a.s, sc, a.scale_f16) : 1.0f;
+                    z = (a.z && c < nchunks) ? a.z[sc] : 0;
+                } else {
+                    PairRange<T> pr;
+                    pr.add(raw[i], a.sym);
+                    float hi, lo;
+                    pr.result(a.sym, hi, lo);
+                    for (int o = 1; o < gl; o <<= 1) {
+                        hi = fmaxf(hi, __shfl_xor_sync(0xffffffffu, hi, o));
+                        lo = fminf(lo, __shfl_xor_sync(0xffffffffu, lo, o));
+                    }
+                    scale_zero(lo, hi, a.qmin, a.qmax, a.sym, a.scale_f16, s, z);
+                    if (c < nchunks && (lane & (gl - 1)) == 0) {
+                        store_scale(a.s, sc, a.scale_f16, s);
+                        if (a.z) a.z[sc] = z;
+                    }
+                }
+                if (c < nchunks) quant_chunk(raw[i], c, make_scope(s, z));
+            }
         }
     }
 }
@@ -1159,6 +1253,19 @@ static cudaError_t run_quantize_t(QuantArgs a, int xt, const qlin_qparams* p, vo
         const size_t row_bytes = (size_t)a.cols * sizeof(float);
         const size_t raw_bytes = (size_t)a.cols * 2;
         const uint32_t buf_stride = (uint32_t)((raw_bytes + 127) & ~(size_t)127);
+        if (a.gran == QLIN_PER_ROW && !a.absmax_out && xt != QLIN_F32 && a.smooth_mode == QLIN_SMOOTH_NONE &&
+            nchunks <= 512) {
+            int64_t grid = ceil_div(a.rows, 8);
+            const int64_t cap = (int64_t)num_sms() * 8;
+            if (grid > cap) grid = cap;
+            if (nchunks <= 128)
+                k_quant_warprows<T, 4><<<(unsigned)grid, 256, 0, st>>>(a);
+            else if (nchunks <= 256)
+                k_quant_warprows<T, 8><<<(unsigned)grid, 256, 0, st>>>(a);
+            else
+                k_quant_warprows<T, 16><<<(unsigned)grid, 256, 0, st>>>(a);
+            return cudaGetLastError();
+        }
         if (a.gran == QLIN_PER_ROW && !a.absmax_out && nchunks > 512 && xt != QLIN_F32 &&
             a.smooth_mode == QLIN_SMOOTH_NONE && 2 * (size_t)buf_stride <= 200 * 1024) {
             const int nbuf = 3 * (size_t)buf_stride <= 200 * 1024 ? 3 : 2;

@@ -263,6 +263,99 @@ def measure_int8_reference_peak(dev):
         return None
 
 
+# ------------------------------------------------------------------ the other configurations
+def _time_calls(fn, n_iter=20, n_warm=3):
+    """Mean seconds per call of fn(i) over n_iter calls (CUDA events)."""
+    for i in range(n_warm):
+        fn(i)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for i in range(n_iter):
+        fn(i)
+    e1.record()
+    e1.synchronize()
+    return e0.elapsed_time(e1) / 1e3 / n_iter
+
+
+def measure_other_configs(dev, peaks, int8_peak):
+    """Time the remaining workloads outside the step: W4A16 decode 4096 x 4096
+    (M = 1, 4, 16), W8A8 prefill 2048 x 11008 x 4096, and the quantize /
+    dequantize sweep on [16384 x 4096] bf16.  Each timed call reads inputs
+    larger than L2 or a distinct copy from a ring of >= 4 x L2."""
+    hbm = peaks["hbm_gbs"] * 1e9
+    out = {}
+    ring_bytes = 4 * L2_BYTES
+    # W4A16 decode: INT4 symmetric, g = 128, binary16 scales
+    Nd, Kd = 4096, 4096
+    wdec = inputs.to_bf16(inputs.normal((Nd, Kd), 0.02, 0)).to(dev)
+    p4 = qlin.make_params("s4", "group", group=128, scale_f16=True)
+    q4, s4, _ = qlin.quantize(wdec, p4)
+    w_bytes = Nd * Kd // 2 + Nd * (Kd // 128) * 2
+    copies = [qlin.pack_w4(q4, s4, None, Nd, Kd, 128) for _ in range(ring_bytes // w_bytes + 1)]
+    dec = {}
+    for m in (1, 4, 16):
+        x = inputs.to_bf16(inputs.normal((m, Kd), 1.0, 1)).to(dev)
+        y = torch.empty((m, Nd), dtype=torch.bfloat16, device=dev)
+        nb = qlin.qlin_workspace_size(qlin.QLIN_OP_GEMM_W4A16, m, Nd, Kd)
+        ws = torch.empty(max(nb, 16), dtype=torch.uint8, device=dev)
+        t = _time_calls(lambda i: qlin.qlin_gemm_w4a16(x, copies[i % len(copies)][0], copies[i % len(copies)][1], m,
+                                                       y, ws, nb, None))
+        b = w_bytes + m * Kd * 2 + m * Nd * 2
+        dec["M%d" % m] = {"us": t * 1e6, "weight_gbs": w_bytes / t / 1e9, "roofline_frac": b / hbm / t}
+    out["w4a16_decode_4096x4096_s4_g128"] = dec
+    del copies, q4, s4, wdec
+    # W8A8 prefill (SmoothQuant-smoothed X and W, per-token / per-channel INT8)
+    x, w, _ = inputs.w8a8_prefill()
+    xd, wd = x.to(dev), w.to(dev)
+    sm = qlin.smooth_factors(qlin.absmax(xd, qlin.QLIN_PER_COL), qlin.absmax(wd, qlin.QLIN_PER_COL), 0.5)
+    qx, sx, _ = qlin.quantize(xd, qlin.make_params("s8", "row", smooth_mode=qlin.QLIN_SMOOTH_DIVIDE), smooth=sm)
+    qw, sw, _ = qlin.quantize(wd, qlin.make_params("s8", "row", smooth_mode=qlin.QLIN_SMOOTH_MULTIPLY), smooth=sm)
+    Mp, Np, Kp = qx.shape[0], qw.shape[0], qx.shape[1]
+    nrep = ring_bytes // ((Mp + Np) * Kp) + 1
+    ring = [(qx.clone(), qw.clone()) for _ in range(nrep)]
+    y = torch.empty((Mp, Np), dtype=torch.bfloat16, device=dev)
+    nb = qlin.qlin_workspace_size(qlin.QLIN_OP_GEMM_W8A8, Mp, Np, Kp)
+    ws = torch.empty(max(nb, 16), dtype=torch.uint8, device=dev)
+    t = _time_calls(lambda i: qlin.qlin_gemm_w8a8(ring[i % nrep][0], sx, ring[i % nrep][1], sw, Mp, Np, Kp, y,
+                                                  qlin.QLIN_BF16, None, ws, nb, None))
+    ops = 2.0 * Mp * Np * Kp
+    out["w8a8_prefill_%dx%dx%d" % (Mp, Np, Kp)] = {"us": t * 1e6, "tops": ops / t / 1e12,
+                                                   "roofline_frac": ops / (int8_peak * 1e12) / t}
+    del ring, qx, qw, xd, wd, x, w
+    # quantize / dequantize sweep
+    xs = inputs.sweep_tensor().to(dev)
+    R_, C_ = xs.shape
+    sweep = {}
+    modes = [("s8", "tensor", 0), ("s8", "row", 0), ("s8", "col", 0), ("s8", "group", 32), ("s8", "group", 64),
+             ("s8", "group", 128), ("s4", "tensor", 0), ("s4", "row", 0), ("s4", "group", 128), ("u8", "tensor", 0),
+             ("u8", "row", 0), ("u8", "col", 0), ("u8", "group", 128)]
+    for code, gran, g in modes:
+        p = qlin.make_params(code, gran, group=g)
+        q, s_, z_ = qlin.quantize(xs, p)
+        nb = qlin.qlin_workspace_size(qlin.QLIN_OP_QUANTIZE, R_, C_, 0, p)
+        ws = torch.empty(max(nb, 16), dtype=torch.uint8, device=dev)
+        t = _time_calls(lambda i: qlin.qlin_quantize(xs, qlin.QLIN_BF16, R_, C_, C_, None, p, q, s_, z_, ws, nb, None))
+        b = R_ * C_ * 2 + q.numel() + s_.numel() * s_.element_size() + (0 if z_ is None else z_.numel() * 4)
+        key = "quantize_%s_%s%s" % (code, gran, g if g else "")
+        sweep[key] = {"us": t * 1e6, "gbs": b / t / 1e9, "roofline_frac": b / hbm / t}
+        if (code, gran) in (("s8", "row"), ("s4", "group")):
+            yq = torch.empty((R_, C_), dtype=torch.bfloat16, device=dev)
+            t = _time_calls(lambda i: qlin.qlin_dequantize(q, s_, z_, p, R_, C_, yq, qlin.QLIN_BF16, None))
+            b = q.numel() + s_.numel() * s_.element_size() + R_ * C_ * 2
+            sweep["dequantize_%s_%s%s" % (code, gran, g if g else "")] = {"us": t * 1e6, "gbs": b / t / 1e9,
+                                                                           "roofline_frac": b / hbm / t}
+    p = qlin.make_params("s8", "tensor", percentile=99.9)
+    q, s_, z_ = qlin.quantize(xs, p)
+    nb = qlin.qlin_workspace_size(qlin.QLIN_OP_QUANTIZE, R_, C_, 0, p)
+    ws = torch.empty(max(nb, 16), dtype=torch.uint8, device=dev)
+    t = _time_calls(lambda i: qlin.qlin_quantize(xs, qlin.QLIN_BF16, R_, C_, C_, None, p, q, s_, z_, ws, nb, None))
+    b = R_ * C_ * 2 + q.numel() + 4
+    sweep["quantize_s8_tensor_p99.9"] = {"us": t * 1e6, "gbs": b / t / 1e9, "roofline_frac": b / hbm / t}
+    out["sweep_16384x4096_bf16"] = sweep
+    return out
+
+
 # ------------------------------------------------------------------ CPU baseline (oracle)
 def oracle_step_seconds(rows_w8, threads):
     """Time the CPU oracle on a bounded sample of one step; return
@@ -419,6 +512,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the timings of the other workloads (decode, prefill, sweep)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
@@ -533,6 +628,12 @@ def main():
     e2e_t = max_over_ranks(e0.elapsed_time(e1) / 1e3 / args.e2e_steps, world, dev)
     e2e_value = world * 100.0 * t_roof / e2e_t
 
+    configs = None
+    if not args.no_configs:
+        configs = measure_other_configs(dev, peaks, int8_peak)
+        if qlin.qlin_device_error() != 0:
+            raise RuntimeError("device-side error in the configuration measurements")
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         threads = cpu_threads()
@@ -554,7 +655,8 @@ def main():
                "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                        "ms_per_step": e2e_t * 1e3},
                "gpu_launches": step.launches_per_step() * args.steps,
-               "clocks": clock_info, "peaks": peaks, "int8_ref_tflops": int8_ref, "detail": detail}
+               "clocks": clock_info, "peaks": peaks, "int8_ref_tflops": int8_ref, "detail": detail,
+               "configs": configs}
         print(json.dumps(out))
     if world > 1:
         torch.distributed.destroy_process_group()
