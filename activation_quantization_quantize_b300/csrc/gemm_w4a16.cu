@@ -557,7 +557,7 @@ static cudaError_t launch_gemv2(const __nv_bfloat16* x, const uint8_t* blob, con
                                 __nv_bfloat16* y, cudaStream_t st) {
     constexpr int smem = 8 * GV_P * gemv2_stage_bytes<NT>();
     static_assert(smem >= 8 * NT * 16 * 16 * 4, "reduction tile must fit in the ring");
-    cudaError_t e = cudaFuncSetAttribute(k_w4_gemv2<MT, NT, G128>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    cudaError_t e = ensure_smem((const void*)k_w4_gemv2<MT, NT, G128>, smem);
     if (e != cudaSuccess) return e;
     k_w4_gemv2<MT, NT, G128><<<(unsigned)(h.N / (16 * NT)), 256, smem, st>>>(x, blob, h, M, y);
     return cudaGetLastError();
@@ -574,7 +574,7 @@ template <int MT, int NT>
 static cudaError_t launch_gemv(const __nv_bfloat16* x, const uint8_t* blob, const qlin_w4_header& h, int64_t M,
                                __nv_bfloat16* y, cudaStream_t st) {
     constexpr int smem = gemv_smem_bytes<NT>();
-    cudaError_t e = cudaFuncSetAttribute(k_w4_gemv<MT, NT>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    cudaError_t e = ensure_smem((const void*)k_w4_gemv<MT, NT>, smem);
     if (e != cudaSuccess) return e;
     k_w4_gemv<MT, NT><<<(unsigned)(h.N / (16 * NT)), 256, smem, st>>>(x, blob, h, M, y);
     return cudaGetLastError();
@@ -1154,7 +1154,7 @@ cudaError_t run_gemm_w4a16(const void* x, const void* packed, const qlin_w4_head
     a.part = (plan.nsplit > 1) ? reinterpret_cast<float*>(ws) : nullptr;
     a.y = yb;
     const size_t smem = w4tc::smem_bytes(plan.ntok);
-    cudaError_t e = cudaFuncSetAttribute(k_w4_gemm_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    cudaError_t e = ensure_smem((const void*)k_w4_gemm_tc, (int)smem);
     if (e != cudaSuccess) return e;
     dim3 grid((unsigned)(h->N / w4tc::BMW), (unsigned)plan.nsplit, (unsigned)plan.mtiles);
     k_w4_gemm_tc<<<grid, w4tc::THREADS, smem, st>>>(tmap, a);

@@ -695,7 +695,7 @@ cudaError_t run_gemm_w8a8(const int8_t* qx, const float* sx, const int8_t* qw, c
     if (w8a8_kernel_choice() == 1) {
         using namespace w8;
         size_t smem = (size_t)2 * STAGES * TILE_BYTES;
-        cudaError_t e = cudaFuncSetAttribute(k_w8a8_mma, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        cudaError_t e = ensure_smem((const void*)k_w8a8_mma, (int)smem);
         if (e != cudaSuccess) return e;
         dim3 grid((unsigned)ceil_div(N, BN), (unsigned)ceil_div(M, BM));
         k_w8a8_mma<<<grid, THREADS, smem, st>>>(qx, sx, qw, sw, M, N, K, y, yt, acc_out);
@@ -720,7 +720,7 @@ cudaError_t run_gemm_w8a8(const int8_t* qx, const float* sx, const int8_t* qw, c
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
         return cudaErrorInvalidValue;
-    cudaError_t e = cudaFuncSetAttribute(k_w8a8_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
+    cudaError_t e = ensure_smem((const void*)k_w8a8_tc, (int)SMEM_BYTES);
     if (e != cudaSuccess) return e;
     W8TcArgs a;
     a.sx = sx;

@@ -12,6 +12,10 @@ namespace qlin {
 
 int num_sms();
 int64_t percentile_rank(int64_t n, double p);
+// Raise a kernel's dynamic shared-memory limit on the current device to at
+// least `bytes`, calling the runtime only the first time a (kernel, device)
+// pair needs a larger limit (the call costs host time on every launch).
+cudaError_t ensure_smem(const void* kernel, int bytes);
 
 size_t quantize_ws_bytes(int64_t rows, int64_t cols, const qlin_qparams* p);
 cudaError_t run_quantize(const void* x, int xt, int64_t rows, int64_t cols, int64_t ld, const float* smooth,

@@ -17,6 +17,9 @@
 //   k_*_generic     scalar fallbacks for unaligned or odd shapes.
 //   k_hist*/k_select percentile clipping (exact radix select on |x| bits).
 //   k_dequant       x^ = fl(s (q - z)) rounded to the output type.
+#include <map>
+#include <mutex>
+
 #include "qlin_common.cuh"
 #include "qlin_internal.h"
 #include "tc_ptx.cuh"
@@ -1145,6 +1148,20 @@ __global__ void k_smooth_factors(const float* xmax, const float* wmax, int64_t K
 
 // ------------------------------------------------------------------ host launchers
 static int g_num_sms = 0;
+cudaError_t ensure_smem(const void* kernel, int bytes) {
+    static std::mutex mu;
+    static std::map<std::pair<const void*, int>, int> raised;  // (kernel, device) -> bytes
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    std::lock_guard<std::mutex> lock(mu);
+    int& have = raised[std::make_pair(kernel, dev)];
+    if (have >= bytes) return cudaSuccess;
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e == cudaSuccess) have = bytes;
+    return e;
+}
+
 int num_sms() {
     if (g_num_sms == 0) {
         int dev = 0;
@@ -1270,8 +1287,7 @@ static cudaError_t run_quantize_t(QuantArgs a, int xt, const qlin_qparams* p, vo
             a.smooth_mode == QLIN_SMOOTH_NONE && 2 * (size_t)buf_stride <= 200 * 1024) {
             const int nbuf = 3 * (size_t)buf_stride <= 200 * 1024 ? 3 : 2;
             const int smem = nbuf * (int)buf_stride;
-            cudaError_t e = cudaFuncSetAttribute(k_quant_rows_bulk<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                 smem);
+            cudaError_t e = ensure_smem((const void*)k_quant_rows_bulk<T>, smem);
             if (e != cudaSuccess) return e;
             int64_t grid = num_sms();
             if (grid > a.rows) grid = a.rows;
@@ -1280,8 +1296,7 @@ static cudaError_t run_quantize_t(QuantArgs a, int xt, const qlin_qparams* p, vo
         }
         if (a.gran == QLIN_PER_ROW && !a.absmax_out && nchunks > 512 && xt != QLIN_F32 &&
             a.smooth_mode == QLIN_SMOOTH_NONE && raw_bytes <= 56 * 1024) {
-            cudaError_t e = cudaFuncSetAttribute(k_quant_rows16<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                 (int)raw_bytes);
+            cudaError_t e = ensure_smem((const void*)k_quant_rows16<T>, (int)raw_bytes);
             if (e != cudaSuccess) return e;
             int64_t grid = (int64_t)num_sms() * 4;
             if (grid > a.rows) grid = a.rows;
@@ -1289,8 +1304,7 @@ static cudaError_t run_quantize_t(QuantArgs a, int xt, const qlin_qparams* p, vo
             return cudaGetLastError();
         }
         if (a.gran == QLIN_PER_ROW && !a.absmax_out && nchunks > 1024 && row_bytes <= 113 * 1024) {
-            cudaError_t e = cudaFuncSetAttribute(k_quant_longrows<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                 (int)row_bytes);
+            cudaError_t e = ensure_smem((const void*)k_quant_longrows<T>, (int)row_bytes);
             if (e != cudaSuccess) return e;
             int64_t grid = (int64_t)num_sms() * 2;
             if (grid > a.rows) grid = a.rows;
@@ -1309,7 +1323,7 @@ static cudaError_t run_quantize_t(QuantArgs a, int xt, const qlin_qparams* p, vo
             uint32_t* sel = hist2 + kHist2;
             uint64_t k = (uint64_t)percentile_rank(n, p->clip_percentile);
             if ((e = cudaMemsetAsync(ws, 0, (size_t)(kHist1 + kHist2 + 4) * 4, st)) != cudaSuccess) return e;
-            cudaFuncSetAttribute(k_hist1<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, kHist1 * 4);
+            ensure_smem((const void*)k_hist1<T>, kHist1 * 4);
             k_hist1<T><<<num_sms(), 1024, kHist1 * 4, st>>>(a, hist1);
             // Low 16 bits of |x| are zero for unsmoothed bf16 input.
             bool need2 = !(xt == QLIN_BF16 && a.smooth_mode == QLIN_SMOOTH_NONE);

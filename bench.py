@@ -278,6 +278,32 @@ def _time_calls(fn, n_iter=20, n_warm=3):
     return e0.elapsed_time(e1) / 1e3 / n_iter
 
 
+def _time_graph(fn, n_calls):
+    """Mean seconds per call of fn(0) .. fn(n_calls - 1) replayed from one
+    captured CUDA graph (no host launch cost between calls), as a decode loop
+    would run them."""
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        for i in range(3):
+            fn(i)
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for i in range(n_calls):
+            fn(i)
+    g.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    g.replay()
+    e1.record()
+    e1.synchronize()
+    del g
+    return e0.elapsed_time(e1) / 1e3 / n_calls
+
+
 def measure_other_configs(dev, peaks, int8_peak):
     """Time the remaining workloads outside the step: W4A16 decode 4096 x 4096
     (M = 1, 4, 16), W8A8 prefill 2048 x 11008 x 4096, and the quantize /
@@ -299,10 +325,13 @@ def measure_other_configs(dev, peaks, int8_peak):
         y = torch.empty((m, Nd), dtype=torch.bfloat16, device=dev)
         nb = qlin.qlin_workspace_size(qlin.QLIN_OP_GEMM_W4A16, m, Nd, Kd)
         ws = torch.empty(max(nb, 16), dtype=torch.uint8, device=dev)
-        t = _time_calls(lambda i: qlin.qlin_gemm_w4a16(x, copies[i % len(copies)][0], copies[i % len(copies)][1], m,
-                                                       y, ws, nb, None))
+        call = lambda i: qlin.qlin_gemm_w4a16(x, copies[i % len(copies)][0], copies[i % len(copies)][1], m,  # noqa: E731
+                                               y, ws, nb, None)
+        t_eager = _time_calls(call)
+        t = _time_graph(call, len(copies))
         b = w_bytes + m * Kd * 2 + m * Nd * 2
-        dec["M%d" % m] = {"us": t * 1e6, "weight_gbs": w_bytes / t / 1e9, "roofline_frac": b / hbm / t}
+        dec["M%d" % m] = {"us": t * 1e6, "weight_gbs": w_bytes / t / 1e9, "roofline_frac": b / hbm / t,
+                          "us_eager": t_eager * 1e6, "timing": "CUDA graph of %d calls over distinct copies" % len(copies)}
     out["w4a16_decode_4096x4096_s4_g128"] = dec
     del copies, q4, s4, wdec
     # W8A8 prefill (SmoothQuant-smoothed X and W, per-token / per-channel INT8)
