@@ -300,94 +300,11 @@ __global__ void __launch_bounds__(512, 2) k_quant_longrows(QuantArgs a) {
     }
 }
 
-// ------------------------------------------------------------------ long rows, 16-bit input, no smoothing
-// Per-row scopes of long bf16/f16 rows without smoothing: the raw 16-bit row
-// is staged in shared memory (cols * 2 bytes, so up to four CTAs per SM), pass
-// 1 loads and reduces, pass 2 re-reads the staged row and writes the codes.
-// With dynamic scales |x/s| <= qmax (+ rounding), so the far-range branch of
-// the code computation is never taken.
-template <typename T>
-__global__ void __launch_bounds__(256, 4) k_quant_rows16(QuantArgs a) {
-    extern __shared__ uint4 xs16[];  // [cols / 8] raw 16-bit chunks
-    __shared__ float red_hi[8], red_lo[8];
-    const int tid = threadIdx.x, nt = blockDim.x;
-    const int64_t nchunks = a.cols / 8;
-    const uint4* __restrict__ xg = reinterpret_cast<const uint4*>(a.x);
-    const CodeRange cr = make_range(a.qmin, a.qmax);
-    for (int64_t r = blockIdx.x; r < a.rows; r += gridDim.x) {
-        const uint4* __restrict__ xr = xg + r * (a.ld / 8);
-        float hi = 0.0f, lo = 0.0f;
-        for (int64_t c0 = tid; c0 < nchunks; c0 += 4 * (int64_t)nt) {
-            uint4 raw[4];
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const int64_t c = c0 + (int64_t)u * nt;
-                raw[u] = (c < nchunks) ? __ldg(xr + c) : make_uint4(0, 0, 0, 0);
-            }
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const int64_t c = c0 + (int64_t)u * nt;
-                if (c >= nchunks) break;
-                xs16[c] = raw[u];
-                float v[8];
-                unpack8<T>(raw[u], v);
-#pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    if (a.sym) {
-                        hi = fmaxf(hi, fabsf(v[j]));
-                    } else {
-                        hi = fmaxf(hi, v[j]);
-                        lo = fminf(lo, v[j]);
-                    }
-                }
-            }
-        }
-        hi = warp_max(hi);
-        lo = warp_min(lo);
-        if ((tid & 31) == 0) {
-            red_hi[tid >> 5] = hi;
-            red_lo[tid >> 5] = lo;
-        }
-        __syncthreads();
-        hi = 0.0f;
-        lo = 0.0f;
-        for (int w = 0; w < (nt >> 5); ++w) {
-            hi = fmaxf(hi, red_hi[w]);
-            lo = fminf(lo, red_lo[w]);
-        }
-        float s;
-        int z;
-        if (a.static_scale) {
-            s = load_scale(a.s, r, a.scale_f16);
-            z = a.z ? a.z[r] : 0;
-        } else {
-            scale_zero(lo, hi, a.qmin, a.qmax, a.sym, a.scale_f16, s, z);
-            if (tid == 0) {
-                store_scale(a.s, r, a.scale_f16, s);
-                if (a.z) a.z[r] = z;
-            }
-        }
-        const ScopeParams p = make_scope(s, z);
-        for (int64_t c = tid; c < nchunks; c += nt) {
-            float v[8];
-            unpack8<T>(xs16[c], v);
-            uint32_t cb[8];
-            if (a.static_scale) {
-                code_bits8<false>(v, p, cr, cb);
-            } else {
-                code_bits8<true>(v, p, cr, cb);
-            }
-            store_codes8(a.q, r, a.cols, c, a.code4, cb);
-        }
-        __syncthreads();  // xs16 and red_* are reused by the next row
-    }
-}
-
 // Per-token quantize of 16-bit rows streamed through shared memory by bulk
 // copies.  One persistent CTA per SM keeps `nbuf` (2 or 3) row buffers: while
 // it reduces and quantizes row i from one, the copies of its next rows land in
-// the others, so every SM keeps nbuf - 1 rows in flight.  Same arithmetic as
-// k_quant_rows16.
+// the others, so every SM keeps nbuf - 1 rows in flight.  The codes come from
+// code_bits8, as in the other row kernels.
 constexpr int kBulkThreads = 512;
 
 // Running range of packed 16-bit pairs: |x| max (symmetric) or max and min.
@@ -556,7 +473,9 @@ __global__ void __launch_bounds__(kBulkThreads, 1) k_quant_rows_bulk(QuantArgs a
 // 16-bit rows of at most 32 * NC eight-value chunks: one warp per row, the row
 // held in registers (lane l holds chunks l, l + 32, ...), every reduction a
 // register shuffle.  Many warps per SM keep many rows in flight.  Same
-// arithmetic as k_quant_rows16 / k_quant_rows_bulk.
+// arithmetic as k_quant_rows_bulk.  (The launcher uses it for per-row scopes:
+// per-group scopes recompute the group's scale in every lane, which costs more
+// than the register-resident k_quant_rows.)
 template <typename T, int NC>
 __global__ void __launch_bounds__(256) k_quant_warprows(QuantArgs a) {
     const int lane = threadIdx.x & 31;
@@ -1294,15 +1213,6 @@ static cudaError_t run_quantize_t(QuantArgs a, int xt, const qlin_qparams* p, vo
             k_quant_rows_bulk<T><<<(unsigned)grid, kBulkThreads, smem, st>>>(a, buf_stride, nbuf);
             return cudaGetLastError();
         }
-        if (a.gran == QLIN_PER_ROW && !a.absmax_out && nchunks > 512 && xt != QLIN_F32 &&
-            a.smooth_mode == QLIN_SMOOTH_NONE && raw_bytes <= 56 * 1024) {
-            cudaError_t e = ensure_smem((const void*)k_quant_rows16<T>, (int)raw_bytes);
-            if (e != cudaSuccess) return e;
-            int64_t grid = (int64_t)num_sms() * 4;
-            if (grid > a.rows) grid = a.rows;
-            k_quant_rows16<T><<<(unsigned)grid, 256, raw_bytes, st>>>(a);
-            return cudaGetLastError();
-        }
         if (a.gran == QLIN_PER_ROW && !a.absmax_out && nchunks > 1024 && row_bytes <= 113 * 1024) {
             cudaError_t e = ensure_smem((const void*)k_quant_longrows<T>, (int)row_bytes);
             if (e != cudaSuccess) return e;
@@ -1436,10 +1346,10 @@ cudaError_t run_dequantize(const void* q, const void* s, const int32_t* z, const
     int ys = (yt == QLIN_F32) ? 4 : 2;
     bool vec = (cols % 8 == 0) && (p->gran != QLIN_PER_GROUP || p->group % 8 == 0) &&
                ((uintptr_t)q % (d.code4 ? 4 : 8) == 0) && ((uintptr_t)y % (8 * ys) == 0);
-    const bool rows16 = (cols % 16 == 0) && (p->gran != QLIN_PER_COL) &&
+    const bool seg16 = (cols % 16 == 0) && (p->gran != QLIN_PER_COL) &&
                         (p->gran != QLIN_PER_GROUP || p->group % 16 == 0) &&
                         ((uintptr_t)q % (d.code4 ? 8 : 16) == 0) && ((uintptr_t)y % 16 == 0);
-    if (rows16)
+    if (seg16)
         k_dequant_rows<<<blocks, 256, 0, st>>>(d);
     else if (vec)
         k_dequant_vec<<<blocks, 256, 0, st>>>(d);
