@@ -316,3 +316,45 @@ def test_w4a16_gemv_two_tiles_per_cta(group, M, asym):
     what = w4_oracle_weight(q, s, z, p, N, K, group, rows=rows)
     yo = oracle.matmul_f64(host_f32(x), what)
     assert rel_err_out(host_f32(y)[:, rows], yo) < GEMM_REL_TOL
+
+
+@pytest.mark.parametrize("M", [64, 256])
+def test_w4a16_back_to_back_calls(M):
+    """Many calls queued back to back, alternating two packed copies (as a
+    serving loop issues them): no device-side wait runs out and every call
+    gives the same bits as a lone call."""
+    N, K = 8192, 28672
+    w = inputs.downproj_weight()
+    x = inputs.downproj_activation(M).cuda()
+    copies = []
+    for scale in (1.0, 0.5):
+        p, q, s, z, packed, hdr = w4_prepare((w.float() * scale).to(torch.bfloat16).cuda(), 128, True)
+        copies.append((packed, hdr))
+    refs = []
+    for packed, hdr in copies:
+        refs.append(qlin.gemm_w4a16(x, packed, hdr))
+        torch.cuda.synchronize()
+    assert qlin.qlin_device_error() == 0
+    ys = [None, None]
+    for i in range(24):
+        packed, hdr = copies[i % 2]
+        ys[i % 2] = qlin.gemm_w4a16(x, packed, hdr)
+    torch.cuda.synchronize()
+    assert qlin.qlin_device_error() == 0
+    assert torch.equal(ys[0], refs[0]) and torch.equal(ys[1], refs[1])
+
+
+def test_w8a8_back_to_back_calls():
+    """W8A8 calls queued back to back (split tail tiles and drains included):
+    no device-side wait runs out and the bits match a lone call."""
+    M, N, K = 2048, 4096, 28672
+    p8 = qlin.make_params("s8", "row")
+    qx, sx, _ = qlin.quantize(inputs.downproj_activation(M, outliers=True).cuda(), p8)
+    qw, sw, _ = qlin.quantize(inputs.downproj_weight(N=N).cuda(), p8)
+    ref = qlin.gemm_w8a8(qx, sx, qw, sw)
+    torch.cuda.synchronize()
+    for _ in range(24):
+        y = qlin.gemm_w8a8(qx, sx, qw, sw)
+    torch.cuda.synchronize()
+    assert qlin.qlin_device_error() == 0
+    assert torch.equal(y, ref)
