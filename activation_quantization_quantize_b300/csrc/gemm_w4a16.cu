@@ -713,7 +713,8 @@ constexpr size_t SMEM_LIMIT = 232448;     // dynamic shared memory per CTA
 // The activation tiles have their own, deeper ring: their TMA latency (L2
 // under the weight stream) would otherwise bound the k-block rate.
 __host__ __device__ constexpr int b_bytes(int ntok) { return ntok * BK * 2; }  // ntok rows of 128 B
-inline int a_stages(int ntok) { return ntok > 128 ? 3 : A_STAGES_MAX; }  // EXP
+// 256 tokens: 3 A stages, which leaves room for 5 activation stages of 32 KB.
+inline int a_stages(int ntok) { return ntok > 128 ? 3 : A_STAGES_MAX; }
 inline int b_stages(int ntok) {
     int s = (int)((SMEM_LIMIT - 1024 - RING_BYTES - BAR_BYTES - (size_t)a_stages(ntok) * A_BYTES) / b_bytes(ntok));
     return s < B_STAGES_MAX ? s : B_STAGES_MAX;
@@ -1021,6 +1022,347 @@ __global__ void __launch_bounds__(w4tc::THREADS, 1) k_w4_gemm_tc(const __grid_co
     }
 }
 
+// ------------------------------------------------------------------ W4A16 GEMM, A operand in TMEM (M <= 128 per CTA)
+// The same roles and pipeline as k_w4_gemm_tc, but the converters write the
+// dequantized weight tile into tensor memory with tcgen05.st and the MMA reads
+// A from there (tcgen05.mma with an [a-tmem] operand).  That takes the 16 KB
+// store of each k-block and the tensor core's 16 KB read of it off the
+// shared-memory ports, which bound the shared-memory version at these sizes.
+// TMEM holds everything for up to 128 tokens: two accumulators, the promoted
+// sums and 4 (or 8, for <= 64 tokens) A stages of 32 columns.
+namespace w4tm {
+constexpr int BMW = 128;
+constexpr int BK = 64;
+constexpr int NCONV_WARPS = 16;  // warp w: TMEM quarter w % 4, tile half (w >> 2) & 1, k-block parity w >> 3
+constexpr int EPI_WARP0 = 16;
+constexpr int MMA_WARP = 20;
+constexpr int TMA_WARP = 21;
+constexpr int THREADS = 22 * 32;
+constexpr uint32_t TMEM_COLS = 512;
+constexpr int B_STAGES_MAX = 16;
+constexpr int BAR_BYTES = 512;
+constexpr size_t SMEM_LIMIT = 232448;
+__host__ __device__ constexpr int b_bytes(int ntok) { return ntok * BK * 2; }
+// TMEM columns: accumulator b at b * acc_stride, promoted sums at
+// 2 * acc_stride, A stage s (128 lanes x 32 columns = 128 rows x 64 bf16, k
+// pairs packed low-first) at a_col0 + 32 s.
+__host__ __device__ inline int acc_stride(int ntok) { return ntok <= 64 ? 64 : 128; }
+__host__ __device__ inline int a_col0(int ntok) { return ntok <= 64 ? 256 : 384; }
+__host__ __device__ inline int a_stages(int ntok) { return ntok <= 64 ? 8 : 4; }
+constexpr int CRING = 6;  // cp.async ring depth (own k-blocks) of each converter warp
+constexpr int CR_WARP_BYTES = CRING * (512 + 256);  // codes [CRING][32 chunks][16 B] + group words [CRING][32][8 B]
+constexpr int RING_BYTES = NCONV_WARPS * CR_WARP_BYTES;
+inline int b_stages(int ntok) {
+    int s = (int)((SMEM_LIMIT - 1024 - RING_BYTES - BAR_BYTES) / b_bytes(ntok));
+    return s < B_STAGES_MAX ? s : B_STAGES_MAX;
+}
+inline size_t smem_bytes(int ntok) { return 1024 + (size_t)b_stages(ntok) * b_bytes(ntok) + RING_BYTES + BAR_BYTES; }
+}  // namespace w4tm
+
+// 16 TMEM lanes x 4 x 256 bits: in repetition r, thread (g = lane / 4, t = lane % 4)
+// writes r[4r], r[4r+1] to lane g, columns 8r + 2t, 8r + 2t + 1, and r[4r+2],
+// r[4r+3] to lane g + 8, same columns (base lane and column from taddr).
+__device__ __forceinline__ void tmem_st_16x256b_x4(uint32_t taddr, const uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.16x256b.x4.b32 [%0], "
+        "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
+        "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+        : "memory");
+}
+// D[tmem] (+)= A[tmem] * B[smem desc]^T, kind::f16; A is 128 lanes (rows) x 8
+// columns (16 k) from a_tmem.
+__device__ __forceinline__ void mma_f16_tmem_a(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                               uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+__global__ void __launch_bounds__(w4tm::THREADS, 1) k_w4_gemm_tm(const __grid_constant__ CUtensorMap tmx, W4TcArgs a) {
+    using namespace w4tm;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+    const int SA = a_stages(a.ntok), SB = a.b_stages;
+    const uint32_t B_BYTES = (uint32_t)b_bytes(a.ntok);
+    uint8_t* tilesB = smem;                                  // [SB][ntok * 128 B], 1024-aligned
+    uint8_t* cring = tilesB + (size_t)SB * B_BYTES;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(cring + RING_BYTES);
+    volatile uint32_t* misc = reinterpret_cast<volatile uint32_t*>(bars + 2 * SA + 2 * SB + 5);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 2);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t N = a.h.N;
+    const int64_t nblk = blockIdx.x;
+    const int split = blockIdx.y;
+    const int64_t m0 = (int64_t)blockIdx.z * a.ntok;
+    const int c_begin = (int)((int64_t)a.nchunk * split / a.nsplit);
+    const int c_end = (int)((int64_t)a.nchunk * (split + 1) / a.nsplit);
+    const int nkb = c_end - c_begin;
+    const uint32_t ACC_STRIDE = (uint32_t)acc_stride(a.ntok), A_COL0 = (uint32_t)a_col0(a.ntok);
+
+    const uint32_t bar0 = tc::smem_addr(bars);
+    auto fullA = [&](int s) { return bar0 + 8u * s; };
+    auto emptyA = [&](int s) { return bar0 + 8u * (SA + s); };
+    auto fullB = [&](int s) { return bar0 + 8u * (2 * SA + s); };
+    auto emptyB = [&](int s) { return bar0 + 8u * (2 * SA + SB + s); };
+    const uint32_t acc_full0 = bar0 + 8u * (2 * SA + 2 * SB);
+    auto acc_full = [&](int b) { return acc_full0 + 8u * b; };
+    auto acc_empty = [&](int b) { return acc_full0 + 16u + 8u * b; };
+    const uint32_t done_bar = acc_full0 + 32u;
+    const int chain_len = a.promote > 0 ? a.promote : (nkb > 0 ? nkb : 1);
+    const int nchains = nkb > 0 ? (nkb + chain_len - 1) / chain_len : 0;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < SA; ++s) {
+            tc::mbar_init(fullA(s), 8);
+            tc::mbar_init(emptyA(s), 1);
+        }
+        for (int s = 0; s < SB; ++s) {
+            tc::mbar_init(fullB(s), 1);
+            tc::mbar_init(emptyB(s), 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            tc::mbar_init(acc_full(b), 1);
+            tc::mbar_init(acc_empty(b), 4);
+        }
+        tc::mbar_init(done_bar, 1);
+        misc[2] = 0;
+        tc::mbar_init_fence();
+    }
+    if (warp == MMA_WARP) {
+        tc::tmem_alloc(tc::smem_addr((const void*)&misc[0]), TMEM_COLS);
+        tc::tmem_relinquish();
+    }
+    tc::tc_fence_before();
+    __syncthreads();
+    tc::tc_fence_after();
+    const uint32_t tmem = misc[0];
+
+    if (warp < NCONV_WARPS) {
+        // Warp w converts the 16-row tile 2 (w % 4) + ((w >> 2) & 1) for the
+        // k-blocks of parity w >> 3 and stores it into its own TMEM quarter.
+        // Lane (g, t) copies its packed 16 bytes (k 16t .. 16t+15 of rows g and
+        // g+8) to ring chunk 8t + g; after the warp's copies land it reads word t
+        // of chunks 8r + g, r = 0..3, i.e. k 16r + 4t .. 16r + 4t + 3, which is
+        // what the 16x256b TMEM store wants from this lane.
+        const int q = warp & 3, hsel = (warp >> 2) & 1, par = warp >> 3;
+        const int ntl = 2 * q + hsel;
+        const int gq = lane >> 2, t = lane & 3;
+        const int64_t nt = nblk * 8 + ntl;
+        const int64_t ngr = a.h.K / a.h.group;
+        const int gshift = __ffs(a.h.group) - 1;
+        const bool asym = a.h.asym != 0;
+        const bool g32 = a.h.group == 32;
+        const int zshift = 8 * (gq & 3);
+        const uint8_t* gcodes = a.blob + a.h.codes_off + (nt * a.nchunk + c_begin) * 512 + lane * 16;
+        const uint8_t* gsc = a.blob + a.h.scales_off + nt * ngr * 32 + gq * 4;
+        const uint8_t* gze = a.blob + a.h.zeros_off + nt * ngr * 8 + (gq & 4);
+        uint8_t* rp = cring + warp * CR_WARP_BYTES;
+        const uint32_t rc = tc::smem_addr(rp) + (uint32_t)(8 * t + gq) * 16;  // codes [CRING][32 chunks][16 B]
+        const uint32_t rm = tc::smem_addr(rp + CRING * 512) + lane * 8;          // words [CRING][32][8 B]
+        const uint32_t t_lane = (uint32_t)(32 * q + 16 * hsel) << 16;
+        int kb_issue = par, slot_issue = 0;
+        auto issue = [&]() {
+            if (kb_issue < nkb) {
+                const int64_t gi = ((int64_t)(c_begin + kb_issue) * 64 + 16 * t) >> gshift;
+                cp_async16(rc + slot_issue * 512, gcodes + (int64_t)kb_issue * 512);
+                cp_async4(rm + slot_issue * 256, gsc + gi * 32);
+                if (asym) cp_async4(rm + slot_issue * 256 + 4, gze + gi * 8);
+            }
+            cp_async_commit();
+            kb_issue += 2;
+            slot_issue = slot_issue + 1 == CRING ? 0 : slot_issue + 1;
+        };
+#pragma unroll 1
+        for (int i = 0; i < CRING - 1; ++i) issue();
+        int s = par, slot = 0;
+        uint32_t ph = 0u;
+        for (int kb = par; kb < nkb; kb += 2) {
+            issue();
+            cp_async_wait<CRING - 1>();
+            __syncwarp();  // the other lanes' copies of this slot have landed
+            const uint8_t* cs = rp + slot * 512 + gq * 16 + t * 4;
+            uint32_t u[4];
+#pragma unroll
+            for (int r = 0; r < 4; ++r) u[r] = *reinterpret_cast<const uint32_t*>(cs + r * 128);
+            // group words of lanes (g, 0) and (g, 2): k 0..31 and 32..63 of the block
+            const uint8_t* ms = rp + CRING * 512 + slot * 256 + gq * 32;
+            const uint2 mw0 = *reinterpret_cast<const uint2*>(ms);
+            const uint2 mw1 = g32 ? *reinterpret_cast<const uint2*>(ms + 16) : mw0;
+            __syncwarp();  // every lane has read the slot before it is refilled
+            slot = slot + 1 == CRING ? 0 : slot + 1;
+            DqRaw d0, d1;
+            d0.s2 = mw0.x;
+            d0.zb = asym ? (mw0.y >> zshift) & 0xFFu : 0x88u;
+            d1.s2 = mw1.x;
+            d1.zb = asym ? (mw1.y >> zshift) & 0xFFu : 0x88u;
+            RowDq rg0, rh0, rg1, rh1;
+            build_dq(d0, rg0, rh0);
+            if (g32)
+                build_dq(d1, rg1, rh1);
+            else {
+                rg1 = rg0;
+                rh1 = rh0;
+            }
+            uint32_t st[16];
+#pragma unroll
+            for (int r = 0; r < 4; ++r) {
+                uint32_t f[4];
+                if (r < 2)
+                    dq_word(u[r], rg0, rh0, f);
+                else
+                    dq_word(u[r], rg1, rh1, f);
+                st[4 * r + 0] = f[0];  // row g,   k 16r+4t, +1
+                st[4 * r + 1] = f[2];  // row g,   k 16r+4t+2, +3
+                st[4 * r + 2] = f[1];  // row g+8
+                st[4 * r + 3] = f[3];
+            }
+            if (!tc::mbar_wait_warp(emptyA(s), ph ^ 1u, abort_flag)) break;
+            tc::tc_fence_after();
+            tmem_st_16x256b_x4(tmem + t_lane + A_COL0 + 32u * (uint32_t)s, st);
+            tc::tmem_wait_st();
+            tc::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) tc::mbar_arrive(fullA(s));
+            s += 2;
+            if (s >= SA) {
+                s -= SA;
+                ph ^= 1u;
+            }
+        }
+        cp_async_wait<0>();
+    } else if (warp == TMA_WARP) {
+        if (lane == 0) {
+            const uint32_t tx = (uint32_t)a.ntok * BK * 2;
+            int s = 0;
+            uint32_t ph = 0;
+            for (int kb = 0; kb < nkb; ++kb) {
+                if (!tc::mbar_wait(emptyB(s), ph ^ 1u, abort_flag)) break;
+                tc::mbar_arrive_expect_tx(fullB(s), tx);
+                const uint32_t dstB = tc::smem_addr(tilesB + (size_t)s * B_BYTES);
+                tc::tma_load_2d(dstB, &tmx, (c_begin + kb) * BK, (int)m0, fullB(s));
+                if (++s == SB) {
+                    s = 0;
+                    ph ^= 1u;
+                }
+            }
+        }
+        __syncwarp();
+    } else if (warp == MMA_WARP) {
+        const uint32_t tB_addr = tc::smem_addr(tilesB);
+        int c = 0, in_chain = 0;
+        int s = 0, sb = 0;
+        uint32_t ph = 0, phb = 0;
+        for (int kb = 0; kb < nkb; ++kb) {
+            if (!tc::mbar_wait_warp(fullB(sb), phb, abort_flag)) break;
+            if (!tc::mbar_wait_warp(fullA(s), ph, abort_flag)) break;
+            if (in_chain == chain_len) {
+                if (tc::elect_one()) tc::mma_commit(acc_full(c & 1));
+                __syncwarp();
+                ++c;
+                in_chain = 0;
+                if (c >= 2 && !tc::mbar_wait_warp(acc_empty(c & 1), ((c >> 1) - 1) & 1u, abort_flag)) break;
+            }
+            tc::tc_fence_after();
+            const uint64_t bd = tc::desc_sw128(tB_addr + (uint32_t)sb * B_BYTES);
+            const uint32_t at = tmem + A_COL0 + 32u * (uint32_t)s;
+            const uint32_t dacc = tmem + ACC_STRIDE * (uint32_t)(c & 1);
+            if (tc::elect_one()) {
+#pragma unroll
+                for (int j = 0; j < BK / 16; ++j)
+                    mma_f16_tmem_a(dacc, at + 8u * j, bd + 2 * j, a.idesc, (in_chain > 0 || j > 0) ? 1u : 0u);
+                tc::mma_commit(emptyA(s));
+                tc::mma_commit(emptyB(sb));
+            }
+            __syncwarp();
+            ++in_chain;
+            if (++s == SA) {
+                s = 0;
+                ph ^= 1u;
+            }
+            if (++sb == SB) {
+                sb = 0;
+                phb ^= 1u;
+            }
+        }
+        if (tc::elect_one()) {
+            if (nkb > 0) tc::mma_commit(acc_full(c & 1));
+            tc::mma_commit(done_bar);
+        }
+        __syncwarp();
+        tc::mbar_wait_warp(done_bar, 0, abort_flag);
+    } else {
+        const int q = warp & 3;
+        const uint32_t lane_base = (uint32_t)(32 * q) << 16;
+        const int64_t n = nblk * BMW + 32 * q + lane;
+        const uint32_t t_sum = tmem + lane_base + 2u * ACC_STRIDE;
+        for (int c = 0; c < nchains; ++c) {
+            const int b = c & 1;
+            const uint32_t t_acc = tmem + lane_base + ACC_STRIDE * (uint32_t)b;
+            if (!tc::mbar_wait_warp(acc_full(b), (uint32_t)(c >> 1) & 1u, abort_flag)) break;
+            tc::tc_fence_after();
+            if (c + 1 < nchains) {
+                for (int col = 0; col < a.ntok; col += 16) {
+                    uint32_t v[16], r[16];
+                    tc::tmem_ld16(t_acc + col, v);
+                    if (c > 0) tc::tmem_ld16(t_sum + col, r);
+                    tc::tmem_wait_ld();
+#pragma unroll
+                    for (int j = 0; j < 16; ++j)
+                        r[j] = c > 0 ? __float_as_uint(__uint_as_float(r[j]) + __uint_as_float(v[j])) : v[j];
+                    tc::tmem_st16(t_sum + col, r);
+                }
+                tc::tmem_wait_st();
+                tc::tc_fence_before();
+                __syncwarp();
+                if (lane == 0) tc::mbar_arrive(acc_empty(b));
+                continue;
+            }
+            for (int col = 0; col < a.ntok; col += 16) {
+                __syncwarp();
+                uint32_t v[16], r[16];
+                tc::tmem_ld16(t_acc + col, v);
+                if (c > 0) tc::tmem_ld16(t_sum + col, r);
+                tc::tmem_wait_ld();
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    float f = __uint_as_float(v[j]);
+                    if (c > 0) f += __uint_as_float(r[j]);
+                    const int64_t m = m0 + col + j;
+                    if (col + j < a.ntok && m < a.M) {
+                        if (a.part)
+                            a.part[((int64_t)split * a.M + m) * N + n] = f;
+                        else
+                            a.y[m * N + n] = __float2bfloat16_rn(f);
+                    }
+                }
+            }
+        }
+        if (nkb == 0 && !*abort_flag) {
+            for (int64_t j = 0; j < a.ntok; ++j) {
+                const int64_t m = m0 + j;
+                if (m < a.M) {
+                    if (a.part)
+                        a.part[((int64_t)split * a.M + m) * N + n] = 0.0f;
+                    else
+                        a.y[m * N + n] = __float2bfloat16_rn(0.0f);
+                }
+            }
+        }
+    }
+
+    tc::tc_fence_before();
+    __syncthreads();
+    if (warp == MMA_WARP) {
+        tc::tc_fence_after();
+        tc::tmem_dealloc(tmem, TMEM_COLS);
+    }
+}
+
 // y[m, n] = bf16( sum_s part[s, m, n] ), summed in split order.
 __global__ void k_w4_reduce(const float* __restrict__ part, int nsplit, int64_t MN, __nv_bfloat16* __restrict__ y) {
     for (int64_t i = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) * 4; i < MN; i += (int64_t)gridDim.x * blockDim.x * 4) {
@@ -1087,10 +1429,16 @@ size_t w4a16_ws_bytes(int64_t M, int64_t N, int64_t K) {
     return (size_t)p.nsplit * M * N * sizeof(float);
 }
 
-// 1: force the mma.sync GEMM for M > 16 (comparison); read on every call.
+// QLIN_W4A16_KERNEL=mma forces the mma.sync GEMM for M > 16, =smem the
+// tcgen05 GEMM with the A operand in shared memory (comparisons); read on
+// every call.
 static bool w4_force_mma() {
     const char* e = getenv("QLIN_W4A16_KERNEL");
     return e && strcmp(e, "mma") == 0;
+}
+static bool w4_force_smem_a() {
+    const char* e = getenv("QLIN_W4A16_KERNEL");
+    return e && strcmp(e, "smem") == 0;
 }
 
 // k-blocks per accumulation chain.  The tensor cores' fp32 accumulation loses
@@ -1147,17 +1495,22 @@ cudaError_t run_gemm_w4a16(const void* x, const void* packed, const qlin_w4_head
     a.ntok = plan.ntok;
     a.nchunk = (int)(h->K / 64);
     a.nsplit = plan.nsplit;
-    a.a_stages = w4tc::a_stages(plan.ntok);
-    a.b_stages = w4tc::b_stages(plan.ntok);
+    const bool tmem_a = plan.ntok <= 128 && !w4_force_smem_a();  // A operand in TMEM (k_w4_gemm_tm)
+    a.a_stages = tmem_a ? w4tm::a_stages(plan.ntok) : w4tc::a_stages(plan.ntok);
+    a.b_stages = tmem_a ? w4tm::b_stages(plan.ntok) : w4tc::b_stages(plan.ntok);
     a.promote = w4_promote(plan.ntok);
     a.idesc = tc::idesc_f16(w4tc::BMW, plan.ntok, true);
     a.part = (plan.nsplit > 1) ? reinterpret_cast<float*>(ws) : nullptr;
     a.y = yb;
-    const size_t smem = w4tc::smem_bytes(plan.ntok);
-    cudaError_t e = ensure_smem((const void*)k_w4_gemm_tc, (int)smem);
+    const void* kern = tmem_a ? (const void*)k_w4_gemm_tm : (const void*)k_w4_gemm_tc;
+    const size_t smem = tmem_a ? w4tm::smem_bytes(plan.ntok) : w4tc::smem_bytes(plan.ntok);
+    cudaError_t e = ensure_smem(kern, (int)smem);
     if (e != cudaSuccess) return e;
     dim3 grid((unsigned)(h->N / w4tc::BMW), (unsigned)plan.nsplit, (unsigned)plan.mtiles);
-    k_w4_gemm_tc<<<grid, w4tc::THREADS, smem, st>>>(tmap, a);
+    if (tmem_a)
+        k_w4_gemm_tm<<<grid, w4tm::THREADS, smem, st>>>(tmap, a);
+    else
+        k_w4_gemm_tc<<<grid, w4tc::THREADS, smem, st>>>(tmap, a);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     if (plan.nsplit > 1) {
         int64_t MN = M * h->N;

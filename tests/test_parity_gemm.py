@@ -274,6 +274,27 @@ def test_w4a16_tensor_core_vs_legacy_kernel(M, monkeypatch):
     assert qlin.qlin_device_error() == 0
 
 
+@pytest.mark.parametrize("asym", [False, True])
+@pytest.mark.parametrize("group", [32, 64, 128])
+@pytest.mark.parametrize("M", [17, 64, 100, 128])
+def test_w4a16_tmem_a_matches_smem_a(M, group, asym, monkeypatch):
+    """Up to 128 tokens the converters write the weight tile into TMEM; the
+    shared-memory-operand kernel issues the same MMAs in the same order, so the
+    two give the same bits (K = 2048: chains of 8 k-blocks and a split)."""
+    N, K = 384, 2048
+    w = torch.from_numpy(inputs.normal((N, K), 0.02, 41 + group)).to(torch.bfloat16).cuda()
+    x = torch.from_numpy(inputs.normal((M, K), 1.0, 42 + M)).to(torch.bfloat16).cuda()
+    p, q, s, z, packed, hdr = w4_prepare(w, group, asym)
+    y_tm = qlin.gemm_w4a16(x, packed, hdr)
+    monkeypatch.setenv("QLIN_W4A16_KERNEL", "smem")
+    y_sm = qlin.gemm_w4a16(x, packed, hdr)
+    torch.cuda.synchronize()
+    assert qlin.qlin_device_error() == 0
+    assert torch.equal(y_tm, y_sm)
+    yo = oracle.matmul_f64(host_f32(x), w4_oracle_weight(q, s, z, p, N, K, group))
+    assert rel_err_out(host_f32(y_tm), yo) < GEMM_REL_TOL
+
+
 def test_w4a16_reproducible():
     """Split-K partial sums are added in a fixed order: two calls agree bit for bit."""
     w = torch.from_numpy(inputs.normal((1024, 8192), 0.02, 23)).to(torch.bfloat16).cuda()
