@@ -1033,7 +1033,7 @@ __global__ void __launch_bounds__(w4tc::THREADS, 1) k_w4_gemm_tc(const __grid_co
 namespace w4tm {
 constexpr int BMW = 128;
 constexpr int BK = 64;
-constexpr int NCONV_WARPS = 16;  // warp w: TMEM quarter w % 4, tile half (w >> 2) & 1, k-block parity w >> 3
+constexpr int NCONV_WARPS = 16;  // warp w: TMEM quarter w % 4, tile half (w >> 2) & 1, 64-k half w >> 3 of each stage
 constexpr int EPI_WARP0 = 16;
 constexpr int MMA_WARP = 20;
 constexpr int TMA_WARP = 21;
@@ -1042,21 +1042,27 @@ constexpr uint32_t TMEM_COLS = 512;
 constexpr int B_STAGES_MAX = 16;
 constexpr int BAR_BYTES = 512;
 constexpr size_t SMEM_LIMIT = 232448;
-__host__ __device__ constexpr int b_bytes(int ntok) { return ntok * BK * 2; }
+// A pipeline stage covers 128 k: two 64-k blocks, one per converter half, and
+// two 64-k activation boxes.  One stage costs the MMA warp one wait per
+// operand, 8 MMAs and 2 commits.
+__host__ __device__ constexpr int b_bytes(int ntok) { return ntok * BK * 2; }  // one 64-k box of X
+__host__ __device__ constexpr int b_stage_bytes(int ntok) { return 2 * b_bytes(ntok); }
 // TMEM columns: accumulator b at b * acc_stride, promoted sums at
-// 2 * acc_stride, A stage s (128 lanes x 32 columns = 128 rows x 64 bf16, k
-// pairs packed low-first) at a_col0 + 32 s.
+// 2 * acc_stride, A stage s (128 lanes x 64 columns = 128 rows x 128 bf16, k
+// pairs packed low-first; columns 0-31 hold k 0-63) at a_col0 + 64 s.
 __host__ __device__ inline int acc_stride(int ntok) { return ntok <= 64 ? 64 : 128; }
 __host__ __device__ inline int a_col0(int ntok) { return ntok <= 64 ? 256 : 384; }
-__host__ __device__ inline int a_stages(int ntok) { return ntok <= 64 ? 8 : 4; }
+__host__ __device__ inline int a_stages(int ntok) { return ntok <= 64 ? 4 : 2; }
 constexpr int CRING = 6;  // cp.async ring depth (own k-blocks) of each converter warp
 constexpr int CR_WARP_BYTES = CRING * (512 + 256);  // codes [CRING][32 chunks][16 B] + group words [CRING][32][8 B]
 constexpr int RING_BYTES = NCONV_WARPS * CR_WARP_BYTES;
 inline int b_stages(int ntok) {
-    int s = (int)((SMEM_LIMIT - 1024 - RING_BYTES - BAR_BYTES) / b_bytes(ntok));
+    int s = (int)((SMEM_LIMIT - 1024 - RING_BYTES - BAR_BYTES) / b_stage_bytes(ntok));
     return s < B_STAGES_MAX ? s : B_STAGES_MAX;
 }
-inline size_t smem_bytes(int ntok) { return 1024 + (size_t)b_stages(ntok) * b_bytes(ntok) + RING_BYTES + BAR_BYTES; }
+inline size_t smem_bytes(int ntok) {
+    return 1024 + (size_t)b_stages(ntok) * b_stage_bytes(ntok) + RING_BYTES + BAR_BYTES;
+}
 }  // namespace w4tm
 
 // 16 TMEM lanes x 4 x 256 bits: in repetition r, thread (g = lane / 4, t = lane % 4)
@@ -1087,8 +1093,8 @@ __global__ void __launch_bounds__(w4tm::THREADS, 1) k_w4_gemm_tm(const __grid_co
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
     const int SA = a_stages(a.ntok), SB = a.b_stages;
-    const uint32_t B_BYTES = (uint32_t)b_bytes(a.ntok);
-    uint8_t* tilesB = smem;                                  // [SB][ntok * 128 B], 1024-aligned
+    const uint32_t B_HALF = (uint32_t)b_bytes(a.ntok), B_BYTES = 2u * B_HALF;
+    uint8_t* tilesB = smem;                                  // [SB][2][ntok * 128 B], 1024-aligned
     uint8_t* cring = tilesB + (size_t)SB * B_BYTES;
     uint64_t* bars = reinterpret_cast<uint64_t*>(cring + RING_BYTES);
     volatile uint32_t* misc = reinterpret_cast<volatile uint32_t*>(bars + 2 * SA + 2 * SB + 5);
@@ -1102,6 +1108,7 @@ __global__ void __launch_bounds__(w4tm::THREADS, 1) k_w4_gemm_tm(const __grid_co
     const int c_begin = (int)((int64_t)a.nchunk * split / a.nsplit);
     const int c_end = (int)((int64_t)a.nchunk * (split + 1) / a.nsplit);
     const int nkb = c_end - c_begin;
+    const int nst = (nkb + 1) >> 1;  // stages; with an odd count the last holds one 64-k block
     const uint32_t ACC_STRIDE = (uint32_t)acc_stride(a.ntok), A_COL0 = (uint32_t)a_col0(a.ntok);
 
     const uint32_t bar0 = tc::smem_addr(bars);
@@ -1113,12 +1120,13 @@ __global__ void __launch_bounds__(w4tm::THREADS, 1) k_w4_gemm_tm(const __grid_co
     auto acc_full = [&](int b) { return acc_full0 + 8u * b; };
     auto acc_empty = [&](int b) { return acc_full0 + 16u + 8u * b; };
     const uint32_t done_bar = acc_full0 + 32u;
-    const int chain_len = a.promote > 0 ? a.promote : (nkb > 0 ? nkb : 1);
-    const int nchains = nkb > 0 ? (nkb + chain_len - 1) / chain_len : 0;
+    // chains of a.promote 64-k blocks, rounded up to whole stages
+    const int chain_st = a.promote > 0 ? (a.promote + 1) >> 1 : (nst > 0 ? nst : 1);
+    const int nchains = nst > 0 ? (nst + chain_st - 1) / chain_st : 0;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < SA; ++s) {
-            tc::mbar_init(fullA(s), 8);
+            tc::mbar_init(fullA(s), 16);  // every converter warp, each stage
             tc::mbar_init(emptyA(s), 1);
         }
         for (int s = 0; s < SB; ++s) {
@@ -1143,8 +1151,8 @@ __global__ void __launch_bounds__(w4tm::THREADS, 1) k_w4_gemm_tm(const __grid_co
     const uint32_t tmem = misc[0];
 
     if (warp < NCONV_WARPS) {
-        // Warp w converts the 16-row tile 2 (w % 4) + ((w >> 2) & 1) for the
-        // k-blocks of parity w >> 3 and stores it into its own TMEM quarter.
+        // Warp w converts the 16-row tile 2 (w % 4) + ((w >> 2) & 1), 64-k half
+        // w >> 3 of every stage, and stores it into its own TMEM quarter.
         // Lane (g, t) copies its packed 16 bytes (k 16t .. 16t+15 of rows g and
         // g+8) to ring chunk 8t + g; after the warp's copies land it reads word t
         // of chunks 8r + g, r = 0..3, i.e. k 16r + 4t .. 16r + 4t + 3, which is
@@ -1179,9 +1187,13 @@ __global__ void __launch_bounds__(w4tm::THREADS, 1) k_w4_gemm_tm(const __grid_co
         };
 #pragma unroll 1
         for (int i = 0; i < CRING - 1; ++i) issue();
-        int s = par, slot = 0;
+        int s = 0, slot = 0;
         uint32_t ph = 0u;
-        for (int kb = par; kb < nkb; kb += 2) {
+        for (int st_i = 0; st_i < nst; ++st_i) {
+            // With an odd k-block count the second half of the last stage is
+            // empty: those warps still take the stage (wait, arrive) so that
+            // its barrier phase completes, but store nothing.
+            const bool has = 2 * st_i + par < nkb;
             issue();
             cp_async_wait<CRING - 1>();
             __syncwarp();  // the other lanes' copies of this slot have landed
@@ -1223,28 +1235,31 @@ __global__ void __launch_bounds__(w4tm::THREADS, 1) k_w4_gemm_tm(const __grid_co
             }
             if (!tc::mbar_wait_warp(emptyA(s), ph ^ 1u, abort_flag)) break;
             tc::tc_fence_after();
-            tmem_st_16x256b_x4(tmem + t_lane + A_COL0 + 32u * (uint32_t)s, st);
-            tc::tmem_wait_st();
+            if (has) {
+                tmem_st_16x256b_x4(tmem + t_lane + A_COL0 + 64u * (uint32_t)s + 32u * (uint32_t)par, st);
+                tc::tmem_wait_st();
+            }
             tc::tc_fence_before();
             __syncwarp();
             if (lane == 0) tc::mbar_arrive(fullA(s));
-            s += 2;
-            if (s >= SA) {
-                s -= SA;
+            if (++s == SA) {
+                s = 0;
                 ph ^= 1u;
             }
         }
         cp_async_wait<0>();
     } else if (warp == TMA_WARP) {
         if (lane == 0) {
-            const uint32_t tx = (uint32_t)a.ntok * BK * 2;
             int s = 0;
             uint32_t ph = 0;
-            for (int kb = 0; kb < nkb; ++kb) {
+            for (int st_i = 0; st_i < nst; ++st_i) {
+                const int nh = 2 * st_i + 1 < nkb ? 2 : 1;  // 64-k boxes in this stage
                 if (!tc::mbar_wait(emptyB(s), ph ^ 1u, abort_flag)) break;
-                tc::mbar_arrive_expect_tx(fullB(s), tx);
+                tc::mbar_arrive_expect_tx(fullB(s), (uint32_t)nh * B_HALF);
                 const uint32_t dstB = tc::smem_addr(tilesB + (size_t)s * B_BYTES);
-                tc::tma_load_2d(dstB, &tmx, (c_begin + kb) * BK, (int)m0, fullB(s));
+                for (int hh = 0; hh < nh; ++hh)
+                    tc::tma_load_2d(dstB + (uint32_t)hh * B_HALF, &tmx, (c_begin + 2 * st_i + hh) * BK, (int)m0,
+                                    fullB(s));
                 if (++s == SB) {
                     s = 0;
                     ph ^= 1u;
@@ -1257,10 +1272,10 @@ __global__ void __launch_bounds__(w4tm::THREADS, 1) k_w4_gemm_tm(const __grid_co
         int c = 0, in_chain = 0;
         int s = 0, sb = 0;
         uint32_t ph = 0, phb = 0;
-        for (int kb = 0; kb < nkb; ++kb) {
+        for (int st_i = 0; st_i < nst; ++st_i) {
             if (!tc::mbar_wait_warp(fullB(sb), phb, abort_flag)) break;
             if (!tc::mbar_wait_warp(fullA(s), ph, abort_flag)) break;
-            if (in_chain == chain_len) {
+            if (in_chain == chain_st) {
                 if (tc::elect_one()) tc::mma_commit(acc_full(c & 1));
                 __syncwarp();
                 ++c;
@@ -1268,13 +1283,17 @@ __global__ void __launch_bounds__(w4tm::THREADS, 1) k_w4_gemm_tm(const __grid_co
                 if (c >= 2 && !tc::mbar_wait_warp(acc_empty(c & 1), ((c >> 1) - 1) & 1u, abort_flag)) break;
             }
             tc::tc_fence_after();
-            const uint64_t bd = tc::desc_sw128(tB_addr + (uint32_t)sb * B_BYTES);
-            const uint32_t at = tmem + A_COL0 + 32u * (uint32_t)s;
+            const int nh = 2 * st_i + 1 < nkb ? 2 : 1;
+            const uint32_t at = tmem + A_COL0 + 64u * (uint32_t)s;
             const uint32_t dacc = tmem + ACC_STRIDE * (uint32_t)(c & 1);
             if (tc::elect_one()) {
+                for (int hh = 0; hh < nh; ++hh) {
+                    const uint64_t bd = tc::desc_sw128(tB_addr + (uint32_t)sb * B_BYTES + (uint32_t)hh * B_HALF);
 #pragma unroll
-                for (int j = 0; j < BK / 16; ++j)
-                    mma_f16_tmem_a(dacc, at + 8u * j, bd + 2 * j, a.idesc, (in_chain > 0 || j > 0) ? 1u : 0u);
+                    for (int j = 0; j < BK / 16; ++j)
+                        mma_f16_tmem_a(dacc, at + 32u * hh + 8u * j, bd + 2 * j, a.idesc,
+                                       (in_chain > 0 || hh > 0 || j > 0) ? 1u : 0u);
+                }
                 tc::mma_commit(emptyA(s));
                 tc::mma_commit(emptyB(sb));
             }
@@ -1290,7 +1309,7 @@ __global__ void __launch_bounds__(w4tm::THREADS, 1) k_w4_gemm_tm(const __grid_co
             }
         }
         if (tc::elect_one()) {
-            if (nkb > 0) tc::mma_commit(acc_full(c & 1));
+            if (nst > 0) tc::mma_commit(acc_full(c & 1));  // the last chain
             tc::mma_commit(done_bar);
         }
         __syncwarp();

@@ -295,6 +295,25 @@ def test_w4a16_tmem_a_matches_smem_a(M, group, asym, monkeypatch):
     assert rel_err_out(host_f32(y_tm), yo) < GEMM_REL_TOL
 
 
+@pytest.mark.parametrize("M", [17, 64])
+def test_w4a16_tmem_a_odd_k_block_count(M, monkeypatch):
+    """K = 1088 is 17 blocks of 64 k, split 8 + 9: the last 128-k stage of a
+    split holds a single block.  Same bits as the shared-memory kernel, which
+    steps one 64-k block at a time."""
+    N, K = 256, 1088
+    w = torch.from_numpy(inputs.normal((N, K), 0.02, 51)).to(torch.bfloat16).cuda()
+    x = torch.from_numpy(inputs.normal((M, K), 1.0, 52)).to(torch.bfloat16).cuda()
+    p, q, s, z, packed, hdr = w4_prepare(w, 64, True)
+    y_tm = qlin.gemm_w4a16(x, packed, hdr)
+    monkeypatch.setenv("QLIN_W4A16_KERNEL", "smem")
+    y_sm = qlin.gemm_w4a16(x, packed, hdr)
+    torch.cuda.synchronize()
+    assert qlin.qlin_device_error() == 0
+    assert torch.equal(y_tm, y_sm)
+    yo = oracle.matmul_f64(host_f32(x), w4_oracle_weight(q, s, z, p, N, K, 64))
+    assert rel_err_out(host_f32(y_tm), yo) < GEMM_REL_TOL
+
+
 def test_w4a16_reproducible():
     """Split-K partial sums are added in a fixed order: two calls agree bit for bit."""
     w = torch.from_numpy(inputs.normal((1024, 8192), 0.02, 23)).to(torch.bfloat16).cuda()
