@@ -1023,13 +1023,15 @@ __global__ void __launch_bounds__(w4tc::THREADS, 1) k_w4_gemm_tc(const __grid_co
 }
 
 // ------------------------------------------------------------------ W4A16 GEMM, A operand in TMEM (M <= 128 per CTA)
-// The same roles and pipeline as k_w4_gemm_tc, but the converters write the
-// dequantized weight tile into tensor memory with tcgen05.st and the MMA reads
-// A from there (tcgen05.mma with an [a-tmem] operand).  That takes the 16 KB
-// store of each k-block and the tensor core's 16 KB read of it off the
-// shared-memory ports, which bound the shared-memory version at these sizes.
-// TMEM holds everything for up to 128 tokens: two accumulators, the promoted
-// sums and 4 (or 8, for <= 64 tokens) A stages of 32 columns.
+// The same roles as k_w4_gemm_tc, but the converters write the dequantized
+// weight tile into tensor memory with tcgen05.st and the MMA reads A from there
+// (tcgen05.mma with an [a-tmem] operand).  That takes the 16 KB store of each
+// 64-k block and the tensor core's 16 KB read of it off the shared-memory
+// ports, which bound the shared-memory version at these sizes.  Stages cover
+// 128 k, so the single MMA-issuing warp pays its waits and commits once per
+// two 64-k blocks.  TMEM holds everything for up to 128 tokens: two
+// accumulators, the promoted sums and 2 (or 4, for <= 64 tokens) A stages of
+// 64 columns.
 namespace w4tm {
 constexpr int BMW = 128;
 constexpr int BK = 64;
