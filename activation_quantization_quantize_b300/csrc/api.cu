@@ -64,6 +64,28 @@ int check_qparams(const qlin_qparams* p, int64_t rows, int64_t cols) {
 
 }  // namespace
 
+namespace qlin {
+
+// Every argument check of qlin_quantize except the workspace: QLIN_OK,
+// QLIN_NOTHING_TO_DO (valid, empty input) or a negative qlin_status.
+int quantize_check(const void* x, int xt, int64_t rows, int64_t cols, int64_t ld, const float* smooth,
+                   const qlin_qparams* p, const void* q, const void* s, const int32_t* z) {
+    int rc = check_qparams(p, rows, cols);
+    if (rc != QLIN_OK) return rc;
+    if (!is_float_type(xt) || ld < cols) return QLIN_ERR_ARG;
+    if (rows == 0 || cols == 0) return QLIN_NOTHING_TO_DO;
+    if (!x || !q || !s) return QLIN_ERR_ARG;
+    if (!p->symmetric && !z) return QLIN_ERR_ARG;
+    if (p->smooth_mode != QLIN_SMOOTH_NONE && !smooth) return QLIN_ERR_ARG;
+    if (!aligned(x, type_bytes(xt)) || !aligned(s, p->scale_dtype == QLIN_F16 ? 2 : 4) || (z && !aligned(z, 4)))
+        return QLIN_ERR_ARG;
+    if (p->clip_percentile > 0.0 && (!p->symmetric || p->gran != QLIN_PER_TENSOR)) return QLIN_ERR_UNSUPPORTED;
+    if (p->static_scale && p->clip_percentile > 0.0) return QLIN_ERR_ARG;
+    return QLIN_OK;
+}
+
+}  // namespace qlin
+
 extern "C" {
 
 int qlin_version(void) { return 10000; }
@@ -101,17 +123,9 @@ size_t qlin_workspace_size(int op, int64_t M, int64_t N, int64_t K, const qlin_q
 
 int qlin_quantize(const void* x, qlin_dtype xt, int64_t rows, int64_t cols, int64_t ld, const float* smooth,
                   const qlin_qparams* p, void* q, void* s, int32_t* z, void* ws, size_t ws_bytes, void* stream) {
-    int rc = check_qparams(p, rows, cols);
+    int rc = quantize_check(x, xt, rows, cols, ld, smooth, p, q, s, z);
+    if (rc == QLIN_NOTHING_TO_DO) return QLIN_OK;
     if (rc != QLIN_OK) return rc;
-    if (!is_float_type(xt) || ld < cols) return QLIN_ERR_ARG;
-    if (rows == 0 || cols == 0) return QLIN_OK;
-    if (!x || !q || !s) return QLIN_ERR_ARG;
-    if (!p->symmetric && !z) return QLIN_ERR_ARG;
-    if (p->smooth_mode != QLIN_SMOOTH_NONE && !smooth) return QLIN_ERR_ARG;
-    if (!aligned(x, type_bytes(xt)) || !aligned(s, p->scale_dtype == QLIN_F16 ? 2 : 4) || (z && !aligned(z, 4)))
-        return QLIN_ERR_ARG;
-    if (p->clip_percentile > 0.0 && (!p->symmetric || p->gran != QLIN_PER_TENSOR)) return QLIN_ERR_UNSUPPORTED;
-    if (p->static_scale && p->clip_percentile > 0.0) return QLIN_ERR_ARG;
     size_t need = quantize_ws_bytes(rows, cols, p);
     if (need > 0 && (!ws || ws_bytes < need || !aligned(ws, 16))) return QLIN_ERR_WORKSPACE;
     return cuda_status(run_quantize(x, xt, rows, cols, ld, smooth, p, q, s, z, ws, (cudaStream_t)stream));
@@ -211,6 +225,16 @@ int qlin_gemm_w4a16(const void* x, const void* packed, const qlin_w4_header* hdr
     size_t need = w4a16_ws_bytes(M, hdr->N, hdr->K);
     if (need > 0 && (!ws || ws_bytes < need || !aligned(ws, 16))) return QLIN_ERR_WORKSPACE;
     return cuda_status(run_gemm_w4a16(x, packed, hdr, M, y, ws, (cudaStream_t)stream));
+}
+
+int qlin_debug_stall_producers(int enable, long long wait_limit_cycles) {
+    if (enable && wait_limit_cycles <= 0) return QLIN_ERR_ARG;
+    const int stall = enable ? 1 : 0;
+    const long long limit = enable ? wait_limit_cycles : kDefaultWaitLimitCycles;
+    if (cudaDeviceSynchronize() != cudaSuccess) return QLIN_ERR_CUDA;
+    if (cudaMemcpyToSymbol(g_wait_limit_cycles, &limit, sizeof limit) != cudaSuccess) return QLIN_ERR_CUDA;
+    if (cudaMemcpyToSymbol(g_stall_producers, &stall, sizeof stall) != cudaSuccess) return QLIN_ERR_CUDA;
+    return cudaDeviceSynchronize() == cudaSuccess ? QLIN_OK : QLIN_ERR_CUDA;
 }
 
 int qlin_device_error(void* stream) {

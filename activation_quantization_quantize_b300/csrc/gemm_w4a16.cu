@@ -885,7 +885,7 @@ __global__ void __launch_bounds__(w4tc::THREADS, 1) k_w4_gemm_tc(const __grid_co
         cp_async_wait<0>();
     } else if (warp == TMA_WARP) {
         // ---------------------------------------------------------- activation tiles (TMA)
-        if (lane == 0) {
+        if (lane == 0 && !tc::producers_stalled()) {
             const uint32_t tx = (uint32_t)a.ntok * BK * 2;
             int s = 0;
             uint32_t ph = 0;
@@ -950,7 +950,8 @@ __global__ void __launch_bounds__(w4tc::THREADS, 1) k_w4_gemm_tc(const __grid_co
             tc::mma_commit(done_bar);
         }
         __syncwarp();
-        tc::mbar_wait_warp(done_bar, 0, abort_flag);
+        tc::mbar_wait_drain(done_bar, 0);
+        __syncwarp();
     } else {
         // ---------------------------------------------------------- promotions + epilogue
         const int q = warp & 3;
@@ -1251,7 +1252,7 @@ __global__ void __launch_bounds__(w4tm::THREADS, 1) k_w4_gemm_tm(const __grid_co
         }
         cp_async_wait<0>();
     } else if (warp == TMA_WARP) {
-        if (lane == 0) {
+        if (lane == 0 && !tc::producers_stalled()) {
             int s = 0;
             uint32_t ph = 0;
             for (int st_i = 0; st_i < nst; ++st_i) {
@@ -1315,7 +1316,8 @@ __global__ void __launch_bounds__(w4tm::THREADS, 1) k_w4_gemm_tm(const __grid_co
             tc::mma_commit(done_bar);
         }
         __syncwarp();
-        tc::mbar_wait_warp(done_bar, 0, abort_flag);
+        tc::mbar_wait_drain(done_bar, 0);
+        __syncwarp();
     } else {
         const int q = warp & 3;
         const uint32_t lane_base = (uint32_t)(32 * q) << 16;
@@ -1467,13 +1469,10 @@ static bool w4_force_smem_a() {
 // error near 2e-5 of the output scale, every 32 near 2e-4 (8192 x 28672 UINT4).
 // With ntok <= 128 two TMEM accumulators alternate and promotion does not
 // stall the MMAs; above that one accumulator must be drained in place, so the
-// chains are longer.  QLIN_W4A16_PROMOTE overrides (0: one chain); read on
-// every call.
-static int w4_promote(int ntok) {
-    const char* e = getenv("QLIN_W4A16_PROMOTE");
-    if (e) return atoi(e);
-    return ntok <= 128 ? 8 : 32;
-}
+// chains are longer.  Both lengths are even, so the TMEM-operand kernel
+// (128-k stages) and the shared-memory-operand kernel (64-k blocks) promote
+// after the same k-blocks and give the same bits.
+static int w4_promote(int ntok) { return ntok <= 128 ? 8 : 32; }
 
 cudaError_t run_gemm_w4a16(const void* x, const void* packed, const qlin_w4_header* h, int64_t M, void* y, void* ws,
                            cudaStream_t st) {

@@ -444,7 +444,7 @@ __global__ void __launch_bounds__(w8tc::THREADS, 1)
         }
     } else if (warp == TMA_WARP) {
         // ---------------------------------------------------------- int8 tile loads
-        if (lane == 0) {
+        if (lane == 0 && !tc::producers_stalled()) {
             for (int kb = 0; kb < nkb; ++kb) {
                 const int s8 = kb % S8;
                 const uint32_t ph8 = (uint32_t)(kb / S8) & 1u;
@@ -525,7 +525,8 @@ __global__ void __launch_bounds__(w8tc::THREADS, 1)
             tc::mma_commit(done_bar);
         }
         __syncwarp();
-        tc::mbar_wait_warp(done_bar, 0, abort_flag);
+        tc::mbar_wait_drain(done_bar, 0);
+        __syncwarp();
     } else {
         // ---------------------------------------------------------- drains + epilogue
         const int q = warp & 3;  // TMEM lane quarter of this warp

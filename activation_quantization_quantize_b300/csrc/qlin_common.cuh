@@ -23,6 +23,14 @@ __device__ int g_device_error = 0;
 
 __device__ __forceinline__ void raise_device_error(int code) { atomicExch(&g_device_error, code); }
 
+// Cycle limit of every bounded device-side wait (about 2 s at 2 GHz).
+constexpr long long kDefaultWaitLimitCycles = 4000000000LL;
+__device__ long long g_wait_limit_cycles = kDefaultWaitLimitCycles;
+// Failure-detection test hook (qlin_debug_stall_producers): while non-zero,
+// the producer roles of the pipelined kernels issue no copies, so the
+// consumers' bounded waits run out and the kernels take their abort path.
+__device__ int g_stall_producers = 0;
+
 // ---------------------------------------------------------------- loads / stores
 template <typename T>
 __device__ __forceinline__ float to_f32(T v);

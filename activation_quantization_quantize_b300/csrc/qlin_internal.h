@@ -18,6 +18,11 @@ int64_t percentile_rank(int64_t n, double p);
 cudaError_t ensure_smem(const void* kernel, int bytes);
 
 size_t quantize_ws_bytes(int64_t rows, int64_t cols, const qlin_qparams* p);
+// Argument checks of qlin_quantize (all but the workspace); returns QLIN_OK,
+// QLIN_NOTHING_TO_DO for a valid empty input, or a negative qlin_status.
+constexpr int QLIN_NOTHING_TO_DO = 1;
+int quantize_check(const void* x, int xt, int64_t rows, int64_t cols, int64_t ld, const float* smooth,
+                   const qlin_qparams* p, const void* q, const void* s, const int32_t* z);
 cudaError_t run_quantize(const void* x, int xt, int64_t rows, int64_t cols, int64_t ld, const float* smooth,
                          const qlin_qparams* p, void* q, void* s, int32_t* z, void* ws, cudaStream_t st);
 cudaError_t run_absmax(const void* x, int xt, int64_t rows, int64_t cols, int64_t ld, int gran, int group,

@@ -384,7 +384,8 @@ __global__ void __launch_bounds__(kBulkThreads, 1) k_quant_rows_bulk(QuantArgs a
         tc::mbar_arrive_expect_tx(bar0 + 8u * b, row_bytes);
         tc::bulk_load(buf0 + (uint32_t)b * buf_stride, xg + r * a.ld * 2, row_bytes, bar0 + 8u * b);
     };
-    if (tid == 0) {
+    const bool stalled = tc::producers_stalled();
+    if (tid == 0 && !stalled) {
         for (int b = 0; b < nbuf; ++b)
             if (blockIdx.x + (int64_t)b * gridDim.x < a.rows) issue(blockIdx.x + (int64_t)b * gridDim.x, b);
     }
@@ -461,7 +462,7 @@ __global__ void __launch_bounds__(kBulkThreads, 1) k_quant_rows_bulk(QuantArgs a
             }
         }
         __syncthreads();  // buffer b and red_* are free
-        if (tid == 0 && r + (int64_t)nbuf * gridDim.x < a.rows) issue(r + (int64_t)nbuf * gridDim.x, b);
+        if (tid == 0 && !stalled && r + (int64_t)nbuf * gridDim.x < a.rows) issue(r + (int64_t)nbuf * gridDim.x, b);
         if (++b == nbuf) {
             b = 0;
             ph ^= 1u;
@@ -707,6 +708,57 @@ __device__ __forceinline__ float load_smoothed(const QuantArgs& a, int64_t r, in
     if (a.smooth_mode == QLIN_SMOOTH_DIVIDE) return __fdiv_rn(v, a.smooth[c]);
     if (a.smooth_mode == QLIN_SMOOTH_MULTIPLY) return v * a.smooth[c];
     return v;
+}
+
+// Row-local scopes (per-row, per-group) of rows the vector kernels cannot
+// take (unaligned, odd lengths, very long rows): one CTA per scope reduces its
+// range and writes the stored scale and zero point straight into the caller's
+// s / z (or the statistic into absmax_out), so no workspace is needed; the
+// codes then come from k_quant_generic.
+template <typename T>
+__global__ void __launch_bounds__(256) k_scope_stats(QuantArgs a) {
+    const bool grp = a.gran == QLIN_PER_GROUP;
+    const int64_t ngr = grp ? a.cols / a.group : 1;
+    const int64_t len = grp ? a.group : a.cols;
+    const int64_t nsc = a.rows * ngr;
+    __shared__ float red_hi[8], red_lo[8];
+    const int tid = threadIdx.x;
+    for (int64_t sc = blockIdx.x; sc < nsc; sc += gridDim.x) {
+        const int64_t r = sc / ngr, c0 = (sc - r * ngr) * len;
+        float hi = 0.0f, lo = 0.0f;
+        for (int64_t i = tid; i < len; i += blockDim.x) {
+            const float v = load_smoothed<T>(a, r, c0 + i);
+            if (a.sym) {
+                hi = fmaxf(hi, fabsf(v));
+            } else {
+                hi = fmaxf(hi, v);
+                lo = fminf(lo, v);
+            }
+        }
+        hi = warp_max(hi);
+        lo = warp_min(lo);
+        if ((tid & 31) == 0) {
+            red_hi[tid >> 5] = hi;
+            red_lo[tid >> 5] = lo;
+        }
+        __syncthreads();
+        if (tid == 0) {
+            for (int w = 1; w < (int)(blockDim.x >> 5); ++w) {
+                hi = fmaxf(hi, red_hi[w]);
+                lo = fminf(lo, red_lo[w]);
+            }
+            if (a.absmax_out) {
+                a.absmax_out[sc] = hi;
+            } else {
+                float s;
+                int z;
+                scale_zero(lo, hi, a.qmin, a.qmax, a.sym, a.scale_f16, s, z);
+                store_scale(a.s, sc, a.scale_f16, s);
+                if (a.z) a.z[sc] = z;
+            }
+        }
+        __syncthreads();  // red_* are reused by the next scope
+    }
 }
 
 template <typename T>
@@ -1172,10 +1224,9 @@ size_t quantize_ws_bytes(int64_t rows, int64_t cols, const qlin_qparams* p) {
     if (p->clip_percentile > 0.0) return (size_t)(kHist1 + kHist2 + 4) * 4;
     if (p->gran == QLIN_PER_TENSOR) return 2 * 4;
     if (p->gran == QLIN_PER_COL) return (size_t)cols * 2 * 4;
-    // per-row / per-group: the fused row kernel needs nothing; the generic
-    // fallback needs one pair of words per scope.
-    int64_t ns = (p->gran == QLIN_PER_ROW) ? rows : (p->group > 0 ? rows * (cols / p->group) : 0);
-    return (size_t)ns * 2 * 4;
+    // per-row / per-group: every kernel that serves these scopes (the fused
+    // row kernels and k_scope_stats) keeps its statistics on chip
+    return 0;
 }
 
 template <typename T>
@@ -1224,7 +1275,21 @@ static cudaError_t run_quantize_t(QuantArgs a, int xt, const qlin_qparams* p, vo
         return launch_rows<T>(a, st);
     }
 
-    // Stats (dynamic) -> finalize -> codes.
+    if (row_local) {
+        // rows the vector kernels cannot take: per-scope statistics straight
+        // into s / z, then scalar codes
+        if (!a.static_scale) {
+            int64_t nsc = nscopes_of(a);
+            int64_t grid = nsc < (int64_t)gblocks * 2 ? nsc : (int64_t)gblocks * 2;
+            k_scope_stats<T><<<(unsigned)grid, 256, 0, st>>>(a);
+            if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        }
+        if (a.absmax_out) return cudaSuccess;
+        k_quant_generic<T><<<gblocks, 256, 0, st>>>(a);
+        return cudaGetLastError();
+    }
+
+    // Per-tensor / per-column: stats (dynamic) -> finalize -> codes.
     if (!a.static_scale) {
         uint32_t* stat = reinterpret_cast<uint32_t*>(ws);
         if (p->clip_percentile > 0.0) {
@@ -1233,7 +1298,7 @@ static cudaError_t run_quantize_t(QuantArgs a, int xt, const qlin_qparams* p, vo
             uint32_t* sel = hist2 + kHist2;
             uint64_t k = (uint64_t)percentile_rank(n, p->clip_percentile);
             if ((e = cudaMemsetAsync(ws, 0, (size_t)(kHist1 + kHist2 + 4) * 4, st)) != cudaSuccess) return e;
-            ensure_smem((const void*)k_hist1<T>, kHist1 * 4);
+            if ((e = ensure_smem((const void*)k_hist1<T>, kHist1 * 4)) != cudaSuccess) return e;
             k_hist1<T><<<num_sms(), 1024, kHist1 * 4, st>>>(a, hist1);
             // Low 16 bits of |x| are zero for unsmoothed bf16 input.
             bool need2 = !(xt == QLIN_BF16 && a.smooth_mode == QLIN_SMOOTH_NONE);
@@ -1245,7 +1310,7 @@ static cudaError_t run_quantize_t(QuantArgs a, int xt, const qlin_qparams* p, vo
         } else {
             int64_t ns = nscopes_of(a);
             if ((e = cudaMemsetAsync(ws, 0, (size_t)ns * 8, st)) != cudaSuccess) return e;
-            if (!row_local && strip_ok(a, xt)) {
+            if (strip_ok(a, xt)) {
                 dim3 grid;
                 int rpb;
                 strip_grid(a.cols / 8, a.rows, grid, rpb);
@@ -1258,7 +1323,7 @@ static cudaError_t run_quantize_t(QuantArgs a, int xt, const qlin_qparams* p, vo
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
     if (a.absmax_out) return cudaGetLastError();
-    if (!row_local && strip_ok(a, xt)) {
+    if (strip_ok(a, xt)) {
         dim3 grid;
         int rpb;
         strip_grid(a.cols / 8, a.rows, grid, rpb);

@@ -39,23 +39,45 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 }
 
 // Bounded wait for the phase of parity `parity` to complete.  Returns false
-// (and raises the abort flag / device error) after ~`limit_cycles`.
-constexpr long long kWaitLimitCycles = 4000000000LL;  // ~2 s at 2 GHz
-
+// when the CTA's abort flag is up, or after g_wait_limit_cycles (then it
+// raises the abort flag and records QLIN_ERR_TIMEOUT in the device error word).
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
     if (mbar_try_wait(bar, parity)) return true;
+    const long long limit = *reinterpret_cast<volatile long long*>(&g_wait_limit_cycles);
     long long t0 = clock64();
     for (uint32_t i = 1;; ++i) {
         if (mbar_try_wait(bar, parity)) return true;
         if ((i & 255u) == 0) {
             if (*abort_flag) return false;
-            if (clock64() - t0 > kWaitLimitCycles) {
+            if (clock64() - t0 > limit) {
                 *abort_flag = 1;
                 raise_device_error(QLIN_ERR_TIMEOUT);
                 return false;
             }
         }
     }
+}
+
+// Bounded wait that ignores the abort flag: the MMA issuer's last wait, for
+// the commit that covers every MMA it issued.  Those MMAs depend on nothing
+// else, so the commit arrives even after an abort, and TMEM is freed only
+// once no MMA can still write it.
+__device__ __forceinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const long long limit = *reinterpret_cast<volatile long long*>(&g_wait_limit_cycles);
+    long long t0 = clock64();
+    for (uint32_t i = 1;; ++i) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((i & 255u) == 0 && clock64() - t0 > limit) {
+            raise_device_error(QLIN_ERR_TIMEOUT);
+            return false;
+        }
+    }
+}
+
+// True while the failure-detection test hook holds the producers back.
+__device__ __forceinline__ bool producers_stalled() {
+    return *reinterpret_cast<volatile int*>(&g_stall_producers) != 0;
 }
 
 // Warp-uniform bounded wait: every lane waits, and the warp agrees on the

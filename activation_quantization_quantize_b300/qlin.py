@@ -74,6 +74,8 @@ def load():
         L.qlin_gemm_w8a8.argtypes = [_P, _P, _P, _P, _I64, _I64, _I64, _P, C.c_int, _P, _P, C.c_size_t, _P]
         L.qlin_gemm_w4a16.argtypes = [_P, _P, C.POINTER(qlin_w4_header), _I64, _P, _P, C.c_size_t, _P]
         L.qlin_device_error.argtypes = [_P]
+        L.qlin_debug_stall_producers.argtypes = [C.c_int, C.c_longlong]
+        L.qlin_debug_stall_producers.restype = C.c_int
         L.qlin_quantize_noalloc.argtypes = [_P, C.c_int, _I64, _I64, _I64, _P, C.POINTER(qlin_qparams),
                                             _P, _P, _P, _P]
         L.qlin_quantize_noalloc.restype = C.c_int
@@ -173,6 +175,11 @@ def qlin_quantize_noalloc(x, xt, rows, cols, ld, smooth, p, q, s, z, stream=None
 
 def qlin_device_error(stream=None):
     return load().qlin_device_error(_stream(stream))
+
+
+def qlin_debug_stall_producers(enable, wait_limit_cycles=0):
+    return _check("qlin_debug_stall_producers", load().qlin_debug_stall_producers(1 if enable else 0,
+                                                                                 int(wait_limit_cycles)))
 
 
 # ----------------------------------------------------------------------------- conveniences

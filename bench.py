@@ -200,6 +200,9 @@ class Step:
         self.ws_q_bytes = nb
         self.y8 = torch.empty((M8, N), dtype=torch.bfloat16, device=dev)
         self.y4 = [torch.empty((m, N), dtype=torch.bfloat16, device=dev) for m in W4_MS]
+        # buffer sets of the step's inputs and outputs: set 0 is the above; the
+        # end-to-end run adds a second so that copies overlap the compute
+        self.sets = [(self.x, self.xs, self.y8, self.y4)]
         self.xhat = torch.empty((M8, K), dtype=torch.bfloat16, device=dev)
         self.ws4 = []
         for m in W4_MS:
@@ -220,22 +223,30 @@ class Step:
         w8 = 1 + (1 if self.ws8_bytes > drain_bytes else 0)
         return 1 + w8 + sum(1 + (1 if nb4 > 0 else 0) for _, nb4 in self.ws4) + 1
 
-    def run(self, stream, events=None):
-        """Enqueue one step; events (len 8) bracket each kernel if given."""
+    def add_buffer_set(self):
+        dev = self.dev
+        self.sets.append((torch.empty_like(self.x), [torch.empty_like(t) for t in self.xs],
+                          torch.empty_like(self.y8), [torch.empty_like(t) for t in self.y4]))
+
+    def run(self, stream, events=None, buf=0):
+        """Enqueue one step on buffer set `buf`; events (len 8) bracket each
+        kernel if given."""
+        x, xs, y8, y4 = self.sets[buf]
+
         def ev(i):
             if events is not None:
                 events[i].record(stream)
         ev(0)
-        qlin.qlin_quantize(self.x, qlin.QLIN_BF16, M8, K, K, None, self.px, self.qx, self.sx, None,
+        qlin.qlin_quantize(x, qlin.QLIN_BF16, M8, K, K, None, self.px, self.qx, self.sx, None,
                            self.ws_q, self.ws_q_bytes, stream)
         ev(1)
-        qlin.qlin_gemm_w8a8(self.qx, self.sx, self.qw, self.sw, M8, N, K, self.y8, qlin.QLIN_BF16, None,
+        qlin.qlin_gemm_w8a8(self.qx, self.sx, self.qw, self.sw, M8, N, K, y8, qlin.QLIN_BF16, None,
                             self.ws8, self.ws8_bytes, stream)
         ev(2)
         for i, m in enumerate(W4_MS):
             packed, hdr = self.w4[i % len(self.w4)]
             ws4, nb4 = self.ws4[i]
-            qlin.qlin_gemm_w4a16(self.xs[i], packed, hdr, m, self.y4[i], ws4, nb4, stream)
+            qlin.qlin_gemm_w4a16(xs[i], packed, hdr, m, y4[i], ws4, nb4, stream)
             ev(3 + i)
         qlin.qlin_dequantize(self.qx, self.sx, None, self.px, M8, K, self.xhat, qlin.QLIN_BF16, stream)
         ev(7)
@@ -352,10 +363,13 @@ def measure_other_configs(dev, peaks, int8_peak):
     out["w8a8_prefill_%dx%dx%d" % (Mp, Np, Kp)] = {"us": t * 1e6, "tops": ops / t / 1e12,
                                                    "roofline_frac": ops / (int8_peak * 1e12) / t}
     del ring, qx, qw, xd, wd, x, w
-    # quantize / dequantize sweep
+    # quantize / dequantize sweep: every timed call reads a distinct copy of
+    # its input from a ring of at least 4 x L2
     xs = inputs.sweep_tensor().to(dev)
     R_, C_ = xs.shape
-    sweep = {}
+    n_ring = -(-ring_bytes // (R_ * C_ * 2))
+    xring = [xs] + [xs.clone() for _ in range(n_ring - 1)]
+    sweep = {"ring": "%d input copies (%.0f MB) rotated per call" % (n_ring, n_ring * R_ * C_ * 2 / 1e6)}
     modes = [("s8", "tensor", 0), ("s8", "row", 0), ("s8", "col", 0), ("s8", "group", 32), ("s8", "group", 64),
              ("s8", "group", 128), ("s4", "tensor", 0), ("s4", "row", 0), ("s4", "group", 128), ("u8", "tensor", 0),
              ("u8", "row", 0), ("u8", "col", 0), ("u8", "group", 128)]
@@ -364,13 +378,18 @@ def measure_other_configs(dev, peaks, int8_peak):
         q, s_, z_ = qlin.quantize(xs, p)
         nb = qlin.qlin_workspace_size(qlin.QLIN_OP_QUANTIZE, R_, C_, 0, p)
         ws = torch.empty(max(nb, 16), dtype=torch.uint8, device=dev)
-        t = _time_calls(lambda i: qlin.qlin_quantize(xs, qlin.QLIN_BF16, R_, C_, C_, None, p, q, s_, z_, ws, nb, None))
+        t = _time_calls(lambda i: qlin.qlin_quantize(xring[i % n_ring], qlin.QLIN_BF16, R_, C_, C_, None, p, q, s_,
+                                                     z_, ws, nb, None))
         b = R_ * C_ * 2 + q.numel() + s_.numel() * s_.element_size() + (0 if z_ is None else z_.numel() * 4)
         key = "quantize_%s_%s%s" % (code, gran, g if g else "")
         sweep[key] = {"us": t * 1e6, "gbs": b / t / 1e9, "roofline_frac": b / hbm / t}
         if (code, gran) in (("s8", "row"), ("s4", "group")):
             yq = torch.empty((R_, C_), dtype=torch.bfloat16, device=dev)
-            t = _time_calls(lambda i: qlin.qlin_dequantize(q, s_, z_, p, R_, C_, yq, qlin.QLIN_BF16, None))
+            nq = -(-ring_bytes // q.numel())
+            qring = [q] + [q.clone() for _ in range(nq - 1)]
+            t = _time_calls(lambda i: qlin.qlin_dequantize(qring[i % nq], s_, z_, p, R_, C_, yq, qlin.QLIN_BF16,
+                                                           None))
+            del qring
             b = q.numel() + s_.numel() * s_.element_size() + R_ * C_ * 2
             sweep["dequantize_%s_%s%s" % (code, gran, g if g else "")] = {"us": t * 1e6, "gbs": b / t / 1e9,
                                                                            "roofline_frac": b / hbm / t}
@@ -378,53 +397,60 @@ def measure_other_configs(dev, peaks, int8_peak):
     q, s_, z_ = qlin.quantize(xs, p)
     nb = qlin.qlin_workspace_size(qlin.QLIN_OP_QUANTIZE, R_, C_, 0, p)
     ws = torch.empty(max(nb, 16), dtype=torch.uint8, device=dev)
-    t = _time_calls(lambda i: qlin.qlin_quantize(xs, qlin.QLIN_BF16, R_, C_, C_, None, p, q, s_, z_, ws, nb, None))
+    t = _time_calls(lambda i: qlin.qlin_quantize(xring[i % n_ring], qlin.QLIN_BF16, R_, C_, C_, None, p, q, s_, z_,
+                                                 ws, nb, None))
     b = R_ * C_ * 2 + q.numel() + 4
     sweep["quantize_s8_tensor_p99.9"] = {"us": t * 1e6, "gbs": b / t / 1e9, "roofline_frac": b / hbm / t}
     out["sweep_16384x4096_bf16"] = sweep
+    del xring
     return out
 
 
 # ------------------------------------------------------------------ CPU baseline (oracle)
-def oracle_step_seconds(rows_w8, threads):
-    """Time the CPU oracle on a bounded sample of one step; return
-    (extrapolated seconds of a full step, sample description)."""
+_SAMPLE_INPUTS = {}
+
+
+def oracle_sample_seconds(rows_w8, threads):
+    """Time the CPU oracle on a bounded sample of one step: rows_w8 of the
+    4096 activation rows (quantize with the SmoothQuant divide, W8A8 int64
+    sums and the binary64 epilogue against all 8192 weight rows, dequantize)
+    and the same fraction of the 8192 W4 output channels (their dequantized
+    weights and the binary64 products with M = 1, 8, 64, 256 tokens).
+    Returns (seconds, fraction of the step's work, description)."""
     import oracle
     from activation_quantization_quantize_b300.inputs import normal
 
-    oracle.set_threads(threads)
-    rng_rows = rows_w8
-    x = normal((rng_rows, K), 1.0, 101)
-    sm = np.random.default_rng(102).uniform(0.2, 5, K).astype(np.float32)
-    wq = np.random.default_rng(103).integers(-127, 128, (N, K)).astype(np.int8)
-    sw = np.random.default_rng(104).uniform(1e-4, 1e-3, N).astype(np.float32)
-    w4q = np.random.default_rng(105).integers(0, 16, (N, K)).astype(np.int32)
-    w4s = np.random.default_rng(106).uniform(1e-4, 1e-3, N * (K // GROUP)).astype(np.float32)
-    w4z = np.random.default_rng(107).integers(0, 16, N * (K // GROUP)).astype(np.int32)
-    t = {}
+    used = oracle.set_threads(threads)
+    frac = rows_w8 / M8
+    n4 = max(1, int(round(N * frac)))
+    if _SAMPLE_INPUTS.get("rows") != rows_w8:       # drawn once per process, outside the timing
+        _SAMPLE_INPUTS.clear()
+        _SAMPLE_INPUTS.update(
+            rows=rows_w8, x=normal((rows_w8, K), 1.0, 101),
+            sm=np.random.default_rng(102).uniform(0.2, 5, K).astype(np.float32),
+            wq=np.random.default_rng(103).integers(-127, 128, (N, K)).astype(np.int8),
+            sw=np.random.default_rng(104).uniform(1e-4, 1e-3, N).astype(np.float32),
+            w4q=np.random.default_rng(105).integers(0, 16, (n4, K)).astype(np.int32),
+            w4s=np.random.default_rng(106).uniform(1e-4, 1e-3, n4 * (K // GROUP)).astype(np.float32),
+            w4z=np.random.default_rng(107).integers(0, 16, n4 * (K // GROUP)).astype(np.int32),
+            xs=[normal((m, K), 1.0, 108 + m) for m in W4_MS])
+    d = _SAMPLE_INPUTS
+    x, sm, wq, sw, w4q, w4s, w4z, xs = d["x"], d["sm"], d["wq"], d["sw"], d["w4q"], d["w4s"], d["w4z"], d["xs"]
     t0 = time.perf_counter()
     qx, sx, _ = oracle.quantize(x, -127, 127, True, oracle.PER_ROW, smooth=sm, smooth_mode=oracle.SMOOTH_DIVIDE)
-    t["quantize"] = time.perf_counter() - t0
-    t0 = time.perf_counter()
     acc = oracle.w8a8_acc(qx.astype(np.int8), wq)
     oracle.w8a8_out(acc, sx, sw)
-    t["gemm_w8a8"] = time.perf_counter() - t0
-    t0 = time.perf_counter()
-    what = oracle.w4_dequant(w4q, w4s, w4z, GROUP)
-    t["w4_dequant"] = time.perf_counter() - t0
-    x1 = normal((1, K), 1.0, 108)
-    t0 = time.perf_counter()
-    oracle.matmul_f64(x1, what)
-    t["gemm_w4a16_m1"] = time.perf_counter() - t0
-    t0 = time.perf_counter()
+    for _ in W4_MS:                       # each call of the step reads its own copy of the weight
+        what = oracle.w4_dequant(w4q, w4s, w4z, GROUP)
+    for xm in xs:
+        oracle.matmul_f64(xm, what)
     oracle.dequantize(qx, sx, None, oracle.PER_ROW)
-    t["dequantize"] = time.perf_counter() - t0
-    scale = M8 / rows_w8
-    full = (t["quantize"] + t["gemm_w8a8"] + t["dequantize"]) * scale
-    full += len(W4_MS) * t["w4_dequant"] + sum(m * t["gemm_w4a16_m1"] for m in W4_MS)
-    sample = ("oracle on %d of %d activation rows (quantize, W8A8 int64 sums, dequantize), "
-              "full W4 dequant + an M=1 fp64 GEMV; extrapolated linearly to one step" % (rows_w8, M8))
-    return full, sample
+    sec = time.perf_counter() - t0
+    desc = ("oracle on %d of %d activation rows (quantize, W8A8 int64 sums + binary64 epilogue, dequantize) "
+            "and %d of %d W4 output channels (dequant + binary64 products at M = 1/8/64/256): %.4f of one "
+            "step; OpenMP over rows in the W8A8 sums and binary64 products (%d threads), the quantize, "
+            "dequantize and W4 dequant are single-threaded in the oracle" % (rows_w8, M8, n4, N, frac, used))
+    return sec, frac, desc
 
 
 def cpu_threads():
@@ -432,6 +458,12 @@ def cpu_threads():
         return len(os.sched_getaffinity(0))
     except AttributeError:
         return os.cpu_count() or 1
+
+
+def cpu_rows(threads):
+    """Activation rows of the oracle sample: two per thread (at least 32), so
+    the row-parallel loops keep every core busy."""
+    return 2 * max(16, threads)
 
 
 # ------------------------------------------------------------------ main
@@ -458,7 +490,8 @@ def max_over_ranks(v, world, dev):
 
 
 def run_reference(args, world, rank):
-    """The oracle as it stands on the host cores, on bounded samples of the step."""
+    """The oracle as it stands on the host cores, one bounded sample of the
+    step per timed step (the same sample as the cpu_baseline leg)."""
     if rank != 0:
         return
     peaks = load_peaks()
@@ -466,23 +499,25 @@ def run_reference(args, world, rank):
     int8_peak = peaks["bf16_tflops"]
     t_roof = sum(roofline_seconds(b, f, peaks, int8_peak) for b, f in bf.values())
     threads = cpu_threads()
-    per_step_budget = 150.0 / max(1, args.steps + args.warmup)
-    rows = 1 if per_step_budget < 4.0 else 2
+    rows = cpu_rows(threads)
     for _ in range(args.warmup):
-        oracle_step_seconds(rows, threads)
+        oracle_sample_seconds(rows, threads)
     times = []
     t0 = time.perf_counter()
     for _ in range(args.steps):
-        full, sample = oracle_step_seconds(rows, threads)
-        times.append(full)
+        sec, frac, sample = oracle_sample_seconds(rows, threads)
+        times.append(sec)
     wall = time.perf_counter() - t0
     step = statistics.mean(times)
-    value = 100.0 * t_roof / step
+    value = 100.0 * frac * t_roof / step
     out = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
            "steps": args.steps, "warmup": args.warmup, "ms_per_step": step * 1e3, "higher_is_better": True,
            "scaling": "weak", "vs_baseline": None, "dtype": "int64+f64", "data": "synthetic",
            "config": {"workload": "70B down-projection W[8192x28672]: quantize+W8A8 M=4096, W4A16 M=1/8/64/256",
-                      "note": "CPU oracle on bounded samples per step, extrapolated", "sample_wall_s": wall},
+                      "step": "a %.4f sample of the step's work (same as cpu_baseline); value = roofline time "
+                              "of that sample / its measured time" % frac,
+                      "timed_wall_s": wall},
+           "extrapolated_ms_per_full_step": step / frac * 1e3,
            "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle", "sample": sample},
            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(out))
@@ -540,7 +575,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--no-configs", action="store_true",
                     help="skip the timings of the other workloads (decode, prefill, sweep)")
     args = ap.parse_args()
@@ -625,37 +660,75 @@ def main():
     detail["w4a16_decode_weight_gbs_m1"] = w4_weight_bytes / per_kernel["gemm_w4a16_m1"] / 1e9
     detail["w4a16_decode_frac_m1"] = detail["w4a16_decode_weight_gbs_m1"] / peaks["hbm_gbs"]
 
-    # end to end through the C ABI with host buffers: H2D of the step's
-    # activations, the step, D2H of its outputs
+    # end to end through the C ABI with host buffers: every step copies its
+    # activations in from pinned host memory and its outputs back.  Two
+    # device buffer sets alternate, so the copies of step i+1's inputs (one
+    # stream) and of step i-1's outputs (another stream) overlap step i.
+    step.add_buffer_set()
     x_host = step.x.cpu().pin_memory()
     xs_host = [t.cpu().pin_memory() for t in step.xs]
     y8_host = torch.empty(step.y8.shape, dtype=step.y8.dtype).pin_memory()
     y4_host = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in step.y4]
     h2d = x_host.numel() * 2 + sum(t.numel() * 2 for t in xs_host)
     d2h = y8_host.numel() * 2 + sum(t.numel() * 2 for t in y4_host)
+    s_in, s_out = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+    ev_in_ready = [torch.cuda.Event() for _ in range(2)]
+    ev_in_free = [torch.cuda.Event() for _ in range(2)]
+    ev_out_ready = [torch.cuda.Event() for _ in range(2)]
+    ev_out_free = [torch.cuda.Event() for _ in range(2)]
 
-    def e2e_step():
-        step.x.copy_(x_host, non_blocking=True)
-        for d_, h_ in zip(step.xs, xs_host):
-            d_.copy_(h_, non_blocking=True)
-        step.run(stream)
-        y8_host.copy_(step.y8, non_blocking=True)
-        for h_, d_ in zip(y4_host, step.y4):
-            h_.copy_(d_, non_blocking=True)
+    def issue_h2d(i):
+        b = i % 2
+        x_d, xs_d, _, _ = step.sets[b]
+        s_in.wait_event(ev_in_free[b])            # the step that last read set b is done
+        with torch.cuda.stream(s_in):
+            x_d.copy_(x_host, non_blocking=True)
+            for d_, h_ in zip(xs_d, xs_host):
+                d_.copy_(h_, non_blocking=True)
+        ev_in_ready[b].record(s_in)
 
-    with torch.cuda.stream(stream):
-        for _ in range(2):
-            e2e_step()
-        stream.synchronize()
-        barrier(world)
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for _ in range(args.e2e_steps):
-            e2e_step()
-        e1.record(stream)
-        stream.synchronize()
+    def e2e_run(n):
+        issue_h2d(0)
+        for i in range(n):
+            b = i % 2
+            if i + 1 < n:
+                issue_h2d(i + 1)
+            stream.wait_event(ev_in_ready[b])
+            stream.wait_event(ev_out_free[b])      # the outputs of step i-2 have left set b
+            step.run(stream, buf=b)
+            ev_in_free[b].record(stream)
+            ev_out_ready[b].record(stream)
+            s_out.wait_event(ev_out_ready[b])
+            _, _, y8_d, y4_d = step.sets[b]
+            with torch.cuda.stream(s_out):
+                y8_host.copy_(y8_d, non_blocking=True)
+                for h_, d_ in zip(y4_host, y4_d):
+                    h_.copy_(d_, non_blocking=True)
+            ev_out_free[b].record(s_out)
+        stream.wait_stream(s_out)
+        stream.wait_stream(s_in)
+
+    e2e_run(3)
+    stream.synchronize()
+    barrier(world)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    s_in.wait_event(e0)
+    s_out.wait_event(e0)
+    e2e_run(args.e2e_steps)
+    e1.record(stream)
+    stream.synchronize()
     e2e_t = max_over_ranks(e0.elapsed_time(e1) / 1e3 / args.e2e_steps, world, dev)
     e2e_value = world * 100.0 * t_roof / e2e_t
+    # copy bandwidth alone (no compute), for the record
+    c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    c0.record(s_in)
+    with torch.cuda.stream(s_in):
+        for _ in range(3):
+            step.sets[1][0].copy_(x_host, non_blocking=True)
+    c1.record(s_in)
+    s_in.synchronize()
+    h2d_gbs = 3 * x_host.numel() * 2 / (c0.elapsed_time(c1) / 1e3) / 1e9
 
     configs = None
     if not args.no_configs:
@@ -666,9 +739,14 @@ def main():
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         threads = cpu_threads()
-        full, sample = oracle_step_seconds(4, threads)
-        cpu = {"value": 100.0 * t_roof / full, "unit": UNIT, "cores": threads, "kind": "oracle",
-               "sample": sample, "seconds_per_step": full}
+        rows = cpu_rows(threads)
+        sec = min(oracle_sample_seconds(rows, threads)[0] for _ in range(3))
+        _, frac, sample = oracle_sample_seconds(rows, threads)
+        sec1, _, _ = oracle_sample_seconds(rows, 1)
+        cpu = {"value": 100.0 * frac * t_roof / sec, "unit": UNIT, "cores": threads, "kind": "oracle",
+               "sample": sample, "sample_seconds": sec, "sample_fraction": frac,
+               "extrapolated_seconds_per_step": sec / frac,
+               "single_thread": {"value": 100.0 * frac * t_roof / sec1, "sample_seconds": sec1, "cores": 1}}
 
     if rank == 0:
         out = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
@@ -682,7 +760,9 @@ def main():
                           "parallelism": "replicas" if world > 1 else "single GPU"},
                "roofline": roofline, "cpu_baseline": cpu,
                "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                       "ms_per_step": e2e_t * 1e3},
+                       "ms_per_step": e2e_t * 1e3, "steps": args.e2e_steps, "h2d_copy_gbs": h2d_gbs,
+                       "overlap": "inputs of step i+1 and outputs of step i-1 copied on two side streams "
+                                  "while step i computes (two device buffer sets)"},
                "gpu_launches": step.launches_per_step() * args.steps,
                "clocks": clock_info, "peaks": peaks, "int8_ref_tflops": int8_ref, "detail": detail,
                "configs": configs}

@@ -97,7 +97,8 @@ const char *qlin_status_string(int status);
 /*
  * Bytes of device workspace an operation needs (0 = none; pass ws = NULL).
  * For QLIN_OP_QUANTIZE and QLIN_OP_ABSMAX, M = rows, N = cols, K ignored
- * (for ABSMAX, p->gran selects the granularity).  The workspace is scratch
+ * (for ABSMAX, p->gran selects the granularity); per-row and per-group scopes
+ * and static scales need none.  The workspace is scratch
  * owned by the caller; it may be reused once the call's work on `stream`
  * has completed.
  */
@@ -255,10 +256,14 @@ int qlin_gemm_w4a16(const void *x, const void *packed, const qlin_w4_header *hdr
  *   - Limit: an operation whose workspace (qlin_workspace_size with
  *     QLIN_OP_QUANTIZE) exceeds QLIN_NOALLOC_SCRATCH_BYTES returns
  *     QLIN_ERR_WORKSPACE and launches nothing (e.g. per-column statistics of
- *     more than 65,536 columns).
- *   - The first call on a device looks up the array's device address with
- *     cudaGetSymbolAddress (once per device, with that device current); make
- *     that first call before any stream capture.
+ *     more than 65,536 columns).  Per-row and per-group scopes and static
+ *     scales need no scratch at any size.  Argument errors are reported
+ *     before the limit is checked, exactly as qlin_quantize reports them.
+ *   - A call that needs the scratch looks up the array's device address with
+ *     cudaGetSymbolAddress (with the call's device current).  Outside stream
+ *     capture it does so on every call; during a capture it uses the address
+ *     an earlier call on that device found, so make one call on each device
+ *     before capturing (a first call during a capture returns QLIN_ERR_CUDA).
  *   - Every call on a device shares the one array, and the array keeps the
  *     last call's contents; each call clears what it needs zeroed on its own
  *     stream.  Calls whose work overlaps on the GPU (other streams, other host
@@ -277,6 +282,21 @@ int qlin_quantize_noalloc(const void *x, qlin_dtype xt, int64_t rows, int64_t co
  * unspecified).  Returns QLIN_ERR_CUDA if the synchronization itself fails.
  */
 int qlin_device_error(void *stream);
+
+/*
+ * qlin_debug_stall_producers -- failure-detection test hook (not part of the
+ * method).  With enable = 1, the producer roles of the pipelined kernels
+ * (the TMA / bulk-copy issuers of the W8A8 and W4A16 tensor-core GEMMs and of
+ * the streamed per-token quantizer) issue no copies, and every bounded
+ * device-side wait gives up after wait_limit_cycles (> 0) SM clock cycles.
+ * The waiting roles then time out, record QLIN_ERR_TIMEOUT in the device error
+ * word (qlin_device_error), wait (bounded) for the MMAs they issued, free
+ * their TMEM and return; their outputs are unspecified.  enable = 0 restores
+ * normal operation and the default limit (4e9 cycles, about 2 s).  Applies to
+ * the current device; synchronizes it before and after.  Returns QLIN_OK,
+ * QLIN_ERR_ARG (enable with a non-positive limit) or QLIN_ERR_CUDA.
+ */
+int qlin_debug_stall_producers(int enable, long long wait_limit_cycles);
 
 #ifdef __cplusplus
 }

@@ -124,3 +124,36 @@ def test_host_validation_without_gpu(lib):
     assert L.qlin_pack_w4(fake, fake, None, 64, 256, 128, C.c_void_p(0x10010), 1 << 20, None,
                           None) == qlin.QLIN_ERR_ARG   # packed must be 256-byte aligned
     assert L.qlin_smooth_factors(fake, fake, 16, C.c_float(1.5), fake, None) == qlin.QLIN_ERR_ARG
+
+
+def test_noalloc_reports_argument_errors_first(lib):
+    """qlin_quantize_noalloc checks its arguments exactly as qlin_quantize does
+    before it looks at the scratch limit: a bad group is QLIN_ERR_ARG, not
+    QLIN_ERR_WORKSPACE, even for a size whose statistics would not fit."""
+    L = lib
+    fake = C.c_void_p(0x10000)
+    p = qlin.make_params("s8", "col")
+    p.group = -5
+    p.gran = 7                                          # no such granularity
+    assert L.qlin_quantize_noalloc(fake, qlin.QLIN_BF16, 4, 1 << 20, 1 << 20, None, C.byref(p), fake, fake,
+                                   None, None) == qlin.QLIN_ERR_ARG
+    p = qlin.make_params("s8", "group", group=-128)
+    assert L.qlin_quantize_noalloc(fake, qlin.QLIN_BF16, 4, 4096, 4096, None, C.byref(p), fake, fake,
+                                   None, None) == qlin.QLIN_ERR_ARG
+    p = qlin.make_params("u8", "col", percentile=99.9)  # percentile: symmetric per-tensor only
+    assert L.qlin_quantize_noalloc(fake, qlin.QLIN_BF16, 4, 1 << 20, 1 << 20, None, C.byref(p), fake, fake,
+                                   fake, None) == qlin.QLIN_ERR_UNSUPPORTED
+    p = qlin.make_params("s8", "col")                   # valid, but 8 MB of statistics > the scratch
+    assert L.qlin_quantize_noalloc(fake, qlin.QLIN_BF16, 4, 1 << 20, 1 << 20, None, C.byref(p), fake, fake,
+                                   None, None) == qlin.QLIN_ERR_WORKSPACE
+
+
+def test_row_local_scopes_need_no_workspace(lib):
+    for code, gran, g in [("s8", "row", 0), ("u4", "group", 128), ("u8", "group", 7), ("s4", "row", 0)]:
+        p = qlin.make_params(code, gran, group=g)
+        for rows, cols in [(1, 14), (4096, 4096), (8192, 28672), (3, 100003 * 7 if g == 7 else 100002)]:
+            assert qlin.qlin_workspace_size(qlin.QLIN_OP_QUANTIZE, rows, cols, 0, p) == 0
+
+
+def test_stall_hook_validates_without_gpu(lib):
+    assert lib.qlin_debug_stall_producers(1, 0) == qlin.QLIN_ERR_ARG

@@ -221,11 +221,35 @@ def test_scale_f16_is_the_stored_scale(orc):
     rng = np.random.default_rng(4)
     x = (rng.standard_normal((8, 256)) * 0.02).astype(np.float32)
     q, s, z = orc.quantize(x, -7, 7, True, orc.PER_GROUP, 128, scale_f16=True)
-    s32 = (orc.absmax(x, orc.PER_GROUP, 128) / np.float32(7)).astype(np.float32)
+    # group maxima by numpy (8 rows x 2 groups of 128), binary32 division by 7,
+    # then numpy's nearest-even binary16 rounding
+    gmax = np.abs(x).reshape(8, 2, 128).max(axis=2).reshape(-1)
+    s32 = (gmax / np.float32(7)).astype(np.float32)
     np.testing.assert_array_equal(s, s32.astype(np.float16).astype(np.float32))
     sc = np.arange(8)[:, None] * 2 + np.arange(256)[None, :] // 128
     expect = np.clip(np.rint(x / s[sc]), -7, 7)
     np.testing.assert_array_equal(q, expect)
+
+
+@pytest.mark.parametrize("shape", [(1, 1), (5, 24), (37, 512)])
+def test_absmax_every_granularity_against_numpy(orc, shape):
+    """orc_absmax against numpy's max of |x| along the scope's axes: per tensor,
+    per row (axis 1), per column (axis 0) and per group of g consecutive
+    elements of a row ([L19] section 4; [CH11] table 11-1; [CH11] 11.4.5
+    step 1 for the channel maxima)."""
+    rows, cols = shape
+    rng = np.random.default_rng(rows * 31 + cols)
+    x = rng.standard_normal((rows, cols)).astype(np.float32)
+    x[rows // 2, cols // 2] = -1000.0                      # a negative extreme: |x| must be taken
+    a = np.abs(x)
+    np.testing.assert_array_equal(orc.absmax(x, orc.PER_TENSOR), np.array([a.max()], np.float32))
+    np.testing.assert_array_equal(orc.absmax(x, orc.PER_ROW), a.max(axis=1))
+    np.testing.assert_array_equal(orc.absmax(x, orc.PER_COL), a.max(axis=0))
+    for g in (1, 8, cols):
+        if cols % g == 0:
+            np.testing.assert_array_equal(orc.absmax(x, orc.PER_GROUP, g),
+                                          a.reshape(rows, cols // g, g).max(axis=2).reshape(-1))
+    assert orc.absmax(np.zeros((3, 8), np.float32), orc.PER_ROW).tolist() == [0.0, 0.0, 0.0]
 
 
 def test_granularity_scopes(orc):

@@ -116,19 +116,46 @@ def test_w8a8_prefill_config_sampled(smooth):
     assert rel_err_out(host_f32(y)[rows], yo) < GEMM_REL_TOL
 
 
-def test_w8a8_downproj_sampled():
-    """4096 x 8192 x 28672 with outlier channels: 16 sampled rows x all N."""
-    torch.manual_seed(0)
+def stratified_rows(M, tile, per_tile, seed):
+    """per_tile distinct random rows from every tile of `tile` rows."""
+    rng = np.random.default_rng(seed)
+    rows = []
+    for t0 in range(0, M, tile):
+        n = min(tile, M - t0)
+        rows.extend(t0 + rng.choice(n, min(per_tile, n), replace=False))
+    return np.sort(np.array(rows))
+
+
+@pytest.mark.parametrize("folded", [False, True])
+def test_w8a8_downproj_sampled(folded):
+    """4096 x 8192 x 28672 with outlier channels: two random rows from every
+    256-row tile, all 8192 columns (so every output tile, the split-K tail
+    tiles of the last wave included, is checked).  folded: the step's input,
+    X' = bf16(X / s) with the SmoothQuant factors (alpha = 0.5) folded into
+    the previous layer and W smoothed offline (multiply mode), whose larger
+    codes make the exact accumulation drain about once per tile."""
     x = inputs.downproj_activation(4096, outliers=True)
     w = inputs.downproj_weight()
     xd, wd = x.cuda(), w.cuda()
-    del x
-    qx, sx, qw, sw, acc, y = w8a8_run(xd, wd, torch.bfloat16)
-    rows = np.sort(np.random.default_rng(6).choice(4096, 16, replace=False))
-    acco = oracle.w8a8_acc(qx[rows].cpu().numpy(), qw.cpu().numpy())
+    del x, w
+    sm = None
+    if folded:
+        sm = qlin.smooth_factors(qlin.absmax(xd, qlin.QLIN_PER_COL), qlin.absmax(wd, qlin.QLIN_PER_COL), 0.5)
+        xd = (xd.float() / sm[None, :]).to(torch.bfloat16)
+        pw = qlin.make_params("s8", "row", smooth_mode=qlin.QLIN_SMOOTH_MULTIPLY)
+        qw, sw, _ = qlin.quantize(wd, pw, smooth=sm)
+        qx, sx, _ = qlin.quantize(xd, qlin.make_params("s8", "row"))
+        acc = torch.empty((4096, 8192), dtype=torch.int32, device="cuda")
+        y = qlin.gemm_w8a8(qx, sx, qw, sw, out_dtype=torch.bfloat16, acc_out=acc)
+        torch.cuda.synchronize()
+    else:
+        qx, sx, qw, sw, acc, y = w8a8_run(xd, wd, torch.bfloat16)
+    rows = stratified_rows(4096, 256, 2, 6 + int(folded))
+    acco = oracle.w8a8_acc(qx[torch.from_numpy(rows).cuda()].cpu().numpy(), qw.cpu().numpy())
     np.testing.assert_array_equal(acc.cpu().numpy()[rows], acco)
     yo = oracle.w8a8_out(acco, sx.cpu().numpy()[rows], sw.cpu().numpy())
     assert rel_err_out(host_f32(y)[rows], yo) < GEMM_REL_TOL
+    assert qlin.qlin_device_error() == 0
 
 
 # ------------------------------------------------------------------ W4A16

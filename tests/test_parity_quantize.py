@@ -272,3 +272,73 @@ def test_sweep_global_scopes(sweep, code, gran):
 def test_sweep_percentile(sweep):
     xd, xh = sweep
     run_case(xd, xh, qlin.make_params("s8", "tensor", percentile=99.9))
+
+
+# ------------------------------------------------------------- dequantize at full size
+def _dequant_check(q, s, z, p, rows, cols, out=torch.bfloat16, row_sets=None):
+    """GPU dequantize of the whole tensor against the oracle's dequantize of
+    the same codes / scales / zero points, element by element, bit-exact
+    (one binary32 product s*(q-z), then one rounding to the output type).
+    The oracle side runs on row_sets (all rows in blocks when None)."""
+    y = qlin.dequantize(q, s, z, p, rows, cols, out_dtype=out)
+    torch.cuda.synchronize()
+    gran = {0: 0, 1: 1, 2: 2, 3: 3}[p.gran]
+    ngr = {0: 1, 1: 1, 2: 1, 3: cols // max(p.group, 1)}[p.gran]
+    sh = scales_f32(s)
+    zh = None if p.symmetric else z.cpu().numpy()
+    if row_sets is None:
+        row_sets = [np.arange(r0, min(rows, r0 + 1024)) for r0 in range(0, rows, 1024)]
+    for rs in row_sets:
+        idx = torch.from_numpy(rs).cuda()
+        qi = codes_to_int(q[idx], p, len(rs), cols)
+        if p.gran == qlin.QLIN_PER_ROW:
+            ss, zz = sh[rs], (None if zh is None else zh[rs])
+        elif p.gran == qlin.QLIN_PER_GROUP:
+            ss = sh.reshape(rows, ngr)[rs].reshape(-1)
+            zz = None if zh is None else zh.reshape(rows, ngr)[rs].reshape(-1)
+        else:
+            ss, zz = sh, zh
+        yo = oracle.dequantize(qi, ss, zz, gran, p.group)
+        if out == torch.bfloat16:
+            yo = oracle.round_bf16(yo)
+        elif out == torch.float16:
+            yo = yo.astype(np.float16).astype(np.float32)
+        np.testing.assert_array_equal(host_f32(y[idx]), yo)
+
+
+@pytest.mark.parametrize("out", [torch.bfloat16, torch.float32, torch.float16])
+def test_dequantize_downproj_rows_full_size(out):
+    """4096 x 28672 per-token INT8 (the step's call): every row takes two
+    segments of 1024 16-code chunks, and the 8192 (row, segment) units exceed
+    the grid, so the kernel grid-strides.  Whole tensor, bit-exact."""
+    rows, cols = 4096, 28672
+    x = inputs.downproj_activation(rows, outliers=True).cuda()
+    p = qlin.make_params("s8", "row")
+    q, s, z = qlin.quantize(x, p)
+    del x
+    _dequant_check(q, s, z, p, rows, cols, out)
+
+
+@pytest.mark.parametrize("code,gran,group", [("s8", "row", 0), ("s4", "group", 128), ("u8", "tensor", 0),
+                                             ("u8", "group", 64)])
+def test_dequantize_sweep_full_size(sweep, code, gran, group):
+    """The 16384 x 4096 sweep tensor (16384 units, far more than the grid)
+    dequantized at full size; the oracle checks every row."""
+    xd, xh = sweep
+    rows, cols = xh.shape
+    p = qlin.make_params(code, gran, group=group, scale_f16=(gran == "group"))
+    q, s, z = qlin.quantize(xd, p)
+    _dequant_check(q, s, z, p, rows, cols)
+
+
+def test_dequantize_asym_groups_long_rows():
+    """Asymmetric UINT8 per-group (g = 128) on rows of 17,408 values (more
+    than one 16,384-value segment per row) and a ragged row count."""
+    rows, cols = 33, 17408
+    xd, xh = make_x(rows, cols, seed=1717, dtype="bf16")
+    p = qlin.make_params("u8", "group", group=128)
+    q, s, z = qlin.quantize(xd, p)
+    qo, so, zo = oracle_quantize(xh, p)
+    np.testing.assert_array_equal(codes_to_int(q, p, rows, cols), qo)
+    for out in (torch.bfloat16, torch.float32):
+        _dequant_check(q, s, z, p, rows, cols, out)

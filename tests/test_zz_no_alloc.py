@@ -62,6 +62,32 @@ def test_noalloc_matches_workspace_entry_point(code, gran, group, pct):
     assert qlin.qlin_device_error() == 0
 
 
+@pytest.mark.parametrize("code,asym", [("s4", False), ("u4", True)])
+def test_noalloc_many_groups_needs_no_scratch(code, asym):
+    """A 4096 x 4096 weight in groups of 128 (131,072 groups, the W4A16 decode
+    weight): row-local scopes keep their statistics on chip, so the call needs
+    none of the scratch, succeeds and matches qlin_quantize, twice in a row."""
+    dev = torch.device("cuda", 0)
+    rows, cols = 4096, 4096
+    lib = qlin.load()
+    p = qlin.make_params(code, "group", group=128, scale_f16=True)
+    assert qlin.qlin_workspace_size(qlin.QLIN_OP_QUANTIZE, rows, cols, 0, p) == 0
+    for call in range(2):
+        w = torch.from_numpy(inputs.normal((rows, cols), 0.02 * (1 + call), 310 + call)).to(torch.bfloat16).to(dev)
+        q1, s1, z1 = qlin.quantize(w, p)
+        q2, s2, z2 = _outputs(p, rows, cols, dev)
+        stream = torch.cuda.current_stream().cuda_stream
+        rc = lib.qlin_quantize_noalloc(w.data_ptr(), qlin.QLIN_BF16, rows, cols, cols, None, C.byref(p),
+                                       q2.data_ptr(), s2.data_ptr(), z2.data_ptr() if asym else None, stream)
+        assert rc == qlin.QLIN_OK
+        torch.cuda.synchronize()
+        assert torch.equal(q1.view(torch.uint8), q2)
+        assert torch.equal(s1, s2)
+        if asym:
+            assert torch.equal(z1, z2)
+    assert qlin.qlin_device_error() == 0
+
+
 def test_noalloc_rejects_oversized_scratch():
     lib = qlin.load()
     p = qlin.make_params("s8", "col")
