@@ -73,6 +73,10 @@ def _declare(L):
     L.orc_w4_dequant.restype = None
     L.orc_matmul_f64.argtypes = [_f32p, _f32p, _i64, _i64, _i64, _f64p]
     L.orc_matmul_f64.restype = None
+    L.orc_w4a8_acc.argtypes = [_i8p, _i32p, C.c_void_p, _i64, _i64, _i64, _i64, _i64p]
+    L.orc_w4a8_acc.restype = None
+    L.orc_w4a8_out.argtypes = [_i64p, _f32p, _f32p, _i64, _i64, _i64, _f64p]
+    L.orc_w4a8_out.restype = None
     L.orc_set_threads.argtypes = [C.c_int]
     L.orc_set_threads.restype = C.c_int
 
@@ -231,4 +235,25 @@ def matmul_f64(x, w):
     N = w.shape[0]
     y = np.zeros((M, N), dtype=np.float64)
     lib().orc_matmul_f64(x, w, M, N, K, y)
+    return y
+
+
+def w4a8_acc(qx, q, z, g):
+    """Exact per-group integer sums acc[g][m][n] = sum_{k in g} qx[m,k] (q[n,k] - z[n,g])."""
+    qx = np.ascontiguousarray(qx, dtype=np.int8)
+    q = np.ascontiguousarray(q, dtype=np.int32)
+    M, K = qx.shape
+    N = q.shape[0]
+    acc = np.zeros((K // g, M, N), dtype=np.int64)
+    zz = None if z is None else np.ascontiguousarray(z, dtype=np.int32)
+    lib().orc_w4a8_acc(qx, q, _ptr(zz), M, N, K, int(g), acc)
+    return acc
+
+
+def w4a8_out(acc, sx, s):
+    """y[m,n] = sx[m] * sum_g s[n,g] * acc[g][m][n] in binary64."""
+    acc = np.ascontiguousarray(acc, dtype=np.int64)
+    ng, M, N = acc.shape
+    y = np.zeros((M, N), dtype=np.float64)
+    lib().orc_w4a8_out(acc, _f32(sx), _f32(s), M, N, ng, y)
     return y

@@ -405,6 +405,50 @@ void orc_matmul_f64(const float *x, const float *w, int64_t M, int64_t N, int64_
 }
 
 /* ------------------------------------------------------------------------ */
+/* W4A8 linear layer: group-wise INT4 weights x per-token INT8 activations   */
+/* ([CH11] 11.4.5 step 6 and 11.9.7: AWQ-style INT4 weights with             */
+/* SmoothQuant INT8 activations; integer products summed exactly, then the   */
+/* scales).  Each weight group g (g consecutive k of a row) has its own      */
+/* scale s[n,g] and zero point z[n,g], so the integer sums are kept per      */
+/* group and the scales are applied afterwards:                              */
+/*   acc[g][m][n] = sum_{k in group g} qx[m,k] * (q[n,k] - z[n,g])           */
+/*   y[m][n]      = sx[m] * sum_g s[n,g] * acc[g][m][n]     (binary64)        */
+/* which is the product of the dequantized operands x^ = sx*qx and           */
+/* w^ = s*(q - z).                                                           */
+/* ------------------------------------------------------------------------ */
+
+/* qx: M x K int8 codes; q: N x K int32 weight codes; z: N x K/g or NULL
+ * (symmetric codes, z = 0); acc: (K/g) x M x N int64. */
+void orc_w4a8_acc(const int8_t *qx, const int32_t *q, const int32_t *z, int64_t M, int64_t N, int64_t K,
+                  int64_t g, int64_t *acc)
+{
+    int64_t ng = K / g;
+#pragma omp parallel for schedule(static)
+    for (int64_t m = 0; m < M; ++m)
+        for (int64_t n = 0; n < N; ++n)
+            for (int64_t gi = 0; gi < ng; ++gi) {
+                int64_t zz = z ? z[n * ng + gi] : 0;
+                int64_t sum = 0;
+                for (int64_t k = gi * g; k < (gi + 1) * g; ++k)
+                    sum += (int64_t)qx[m * K + k] * ((int64_t)q[n * K + k] - zz);
+                acc[(gi * M + m) * N + n] = sum;
+            }
+}
+
+/* y[m][n] = sx[m] * sum_g s[n,g] * acc[g][m][n] in binary64; s holds the
+ * stored (binary16-rounded) scales, N x K/g. */
+void orc_w4a8_out(const int64_t *acc, const float *sx, const float *s, int64_t M, int64_t N, int64_t ng, double *y)
+{
+    for (int64_t m = 0; m < M; ++m)
+        for (int64_t n = 0; n < N; ++n) {
+            double t = 0.0;
+            for (int64_t gi = 0; gi < ng; ++gi)
+                t += (double)s[n * ng + gi] * (double)acc[(gi * M + m) * N + n];
+            y[m * N + n] = (double)sx[m] * t;
+        }
+}
+
+/* ------------------------------------------------------------------------ */
 /* Threads used by the OpenMP loops above (1 when built without OpenMP).     */
 /* ------------------------------------------------------------------------ */
 int orc_set_threads(int n)

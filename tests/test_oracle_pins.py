@@ -465,3 +465,74 @@ def test_oracle_rejects_undefined_arguments(orc):
         orc.quantize(x, 0, 255, False, orc.PER_TENSOR, percentile=99.9)  # percentile is symmetric
     with pytest.raises(ValueError):
         orc.quantize(x, -128, 127, True, orc.PER_TENSOR)          # symmetric needs qmin = -qmax
+
+
+# ------------------------------------------------------------- W4A8 (group-wise INT4 x per-token INT8)
+def test_w4a8_group_sums_brute_force(orc):
+    """Exact per-group integer sums by plain Python loops ([CH11] 11.4.5
+    step 6: integer products summed exactly; groups of g consecutive k)."""
+    rng = np.random.default_rng(21)
+    M, N, K, g = 3, 5, 64, 16
+    qx = rng.integers(-127, 128, (M, K)).astype(np.int8)
+    q = rng.integers(0, 16, (N, K)).astype(np.int32)
+    z = rng.integers(0, 16, (N, K // g)).astype(np.int32)
+    acc = orc.w4a8_acc(qx, q, z.reshape(-1), g)
+    assert acc.shape == (K // g, M, N)
+    for gi in range(K // g):
+        for m in range(M):
+            for n in range(N):
+                want = sum(int(qx[m, k]) * (int(q[n, k]) - int(z[n, gi])) for k in range(gi * g, (gi + 1) * g))
+                assert acc[gi, m, n] == want
+    # extremes: 127 * 15 * 128 per group
+    qx = np.full((1, 128), 127, np.int8)
+    q = np.full((1, 128), 15, np.int32)
+    assert orc.w4a8_acc(qx, q, np.zeros(1, np.int32), 128)[0, 0, 0] == 127 * 15 * 128
+    # symmetric codes: z = NULL means z = 0
+    qx = rng.integers(-127, 128, (2, 32)).astype(np.int8)
+    q = rng.integers(-7, 8, (4, 32)).astype(np.int32)
+    np.testing.assert_array_equal(orc.w4a8_acc(qx, q, None, 32)[0], qx.astype(np.int64) @ q.T.astype(np.int64))
+
+
+def test_w4a8_one_group_is_w8a8(orc):
+    """With a single group per row and z = 0 the W4A8 layer is the W8A8 layer
+    with per-output-channel scales ([L19] section 6): same sums, same y."""
+    rng = np.random.default_rng(22)
+    M, N, K = 4, 6, 96
+    qx = rng.integers(-127, 128, (M, K)).astype(np.int8)
+    q = rng.integers(-7, 8, (N, K)).astype(np.int32)
+    sx = rng.uniform(1e-3, 1e-1, M).astype(np.float32)
+    s = rng.uniform(1e-3, 1e-1, N).astype(np.float32)
+    acc = orc.w4a8_acc(qx, q, None, K)
+    acc8 = orc.w8a8_acc(qx, q.astype(np.int8))
+    np.testing.assert_array_equal(acc[0], acc8)
+    np.testing.assert_array_equal(orc.w4a8_out(acc, sx, s), orc.w8a8_out(acc8, sx, s))
+
+
+def test_w4a8_error_identity(orc):
+    """y^ - y = dW x + W dx + dW dx ([QDC] section 1, the error of y = W x when
+    both operands are quantized): the oracle's W4A8 output is the product of
+    the dequantized operands x^ = sx qx (per token) and w^ = s (q - z) (per
+    group), with the orientation y[m,n] = sum_k x[m,k] w[n,k]."""
+    rng = np.random.default_rng(23)
+    M, N, K, g = 6, 10, 256, 64
+    x = rng.standard_normal((M, K)).astype(np.float32)
+    x[:, 7] *= 30.0
+    w = (rng.standard_normal((N, K)) * 0.02).astype(np.float32)
+    qx, sx, _ = orc.quantize(x, -127, 127, True, orc.PER_ROW)
+    q, s, z = orc.quantize(w, 0, 15, False, orc.PER_GROUP, g, scale_f16=True)
+    yq = orc.w4a8_out(orc.w4a8_acc(qx.astype(np.int8), q, z, g), sx, s)
+    xh = sx.astype(np.float64)[:, None] * qx
+    sc = np.repeat(s.reshape(N, K // g).astype(np.float64), g, axis=1)
+    zc = np.repeat(z.reshape(N, K // g), g, axis=1)
+    wh = sc * (q - zc)
+    x64, w64 = x.astype(np.float64), w.astype(np.float64)
+    dx, dw = xh - x64, wh - w64
+    y = x64 @ w64.T
+    lhs = yq - y
+    rhs = x64 @ dw.T + dx @ w64.T + dx @ dw.T
+    np.testing.assert_allclose(lhs, rhs, rtol=0, atol=1e-12 * np.abs(y).max())
+    np.testing.assert_allclose(yq, xh @ wh.T, rtol=1e-13, atol=1e-15)
+    # a weight row whose codes all equal their zero point contributes exactly 0
+    q2 = q.copy()
+    q2[3] = np.repeat(z.reshape(N, K // g)[3], g)
+    assert np.all(orc.w4a8_out(orc.w4a8_acc(qx.astype(np.int8), q2, z, g), sx, s)[:, 3] == 0.0)
