@@ -77,6 +77,17 @@ def _declare(L):
     L.orc_w4a8_acc.restype = None
     L.orc_w4a8_out.argtypes = [_i64p, _f32p, _f32p, _i64, _i64, _i64, _f64p]
     L.orc_w4a8_out.restype = None
+    L.orc_channel_absmax_update.argtypes = [_f32p, _i64, _i64, _f32p]
+    L.orc_channel_absmax_update.restype = None
+    L.orc_fold_layernorm.argtypes = [_f32p, C.c_void_p, _f32p, _i64, _f32p, C.c_void_p]
+    L.orc_fold_layernorm.restype = None
+    L.orc_quant_error.argtypes = [_f32p, _i64, _i64, C.c_void_p, C.c_int, _i32p, _f32p, C.c_void_p, C.c_int,
+                                  _i64, _f64p]
+    L.orc_quant_error.restype = None
+    L.orc_llmint8_outlier_cols.argtypes = [_f32p, _i64, _i64, C.c_float, _i32p]
+    L.orc_llmint8_outlier_cols.restype = _i64
+    L.orc_llmint8_out.argtypes = [_f32p, _i8p, _f32p, _f32p, _i64p, _i32p, _i64, _i64, _i64, _i64, _f64p]
+    L.orc_llmint8_out.restype = None
     L.orc_set_threads.argtypes = [C.c_int]
     L.orc_set_threads.restype = C.c_int
 
@@ -257,3 +268,104 @@ def w4a8_out(acc, sx, s):
     y = np.zeros((M, N), dtype=np.float64)
     lib().orc_w4a8_out(acc, _f32(sx), _f32(s), M, N, ng, y)
     return y
+
+
+# ---------------------------------------------------------------- SmoothQuant calibration
+def channel_absmax_update(x, running):
+    """running[j] = max(running[j], max_i |x[i, j]|), in place; returns running."""
+    x = _f32(x)
+    assert running.dtype == np.float32 and running.flags["C_CONTIGUOUS"]
+    lib().orc_channel_absmax_update(x, x.shape[0], x.shape[1], running)
+    return running
+
+
+def fold_layernorm(gamma, beta, s):
+    """(gamma / s, beta / s) in binary32 (beta may be None)."""
+    gamma, s = _f32(gamma), _f32(s)
+    g_out = np.zeros_like(gamma)
+    b = None if beta is None else _f32(beta)
+    b_out = None if beta is None else np.zeros_like(gamma)
+    lib().orc_fold_layernorm(gamma, _ptr(b), s, gamma.size, g_out, _ptr(b_out))
+    return g_out, b_out
+
+
+def quant_error(x, q, s, z, gran, group=0, smooth=None, smooth_mode=SMOOTH_NONE):
+    """(sum (x' - x^)^2, sum x'^2, max |x' - x^|) in binary64."""
+    x = _f32(x)
+    rows, cols = x.shape
+    q = np.ascontiguousarray(q, dtype=np.int32)
+    out = np.zeros(3, dtype=np.float64)
+    sm = None if smooth is None else _f32(smooth)
+    zz = None if z is None else np.ascontiguousarray(z, dtype=np.int32)
+    lib().orc_quant_error(x, rows, cols, _ptr(sm), smooth_mode, q, _f32(s), _ptr(zz), gran, int(group), out)
+    return out
+
+
+# ---------------------------------------------------------------- LLM.int8()
+def llmint8_outlier_cols(x, threshold):
+    x = _f32(x)
+    cols = np.zeros(x.shape[1], dtype=np.int32)
+    n = lib().orc_llmint8_outlier_cols(x, x.shape[0], x.shape[1], float(threshold), cols)
+    return cols[:n].copy()
+
+
+def llmint8_out(x, qw, sw, sx, acc, cols):
+    x = _f32(x)
+    M, K = x.shape
+    qw = np.ascontiguousarray(qw, dtype=np.int8)
+    N = qw.shape[0]
+    y = np.zeros((M, N), dtype=np.float64)
+    cols = np.ascontiguousarray(cols, dtype=np.int32)
+    lib().orc_llmint8_out(x, qw, _f32(sw), _f32(sx), np.ascontiguousarray(acc, dtype=np.int64), cols, cols.size,
+                          M, N, K, y)
+    return y
+
+
+def llmint8(x, qw, sw, threshold):
+    """The whole decomposition: outlier channels, per-token INT8 codes of the
+    normal channels (outlier channels zeroed, so they neither widen the scale
+    nor add to the INT8 sums), the INT8 sums, and y in binary64."""
+    x = _f32(x)
+    cols = llmint8_outlier_cols(x, threshold)
+    xn = x.copy()
+    xn[:, cols] = 0.0
+    qx, sx, _ = quantize(xn, -127, 127, True, PER_ROW)
+    acc = w8a8_acc(qx.astype(np.int8), qw)
+    return cols, qx, sx, acc, llmint8_out(x, qw, sw, sx, acc, cols)
+
+
+# ---------------------------------------------------------------- KV-cache quantization
+def kv_cache_reference(k, v, group, residual, head_dim, bits):
+    """KV-cache quantization in token groups outside a recent window ([CH11]
+    11.6.3-11.6.5: K per channel, V per token, the most recent tokens kept in
+    16-bit; KIVI's grouped, on-demand quantization).
+
+    k, v: binary32 [T x C] (the 16-bit values the cache received).  The first
+    Tq = group * floor(max(T - residual, 0) / group) tokens are quantized in
+    groups of `group` tokens with asymmetric codes [0, 2^bits - 1]: K with one
+    scale / zero point per (group, channel) (min-max over the group's tokens),
+    V with one per (token, head) (min-max over head_dim channels).  Returns a
+    dict with the codes, scales and zero points of the quantized part, Tq,
+    and the cache as read back (binary32): dequantized s * (q - z) for
+    t < Tq, the original values for t >= Tq."""
+    k, v = _f32(k), _f32(v)
+    T, C = k.shape
+    qmax = (1 << bits) - 1
+    tq = group * (max(T - residual, 0) // group)
+    ng = tq // group
+    kq = np.zeros((tq, C), np.int32)
+    ks = np.zeros((ng, C), np.float32)
+    kz = np.zeros((ng, C), np.int32)
+    for gi in range(ng):
+        blk = k[gi * group:(gi + 1) * group]
+        q, s, z = quantize(blk, 0, qmax, False, PER_COL)
+        kq[gi * group:(gi + 1) * group], ks[gi], kz[gi] = q, s, z
+    vq, vs, vz = (quantize(v[:tq], 0, qmax, False, PER_GROUP, head_dim) if tq
+                  else (np.zeros((0, C), np.int32), np.zeros(0, np.float32), np.zeros(0, np.int32)))
+    khat, vhat = k.copy(), v.copy()
+    if tq:
+        for gi in range(ng):
+            khat[gi * group:(gi + 1) * group] = dequantize(kq[gi * group:(gi + 1) * group], ks[gi], kz[gi], PER_COL)
+        vhat[:tq] = dequantize(vq, vs, vz, PER_GROUP, head_dim)
+    return dict(tq=tq, k_codes=kq, k_scale=ks, k_zero=kz, v_codes=vq, v_scale=vs.reshape(tq, C // head_dim),
+                v_zero=vz.reshape(tq, C // head_dim), k_hat=khat, v_hat=vhat)

@@ -449,6 +449,99 @@ void orc_w4a8_out(const int64_t *acc, const float *sx, const float *s, int64_t M
 }
 
 /* ------------------------------------------------------------------------ */
+/* SmoothQuant calibration ([CH11] 11.4.3 table 11-4, 11.4.4, 11.4.5 steps   */
+/* 1-3; [QDC] 2.3)                                                           */
+/* ------------------------------------------------------------------------ */
+
+/* Running per-channel maxima over calibration batches:
+ * running[j] = max(running[j], max_i |x[i][j]|). */
+void orc_channel_absmax_update(const float *x, int64_t rows, int64_t cols, float *running)
+{
+    for (int64_t r = 0; r < rows; ++r)
+        for (int64_t c = 0; c < cols; ++c) {
+            float a = fabsf(x[r * cols + c]);
+            if (a > running[c]) running[c] = a;
+        }
+}
+
+/* Folding diag(s)^-1 into the LayerNorm that produces X: LN(x) diag(s)^-1 is
+ * a LayerNorm with gamma'_j = gamma_j / s_j and beta'_j = beta_j / s_j
+ * (binary32 divisions).  beta may be NULL. */
+void orc_fold_layernorm(const float *gamma, const float *beta, const float *s, int64_t K,
+                        float *gamma_out, float *beta_out)
+{
+    for (int64_t j = 0; j < K; ++j) {
+        gamma_out[j] = gamma[j] / s[j];
+        if (beta && beta_out) beta_out[j] = beta[j] / s[j];
+    }
+}
+
+/* Quantization error of a tensor against its (smoothed) original:
+ * x'[r][c] = x[r][c] / smooth[c] (divide mode, binary32) or x[r][c] * smooth[c]
+ * (multiply mode) or x itself; xhat = fl(s * (q - z)) of the scope.
+ * out[0] = sum (x' - xhat)^2, out[1] = sum x'^2, out[2] = max |x' - xhat|,
+ * the sums in binary64 in row-major order. */
+void orc_quant_error(const float *x, int64_t rows, int64_t cols, const float *smooth, int smooth_mode,
+                     const int32_t *q, const float *s, const int32_t *z, int gran, int64_t group, double *out)
+{
+    double se = 0.0, sx = 0.0, mx = 0.0;
+    for (int64_t r = 0; r < rows; ++r)
+        for (int64_t c = 0; c < cols; ++c) {
+            int64_t sc = scope_of(gran, r, c, cols, group);
+            float v = smooth_one(x[r * cols + c], smooth, smooth_mode, c);
+            float xh = s[sc] * (float)(q[r * cols + c] - (z ? z[sc] : 0));
+            double d = (double)v - (double)xh;
+            se += d * d;
+            sx += (double)v * (double)v;
+            if (fabs(d) > mx) mx = fabs(d);
+        }
+    out[0] = se;
+    out[1] = sx;
+    out[2] = mx;
+}
+
+/* ------------------------------------------------------------------------ */
+/* LLM.int8() mixed-precision decomposition ([L19] sections 9-11):           */
+/*   XW = X_normal W_normal (INT8, vector-wise scales) + X_outlier W_outlier   */
+/* (16-bit).  Outlier dimensions are the input channels j with               */
+/* max_m |x[m][j]| > threshold.  The weight is stored once in INT8 (per      */
+/* output channel, scales sw); its outlier columns take part in the 16-bit   */
+/* product dequantized, w^[n][j] = sw[n] * qw[n][j].                         */
+/* ------------------------------------------------------------------------ */
+
+/* Ascending list of the outlier channels of x (rows x cols); returns their
+ * number. */
+int64_t orc_llmint8_outlier_cols(const float *x, int64_t rows, int64_t cols, float threshold, int32_t *cols_out)
+{
+    int64_t n = 0;
+    for (int64_t c = 0; c < cols; ++c) {
+        int outlier = 0;
+        for (int64_t r = 0; r < rows; ++r)
+            if (fabsf(x[r * cols + c]) > threshold) outlier = 1;
+        if (outlier) cols_out[n++] = (int32_t)c;
+    }
+    return n;
+}
+
+/* y[m][n] = sw[n] * (sx[m] * acc[m][n] + sum_{j in cols} x[m][j] * qw[n][j])
+ * in binary64: acc holds the INT8 sums over the normal channels (the
+ * outlier channels' activation codes are 0), the second term is the 16-bit
+ * product of the outlier channels with the dequantized weight (the factor
+ * sw[n] taken out of the sum). */
+void orc_llmint8_out(const float *x, const int8_t *qw, const float *sw, const float *sx, const int64_t *acc,
+                     const int32_t *cols, int64_t n_out, int64_t M, int64_t N, int64_t K, double *y)
+{
+#pragma omp parallel for schedule(static)
+    for (int64_t m = 0; m < M; ++m)
+        for (int64_t n = 0; n < N; ++n) {
+            double o = 0.0;
+            for (int64_t i = 0; i < n_out; ++i)
+                o += (double)x[m * K + cols[i]] * (double)qw[n * K + cols[i]];
+            y[m * N + n] = (double)sw[n] * ((double)sx[m] * (double)acc[m * N + n] + o);
+        }
+}
+
+/* ------------------------------------------------------------------------ */
 /* Threads used by the OpenMP loops above (1 when built without OpenMP).     */
 /* ------------------------------------------------------------------------ */
 int orc_set_threads(int n)

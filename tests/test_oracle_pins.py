@@ -536,3 +536,165 @@ def test_w4a8_error_identity(orc):
     q2 = q.copy()
     q2[3] = np.repeat(z.reshape(N, K // g)[3], g)
     assert np.all(orc.w4a8_out(orc.w4a8_acc(qx.astype(np.int8), q2, z, g), sx, s)[:, 3] == 0.0)
+
+
+# ------------------------------------------------------------- SmoothQuant calibration
+def test_channel_absmax_update_is_the_max_over_all_batches(orc):
+    """Calibration keeps max|X_j| over every batch seen ([CH11] 11.4.5 steps
+    1-2): the running maxima equal numpy's max over the concatenated batches."""
+    rng = np.random.default_rng(31)
+    batches = [rng.standard_normal((n, 48)).astype(np.float32) * rng.uniform(0.5, 3) for n in (3, 7, 1, 12)]
+    batches[2][0, 5] = -900.0
+    run = np.zeros(48, np.float32)
+    for b in batches:
+        orc.channel_absmax_update(b, run)
+    np.testing.assert_array_equal(run, np.abs(np.concatenate(batches)).max(axis=0))
+
+
+def test_fold_layernorm_equivalence(orc):
+    """LN(x) diag(s)^-1 is the LayerNorm with gamma / s and beta / s ([CH11]
+    11.4.4: the smoothing is absorbed by the previous LayerNorm's gamma): the
+    folded parameters are binary32 quotients, and the folded LayerNorm equals
+    the unfolded one divided by s up to those roundings."""
+    rng = np.random.default_rng(32)
+    K = 256
+    gamma = rng.uniform(0.5, 1.5, K).astype(np.float32)
+    beta = rng.uniform(-0.2, 0.2, K).astype(np.float32)
+    s = rng.uniform(0.1, 20.0, K).astype(np.float32)
+    g2, b2 = orc.fold_layernorm(gamma, beta, s)
+    np.testing.assert_array_equal(g2, gamma / s)           # IEEE binary32 division
+    np.testing.assert_array_equal(b2, beta / s)
+    x = rng.standard_normal((5, K)) * 3 + 1
+    mu = x.mean(axis=1, keepdims=True)
+    sd = np.sqrt(x.var(axis=1, keepdims=True) + 1e-5)
+    ln = (x - mu) / sd * gamma + beta
+    ln2 = (x - mu) / sd * g2.astype(np.float64) + b2.astype(np.float64)
+    np.testing.assert_allclose(ln2, ln / s, rtol=2e-7, atol=1e-7 * np.abs(ln / s).max())
+    g3, b3 = orc.fold_layernorm(gamma, None, s)
+    assert b3 is None and np.array_equal(g3, g2)
+
+
+def test_quant_error_statistics(orc):
+    """Sum of squared errors, sum of squares and max error of x' - s(q - z) in
+    binary64, against numpy on the same dequantized values; a value on the
+    grid has no error."""
+    rng = np.random.default_rng(33)
+    x = rng.standard_normal((6, 40)).astype(np.float32)
+    sm = rng.uniform(0.5, 2.0, 40).astype(np.float32)
+    for mode, xs in ((orc.SMOOTH_NONE, x), (orc.SMOOTH_DIVIDE, x / sm), (orc.SMOOTH_MULTIPLY, x * sm)):
+        q, s, z = orc.quantize(x, 0, 255, False, orc.PER_GROUP, 8, smooth=sm if mode else None, smooth_mode=mode)
+        e = orc.quant_error(x, q, s, z, orc.PER_GROUP, 8, smooth=sm if mode else None, smooth_mode=mode)
+        sc = np.repeat(s.reshape(6, 5), 8, axis=1)
+        zc = np.repeat(z.reshape(6, 5), 8, axis=1)
+        xh = (sc * (q - zc).astype(np.float32)).astype(np.float32)
+        d = xs.astype(np.float64) - xh.astype(np.float64)
+        np.testing.assert_allclose(e[0], (d * d).sum(), rtol=1e-12)
+        np.testing.assert_allclose(e[1], (xs.astype(np.float64) ** 2).sum(), rtol=1e-12)
+        assert e[2] == np.abs(d).max()
+    g = np.array([[0.5, -1.0, 2.0, 0.25]], np.float32)      # multiples of s = 0.25: exact codes
+    q, s, z = orc.quantize(g, -8, 8, True, orc.PER_TENSOR)
+    assert list(orc.quant_error(g, q, s, z, orc.PER_TENSOR)) == [0.0, float((g.astype(np.float64) ** 2).sum()), 0.0]
+
+
+def _outlier_layer(seed, M=64, N=96, K=256, n_out=4):
+    rng = np.random.default_rng(seed)
+    x = rng.standard_normal((M, K)).astype(np.float32)
+    cols = np.sort(rng.choice(K, n_out, replace=False))
+    x[:, cols] *= rng.uniform(20, 60, n_out).astype(np.float32)
+    w = (rng.standard_normal((N, K)) * 0.02).astype(np.float32)
+    return x, w, cols
+
+
+def test_smoothquant_alpha_table(orc):
+    """[CH11] table 11-4: raising alpha moves quantization difficulty from the
+    activations to the weights -- the INT8 error of the smoothed activations
+    (per token) falls and that of the smoothed weights (per output channel)
+    rises, alpha = 0.3 < 0.5 < 0.7.  Relative Frobenius errors on inputs with
+    outlier channels."""
+    x, w, _ = _outlier_layer(34, M=128, N=128, K=512, n_out=6)
+    xmax, wmax = orc.absmax(x, orc.PER_COL), orc.absmax(w, orc.PER_COL)
+    act, wgt = [], []
+    for alpha in (0.3, 0.5, 0.7):
+        s = orc.smooth_factors(xmax, wmax, alpha)
+        qx, sx, zx = orc.quantize(x, -127, 127, True, orc.PER_ROW, smooth=s, smooth_mode=orc.SMOOTH_DIVIDE)
+        qw, sw, zw = orc.quantize(w, -127, 127, True, orc.PER_ROW, smooth=s, smooth_mode=orc.SMOOTH_MULTIPLY)
+        ea = orc.quant_error(x, qx, sx, None, orc.PER_ROW, smooth=s, smooth_mode=orc.SMOOTH_DIVIDE)
+        ew = orc.quant_error(w, qw, sw, None, orc.PER_ROW, smooth=s, smooth_mode=orc.SMOOTH_MULTIPLY)
+        act.append(np.sqrt(ea[0] / ea[1]))
+        wgt.append(np.sqrt(ew[0] / ew[1]))
+    assert act[0] > act[1] > act[2]
+    assert wgt[0] < wgt[1] < wgt[2]
+
+
+# ------------------------------------------------------------- LLM.int8()
+def test_llmint8_outlier_channels_by_numpy(orc):
+    x, _, cols = _outlier_layer(41)
+    got = orc.llmint8_outlier_cols(x, 6.0)
+    np.testing.assert_array_equal(got, np.nonzero(np.abs(x).max(axis=0) > 6.0)[0])
+    assert set(cols).issubset(set(got.tolist()))
+    assert orc.llmint8_outlier_cols(x, 1e9).size == 0
+    np.testing.assert_array_equal(orc.llmint8_outlier_cols(x, -1.0), np.arange(x.shape[1]))
+
+
+def test_llmint8_decomposition(orc):
+    """XW = X_normal W + X_outlier W ([L19] section 10): with no outlier
+    channel the layer is the W8A8 layer; with outliers the INT8 part sees
+    zeros in those channels, the 16-bit part is an fp64 product with the
+    dequantized weight columns, and the result beats plain per-token INT8 on
+    outlier inputs."""
+    x, w, _ = _outlier_layer(42)
+    qw, sw, _ = orc.quantize(w, -127, 127, True, orc.PER_ROW)
+    qw8 = qw.astype(np.int8)
+    cols, qx, sx, acc, y = orc.llmint8(x, qw8, sw, 1e9)          # no outliers
+    assert cols.size == 0
+    qx0, sx0, _ = orc.quantize(x, -127, 127, True, orc.PER_ROW)
+    np.testing.assert_array_equal(qx, qx0)
+    np.testing.assert_array_equal(y, orc.w8a8_out(orc.w8a8_acc(qx0.astype(np.int8), qw8), sx0, sw))
+    cols, qx, sx, acc, y = orc.llmint8(x, qw8, sw, 6.0)
+    assert cols.size >= 4 and np.all(qx[:, cols] == 0)
+    normal = np.setdiff1d(np.arange(x.shape[1]), cols)
+    np.testing.assert_array_equal(sx, (np.abs(x[:, normal]).max(axis=1) / np.float32(127)).astype(np.float32))
+    wh = sw.astype(np.float64)[:, None] * qw                       # dequantized weight
+    xh = x.astype(np.float64).copy()
+    xh[:, normal] = sx.astype(np.float64)[:, None] * qx[:, normal]
+    np.testing.assert_allclose(y, xh @ wh.T, rtol=1e-12, atol=1e-14)
+    exact = x.astype(np.float64) @ w.astype(np.float64).T
+    y8 = orc.w8a8_out(orc.w8a8_acc(qx0.astype(np.int8), qw8), sx0, sw)
+    assert np.linalg.norm(y - exact) < 0.5 * np.linalg.norm(y8 - exact)
+
+
+# ------------------------------------------------------------- KV cache
+def test_kv_cache_reference_scopes_and_window(orc):
+    """[CH11] 11.6.3-11.6.5: K quantized per channel over each group of G
+    tokens, V per token (per head), the most recent tokens kept in 16-bit;
+    groups are quantized once they have left the window.  Scales against
+    numpy min-max, codes in range, the s/2 bound, and exact passthrough."""
+    rng = np.random.default_rng(51)
+    T, C, D, G, R, bits = 77, 32, 8, 16, 20, 4
+    k = rng.standard_normal((T, C)).astype(np.float32)
+    k[:, 3] *= 30.0                                                # a K outlier channel
+    v = rng.standard_normal((T, C)).astype(np.float32)
+    r = orc.kv_cache_reference(k, v, G, R, D, bits)
+    assert r["tq"] == 48                                           # 16 * floor((77 - 20) / 16)
+    qmax = 15
+    for gi in range(3):
+        blk = k[gi * G:(gi + 1) * G]
+        hi = np.maximum(blk.max(axis=0), 0)
+        lo = np.minimum(blk.min(axis=0), 0)
+        np.testing.assert_array_equal(r["k_scale"][gi], ((hi - lo) / np.float32(qmax)).astype(np.float32))
+    vb = v[:48].reshape(48, C // D, D)
+    hi = np.maximum(vb.max(axis=2), 0)
+    lo = np.minimum(vb.min(axis=2), 0)
+    np.testing.assert_array_equal(r["v_scale"], ((hi - lo) / np.float32(qmax)).astype(np.float32))
+    assert r["k_codes"].min() >= 0 and r["k_codes"].max() <= qmax
+    assert r["v_codes"].min() >= 0 and r["v_codes"].max() <= qmax
+    ks = np.repeat(r["k_scale"], G, axis=0)
+    assert np.all(np.abs(r["k_hat"][:48] - k[:48]) <= ks / 2 * (1 + 1e-6))
+    vs = np.repeat(r["v_scale"], D, axis=1)
+    assert np.all(np.abs(r["v_hat"][:48] - v[:48]) <= vs / 2 * (1 + 1e-6))
+    np.testing.assert_array_equal(r["k_hat"][48:], k[48:])
+    np.testing.assert_array_equal(r["v_hat"][48:], v[48:])
+    # inside the window nothing is quantized; one more group once it has left
+    assert orc.kv_cache_reference(k[:R], v[:R], G, R, D, bits)["tq"] == 0
+    assert orc.kv_cache_reference(k[:R + G - 1], v[:R + G - 1], G, R, D, bits)["tq"] == 0
+    assert orc.kv_cache_reference(k[:R + G], v[:R + G], G, R, D, bits)["tq"] == G
