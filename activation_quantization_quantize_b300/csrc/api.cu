@@ -62,6 +62,20 @@ int check_qparams(const qlin_qparams* p, int64_t rows, int64_t cols) {
     return QLIN_OK;
 }
 
+// A packed W4 header must describe a layout-1 blob this library writes.
+int check_w4_header(const qlin_w4_header* hdr) {
+    if (hdr->magic != QLIN_W4_MAGIC || hdr->version != QLIN_W4_VERSION) return QLIN_ERR_LAYOUT;
+    if (hdr->N <= 0 || hdr->K <= 0 || (hdr->group != 32 && hdr->group != 64 && hdr->group != 128))
+        return QLIN_ERR_LAYOUT;
+    if (hdr->K % 64 != 0 || hdr->N % 16 != 0) return QLIN_ERR_LAYOUT;
+    qlin_w4_header ref;
+    w4_layout(hdr->N, hdr->K, hdr->group, hdr->asym ? 1 : 0, &ref);
+    if (ref.codes_off != hdr->codes_off || ref.scales_off != hdr->scales_off || ref.zeros_off != hdr->zeros_off ||
+        ref.total_bytes != hdr->total_bytes)
+        return QLIN_ERR_LAYOUT;
+    return QLIN_OK;
+}
+
 }  // namespace
 
 namespace qlin {
@@ -117,6 +131,8 @@ size_t qlin_workspace_size(int op, int64_t M, int64_t N, int64_t K, const qlin_q
     }
     case QLIN_OP_GEMM_W8A8: return w8a8_ws_bytes(M, N, K);
     case QLIN_OP_GEMM_W4A16: return w4a16_ws_bytes(M, N, K);
+    case QLIN_OP_GEMM_W4A8: return w4a8_ws_bytes(M, N, K);
+    case QLIN_OP_QUANT_ERROR: return quant_error_ws_bytes();
     default: return 0;
     }
 }
@@ -210,15 +226,8 @@ int qlin_gemm_w8a8(const int8_t* qx, const float* sx, const int8_t* qw, const fl
 int qlin_gemm_w4a16(const void* x, const void* packed, const qlin_w4_header* hdr, int64_t M, void* y, void* ws,
                     size_t ws_bytes, void* stream) {
     if (!hdr || M < 0) return QLIN_ERR_ARG;
-    if (hdr->magic != QLIN_W4_MAGIC || hdr->version != QLIN_W4_VERSION) return QLIN_ERR_LAYOUT;
-    qlin_w4_header ref;
-    if (hdr->N <= 0 || hdr->K <= 0 || (hdr->group != 32 && hdr->group != 64 && hdr->group != 128))
-        return QLIN_ERR_LAYOUT;
-    if (hdr->K % 64 != 0 || hdr->N % 16 != 0) return QLIN_ERR_LAYOUT;
-    w4_layout(hdr->N, hdr->K, hdr->group, hdr->asym ? 1 : 0, &ref);
-    if (ref.codes_off != hdr->codes_off || ref.scales_off != hdr->scales_off || ref.zeros_off != hdr->zeros_off ||
-        ref.total_bytes != hdr->total_bytes)
-        return QLIN_ERR_LAYOUT;
+    int rc = check_w4_header(hdr);
+    if (rc != QLIN_OK) return rc;
     if (M == 0) return QLIN_OK;
     if (!x || !packed || !y) return QLIN_ERR_ARG;
     if (!aligned(x, 16) || !aligned(packed, 256) || !aligned(y, 16)) return QLIN_ERR_ARG;
@@ -235,6 +244,52 @@ int qlin_debug_stall_producers(int enable, long long wait_limit_cycles) {
     if (cudaMemcpyToSymbol(g_wait_limit_cycles, &limit, sizeof limit) != cudaSuccess) return QLIN_ERR_CUDA;
     if (cudaMemcpyToSymbol(g_stall_producers, &stall, sizeof stall) != cudaSuccess) return QLIN_ERR_CUDA;
     return cudaDeviceSynchronize() == cudaSuccess ? QLIN_OK : QLIN_ERR_CUDA;
+}
+
+int qlin_gemm_w4a8(const int8_t* qx, const float* sx, const void* packed, const qlin_w4_header* hdr, int64_t M,
+                   void* y, qlin_dtype yt, int32_t* acc_out, void* ws, size_t ws_bytes, void* stream) {
+    if (!hdr || M < 0) return QLIN_ERR_ARG;
+    if (yt != QLIN_F32 && yt != QLIN_BF16) return QLIN_ERR_ARG;
+    int rc = check_w4_header(hdr);
+    if (rc != QLIN_OK) return rc;
+    if (M == 0) return QLIN_OK;
+    if (!qx || !sx || !packed || !y) return QLIN_ERR_ARG;
+    if (!aligned(qx, 16) || !aligned(sx, 4) || !aligned(packed, 256) || !aligned(y, type_bytes(yt)) ||
+        (acc_out && !aligned(acc_out, 4)))
+        return QLIN_ERR_ARG;
+    size_t need = w4a8_ws_bytes(M, hdr->N, hdr->K);
+    if (need > 0 && (!ws || ws_bytes < need || !aligned(ws, 16))) return QLIN_ERR_WORKSPACE;
+    return cuda_status(run_gemm_w4a8(qx, sx, packed, hdr, M, y, yt, acc_out, ws, (cudaStream_t)stream));
+}
+
+int qlin_absmax_update(const void* x, qlin_dtype xt, int64_t rows, int64_t cols, int64_t ld, float* running,
+                       void* stream) {
+    if (!is_float_type(xt) || rows < 0 || cols < 0 || ld < cols) return QLIN_ERR_ARG;
+    if (rows == 0 || cols == 0) return QLIN_OK;
+    if (!x || !running || !aligned(x, type_bytes(xt)) || !aligned(running, 4)) return QLIN_ERR_ARG;
+    return cuda_status(run_absmax_update(x, xt, rows, cols, ld, running, (cudaStream_t)stream));
+}
+
+int qlin_fold_layernorm(const float* gamma, const float* beta, const float* s, int64_t K, float* gamma_out,
+                        float* beta_out, void* stream) {
+    if (K < 0 || (beta && !beta_out) || (!beta && beta_out)) return QLIN_ERR_ARG;
+    if (K == 0) return QLIN_OK;
+    if (!gamma || !s || !gamma_out) return QLIN_ERR_ARG;
+    return cuda_status(run_fold_layernorm(gamma, beta, s, K, gamma_out, beta_out, (cudaStream_t)stream));
+}
+
+int qlin_quant_error(const void* x, qlin_dtype xt, int64_t rows, int64_t cols, int64_t ld, const float* smooth,
+                     const qlin_qparams* p, const void* q, const void* s, const int32_t* z, double* out, void* ws,
+                     size_t ws_bytes, void* stream) {
+    int rc = check_qparams(p, rows, cols);
+    if (rc != QLIN_OK) return rc;
+    if (!is_float_type(xt) || ld < cols || !out) return QLIN_ERR_ARG;
+    if (!x && rows * cols > 0) return QLIN_ERR_ARG;
+    if (!q || !s || (!p->symmetric && !z)) return QLIN_ERR_ARG;
+    if (p->smooth_mode != QLIN_SMOOTH_NONE && !smooth) return QLIN_ERR_ARG;
+    if (!aligned(out, 8)) return QLIN_ERR_ARG;
+    if (!ws || ws_bytes < quant_error_ws_bytes() || !aligned(ws, 16)) return QLIN_ERR_WORKSPACE;
+    return cuda_status(run_quant_error(x, xt, rows, cols, ld, smooth, p, q, s, z, out, ws, (cudaStream_t)stream));
 }
 
 int qlin_device_error(void* stream) {

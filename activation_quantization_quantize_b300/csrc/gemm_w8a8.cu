@@ -231,7 +231,7 @@ __device__ __forceinline__ int abs_sum4(uint32_t w, int acc) {
 template <int W>
 __device__ __forceinline__ void store_row(const int (&tot)[W], int64_t m, int64_t nb, int64_t N, float sxm,
                                             const float* __restrict__ sw, void* __restrict__ y, int yt,
-                                            int32_t* __restrict__ acc_out) {
+                                            int32_t* __restrict__ acc_out, const float* __restrict__ add) {
     const bool full = (nb + W <= N) && (N % 8 == 0);
     if (acc_out) {
         int32_t* ap = acc_out + m * N + nb;
@@ -248,6 +248,7 @@ __device__ __forceinline__ void store_row(const int (&tot)[W], int64_t m, int64_
     for (int j = 0; j < W; ++j) {
         float swn = (nb + j < N) ? __ldg(sw + nb + j) : 0.0f;
         f[j] = ((float)tot[j] * sxm) * swn;
+        if (add && nb + j < N) f[j] = fmaf(__ldg(add + m * N + nb + j), swn, f[j]);
     }
     if (yt == QLIN_BF16) {
         __nv_bfloat16* yp = reinterpret_cast<__nv_bfloat16*>(y) + m * N + nb;
@@ -290,6 +291,7 @@ struct W8TcArgs {
     int32_t* acc_out;
     int32_t* drain;   // [M][N] INT32 partial sums, written only when a drain occurs
     int32_t* part;    // [tail tiles][tail_split][BM][BN] INT32 sums of the split tail tiles
+    const float* add; // NULL, or [M][N] binary32 terms added before the output scale: y = (acc*sx + add)*sw
     int64_t full_tiles;  // CTAs [0, full_tiles) own whole tiles
     int tail_split;      // K parts of each later tile (one CTA per part)
     int num_m_tiles;
@@ -580,7 +582,7 @@ __global__ void __launch_bounds__(w8tc::THREADS, 1)
                                 if (nb + j < p.N) dp[j] = tot[j];
                         }
                     } else {
-                        store_row<16>(tot, m, nb, p.N, sxm, p.sw, p.y, p.yt, p.acc_out);
+                        store_row<16>(tot, m, nb, p.N, sxm, p.sw, p.y, p.yt, p.acc_out, p.add);
                     }
                 }
             }
@@ -629,7 +631,7 @@ __global__ void __launch_bounds__(256) k_w8a8_tail(W8TcArgs p, int tail_tiles) {
                 tot[4 * j + 3] += v.w;
             }
         }
-        store_row<16>(tot, m, nb, p.N, p.sx[m], p.sw, p.y, p.yt, p.acc_out);
+        store_row<16>(tot, m, nb, p.N, p.sx[m], p.sw, p.y, p.yt, p.acc_out, p.add);
     }
 }
 
@@ -692,8 +694,8 @@ static int w8a8_kernel_choice() {
 }
 
 cudaError_t run_gemm_w8a8(const int8_t* qx, const float* sx, const int8_t* qw, const float* sw, int64_t M, int64_t N,
-                          int64_t K, void* y, int yt, int32_t* acc_out, void* ws, cudaStream_t st) {
-    if (w8a8_kernel_choice() == 1) {
+                          int64_t K, void* y, int yt, int32_t* acc_out, void* ws, cudaStream_t st, const float* add) {
+    if (w8a8_kernel_choice() == 1 && !add) {
         using namespace w8;
         size_t smem = (size_t)2 * STAGES * TILE_BYTES;
         cudaError_t e = ensure_smem((const void*)k_w8a8_mma, (int)smem);
@@ -732,6 +734,7 @@ cudaError_t run_gemm_w8a8(const int8_t* qx, const float* sx, const int8_t* qw, c
     a.y = y;
     a.yt = yt;
     a.acc_out = acc_out;
+    a.add = add;
     a.drain = reinterpret_cast<int32_t*>(ws);
     a.part = reinterpret_cast<int32_t*>(reinterpret_cast<uint8_t*>(ws) + w8a8_drain_bytes(M, N));  // 16-byte aligned
     a.full_tiles = pl.full_tiles;

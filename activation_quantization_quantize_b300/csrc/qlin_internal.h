@@ -35,7 +35,8 @@ cudaError_t run_smooth_factors(const float* xmax, const float* wmax, int64_t K, 
 // W8A8 (gemm_w8a8.cu)
 size_t w8a8_ws_bytes(int64_t M, int64_t N, int64_t K);
 cudaError_t run_gemm_w8a8(const int8_t* qx, const float* sx, const int8_t* qw, const float* sw, int64_t M,
-                          int64_t N, int64_t K, void* y, int yt, int32_t* acc_out, void* ws, cudaStream_t st);
+                          int64_t N, int64_t K, void* y, int yt, int32_t* acc_out, void* ws, cudaStream_t st,
+                          const float* add = nullptr);
 
 // W4A16 (gemm_w4a16.cu)
 void w4_layout(int64_t N, int64_t K, int group, int asym, qlin_w4_header* h);
@@ -44,5 +45,20 @@ cudaError_t run_pack_w4(const void* q, const void* s_f16, const int32_t* z, cons
 size_t w4a16_ws_bytes(int64_t M, int64_t N, int64_t K);
 cudaError_t run_gemm_w4a16(const void* x, const void* packed, const qlin_w4_header* h, int64_t M, void* y,
                            void* ws, cudaStream_t st);
+
+// W4A8 (gemm_w4a8.cu)
+size_t w4a8_ws_bytes(int64_t M, int64_t N, int64_t K);
+cudaError_t run_gemm_w4a8(const int8_t* qx, const float* sx, const void* packed, const qlin_w4_header* h, int64_t M,
+                          void* y, int yt, int32_t* acc_out, void* ws, cudaStream_t st);
+
+// SmoothQuant calibration (calib.cu)
+cudaError_t run_absmax_update(const void* x, int xt, int64_t rows, int64_t cols, int64_t ld, float* running,
+                              cudaStream_t st);
+cudaError_t run_fold_layernorm(const float* gamma, const float* beta, const float* s, int64_t K, float* gamma_out,
+                               float* beta_out, cudaStream_t st);
+size_t quant_error_ws_bytes();
+cudaError_t run_quant_error(const void* x, int xt, int64_t rows, int64_t cols, int64_t ld, const float* smooth,
+                            const qlin_qparams* p, const void* q, const void* s, const int32_t* z, double* out,
+                            void* ws, cudaStream_t st);
 
 }  // namespace qlin

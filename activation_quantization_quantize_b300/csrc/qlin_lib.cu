@@ -3,5 +3,7 @@
 #include "quantize.cu"
 #include "gemm_w8a8.cu"
 #include "gemm_w4a16.cu"
+#include "gemm_w4a8.cu"
+#include "calib.cu"
 #include "api.cu"
 #include "noalloc.cu"

@@ -19,6 +19,7 @@
 //   k_dequant       x^ = fl(s (q - z)) rounded to the output type.
 #include <map>
 #include <mutex>
+#include <type_traits>
 
 #include "qlin_common.cuh"
 #include "qlin_internal.h"
@@ -300,12 +301,16 @@ __global__ void __launch_bounds__(512, 2) k_quant_longrows(QuantArgs a) {
     }
 }
 
-// Per-token quantize of 16-bit rows streamed through shared memory by bulk
-// copies.  One persistent CTA per SM keeps `nbuf` (2 or 3) row buffers: while
-// it reduces and quantizes row i from one, the copies of its next rows land in
-// the others, so every SM keeps nbuf - 1 rows in flight.  The codes come from
-// code_bits8, as in the other row kernels.
-constexpr int kBulkThreads = 512;
+// ------------------------------------------------------------------ row-local kernels for 16-bit rows
+// The kernels below take per-row and per-group scopes of bf16 / fp16 rows
+// without smoothing (the activation path: SmoothQuant's 1/s is folded into
+// the previous layer).  Their modes are compile-time parameters, so the chunk
+// loops carry no run-time branches; indices inside a row are 32-bit.
+//   SYM / STATIC : dynamic symmetric scopes (no clamp, since |rne(x/s)| <=
+//                  qmax when s comes from the scope's own max|x|), dynamic
+//                  asymmetric scopes (clamp), or static scales (clamp and
+//                  far-range test).
+//   CODE4        : two codes per byte.
 
 // Running range of packed 16-bit pairs: |x| max (symmetric) or max and min.
 template <typename T>
@@ -313,7 +318,7 @@ struct PairRange;
 template <>
 struct PairRange<__nv_bfloat16> {
     __nv_bfloat162 hi = __floats2bfloat162_rn(0.0f, 0.0f), lo = __floats2bfloat162_rn(0.0f, 0.0f);
-    __device__ __forceinline__ void add(const uint4 u, int sym) {
+    __device__ __forceinline__ void add(const uint4 u, bool sym) {
         const uint32_t w[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
@@ -326,7 +331,7 @@ struct PairRange<__nv_bfloat16> {
             }
         }
     }
-    __device__ __forceinline__ void result(int sym, float& h, float& l) const {
+    __device__ __forceinline__ void result(bool sym, float& h, float& l) const {
         h = fmaxf(__low2float(hi), __high2float(hi));
         l = sym ? 0.0f : fminf(__low2float(lo), __high2float(lo));
     }
@@ -334,7 +339,7 @@ struct PairRange<__nv_bfloat16> {
 template <>
 struct PairRange<__half> {
     __half2 hi = __floats2half2_rn(0.0f, 0.0f), lo = __floats2half2_rn(0.0f, 0.0f);
-    __device__ __forceinline__ void add(const uint4 u, int sym) {
+    __device__ __forceinline__ void add(const uint4 u, bool sym) {
         const uint32_t w[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
@@ -347,25 +352,48 @@ struct PairRange<__half> {
             }
         }
     }
-    __device__ __forceinline__ void result(int sym, float& h, float& l) const {
+    __device__ __forceinline__ void result(bool sym, float& h, float& l) const {
         h = fmaxf(__low2float(hi), __high2float(hi));
         l = sym ? 0.0f : fminf(__low2float(lo), __high2float(lo));
     }
 };
-template <>
-struct PairRange<float> {  // not used: binary32 rows take another kernel
-    __device__ __forceinline__ void add(const uint4, int) {}
-    __device__ __forceinline__ void result(int, float& h, float& l) const { h = l = 0.0f; }
-};
 
-template <typename T>
-__global__ void __launch_bounds__(kBulkThreads, 1) k_quant_rows_bulk(QuantArgs a, uint32_t buf_stride, int nbuf) {
+template <bool CODE4>
+__device__ __forceinline__ void put_codes8(uint8_t* __restrict__ qrow, uint32_t c, const uint32_t cb[8]) {
+    if (CODE4)
+        reinterpret_cast<uint32_t*>(qrow)[c] = pack_nibbles8(cb);
+    else
+        reinterpret_cast<uint2*>(qrow)[c] =
+            make_uint2(pack_bytes4(cb[0], cb[1], cb[2], cb[3]), pack_bytes4(cb[4], cb[5], cb[6], cb[7]));
+}
+
+template <typename T, bool SYM, bool STATIC>
+__device__ __forceinline__ void codes_of_chunk(const uint4 raw, const ScopeParams& sp, const CodeRange& cr,
+                                               uint32_t cb[8]) {
+    float v[8];
+    unpack8<T>(raw, v);
+    if (STATIC)
+        code_bits8<false>(v, sp, cr, cb);
+    else if (SYM)
+        code_bits8<true, false>(v, sp, cr, cb);
+    else
+        code_bits8<true>(v, sp, cr, cb);
+}
+
+// Per-token scopes of long rows (more than 4096 values) streamed through
+// shared memory by bulk copies.  Each persistent CTA keeps `nbuf` row buffers:
+// while it reduces and quantizes one row, the copies of its next rows land in
+// the others.  NT threads per CTA; two CTAs of 256 threads with two buffers
+// each fit an SM for rows of up to 28,672 values, so one CTA's barriers
+// overlap the other's work.
+template <typename T, bool SYM, bool STATIC, bool CODE4, int NT>
+__global__ void __launch_bounds__(NT) k_qrow_bulk(QuantArgs a, uint32_t buf_stride, int nbuf) {
     extern __shared__ __align__(128) uint8_t qb_smem[];
-    __shared__ float red_hi[kBulkThreads / 32], red_lo[kBulkThreads / 32];
+    __shared__ float red_hi[NT / 32], red_lo[NT / 32];
     __shared__ __align__(8) uint64_t bar[3];
     __shared__ int abort_flag;
-    const int tid = threadIdx.x, nt = blockDim.x;
-    const int nchunks = (int)(a.cols / 8);  // <= 4096
+    const int tid = threadIdx.x;
+    const uint32_t nchunks = (uint32_t)(a.cols / 8);
     const uint32_t row_bytes = (uint32_t)(a.cols * 2);
     const CodeRange cr = make_range(a.qmin, a.qmax);
     const uint32_t bar0 = tc::smem_addr(&bar[0]);
@@ -389,77 +417,51 @@ __global__ void __launch_bounds__(kBulkThreads, 1) k_quant_rows_bulk(QuantArgs a
         for (int b = 0; b < nbuf; ++b)
             if (blockIdx.x + (int64_t)b * gridDim.x < a.rows) issue(blockIdx.x + (int64_t)b * gridDim.x, b);
     }
+    const int64_t qld = CODE4 ? a.cols / 2 : a.cols;
     int b = 0;
     uint32_t ph = 0;
     for (int64_t r = blockIdx.x; r < a.rows; r += gridDim.x) {
         const bool ok = tc::mbar_wait(bar0 + 8u * b, ph, &abort_flag);
         if (!__syncthreads_and(ok)) break;
         const uint4* xs16 = reinterpret_cast<const uint4*>(qb_smem + (size_t)b * buf_stride);
-        // pass 1: range of the row on packed 16-bit pairs (exact; NaN-ignoring
-        // like fmaxf), four chunks in flight per thread
-        PairRange<T> pr;
-        for (int c0 = tid; c0 < nchunks; c0 += 4 * nt) {
-            uint4 raw[4];
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const int c = c0 + u * nt;
-                raw[u] = c < nchunks ? xs16[c] : make_uint4(0, 0, 0, 0);
-            }
-#pragma unroll
-            for (int u = 0; u < 4; ++u) pr.add(raw[u], a.sym);
-        }
-        float hi, lo;
-        pr.result(a.sym, hi, lo);
-        hi = warp_max(hi);
-        lo = warp_min(lo);
-        if ((tid & 31) == 0) {
-            red_hi[tid >> 5] = hi;
-            red_lo[tid >> 5] = lo;
-        }
-        __syncthreads();
-        hi = 0.0f;
-        lo = 0.0f;
-        for (int w = 0; w < (nt >> 5); ++w) {
-            hi = fmaxf(hi, red_hi[w]);
-            lo = fminf(lo, red_lo[w]);
-        }
         float s;
         int z;
-        if (a.static_scale) {
+        if (STATIC) {
             s = load_scale(a.s, r, a.scale_f16);
             z = a.z ? a.z[r] : 0;
         } else {
-            scale_zero(lo, hi, a.qmin, a.qmax, a.sym, a.scale_f16, s, z);
+            PairRange<T> pr;
+#pragma unroll 4
+            for (uint32_t c = tid; c < nchunks; c += NT) pr.add(xs16[c], SYM);
+            float hi, lo;
+            pr.result(SYM, hi, lo);
+            hi = warp_max(hi);
+            if (!SYM) lo = warp_min(lo);
+            if ((tid & 31) == 0) {
+                red_hi[tid >> 5] = hi;
+                red_lo[tid >> 5] = lo;
+            }
+            __syncthreads();
+            hi = red_hi[0];
+            lo = red_lo[0];
+#pragma unroll
+            for (int w = 1; w < NT / 32; ++w) {
+                hi = fmaxf(hi, red_hi[w]);
+                if (!SYM) lo = fminf(lo, red_lo[w]);
+            }
+            scale_zero(lo, hi, a.qmin, a.qmax, SYM, a.scale_f16, s, z);
             if (tid == 0) {
                 store_scale(a.s, r, a.scale_f16, s);
-                if (a.z) a.z[r] = z;
+                if (!SYM) a.z[r] = z;
             }
         }
-        const ScopeParams p = make_scope(s, z);
-        // pass 2: codes, four chunks in flight per thread
-        for (int c0 = tid; c0 < nchunks; c0 += 4 * nt) {
-            uint4 raw[4];
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const int c = c0 + u * nt;
-                if (c < nchunks) raw[u] = xs16[c];
-            }
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const int c = c0 + u * nt;
-                if (c >= nchunks) break;
-                float v[8];
-                unpack8<T>(raw[u], v);
-                uint32_t cb[8];
-                if (a.static_scale) {
-                    code_bits8<false>(v, p, cr, cb);
-                } else if (a.sym) {
-                    code_bits8<true, false>(v, p, cr, cb);
-                } else {
-                    code_bits8<true>(v, p, cr, cb);
-                }
-                store_codes8(a.q, r, a.cols, c, a.code4, cb);
-            }
+        const ScopeParams sp = make_scope(s, z);
+        uint8_t* qrow = reinterpret_cast<uint8_t*>(a.q) + r * qld;
+#pragma unroll 4
+        for (uint32_t c = tid; c < nchunks; c += NT) {
+            uint32_t cb[8];
+            codes_of_chunk<T, SYM, STATIC>(xs16[c], sp, cr, cb);
+            put_codes8<CODE4>(qrow, c, cb);
         }
         __syncthreads();  // buffer b and red_* are free
         if (tid == 0 && !stalled && r + (int64_t)nbuf * gridDim.x < a.rows) issue(r + (int64_t)nbuf * gridDim.x, b);
@@ -470,97 +472,90 @@ __global__ void __launch_bounds__(kBulkThreads, 1) k_quant_rows_bulk(QuantArgs a
     }
 }
 
-// Row-local scopes (per-row, or per-group with g/8 a power of two <= 32) of
-// 16-bit rows of at most 32 * NC eight-value chunks: one warp per row, the row
-// held in registers (lane l holds chunks l, l + 32, ...), every reduction a
-// register shuffle.  Many warps per SM keep many rows in flight.  Same
-// arithmetic as k_quant_rows_bulk.  (The launcher uses it for per-row scopes:
-// per-group scopes recompute the group's scale in every lane, which costs more
-// than the register-resident k_quant_rows.)
-template <typename T, int NC>
-__global__ void __launch_bounds__(256) k_quant_warprows(QuantArgs a) {
+// Row-local scopes of 16-bit rows of at most 32 * NC eight-value chunks: one
+// warp per row, the row held in registers (lane l holds chunks l, l + 32,
+// ...), every reduction a register shuffle, many warps per SM in flight.
+// ROW: one scope per row; else groups of g = 8 * gl values (gl a power of two
+// <= 32), whose gl lanes reduce together.
+template <typename T, bool SYM, bool STATIC, bool CODE4, bool ROW, int NC>
+__global__ void __launch_bounds__(256) k_qrow_warp(QuantArgs a) {
     const int lane = threadIdx.x & 31;
     const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
-    const int64_t nchunks = a.cols / 8;
-    const bool per_row = a.gran == QLIN_PER_ROW;
-    const int gl = per_row ? 32 : a.group / 8;  // lanes (chunks) per scope within one i
-    const int64_t ngr = per_row ? 1 : a.cols / a.group;
+    const uint32_t nchunks = (uint32_t)(a.cols / 8);
+    const int gl = ROW ? 32 : a.group / 8;
+    const uint32_t ngr = ROW ? 1u : (uint32_t)(a.cols / a.group);
     const CodeRange cr = make_range(a.qmin, a.qmax);
-    const uint4* __restrict__ xg = reinterpret_cast<const uint4*>(a.x);
+    const int64_t qld = CODE4 ? a.cols / 2 : a.cols;
     for (int64_t r = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; r < a.rows; r += nwarps) {
-        const uint4* __restrict__ xr = xg + r * (a.ld / 8);
+        const uint4* __restrict__ xr = reinterpret_cast<const uint4*>(reinterpret_cast<const uint8_t*>(a.x) + r * a.ld * 2);
+        uint8_t* qrow = reinterpret_cast<uint8_t*>(a.q) + r * qld;
         uint4 raw[NC];
 #pragma unroll
         for (int i = 0; i < NC; ++i) {
-            const int64_t c = lane + 32 * i;
+            const uint32_t c = lane + 32u * i;
             raw[i] = c < nchunks ? __ldg(xr + c) : make_uint4(0, 0, 0, 0);
         }
-        auto quant_chunk = [&](const uint4& u, int64_t c, const ScopeParams& sp) {
-            float v[8];
-            unpack8<T>(u, v);
-            uint32_t cb[8];
-            if (a.static_scale) {
-                code_bits8<false>(v, sp, cr, cb);
-            } else if (a.sym) {
-                code_bits8<true, false>(v, sp, cr, cb);
-            } else {
-                code_bits8<true>(v, sp, cr, cb);
-            }
-            store_codes8(a.q, r, a.cols, c, a.code4, cb);
-        };
-        if (per_row) {
+        if (ROW) {
             float s;
             int z;
-            if (a.static_scale) {
+            if (STATIC) {
                 s = load_scale(a.s, r, a.scale_f16);
                 z = a.z ? a.z[r] : 0;
             } else {
                 PairRange<T> pr;
 #pragma unroll
-                for (int i = 0; i < NC; ++i) pr.add(raw[i], a.sym);  // zero padding: the range includes 0
+                for (int i = 0; i < NC; ++i) pr.add(raw[i], SYM);  // zero padding: the range includes 0
                 float hi, lo;
-                pr.result(a.sym, hi, lo);
+                pr.result(SYM, hi, lo);
                 hi = warp_max(hi);
-                lo = warp_min(lo);
-                scale_zero(lo, hi, a.qmin, a.qmax, a.sym, a.scale_f16, s, z);
+                if (!SYM) lo = warp_min(lo);
+                scale_zero(lo, hi, a.qmin, a.qmax, SYM, a.scale_f16, s, z);
                 if (lane == 0) {
                     store_scale(a.s, r, a.scale_f16, s);
-                    if (a.z) a.z[r] = z;
+                    if (!SYM) a.z[r] = z;
                 }
             }
             const ScopeParams sp = make_scope(s, z);
 #pragma unroll
             for (int i = 0; i < NC; ++i) {
-                const int64_t c = lane + 32 * i;
-                if (c < nchunks) quant_chunk(raw[i], c, sp);
+                const uint32_t c = lane + 32u * i;
+                if (c < nchunks) {
+                    uint32_t cb[8];
+                    codes_of_chunk<T, SYM, STATIC>(raw[i], sp, cr, cb);
+                    put_codes8<CODE4>(qrow, c, cb);
+                }
             }
         } else {
 #pragma unroll
             for (int i = 0; i < NC; ++i) {
-                const int64_t c = lane + 32 * i;
-                if (32 * i >= nchunks) break;  // warp-uniform
+                if (32u * i >= nchunks) break;  // warp-uniform
+                const uint32_t c = lane + 32u * i;
                 const int64_t sc = r * ngr + c / gl;
                 float s;
                 int z;
-                if (a.static_scale) {
+                if (STATIC) {
                     s = c < nchunks ? load_scale(a.s, sc, a.scale_f16) : 1.0f;
                     z = (a.z && c < nchunks) ? a.z[sc] : 0;
                 } else {
                     PairRange<T> pr;
-                    pr.add(raw[i], a.sym);
+                    pr.add(raw[i], SYM);
                     float hi, lo;
-                    pr.result(a.sym, hi, lo);
+                    pr.result(SYM, hi, lo);
                     for (int o = 1; o < gl; o <<= 1) {
                         hi = fmaxf(hi, __shfl_xor_sync(0xffffffffu, hi, o));
-                        lo = fminf(lo, __shfl_xor_sync(0xffffffffu, lo, o));
+                        if (!SYM) lo = fminf(lo, __shfl_xor_sync(0xffffffffu, lo, o));
                     }
-                    scale_zero(lo, hi, a.qmin, a.qmax, a.sym, a.scale_f16, s, z);
+                    scale_zero(lo, hi, a.qmin, a.qmax, SYM, a.scale_f16, s, z);
                     if (c < nchunks && (lane & (gl - 1)) == 0) {
                         store_scale(a.s, sc, a.scale_f16, s);
-                        if (a.z) a.z[sc] = z;
+                        if (!SYM) a.z[sc] = z;
                     }
                 }
-                if (c < nchunks) quant_chunk(raw[i], c, make_scope(s, z));
+                if (c < nchunks) {
+                    uint32_t cb[8];
+                    codes_of_chunk<T, SYM, STATIC>(raw[i], make_scope(s, z), cr, cb);
+                    put_codes8<CODE4>(qrow, c, cb);
+                }
             }
         }
     }
@@ -1163,6 +1158,70 @@ static bool rows_kernel_ok(const QuantArgs& a, int xt) {
     return true;
 }
 
+template <typename T, bool SYM, bool STATIC, bool CODE4>
+static cudaError_t launch_qrow_warp_m(const QuantArgs& a, cudaStream_t st) {
+    const int64_t nchunks = a.cols / 8;
+    int64_t grid = ceil_div(a.rows, 8);  // 8 warps (rows) per CTA
+    const int64_t cap = (int64_t)num_sms() * 8;
+    if (grid > cap) grid = cap;
+    const bool row = a.gran == QLIN_PER_ROW;
+    if (nchunks <= 128) {
+        if (row)
+            k_qrow_warp<T, SYM, STATIC, CODE4, true, 4><<<(unsigned)grid, 256, 0, st>>>(a);
+        else
+            k_qrow_warp<T, SYM, STATIC, CODE4, false, 4><<<(unsigned)grid, 256, 0, st>>>(a);
+    } else {
+        if (row)
+            k_qrow_warp<T, SYM, STATIC, CODE4, true, 16><<<(unsigned)grid, 256, 0, st>>>(a);
+        else
+            k_qrow_warp<T, SYM, STATIC, CODE4, false, 16><<<(unsigned)grid, 256, 0, st>>>(a);
+    }
+    return cudaGetLastError();
+}
+
+template <typename T>
+static cudaError_t launch_qrow_warp(const QuantArgs& a, cudaStream_t st) {
+    if (a.static_scale)
+        return a.code4 ? launch_qrow_warp_m<T, true, true, true>(a, st) : launch_qrow_warp_m<T, true, true, false>(a, st);
+    if (a.sym)
+        return a.code4 ? launch_qrow_warp_m<T, true, false, true>(a, st) : launch_qrow_warp_m<T, true, false, false>(a, st);
+    return a.code4 ? launch_qrow_warp_m<T, false, false, true>(a, st) : launch_qrow_warp_m<T, false, false, false>(a, st);
+}
+
+// Shared memory of one SM: two CTAs of two row buffers each fit it for rows of
+// up to 28,672 16-bit values; longer rows take one CTA of 512 threads.
+constexpr size_t kSmemPerSM = 233472;
+
+template <typename T, bool SYM, bool STATIC, bool CODE4>
+static cudaError_t launch_qrow_bulk_m(const QuantArgs& a, uint32_t buf_stride, cudaStream_t st) {
+    const bool two = 2 * (2 * (size_t)buf_stride + 1024 + 512) <= kSmemPerSM;
+    const int nbuf = two ? 2 : (3 * (size_t)buf_stride <= 200 * 1024 ? 3 : 2);
+    const int smem = nbuf * (int)buf_stride;
+    const void* kern = two ? (const void*)k_qrow_bulk<T, SYM, STATIC, CODE4, 256>
+                           : (const void*)k_qrow_bulk<T, SYM, STATIC, CODE4, 512>;
+    cudaError_t e = ensure_smem(kern, smem);
+    if (e != cudaSuccess) return e;
+    int64_t grid = (int64_t)num_sms() * (two ? 2 : 1);
+    if (grid > a.rows) grid = a.rows;
+    if (two)
+        k_qrow_bulk<T, SYM, STATIC, CODE4, 256><<<(unsigned)grid, 256, smem, st>>>(a, buf_stride, nbuf);
+    else
+        k_qrow_bulk<T, SYM, STATIC, CODE4, 512><<<(unsigned)grid, 512, smem, st>>>(a, buf_stride, nbuf);
+    return cudaGetLastError();
+}
+
+template <typename T>
+static cudaError_t launch_qrow_bulk(const QuantArgs& a, uint32_t buf_stride, cudaStream_t st) {
+    if (a.static_scale)
+        return a.code4 ? launch_qrow_bulk_m<T, true, true, true>(a, buf_stride, st)
+                       : launch_qrow_bulk_m<T, true, true, false>(a, buf_stride, st);
+    if (a.sym)
+        return a.code4 ? launch_qrow_bulk_m<T, true, false, true>(a, buf_stride, st)
+                       : launch_qrow_bulk_m<T, true, false, false>(a, buf_stride, st);
+    return a.code4 ? launch_qrow_bulk_m<T, false, false, true>(a, buf_stride, st)
+                   : launch_qrow_bulk_m<T, false, false, false>(a, buf_stride, st);
+}
+
 template <typename T>
 static cudaError_t launch_rows(const QuantArgs& a, cudaStream_t st) {
     int64_t nchunks = a.cols / 8;
@@ -1240,29 +1299,11 @@ static cudaError_t run_quantize_t(QuantArgs a, int xt, const qlin_qparams* p, vo
         const size_t row_bytes = (size_t)a.cols * sizeof(float);
         const size_t raw_bytes = (size_t)a.cols * 2;
         const uint32_t buf_stride = (uint32_t)((raw_bytes + 127) & ~(size_t)127);
-        if (a.gran == QLIN_PER_ROW && !a.absmax_out && xt != QLIN_F32 && a.smooth_mode == QLIN_SMOOTH_NONE &&
-            nchunks <= 512) {
-            int64_t grid = ceil_div(a.rows, 8);
-            const int64_t cap = (int64_t)num_sms() * 8;
-            if (grid > cap) grid = cap;
-            if (nchunks <= 128)
-                k_quant_warprows<T, 4><<<(unsigned)grid, 256, 0, st>>>(a);
-            else if (nchunks <= 256)
-                k_quant_warprows<T, 8><<<(unsigned)grid, 256, 0, st>>>(a);
-            else
-                k_quant_warprows<T, 16><<<(unsigned)grid, 256, 0, st>>>(a);
-            return cudaGetLastError();
-        }
-        if (a.gran == QLIN_PER_ROW && !a.absmax_out && nchunks > 512 && xt != QLIN_F32 &&
-            a.smooth_mode == QLIN_SMOOTH_NONE && 2 * (size_t)buf_stride <= 200 * 1024) {
-            const int nbuf = 3 * (size_t)buf_stride <= 200 * 1024 ? 3 : 2;
-            const int smem = nbuf * (int)buf_stride;
-            cudaError_t e = ensure_smem((const void*)k_quant_rows_bulk<T>, smem);
-            if (e != cudaSuccess) return e;
-            int64_t grid = num_sms();
-            if (grid > a.rows) grid = a.rows;
-            k_quant_rows_bulk<T><<<(unsigned)grid, kBulkThreads, smem, st>>>(a, buf_stride, nbuf);
-            return cudaGetLastError();
+        if constexpr (!std::is_same<T, float>::value) {
+            const bool fast16 = !a.absmax_out && a.smooth_mode == QLIN_SMOOTH_NONE;
+            if (fast16 && nchunks <= 512) return launch_qrow_warp<T>(a, st);
+            if (fast16 && a.gran == QLIN_PER_ROW && 2 * (size_t)buf_stride <= 200 * 1024)
+                return launch_qrow_bulk<T>(a, buf_stride, st);
         }
         if (a.gran == QLIN_PER_ROW && !a.absmax_out && nchunks > 1024 && row_bytes <= 113 * 1024) {
             cudaError_t e = ensure_smem((const void*)k_quant_longrows<T>, (int)row_bytes);

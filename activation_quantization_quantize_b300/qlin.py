@@ -23,7 +23,8 @@ QLIN_F32, QLIN_BF16, QLIN_F16, QLIN_S8, QLIN_U8, QLIN_S4, QLIN_U4, QLIN_S32 = ra
 # qlin_smooth
 QLIN_SMOOTH_NONE, QLIN_SMOOTH_DIVIDE, QLIN_SMOOTH_MULTIPLY = 0, 1, 2
 # operations
-QLIN_OP_QUANTIZE, QLIN_OP_ABSMAX, QLIN_OP_GEMM_W8A8, QLIN_OP_GEMM_W4A16 = 0, 1, 2, 3
+QLIN_OP_QUANTIZE, QLIN_OP_ABSMAX, QLIN_OP_GEMM_W8A8, QLIN_OP_GEMM_W4A16, QLIN_OP_GEMM_W4A8 = 0, 1, 2, 3, 4
+QLIN_OP_QUANT_ERROR = 5
 QLIN_W4_MAGIC, QLIN_W4_VERSION = 0x34574C51, 1
 
 
@@ -73,6 +74,14 @@ def load():
                                    C.POINTER(qlin_w4_header), _P]
         L.qlin_gemm_w8a8.argtypes = [_P, _P, _P, _P, _I64, _I64, _I64, _P, C.c_int, _P, _P, C.c_size_t, _P]
         L.qlin_gemm_w4a16.argtypes = [_P, _P, C.POINTER(qlin_w4_header), _I64, _P, _P, C.c_size_t, _P]
+        L.qlin_gemm_w4a8.argtypes = [_P, _P, _P, C.POINTER(qlin_w4_header), _I64, _P, C.c_int, _P, _P, C.c_size_t, _P]
+        L.qlin_gemm_w4a8.restype = C.c_int
+        L.qlin_absmax_update.argtypes = [_P, C.c_int, _I64, _I64, _I64, _P, _P]
+        L.qlin_fold_layernorm.argtypes = [_P, _P, _P, _I64, _P, _P, _P]
+        L.qlin_quant_error.argtypes = [_P, C.c_int, _I64, _I64, _I64, _P, C.POINTER(qlin_qparams), _P, _P, _P, _P,
+                                       _P, C.c_size_t, _P]
+        for name in ("qlin_absmax_update", "qlin_fold_layernorm", "qlin_quant_error"):
+            getattr(L, name).restype = C.c_int
         L.qlin_device_error.argtypes = [_P]
         L.qlin_debug_stall_producers.argtypes = [C.c_int, C.c_longlong]
         L.qlin_debug_stall_producers.restype = C.c_int
@@ -166,6 +175,12 @@ def qlin_gemm_w8a8(qx, sx, qw, sw, M, N, K, y, yt, acc_out, ws, ws_bytes, stream
 def qlin_gemm_w4a16(x, packed, hdr, M, y, ws, ws_bytes, stream=None):
     return _check("qlin_gemm_w4a16", load().qlin_gemm_w4a16(
         _ptr(x), _ptr(packed), C.byref(hdr), M, _ptr(y), _ptr(ws), ws_bytes, _stream(stream)))
+
+
+def qlin_gemm_w4a8(qx, sx, packed, hdr, M, y, yt, acc_out, ws, ws_bytes, stream=None):
+    return _check("qlin_gemm_w4a8", load().qlin_gemm_w4a8(
+        _ptr(qx), _ptr(sx), _ptr(packed), C.byref(hdr), M, _ptr(y), yt, _ptr(acc_out), _ptr(ws), ws_bytes,
+        _stream(stream)))
 
 
 def qlin_quantize_noalloc(x, xt, rows, cols, ld, smooth, p, q, s, z, stream=None):
@@ -289,3 +304,53 @@ def gemm_w4a16(x, packed, hdr, stream=None, y=None):
     ws = torch.empty(nbytes, dtype=torch.uint8, device=x.device) if nbytes else None
     qlin_gemm_w4a16(x, packed, hdr, M, y, ws, nbytes, stream)
     return y
+
+
+def gemm_w4a8(qx, sx, packed, hdr, out_dtype=torch.bfloat16, acc_out=None, stream=None, y=None):
+    """W4A8: per-token INT8 codes qx [M x K] with scales sx, packed INT4 weight."""
+    M = qx.shape[0]
+    if y is None:
+        y = torch.empty((M, hdr.N), dtype=out_dtype, device=qx.device)
+    nbytes = qlin_workspace_size(QLIN_OP_GEMM_W4A8, M, hdr.N, hdr.K)
+    ws = torch.empty(nbytes, dtype=torch.uint8, device=qx.device) if nbytes else None
+    qlin_gemm_w4a8(qx, sx, packed, hdr, M, y, _TORCH_DT[y.dtype], acc_out, ws, nbytes, stream)
+    return y
+
+
+def qlin_absmax_update(x, xt, rows, cols, ld, running, stream=None):
+    return _check("qlin_absmax_update", load().qlin_absmax_update(_ptr(x), xt, rows, cols, ld, _ptr(running),
+                                                                  _stream(stream)))
+
+
+def qlin_fold_layernorm(gamma, beta, s, K, gamma_out, beta_out, stream=None):
+    return _check("qlin_fold_layernorm", load().qlin_fold_layernorm(_ptr(gamma), _ptr(beta), _ptr(s), K,
+                                                                    _ptr(gamma_out), _ptr(beta_out), _stream(stream)))
+
+
+def qlin_quant_error(x, xt, rows, cols, ld, smooth, p, q, s, z, out, ws, ws_bytes, stream=None):
+    return _check("qlin_quant_error", load().qlin_quant_error(
+        _ptr(x), xt, rows, cols, ld, _ptr(smooth), C.byref(p), _ptr(q), _ptr(s), _ptr(z), _ptr(out), _ptr(ws),
+        ws_bytes, _stream(stream)))
+
+
+def absmax_update(x, running, stream=None):
+    rows, cols = x.shape
+    qlin_absmax_update(x, dtype_code(x), rows, cols, x.stride(0), running, stream)
+    return running
+
+
+def fold_layernorm(gamma, beta, s, stream=None):
+    g2 = torch.empty_like(gamma)
+    b2 = None if beta is None else torch.empty_like(beta)
+    qlin_fold_layernorm(gamma, beta, s, gamma.numel(), g2, b2, stream)
+    return g2, b2
+
+
+def quant_error(x, p, q, s, z, smooth=None, stream=None):
+    """(sum (x' - x^)^2, sum x'^2, max |x' - x^|) as a device binary64 tensor."""
+    rows, cols = x.shape
+    out = torch.empty(3, dtype=torch.float64, device=x.device)
+    n = qlin_workspace_size(QLIN_OP_QUANT_ERROR, 0, 0, 0)
+    ws = torch.empty(n, dtype=torch.uint8, device=x.device)
+    qlin_quant_error(x, dtype_code(x), rows, cols, x.stride(0), smooth, p, q, s, z, out, ws, n, stream)
+    return out

@@ -86,7 +86,8 @@ typedef struct {
 } qlin_qparams;
 
 /* Operation ids for qlin_workspace_size. */
-enum { QLIN_OP_QUANTIZE = 0, QLIN_OP_ABSMAX = 1, QLIN_OP_GEMM_W8A8 = 2, QLIN_OP_GEMM_W4A16 = 3 };
+enum { QLIN_OP_QUANTIZE = 0, QLIN_OP_ABSMAX = 1, QLIN_OP_GEMM_W8A8 = 2, QLIN_OP_GEMM_W4A16 = 3,
+       QLIN_OP_GEMM_W4A8 = 4, QLIN_OP_QUANT_ERROR = 5 };
 
 /* Library version (major*10000 + minor*100 + patch). */
 int qlin_version(void);
@@ -169,6 +170,46 @@ int qlin_absmax(const void *x, qlin_dtype xt, int64_t rows, int64_t cols, int64_
 int qlin_smooth_factors(const float *xmax, const float *wmax, int64_t K, float alpha,
                         float *s, void *stream);
 
+/*
+ * qlin_absmax_update -- SmoothQuant calibration ([CH11] 11.4.5 steps 1-2):
+ * running[j] = max(running[j], max_i |x[i][j]|) over one calibration batch,
+ * so that after all batches running holds max|X_j| over the calibration data.
+ *   x        device, rows x cols of type xt, row stride ld.
+ *   running  device binary32 [cols], non-negative (start from zeros); updated
+ *            in place.  The result does not depend on the order of the
+ *            updates.
+ */
+int qlin_absmax_update(const void *x, qlin_dtype xt, int64_t rows, int64_t cols, int64_t ld, float *running,
+                       void *stream);
+
+/*
+ * qlin_fold_layernorm -- absorbs X diag(s)^-1 into the LayerNorm that
+ * produces X ([CH11] 11.4.4: LayerNorm(X) diag(s)^-1 = LayerNorm'(X) with
+ * gamma' = gamma / s; the bias likewise): gamma_out[j] = fl(gamma[j] / s[j]),
+ * beta_out[j] = fl(beta[j] / s[j]) (correctly rounded binary32 divisions).
+ * beta and beta_out are both NULL for a LayerNorm without bias (RMSNorm).
+ * All pointers device binary32 arrays of K values.
+ */
+int qlin_fold_layernorm(const float *gamma, const float *beta, const float *s, int64_t K, float *gamma_out,
+                        float *beta_out, void *stream);
+
+/*
+ * qlin_quant_error -- quantization-error statistics of a tensor, the measure
+ * behind the choice of the migration strength alpha ([CH11] 11.4.3 table
+ * 11-4: activation and weight INT8 error per alpha).  For every element,
+ * x' = x (smoothed by `smooth` as p->smooth_mode says, the binary32 value the
+ * quantizer sees) and x^ = fl(s * (q - z)) of its scope; writes
+ *   out[0] = sum (x' - x^)^2,  out[1] = sum x'^2,  out[2] = max |x' - x^|
+ * in binary64 to the device array out.  q, s, z are in the layouts
+ * qlin_quantize writes for p.  The sums are taken in a fixed order, so the
+ * result is reproducible.
+ *   ws  device workspace of qlin_workspace_size(QLIN_OP_QUANT_ERROR, ...)
+ *       bytes.
+ */
+int qlin_quant_error(const void *x, qlin_dtype xt, int64_t rows, int64_t cols, int64_t ld, const float *smooth,
+                     const qlin_qparams *p, const void *q, const void *s, const int32_t *z, double *out, void *ws,
+                     size_t ws_bytes, void *stream);
+
 /* Header at the start of a packed INT4 weight blob (layout version 1). */
 #define QLIN_W4_MAGIC 0x34574C51u  /* "QLW4" */
 #define QLIN_W4_VERSION 1u
@@ -239,6 +280,30 @@ int qlin_gemm_w8a8(const int8_t *qx, const float *sx, const int8_t *qw, const fl
  */
 int qlin_gemm_w4a16(const void *x, const void *packed, const qlin_w4_header *hdr, int64_t M,
                     void *y, void *ws, size_t ws_bytes, void *stream);
+
+/*
+ * qlin_gemm_w4a8 -- W4A8 linear layer: group-wise INT4 weights (the packed
+ * blob of qlin_pack_w4) x per-token INT8 activations ([CH11] 11.4.5 step 6,
+ * integer products summed exactly, then the scales; [CH11] 11.9.7 and
+ * 11.10.2: AWQ INT4 weights combined with SmoothQuant INT8 activations).
+ * Every weight group g has its own scale, so the exact integer sums are kept
+ * per group:
+ *   acc_g[m,n] = sum_{k in g} qx[m,k] * (q[n,k] - z[n,g])   (exact, int32)
+ *   y[m,n]     = sx[m] * sum_g s[n,g] * acc_g[m,n]          (binary32, one
+ *                rounding to yt at the end)
+ * with z = 0 for symmetric INT4 codes.
+ *   qx     device int8 [M x K] per-token codes, row-major, 16-byte aligned.
+ *   sx     device binary32 [M] per-token scales.
+ *   packed device blob written by qlin_pack_w4; hdr its header (host copy).
+ *   y      device [M x N] of type yt (F32 or BF16), row-major.
+ *   acc_out NULL, or device int32 [K/g][M][N]: the exact per-group sums
+ *          acc_g (a test aid; the call zeroes it first).
+ *   ws     device workspace of qlin_workspace_size(QLIN_OP_GEMM_W4A8, M, N, K)
+ *          bytes (NULL when 0).
+ * Results are reproducible: partial sums are added in a fixed order.
+ */
+int qlin_gemm_w4a8(const int8_t *qx, const float *sx, const void *packed, const qlin_w4_header *hdr, int64_t M,
+                   void *y, qlin_dtype yt, int32_t *acc_out, void *ws, size_t ws_bytes, void *stream);
 
 /*
  * qlin_quantize_noalloc -- qlin_quantize for callers that cannot allocate

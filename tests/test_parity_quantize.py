@@ -58,7 +58,7 @@ def test_quantize_dynamic(dtype, code, gran, shape):
     run_case(xd, xh, qlin.make_params(code, gran))
 
 
-@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("dtype", ["bf16", "f16", "f32"])
 @pytest.mark.parametrize("code", CODES)
 @pytest.mark.parametrize("group", [8, 32, 64, 128])
 @pytest.mark.parametrize("shape", [(3, 128), (17, 384), (64, 4096), (2, 28672)])
