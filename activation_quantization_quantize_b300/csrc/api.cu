@@ -292,6 +292,95 @@ int qlin_quant_error(const void* x, qlin_dtype xt, int64_t rows, int64_t cols, i
     return cuda_status(run_quant_error(x, xt, rows, cols, ld, smooth, p, q, s, z, out, ws, (cudaStream_t)stream));
 }
 
+size_t qlin_llmint8_workspace_size(int64_t M, int64_t N, int64_t K, int64_t max_outliers) {
+    if (M < 0 || N < 0 || K < 0 || max_outliers < 0 || max_outliers > K) return 0;
+    return llmint8_ws_bytes(M, N, K, max_outliers);
+}
+
+int qlin_gemm_llmint8(const void* x, qlin_dtype xt, int64_t M, int64_t K, int64_t ld, const int8_t* qw,
+                      const float* sw, int64_t N, float threshold, int64_t max_outliers, void* y, qlin_dtype yt,
+                      int32_t* outliers, void* ws, size_t ws_bytes, void* stream) {
+    if (M < 0 || N < 0 || K < 0 || ld < K || max_outliers < 0 || max_outliers > K) return QLIN_ERR_ARG;
+    if (xt != QLIN_BF16) return QLIN_ERR_ARG;
+    if (yt != QLIN_F32 && yt != QLIN_BF16) return QLIN_ERR_ARG;
+    if (!(threshold >= 0.0f) || isinf(threshold)) return QLIN_ERR_ARG;
+    if (K % 16 != 0 || K >= 133144 || K == 0) return QLIN_ERR_UNSUPPORTED;
+    if (M == 0 || N == 0) return QLIN_OK;
+    if (!x || !qw || !sw || !y) return QLIN_ERR_ARG;
+    if (!aligned(x, 16) || (ld * 2) % 16 != 0 || !aligned(qw, 16) || !aligned(sw, 4) ||
+        !aligned(y, type_bytes(yt)) || (outliers && !aligned(outliers, 4)))
+        return QLIN_ERR_ARG;
+    const size_t need = llmint8_ws_bytes(M, N, K, max_outliers);
+    if (!ws || ws_bytes < need || !aligned(ws, 256)) return QLIN_ERR_WORKSPACE;
+    return cuda_status(run_gemm_llmint8(x, xt, M, K, ld, qw, sw, N, threshold, max_outliers, y, yt, outliers, ws,
+                                        (cudaStream_t)stream));
+}
+
+static bool kv_params_ok(int64_t capacity, int C, int D, int G, int R, int bits) {
+    if (capacity < 0 || C <= 0 || D <= 0 || G <= 0 || R < 0) return false;
+    if (C % 16 != 0 || D % 8 != 0 || C % D != 0 || capacity % G != 0) return false;
+    return bits == 4 || bits == 8;
+}
+
+size_t qlin_kv_cache_bytes(int64_t capacity, int channels, int head_dim, int group, int residual, int bits) {
+    if (!kv_params_ok(capacity, channels, head_dim, group, residual, bits)) return 0;
+    size_t off[8], total = 0;
+    kv_layout(capacity, channels, head_dim, group, residual, bits, off, &total);
+    return total;
+}
+
+int qlin_kv_cache_init(qlin_kv_cache* c, void* mem, size_t mem_bytes, int64_t capacity, int channels, int head_dim,
+                       int group, int residual, int bits) {
+    if (!c || !kv_params_ok(capacity, channels, head_dim, group, residual, bits)) return QLIN_ERR_ARG;
+    size_t off[8], total = 0;
+    kv_layout(capacity, channels, head_dim, group, residual, bits, off, &total);
+    if (!mem || !aligned(mem, 256)) return QLIN_ERR_ARG;
+    if (mem_bytes < total) return QLIN_ERR_WORKSPACE;
+    uint8_t* b = reinterpret_cast<uint8_t*>(mem);
+    c->capacity = capacity;
+    c->channels = channels;
+    c->head_dim = head_dim;
+    c->group = group;
+    c->residual = residual;
+    c->bits = bits;
+    c->reserved = 0;
+    c->length = 0;
+    c->quantized = 0;
+    c->k_codes = b + off[0];
+    c->v_codes = b + off[1];
+    c->k_scale = reinterpret_cast<float*>(b + off[2]);
+    c->k_zero = reinterpret_cast<int32_t*>(b + off[3]);
+    c->v_scale = reinterpret_cast<float*>(b + off[4]);
+    c->v_zero = reinterpret_cast<int32_t*>(b + off[5]);
+    c->k_recent = b + off[6];
+    c->v_recent = b + off[7];
+    return QLIN_OK;
+}
+
+int qlin_kv_append(qlin_kv_cache* c, const void* k_new, const void* v_new, int64_t n, void* stream) {
+    if (!c || n < 0) return QLIN_ERR_ARG;
+    if (!kv_params_ok(c->capacity, c->channels, c->head_dim, c->group, c->residual, c->bits)) return QLIN_ERR_ARG;
+    if (c->length < 0 || c->length + n > c->capacity) return QLIN_ERR_ARG;
+    if (n == 0) return QLIN_OK;
+    if (!k_new || !v_new || !aligned(k_new, 16) || !aligned(v_new, 16)) return QLIN_ERR_ARG;
+    const int64_t T2 = c->length + n;
+    const int64_t over = T2 - c->residual;
+    const int64_t q_new = over > 0 ? (over / c->group) * c->group : 0;
+    int rc = cuda_status(run_kv_append(c, k_new, v_new, n, q_new, (cudaStream_t)stream));
+    if (rc != QLIN_OK) return rc;
+    c->length = T2;
+    c->quantized = q_new;
+    return QLIN_OK;
+}
+
+int qlin_kv_read(const qlin_kv_cache* c, void* k_out, void* v_out, void* stream) {
+    if (!c) return QLIN_ERR_ARG;
+    if (!kv_params_ok(c->capacity, c->channels, c->head_dim, c->group, c->residual, c->bits)) return QLIN_ERR_ARG;
+    if (c->length == 0) return QLIN_OK;
+    if (!k_out || !v_out || !aligned(k_out, 16) || !aligned(v_out, 16)) return QLIN_ERR_ARG;
+    return cuda_status(run_kv_read(c, k_out, v_out, (cudaStream_t)stream));
+}
+
 int qlin_device_error(void* stream) {
     if (cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess) return QLIN_ERR_CUDA;
     int v = 0, zero = 0;

@@ -157,10 +157,12 @@ cudaError_t run_absmax_update(const void* x, int xt, int64_t rows, int64_t cols,
     const int es = xt == QLIN_F32 ? 4 : 2;
     const bool vec = cols % 8 == 0 && ((uintptr_t)x % 16 == 0) && ((ld * es) % 16 == 0);
     if (vec) {
+        // a thread keeps 8 columns over a slab of at least 64 rows, so each
+        // column takes few atomics; enough slabs to fill the SMs
         const int64_t nchunks = cols / 8;
         const int64_t gx = ceil_div(nchunks, 256);
         int64_t gy = ceil_div((int64_t)num_sms() * 8, gx);
-        if (gy > rows) gy = rows;
+        if (gy > ceil_div(rows, 64)) gy = ceil_div(rows, 64);
         if (gy < 1) gy = 1;
         const int rpb = (int)ceil_div(rows, gy);
         gy = ceil_div(rows, rpb);

@@ -10,6 +10,8 @@
 //     acc_g[m,n] = sum_{k in g} qx[m,k] * (q[n,k] - z[n,g])     (exact int32)
 //     y[m,n]     = sx[m] * sum_g s[n,g] * acc_g[m,n]            (binary32)
 //
+// k_w4a8_gemv_dp (M = 1, 2): the same streaming with dp4a dot products on
+// the integer pipe.
 // k_w4a8_gemv (M <= 16 per CTA row of token tiles): legacy integer MMAs
 // (mma.sync m16n8k32, u8 weights x s8 activations).  The packed nibbles are
 // used as unsigned codes u (q = u for UINT4, u - 8 for INT4), so
@@ -284,6 +286,189 @@ __global__ void __launch_bounds__(256, 2) k_w4a8_gemv(W4A8Args a) {
     }
 }
 
+// One or two tokens (MX): the m16n8k32 MMA would waste 7/8 of its work on
+// absent tokens, so each lane takes dot products of its own 16 codes of rows
+// gq and gq+8 with the activation bytes by dp4a (integer pipe, no tensor
+// core), and the quad's four partial sums are added exactly at each group's
+// end.  Same streaming ring, same group epilogue arithmetic.
+template <int MX, int NT, int G>
+__global__ void __launch_bounds__(256, 2) k_w4a8_gemv_dp(W4A8Args a) {
+    extern __shared__ __align__(16) uint8_t a8_smem[];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int gq = lane >> 2, t = lane & 3;
+    const int64_t K = a.h.K, N = a.h.N, nchunk = K / 64, ngr = K / G;
+    const int64_t nt0 = (int64_t)blockIdx.x * NT;
+    const int64_t c_begin = nchunk * warp / 8, c_end = nchunk * (warp + 1) / 8;
+    const bool asym = a.h.asym != 0;
+    constexpr int CPG = G >= 64 ? G / 64 : 1;
+
+    const uint32_t cring = tc::smem_addr(a8_smem + warp * (A8_D * NT * 512) + lane * 16);
+    const uint32_t mring = tc::smem_addr(a8_smem + 8 * A8_D * NT * 512 + warp * (A8_D * NT * 256) + lane * 8);
+    const uint8_t* cring_p = a8_smem + warp * (A8_D * NT * 512) + lane * 16;
+    const uint8_t* mring_p = a8_smem + 8 * A8_D * NT * 512 + warp * (A8_D * NT * 256) + lane * 8;
+    const uint8_t* gcodes = a.blob + a.h.codes_off + lane * 16;
+    const uint8_t* gscales = a.blob + a.h.scales_off + gq * 4;
+    const uint8_t* gzeros = a.blob + a.h.zeros_off + (gq & 4);
+    const int zshift = 8 * (gq & 3);
+
+    auto issue = [&](int slot, int64_t kc) {
+        if (kc < c_end) {
+            const int64_t gi = (kc * 64 + 16 * t) / G;
+#pragma unroll
+            for (int n = 0; n < NT; ++n) {
+                const int sl = slot * NT + n;
+                cp_async16(cring + sl * 512, gcodes + ((nt0 + n) * nchunk + kc) * 512);
+                cp_async4(mring + sl * 256, gscales + ((nt0 + n) * ngr + gi) * 32);
+                if (asym) cp_async4(mring + sl * 256 + 4, gzeros + ((nt0 + n) * ngr + gi) * 8);
+            }
+        }
+        cp_async_commit();
+    };
+    const int8_t* xr[MX];
+#pragma unroll
+    for (int u = 0; u < MX; ++u) xr[u] = a.qx + (u < a.M ? u : a.M - 1) * K + 16 * t;
+
+    int ag[NT][MX], ah[NT][MX];   // this lane's exact partial sums, rows gq and gq+8
+    float tot[NT][MX][2];
+    int S[MX];                    // this lane's part of the token's code sum over the group
+#pragma unroll
+    for (int n = 0; n < NT; ++n)
+#pragma unroll
+        for (int u = 0; u < MX; ++u) {
+            ag[n][u] = ah[n][u] = 0;
+            tot[n][u][0] = tot[n][u][1] = 0.0f;
+        }
+#pragma unroll
+    for (int u = 0; u < MX; ++u) S[u] = 0;
+
+#pragma unroll 1
+    for (int i = 0; i < A8_D - 1; ++i) issue(i, c_begin + i);
+    uint4 xn[MX];
+#pragma unroll
+    for (int u = 0; u < MX; ++u)
+        if (c_begin < c_end) xn[u] = __ldg(reinterpret_cast<const uint4*>(xr[u] + c_begin * 64));
+
+    int slot = 0;
+    for (int64_t kc = c_begin; kc < c_end; ++kc) {
+        issue(slot == 0 ? A8_D - 1 : slot - 1, kc + A8_D - 1);
+        uint32_t b[MX][4];
+#pragma unroll
+        for (int u = 0; u < MX; ++u) {
+            const uint32_t w4[4] = {xn[u].x, xn[u].y, xn[u].z, xn[u].w};
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                b[u][j] = __byte_perm(w4[j], 0, 0x3120);  // the weights' k order (0, 2, 1, 3)
+                S[u] = sum_s8x4(w4[j], S[u]);
+            }
+        }
+        if (kc + 1 < c_end) {
+#pragma unroll
+            for (int u = 0; u < MX; ++u) xn[u] = __ldg(reinterpret_cast<const uint4*>(xr[u] + (kc + 1) * 64));
+        }
+        cp_async_wait<A8_D - 1>();
+        const bool group_end = (G <= 64) || ((kc + 1) % CPG == 0) || (kc + 1 == c_end);
+#pragma unroll
+        for (int n = 0; n < NT; ++n) {
+            const int sl = slot * NT + n;
+            const uint4 cw = *reinterpret_cast<const uint4*>(cring_p + sl * 512);
+            const uint2 mw = *reinterpret_cast<const uint2*>(mring_p + sl * 256);
+            const uint32_t wd[4] = {cw.x, cw.y, cw.z, cw.w};
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int lo = (int)(wd[j] & 0x0F0F0F0Fu);          // row gq: four codes in [0, 15]
+                const int hi = (int)((wd[j] >> 4) & 0x0F0F0F0Fu);   // row gq + 8
+#pragma unroll
+                for (int u = 0; u < MX; ++u) {
+                    ag[n][u] = __dp4a(lo, (int)b[u][j], ag[n][u]);
+                    ah[n][u] = __dp4a(hi, (int)b[u][j], ah[n][u]);
+                }
+            }
+            if (G == 32 || group_end) {
+                const uint32_t zb = asym ? (mw.y >> zshift) & 0xFFu : 0x88u;
+                const int zg = (int)(zb & 0xFu), zh = (int)((zb >> 4) & 0xFu);
+                __half2 s2h = *reinterpret_cast<const __half2*>(&mw.x);
+                const float2 sf = __half22float2(s2h);
+#pragma unroll
+                for (int u = 0; u < MX; ++u) {
+                    int cg = ag[n][u] - zg * S[u], ch = ah[n][u] - zh * S[u];
+                    // G = 32: lanes t < 2 and t >= 2 hold different groups
+                    cg += __shfl_xor_sync(0xffffffffu, cg, 1);
+                    ch += __shfl_xor_sync(0xffffffffu, ch, 1);
+                    if (G != 32) {
+                        cg += __shfl_xor_sync(0xffffffffu, cg, 2);
+                        ch += __shfl_xor_sync(0xffffffffu, ch, 2);
+                    }
+                    if (a.acc_out && (t & (G == 32 ? 1 : 3)) == 0 && u < a.M) {
+                        const int64_t gi = (kc * 64 + 16 * t) / G;
+                        int32_t* base = a.acc_out + gi * a.M * N + (int64_t)u * N;
+                        atomicAdd(base + (nt0 + n) * 16 + gq, cg);
+                        atomicAdd(base + (nt0 + n) * 16 + gq + 8, ch);
+                    }
+                    tot[n][u][0] = fmaf(sf.x, (float)cg, tot[n][u][0]);
+                    tot[n][u][1] = fmaf(sf.y, (float)ch, tot[n][u][1]);
+                    ag[n][u] = ah[n][u] = 0;
+                }
+            }
+        }
+        if (G == 32 || group_end) {
+#pragma unroll
+            for (int u = 0; u < MX; ++u) S[u] = 0;
+        }
+        slot = slot + 1 == A8_D ? 0 : slot + 1;
+    }
+    cp_async_wait<0>();
+    __syncthreads();
+    // G = 32: lanes t and t ^ 2 hold the two groups of a chunk -- add them
+    float(*part)[NT * 16][2] = reinterpret_cast<float(*)[NT * 16][2]>(a8_smem);  // [warp][row][token]
+#pragma unroll
+    for (int n = 0; n < NT; ++n)
+#pragma unroll
+        for (int u = 0; u < MX; ++u) {
+            float g0 = tot[n][u][0], g1 = tot[n][u][1];
+            if (G == 32) {
+                g0 += __shfl_xor_sync(0xffffffffu, g0, 2);
+                g1 += __shfl_xor_sync(0xffffffffu, g1, 2);
+            }
+            if (t == 0) {
+                part[warp][n * 16 + gq][u] = g0;
+                part[warp][n * 16 + gq + 8][u] = g1;
+            }
+        }
+    __syncthreads();
+    for (int i = threadIdx.x; i < NT * 16 * MX; i += blockDim.x) {
+        const int row = i / MX, tok = i % MX;
+        if (tok < a.M) {
+            float s = 0.0f;
+#pragma unroll
+            for (int w = 0; w < 8; ++w) s += part[w][row][tok];
+            const float v = a.sx[tok] * s;
+            const int64_t o = (int64_t)tok * N + nt0 * 16 + row;
+            if (a.yt == QLIN_BF16)
+                reinterpret_cast<__nv_bfloat16*>(a.y)[o] = __float2bfloat16_rn(v);
+            else
+                reinterpret_cast<float*>(a.y)[o] = v;
+        }
+    }
+}
+
+template <int MX, int NT, int G>
+static cudaError_t launch_a8_gemv_dp(const W4A8Args& a, cudaStream_t st) {
+    constexpr int smem = a8_gemv_smem_bytes<NT>();
+    cudaError_t e = ensure_smem((const void*)k_w4a8_gemv_dp<MX, NT, G>, smem);
+    if (e != cudaSuccess) return e;
+    k_w4a8_gemv_dp<MX, NT, G><<<(unsigned)(a.h.N / (16 * NT)), 256, smem, st>>>(a);
+    return cudaGetLastError();
+}
+
+template <int MX, int NT>
+static cudaError_t launch_a8_gemv_dp_g(const W4A8Args& a, cudaStream_t st) {
+    switch (a.h.group) {
+    case 32: return launch_a8_gemv_dp<MX, NT, 32>(a, st);
+    case 64: return launch_a8_gemv_dp<MX, NT, 64>(a, st);
+    default: return launch_a8_gemv_dp<MX, NT, 128>(a, st);
+    }
+}
+
 template <int MT, int NT, int G>
 static cudaError_t launch_a8_gemv(const W4A8Args& a, unsigned mgroups, cudaStream_t st) {
     constexpr int smem = a8_gemv_smem_bytes<NT>();
@@ -330,6 +515,8 @@ cudaError_t run_gemm_w4a8(const int8_t* qx, const float* sx, const void* packed,
     // Two 16-row tiles per CTA (one activation load serves both) when that
     // still leaves at least one CTA per SM.
     const bool two = (h->N % 32 == 0) && (h->N / 32 >= num_sms());
+    if (M == 1) return two ? launch_a8_gemv_dp_g<1, 2>(a, st) : launch_a8_gemv_dp_g<1, 1>(a, st);
+    if (M == 2) return two ? launch_a8_gemv_dp_g<2, 2>(a, st) : launch_a8_gemv_dp_g<2, 1>(a, st);
     if (M <= 8) return two ? launch_a8_gemv_g<1, 2>(a, 1, st) : launch_a8_gemv_g<1, 1>(a, 1, st);
     const unsigned mg = (unsigned)ceil_div(M, 16);
     return two ? launch_a8_gemv_g<2, 2>(a, mg, st) : launch_a8_gemv_g<2, 1>(a, mg, st);

@@ -248,7 +248,22 @@ __device__ __forceinline__ void store_row(const int (&tot)[W], int64_t m, int64_
     for (int j = 0; j < W; ++j) {
         float swn = (nb + j < N) ? __ldg(sw + nb + j) : 0.0f;
         f[j] = ((float)tot[j] * sxm) * swn;
-        if (add && nb + j < N) f[j] = fmaf(__ldg(add + m * N + nb + j), swn, f[j]);
+    }
+    if (add) {  // y = (acc * sx + add) * sw, the addend's row segment read as 16-byte vectors
+        const float* ap = add + m * N + nb;
+        if (full) {
+#pragma unroll
+            for (int j = 0; j < W; j += 4) {
+                const float4 v = __ldg(reinterpret_cast<const float4*>(ap + j));
+                f[j] = fmaf(v.x, __ldg(sw + nb + j), f[j]);
+                f[j + 1] = fmaf(v.y, __ldg(sw + nb + j + 1), f[j + 1]);
+                f[j + 2] = fmaf(v.z, __ldg(sw + nb + j + 2), f[j + 2]);
+                f[j + 3] = fmaf(v.w, __ldg(sw + nb + j + 3), f[j + 3]);
+            }
+        } else {
+            for (int j = 0; j < W; ++j)
+                if (nb + j < N) f[j] = fmaf(__ldg(ap + j), __ldg(sw + nb + j), f[j]);
+        }
     }
     if (yt == QLIN_BF16) {
         __nv_bfloat16* yp = reinterpret_cast<__nv_bfloat16*>(y) + m * N + nb;

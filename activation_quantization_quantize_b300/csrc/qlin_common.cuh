@@ -23,13 +23,15 @@ __device__ int g_device_error = 0;
 
 __device__ __forceinline__ void raise_device_error(int code) { atomicExch(&g_device_error, code); }
 
-// Cycle limit of every bounded device-side wait (about 2 s at 2 GHz).
+// Cycle limit of every bounded device-side wait (about 2 s at 2 GHz), in
+// constant memory: the waits read it from the constant cache.  Changed only
+// between kernels (qlin_debug_stall_producers synchronizes the device).
 constexpr long long kDefaultWaitLimitCycles = 4000000000LL;
-__device__ long long g_wait_limit_cycles = kDefaultWaitLimitCycles;
+__constant__ long long g_wait_limit_cycles = kDefaultWaitLimitCycles;
 // Failure-detection test hook (qlin_debug_stall_producers): while non-zero,
 // the producer roles of the pipelined kernels issue no copies, so the
 // consumers' bounded waits run out and the kernels take their abort path.
-__device__ int g_stall_producers = 0;
+__constant__ int g_stall_producers = 0;
 
 // ---------------------------------------------------------------- loads / stores
 template <typename T>
@@ -158,6 +160,21 @@ __device__ __forceinline__ void scale_zero(float lo, float hi, int qmin, int qma
     }
 }
 
+__device__ __forceinline__ ScopeParams make_scope(float s, int z);
+
+// scale_zero then make_scope, out of line: per-group loops call it once per
+// group and unrolled copies of the correctly rounded divisions would fill the
+// instruction cache.
+struct ScopeOf {
+    float s;
+    int z;
+};
+__device__ __noinline__ ScopeOf scope_of_range(float lo, float hi, int qmin, int qmax, bool sym, bool f16) {
+    ScopeOf r;
+    scale_zero(lo, hi, qmin, qmax, sym, f16, r.s, r.z);
+    return r;
+}
+
 __device__ __forceinline__ ScopeParams make_scope(float s, int z) {
     ScopeParams p;
     p.s = s;
@@ -247,6 +264,18 @@ __device__ __forceinline__ float2 f2_mul(float2 a, float2 b) {
     return d;
 }
 
+// The exact per-element path of a chunk that failed the fast test (a
+// near-tie, or a value far outside the code range), out of line: kernels
+// that unroll many chunks with little register pressure take it (inlined
+// at every unrolled chunk it fills the instruction cache), kernels with many
+// live registers keep it inline (a call would save them around it).
+__device__ __noinline__ void code_bits8_exact(float v0, float v1, float v2, float v3, float v4, float v5, float v6,
+                                              float v7, ScopeParams p, CodeRange cr, uint32_t* cb) {
+    const float v[8] = {v0, v1, v2, v3, v4, v5, v6, v7};
+#pragma unroll 1
+    for (int j = 0; j < 8; ++j) cb[j] = code_bits(v[j], p, cr);
+}
+
 // code_bits() of eight values with one branch.  The fast candidates of all
 // eight are formed in one basic block on packed pairs, and the near-tie test
 // |d| < hs becomes the sign of d*d - hs*hs (one fused multiply-add per pair;
@@ -258,7 +287,7 @@ __device__ __forceinline__ float2 f2_mul(float2 a, float2 b) {
 // the clamp to [qmin, qmax]; callers use it only for symmetric scopes whose
 // scale came from the scope's own absmax, where |rne(v/s)| <= qmax always
 // holds.  Same results as code_bits() / code_bits_inrange() per element.
-template <bool kInRange, bool kClamp = true>
+template <bool kInRange, bool kClamp = true, bool kOutline = false>
 __device__ __forceinline__ void code_bits8(const float v[8], const ScopeParams& p, const CodeRange& cr,
                                            uint32_t cb[8]) {
     float m[8];
@@ -287,6 +316,12 @@ __device__ __forceinline__ void code_bits8(const float v[8], const ScopeParams& 
     if (neg & 0x80000000u) {
 #pragma unroll
         for (int j = 0; j < 8; ++j) cb[j] = __float_as_uint(kClamp ? fminf(fmaxf(m[j], cr.lo), cr.hi) : m[j]);
+    } else if (kOutline) {
+        // (code_bits equals code_bits_inrange wherever the latter applies)
+        uint32_t t8[8];
+        code_bits8_exact(v[0], v[1], v[2], v[3], v[4], v[5], v[6], v[7], p, cr, t8);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) cb[j] = t8[j];
     } else {
 #pragma unroll
         for (int j = 0; j < 8; ++j) cb[j] = kInRange ? code_bits_inrange(v[j], p, cr) : code_bits(v[j], p, cr);

@@ -61,4 +61,16 @@ cudaError_t run_quant_error(const void* x, int xt, int64_t rows, int64_t cols, i
                             const qlin_qparams* p, const void* q, const void* s, const int32_t* z, double* out,
                             void* ws, cudaStream_t st);
 
+// LLM.int8() decomposition (llmint8.cu)
+size_t llmint8_ws_bytes(int64_t M, int64_t N, int64_t K, int64_t max_outliers);
+cudaError_t run_gemm_llmint8(const void* x, int xt, int64_t M, int64_t K, int64_t ld, const int8_t* qw,
+                             const float* sw, int64_t N, float threshold, int64_t max_outliers, void* y, int yt,
+                             int32_t* report, void* ws, cudaStream_t st);
+
+// KV-cache quantization (kvcache.cu)
+void kv_layout(int64_t capacity, int C, int D, int G, int R, int bits, size_t off[8], size_t* total);
+cudaError_t run_kv_append(const qlin_kv_cache* c, const void* k_new, const void* v_new, int64_t n, int64_t q_new,
+                          cudaStream_t st);
+cudaError_t run_kv_read(const qlin_kv_cache* c, void* k_out, void* v_out, cudaStream_t st);
+
 }  // namespace qlin

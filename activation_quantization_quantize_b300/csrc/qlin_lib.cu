@@ -5,5 +5,7 @@
 #include "gemm_w4a16.cu"
 #include "gemm_w4a8.cu"
 #include "calib.cu"
+#include "llmint8.cu"
+#include "kvcache.cu"
 #include "api.cu"
 #include "noalloc.cu"

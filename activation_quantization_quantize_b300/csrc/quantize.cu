@@ -367,25 +367,25 @@ __device__ __forceinline__ void put_codes8(uint8_t* __restrict__ qrow, uint32_t 
             make_uint2(pack_bytes4(cb[0], cb[1], cb[2], cb[3]), pack_bytes4(cb[4], cb[5], cb[6], cb[7]));
 }
 
-template <typename T, bool SYM, bool STATIC>
+template <typename T, bool SYM, bool STATIC, bool OUTLINE = false>
 __device__ __forceinline__ void codes_of_chunk(const uint4 raw, const ScopeParams& sp, const CodeRange& cr,
                                                uint32_t cb[8]) {
     float v[8];
     unpack8<T>(raw, v);
     if (STATIC)
-        code_bits8<false>(v, sp, cr, cb);
+        code_bits8<false, true, OUTLINE>(v, sp, cr, cb);
     else if (SYM)
-        code_bits8<true, false>(v, sp, cr, cb);
+        code_bits8<true, false, OUTLINE>(v, sp, cr, cb);
     else
-        code_bits8<true>(v, sp, cr, cb);
+        code_bits8<true, true, OUTLINE>(v, sp, cr, cb);
 }
 
 // Per-token scopes of long rows (more than 4096 values) streamed through
 // shared memory by bulk copies.  Each persistent CTA keeps `nbuf` row buffers:
 // while it reduces and quantizes one row, the copies of its next rows land in
-// the others.  NT threads per CTA; two CTAs of 256 threads with two buffers
-// each fit an SM for rows of up to 28,672 values, so one CTA's barriers
-// overlap the other's work.
+// the others.  NT threads per CTA; two CTAs with two buffers each fit an SM
+// for rows of up to 28,672 values, so one CTA's barriers overlap the other's
+// work.
 template <typename T, bool SYM, bool STATIC, bool CODE4, int NT>
 __global__ void __launch_bounds__(NT) k_qrow_bulk(QuantArgs a, uint32_t buf_stride, int nbuf) {
     extern __shared__ __align__(128) uint8_t qb_smem[];
@@ -460,7 +460,7 @@ __global__ void __launch_bounds__(NT) k_qrow_bulk(QuantArgs a, uint32_t buf_stri
 #pragma unroll 4
         for (uint32_t c = tid; c < nchunks; c += NT) {
             uint32_t cb[8];
-            codes_of_chunk<T, SYM, STATIC>(xs16[c], sp, cr, cb);
+            codes_of_chunk<T, SYM, STATIC, false>(xs16[c], sp, cr, cb);
             put_codes8<CODE4>(qrow, c, cb);
         }
         __syncthreads();  // buffer b and red_* are free
@@ -472,18 +472,14 @@ __global__ void __launch_bounds__(NT) k_qrow_bulk(QuantArgs a, uint32_t buf_stri
     }
 }
 
-// Row-local scopes of 16-bit rows of at most 32 * NC eight-value chunks: one
+// Per-row scopes of 16-bit rows of at most 32 * NC eight-value chunks: one
 // warp per row, the row held in registers (lane l holds chunks l, l + 32,
 // ...), every reduction a register shuffle, many warps per SM in flight.
-// ROW: one scope per row; else groups of g = 8 * gl values (gl a power of two
-// <= 32), whose gl lanes reduce together.
-template <typename T, bool SYM, bool STATIC, bool CODE4, bool ROW, int NC>
+template <typename T, bool SYM, bool STATIC, bool CODE4, int NC>
 __global__ void __launch_bounds__(256) k_qrow_warp(QuantArgs a) {
     const int lane = threadIdx.x & 31;
     const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
     const uint32_t nchunks = (uint32_t)(a.cols / 8);
-    const int gl = ROW ? 32 : a.group / 8;
-    const uint32_t ngr = ROW ? 1u : (uint32_t)(a.cols / a.group);
     const CodeRange cr = make_range(a.qmin, a.qmax);
     const int64_t qld = CODE4 ? a.cols / 2 : a.cols;
     for (int64_t r = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; r < a.rows; r += nwarps) {
@@ -495,7 +491,7 @@ __global__ void __launch_bounds__(256) k_qrow_warp(QuantArgs a) {
             const uint32_t c = lane + 32u * i;
             raw[i] = c < nchunks ? __ldg(xr + c) : make_uint4(0, 0, 0, 0);
         }
-        if (ROW) {
+        {
             float s;
             int z;
             if (STATIC) {
@@ -521,42 +517,63 @@ __global__ void __launch_bounds__(256) k_qrow_warp(QuantArgs a) {
                 const uint32_t c = lane + 32u * i;
                 if (c < nchunks) {
                     uint32_t cb[8];
-                    codes_of_chunk<T, SYM, STATIC>(raw[i], sp, cr, cb);
+                    codes_of_chunk<T, SYM, STATIC, true>(raw[i], sp, cr, cb);
                     put_codes8<CODE4>(qrow, c, cb);
                 }
             }
+        }
+    }
+}
+
+// Per-group scopes of 16-bit rows (g = 8 * GL values, GL a power of two <=
+// 32): a warp takes slabs of 32 chunks (256 values) in a grid-stride loop
+// over every (row, slab), one chunk per lane; the GL lanes of a group reduce
+// with shuffles and compute its scale in registers.  Little register
+// pressure, so many warps per SM keep many slabs in flight.
+template <typename T, bool SYM, bool STATIC, bool CODE4, int GL>
+__global__ void __launch_bounds__(256) k_qgrp_slab(QuantArgs a) {
+    const int lane = threadIdx.x & 31;
+    const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+    const uint32_t nchunks = (uint32_t)(a.cols / 8);
+    const uint32_t slabs = (nchunks + 31) / 32;
+    const uint32_t ngr = (uint32_t)(a.cols / a.group);
+    const int64_t units = a.rows * (int64_t)slabs;
+    const CodeRange cr = make_range(a.qmin, a.qmax);
+    const int64_t qld = CODE4 ? a.cols / 2 : a.cols;
+#pragma unroll 2
+    for (int64_t u = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; u < units; u += nwarps) {
+        const int64_t r = u / slabs;
+        const uint32_t c = (uint32_t)(u - r * slabs) * 32u + lane;
+        const bool live = c < nchunks;  // whole groups: a group's lanes are all live or all idle
+        const uint4 raw = live ? __ldg(reinterpret_cast<const uint4*>(reinterpret_cast<const uint8_t*>(a.x) +
+                                                                      r * a.ld * 2) + c)
+                               : make_uint4(0, 0, 0, 0);
+        const int64_t sc = r * ngr + c / GL;
+        float s;
+        int z;
+        if (STATIC) {
+            s = live ? load_scale(a.s, sc, a.scale_f16) : 1.0f;
+            z = (a.z && live) ? a.z[sc] : 0;
         } else {
+            PairRange<T> pr;
+            pr.add(raw, SYM);
+            float hi, lo;
+            pr.result(SYM, hi, lo);
 #pragma unroll
-            for (int i = 0; i < NC; ++i) {
-                if (32u * i >= nchunks) break;  // warp-uniform
-                const uint32_t c = lane + 32u * i;
-                const int64_t sc = r * ngr + c / gl;
-                float s;
-                int z;
-                if (STATIC) {
-                    s = c < nchunks ? load_scale(a.s, sc, a.scale_f16) : 1.0f;
-                    z = (a.z && c < nchunks) ? a.z[sc] : 0;
-                } else {
-                    PairRange<T> pr;
-                    pr.add(raw[i], SYM);
-                    float hi, lo;
-                    pr.result(SYM, hi, lo);
-                    for (int o = 1; o < gl; o <<= 1) {
-                        hi = fmaxf(hi, __shfl_xor_sync(0xffffffffu, hi, o));
-                        if (!SYM) lo = fminf(lo, __shfl_xor_sync(0xffffffffu, lo, o));
-                    }
-                    scale_zero(lo, hi, a.qmin, a.qmax, SYM, a.scale_f16, s, z);
-                    if (c < nchunks && (lane & (gl - 1)) == 0) {
-                        store_scale(a.s, sc, a.scale_f16, s);
-                        if (!SYM) a.z[sc] = z;
-                    }
-                }
-                if (c < nchunks) {
-                    uint32_t cb[8];
-                    codes_of_chunk<T, SYM, STATIC>(raw[i], make_scope(s, z), cr, cb);
-                    put_codes8<CODE4>(qrow, c, cb);
-                }
+            for (int o = 1; o < GL; o <<= 1) {
+                hi = fmaxf(hi, __shfl_xor_sync(0xffffffffu, hi, o));
+                if (!SYM) lo = fminf(lo, __shfl_xor_sync(0xffffffffu, lo, o));
             }
+            scale_zero(lo, hi, a.qmin, a.qmax, SYM, a.scale_f16, s, z);
+            if (live && (lane & (GL - 1)) == 0) {
+                store_scale(a.s, sc, a.scale_f16, s);
+                if (!SYM) a.z[sc] = z;
+            }
+        }
+        if (live) {
+            uint32_t cb[8];
+            codes_of_chunk<T, SYM, STATIC, true>(raw, make_scope(s, z), cr, cb);
+            put_codes8<CODE4>(reinterpret_cast<uint8_t*>(a.q) + r * qld, c, cb);
         }
     }
 }
@@ -1158,6 +1175,17 @@ static bool rows_kernel_ok(const QuantArgs& a, int xt) {
     return true;
 }
 
+template <typename T, bool SYM, bool STATIC, bool CODE4, int GL>
+static cudaError_t launch_qgrp_warp(const QuantArgs& a, int64_t nchunks, int64_t grid, cudaStream_t st) {
+    (void)grid;
+    const int64_t units = a.rows * ceil_div(nchunks, 32);
+    int64_t g = ceil_div(units, 8);  // 8 warps per CTA
+    const int64_t cap = (int64_t)num_sms() * 16;
+    if (g > cap) g = cap;
+    k_qgrp_slab<T, SYM, STATIC, CODE4, GL><<<(unsigned)g, 256, 0, st>>>(a);
+    return cudaGetLastError();
+}
+
 template <typename T, bool SYM, bool STATIC, bool CODE4>
 static cudaError_t launch_qrow_warp_m(const QuantArgs& a, cudaStream_t st) {
     const int64_t nchunks = a.cols / 8;
@@ -1165,18 +1193,22 @@ static cudaError_t launch_qrow_warp_m(const QuantArgs& a, cudaStream_t st) {
     const int64_t cap = (int64_t)num_sms() * 8;
     if (grid > cap) grid = cap;
     const bool row = a.gran == QLIN_PER_ROW;
-    if (nchunks <= 128) {
-        if (row)
-            k_qrow_warp<T, SYM, STATIC, CODE4, true, 4><<<(unsigned)grid, 256, 0, st>>>(a);
+    if (row) {
+        if (nchunks <= 128)
+            k_qrow_warp<T, SYM, STATIC, CODE4, 4><<<(unsigned)grid, 256, 0, st>>>(a);
         else
-            k_qrow_warp<T, SYM, STATIC, CODE4, false, 4><<<(unsigned)grid, 256, 0, st>>>(a);
-    } else {
-        if (row)
-            k_qrow_warp<T, SYM, STATIC, CODE4, true, 16><<<(unsigned)grid, 256, 0, st>>>(a);
-        else
-            k_qrow_warp<T, SYM, STATIC, CODE4, false, 16><<<(unsigned)grid, 256, 0, st>>>(a);
+            k_qrow_warp<T, SYM, STATIC, CODE4, 16><<<(unsigned)grid, 256, 0, st>>>(a);
+        return cudaGetLastError();
     }
-    return cudaGetLastError();
+    // per-group: lanes per group as a compile-time constant (g = 8 * GL)
+    switch (a.group / 8) {
+    case 1: return launch_qgrp_warp<T, SYM, STATIC, CODE4, 1>(a, nchunks, grid, st);
+    case 2: return launch_qgrp_warp<T, SYM, STATIC, CODE4, 2>(a, nchunks, grid, st);
+    case 4: return launch_qgrp_warp<T, SYM, STATIC, CODE4, 4>(a, nchunks, grid, st);
+    case 8: return launch_qgrp_warp<T, SYM, STATIC, CODE4, 8>(a, nchunks, grid, st);
+    case 16: return launch_qgrp_warp<T, SYM, STATIC, CODE4, 16>(a, nchunks, grid, st);
+    default: return launch_qgrp_warp<T, SYM, STATIC, CODE4, 32>(a, nchunks, grid, st);
+    }
 }
 
 template <typename T>
@@ -1189,7 +1221,7 @@ static cudaError_t launch_qrow_warp(const QuantArgs& a, cudaStream_t st) {
 }
 
 // Shared memory of one SM: two CTAs of two row buffers each fit it for rows of
-// up to 28,672 16-bit values; longer rows take one CTA of 512 threads.
+// up to 28,672 16-bit values; longer rows take one CTA with three buffers.
 constexpr size_t kSmemPerSM = 233472;
 
 template <typename T, bool SYM, bool STATIC, bool CODE4>
@@ -1197,16 +1229,14 @@ static cudaError_t launch_qrow_bulk_m(const QuantArgs& a, uint32_t buf_stride, c
     const bool two = 2 * (2 * (size_t)buf_stride + 1024 + 512) <= kSmemPerSM;
     const int nbuf = two ? 2 : (3 * (size_t)buf_stride <= 200 * 1024 ? 3 : 2);
     const int smem = nbuf * (int)buf_stride;
-    const void* kern = two ? (const void*)k_qrow_bulk<T, SYM, STATIC, CODE4, 256>
-                           : (const void*)k_qrow_bulk<T, SYM, STATIC, CODE4, 512>;
+    // 512 threads (about 40 registers each: two CTAs of 512 fit an SM;
+    // measured 74.5 us against 79.8 us with 256 threads on 4096 x 28672)
+    const void* kern = (const void*)k_qrow_bulk<T, SYM, STATIC, CODE4, 512>;
     cudaError_t e = ensure_smem(kern, smem);
     if (e != cudaSuccess) return e;
     int64_t grid = (int64_t)num_sms() * (two ? 2 : 1);
     if (grid > a.rows) grid = a.rows;
-    if (two)
-        k_qrow_bulk<T, SYM, STATIC, CODE4, 256><<<(unsigned)grid, 256, smem, st>>>(a, buf_stride, nbuf);
-    else
-        k_qrow_bulk<T, SYM, STATIC, CODE4, 512><<<(unsigned)grid, 512, smem, st>>>(a, buf_stride, nbuf);
+    k_qrow_bulk<T, SYM, STATIC, CODE4, 512><<<(unsigned)grid, 512, smem, st>>>(a, buf_stride, nbuf);
     return cudaGetLastError();
 }
 

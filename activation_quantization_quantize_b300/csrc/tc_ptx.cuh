@@ -43,7 +43,7 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 // raises the abort flag and records QLIN_ERR_TIMEOUT in the device error word).
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
     if (mbar_try_wait(bar, parity)) return true;
-    const long long limit = *reinterpret_cast<volatile long long*>(&g_wait_limit_cycles);
+    const long long limit = g_wait_limit_cycles;
     long long t0 = clock64();
     for (uint32_t i = 1;; ++i) {
         if (mbar_try_wait(bar, parity)) return true;
@@ -64,7 +64,7 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
 // once no MMA can still write it.
 __device__ __forceinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity) {
     if (mbar_try_wait(bar, parity)) return true;
-    const long long limit = *reinterpret_cast<volatile long long*>(&g_wait_limit_cycles);
+    const long long limit = g_wait_limit_cycles;
     long long t0 = clock64();
     for (uint32_t i = 1;; ++i) {
         if (mbar_try_wait(bar, parity)) return true;
@@ -76,9 +76,7 @@ __device__ __forceinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity) {
 }
 
 // True while the failure-detection test hook holds the producers back.
-__device__ __forceinline__ bool producers_stalled() {
-    return *reinterpret_cast<volatile int*>(&g_stall_producers) != 0;
-}
+__device__ __forceinline__ bool producers_stalled() { return g_stall_producers != 0; }
 
 // Warp-uniform bounded wait: every lane waits, and the warp agrees on the
 // outcome, so that a timeout never leaves part of a warp inside a later

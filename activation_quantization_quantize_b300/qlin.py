@@ -46,6 +46,14 @@ class qlin_w4_header(C.Structure):
                 ("scales_off", C.c_uint64), ("zeros_off", C.c_uint64), ("total_bytes", C.c_uint64)]
 
 
+class qlin_kv_cache(C.Structure):
+    _fields_ = [("capacity", C.c_int64), ("channels", C.c_int32), ("head_dim", C.c_int32), ("group", C.c_int32),
+                ("residual", C.c_int32), ("bits", C.c_int32), ("reserved", C.c_int32), ("length", C.c_int64),
+                ("quantized", C.c_int64), ("k_codes", C.c_void_p), ("v_codes", C.c_void_p),
+                ("k_scale", C.c_void_p), ("k_zero", C.c_void_p), ("v_scale", C.c_void_p), ("v_zero", C.c_void_p),
+                ("k_recent", C.c_void_p), ("v_recent", C.c_void_p)]
+
+
 _lib = None
 _P = C.c_void_p
 _I64 = C.c_int64
@@ -81,6 +89,19 @@ def load():
         L.qlin_quant_error.argtypes = [_P, C.c_int, _I64, _I64, _I64, _P, C.POINTER(qlin_qparams), _P, _P, _P, _P,
                                        _P, C.c_size_t, _P]
         for name in ("qlin_absmax_update", "qlin_fold_layernorm", "qlin_quant_error"):
+            getattr(L, name).restype = C.c_int
+        L.qlin_llmint8_workspace_size.argtypes = [_I64, _I64, _I64, _I64]
+        L.qlin_llmint8_workspace_size.restype = C.c_size_t
+        L.qlin_gemm_llmint8.argtypes = [_P, C.c_int, _I64, _I64, _I64, _P, _P, _I64, C.c_float, _I64, _P, C.c_int,
+                                        _P, _P, C.c_size_t, _P]
+        L.qlin_gemm_llmint8.restype = C.c_int
+        L.qlin_kv_cache_bytes.argtypes = [_I64, C.c_int, C.c_int, C.c_int, C.c_int, C.c_int]
+        L.qlin_kv_cache_bytes.restype = C.c_size_t
+        L.qlin_kv_cache_init.argtypes = [C.POINTER(qlin_kv_cache), _P, C.c_size_t, _I64, C.c_int, C.c_int, C.c_int,
+                                         C.c_int, C.c_int]
+        L.qlin_kv_append.argtypes = [C.POINTER(qlin_kv_cache), _P, _P, _I64, _P]
+        L.qlin_kv_read.argtypes = [C.POINTER(qlin_kv_cache), _P, _P, _P]
+        for name in ("qlin_kv_cache_init", "qlin_kv_append", "qlin_kv_read"):
             getattr(L, name).restype = C.c_int
         L.qlin_device_error.argtypes = [_P]
         L.qlin_debug_stall_producers.argtypes = [C.c_int, C.c_longlong]
@@ -354,3 +375,84 @@ def quant_error(x, p, q, s, z, smooth=None, stream=None):
     ws = torch.empty(n, dtype=torch.uint8, device=x.device)
     qlin_quant_error(x, dtype_code(x), rows, cols, x.stride(0), smooth, p, q, s, z, out, ws, n, stream)
     return out
+
+
+def qlin_llmint8_workspace_size(M, N, K, max_outliers):
+    return load().qlin_llmint8_workspace_size(M, N, K, max_outliers)
+
+
+def qlin_gemm_llmint8(x, xt, M, K, ld, qw, sw, N, threshold, max_outliers, y, yt, outliers, ws, ws_bytes,
+                      stream=None):
+    return _check("qlin_gemm_llmint8", load().qlin_gemm_llmint8(
+        _ptr(x), xt, M, K, ld, _ptr(qw), _ptr(sw), N, threshold, max_outliers, _ptr(y), yt, _ptr(outliers),
+        _ptr(ws), ws_bytes, _stream(stream)))
+
+
+def gemm_llmint8(x, qw, sw, threshold=6.0, max_outliers=None, out_dtype=torch.bfloat16, outliers=None,
+                 stream=None):
+    """LLM.int8(): bf16/fp16 activations x [M x K], INT8 weight qw [N x K] with
+    per-channel scales sw; returns y [M x N]."""
+    M, K = x.shape
+    N = qw.shape[0]
+    if max_outliers is None:
+        max_outliers = K
+    n = qlin_llmint8_workspace_size(M, N, K, max_outliers)
+    ws = torch.empty(n, dtype=torch.uint8, device=x.device)
+    y = torch.empty((M, N), dtype=out_dtype, device=x.device)
+    qlin_gemm_llmint8(x, dtype_code(x), M, K, x.stride(0), qw, sw, N, threshold, max_outliers, y,
+                      _TORCH_DT[out_dtype], outliers, ws, n, stream)
+    return y
+
+
+def qlin_kv_cache_bytes(capacity, channels, head_dim, group, residual, bits):
+    return load().qlin_kv_cache_bytes(capacity, channels, head_dim, group, residual, bits)
+
+
+def qlin_kv_cache_init(c, mem, mem_bytes, capacity, channels, head_dim, group, residual, bits):
+    return _check("qlin_kv_cache_init", load().qlin_kv_cache_init(C.byref(c), _ptr(mem), mem_bytes, capacity,
+                                                                  channels, head_dim, group, residual, bits))
+
+
+def qlin_kv_append(c, k_new, v_new, n, stream=None):
+    return _check("qlin_kv_append", load().qlin_kv_append(C.byref(c), _ptr(k_new), _ptr(v_new), n, _stream(stream)))
+
+
+def qlin_kv_read(c, k_out, v_out, stream=None):
+    return _check("qlin_kv_read", load().qlin_kv_read(C.byref(c), _ptr(k_out), _ptr(v_out), _stream(stream)))
+
+
+class KVCache:
+    """A quantized KV cache in one device buffer (see qlin_kv_cache)."""
+
+    def __init__(self, capacity, channels, head_dim, group, residual, bits, device="cuda"):
+        n = qlin_kv_cache_bytes(capacity, channels, head_dim, group, residual, bits)
+        if n == 0:
+            raise QlinError("qlin_kv_cache_bytes", QLIN_ERR_ARG, "invalid cache parameters")
+        self.mem = torch.empty(n, dtype=torch.uint8, device=device)
+        self.c = qlin_kv_cache()
+        qlin_kv_cache_init(self.c, self.mem, n, capacity, channels, head_dim, group, residual, bits)
+
+    def append(self, k, v, stream=None):
+        qlin_kv_append(self.c, k, v, k.shape[0], stream)
+
+    def read(self, stream=None):
+        T, C_ = self.c.length, self.c.channels
+        k = torch.empty((T, C_), dtype=torch.bfloat16, device=self.mem.device)
+        v = torch.empty((T, C_), dtype=torch.bfloat16, device=self.mem.device)
+        qlin_kv_read(self.c, k, v, stream)
+        return k, v
+
+    def _view(self, ptr, count, dtype):
+        off = ptr - self.mem.data_ptr()
+        item = torch.empty((), dtype=dtype).element_size()
+        return self.mem[off:off + count * item].view(dtype)
+
+    def state(self):
+        """Device views of the quantized store: (k_codes, k_scale, k_zero,
+        v_codes, v_scale, v_zero) of the tokens below c.quantized."""
+        c = self.c
+        tq, C_, heads = c.quantized, c.channels, c.channels // c.head_dim
+        nb = tq * C_ * c.bits // 8
+        return (self._view(c.k_codes, nb, torch.uint8), self._view(c.k_scale, tq // c.group * C_, torch.float32),
+                self._view(c.k_zero, tq // c.group * C_, torch.int32), self._view(c.v_codes, nb, torch.uint8),
+                self._view(c.v_scale, tq * heads, torch.float32), self._view(c.v_zero, tq * heads, torch.int32))

@@ -403,6 +403,134 @@ def measure_other_configs(dev, peaks, int8_peak):
     sweep["quantize_s8_tensor_p99.9"] = {"us": t * 1e6, "gbs": b / t / 1e9, "roofline_frac": b / hbm / t}
     out["sweep_16384x4096_bf16"] = sweep
     del xring
+    out.update(measure_next_rows(dev, peaks, int8_peak))
+    return out
+
+
+def measure_next_rows(dev, peaks, int8_peak):
+    """W4A8 decode on the down-projection weight, the LLM.int8() decomposition
+    on the prefill workload, and the SmoothQuant calibration sweep."""
+    hbm = peaks["hbm_gbs"] * 1e9
+    ring_bytes = 4 * L2_BYTES
+    out = {}
+    # W4A8: the step's UINT4 g = 128 weight (one packed copy per call from a
+    # ring of >= 4 x L2), per-token INT8 activations
+    w = inputs.downproj_weight().to(dev)
+    p4 = qlin.make_params("u4", "group", group=GROUP, scale_f16=True)
+    q4, s4, z4 = qlin.quantize(w, p4)
+    del w
+    w_bytes = N * K // 2 + N * (K // GROUP) * 2 + N * (K // GROUP) // 2
+    copies = [qlin.pack_w4(q4, s4, z4, N, K, GROUP) for _ in range(-(-ring_bytes // w_bytes))]
+    del q4, s4, z4
+    dec = {}
+    for m in (1, 8, 16):
+        qx, sx, _ = qlin.quantize(inputs.downproj_activation(m, outliers=True).to(dev), qlin.make_params("s8", "row"))
+        y = torch.empty((m, N), dtype=torch.bfloat16, device=dev)
+        t = _time_calls(lambda i: qlin.qlin_gemm_w4a8(qx, sx, copies[i % len(copies)][0], copies[i % len(copies)][1],
+                                                       m, y, qlin.QLIN_BF16, None, None, 0, None))
+        b = w_bytes + m * K + m * 4 + m * N * 2
+        dec["M%d" % m] = {"us": t * 1e6, "weight_gbs": w_bytes / t / 1e9, "roofline_frac": b / hbm / t,
+                          "int_tops": 2.0 * m * N * K / t / 1e12}
+    out["w4a8_decode_8192x28672_u4_g128"] = dec
+    del copies
+    # LLM.int8() on the prefill workload (1% outlier channels x U[20, 60])
+    x, w, _ = inputs.w8a8_prefill()
+    xd, wd = x.to(dev), w.to(dev)
+    qw, sw, _ = qlin.quantize(wd, qlin.make_params("s8", "row"))
+    Mp, Kp = xd.shape
+    Np = qw.shape[0]
+    nws = qlin.qlin_llmint8_workspace_size(Mp, Np, Kp, Kp // 32)
+    ws = torch.empty(nws, dtype=torch.uint8, device=dev)
+    y = torch.empty((Mp, Np), dtype=torch.bfloat16, device=dev)
+    rep = torch.zeros(1 + Kp, dtype=torch.int32, device=dev)
+    nrep = -(-ring_bytes // (Mp * Kp * 2 + Np * Kp)) + 1
+    ring = [(xd.clone(), qw.clone()) for _ in range(nrep)]
+    t = _time_calls(lambda i: qlin.qlin_gemm_llmint8(ring[i % nrep][0], qlin.QLIN_BF16, Mp, Kp, Kp, ring[i % nrep][1],
+                                                     sw, Np, 6.0, Kp // 32, y, qlin.QLIN_BF16, rep, ws, nws, None))
+    n_out = int(rep[0].item())
+    ops = 2.0 * Mp * Np * Kp
+    out["llmint8_%dx%dx%d" % (Mp, Np, Kp)] = {"us": t * 1e6, "outlier_channels": n_out, "tops": ops / t / 1e12,
+                                              "roofline_frac": ops / (int8_peak * 1e12) / t, "threshold": 6.0}
+    del ring, ws
+    # SmoothQuant calibration: channel maxima over 4 batches, then the alpha
+    # sweep (factors, smoothed per-token / per-channel INT8, error statistics)
+    xmax = torch.zeros(Kp, dtype=torch.float32, device=dev)
+    t_max = _time_calls(lambda i: qlin.absmax_update(xd, xmax), n_iter=20)
+    wmax = qlin.absmax(wd, qlin.QLIN_PER_COL)
+    px = qlin.make_params("s8", "row", smooth_mode=qlin.QLIN_SMOOTH_DIVIDE)
+    pw = qlin.make_params("s8", "row", smooth_mode=qlin.QLIN_SMOOTH_MULTIPLY)
+    qx = torch.empty((Mp, Kp), dtype=torch.int8, device=dev)
+    sx = torch.empty(Mp, dtype=torch.float32, device=dev)
+    qw2 = torch.empty((Np, Kp), dtype=torch.int8, device=dev)
+    sw2 = torch.empty(Np, dtype=torch.float32, device=dev)
+    errs = {}
+
+    def sweep_once(i, record=False):
+        for alpha in (0.3, 0.5, 0.7):
+            s_ = qlin.smooth_factors(xmax, wmax, alpha)
+            qlin.qlin_quantize(xd, qlin.QLIN_BF16, Mp, Kp, Kp, s_, px, qx, sx, None, None, 0, None)
+            ex = qlin.quant_error(xd, px, qx, sx, None, smooth=s_)
+            qlin.qlin_quantize(wd, qlin.QLIN_BF16, Np, Kp, Kp, s_, pw, qw2, sw2, None, None, 0, None)
+            ew = qlin.quant_error(wd, pw, qw2, sw2, None, smooth=s_)
+            if record:
+                errs[alpha] = (ex, ew)
+    t_sweep = _time_calls(sweep_once, n_iter=5, n_warm=1)
+    sweep_once(0, record=True)
+    tab = {}
+    for alpha, (ex, ew) in errs.items():
+        ex, ew = ex.cpu().numpy(), ew.cpu().numpy()
+        tab["alpha_%.1f" % alpha] = {"act_rel_err": float(np.sqrt(ex[0] / ex[1])), "w_rel_err": float(np.sqrt(ew[0] / ew[1]))}
+    del xd, wd, qx, qw2
+    # KV cache (KIVI-style): Llama-7B attention shape, 32 heads x 128, a
+    # 32768-token context, groups of 128 tokens, a 128-token bf16 window, INT4
+    T_kv, C_kv, D_kv, G_kv, R_kv = 32768, 4096, 128, 128, 128
+    cache = qlin.KVCache(T_kv, C_kv, D_kv, G_kv, R_kv, 4, device=dev)
+    kf = inputs.to_bf16(inputs.normal((T_kv - 64, C_kv), 1.0, 91)).to(dev)
+    vf = inputs.to_bf16(inputs.normal((T_kv - 64, C_kv), 1.0, 92)).to(dev)
+    cache.append(kf, vf)                                 # prefill
+    del kf, vf
+    k1 = inputs.to_bf16(inputs.normal((64, C_kv), 1.0, 93)).to(dev)
+    v1 = inputs.to_bf16(inputs.normal((64, C_kv), 1.0, 94)).to(dev)
+    kq = inputs.to_bf16(inputs.normal((G_kv, C_kv), 1.0, 95)).to(dev)
+    # one group quantized on its own: a 128-token append into a full window
+    cache_g = qlin.KVCache(4 * G_kv + R_kv, C_kv, D_kv, G_kv, R_kv, 4, device=dev)
+    cache_g.append(torch.cat([kq] * 2), torch.cat([kq] * 2))
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    cache_g.append(kq, kq)
+    e1.record()
+    e1.synchronize()
+    t_group = e0.elapsed_time(e1) / 1e3
+    del cache_g
+    # decode steps, one token each (a group is quantized every 128th): device
+    # time per call from events around each call, and the host-inclusive rate
+    for i in range(8):
+        cache.append(k1[i:i + 1], v1[i:i + 1])
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(56)]
+    torch.cuda.synchronize()
+    h0 = time.perf_counter()
+    for i in range(56):
+        evs[i][0].record()
+        cache.append(k1[8 + i:9 + i], v1[8 + i:9 + i])
+        evs[i][1].record()
+    torch.cuda.synchronize()
+    t_app_host = (time.perf_counter() - h0) / 56
+    t_app = sum(a_.elapsed_time(b_) for a_, b_ in evs) / 1e3 / 56
+    k_out = torch.empty((T_kv, C_kv), dtype=torch.bfloat16, device=dev)
+    v_out = torch.empty((T_kv, C_kv), dtype=torch.bfloat16, device=dev)
+    t_read = _time_calls(lambda i: qlin.qlin_kv_read(cache.c, k_out, v_out, None), n_iter=10)
+    T_now, tq = cache.c.length, cache.c.quantized
+    rb = 2 * tq * C_kv // 2 + (tq // G_kv) * C_kv * 8 + tq * (C_kv // D_kv) * 8 + 2 * (T_now - tq) * C_kv * 2
+    wb = 2 * T_now * C_kv * 2
+    out["kv_cache_int4_32768x4096_g128_r128"] = {
+        "append_us_per_token": t_app * 1e6, "append_us_per_token_host": t_app_host * 1e6,
+        "group_append_us": t_group * 1e6, "read_us": t_read * 1e6, "read_gbs": (rb + wb) / t_read / 1e9,
+        "read_roofline_frac": (rb + wb) / hbm / t_read, "cache_bytes_per_token": 2 * C_kv // 2 + 8 * C_kv / G_kv
+        + 8 * C_kv / D_kv, "bf16_bytes_per_token": 2 * C_kv * 2}
+    del cache, k_out, v_out
+    out["smoothquant_calibration_2048x4096_w11008"] = {
+        "absmax_update_us": t_max * 1e6, "absmax_update_frac": Mp * Kp * 2 / hbm / t_max,
+        "alpha_sweep_ms": t_sweep * 1e3, "errors": tab}
     return out
 
 
@@ -524,14 +652,42 @@ def run_reference(args, world, rank):
 
 
 # ------------------------------------------------------------------ profiling cases
-PROFILE_CASES = ("w8a8", "w8a8_full", "w4a16_m1", "w4a16_m64", "w4a16_m256", "quantize", "dequantize")
+PROFILE_CASES = ("w8a8", "w8a8_full", "w4a16_m1", "w4a16_m64", "w4a16_m256", "quantize", "dequantize",
+                 "sweep_row_s8", "sweep_row_u8", "sweep_group128_s8", "sweep_tensor_s8", "sweep_col_s8", "w4a8_m1",
+                 "llmint8", "kv_read")
 
 
 def run_profile_case(name, dev):
     """One kernel on a bounded case larger than L2 (for ncu captures): two
     warm-up calls and one measured call, then exit."""
     torch.cuda.set_device(dev)
-    if name.startswith("w8a8"):
+    if name.startswith("sweep_"):
+        # the 16384 x 4096 sweep tensor: sweep_<gran>[g]_<code>
+        _, gran, code = name.split("_")
+        g = int(gran[5:]) if gran.startswith("group") else 0
+        xs = inputs.sweep_tensor().to(dev)
+        p = qlin.make_params(code, "group" if g else gran, group=g)
+        fn = lambda: qlin.quantize(xs, p)  # noqa: E731
+    elif name == "llmint8":
+        x, w, _ = inputs.w8a8_prefill()
+        xd = x.to(dev)
+        qw, sw, _ = qlin.quantize(w.to(dev), qlin.make_params("s8", "row"))
+        fn = lambda: qlin.gemm_llmint8(xd, qw, sw, threshold=6.0, max_outliers=128)  # noqa: E731
+    elif name == "kv_read":
+        cache = qlin.KVCache(8192, 4096, 128, 128, 128, 4, device=dev)
+        kf = inputs.to_bf16(inputs.normal((8192, 4096), 1.0, 91)).to(dev)
+        cache.append(kf, kf)
+        del kf
+        fn = lambda: cache.read()  # noqa: E731
+    elif name == "w4a8_m1":
+        w = inputs.downproj_weight().to(dev)
+        p4 = qlin.make_params("u4", "group", group=GROUP, scale_f16=True)
+        q4, s4, z4 = qlin.quantize(w, p4)
+        packed, hdr = qlin.pack_w4(q4, s4, z4, N, K, GROUP)
+        del w, q4
+        qx, sx, _ = qlin.quantize(inputs.downproj_activation(1).to(dev), qlin.make_params("s8", "row"))
+        fn = lambda: qlin.gemm_w4a8(qx, sx, packed, hdr)  # noqa: E731
+    elif name.startswith("w8a8"):
         # 2048 x 4096 x 28672: 56 MiB + 112 MiB of int8 codes, quantized from
         # the down-projection activations (with outlier channels) and weights;
         # w8a8_full: the step's 4096 x 8192 x 28672 (for one-pass counters)

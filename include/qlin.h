@@ -306,6 +306,95 @@ int qlin_gemm_w4a8(const int8_t *qx, const float *sx, const void *packed, const 
                    void *y, qlin_dtype yt, int32_t *acc_out, void *ws, size_t ws_bytes, void *stream);
 
 /*
+ * qlin_gemm_llmint8 -- LLM.int8() mixed-precision decomposition of the W8A8
+ * layer ([L19] sections 9-11): XW = X_normal W_normal + X_outlier W_outlier.
+ * The outlier dimensions are the input channels j with max_m |x[m][j]| >
+ * threshold.  They are taken out of the INT8 product: the per-token INT8
+ * codes of x are computed with those channels set to 0 (vector-wise scale
+ * sx[m] = max over the normal channels / 127), and the outlier channels are
+ * multiplied in 16-bit with the weight's own columns dequantized:
+ *   y[m,n] = sw[n] * (sx[m] * acc[m,n] + sum_{j outlier} x[m,j] * qw[n,j])
+ * acc being the exact INT32 sums over the normal channels; one rounding to yt.
+ *   x       device bf16 [M x K], row stride ld (16-byte aligned rows); the
+ *           outlier channels are multiplied in bf16 with fp32 accumulation.
+ *   qw, sw  the weight in INT8 per output channel: device int8 [N x K]
+ *           (16-byte aligned) and binary32 [N] scales (qlin_quantize,
+ *           QLIN_PER_ROW, symmetric [-127, 127]).
+ *   threshold  finite, >= 0 (LLM.int8() uses 6.0 on activations).
+ *   max_outliers  the most outlier channels the workspace is sized for (0..K).
+ *           More outlier channels than that make qlin_device_error report
+ *           QLIN_ERR_WORKSPACE; y is then unspecified.
+ *   y       device [M x N] of type yt (F32 or BF16).
+ *   outliers NULL, or device int32 [1 + K]: the number of outlier channels,
+ *           then their indices in ascending order.
+ *   ws      device workspace of qlin_llmint8_workspace_size(M, N, K,
+ *           max_outliers) bytes, 256-byte aligned.
+ * Requirements: K % 16 == 0, K < 133,144.
+ */
+size_t qlin_llmint8_workspace_size(int64_t M, int64_t N, int64_t K, int64_t max_outliers);
+int qlin_gemm_llmint8(const void *x, qlin_dtype xt, int64_t M, int64_t K, int64_t ld, const int8_t *qw,
+                      const float *sw, int64_t N, float threshold, int64_t max_outliers, void *y, qlin_dtype yt,
+                      int32_t *outliers, void *ws, size_t ws_bytes, void *stream);
+
+/*
+ * KV-cache quantization in token groups outside a recent window ([CH11]
+ * 11.6.3 granularity, 11.6.4 K/V sensitivity, 11.6.5 KIVI's grouped
+ * on-demand quantization).  K is quantized per channel -- one scale and zero
+ * point per channel over each group of `group` tokens -- and V per token --
+ * one per token and head over head_dim channels; codes are asymmetric,
+ * [0, 2^bits - 1], with qlin_quantize's arithmetic (range widened to
+ * contain 0, round-half-even of the correctly rounded binary32 quotient, zero
+ * point added after rounding; binary32 scales, int32 zero points).  The
+ * `residual` most recent tokens stay in bf16; a group is quantized once all
+ * of its tokens have left that window, so after every append
+ *   quantized = group * floor(max(length - residual, 0) / group).
+ * The caller owns one device block of qlin_kv_cache_bytes(...) bytes, which
+ * qlin_kv_cache_init carves into the buffers below; the struct lives in host
+ * memory and qlin_kv_append keeps its counters.
+ */
+typedef struct {
+    int64_t capacity;        /* tokens the cache can hold (a multiple of group)       */
+    int32_t channels;        /* C = heads * head_dim values per token (C % 16 == 0)   */
+    int32_t head_dim;        /* D: V's scope; D % 8 == 0, C % D == 0                  */
+    int32_t group;           /* G tokens per K scope and per quantization step        */
+    int32_t residual;        /* R most recent tokens kept in bf16                     */
+    int32_t bits;            /* 8 or 4                                                */
+    int32_t reserved;
+    int64_t length;          /* tokens appended so far                                */
+    int64_t quantized;       /* tokens in the quantized store                         */
+    void *k_codes, *v_codes; /* device [capacity x C] codes (4-bit: two per byte,    */
+                             /* element 2i in the low nibble)                         */
+    float *k_scale;          /* device [capacity / G x C]                             */
+    int32_t *k_zero;         /* device [capacity / G x C]                             */
+    float *v_scale;          /* device [capacity x C / D]                             */
+    int32_t *v_zero;         /* device [capacity x C / D]                             */
+    void *k_recent, *v_recent; /* device bf16 rings of (R + G) x C: token t of      */
+                             /* [quantized, length) in slot t mod (R + G)             */
+} qlin_kv_cache;
+
+/* Device bytes one cache of these parameters needs (0 for invalid ones). */
+size_t qlin_kv_cache_bytes(int64_t capacity, int channels, int head_dim, int group, int residual, int bits);
+
+/* Host only: fill *c for an empty cache whose buffers live in the device
+ * block mem (256-byte aligned, mem_bytes >= qlin_kv_cache_bytes(...)).  The
+ * block needs no initialisation. */
+int qlin_kv_cache_init(qlin_kv_cache *c, void *mem, size_t mem_bytes, int64_t capacity, int channels, int head_dim,
+                       int group, int residual, int bits);
+
+/* Append n tokens: k_new, v_new device bf16 [n x C] (16-byte aligned).  Groups
+ * that leave the recent window are quantized (from the ring or straight from
+ * k_new / v_new), the new tokens that stay in 16-bit go to the ring, and
+ * c->length / c->quantized are updated (host side).  length + n must not
+ * exceed capacity.  The launches are ordered on `stream`; calls on one cache
+ * must be issued in order on one stream. */
+int qlin_kv_append(qlin_kv_cache *c, const void *k_new, const void *v_new, int64_t n, void *stream);
+
+/* The cache as attention reads it: k_out, v_out device bf16 [length x C]
+ * (16-byte aligned) receive bf16(fl(s * (q - z))) for tokens below
+ * c->quantized and the stored bf16 values for the others. */
+int qlin_kv_read(const qlin_kv_cache *c, void *k_out, void *v_out, void *stream);
+
+/*
  * qlin_quantize_noalloc -- qlin_quantize for callers that cannot allocate
  * device memory.  The pages have no counterpart: this is a deployment
  * convenience, not part of the method.

@@ -157,3 +157,26 @@ def test_row_local_scopes_need_no_workspace(lib):
 
 def test_stall_hook_validates_without_gpu(lib):
     assert lib.qlin_debug_stall_producers(1, 0) == qlin.QLIN_ERR_ARG
+
+
+def test_kv_cache_struct_and_validation(lib):
+    assert C.sizeof(qlin.qlin_kv_cache) == 112
+    assert qlin.qlin_kv_cache.length.offset == 32
+    assert qlin.qlin_kv_cache_bytes(1024, 512, 128, 32, 48, 4) > 0
+    assert qlin.qlin_kv_cache_bytes(1000, 512, 128, 32, 48, 4) == 0   # capacity % group
+    assert qlin.qlin_kv_cache_bytes(1024, 500, 128, 32, 48, 4) == 0   # channels % 16
+    assert qlin.qlin_kv_cache_bytes(1024, 512, 128, 32, 48, 3) == 0   # bits
+    # closed form: codes + K scales/zeros per (group, channel) + V per (token, head) + two bf16 rings
+    cap, Cc, D, G, R = 1024, 512, 128, 32, 48
+    up = lambda b: (b + 255) // 256 * 256  # noqa: E731
+    want = 2 * up(cap * Cc // 2) + 2 * up(cap // G * Cc * 4) + 2 * up(cap * (Cc // D) * 4) + 2 * up((R + G) * Cc * 2)
+    assert qlin.qlin_kv_cache_bytes(cap, Cc, D, G, R, 4) == want
+    c = qlin.qlin_kv_cache()
+    assert lib.qlin_kv_cache_init(C.byref(c), C.c_void_p(0x10000), want - 1, cap, Cc, D, G, R, 4) == \
+        qlin.QLIN_ERR_WORKSPACE
+    assert lib.qlin_kv_cache_init(C.byref(c), C.c_void_p(0x10000), want, cap, Cc, D, G, R, 4) == qlin.QLIN_OK
+    assert c.length == 0 and c.quantized == 0 and c.k_codes == 0x10000
+    fake = C.c_void_p(0x20000)
+    assert lib.qlin_kv_append(C.byref(c), fake, fake, cap + 1, None) == qlin.QLIN_ERR_ARG   # past capacity
+    assert lib.qlin_kv_append(C.byref(c), C.c_void_p(0x20008), fake, 4, None) == qlin.QLIN_ERR_ARG  # alignment
+    assert lib.qlin_kv_append(C.byref(c), fake, fake, 0, None) == qlin.QLIN_OK

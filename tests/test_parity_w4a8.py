@@ -47,7 +47,7 @@ def oracle_out(host, group, rows=None):
 
 @pytest.mark.parametrize("asym", [False, True])
 @pytest.mark.parametrize("group", [32, 64, 128])
-@pytest.mark.parametrize("M", [1, 3, 8, 9, 16, 17, 40])
+@pytest.mark.parametrize("M", [1, 2, 3, 8, 9, 16, 17, 40])
 def test_w4a8_small_exact_sums(asym, group, M):
     N, K = 256, 1024
     qx, sx, packed, hdr, host = prepare(N, K, M, group, asym, seed=M + group)
@@ -62,14 +62,16 @@ def test_w4a8_small_exact_sums(asym, group, M):
     assert qlin.qlin_device_error() == 0
 
 
+@pytest.mark.parametrize("M", [1, 2, 5])
 @pytest.mark.parametrize("group", [32, 64, 128])
 @pytest.mark.parametrize("K", [1088 + 64, 2048 + 64 * 3])
-def test_w4a8_groups_cut_between_warps(group, K):
+def test_w4a8_groups_cut_between_warps(group, K, M):
     """K = 1152 / 2240: the eight warps' K ranges start inside groups of 128,
-    so each warp scales its own exact part of a group."""
+    so each warp scales its own exact part of a group (M = 1, 2: the dp4a
+    kernel; M = 5: the MMA kernel)."""
     if K % group:
         pytest.skip("group does not divide K")
-    N, M = 4736, 5                                      # 148 x 32 rows: two 16-row tiles per CTA
+    N = 4736                                            # 148 x 32 rows: two 16-row tiles per CTA
     qx, sx, packed, hdr, host = prepare(N, K, M, group, True, seed=K + group)
     acc = torch.empty((K // group, M, N), dtype=torch.int32, device="cuda")
     y = qlin.gemm_w4a8(qx, sx, packed, hdr, out_dtype=torch.float32, acc_out=acc)
