@@ -328,6 +328,42 @@ __device__ __forceinline__ void code_bits8(const float v[8], const ScopeParams& 
     }
 }
 
+// code_bits8 with one scope per element (per-column scopes): the same packed
+// fast path with per-lane constants; a chunk that fails takes the exact
+// per-element path.
+template <bool kInRange, bool kClamp>
+__device__ __forceinline__ void code_bits8_cols(const float v[8], const ScopeParams sp[8], const CodeRange& cr,
+                                                uint32_t cb[8]) {
+    float m[8];
+    uint32_t neg = 0xFFFFFFFFu;
+    const float2 nlim2 = make_float2(-16777216.0f, -16777216.0f);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const ScopeParams& p0 = sp[2 * j];
+        const ScopeParams& p1 = sp[2 * j + 1];
+        const float2 v2 = make_float2(v[2 * j], v[2 * j + 1]);
+        const float2 t2 = f2_mul(v2, make_float2(p0.r, p1.r));
+        const float2 m2 = f2_add(t2, make_float2(p0.cz, p1.cz));
+        const float2 n2 = f2_add(m2, make_float2(-p0.cz, -p1.cz));
+        const float2 d2 = f2_fma(n2, make_float2(-p0.s, -p1.s), v2);
+        const float2 e2 = f2_fma(d2, d2, make_float2(-p0.hs * p0.hs, -p1.hs * p1.hs));
+        neg &= __float_as_uint(e2.x) & __float_as_uint(e2.y);
+        if (!kInRange) {
+            const float2 g2 = f2_fma(t2, t2, nlim2);
+            neg &= __float_as_uint(g2.x) & __float_as_uint(g2.y);
+        }
+        m[2 * j] = m2.x;
+        m[2 * j + 1] = m2.y;
+    }
+    if (neg & 0x80000000u) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) cb[j] = __float_as_uint(kClamp ? fminf(fmaxf(m[j], cr.lo), cr.hi) : m[j]);
+    } else {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) cb[j] = code_bits(v[j], sp[j], cr);
+    }
+}
+
 // Pack the low bytes of four code_bits() words: byte i <- a[i].
 __device__ __forceinline__ uint32_t pack_bytes4(uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3) {
     uint32_t lo = __byte_perm(a0, a1, 0x0040);

@@ -619,6 +619,7 @@ __global__ void __launch_bounds__(256) k_stats_strip(QuantArgs a, uint32_t* stat
         lo[j] = 0.0f;
     }
     if (st.chunk >= 0) {
+#pragma unroll 4
         for (int64_t r = st.r_begin; r < st.r_end; r += st.r_step) {
             float v[8];
             load8<T>(x + r * a.ld + st.chunk * 8, v);
@@ -677,8 +678,12 @@ __global__ void k_finalize(QuantArgs a, const uint32_t* stat, int64_t nscopes) {
     if (a.z) a.z[i] = z;
 }
 
-// Codes for per-tensor / per-column scopes from the stored (s, z).
-template <typename T>
+// Codes for per-tensor / per-column scopes from the stored (s, z).  MODE 0:
+// dynamic symmetric (no clamp; |rne(x/s)| <= qmax since s came from the same
+// data), 1: dynamic asymmetric (clamp), 2: static scales (clamp and
+// far-range test).  The eight codes of a chunk are decided together on
+// packed pairs; per-column scopes give each element its own constants.
+template <typename T, int MODE, bool PER_COL>
 __global__ void __launch_bounds__(256) k_quant_strip(QuantArgs a, int rows_per_block) {
     const int64_t nchunks = a.cols / 8;
     const T* __restrict__ x = reinterpret_cast<const T*>(a.x);
@@ -688,18 +693,21 @@ __global__ void __launch_bounds__(256) k_quant_strip(QuantArgs a, int rows_per_b
     ScopeParams sp[8];
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
-        int64_t sc = (a.gran == QLIN_PER_COL) ? st.chunk * 8 + j : 0;
-        float s = load_scale(a.s, sc, a.scale_f16);
-        int z = a.z ? a.z[sc] : 0;
+        const int64_t sc = PER_COL ? st.chunk * 8 + j : 0;
+        const float s = load_scale(a.s, sc, a.scale_f16);
+        const int z = a.z ? a.z[sc] : 0;
         sp[j] = make_scope(s, z);
     }
+#pragma unroll 4
     for (int64_t r = st.r_begin; r < st.r_end; r += st.r_step) {
         float v[8];
         load8<T>(x + r * a.ld + st.chunk * 8, v);
         smooth8(v, a.smooth_mode, a.smooth, st.chunk * 8);
         uint32_t cb[8];
-#pragma unroll
-        for (int j = 0; j < 8; ++j) cb[j] = code_bits(v[j], sp[j], cr);
+        if (PER_COL)
+            code_bits8_cols<MODE != 2, MODE != 0>(v, sp, cr, cb);
+        else
+            code_bits8<MODE != 2, MODE != 0>(v, sp[0], cr, cb);
         store_codes8(a.q, r, a.cols, st.chunk, a.code4, cb);
     }
 }
@@ -821,15 +829,29 @@ __global__ void k_quant_generic(QuantArgs a) {
 constexpr int kHist1 = 32768, kHist2 = 65536;
 
 template <typename T>
-__global__ void __launch_bounds__(1024) k_hist1(QuantArgs a, uint32_t* hist1) {
+__global__ void __launch_bounds__(1024) k_hist1(QuantArgs a, uint32_t* hist1, int vec) {
     extern __shared__ uint32_t sh[];
     for (int i = threadIdx.x; i < kHist1; i += blockDim.x) sh[i] = 0;
     __syncthreads();
-    for (int64_t r = blockIdx.x; r < a.rows; r += gridDim.x)
-        for (int64_t c = threadIdx.x; c < a.cols; c += blockDim.x) {
-            float v = fabsf(load_smoothed<T>(a, r, c));
-            atomicAdd(&sh[__float_as_uint(v) >> 16], 1u);
-        }
+    if (vec) {  // rows of whole 16-byte-aligned 8-value chunks
+        const int64_t nchunks = a.cols / 8;
+        const T* __restrict__ x = reinterpret_cast<const T*>(a.x);
+        for (int64_t r = blockIdx.x; r < a.rows; r += gridDim.x)
+#pragma unroll 2
+            for (int64_t c = threadIdx.x; c < nchunks; c += blockDim.x) {
+                float v[8];
+                load8<T>(x + r * a.ld + c * 8, v);
+                smooth8(v, a.smooth_mode, a.smooth, c * 8);
+#pragma unroll
+                for (int j = 0; j < 8; ++j) atomicAdd(&sh[__float_as_uint(fabsf(v[j])) >> 16], 1u);
+            }
+    } else {
+        for (int64_t r = blockIdx.x; r < a.rows; r += gridDim.x)
+            for (int64_t c = threadIdx.x; c < a.cols; c += blockDim.x) {
+                float v = fabsf(load_smoothed<T>(a, r, c));
+                atomicAdd(&sh[__float_as_uint(v) >> 16], 1u);
+            }
+    }
     __syncthreads();
     for (int i = threadIdx.x; i < kHist1; i += blockDim.x)
         if (sh[i]) atomicAdd(&hist1[i], sh[i]);
@@ -1330,7 +1352,10 @@ static cudaError_t run_quantize_t(QuantArgs a, int xt, const qlin_qparams* p, vo
         const size_t raw_bytes = (size_t)a.cols * 2;
         const uint32_t buf_stride = (uint32_t)((raw_bytes + 127) & ~(size_t)127);
         if constexpr (!std::is_same<T, float>::value) {
-            const bool fast16 = !a.absmax_out && a.smooth_mode == QLIN_SMOOTH_NONE;
+            // binary16 scales can saturate at 65504, and then |x/s| is not
+            // bounded by qmax: those calls take kernels that clamp and test
+            // the range of every code
+            const bool fast16 = !a.absmax_out && a.smooth_mode == QLIN_SMOOTH_NONE && !a.scale_f16;
             if (fast16 && nchunks <= 512) return launch_qrow_warp<T>(a, st);
             if (fast16 && a.gran == QLIN_PER_ROW && 2 * (size_t)buf_stride <= 200 * 1024)
                 return launch_qrow_bulk<T>(a, buf_stride, st);
@@ -1370,7 +1395,7 @@ static cudaError_t run_quantize_t(QuantArgs a, int xt, const qlin_qparams* p, vo
             uint64_t k = (uint64_t)percentile_rank(n, p->clip_percentile);
             if ((e = cudaMemsetAsync(ws, 0, (size_t)(kHist1 + kHist2 + 4) * 4, st)) != cudaSuccess) return e;
             if ((e = ensure_smem((const void*)k_hist1<T>, kHist1 * 4)) != cudaSuccess) return e;
-            k_hist1<T><<<num_sms(), 1024, kHist1 * 4, st>>>(a, hist1);
+            k_hist1<T><<<num_sms(), 1024, kHist1 * 4, st>>>(a, hist1, strip_ok(a, xt) ? 1 : 0);
             // Low 16 bits of |x| are zero for unsmoothed bf16 input.
             bool need2 = !(xt == QLIN_BF16 && a.smooth_mode == QLIN_SMOOTH_NONE);
             k_select1<<<1, 1024, 0, st>>>(a, hist1, sel, k, need2 ? 0 : 1);
@@ -1398,7 +1423,18 @@ static cudaError_t run_quantize_t(QuantArgs a, int xt, const qlin_qparams* p, vo
         dim3 grid;
         int rpb;
         strip_grid(a.cols / 8, a.rows, grid, rpb);
-        k_quant_strip<T><<<grid, 256, 0, st>>>(a, rpb);
+        // percentile scales clip values beyond the percentile, and binary16
+        // scales can saturate: both take the fully checked codes
+        const int mode = (a.static_scale || p->clip_percentile > 0.0 || a.scale_f16) ? 2 : (a.sym ? 0 : 1);
+        const bool pc = a.gran == QLIN_PER_COL;
+        switch (mode * 2 + (pc ? 1 : 0)) {
+        case 0: k_quant_strip<T, 0, false><<<grid, 256, 0, st>>>(a, rpb); break;
+        case 1: k_quant_strip<T, 0, true><<<grid, 256, 0, st>>>(a, rpb); break;
+        case 2: k_quant_strip<T, 1, false><<<grid, 256, 0, st>>>(a, rpb); break;
+        case 3: k_quant_strip<T, 1, true><<<grid, 256, 0, st>>>(a, rpb); break;
+        case 4: k_quant_strip<T, 2, false><<<grid, 256, 0, st>>>(a, rpb); break;
+        default: k_quant_strip<T, 2, true><<<grid, 256, 0, st>>>(a, rpb); break;
+        }
     } else {
         k_quant_generic<T><<<gblocks, 256, 0, st>>>(a);
     }

@@ -79,6 +79,21 @@ def test_quantize_f16_scales(code, gran, group):
     run_case(xd, xh, qlin.make_params(code, gran, group=group, scale_f16=True))
 
 
+@pytest.mark.parametrize("code", ["s8", "u8", "s4"])
+@pytest.mark.parametrize("gran,group,cols", [("row", 0, 512), ("row", 0, 8192), ("group", 64, 512),
+                                             ("tensor", 0, 512), ("col", 0, 512)])
+def test_quantize_f16_scale_saturation(code, gran, group, cols):
+    """Values whose scale overflows binary16 (max|x| / qmax > 65504): the
+    stored scale saturates at 65504 and the codes must clip, as the oracle's
+    do (every kernel that serves binary16 scales clamps and range-tests)."""
+    rows = 16
+    xf = inputs.normal((rows, cols), 1.0, 77)
+    xf[:, 3] = 3.0e7                                          # far beyond 65504 * 127
+    xf[5, :] *= 2.0e6
+    xd = torch.from_numpy(xf).to(torch.bfloat16).cuda()
+    run_case(xd, host_f32(xd), qlin.make_params(code, gran, group=group, scale_f16=True))
+
+
 @pytest.mark.parametrize("mode", [qlin.QLIN_SMOOTH_DIVIDE, qlin.QLIN_SMOOTH_MULTIPLY])
 @pytest.mark.parametrize("gran", ["row", "tensor", "col", "group"])
 def test_quantize_smoothing(mode, gran):
