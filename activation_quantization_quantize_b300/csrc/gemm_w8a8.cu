@@ -204,6 +204,10 @@ constexpr uint32_t TMEM_COLS = 512;           // [0,256): rows 0-127, [256,512):
 constexpr uint32_t EV_DRAIN = 1, EV_FINAL = 2;
 constexpr size_t CTRL_BYTES = 2048;
 constexpr size_t SMEM_BYTES = 1024 + (size_t)S16 * STAGE_BYTES + (size_t)S8 * STAGE8_BYTES + CTRL_BYTES;
+// Longest sleep between polls of a warp idle until a tile event: none; the
+// suspending try_wait already frees the warp's issue slots and wakes it as
+// soon as the phase completes (a sleep would delay every drain).
+constexpr uint32_t kIdleSleepNs = 0;
 }  // namespace w8tc
 
 // int8 x4 -> two fp16x2 words, exact: bias to unsigned, place each byte in the
@@ -550,7 +554,7 @@ __global__ void __launch_bounds__(w8tc::THREADS, 1)
         const uint32_t lane_base = (uint32_t)(32 * q) << 16;
         uint32_t ndrain = 0;
         for (uint32_t ev = 0;; ++ev) {
-            if (!tc::mbar_wait_warp(ev_bar, ev & 1u, abort_flag)) break;
+            if (!tc::mbar_wait_warp(ev_bar, ev & 1u, abort_flag, kIdleSleepNs)) break;
             const uint32_t type = misc[1];
             if (!tc::mbar_wait_warp(acc_full, ev & 1u, abort_flag)) break;
             tc::tc_fence_after();
@@ -650,6 +654,422 @@ __global__ void __launch_bounds__(256) k_w8a8_tail(W8TcArgs p, int tail_tiles) {
     }
 }
 
+// ====================================================================== CTA-pair kernel
+// A cluster of two CTAs on two SMs owns a 256 x 256 output tile.  One
+// M = 256 tcgen05 MMA per 16-k step (cta_group::2) covers the pair: CTA r
+// holds activation rows 128 r .. 128 r + 127 of the tile as fp16 in its own
+// TMEM (the A operand, written by tcgen05.st, so it never passes through
+// shared memory) and weight rows 128 r .. 128 r + 127 as fp16 in its shared
+// memory (the B operand; each half is read once for both SMs).
+//
+// Each converter warp fetches its own int8 rows with cp.async into a private
+// ring in shared memory (four k-blocks deep) and reads them back after a
+// thread-local wait, so the int8 tiles need no barrier.  The k-blocks
+// alternate between two converter groups, so that the fixed cost of a
+// warp's hand-off (one wait for a free stage, one arrival) is spent once per
+// two k-blocks.  Roles per CTA: group g = 0, 1: warps 8g .. 8g+3 widen
+// activation rows (warp w: TMEM lanes 32 (w % 4) .., one row per thread) and
+// report each row's sum |q| of the k-block to the even CTA; warps 8g+4 ..
+// 8g+7 widen weight rows into the swizzled B tile; warps 16-19 drain and
+// finish the accumulators of their TMEM lane quarter; warp 20 owns TMEM and,
+// in the even CTA, issues the MMAs; warp 21 of the even CTA tracks the
+// running sum |q| of all 256 rows and posts, per stage, whether the
+// accumulators must be drained before that k-block.  It decides from the
+// sums up to the previous k-block and the bound 64 * 128 on one k-block's
+// sum, so the decision is ready as soon as the stage is full and the
+// reduction over rows runs while the tensor cores work.
+namespace w8p {
+constexpr int BM = 256, HM = 128;              // tile rows, rows per CTA
+constexpr int BN = 256, HN = 128;              // tile columns, weight rows per CTA
+constexpr int BK = 64;
+constexpr int S16 = 4;                         // fp16 operand stages (TMEM A + shared B)
+constexpr int NGROUP = 2;                      // converter groups (k-blocks alternate)
+constexpr int RING = 4;                        // own k-blocks in flight per converter warp
+constexpr int SLOT_BYTES = 32 * BK;            // 32 rows x 64 int8 codes
+constexpr int WARP_RING_BYTES = RING * SLOT_BYTES;
+constexpr int NCONV_WARPS = 8 * NGROUP;
+constexpr int B16_BYTES = HN * BK * 2;         // 16 KB swizzled fp16 B half-tile
+constexpr int EPI_WARP0 = 16, MMA_WARP = 20, MON_WARP = 21;
+constexpr int THREADS = 22 * 32;
+constexpr uint32_t ACC_COL = 0;                // accumulator: 128 lanes x 256 fp32 columns
+constexpr uint32_t A_COL0 = 256;               // A stage s: 32 columns (64 fp16 k) at A_COL0 + 32 s
+constexpr uint32_t TMEM_COLS = 512;
+constexpr uint32_t ROWSUM_LIMIT = w8tc::ROWSUM_LIMIT;
+constexpr uint32_t KB_SUM_MAX = BK * 128;      // largest sum |q| of one row over one k-block
+constexpr uint32_t EV_DRAIN = 1, EV_FINAL = 2;
+constexpr int FULL_ARRIVALS = 2 * 8;           // one group's converter warps, both CTAs
+constexpr int ACC_EMPTY_ARRIVALS = 2 * 4;      // epilogue warps of both CTAs
+constexpr size_t CTRL_BYTES = 8192;
+constexpr size_t SMEM_BYTES = 1024 + (size_t)S16 * B16_BYTES + (size_t)NCONV_WARPS * WARP_RING_BYTES + CTRL_BYTES;
+constexpr uint32_t kIdleSleepNs = w8tc::kIdleSleepNs;
+static_assert(A_COL0 + 32 * S16 <= TMEM_COLS, "TMEM budget");
+static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+static_assert((3 * S16 + 4) * 8 + S16 * BM * 4 + S16 * 4 + 16 <= (int)CTRL_BYTES, "control block");
+static_assert(S16 % NGROUP == 0, "a stage belongs to one converter group");
+}  // namespace w8p
+
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(w8p::THREADS, 1)
+    k_w8a8_pair(const int8_t* __restrict__ qx, const int8_t* __restrict__ qw, W8TcArgs p) {
+    using namespace w8p;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+    uint8_t* tiles = smem;                                   // S16 x fp16 B half-tile
+    uint8_t* rings = smem + S16 * B16_BYTES;                 // per converter warp: RING x 2 KB of int8 rows
+    uint64_t* bars = reinterpret_cast<uint64_t*>(rings + NCONV_WARPS * WARP_RING_BYTES);
+    // bars: full[S16], empty[S16], acc_full, acc_empty, ev, done, dec[S16]
+    uint32_t* rowsum = reinterpret_cast<uint32_t*>(bars + 3 * S16 + 4);  // [S16][BM], even CTA
+    volatile uint32_t* drain_dec = reinterpret_cast<volatile uint32_t*>(rowsum + S16 * BM);  // [S16]
+    volatile uint32_t* misc = drain_dec + S16;  // tmem, event, abort
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 2);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t rank = tc::cluster_rank();
+    const bool leader = rank == 0;
+    int64_t tile = blockIdx.x >> 1;
+    int kpart = 0, nparts = 1;
+    if (tile >= p.full_tiles) {
+        const int64_t u = tile - p.full_tiles;
+        tile = p.full_tiles + u / p.tail_split;
+        kpart = (int)(u % p.tail_split);
+        nparts = p.tail_split;
+    }
+    const int64_t m0 = (tile % p.num_m_tiles) * BM;
+    const int64_t n0 = (tile / p.num_m_tiles) * BN;
+    const int64_t mh = m0 + HM * (int64_t)rank;              // this CTA's first activation row
+    const int64_t nh = n0 + HN * (int64_t)rank;              // this CTA's first weight row
+    const int nkb_all = (int)ceil_div(p.K, BK);
+    const int kb0 = (int)((int64_t)nkb_all * kpart / nparts);
+    const int nkb = (int)((int64_t)nkb_all * (kpart + 1) / nparts) - kb0;
+    const bool split = nparts > 1;
+    int32_t* const dtile = split ? p.part + ((tile - p.full_tiles) * nparts + kpart) * (int64_t)BM * BN
+                                 : p.drain + m0 * p.N + n0;
+    const int64_t dld = split ? BN : p.N;
+
+    const uint32_t bar0 = tc::smem_addr(bars);
+    auto full_bar = [&](int s) { return bar0 + 8u * s; };
+    auto empty_bar = [&](int s) { return bar0 + 8u * (S16 + s); };
+    const uint32_t acc_full = bar0 + 8u * (2 * S16);
+    const uint32_t acc_empty = acc_full + 8u;
+    const uint32_t ev_bar = acc_full + 16u;
+    const uint32_t done_bar = acc_full + 24u;
+    auto dec_bar = [&](int s) { return bar0 + 8u * (2 * S16 + 4 + s); };
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < S16; ++s) {
+            tc::mbar_init(full_bar(s), FULL_ARRIVALS);
+            tc::mbar_init(empty_bar(s), 1);
+        }
+        tc::mbar_init(acc_full, 1);
+        tc::mbar_init(acc_empty, ACC_EMPTY_ARRIVALS);
+        tc::mbar_init(ev_bar, 1);
+        tc::mbar_init(done_bar, 1);
+        for (int s = 0; s < S16; ++s) tc::mbar_init(dec_bar(s), 1);
+        misc[1] = 0;
+        misc[2] = 0;
+        tc::mbar_init_fence();
+    }
+    if (warp == MMA_WARP) {
+        tc::tmem_alloc_pair(tc::smem_addr((const void*)&misc[0]), TMEM_COLS);
+        tc::tmem_relinquish_pair();
+    }
+    tc::tc_fence_before();
+    tc::cluster_sync();  // both CTAs' barriers initialised and TMEM allocated
+    tc::tc_fence_after();
+    const uint32_t tmem = misc[0];
+    // the even CTA's copies of the barriers and row sums the converters report to
+    const uint32_t full_bar_l0 = tc::mapa(full_bar(0), 0);
+    const uint32_t rowsum_l0 = tc::mapa(tc::smem_addr(rowsum), 0);
+    const uint32_t acc_empty_l0 = tc::mapa(acc_empty, 0);
+
+    if (warp < NCONV_WARPS) {
+        // ---------------------------------------------------------- converters
+        const int g = warp >> 3;                 // group: k-blocks g, g + 2, ...
+        const int q = warp & 3;                  // 32-row quarter of this CTA's half
+        const bool is_a = (warp & 4) == 0;
+        const uint32_t ring = tc::smem_addr(rings) + (uint32_t)warp * WARP_RING_BYTES;
+        const uint8_t* ringp = rings + (size_t)warp * WARP_RING_BYTES;
+        const int8_t* src = is_a ? qx : qw;
+        const int64_t row0 = (is_a ? mh : nh) + 32 * q;   // first global row of this warp
+        const int64_t nrows = is_a ? p.M : p.N;
+        // copies: lane l fetches rows 8 j + l / 4 (j = 0..3) of the warp's 32,
+        // 16-byte chunk l % 4 of the 64-code k-block; activation rows are
+        // stored with a 64-byte swizzle (chunk c of row r at 16 (c ^ (r/2 % 4)))
+        // so that reading one row per lane is free of bank conflicts
+        const int cc = lane & 3;
+        // per-lane copy state, fixed for the whole tile: source row pointers
+        // (at this lane's chunk of the first k-block), whether the row exists,
+        // and the destination offsets within a slot
+        const int8_t* gsrc[4];
+        bool row_in[4];
+        uint32_t doff[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int rr = 8 * j + (lane >> 2);
+            const int64_t row = row0 + rr;
+            row_in[j] = row < nrows;
+            gsrc[j] = src + (row_in[j] ? row * p.K + (int64_t)kb0 * BK + 16 * cc : 0);
+            doff[j] = (uint32_t)rr * 64u + ((is_a ? (uint32_t)(cc ^ ((rr >> 1) & 3)) : (uint32_t)cc) << 4);
+        }
+        const int64_t k_lane = (int64_t)kb0 * BK + 16 * cc;  // this lane's k in the first k-block
+        auto issue = [&](int i) {  // own k-block i of this group
+            const int kb = g + NGROUP * i;
+            if (kb < nkb) {
+                const uint32_t slot = ring + (uint32_t)(i % RING) * SLOT_BYTES;
+                const int64_t koff = (int64_t)kb * BK;
+                const bool k_in = k_lane + koff < p.K;
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const bool in = row_in[j] && k_in;
+                    cp_async16_zfill(slot + doff[j], in ? gsrc[j] + koff : src, in);
+                }
+            }
+            cp_async_commit();
+        };
+        // the failure-detection test hook: no copies and no arrivals, so the
+        // monitor's wait for the first stage runs out
+        const int nkb_conv = tc::producers_stalled() ? 0 : nkb;
+        for (int i = 0; i < RING - 1; ++i) issue(i);
+        uint32_t soff[4];  // weight pieces of this lane in the swizzled fp16 tile
+#pragma unroll
+        for (int j = 0; j < 4; ++j) soff[j] = tc::sw128_off((uint32_t)(32 * q + 8 * j + (lane >> 2)), 2u * (uint32_t)cc);
+        for (int i = 0;; ++i) {
+            const int kb = g + NGROUP * i;
+            if (kb >= nkb_conv) break;
+            __syncwarp();  // every lane is done with the slot the next copy overwrites
+            issue(i + RING - 1);
+            cp_async_wait<RING - 1>();
+            __syncwarp();  // all lanes' copies of k-block kb have landed
+            const uint8_t* slot = ringp + (size_t)(i % RING) * SLOT_BYTES;
+            const int s = kb % S16;
+            const uint32_t ph = (uint32_t)(kb / S16) & 1u;
+            if (is_a) {
+                uint4 cur[4];
+                const uint32_t sw = (uint32_t)(lane >> 1) & 3u;
+#pragma unroll
+                for (int c = 0; c < 4; ++c)
+                    cur[c] = *reinterpret_cast<const uint4*>(slot + lane * 64 + ((c ^ sw) << 4));
+                int rsp[4] = {0, 0, 0, 0};  // four independent dp4a chains
+                uint32_t h[32];
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    rsp[0] = abs_sum4(cur[c].x, rsp[0]);
+                    rsp[1] = abs_sum4(cur[c].y, rsp[1]);
+                    rsp[2] = abs_sum4(cur[c].z, rsp[2]);
+                    rsp[3] = abs_sum4(cur[c].w, rsp[3]);
+                    s8x4_to_f16(cur[c].x, h[8 * c + 0], h[8 * c + 1]);
+                    s8x4_to_f16(cur[c].y, h[8 * c + 2], h[8 * c + 3]);
+                    s8x4_to_f16(cur[c].z, h[8 * c + 4], h[8 * c + 5]);
+                    s8x4_to_f16(cur[c].w, h[8 * c + 6], h[8 * c + 7]);
+                }
+                const int rs = (rsp[0] + rsp[1]) + (rsp[2] + rsp[3]);
+                if (!tc::mbar_wait_warp(empty_bar(s), ph ^ 1u, abort_flag)) break;
+                tc::tc_fence_after();
+                tc::tmem_st32(tmem + ((uint32_t)(32 * q) << 16) + A_COL0 + 32u * (uint32_t)s, h);
+                // row sums: the odd CTA's go to the even CTA by st.async,
+                // counted as transaction bytes on the even CTA's barrier
+                const int trow = HM * (int)rank + 32 * q + lane;
+                if (leader)
+                    rowsum[s * BM + trow] = (uint32_t)rs;
+                else
+                    tc::st_async_b32(rowsum_l0 + 4u * (uint32_t)(s * BM + trow), (uint32_t)rs, full_bar_l0 + 8u * s);
+                tc::tmem_wait_st();
+                tc::tc_fence_before();
+                __syncwarp();
+                if (lane == 0) {
+                    if (leader)
+                        tc::mbar_arrive(full_bar(s));
+                    else
+                        tc::mbar_arrive_expect_tx_remote(full_bar_l0 + 8u * s, 32u * 4u);
+                }
+            } else {
+                uint32_t hb[4][8];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const uint4 v = *reinterpret_cast<const uint4*>(slot + (8 * j + (lane >> 2)) * 64 + 16 * cc);
+                    s8x4_to_f16(v.x, hb[j][0], hb[j][1]);
+                    s8x4_to_f16(v.y, hb[j][2], hb[j][3]);
+                    s8x4_to_f16(v.z, hb[j][4], hb[j][5]);
+                    s8x4_to_f16(v.w, hb[j][6], hb[j][7]);
+                }
+                if (!tc::mbar_wait_warp(empty_bar(s), ph ^ 1u, abort_flag)) break;
+                uint8_t* tS = tiles + (size_t)s * B16_BYTES;
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    *reinterpret_cast<uint4*>(tS + soff[j]) = make_uint4(hb[j][0], hb[j][1], hb[j][2], hb[j][3]);
+                    *reinterpret_cast<uint4*>(tS + (soff[j] ^ 16u)) =
+                        make_uint4(hb[j][4], hb[j][5], hb[j][6], hb[j][7]);
+                }
+                tc::fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    if (leader)
+                        tc::mbar_arrive(full_bar(s));
+                    else
+                        tc::mbar_arrive_remote(full_bar_l0 + 8u * s);
+                }
+            }
+        }
+        cp_async_wait<0>();
+    } else if (warp == MMA_WARP) {
+        // ---------------------------------------------------------- MMA issuer (even CTA)
+        if (leader) {
+            const uint32_t IDESC = p.idesc;
+            const uint32_t tiles_addr = tc::smem_addr(tiles);
+            const uint32_t peer_misc1 = tc::mapa(tc::smem_addr((const void*)&misc[1]), 1);
+            const uint32_t peer_ev = tc::mapa(ev_bar, 1);
+            bool started = false;
+            uint32_t ndrain = 0;
+            bool ok = true;
+            // announce an event (drain or final) to the epilogue warps of both CTAs
+            auto post_event = [&](uint32_t type) {
+                misc[1] = type;
+                tc::st_cluster_u32(peer_misc1, type);  // ordered before the release below
+                tc::mbar_arrive(ev_bar);
+                tc::mbar_arrive_cluster(peer_ev);
+                tc::mma_commit_pair(acc_full, 3);
+            };
+            for (int kb = 0; kb < nkb && ok; ++kb) {
+                const int s = kb % S16;
+                const uint32_t ph = (uint32_t)(kb / S16) & 1u;
+                // the monitor's word for this stage: operands full, drain or not
+                if (!tc::mbar_wait_warp(dec_bar(s), ph, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                if (drain_dec[s] != 0) {
+                    if (tc::elect_one()) post_event(EV_DRAIN);
+                    __syncwarp();
+                    if (!tc::mbar_wait_cluster_warp(acc_empty, ndrain & 1u, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    ++ndrain;
+                    started = false;
+                }
+                tc::tc_fence_after();
+                const uint64_t bd = tc::desc_sw128(tiles_addr + (uint32_t)s * B16_BYTES);
+                const uint32_t a_tm = tmem + A_COL0 + 32u * (uint32_t)s;
+                if (tc::elect_one()) {
+#pragma unroll
+                    for (int j = 0; j < BK / 16; ++j)  // 16 k (8 TMEM columns, 32 B of B rows) per MMA
+                        tc::mma_f16_pair_tmem_a(tmem + ACC_COL, a_tm + 8u * j, bd + 2 * j, IDESC,
+                                                (started || j > 0) ? 1u : 0u);
+                    tc::mma_commit_pair(empty_bar(s), 3);
+                }
+                started = true;
+                __syncwarp();
+            }
+            if (tc::elect_one()) {
+                post_event(ok ? EV_FINAL : 0u);
+                tc::mma_commit_pair(done_bar, 3);
+            }
+            __syncwarp();
+        }
+        tc::mbar_wait_drain(done_bar, 0, leader ? 0u : kIdleSleepNs);
+        __syncwarp();
+    } else if (warp == MON_WARP) {
+        // ---------------------------------------------------------- drain monitor (even CTA)
+        if (leader) {
+            uint32_t S[8] = {0, 0, 0, 0, 0, 0, 0, 0};  // running sum|qx| of rows 8 lane .. 8 lane + 7
+            uint32_t smax = 0;                          // max over the 256 rows of S
+            bool started = false;
+            for (int kb = 0; kb < nkb; ++kb) {
+                const int s = kb % S16;
+                const uint32_t ph = (uint32_t)(kb / S16) & 1u;
+                if (!tc::mbar_wait_warp(full_bar(s), ph, abort_flag)) break;
+                // the stage's row sums, read before the stage is handed on
+                const uint4 b0 = *reinterpret_cast<const uint4*>(rowsum + s * BM + lane * 8);
+                const uint4 b1 = *reinterpret_cast<const uint4*>(rowsum + s * BM + lane * 8 + 4);
+                // drain first if a row could pass the limit with this k-block
+                const bool drain = started && smax > ROWSUM_LIMIT - KB_SUM_MAX;
+                if (lane == 0) drain_dec[s] = drain ? 1u : 0u;
+                __syncwarp();
+                if (lane == 0) tc::mbar_arrive(dec_bar(s));
+                const uint32_t B[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+                uint32_t mx = 0;
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    S[i] = (drain ? 0u : S[i]) + B[i];
+                    mx = max(mx, S[i]);
+                }
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+                smax = mx;
+                started = true;
+            }
+        }
+        __syncwarp();
+    } else {
+        // ---------------------------------------------------------- drains + epilogue (own rows)
+        const int q = warp & 3;
+        const uint32_t lane_base = (uint32_t)(32 * q) << 16;
+        const int64_t m = mh + 32 * q + lane;
+        const int64_t trow = (int64_t)HM * rank + 32 * q + lane;  // row within the tile
+        uint32_t ndrain = 0;
+        for (uint32_t ev = 0;; ++ev) {
+            if (!tc::mbar_wait_cluster_warp(ev_bar, ev & 1u, abort_flag, kIdleSleepNs)) break;
+            const uint32_t type = misc[1];
+            if (!tc::mbar_wait_warp(acc_full, ev & 1u, abort_flag)) break;
+            tc::tc_fence_after();
+            if (type != EV_DRAIN && type != EV_FINAL) break;
+            const float sxm = (type == EV_FINAL && m < p.M) ? p.sx[m] : 0.0f;
+            for (int c = 0; c < BN; c += 16) {
+                __syncwarp();
+                uint32_t a[16];
+                tc::tmem_ld16(tmem + lane_base + ACC_COL + c, a);
+                tc::tmem_wait_ld();
+                int tot[16];
+#pragma unroll
+                for (int j = 0; j < 16; ++j) tot[j] = __float2int_rn(__uint_as_float(a[j]));
+                if (m >= p.M) continue;
+                const int64_t nb = n0 + c;
+                if (nb >= p.N) continue;
+                int32_t* dp = dtile + trow * dld + c;
+                const bool full = (nb + 16 <= p.N) && (p.N % 4 == 0);
+                if (ndrain) {
+                    if (full) {
+#pragma unroll
+                        for (int j = 0; j < 16; j += 4) {
+                            int4 v = *reinterpret_cast<const int4*>(dp + j);
+                            tot[j] += v.x;
+                            tot[j + 1] += v.y;
+                            tot[j + 2] += v.z;
+                            tot[j + 3] += v.w;
+                        }
+                    } else {
+                        for (int j = 0; j < 16; ++j)
+                            if (nb + j < p.N) tot[j] += dp[j];
+                    }
+                }
+                if (type == EV_DRAIN || split) {
+                    if (full) {
+#pragma unroll
+                        for (int j = 0; j < 16; j += 4)
+                            *reinterpret_cast<int4*>(dp + j) = make_int4(tot[j], tot[j + 1], tot[j + 2], tot[j + 3]);
+                    } else {
+                        for (int j = 0; j < 16; ++j)
+                            if (nb + j < p.N) dp[j] = tot[j];
+                    }
+                } else {
+                    store_row<16>(tot, m, nb, p.N, sxm, p.sw, p.y, p.yt, p.acc_out, p.add);
+                }
+            }
+            if (type == EV_FINAL) break;
+            ++ndrain;
+            tc::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) tc::mbar_arrive_cluster(acc_empty_l0);
+        }
+    }
+
+    tc::tc_fence_before();
+    tc::cluster_sync();  // no MMA, remote arrival or remote store of the pair is still in flight
+    if (warp == MMA_WARP) {
+        tc::tc_fence_after();
+        tc::tmem_dealloc_pair(tmem, TMEM_COLS);
+    }
+}
+
 // Launch plan of k_w8a8_tc: weight rows per CTA and the split of the last,
 // partial wave of tiles.
 struct W8Plan {
@@ -692,25 +1112,107 @@ static W8Plan w8_plan(int64_t M, int64_t N, int64_t K) {
     return pl;
 }
 
+// Co-resident clusters of k_w8a8_pair (pairs of SMs that can run at once).
+static int w8p_clusters() {
+    static int n = 0;
+    if (n == 0) {
+        int nc = 0;
+        if (ensure_smem((const void*)k_w8a8_pair, (int)w8p::SMEM_BYTES) == cudaSuccess) {
+            cudaLaunchConfig_t cfg = {};
+            cfg.gridDim = dim3((unsigned)(2 * num_sms()));
+            cfg.blockDim = dim3(w8p::THREADS);
+            cfg.dynamicSmemBytes = w8p::SMEM_BYTES;
+            if (cudaOccupancyMaxActiveClusters(&nc, (const void*)k_w8a8_pair, &cfg) != cudaSuccess) nc = 0;
+            (void)cudaGetLastError();
+        }
+        n = nc > 0 ? nc : num_sms() / 2;
+    }
+    return n;
+}
+
+// Launch plan of k_w8a8_pair: 256 x 256 tiles over the co-resident pairs, the
+// last partial wave cut into K parts as for k_w8a8_tc.
+static W8Plan w8p_plan(int64_t M, int64_t N, int64_t K) {
+    using namespace w8p;
+    W8Plan pl{};
+    const int units = w8p_clusters();
+    pl.bn = BN;
+    pl.tiles = ceil_div(M, BM) * ceil_div(N, BN);
+    const int64_t tail = pl.tiles % units;
+    const int64_t nkb = ceil_div(K, BK);
+    pl.split = 1;
+    if (tail > 0) {
+        int64_t sp = units / tail;
+        if (sp > 4) sp = 4;
+        while (sp > 1 && nkb < 4 * sp) --sp;
+        pl.split = (int)sp;
+    }
+    pl.tail_tiles = pl.split > 1 ? tail : 0;
+    pl.full_tiles = pl.tiles - pl.tail_tiles;
+    return pl;
+}
+
 // INT32 tile that drains of the exact accumulation add into (touched only
 // when a drain occurs), then the partial-sum slices of the split tail tiles.
 static size_t w8a8_drain_bytes(int64_t M, int64_t N) { return ((size_t)M * N * sizeof(int32_t) + 15) & ~(size_t)15; }
 
-size_t w8a8_ws_bytes(int64_t M, int64_t N, int64_t K) {
-    const W8Plan pl = w8_plan(M, N, K);
-    return w8a8_drain_bytes(M, N) + (size_t)pl.tail_tiles * pl.split * w8tc::BM * w8tc::BN * sizeof(int32_t);
+static size_t w8_part_bytes(const W8Plan& pl) {
+    return (size_t)pl.tail_tiles * pl.split * w8tc::BM * w8tc::BN * sizeof(int32_t);
 }
 
-// 1 selects the legacy mma.sync kernel (read on every call, so a process can
-// compare both kernels).
+// Enough for either tensor-core kernel (the choice can change between calls).
+size_t w8a8_ws_bytes(int64_t M, int64_t N, int64_t K) {
+    const size_t a = w8_part_bytes(w8_plan(M, N, K)), b = w8_part_bytes(w8p_plan(M, N, K));
+    return w8a8_drain_bytes(M, N) + (a > b ? a : b);
+}
+
+// QLIN_W8A8_KERNEL: "mma" the legacy mma.sync kernel, "tc1" the single-CTA
+// tensor-core kernel; otherwise the CTA-pair kernel.  Read on every call, so
+// a process can compare the kernels (all give the same exact INT32 sums).
 static int w8a8_kernel_choice() {
     const char* e = getenv("QLIN_W8A8_KERNEL");
-    return (e && strcmp(e, "mma") == 0) ? 1 : 0;
+    if (e && strcmp(e, "mma") == 0) return 1;
+    if (e && strcmp(e, "tc1") == 0) return 0;
+    return 2;
+}
+
+static cudaError_t run_w8a8_pair(const int8_t* qx, const float* sx, const int8_t* qw, const float* sw, int64_t M,
+                                 int64_t N, int64_t K, void* y, int yt, int32_t* acc_out, void* ws, cudaStream_t st,
+                                 const float* add) {
+    using namespace w8p;
+    cudaError_t e = ensure_smem((const void*)k_w8a8_pair, (int)SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    const W8Plan pl = w8p_plan(M, N, K);
+    W8TcArgs a;
+    a.sx = sx;
+    a.sw = sw;
+    a.M = M;
+    a.N = N;
+    a.K = K;
+    a.y = y;
+    a.yt = yt;
+    a.acc_out = acc_out;
+    a.add = add;
+    a.drain = reinterpret_cast<int32_t*>(ws);
+    a.part = reinterpret_cast<int32_t*>(reinterpret_cast<uint8_t*>(ws) + w8a8_drain_bytes(M, N));
+    a.full_tiles = pl.full_tiles;
+    a.tail_split = pl.split;
+    a.num_m_tiles = (int)ceil_div(M, BM);
+    a.bn = BN;
+    a.idesc = tc::idesc_f16(BM, BN, false);
+    const int64_t clusters = pl.full_tiles + pl.tail_tiles * pl.split;
+    k_w8a8_pair<<<(unsigned)(2 * clusters), THREADS, SMEM_BYTES, st>>>(qx, qw, a);
+    if ((e = cudaGetLastError()) != cudaSuccess || pl.tail_tiles == 0) return e;
+    const int64_t work = pl.tail_tiles * BM * (BN / 16);
+    k_w8a8_tail<<<(unsigned)ceil_div(work, 256), 256, 0, st>>>(a, (int)pl.tail_tiles);
+    return cudaGetLastError();
 }
 
 cudaError_t run_gemm_w8a8(const int8_t* qx, const float* sx, const int8_t* qw, const float* sw, int64_t M, int64_t N,
                           int64_t K, void* y, int yt, int32_t* acc_out, void* ws, cudaStream_t st, const float* add) {
-    if (w8a8_kernel_choice() == 1 && !add) {
+    const int choice = w8a8_kernel_choice();
+    if (choice == 2) return run_w8a8_pair(qx, sx, qw, sw, M, N, K, y, yt, acc_out, ws, st, add);
+    if (choice == 1 && !add) {
         using namespace w8;
         size_t smem = (size_t)2 * STAGES * TILE_BYTES;
         cudaError_t e = ensure_smem((const void*)k_w8a8_mma, (int)smem);

@@ -38,16 +38,38 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     return ok != 0;
 }
 
+// try_wait that lets the hardware suspend the thread until the phase
+// completes or about kSuspendHintNs have passed: a blocked warp then takes
+// no issue slots, where a polling loop would spend them on every retry.
+constexpr uint32_t kSuspendHintNs = 20000;
+__device__ __forceinline__ bool mbar_try_wait_suspend(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity), "r"(kSuspendHintNs)
+        : "memory");
+    return ok != 0;
+}
+
 // Bounded wait for the phase of parity `parity` to complete.  Returns false
 // when the CTA's abort flag is up, or after g_wait_limit_cycles (then it
 // raises the abort flag and records QLIN_ERR_TIMEOUT in the device error word).
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                          uint32_t max_sleep_ns = 0) {
     if (mbar_try_wait(bar, parity)) return true;
     const long long limit = g_wait_limit_cycles;
     long long t0 = clock64();
+    uint32_t ns = 32;
     for (uint32_t i = 1;; ++i) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if ((i & 255u) == 0) {
+        if (max_sleep_ns) {  // see mbar_wait_drain
+            __nanosleep(ns);
+            if (ns < max_sleep_ns) ns <<= 1;
+        }
+        if (mbar_try_wait_suspend(bar, parity)) return true;
+        {
             if (*abort_flag) return false;
             if (clock64() - t0 > limit) {
                 *abort_flag = 1;
@@ -61,14 +83,22 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
 // Bounded wait that ignores the abort flag: the MMA issuer's last wait, for
 // the commit that covers every MMA it issued.  Those MMAs depend on nothing
 // else, so the commit arrives even after an abort, and TMEM is freed only
-// once no MMA can still write it.
-__device__ __forceinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity) {
+// once no MMA can still write it.  max_sleep_ns > 0: a warp that would poll
+// for a long time (until the end of a tile) sleeps between polls, with a
+// doubling sleep up to that bound, so that it takes no issue slots or
+// barrier-unit bandwidth from the warps that feed the tensor cores.
+__device__ __forceinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity, uint32_t max_sleep_ns = 0) {
     if (mbar_try_wait(bar, parity)) return true;
     const long long limit = g_wait_limit_cycles;
     long long t0 = clock64();
+    uint32_t ns = 32;
     for (uint32_t i = 1;; ++i) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if ((i & 255u) == 0 && clock64() - t0 > limit) {
+        if (max_sleep_ns) {
+            __nanosleep(ns);
+            if (ns < max_sleep_ns) ns <<= 1;
+        }
+        if (mbar_try_wait_suspend(bar, parity)) return true;
+        if (clock64() - t0 > limit) {
             raise_device_error(QLIN_ERR_TIMEOUT);
             return false;
         }
@@ -81,8 +111,9 @@ __device__ __forceinline__ bool producers_stalled() { return g_stall_producers !
 // Warp-uniform bounded wait: every lane waits, and the warp agrees on the
 // outcome, so that a timeout never leaves part of a warp inside a later
 // __syncwarp.
-__device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
-    bool ok = mbar_wait(bar, parity, abort_flag);
+__device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                               uint32_t max_sleep_ns = 0) {
+    bool ok = mbar_wait(bar, parity, abort_flag, max_sleep_ns);
     return __all_sync(0xffffffffu, ok);
 }
 
@@ -201,6 +232,130 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16
 }
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+// ------------------------------------------------------------------ CTA pairs (clusters of 2)
+// Rank of this CTA in its cluster.
+__device__ __forceinline__ uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+// Address, in the cluster's shared window, of the variable at `saddr` (this
+// CTA's shared window) in the CTA of rank `rank`.
+__device__ __forceinline__ uint32_t mapa(uint32_t saddr, uint32_t rank) {
+    uint32_t d;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(d) : "r"(saddr), "r"(rank));
+    return d;
+}
+// Arrive on an mbarrier of any CTA of the cluster (address from mapa), with
+// release semantics at cluster scope.
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cbar) {
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cbar) : "memory");
+}
+// Relaxed arrivals on a barrier of the other CTA, for the per-k-block
+// hand-offs whose data is ordered by its own mechanism (tcgen05 fences, the
+// async-proxy fence, st.async transaction bytes): a release at cluster scope
+// would hold the arriving thread until all its earlier writes are visible
+// cluster-wide.
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t cbar) {
+    asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cbar) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx_remote(uint32_t cbar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.relaxed.cluster.shared::cluster.b64 _, [%0], %1;" ::"r"(cbar), "r"(bytes)
+                 : "memory");
+}
+// 4-byte store into the shared memory of a CTA of the cluster, completing as
+// 4 transaction bytes on the barrier `cbar` of that CTA.
+__device__ __forceinline__ void st_async_b32(uint32_t caddr, uint32_t v, uint32_t cbar) {
+    asm volatile("st.async.weak.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];" ::"r"(caddr), "r"(v),
+                 "r"(cbar)
+                 : "memory");
+}
+__device__ __forceinline__ void st_cluster_u32(uint32_t caddr, uint32_t v) {
+    asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(caddr), "r"(v) : "memory");
+}
+// Every thread of both CTAs: all earlier writes (shared memory included) are
+// visible cluster-wide after it.
+__device__ __forceinline__ void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
+}
+// try_wait with acquire semantics at cluster scope: for barriers that threads
+// of the other CTA of the pair arrive on.
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity), "r"(kSuspendHintNs)
+        : "memory");
+    return ok != 0;
+}
+// mbar_wait_warp for barriers with arrivals from the other CTA of the pair;
+// max_sleep_ns as for mbar_wait_drain.
+__device__ __forceinline__ bool mbar_wait_cluster_warp(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                                       uint32_t max_sleep_ns = 0) {
+    bool ok = true;
+    if (!mbar_try_wait_cluster(bar, parity)) {
+        const long long limit = g_wait_limit_cycles;
+        const long long t0 = clock64();
+        uint32_t ns = 32;
+        for (uint32_t i = 1;; ++i) {
+            if (max_sleep_ns) {
+                __nanosleep(ns);
+                if (ns < max_sleep_ns) ns <<= 1;
+            }
+            if (mbar_try_wait_cluster(bar, parity)) break;
+            {
+                if (*abort_flag) {
+                    ok = false;
+                    break;
+                }
+                if (clock64() - t0 > limit) {
+                    *abort_flag = 1;
+                    raise_device_error(QLIN_ERR_TIMEOUT);
+                    ok = false;
+                    break;
+                }
+            }
+        }
+    }
+    return __all_sync(0xffffffffu, ok);
+}
+
+// tcgen05 with a CTA pair: each CTA's allocating warp runs the pair forms of
+// alloc / relinquish / dealloc; the MMA is issued by the even CTA and reads
+// and writes the TMEM and shared memory of both (A and D rows split by CTA,
+// B rows split by CTA).
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t dst_smem, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem), "r"(ncols)
+                 : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish_pair() {
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+// D[tmem] (+)= A[tmem] * B[smem desc]^T over the pair, kind::f16.
+__device__ __forceinline__ void mma_f16_pair_tmem_a(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                                    uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+// Arrive on the mbarrier at `bar` (shared-window offset) in every CTA of
+// `cta_mask` once the pair MMAs issued so far have completed.
+__device__ __forceinline__ void mma_commit_pair(uint32_t bar, uint16_t cta_mask) {
+    asm volatile(
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(bar),
+        "h"(cta_mask)
+        : "memory");
+}
 
 // ------------------------------------------------------------------ descriptors
 // Shared-memory matrix descriptor, K-major operand in the 128-byte swizzle

@@ -40,7 +40,11 @@ def _w8a8_inputs(M, N, K, seed):
     return qx, sx, qw, sw
 
 
-def test_w8a8_wait_times_out_then_recovers():
+@pytest.mark.parametrize("kernel", ["pair", "tc1"])
+def test_w8a8_wait_times_out_then_recovers(kernel, monkeypatch):
+    """Both tensor-core kernels: the CTA pair (converters stall, the drain
+    monitor's wait runs out) and the single CTA (the TMA warp stalls)."""
+    monkeypatch.setenv("QLIN_W8A8_KERNEL", kernel)
     M, N, K = 256, 512, 2048
     qx, sx, qw, sw = _w8a8_inputs(M, N, K, 1)
     with stalled():

@@ -16,6 +16,14 @@ pytestmark = pytest.mark.gpu
 
 
 # ------------------------------------------------------------------ W8A8
+@pytest.fixture(params=["pair", "tc1"])
+def w8_kernel(request, monkeypatch):
+    """Each W8A8 case runs on both tensor-core kernels: the CTA-pair kernel
+    (the default) and the single-CTA kernel."""
+    monkeypatch.setenv("QLIN_W8A8_KERNEL", request.param)
+    return request.param
+
+
 def w8a8_run(x_dev, w_dev, out_dtype=torch.float32, smooth=None):
     """Quantize X per token (optionally smoothed) and W per output channel on
     the GPU, run the GEMM with acc_out; return device results."""
@@ -31,7 +39,7 @@ def w8a8_run(x_dev, w_dev, out_dtype=torch.float32, smooth=None):
     return qx, sx, qw, sw, acc, y
 
 
-def test_w8a8_tiny_config():
+def test_w8a8_tiny_config(w8_kernel):
     """8x128x256 fp32 with outlier channels 3 and 77, fp32 epilogue."""
     cfg = inputs.w8a8_tiny()
     xd = torch.from_numpy(cfg.x).cuda()
@@ -58,7 +66,7 @@ def test_w8a8_tiny_config():
 
 @pytest.mark.parametrize("M,N,K", [(1, 1, 16), (3, 5, 32), (17, 33, 80), (130, 129, 208), (64, 256, 1040),
                                    (255, 384, 4096), (128, 128, 2048 + 16)])
-def test_w8a8_ragged_exact(M, N, K):
+def test_w8a8_ragged_exact(M, N, K, w8_kernel):
     rng = np.random.default_rng(M * 1000 + N + K)
     qx = torch.from_numpy(rng.integers(-127, 128, (M, K)).astype(np.int8)).cuda()
     qw = torch.from_numpy(rng.integers(-127, 128, (N, K)).astype(np.int8)).cuda()
@@ -75,7 +83,7 @@ def test_w8a8_ragged_exact(M, N, K):
 
 
 @pytest.mark.parametrize("K", [1024, 1040, 4096, 28672])
-def test_w8a8_extreme_sums(K):
+def test_w8a8_extreme_sums(K, w8_kernel):
     """All codes +-127: partial sums reach 16129*K (beyond 2^24 for K > 1040)."""
     M, N = 128, 256
     qx = torch.full((M, K), 127, dtype=torch.int8, device="cuda")
@@ -92,7 +100,7 @@ def test_w8a8_extreme_sums(K):
 
 
 @pytest.mark.parametrize("smooth", [False, True])
-def test_w8a8_prefill_config_sampled(smooth):
+def test_w8a8_prefill_config_sampled(smooth, w8_kernel):
     """2048 x 11008 x 4096 SmoothQuant-style prefill; oracle on 64 sampled rows."""
     x, w, _ = inputs.w8a8_prefill()
     xd, wd = x.cuda(), w.cuda()
@@ -127,7 +135,7 @@ def stratified_rows(M, tile, per_tile, seed):
 
 
 @pytest.mark.parametrize("folded", [False, True])
-def test_w8a8_downproj_sampled(folded):
+def test_w8a8_downproj_sampled(folded, w8_kernel):
     """4096 x 8192 x 28672 with outlier channels: two random rows from every
     256-row tile, all 8192 columns (so every output tile, the split-K tail
     tiles of the last wave included, is checked).  folded: the step's input,
@@ -227,7 +235,7 @@ def test_w4a16_downproj_sampled(M):
 
 
 @pytest.mark.parametrize("M,N,K", [(128, 256, 64), (200, 300, 1056), (64, 512, 28672)])
-def test_w8a8_tensor_core_matches_legacy_kernel(M, N, K, monkeypatch):
+def test_w8a8_tensor_core_matches_legacy_kernel(M, N, K, w8_kernel, monkeypatch):
     """The fp16-tensor-core kernel and the legacy mma.sync s8 kernel give the
     same INT32 sums and the same outputs."""
     rng = np.random.default_rng(M + N + K)
@@ -246,7 +254,7 @@ def test_w8a8_tensor_core_matches_legacy_kernel(M, N, K, monkeypatch):
     assert qlin.qlin_device_error() == 0
 
 
-def test_w8a8_drain_boundary():
+def test_w8a8_drain_boundary(w8_kernel):
     """Rows whose |code| sums cross the 2^24 / 128 drain threshold at different
     k-blocks: every row's sum stays exact."""
     M, N, K = 128, 256, 8192
@@ -262,7 +270,7 @@ def test_w8a8_drain_boundary():
     np.testing.assert_array_equal(acc.cpu().numpy(), acco)
 
 
-def test_w8a8_split_tail_tiles():
+def test_w8a8_split_tail_tiles(w8_kernel):
     """2560 x 4096 x 1024: 160 tiles of 256 x 256, so the 12 tiles after the
     first 148 are cut into K parts whose INT32 sums are added by a second
     kernel; sampled rows of those tiles and of whole tiles stay exact."""
@@ -411,7 +419,7 @@ def test_w4a16_back_to_back_calls(M):
     assert torch.equal(ys[0], refs[0]) and torch.equal(ys[1], refs[1])
 
 
-def test_w8a8_back_to_back_calls():
+def test_w8a8_back_to_back_calls(w8_kernel):
     """W8A8 calls queued back to back (split tail tiles and drains included):
     no device-side wait runs out and the bits match a lone call."""
     M, N, K = 2048, 4096, 28672
