@@ -380,13 +380,17 @@ __device__ __forceinline__ void codes_of_chunk(const uint4 raw, const ScopeParam
         code_bits8<true, true, OUTLINE>(v, sp, cr, cb);
 }
 
-// Per-token scopes of long rows (more than 4096 values) streamed through
-// shared memory by bulk copies.  Each persistent CTA keeps `nbuf` row buffers:
-// while it reduces and quantizes one row, the copies of its next rows land in
-// the others.  NT threads per CTA; two CTAs with two buffers each fit an SM
+// Row-local scopes of 16-bit rows streamed through shared memory by bulk
+// copies.  Each persistent CTA keeps `nbuf` row buffers: while it reduces and
+// quantizes one row, the copies of its next rows land in the others.  NT
+// threads per CTA: 512 for long rows (two such CTAs with two buffers fit an SM
 // for rows of up to 28,672 values, so one CTA's barriers overlap the other's
-// work.
-template <typename T, bool SYM, bool STATIC, bool CODE4, int NT>
+// work), 128 for rows of up to 8192 values (a dozen CTAs share an SM, so many
+// rows are in flight and each row's reduction spans only four warps).
+// GL = 0: per-row scopes (a range pass, a CTA-wide maximum, a code pass);
+// GL > 0: groups of 8 GL values, one pass, the GL lanes of a group reducing
+// with shuffles (no CTA-wide step besides the buffer release).
+template <typename T, bool SYM, bool STATIC, bool CODE4, int NT, int GL>
 __global__ void __launch_bounds__(NT) k_qrow_bulk(QuantArgs a, uint32_t buf_stride, int nbuf) {
     extern __shared__ __align__(128) uint8_t qb_smem[];
     __shared__ float red_hi[NT / 32], red_lo[NT / 32];
@@ -424,6 +428,53 @@ __global__ void __launch_bounds__(NT) k_qrow_bulk(QuantArgs a, uint32_t buf_stri
         const bool ok = tc::mbar_wait(bar0 + 8u * b, ph, &abort_flag);
         if (!__syncthreads_and(ok)) break;
         const uint4* xs16 = reinterpret_cast<const uint4*>(qb_smem + (size_t)b * buf_stride);
+        if constexpr (GL > 0) {
+            // per-group scopes: one pass; every lane of a warp takes part in
+            // the shuffles (groups are whole chunks, so a group's lanes are
+            // all live or all idle)
+            const uint32_t ngr = (uint32_t)(a.cols / a.group);
+            const uint32_t span = (nchunks + 31u) & ~31u;
+            uint8_t* qrow = reinterpret_cast<uint8_t*>(a.q) + r * qld;
+#pragma unroll 2
+            for (uint32_t c = tid; c < span; c += NT) {
+                const bool live = c < nchunks;
+                const uint4 raw = live ? xs16[c] : make_uint4(0, 0, 0, 0);
+                const int64_t sc = r * ngr + c / GL;
+                float s;
+                int z;
+                if (STATIC) {
+                    s = live ? load_scale(a.s, sc, a.scale_f16) : 1.0f;
+                    z = (a.z && live) ? a.z[sc] : 0;
+                } else {
+                    PairRange<T> pr;
+                    pr.add(raw, SYM);
+                    float hi, lo;
+                    pr.result(SYM, hi, lo);
+#pragma unroll
+                    for (int o = 1; o < GL; o <<= 1) {
+                        hi = fmaxf(hi, __shfl_xor_sync(0xffffffffu, hi, o));
+                        if (!SYM) lo = fminf(lo, __shfl_xor_sync(0xffffffffu, lo, o));
+                    }
+                    scale_zero(lo, hi, a.qmin, a.qmax, SYM, a.scale_f16, s, z);
+                    if (live && (tid & (GL - 1)) == 0) {
+                        store_scale(a.s, sc, a.scale_f16, s);
+                        if (!SYM) a.z[sc] = z;
+                    }
+                }
+                if (live) {
+                    uint32_t cb[8];
+                    codes_of_chunk<T, SYM, STATIC, false>(raw, make_scope(s, z), cr, cb);
+                    put_codes8<CODE4>(qrow, c, cb);
+                }
+            }
+            __syncthreads();  // buffer b is free
+            if (tid == 0 && !stalled && r + (int64_t)nbuf * gridDim.x < a.rows) issue(r + (int64_t)nbuf * gridDim.x, b);
+            if (++b == nbuf) {
+                b = 0;
+                ph ^= 1u;
+            }
+            continue;
+        }
         float s;
         int z;
         if (STATIC) {
@@ -1246,20 +1297,51 @@ static cudaError_t launch_qrow_warp(const QuantArgs& a, cudaStream_t st) {
 // up to 28,672 16-bit values; longer rows take one CTA with three buffers.
 constexpr size_t kSmemPerSM = 233472;
 
-template <typename T, bool SYM, bool STATIC, bool CODE4>
-static cudaError_t launch_qrow_bulk_m(const QuantArgs& a, uint32_t buf_stride, cudaStream_t st) {
-    const bool two = 2 * (2 * (size_t)buf_stride + 1024 + 512) <= kSmemPerSM;
-    const int nbuf = two ? 2 : (3 * (size_t)buf_stride <= 200 * 1024 ? 3 : 2);
-    const int smem = nbuf * (int)buf_stride;
-    // 512 threads (about 40 registers each: two CTAs of 512 fit an SM;
-    // measured 74.5 us against 79.8 us with 256 threads on 4096 x 28672)
-    const void* kern = (const void*)k_qrow_bulk<T, SYM, STATIC, CODE4, 512>;
+template <typename T, bool SYM, bool STATIC, bool CODE4, int NT, int GL>
+static cudaError_t launch_qrow_bulk_k(const QuantArgs& a, uint32_t buf_stride, cudaStream_t st) {
+    const void* kern = (const void*)k_qrow_bulk<T, SYM, STATIC, CODE4, NT, GL>;
+    int nbuf, smem;
+    int64_t grid;
+    if (NT == 512) {
+        const bool two = 2 * (2 * (size_t)buf_stride + 1024 + 512) <= kSmemPerSM;
+        nbuf = two ? 2 : (3 * (size_t)buf_stride <= 200 * 1024 ? 3 : 2);
+        smem = nbuf * (int)buf_stride;
+        grid = (int64_t)num_sms() * (two ? 2 : 1);
+    } else {
+        nbuf = 2;
+        smem = nbuf * (int)buf_stride;
+    }
     cudaError_t e = ensure_smem(kern, smem);
     if (e != cudaSuccess) return e;
-    int64_t grid = (int64_t)num_sms() * (two ? 2 : 1);
+    if (NT != 512) {
+        int per_sm = 0;
+        if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, NT, smem)) != cudaSuccess) return e;
+        grid = (int64_t)num_sms() * (per_sm > 0 ? per_sm : 1);
+    }
     if (grid > a.rows) grid = a.rows;
-    k_qrow_bulk<T, SYM, STATIC, CODE4, 512><<<(unsigned)grid, 512, smem, st>>>(a, buf_stride, nbuf);
+    k_qrow_bulk<T, SYM, STATIC, CODE4, NT, GL><<<(unsigned)grid, NT, smem, st>>>(a, buf_stride, nbuf);
     return cudaGetLastError();
+}
+
+// NT = 512 threads for rows of more than 8192 values, 128 for shorter ones
+// (measured on 16384 x 4096 and 4096 x 28672 bf16).
+template <typename T, bool SYM, bool STATIC, bool CODE4, int GL>
+static cudaError_t launch_qrow_bulk_g(const QuantArgs& a, uint32_t buf_stride, cudaStream_t st) {
+    if (a.cols <= 8192) return launch_qrow_bulk_k<T, SYM, STATIC, CODE4, 128, GL>(a, buf_stride, st);
+    return launch_qrow_bulk_k<T, SYM, STATIC, CODE4, 512, GL>(a, buf_stride, st);
+}
+
+template <typename T, bool SYM, bool STATIC, bool CODE4>
+static cudaError_t launch_qrow_bulk_m(const QuantArgs& a, uint32_t buf_stride, cudaStream_t st) {
+    if (a.gran == QLIN_PER_ROW) return launch_qrow_bulk_g<T, SYM, STATIC, CODE4, 0>(a, buf_stride, st);
+    switch (a.group / 8) {
+    case 1: return launch_qrow_bulk_g<T, SYM, STATIC, CODE4, 1>(a, buf_stride, st);
+    case 2: return launch_qrow_bulk_g<T, SYM, STATIC, CODE4, 2>(a, buf_stride, st);
+    case 4: return launch_qrow_bulk_g<T, SYM, STATIC, CODE4, 4>(a, buf_stride, st);
+    case 8: return launch_qrow_bulk_g<T, SYM, STATIC, CODE4, 8>(a, buf_stride, st);
+    case 16: return launch_qrow_bulk_g<T, SYM, STATIC, CODE4, 16>(a, buf_stride, st);
+    default: return launch_qrow_bulk_g<T, SYM, STATIC, CODE4, 32>(a, buf_stride, st);
+    }
 }
 
 template <typename T>
@@ -1311,6 +1393,14 @@ static void strip_grid(int64_t nchunks, int64_t rows, dim3& grid, int& rows_per_
     grid = dim3((unsigned)gx, (unsigned)gy);
 }
 
+// QLIN_QROW: "warp" keeps the register-resident row kernels (per-row rows of
+// up to 4096 values, per-group slabs) for comparisons; read on every call,
+// same codes.
+static int qrow_choice() {
+    const char* e = getenv("QLIN_QROW");
+    return (e && strcmp(e, "warp") == 0) ? 1 : 0;
+}
+
 static bool strip_ok(const QuantArgs& a, int xt) {
     int es = elem_size(xt);
     if (a.cols % 8 != 0 || a.rows == 0) return false;
@@ -1356,9 +1446,8 @@ static cudaError_t run_quantize_t(QuantArgs a, int xt, const qlin_qparams* p, vo
             // bounded by qmax: those calls take kernels that clamp and test
             // the range of every code
             const bool fast16 = !a.absmax_out && a.smooth_mode == QLIN_SMOOTH_NONE && !a.scale_f16;
-            if (fast16 && nchunks <= 512) return launch_qrow_warp<T>(a, st);
-            if (fast16 && a.gran == QLIN_PER_ROW && 2 * (size_t)buf_stride <= 200 * 1024)
-                return launch_qrow_bulk<T>(a, buf_stride, st);
+            if (fast16 && qrow_choice() == 1 && nchunks <= 512) return launch_qrow_warp<T>(a, st);
+            if (fast16 && 2 * (size_t)buf_stride <= 200 * 1024) return launch_qrow_bulk<T>(a, buf_stride, st);
         }
         if (a.gran == QLIN_PER_ROW && !a.absmax_out && nchunks > 1024 && row_bytes <= 113 * 1024) {
             cudaError_t e = ensure_smem((const void*)k_quant_longrows<T>, (int)row_bytes);
