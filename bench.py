@@ -69,14 +69,14 @@ def kernel_bytes_flops():
 
 
 # DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one W8A8 launch
-# at 4096 x 8192 x 28672, from a one-pass ncu capture, and a digest of the
-# sources that kernel was built from: a changed kernel reports no traffic until
-# it is captured again.
-W8A8_TRAFFIC_BYTES = 726.2e6 + 61.2e6
+# (the CTA-pair kernel k_w8a8_pair) at 4096 x 8192 x 28672, from a one-pass
+# ncu capture, and a digest of the sources that kernel was built from: a
+# changed kernel reports no traffic until it is captured again.
+W8A8_TRAFFIC_BYTES = 1099.9e6 + 61.1e6
 W8A8_TRAFFIC_SOURCES = ("activation_quantization_quantize_b300/csrc/gemm_w8a8.cu",
                         "activation_quantization_quantize_b300/csrc/tc_ptx.cuh",
                         "activation_quantization_quantize_b300/csrc/qlin_common.cuh")
-W8A8_TRAFFIC_DIGEST = "6ad71f251b79fe87"
+W8A8_TRAFFIC_DIGEST = "6a277da1499a7dba"
 
 
 def w8a8_traffic_bytes():
@@ -813,7 +813,7 @@ def main():
     roofline = {"bound": "tensor", "achieved": w8_tops, "peak": int8_peak, "unit": "TFLOP/s",
                 "frac": w8_tops / int8_peak, "traffic": w8a8_traffic_bytes(),
                 "traffic_unit": "bytes per launch (DRAM read + write)",
-                "kernel": "gemm_w8a8 (4096x8192x28672 int8 ops)",
+                "kernel": "gemm_w8a8 (k_w8a8_pair, 4096x8192x28672 int8 ops)",
                 "peak_source": "max(bf16 dense %s %.1f, torch._int_mm %s)" % (
                     peaks["source"], peaks["bf16_tflops"], "%.1f" % int8_ref if int8_ref else "n/a")}
     detail = {}
