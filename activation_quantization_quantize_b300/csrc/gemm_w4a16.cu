@@ -829,15 +829,25 @@ __global__ void __launch_bounds__(w4tc::THREADS, 1) k_w4_gemm_tc(const __grid_co
         const uint32_t rc = tc::smem_addr(rp) + lane * 16;               // codes [CRING][32][16 B]
         const uint32_t rm = tc::smem_addr(rp + CRING * 512) + lane * 8;  // words [CRING][32][8 B]
         int kb_issue = par, slot_issue = 0;
+        // running source pointers of this lane's next copy: codes advance by
+        // two 64-k blocks, the group words by the groups those cover (the
+        // lane's k, 64 kb + 16 t, sits in group (64 kb + 16 t) / g)
+        const uint8_t* pc = gcodes + (int64_t)par * 512;
+        const int64_t gi0 = ((int64_t)(c_begin + par) * 64 + 16 * t) >> gshift;
+        const uint8_t* ps = gsc + gi0 * 32;
+        const uint8_t* pz = gze + gi0 * 8;
+        const int gstep = 128 >> gshift;  // groups per two k-blocks (g <= 128)
         auto issue = [&]() {
             if (kb_issue < nkb) {
-                const int64_t gi = ((int64_t)(c_begin + kb_issue) * 64 + 16 * t) >> gshift;
-                cp_async16(rc + slot_issue * 512, gcodes + (int64_t)kb_issue * 512);
-                cp_async4(rm + slot_issue * 256, gsc + gi * 32);
-                if (asym) cp_async4(rm + slot_issue * 256 + 4, gze + gi * 8);
+                cp_async16(rc + slot_issue * 512, pc);
+                cp_async4(rm + slot_issue * 256, ps);
+                if (asym) cp_async4(rm + slot_issue * 256 + 4, pz);
             }
             cp_async_commit();
             kb_issue += 2;
+            pc += 1024;
+            ps += 32 * gstep;
+            pz += 8 * gstep;
             slot_issue = slot_issue + 1 == CRING ? 0 : slot_issue + 1;
         };
 #pragma unroll 1
@@ -1177,15 +1187,25 @@ __global__ void __launch_bounds__(w4tm::THREADS, 1) k_w4_gemm_tm(const __grid_co
         const uint32_t rm = tc::smem_addr(rp + CRING * 512) + lane * 8;          // words [CRING][32][8 B]
         const uint32_t t_lane = (uint32_t)(32 * q + 16 * hsel) << 16;
         int kb_issue = par, slot_issue = 0;
+        // running source pointers of this lane's next copy: codes advance by
+        // two 64-k blocks, the group words by the groups those cover (the
+        // lane's k, 64 kb + 16 t, sits in group (64 kb + 16 t) / g)
+        const uint8_t* pc = gcodes + (int64_t)par * 512;
+        const int64_t gi0 = ((int64_t)(c_begin + par) * 64 + 16 * t) >> gshift;
+        const uint8_t* ps = gsc + gi0 * 32;
+        const uint8_t* pz = gze + gi0 * 8;
+        const int gstep = 128 >> gshift;  // groups per two k-blocks (g <= 128)
         auto issue = [&]() {
             if (kb_issue < nkb) {
-                const int64_t gi = ((int64_t)(c_begin + kb_issue) * 64 + 16 * t) >> gshift;
-                cp_async16(rc + slot_issue * 512, gcodes + (int64_t)kb_issue * 512);
-                cp_async4(rm + slot_issue * 256, gsc + gi * 32);
-                if (asym) cp_async4(rm + slot_issue * 256 + 4, gze + gi * 8);
+                cp_async16(rc + slot_issue * 512, pc);
+                cp_async4(rm + slot_issue * 256, ps);
+                if (asym) cp_async4(rm + slot_issue * 256 + 4, pz);
             }
             cp_async_commit();
             kb_issue += 2;
+            pc += 1024;
+            ps += 32 * gstep;
+            pz += 8 * gstep;
             slot_issue = slot_issue + 1 == CRING ? 0 : slot_issue + 1;
         };
 #pragma unroll 1
