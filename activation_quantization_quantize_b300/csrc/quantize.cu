@@ -388,8 +388,9 @@ __device__ __forceinline__ void codes_of_chunk(const uint4 raw, const ScopeParam
 // work), 128 for rows of up to 8192 values (a dozen CTAs share an SM, so many
 // rows are in flight and each row's reduction spans only four warps).
 // GL = 0: per-row scopes (a range pass, a CTA-wide maximum, a code pass);
-// GL > 0: groups of 8 GL values, one pass, the GL lanes of a group reducing
-// with shuffles (no CTA-wide step besides the buffer release).
+// GL > 0: groups of 8 GL values, one pass, a group's chunks spread over up
+// to GL / 4 lanes that reduce with shuffles (no CTA-wide step besides the
+// buffer release).
 template <typename T, bool SYM, bool STATIC, bool CODE4, int NT, int GL>
 __global__ void __launch_bounds__(NT) k_qrow_bulk(QuantArgs a, uint32_t buf_stride, int nbuf) {
     extern __shared__ __align__(128) uint8_t qb_smem[];
@@ -429,17 +430,23 @@ __global__ void __launch_bounds__(NT) k_qrow_bulk(QuantArgs a, uint32_t buf_stri
         if (!__syncthreads_and(ok)) break;
         const uint4* xs16 = reinterpret_cast<const uint4*>(qb_smem + (size_t)b * buf_stride);
         if constexpr (GL > 0) {
-            // per-group scopes: one pass; every lane of a warp takes part in
-            // the shuffles (groups are whole chunks, so a group's lanes are
-            // all live or all idle)
+            // per-group scopes, one pass: a group's GL chunks go to LPG lanes
+            // of CPL chunks each (chunk p + LPG j of the group for lane p), so
+            // the group's scale is computed once per CPL chunks and the LPG
+            // lanes reduce with shuffles; the lanes of a group read adjacent
+            // chunks (at most two-way bank conflicts)
+            constexpr int CPL = GL < 4 ? GL : 4;
+            constexpr int LPG = GL / CPL;
             const uint32_t ngr = (uint32_t)(a.cols / a.group);
-            const uint32_t span = (nchunks + 31u) & ~31u;
             uint8_t* qrow = reinterpret_cast<uint8_t*>(a.q) + r * qld;
-#pragma unroll 2
-            for (uint32_t c = tid; c < span; c += NT) {
-                const bool live = c < nchunks;
-                const uint4 raw = live ? xs16[c] : make_uint4(0, 0, 0, 0);
-                const int64_t sc = r * ngr + c / GL;
+            for (uint32_t g0 = 0; g0 < ngr; g0 += NT / LPG) {
+                const uint32_t gidx = g0 + (uint32_t)tid / LPG;
+                const bool live = gidx < ngr;  // a group's lanes are all live or all idle
+                const uint32_t c0 = gidx * GL + (uint32_t)tid % LPG;
+                uint4 raw[CPL];
+#pragma unroll
+                for (int j = 0; j < CPL; ++j) raw[j] = live ? xs16[c0 + LPG * j] : make_uint4(0, 0, 0, 0);
+                const int64_t sc = r * ngr + gidx;
                 float s;
                 int z;
                 if (STATIC) {
@@ -447,24 +454,29 @@ __global__ void __launch_bounds__(NT) k_qrow_bulk(QuantArgs a, uint32_t buf_stri
                     z = (a.z && live) ? a.z[sc] : 0;
                 } else {
                     PairRange<T> pr;
-                    pr.add(raw, SYM);
+#pragma unroll
+                    for (int j = 0; j < CPL; ++j) pr.add(raw[j], SYM);
                     float hi, lo;
                     pr.result(SYM, hi, lo);
 #pragma unroll
-                    for (int o = 1; o < GL; o <<= 1) {
+                    for (int o = 1; o < LPG; o <<= 1) {
                         hi = fmaxf(hi, __shfl_xor_sync(0xffffffffu, hi, o));
                         if (!SYM) lo = fminf(lo, __shfl_xor_sync(0xffffffffu, lo, o));
                     }
                     scale_zero(lo, hi, a.qmin, a.qmax, SYM, a.scale_f16, s, z);
-                    if (live && (tid & (GL - 1)) == 0) {
+                    if (live && tid % LPG == 0) {
                         store_scale(a.s, sc, a.scale_f16, s);
                         if (!SYM) a.z[sc] = z;
                     }
                 }
                 if (live) {
-                    uint32_t cb[8];
-                    codes_of_chunk<T, SYM, STATIC, false>(raw, make_scope(s, z), cr, cb);
-                    put_codes8<CODE4>(qrow, c, cb);
+                    const ScopeParams sp = make_scope(s, z);
+#pragma unroll
+                    for (int j = 0; j < CPL; ++j) {
+                        uint32_t cb[8];
+                        codes_of_chunk<T, SYM, STATIC, false>(raw[j], sp, cr, cb);
+                        put_codes8<CODE4>(qrow, c0 + LPG * j, cb);
+                    }
                 }
             }
             __syncthreads();  // buffer b is free
