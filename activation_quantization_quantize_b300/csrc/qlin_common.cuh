@@ -328,25 +328,58 @@ __device__ __forceinline__ void code_bits8(const float v[8], const ScopeParams& 
     }
 }
 
+// Constants of two adjacent per-column scopes as packed pairs: 1/s
+// (approximate), 1.5*2^23 + z, -s and -(hs*hs).
+struct ColPair {
+    float2 r, cz, ns, nhs2;
+};
+__device__ __forceinline__ ColPair make_colpair(const ScopeParams& p0, const ScopeParams& p1) {
+    ColPair c;
+    c.r = make_float2(p0.r, p1.r);
+    c.cz = make_float2(p0.cz, p1.cz);
+    c.ns = make_float2(-p0.s, -p1.s);
+    c.nhs2 = make_float2(-(p0.hs * p0.hs), -(p1.hs * p1.hs));
+    return c;
+}
+// The ScopeParams of one lane of a pair, rebuilt exactly as make_scope
+// builds them (s = -(-s); hs = s * (0.5 - 2^-11)).
+__device__ __forceinline__ ScopeParams colpair_scope(const ColPair& c, int lane) {
+    ScopeParams p;
+    p.s = -(lane ? c.ns.y : c.ns.x);
+    p.r = lane ? c.r.y : c.r.x;
+    p.hs = p.s * 0.49951171875f;
+    p.cz = lane ? c.cz.y : c.cz.x;
+    return p;
+}
+__device__ __forceinline__ float2 f2_sub(float2 a, float2 b) {
+    float2 d;
+    asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
+        "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+        "sub.rn.f32x2 rd, ra, rb;\n\t"
+        "mov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+    return d;
+}
+__device__ __noinline__ uint32_t code_bits_outline(float v, ScopeParams p, CodeRange cr) { return code_bits(v, p, cr); }
+
 // code_bits8 with one scope per element (per-column scopes): the same packed
-// fast path with per-lane constants; a chunk that fails takes the exact
-// per-element path.
+// fast path with per-lane constants (m - cz is the same operation as
+// m + (-cz)); a chunk that fails takes the exact per-element path out of line.
 template <bool kInRange, bool kClamp>
-__device__ __forceinline__ void code_bits8_cols(const float v[8], const ScopeParams sp[8], const CodeRange& cr,
+__device__ __forceinline__ void code_bits8_cols(const float v[8], const ColPair cp[4], const CodeRange& cr,
                                                 uint32_t cb[8]) {
     float m[8];
     uint32_t neg = 0xFFFFFFFFu;
     const float2 nlim2 = make_float2(-16777216.0f, -16777216.0f);
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-        const ScopeParams& p0 = sp[2 * j];
-        const ScopeParams& p1 = sp[2 * j + 1];
         const float2 v2 = make_float2(v[2 * j], v[2 * j + 1]);
-        const float2 t2 = f2_mul(v2, make_float2(p0.r, p1.r));
-        const float2 m2 = f2_add(t2, make_float2(p0.cz, p1.cz));
-        const float2 n2 = f2_add(m2, make_float2(-p0.cz, -p1.cz));
-        const float2 d2 = f2_fma(n2, make_float2(-p0.s, -p1.s), v2);
-        const float2 e2 = f2_fma(d2, d2, make_float2(-p0.hs * p0.hs, -p1.hs * p1.hs));
+        const float2 t2 = f2_mul(v2, cp[j].r);
+        const float2 m2 = f2_add(t2, cp[j].cz);
+        const float2 n2 = f2_sub(m2, cp[j].cz);
+        const float2 d2 = f2_fma(n2, cp[j].ns, v2);
+        const float2 e2 = f2_fma(d2, d2, cp[j].nhs2);
         neg &= __float_as_uint(e2.x) & __float_as_uint(e2.y);
         if (!kInRange) {
             const float2 g2 = f2_fma(t2, t2, nlim2);
@@ -360,7 +393,7 @@ __device__ __forceinline__ void code_bits8_cols(const float v[8], const ScopePar
         for (int j = 0; j < 8; ++j) cb[j] = __float_as_uint(kClamp ? fminf(fmaxf(m[j], cr.lo), cr.hi) : m[j]);
     } else {
 #pragma unroll
-        for (int j = 0; j < 8; ++j) cb[j] = code_bits(v[j], sp[j], cr);
+        for (int j = 0; j < 8; ++j) cb[j] = code_bits_outline(v[j], colpair_scope(cp[j / 2], j & 1), cr);
     }
 }
 

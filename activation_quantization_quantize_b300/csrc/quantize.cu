@@ -19,6 +19,7 @@
 //   k_dequant       x^ = fl(s (q - z)) rounded to the output type.
 #include <map>
 #include <mutex>
+#include <tuple>
 #include <type_traits>
 
 #include "qlin_common.cuh"
@@ -44,6 +45,10 @@ struct QuantArgs {
     void* s;
     int32_t* z;
     float* absmax_out;  // stats-only mode (qlin_absmax), else nullptr
+    // per-tensor / per-column range statistics (see k_stats_strip): when set,
+    // the codes kernels derive each scope's (s, z) from them and the scope's
+    // first reader writes s / z out; else s / z are read from s / z
+    const uint32_t* stat_in = nullptr;
 };
 
 __device__ __forceinline__ float load_scale(const void* s, int64_t i, int f16) {
@@ -54,6 +59,29 @@ __device__ __forceinline__ void store_scale(void* s, int64_t i, int f16, float v
         reinterpret_cast<__half*>(s)[i] = __float2half_rn(v);  // v is already a binary16 value
     else
         reinterpret_cast<float*>(s)[i] = v;
+}
+
+// (s, z) of scope i from the range statistics words, exactly as k_finalize
+// stores them.
+__device__ __forceinline__ ScopeOf scope_from_stat(const QuantArgs& a, const uint32_t* stat, int64_t i) {
+    return scope_of_range(-__uint_as_float(stat[2 * i + 1]), __uint_as_float(stat[2 * i]), a.qmin, a.qmax, a.sym,
+                          a.scale_f16);
+}
+// (s, z) of scope i: derived from a.stat_in (the writer stores them), else
+// read from s / z.
+__device__ __forceinline__ ScopeOf scope_in(const QuantArgs& a, int64_t i, bool writer) {
+    ScopeOf o;
+    if (a.stat_in) {
+        o = scope_from_stat(a, a.stat_in, i);
+        if (writer) {
+            store_scale(a.s, i, a.scale_f16, o.s);
+            if (a.z) a.z[i] = o.z;
+        }
+    } else {
+        o.s = load_scale(a.s, i, a.scale_f16);
+        o.z = a.z ? a.z[i] : 0;
+    }
+    return o;
 }
 
 // Optional smoothing of 8 elements of columns c0..c0+7: x / s_c (correctly
@@ -423,6 +451,14 @@ __global__ void __launch_bounds__(NT) k_qrow_bulk(QuantArgs a, uint32_t buf_stri
             if (blockIdx.x + (int64_t)b * gridDim.x < a.rows) issue(blockIdx.x + (int64_t)b * gridDim.x, b);
     }
     const int64_t qld = CODE4 ? a.cols / 2 : a.cols;
+    // per-tensor static scopes (GL = 0): one (s, z) for every row
+    float s_t = 0.0f;
+    int z_t = 0;
+    if (STATIC && GL == 0 && a.gran == QLIN_PER_TENSOR) {
+        const ScopeOf o = scope_in(a, 0, blockIdx.x == 0 && tid == 0);
+        s_t = o.s;
+        z_t = o.z;
+    }
     int b = 0;
     uint32_t ph = 0;
     for (int64_t r = blockIdx.x; r < a.rows; r += gridDim.x) {
@@ -490,8 +526,13 @@ __global__ void __launch_bounds__(NT) k_qrow_bulk(QuantArgs a, uint32_t buf_stri
         float s;
         int z;
         if (STATIC) {
-            s = load_scale(a.s, r, a.scale_f16);
-            z = a.z ? a.z[r] : 0;
+            if (a.gran == QLIN_PER_TENSOR) {
+                s = s_t;
+                z = z_t;
+            } else {
+                s = load_scale(a.s, r, a.scale_f16);
+                z = a.z ? a.z[r] : 0;
+            }
         } else {
             PairRange<T> pr;
 #pragma unroll 4
@@ -642,71 +683,185 @@ __global__ void __launch_bounds__(256) k_qgrp_slab(QuantArgs a) {
 }
 
 // ------------------------------------------------------------------ column-strip kernels
-// Thread layout shared by the per-tensor / per-column kernels: the block's
-// threads cover `cpb` chunk columns x `rpi` rows per iteration; the block
-// walks rows [r0, r1) of its row slab.
+// Tiling shared by the per-tensor / per-column kernels.  A block of NT
+// threads covers cpb = min(nchunks, 32) chunk columns (8 values each) x
+// rpi = NT / cpb adjacent rows per step, so a warp reads 32 adjacent chunks
+// of one row.  The grid holds gx blocks across the chunk columns and gy
+// blocks down the rows, sized by the host to the blocks that fit on the GPU
+// at once; block y takes row groups y, y + gy, y + 2 gy, ... of rpi rows, so
+// all blocks sweep the matrix together.
+constexpr int kStripThreads = 256;
+
 struct Strip {
-    int64_t chunk;   // chunk column of this thread (-1 when idle)
-    int64_t r_begin, r_end, r_step;
+    int64_t chunk;  // chunk column of this thread (-1 when idle)
+    int64_t r0;     // first row of this thread
+    int64_t step;   // rows between this thread's consecutive rows (gy * rpi)
+    int64_t nr;     // rows of this thread: r0 + i * step, i < nr
 };
 
-__device__ __forceinline__ Strip strip_of(int64_t nchunks, int64_t rows, int rows_per_block) {
-    Strip st;
-    const int nt = blockDim.x, t = threadIdx.x;
-    int64_t cpb = nchunks < nt ? nchunks : nt;        // chunk columns per block
-    int64_t rpi = nt / cpb;                           // rows per iteration
-    int64_t cl = t % cpb, rl = t / cpb;
-    st.chunk = (rl < rpi) ? (int64_t)blockIdx.x * cpb + cl : -1;
-    if (st.chunk >= nchunks) st.chunk = -1;
-    int64_t r0 = (int64_t)blockIdx.y * rows_per_block;
-    int64_t r1 = r0 + rows_per_block;
-    if (r1 > rows) r1 = rows;
-    st.r_begin = r0 + rl;
-    st.r_end = r1;
-    st.r_step = rpi;
-    return st;
+template <int NT = kStripThreads>
+__device__ __forceinline__ Strip strip_of(int64_t nchunks, int64_t rows) {
+    Strip s;
+    const int t = threadIdx.x;
+    const int cpb = nchunks < 32 ? (int)nchunks : 32;
+    const int rpi = NT / cpb;
+    const int rl = t / cpb;
+    const int64_t c = (int64_t)blockIdx.x * cpb + t % cpb;
+    s.chunk = (rl < rpi && c < nchunks) ? c : -1;
+    s.r0 = (int64_t)blockIdx.y * rpi + rl;
+    s.step = (int64_t)gridDim.y * rpi;
+    s.nr = s.r0 < rows ? (rows - 1 - s.r0) / s.step + 1 : 0;
+    return s;
 }
 
-// Range statistics into ws words (binary32 bit patterns of non-negative values,
-// atomicMax): stat[2*scope] = max(max x, 0) (or max|x|), stat[2*scope+1] =
-// -min(min x, 0).  The words start at 0 (memset by the host).
+// One chunk of eight input values as loaded (16 bytes of a 16-bit type, 32
+// of binary32), zero when the row is outside the slab.
 template <typename T>
-__global__ void __launch_bounds__(256) k_stats_strip(QuantArgs a, uint32_t* stat, int rows_per_block) {
+struct Raw8 {
+    uint4 w[sizeof(T) == 4 ? 2 : 1];
+};
+template <typename T>
+__device__ __forceinline__ Raw8<T> raw8_load(const T* p, bool live) {
+    Raw8<T> c;
+#pragma unroll
+    for (int i = 0; i < (int)(sizeof(c.w) / sizeof(uint4)); ++i)
+        c.w[i] = live ? __ldg(reinterpret_cast<const uint4*>(p) + i) : make_uint4(0u, 0u, 0u, 0u);
+    return c;
+}
+
+template <typename T>
+__device__ __forceinline__ void raw8_widen(const Raw8<T>& c, float v[8]) {
+    if constexpr (sizeof(T) == 4) {
+        const uint32_t w[8] = {c.w[0].x, c.w[0].y, c.w[0].z, c.w[0].w, c.w[1].x, c.w[1].y, c.w[1].z, c.w[1].w};
+#pragma unroll
+        for (int j = 0; j < 8; ++j) v[j] = __uint_as_float(w[j]);
+    } else {
+        unpack8<T>(c.w[0], v);
+    }
+}
+
+// Packed pair type of a 16-bit input type.
+template <typename T>
+struct Pair16;
+template <>
+struct Pair16<__nv_bfloat16> {
+    using P = __nv_bfloat162;
+};
+template <>
+struct Pair16<__half> {
+    using P = __half2;
+};
+
+// Range statistics into ws words (binary32 bit patterns of non-negative values,
+// atomicMax): stat[2*scope] = max(max x, 0) (or max|x| when SYM),
+// stat[2*scope+1] = -min(min x, 0).  The words start at 0 (memset by the
+// host).  PACKED (unsmoothed 16-bit input) keeps the running maxima as packed
+// pairs in the input's own format: max and min are exact in any format, and
+// both ignore NaN like fmaxf / fminf.  A zero chunk leaves every statistic
+// unchanged, so rows past the slab load as zeros.  Per-column statistics are
+// reduced over the block's row lanes in shared memory before one atomic per
+// column and statistic.
+template <typename T, bool SYM, bool PER_COL, bool PACKED>
+__global__ void __launch_bounds__(kStripThreads) k_stats_strip(QuantArgs a, uint32_t* stat) {
+    constexpr int U = 8;  // loads in flight per thread
     const int64_t nchunks = a.cols / 8;
-    const T* __restrict__ x = reinterpret_cast<const T*>(a.x);
-    Strip st = strip_of(nchunks, a.rows, rows_per_block);
+    const Strip st = strip_of(nchunks, a.rows);
     float hi[8], lo[8];
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
         hi[j] = 0.0f;
         lo[j] = 0.0f;
     }
-    if (st.chunk >= 0) {
-#pragma unroll 4
-        for (int64_t r = st.r_begin; r < st.r_end; r += st.r_step) {
-            float v[8];
-            load8<T>(x + r * a.ld + st.chunk * 8, v);
-            smooth8(v, a.smooth_mode, a.smooth, st.chunk * 8);
+    if (st.chunk >= 0 && st.nr > 0) {
+        const int64_t rstep = st.step * a.ld;  // elements between this thread's rows
+        const T* p = reinterpret_cast<const T*>(a.x) + st.r0 * a.ld + st.chunk * 8;
+        int64_t left = st.nr;
+        if constexpr (PACKED) {
+            using P = typename Pair16<T>::P;
+            const uint32_t zbits = 0u;
+            const P zero = *reinterpret_cast<const P*>(&zbits);
+            P h[4], l[4];
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                float u = v[j];
-                if (a.sym) {
-                    hi[j] = fmaxf(hi[j], fabsf(u));
-                } else {
-                    hi[j] = fmaxf(hi[j], u);
-                    lo[j] = fminf(lo[j], u);
+            for (int i = 0; i < 4; ++i) {
+                h[i] = zero;
+                l[i] = zero;
+            }
+            for (; left > 0; left -= U, p += U * rstep) {
+                Raw8<T> c[U];
+#pragma unroll
+                for (int k = 0; k < U; ++k) c[k] = raw8_load<T>(p + k * rstep, k < left);
+#pragma unroll
+                for (int k = 0; k < U; ++k) {
+                    const uint32_t w[4] = {c[k].w[0].x, c[k].w[0].y, c[k].w[0].z, c[k].w[0].w};
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const P v = *reinterpret_cast<const P*>(&w[i]);
+                        if (SYM) {
+                            h[i] = __hmax2(h[i], __habs2(v));
+                        } else {
+                            h[i] = __hmax2(h[i], v);
+                            l[i] = __hmin2(l[i], v);
+                        }
+                    }
+                }
+            }
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                hi[2 * i] = __low2float(h[i]);
+                hi[2 * i + 1] = __high2float(h[i]);
+                lo[2 * i] = __low2float(l[i]);
+                lo[2 * i + 1] = __high2float(l[i]);
+            }
+        } else {
+            constexpr int UF = sizeof(T) == 4 ? 2 : 4;
+            for (; left > 0; left -= UF, p += UF * rstep) {
+                Raw8<T> c[UF];
+#pragma unroll
+                for (int k = 0; k < UF; ++k) c[k] = raw8_load<T>(p + k * rstep, k < left);
+#pragma unroll
+                for (int k = 0; k < UF; ++k) {
+                    float v[8];
+                    raw8_widen<T>(c[k], v);
+                    smooth8(v, a.smooth_mode, a.smooth, st.chunk * 8);
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        if (SYM) {
+                            hi[j] = fmaxf(hi[j], fabsf(v[j]));
+                        } else {
+                            hi[j] = fmaxf(hi[j], v[j]);
+                            lo[j] = fminf(lo[j], v[j]);
+                        }
+                    }
                 }
             }
         }
     }
-    if (a.gran == QLIN_PER_COL) {
+    if constexpr (PER_COL) {
+        __shared__ __align__(16) float sh_hi[kStripThreads * 8];
+        __shared__ __align__(16) float sh_lo[SYM ? 4 : kStripThreads * 8];
+        const int cpb = nchunks < 32 ? (int)nchunks : 32;
+        const int rpi = kStripThreads / cpb;
+        const int ncol = cpb * 8;
         if (st.chunk >= 0) {
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                int64_t c = st.chunk * 8 + j;
-                if (hi[j] > 0.0f) atomicMax(&stat[2 * c], __float_as_uint(hi[j]));
-                if (lo[j] < 0.0f) atomicMax(&stat[2 * c + 1], __float_as_uint(-lo[j]));
+            const int base = ((int)threadIdx.x / cpb) * ncol + (threadIdx.x % cpb) * 8;
+            reinterpret_cast<float4*>(sh_hi + base)[0] = make_float4(hi[0], hi[1], hi[2], hi[3]);
+            reinterpret_cast<float4*>(sh_hi + base)[1] = make_float4(hi[4], hi[5], hi[6], hi[7]);
+            if (!SYM) {
+                reinterpret_cast<float4*>(sh_lo + base)[0] = make_float4(lo[0], lo[1], lo[2], lo[3]);
+                reinterpret_cast<float4*>(sh_lo + base)[1] = make_float4(lo[4], lo[5], lo[6], lo[7]);
             }
+        }
+        __syncthreads();
+        const int t = threadIdx.x;
+        const int64_t c = (int64_t)blockIdx.x * ncol + t;
+        if (t < ncol && c < a.cols) {
+            float h = 0.0f, l = 0.0f;
+            for (int k = 0; k < rpi; ++k) {
+                h = fmaxf(h, sh_hi[k * ncol + t]);
+                if (!SYM) l = fminf(l, sh_lo[k * ncol + t]);
+            }
+            if (h > 0.0f) atomicMax(&stat[2 * c], __float_as_uint(h));
+            if (l < 0.0f) atomicMax(&stat[2 * c + 1], __float_as_uint(-l));
         }
     } else {
         float h = 0.0f, l = 0.0f;
@@ -716,7 +871,7 @@ __global__ void __launch_bounds__(256) k_stats_strip(QuantArgs a, uint32_t* stat
             l = fminf(l, lo[j]);
         }
         h = warp_max(h);
-        l = warp_min(l);
+        if (!SYM) l = warp_min(l);
         if ((threadIdx.x & 31) == 0) {
             if (h > 0.0f) atomicMax(&stat[0], __float_as_uint(h));
             if (l < 0.0f) atomicMax(&stat[1], __float_as_uint(-l));
@@ -741,38 +896,92 @@ __global__ void k_finalize(QuantArgs a, const uint32_t* stat, int64_t nscopes) {
     if (a.z) a.z[i] = z;
 }
 
-// Codes for per-tensor / per-column scopes from the stored (s, z).  MODE 0:
-// dynamic symmetric (no clamp; |rne(x/s)| <= qmax since s came from the same
-// data), 1: dynamic asymmetric (clamp), 2: static scales (clamp and
-// far-range test).  The eight codes of a chunk are decided together on
-// packed pairs; per-column scopes give each element its own constants.
-template <typename T, int MODE, bool PER_COL>
-__global__ void __launch_bounds__(256) k_quant_strip(QuantArgs a, int rows_per_block) {
+// Codes for per-tensor / per-column scopes.  MODE 0: dynamic symmetric (no
+// clamp; |rne(x/s)| <= qmax since s came from the same data), 1: dynamic
+// asymmetric (clamp), 2: static scales (clamp and far-range test).  The
+// eight codes of a chunk are decided together on packed pairs; per-column
+// scopes give each element its own constants.  Each thread stages its
+// chunks through a ring of S slots of its own in shared memory by
+// asynchronous copies (S - 1 rows in flight per thread, no registers held
+// for them, no barrier: a thread reads only what it copied); the row loop is
+// unrolled by S so that every slot offset is a constant.  SMOOTHED instances
+// apply the smoothing factors (their divisions take registers).
+template <typename T, int MODE, bool PER_COL, bool SMOOTHED>
+__global__ void __launch_bounds__(kStripThreads, SMOOTHED ? 2 : (PER_COL ? 3 : 4))
+    k_quant_strip(QuantArgs a) {
+    constexpr int W = sizeof(T) == 4 ? 2 : 1;  // 16-byte words per chunk
+    constexpr int S = sizeof(T) == 4 ? 4 : 8;  // ring slots per thread
+    constexpr uint32_t kSlotBytes = W * kStripThreads * 16;
+    __shared__ __align__(16) uint4 ring[S * W * kStripThreads];
     const int64_t nchunks = a.cols / 8;
-    const T* __restrict__ x = reinterpret_cast<const T*>(a.x);
-    Strip st = strip_of(nchunks, a.rows, rows_per_block);
-    if (st.chunk < 0) return;
-    const CodeRange cr = make_range(a.qmin, a.qmax);
-    ScopeParams sp[8];
+    const Strip st = strip_of(nchunks, a.rows);
+    if (st.chunk < 0 || st.nr == 0) return;
+    const int nr = (int)st.nr;
+    const int64_t rstep = st.step * a.ld;
+    // codes: 8 bytes (or 4 of nibbles) per chunk, rows of cols (cols/2) bytes
+    const int64_t qrow = a.code4 ? a.cols / 2 : a.cols;
+    const int64_t qstep = st.step * qrow;
+    uint8_t* qp = reinterpret_cast<uint8_t*>(a.q) + st.r0 * qrow + st.chunk * (a.code4 ? 4 : 8);
+    const T* src = reinterpret_cast<const T*>(a.x) + st.r0 * a.ld + st.chunk * 8;  // next row to copy
+    const uint32_t slot0 = (uint32_t)__cvta_generic_to_shared(&ring[threadIdx.x]);
+    auto copy_row = [&](int slot, bool live) {
+        if (live) {
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-        const int64_t sc = PER_COL ? st.chunk * 8 + j : 0;
-        const float s = load_scale(a.s, sc, a.scale_f16);
-        const int z = a.z ? a.z[sc] : 0;
-        sp[j] = make_scope(s, z);
+            for (int w = 0; w < W; ++w)
+                cp_async16(slot0 + (uint32_t)slot * kSlotBytes + (uint32_t)w * kStripThreads * 16,
+                           reinterpret_cast<const uint4*>(src) + w);
+        }
+        src += rstep;
+        cp_async_commit();
+    };
+#pragma unroll
+    for (int u = 0; u < S - 1; ++u) copy_row(u, u < nr);
+    // (the first copies are in flight while the scopes are set up)
+    const CodeRange cr = make_range(a.qmin, a.qmax);
+    // the first row group's threads write the scopes they derive
+    const bool writer = st.r0 == 0;
+    ScopeParams sp;
+    ColPair cp[4];
+    if constexpr (PER_COL) {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int64_t c0 = st.chunk * 8 + 2 * j;
+            const ScopeOf o0 = scope_in(a, c0, writer), o1 = scope_in(a, c0 + 1, writer);
+            cp[j] = make_colpair(make_scope(o0.s, o0.z), make_scope(o1.s, o1.z));
+        }
+    } else {
+        const ScopeOf o = scope_in(a, 0, writer && st.chunk == 0);
+        sp = make_scope(o.s, o.z);
     }
-#pragma unroll 4
-    for (int64_t r = st.r_begin; r < st.r_end; r += st.r_step) {
-        float v[8];
-        load8<T>(x + r * a.ld + st.chunk * 8, v);
-        smooth8(v, a.smooth_mode, a.smooth, st.chunk * 8);
-        uint32_t cb[8];
-        if (PER_COL)
-            code_bits8_cols<MODE != 2, MODE != 0>(v, sp, cr, cb);
-        else
-            code_bits8<MODE != 2, MODE != 0>(v, sp[0], cr, cb);
-        store_codes8(a.q, r, a.cols, st.chunk, a.code4, cb);
+    for (int j0 = 0; j0 < nr; j0 += S) {
+#pragma unroll
+        for (int u = 0; u < S; ++u) {
+            if (j0 + u >= nr) break;
+            copy_row((u + S - 1) % S, j0 + u + S - 1 < nr);
+            cp_async_wait<S - 1>();
+            Raw8<T> c;
+#pragma unroll
+            for (int w = 0; w < W; ++w) c.w[w] = ring[(u * W + w) * kStripThreads + threadIdx.x];
+            float v[8];
+            raw8_widen<T>(c, v);
+            if constexpr (SMOOTHED) smooth8(v, a.smooth_mode, a.smooth, st.chunk * 8);
+            uint32_t cb[8];
+            if constexpr (PER_COL)
+                code_bits8_cols<MODE != 2, MODE != 0>(v, cp, cr, cb);
+            else
+                code_bits8<MODE != 2, MODE != 0, true>(v, sp, cr, cb);
+            if (a.code4) {
+                *reinterpret_cast<uint32_t*>(qp) = pack_nibbles8(cb);
+            } else {
+                uint2 w;
+                w.x = pack_bytes4(cb[0], cb[1], cb[2], cb[3]);
+                w.y = pack_bytes4(cb[4], cb[5], cb[6], cb[7]);
+                *reinterpret_cast<uint2*>(qp) = w;
+            }
+            qp += qstep;
+        }
     }
+    cp_async_wait<0>();
 }
 
 // ------------------------------------------------------------------ generic (scalar) path
@@ -891,23 +1100,50 @@ __global__ void k_quant_generic(QuantArgs a) {
 // ws words: hist1[32768] | hist2[65536] | sel[4].
 constexpr int kHist1 = 32768, kHist2 = 65536;
 
+constexpr int kHistThreads = 1024;
+
+// Level-1 histogram in shared memory, merged into hist1.  Aligned rows of
+// whole chunks (strip != 0) take the column-strip tiling with several
+// loads in flight per thread; the bin of unsmoothed bf16 input is its own bit
+// pattern without the sign (the top half of the binary32 pattern of |x|).
+// Other rows (strip = 0) take a scalar grid-stride walk.
 template <typename T>
-__global__ void __launch_bounds__(1024) k_hist1(QuantArgs a, uint32_t* hist1, int vec) {
+__global__ void __launch_bounds__(kHistThreads) k_hist1(QuantArgs a, uint32_t* hist1, int strip) {
     extern __shared__ uint32_t sh[];
     for (int i = threadIdx.x; i < kHist1; i += blockDim.x) sh[i] = 0;
     __syncthreads();
-    if (vec) {  // rows of whole 16-byte-aligned 8-value chunks
+    if (strip) {
+        constexpr int U = 4;  // loads in flight per thread
         const int64_t nchunks = a.cols / 8;
-        const T* __restrict__ x = reinterpret_cast<const T*>(a.x);
-        for (int64_t r = blockIdx.x; r < a.rows; r += gridDim.x)
-#pragma unroll 2
-            for (int64_t c = threadIdx.x; c < nchunks; c += blockDim.x) {
-                float v[8];
-                load8<T>(x + r * a.ld + c * 8, v);
-                smooth8(v, a.smooth_mode, a.smooth, c * 8);
+        const Strip sp = strip_of<kHistThreads>(nchunks, a.rows);
+        const bool bits = std::is_same<T, __nv_bfloat16>::value && a.smooth_mode == QLIN_SMOOTH_NONE;
+        if (sp.chunk >= 0) {
+            const int64_t rstep = sp.step * a.ld;
+            const T* p = reinterpret_cast<const T*>(a.x) + sp.r0 * a.ld + sp.chunk * 8;
+            for (int64_t left = sp.nr; left > 0; left -= U, p += U * rstep) {
+                Raw8<T> c[U];
 #pragma unroll
-                for (int j = 0; j < 8; ++j) atomicAdd(&sh[__float_as_uint(fabsf(v[j])) >> 16], 1u);
+                for (int k = 0; k < U; ++k) c[k] = raw8_load<T>(p + k * rstep, k < left);
+#pragma unroll
+                for (int k = 0; k < U; ++k) {
+                    if (k >= left) break;
+                    if (bits) {
+                        const uint32_t w[4] = {c[k].w[0].x, c[k].w[0].y, c[k].w[0].z, c[k].w[0].w};
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            atomicAdd(&sh[w[i] & 0x7FFFu], 1u);
+                            atomicAdd(&sh[(w[i] >> 16) & 0x7FFFu], 1u);
+                        }
+                    } else {
+                        float v[8];
+                        raw8_widen<T>(c[k], v);
+                        smooth8(v, a.smooth_mode, a.smooth, sp.chunk * 8);
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) atomicAdd(&sh[__float_as_uint(fabsf(v[j])) >> 16], 1u);
+                    }
+                }
             }
+        }
     } else {
         for (int64_t r = blockIdx.x; r < a.rows; r += gridDim.x)
             for (int64_t c = threadIdx.x; c < a.cols; c += blockDim.x) {
@@ -930,36 +1166,86 @@ __global__ void k_hist2(QuantArgs a, const uint32_t* sel, uint32_t* hist2) {
         }
 }
 
-// Single CTA of 1024 threads: find the bin holding rank k (1-based) of `hist`
-// (nbins = 1024 * per), write {bin, rank inside bin}.
-__device__ void select_rank(const uint32_t* hist, int per, uint64_t k, uint32_t* out_bin, uint64_t* out_rank) {
-    __shared__ unsigned long long part[1024];
-    const int t = threadIdx.x;
+// Single CTA of 1024 threads: the bin holding rank k (1-based) of `hist`
+// (1024 * PER bins, PER a multiple of 32; total count below 2^32) -- the
+// first bin whose inclusive prefix count reaches k -- and the rank inside
+// it, written to {*out_bin, *out_rank}.  Warp w owns the PER rows of 32 bins
+// from bin w * 32 * PER on and reads them coalesced, keeping each row's sum
+// (lane l holds rows l, l + 32, ...).  A scan of the warp totals picks the
+// warp holding rank k; a scan of its row sums picks the row; a scan of the
+// row picks the bin.  (Were k above the total, the last bin would be
+// returned.)
+template <int PER>
+__device__ void select_rank(const uint32_t* hist, uint64_t k, uint32_t* out_bin, uint64_t* out_rank) {
+    __shared__ unsigned long long wtot[32];
+    constexpr int NP = PER / 32;
+    const unsigned full = 0xFFFFFFFFu;
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+    const uint32_t* seg = hist + (size_t)wid * 32 * PER;
+    uint32_t rsum[NP];
+#pragma unroll
+    for (int j = 0; j < PER; ++j) {
+        const uint32_t r = __reduce_add_sync(full, seg[j * 32 + lane]);
+        if ((j & 31) == lane) rsum[j >> 5] = r;
+    }
     unsigned long long sum = 0;
-    for (int j = 0; j < per; ++j) sum += hist[t * per + j];
-    part[t] = sum;
+#pragma unroll
+    for (int i = 0; i < NP; ++i) sum += rsum[i];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(full, sum, o);
+    if (lane == 0) wtot[wid] = sum;
     __syncthreads();
-    if (t == 0) {
-        unsigned long long acc = 0;
-        int tsel = 1023;
-        for (int i = 0; i < 1024; ++i) {
-            if (acc + part[i] >= k) {
-                tsel = i;
-                break;
-            }
-            acc += part[i];
+    if (wid == 0) {
+        unsigned long long v = wtot[lane];
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const unsigned long long u = __shfl_up_sync(full, v, o);
+            if (lane >= o) v += u;
         }
-        uint32_t bin = (uint32_t)(tsel * per + per - 1);
-        for (int j = 0; j < per; ++j) {
-            uint32_t h = hist[tsel * per + j];
-            if (acc + h >= k) {
-                bin = (uint32_t)(tsel * per + j);
-                break;
+        wtot[lane] = v;  // inclusive totals of warps 0..lane
+    }
+    __syncthreads();
+    const unsigned long long incl = wtot[wid];
+    const unsigned long long excl = wid > 0 ? wtot[wid - 1] : 0ull;
+    if ((incl >= k && (wid == 0 || excl < k)) || (wid == 31 && incl < k)) {
+        // exclusive scan: the lowest lane whose inclusive prefix reaches k
+        auto first_reaching = [&](unsigned long long v, unsigned long long base, int& at,
+                                  unsigned long long& before) -> bool {
+            unsigned long long x = v;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const unsigned long long y = __shfl_up_sync(full, x, o);
+                if (lane >= o) x += y;
             }
-            acc += h;
+            const unsigned hit = __ballot_sync(full, base + x >= k);
+            if (hit) {
+                at = __ffs(hit) - 1;
+                before = __shfl_sync(full, x - v, at);
+                return true;
+            }
+            before = __shfl_sync(full, x, 31);
+            return false;
+        };
+        unsigned long long acc = excl, before = 0;
+        int row = -1, at = 0;
+#pragma unroll
+        for (int i = 0; i < NP; ++i) {
+            if (row < 0) {
+                if (first_reaching(rsum[i], acc, at, before)) row = i * 32 + at;
+                acc += before;
+            }
         }
-        *out_bin = bin;
-        *out_rank = k - acc;
+        uint32_t bin = (uint32_t)(wid * 32 * PER + 32 * PER - 1);
+        if (row >= 0) {
+            const uint32_t h = seg[row * 32 + lane];
+            first_reaching(h, acc, at, before);
+            bin = (uint32_t)(wid * 32 * PER + row * 32 + at);
+            acc += before;
+        }
+        if (lane == 0) {
+            *out_bin = bin;
+            *out_rank = k - acc;
+        }
     }
     __syncthreads();
 }
@@ -969,7 +1255,7 @@ __device__ void select_rank(const uint32_t* hist, int per, uint64_t k, uint32_t*
 __global__ void __launch_bounds__(1024) k_select1(QuantArgs a, const uint32_t* hist1, uint32_t* sel, uint64_t k, int final_) {
     __shared__ uint32_t bin;
     __shared__ uint64_t rk;
-    select_rank(hist1, kHist1 / 1024, k, &bin, &rk);
+    select_rank<kHist1 / 1024>(hist1, k, &bin, &rk);
     if (threadIdx.x == 0) {
         sel[0] = bin;
         sel[1] = (uint32_t)rk;
@@ -987,7 +1273,7 @@ __global__ void __launch_bounds__(1024) k_select1(QuantArgs a, const uint32_t* h
 __global__ void __launch_bounds__(1024) k_select2(QuantArgs a, const uint32_t* hist2, const uint32_t* sel) {
     __shared__ uint32_t bin;
     __shared__ uint64_t rk;
-    select_rank(hist2, kHist2 / 1024, sel[1], &bin, &rk);
+    select_rank<kHist2 / 1024>(hist2, sel[1], &bin, &rk);
     if (threadIdx.x == 0) {
         float T_ = __uint_as_float((sel[0] << 16) | bin);
         float s;
@@ -1393,16 +1679,70 @@ static cudaError_t launch_rows(const QuantArgs& a, cudaStream_t st) {
     return cudaGetLastError();
 }
 
-static void strip_grid(int64_t nchunks, int64_t rows, dim3& grid, int& rows_per_block) {
-    int64_t cpb = nchunks < 256 ? nchunks : 256;
-    int64_t gx = ceil_div(nchunks, cpb);
-    int64_t target = (int64_t)num_sms() * 8;  // blocks in flight
-    int64_t gy = ceil_div(target, gx);
-    if (gy > rows) gy = rows;
+// Grid of the column-strip kernels (nt threads a block): gx blocks across
+// the chunk columns and as many down the rows as fill the GPU once at
+// `per_sm` resident blocks per SM (no more than there are row groups).
+static dim3 strip_grid(int64_t nchunks, int64_t rows, int nt, int per_sm) {
+    const int64_t cpb = nchunks < 32 ? nchunks : 32;
+    const int64_t rpi = nt / cpb;
+    const int64_t gx = ceil_div(nchunks, cpb);
+    const int64_t target = (int64_t)num_sms() * (per_sm > 0 ? per_sm : 1);
+    int64_t gy = target / gx;
+    if (gy > ceil_div(rows, rpi)) gy = ceil_div(rows, rpi);
+    if (gy > 65535) gy = 65535;
     if (gy < 1) gy = 1;
-    rows_per_block = (int)ceil_div(rows, gy);
-    gy = ceil_div(rows, rows_per_block);
-    grid = dim3((unsigned)gx, (unsigned)gy);
+    return dim3((unsigned)gx, (unsigned)gy);
+}
+
+template <typename T>
+using QuantStripFn = void (*)(QuantArgs);
+template <typename T, bool SM>
+static QuantStripFn<T> quant_strip_fn_s(int mode, bool pc) {
+    switch (mode * 2 + (pc ? 1 : 0)) {
+    case 0: return k_quant_strip<T, 0, false, SM>;
+    case 1: return k_quant_strip<T, 0, true, SM>;
+    case 2: return k_quant_strip<T, 1, false, SM>;
+    case 3: return k_quant_strip<T, 1, true, SM>;
+    case 4: return k_quant_strip<T, 2, false, SM>;
+    default: return k_quant_strip<T, 2, true, SM>;
+    }
+}
+template <typename T>
+static QuantStripFn<T> quant_strip_fn(int mode, bool pc, bool smoothed) {
+    return smoothed ? quant_strip_fn_s<T, true>(mode, pc) : quant_strip_fn_s<T, false>(mode, pc);
+}
+template <typename T, bool PACKED>
+static void (*stats_strip_fn_p(bool sym, bool pc))(QuantArgs, uint32_t*) {
+    if (sym) return pc ? k_stats_strip<T, true, true, PACKED> : k_stats_strip<T, true, false, PACKED>;
+    return pc ? k_stats_strip<T, false, true, PACKED> : k_stats_strip<T, false, false, PACKED>;
+}
+// PACKED statistics for unsmoothed 16-bit input.
+template <typename T>
+static void (*stats_strip_fn(bool sym, bool pc, bool smoothed))(QuantArgs, uint32_t*) {
+    if constexpr (sizeof(T) == 2) {
+        if (!smoothed) return stats_strip_fn_p<T, true>(sym, pc);
+    }
+    return stats_strip_fn_p<T, false>(sym, pc);
+}
+
+// Resident blocks per SM of a kernel launch shape (queried once per kernel,
+// shape and device).
+static int blocks_per_sm(const void* kern, int nt, size_t smem) {
+    static std::mutex mu;
+    static std::map<std::tuple<const void*, int, size_t, int>, int> known;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    const auto key = std::make_tuple(kern, nt, smem, dev);
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        auto it = known.find(key);
+        if (it != known.end()) return it->second;
+    }
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, nt, smem) != cudaSuccess || n < 1) n = 1;
+    std::lock_guard<std::mutex> lock(mu);
+    known[key] = n;
+    return n;
 }
 
 // QLIN_QROW: "warp" keeps the register-resident row kernels (per-row rows of
@@ -1486,7 +1826,23 @@ static cudaError_t run_quantize_t(QuantArgs a, int xt, const qlin_qparams* p, vo
         return cudaGetLastError();
     }
 
-    // Per-tensor / per-column: stats (dynamic) -> finalize -> codes.
+    // Per-tensor / per-column: statistics (dynamic) -> codes.  The codes
+    // kernels derive the scopes' (s, z) from the statistics themselves (and
+    // write them out); the scalar fallback and qlin_absmax take k_finalize.
+    const bool strip = strip_ok(a, xt);
+    const bool pc = a.gran == QLIN_PER_COL;
+    const bool smoothed = a.smooth_mode != QLIN_SMOOTH_NONE;
+    // percentile scales clip values beyond the percentile, and binary16
+    // scales can saturate: both take the fully checked codes
+    const int mode = (a.static_scale || p->clip_percentile > 0.0 || a.scale_f16) ? 2 : (a.sym ? 0 : 1);
+    // per-tensor codes of unsmoothed 16-bit rows: the row-streaming kernel
+    // with one scope for all rows
+    uint32_t buf_stride = 0;
+    bool rowcodes = false;
+    if constexpr (!std::is_same<T, float>::value) {
+        buf_stride = (uint32_t)(((size_t)a.cols * 2 + 127) & ~(size_t)127);
+        rowcodes = !pc && !smoothed && strip && a.cols / 8 <= 8 * 512 && 2 * (size_t)buf_stride <= 200 * 1024;
+    }
     if (!a.static_scale) {
         uint32_t* stat = reinterpret_cast<uint32_t*>(ws);
         if (p->clip_percentile > 0.0) {
@@ -1496,7 +1852,13 @@ static cudaError_t run_quantize_t(QuantArgs a, int xt, const qlin_qparams* p, vo
             uint64_t k = (uint64_t)percentile_rank(n, p->clip_percentile);
             if ((e = cudaMemsetAsync(ws, 0, (size_t)(kHist1 + kHist2 + 4) * 4, st)) != cudaSuccess) return e;
             if ((e = ensure_smem((const void*)k_hist1<T>, kHist1 * 4)) != cudaSuccess) return e;
-            k_hist1<T><<<num_sms(), 1024, kHist1 * 4, st>>>(a, hist1, strip_ok(a, xt) ? 1 : 0);
+            if (strip) {
+                const dim3 hgrid = strip_grid(a.cols / 8, a.rows, kHistThreads,
+                                              blocks_per_sm((const void*)k_hist1<T>, kHistThreads, kHist1 * 4));
+                k_hist1<T><<<hgrid, kHistThreads, kHist1 * 4, st>>>(a, hist1, 1);
+            } else {
+                k_hist1<T><<<num_sms(), kHistThreads, kHist1 * 4, st>>>(a, hist1, 0);
+            }
             // Low 16 bits of |x| are zero for unsmoothed bf16 input.
             bool need2 = !(xt == QLIN_BF16 && a.smooth_mode == QLIN_SMOOTH_NONE);
             k_select1<<<1, 1024, 0, st>>>(a, hist1, sel, k, need2 ? 0 : 1);
@@ -1507,35 +1869,31 @@ static cudaError_t run_quantize_t(QuantArgs a, int xt, const qlin_qparams* p, vo
         } else {
             int64_t ns = nscopes_of(a);
             if ((e = cudaMemsetAsync(ws, 0, (size_t)ns * 8, st)) != cudaSuccess) return e;
-            if (strip_ok(a, xt)) {
-                dim3 grid;
-                int rpb;
-                strip_grid(a.cols / 8, a.rows, grid, rpb);
-                k_stats_strip<T><<<grid, 256, 0, st>>>(a, stat, rpb);
+            if (strip) {
+                auto ks = stats_strip_fn<T>(a.sym, pc, smoothed);
+                ks<<<strip_grid(a.cols / 8, a.rows, kStripThreads, blocks_per_sm((const void*)ks, kStripThreads, 0)),
+                     kStripThreads, 0, st>>>(a, stat);
             } else {
                 k_stats_generic<T><<<gblocks, 256, 0, st>>>(a, stat);
             }
-            k_finalize<<<(unsigned)ceil_div(ns, 256), 256, 0, st>>>(a, stat, ns);
+            if (a.absmax_out || !strip)
+                k_finalize<<<(unsigned)ceil_div(ns, 256), 256, 0, st>>>(a, stat, ns);
+            else
+                a.stat_in = stat;
         }
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
     if (a.absmax_out) return cudaGetLastError();
-    if (strip_ok(a, xt)) {
-        dim3 grid;
-        int rpb;
-        strip_grid(a.cols / 8, a.rows, grid, rpb);
-        // percentile scales clip values beyond the percentile, and binary16
-        // scales can saturate: both take the fully checked codes
-        const int mode = (a.static_scale || p->clip_percentile > 0.0 || a.scale_f16) ? 2 : (a.sym ? 0 : 1);
-        const bool pc = a.gran == QLIN_PER_COL;
-        switch (mode * 2 + (pc ? 1 : 0)) {
-        case 0: k_quant_strip<T, 0, false><<<grid, 256, 0, st>>>(a, rpb); break;
-        case 1: k_quant_strip<T, 0, true><<<grid, 256, 0, st>>>(a, rpb); break;
-        case 2: k_quant_strip<T, 1, false><<<grid, 256, 0, st>>>(a, rpb); break;
-        case 3: k_quant_strip<T, 1, true><<<grid, 256, 0, st>>>(a, rpb); break;
-        case 4: k_quant_strip<T, 2, false><<<grid, 256, 0, st>>>(a, rpb); break;
-        default: k_quant_strip<T, 2, true><<<grid, 256, 0, st>>>(a, rpb); break;
+    if (rowcodes) {
+        if constexpr (!std::is_same<T, float>::value) {
+            return a.code4 ? launch_qrow_bulk_g<T, true, true, true, 0>(a, buf_stride, st)
+                           : launch_qrow_bulk_g<T, true, true, false, 0>(a, buf_stride, st);
         }
+    }
+    if (strip) {
+        const QuantStripFn<T> kq = quant_strip_fn<T>(mode, pc, smoothed);
+        kq<<<strip_grid(a.cols / 8, a.rows, kStripThreads, blocks_per_sm((const void*)kq, kStripThreads, 0)),
+             kStripThreads, 0, st>>>(a);
     } else {
         k_quant_generic<T><<<gblocks, 256, 0, st>>>(a);
     }
