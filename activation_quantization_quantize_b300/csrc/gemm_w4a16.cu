@@ -241,6 +241,7 @@ template <int MT, int NT>  // MT: n8 token tiles (1: M <= 8, 2: M <= 16); NT: 16
 __global__ void __launch_bounds__(256, 2) k_w4_gemv(const __nv_bfloat16* __restrict__ x, const uint8_t* __restrict__ blob,
                                                     qlin_w4_header h, int64_t M, __nv_bfloat16* __restrict__ y) {
     extern __shared__ __align__(16) uint8_t gv_smem[];
+    tc::pdl_launch_dependents();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int gq = lane >> 2, t = lane & 3;
     const int64_t K = h.K, nchunk = K / 64, ngr = K / h.group;
@@ -296,6 +297,10 @@ __global__ void __launch_bounds__(256, 2) k_w4_gemv(const __nv_bfloat16* __restr
 
 #pragma unroll
     for (int i = 0; i < GV_D - 1; ++i) issue(i, c_begin + i);
+    // the weights are never written by a kernel that lets its dependents start
+    // early, so their first copies are issued before the wait; the activations
+    // (and y) are touched only after it
+    tc::pdl_wait();
     uint4 xn[MT][2];
     if (c_begin < c_end) load_x(xn, c_begin);
 
@@ -386,6 +391,7 @@ __global__ void __launch_bounds__(256, 2) k_w4_gemv2(const __nv_bfloat16* __rest
                                                      const uint8_t* __restrict__ blob, qlin_w4_header h, int64_t M,
                                                      __nv_bfloat16* __restrict__ y) {
     extern __shared__ __align__(16) uint8_t gv_smem[];
+    tc::pdl_launch_dependents();
     constexpr int SB = gemv2_stage_bytes<NT>();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int gq = lane >> 2, t = lane & 3;
@@ -507,6 +513,8 @@ __global__ void __launch_bounds__(256, 2) k_w4_gemv2(const __nv_bfloat16* __rest
 
 #pragma unroll
     for (int i = 0; i < GV_P - 1; ++i) issue();
+    // weights before the wait, activations (and y) after it (see k_w4_gemv)
+    tc::pdl_wait();
 
     if (MT == 1) {
         // activations one step ahead, double-buffered by a 2x unrolled loop
@@ -552,6 +560,25 @@ __global__ void __launch_bounds__(256, 2) k_w4_gemv2(const __nv_bfloat16* __rest
     }
 }
 
+// Launch with programmatic stream serialization: the kernel may start while
+// the previous kernel of the stream finishes (it waits with griddepcontrol
+// before touching anything that kernel can write).
+template <typename... KArgs, typename... Args>
+static cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                              Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, args...);
+}
+
 template <int MT, int NT, bool G128>
 static cudaError_t launch_gemv2(const __nv_bfloat16* x, const uint8_t* blob, const qlin_w4_header& h, int64_t M,
                                 __nv_bfloat16* y, cudaStream_t st) {
@@ -559,8 +586,8 @@ static cudaError_t launch_gemv2(const __nv_bfloat16* x, const uint8_t* blob, con
     static_assert(smem >= 8 * NT * 16 * 16 * 4, "reduction tile must fit in the ring");
     cudaError_t e = ensure_smem((const void*)k_w4_gemv2<MT, NT, G128>, smem);
     if (e != cudaSuccess) return e;
-    k_w4_gemv2<MT, NT, G128><<<(unsigned)(h.N / (16 * NT)), 256, smem, st>>>(x, blob, h, M, y);
-    return cudaGetLastError();
+    return launch_pdl(k_w4_gemv2<MT, NT, G128>, dim3((unsigned)(h.N / (16 * NT))), dim3(256), smem, st, x, blob, h, M,
+                      y);
 }
 
 template <int MT, int NT>
@@ -576,8 +603,7 @@ static cudaError_t launch_gemv(const __nv_bfloat16* x, const uint8_t* blob, cons
     constexpr int smem = gemv_smem_bytes<NT>();
     cudaError_t e = ensure_smem((const void*)k_w4_gemv<MT, NT>, smem);
     if (e != cudaSuccess) return e;
-    k_w4_gemv<MT, NT><<<(unsigned)(h.N / (16 * NT)), 256, smem, st>>>(x, blob, h, M, y);
-    return cudaGetLastError();
+    return launch_pdl(k_w4_gemv<MT, NT>, dim3((unsigned)(h.N / (16 * NT))), dim3(256), smem, st, x, blob, h, M, y);
 }
 
 // ------------------------------------------------------------------ GEMM (M > 16), mma.sync
@@ -1210,7 +1236,7 @@ __global__ void __launch_bounds__(w4tm::THREADS, 1) k_w4_gemm_tm(const __grid_co
         };
 #pragma unroll 1
         for (int i = 0; i < CRING - 1; ++i) issue();
-        int s = 0, slot = 0;
+        int s = 0, slot = 0, pend = -1;
         uint32_t ph = 0u;
         for (int st_i = 0; st_i < nst; ++st_i) {
             // With an odd k-block count the second half of the last stage is
@@ -1256,19 +1282,30 @@ __global__ void __launch_bounds__(w4tm::THREADS, 1) k_w4_gemm_tm(const __grid_co
                 st[4 * r + 2] = f[1];  // row g+8
                 st[4 * r + 3] = f[3];
             }
+            // A stage's TMEM store is waited for (and the stage handed to the
+            // MMA warp) only after the next stage is converted, so the store's
+            // latency overlaps that conversion instead of stalling the warp.
+            if (pend >= 0) {
+                tc::tmem_wait_st();
+                tc::tc_fence_before();
+                __syncwarp();
+                if (lane == 0) tc::mbar_arrive(fullA(pend));
+                pend = -1;
+            }
             if (!tc::mbar_wait_warp(emptyA(s), ph ^ 1u, abort_flag)) break;
             tc::tc_fence_after();
-            if (has) {
-                tmem_st_16x256b_x4(tmem + t_lane + A_COL0 + 64u * (uint32_t)s + 32u * (uint32_t)par, st);
-                tc::tmem_wait_st();
-            }
-            tc::tc_fence_before();
-            __syncwarp();
-            if (lane == 0) tc::mbar_arrive(fullA(s));
+            if (has) tmem_st_16x256b_x4(tmem + t_lane + A_COL0 + 64u * (uint32_t)s + 32u * (uint32_t)par, st);
+            pend = s;
             if (++s == SA) {
                 s = 0;
                 ph ^= 1u;
             }
+        }
+        tc::tmem_wait_st();
+        if (pend >= 0) {
+            tc::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) tc::mbar_arrive(fullA(pend));
         }
         cp_async_wait<0>();
     } else if (warp == TMA_WARP) {

@@ -386,5 +386,16 @@ __host__ __device__ constexpr uint32_t idesc_f16(int M, int N, bool bf16) {
 // K-major tile (rows of 128 bytes).
 __device__ __forceinline__ uint32_t sw128_off(uint32_t r, uint32_t c) { return r * 128u + ((c ^ (r & 7u)) << 4); }
 
+// Programmatic dependent launch.  launch_dependents lets the next kernel of
+// the stream, when it was launched with programmatic stream serialization,
+// start before this grid ends (it can launch only once every CTA of this grid
+// has started and passed this point or exited).  wait blocks until the
+// previous grid of the stream has completed and its writes are visible; it
+// returns at once when this kernel was launched without the attribute.
+__device__ __forceinline__ void pdl_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 }  // namespace tc
 }  // namespace qlin

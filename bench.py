@@ -398,6 +398,10 @@ def measure_other_configs(dev, peaks, int8_peak):
         b = R_ * C_ * 2 + q.numel() + s_.numel() * s_.element_size() + (0 if z_ is None else z_.numel() * 4)
         key = "quantize_%s_%s%s" % (code, gran, g if g else "")
         sweep[key] = {"us": t * 1e6, "gbs": b / t / 1e9, "roofline_frac": b / hbm / t}
+        if gran in ("tensor", "col"):
+            # a scope spanning rows needs its statistics before any code: the
+            # input is read twice
+            sweep[key]["roofline_frac_two_reads"] = (b + R_ * C_ * 2) / hbm / t
         if (code, gran) in (("s8", "row"), ("s4", "group")):
             yq = torch.empty((R_, C_), dtype=torch.bfloat16, device=dev)
             nq = -(-ring_bytes // q.numel())
@@ -415,7 +419,8 @@ def measure_other_configs(dev, peaks, int8_peak):
     t = _time_calls(lambda i: qlin.qlin_quantize(xring[i % n_ring], qlin.QLIN_BF16, R_, C_, C_, None, p, q, s_, z_,
                                                  ws, nb, None))
     b = R_ * C_ * 2 + q.numel() + 4
-    sweep["quantize_s8_tensor_p99.9"] = {"us": t * 1e6, "gbs": b / t / 1e9, "roofline_frac": b / hbm / t}
+    sweep["quantize_s8_tensor_p99.9"] = {"us": t * 1e6, "gbs": b / t / 1e9, "roofline_frac": b / hbm / t,
+                                         "roofline_frac_two_reads": (b + R_ * C_ * 2) / hbm / t}
     out["sweep_16384x4096_bf16"] = sweep
     del xring
     out.update(measure_next_rows(dev, peaks, int8_peak))
