@@ -670,7 +670,8 @@ def run_reference(args, world, rank):
 
 # ------------------------------------------------------------------ profiling cases
 PROFILE_CASES = ("w8a8", "w8a8_full", "w4a16_m1", "w4a16_m64", "w4a16_m256", "quantize", "dequantize",
-                 "sweep_row_s8", "sweep_row_u8", "sweep_group128_s8", "sweep_tensor_s8", "sweep_col_s8", "w4a8_m1",
+                 "sweep_row_s8", "sweep_row_u8", "sweep_group128_s8", "sweep_tensor_s8", "sweep_col_s8",
+                 "sweep_col_u8", "sweep_tensor_u8", "sweep_tensorp999_s8", "w4a8_m1",
                  "llmint8", "kv_read")
 
 
@@ -679,11 +680,13 @@ def run_profile_case(name, dev):
     warm-up calls and one measured call, then exit."""
     torch.cuda.set_device(dev)
     if name.startswith("sweep_"):
-        # the 16384 x 4096 sweep tensor: sweep_<gran>[g]_<code>
+        # the 16384 x 4096 sweep tensor: sweep_<gran>[g]_<code>; tensorp999:
+        # per-tensor with the 99.9th-percentile clipping scale
         _, gran, code = name.split("_")
         g = int(gran[5:]) if gran.startswith("group") else 0
+        pct = 99.9 if gran == "tensorp999" else 0.0
         xs = inputs.sweep_tensor().to(dev)
-        p = qlin.make_params(code, "group" if g else gran, group=g)
+        p = qlin.make_params(code, "group" if g else ("tensor" if pct else gran), group=g, percentile=pct)
         fn = lambda: qlin.quantize(xs, p)  # noqa: E731
     elif name == "llmint8":
         x, w, _ = inputs.w8a8_prefill()
