@@ -1006,27 +1006,58 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(w8p::THREADS, 1)
         const int64_t m = mh + 32 * q + lane;
         const int64_t trow = (int64_t)HM * rank + 32 * q + lane;  // row within the tile
         uint32_t ndrain = 0;
+        // this thread's row of the drained sums, staged in the converters' rings
+        // (idle once the final event is posted: every k-block has been
+        // converted and consumed); 16-byte unit u of the row sits at u ^ (lane & 7)
+        uint8_t* const srow = rings + (size_t)(32 * q + lane) * (BN * 4);
+        const uint32_t srow_a = tc::smem_addr(srow);
         for (uint32_t ev = 0;; ++ev) {
             if (!tc::mbar_wait_cluster_warp(ev_bar, ev & 1u, abort_flag, kIdleSleepNs)) break;
             const uint32_t type = misc[1];
-            if (!tc::mbar_wait_warp(acc_full, ev & 1u, abort_flag)) break;
+            // the final event after a drain: fetch the row's drained sums while
+            // the last MMAs finish, instead of one global round trip per 16 columns
+            const bool staged = type == EV_FINAL && ndrain != 0 && m < p.M && n0 + BN <= p.N && dld % 4 == 0;
+            if (staged) {
+                const int32_t* src = dtile + trow * dld;
+#pragma unroll 8
+                for (int u = 0; u < BN / 4; ++u) cp_async16(srow_a + (uint32_t)((u ^ (lane & 7)) << 4), src + 4 * u);
+                cp_async_commit();
+            }
+            if (!tc::mbar_wait_warp(acc_full, ev & 1u, abort_flag)) {
+                cp_async_wait<0>();
+                break;
+            }
             tc::tc_fence_after();
+            if (staged) cp_async_wait<0>();
             if (type != EV_DRAIN && type != EV_FINAL) break;
             const float sxm = (type == EV_FINAL && m < p.M) ? p.sx[m] : 0.0f;
+            // the next 16 columns' TMEM load is in flight while this chunk is
+            // converted and stored
+            uint32_t a[16];
+            tc::tmem_ld16(tmem + lane_base + ACC_COL, a);
             for (int c = 0; c < BN; c += 16) {
                 __syncwarp();
-                uint32_t a[16];
-                tc::tmem_ld16(tmem + lane_base + ACC_COL + c, a);
                 tc::tmem_wait_ld();
                 int tot[16];
 #pragma unroll
                 for (int j = 0; j < 16; ++j) tot[j] = __float2int_rn(__uint_as_float(a[j]));
+                if (c + 16 < BN) tc::tmem_ld16(tmem + lane_base + ACC_COL + c + 16, a);
                 if (m >= p.M) continue;
                 const int64_t nb = n0 + c;
                 if (nb >= p.N) continue;
                 int32_t* dp = dtile + trow * dld + c;
                 const bool full = (nb + 16 <= p.N) && (p.N % 4 == 0);
-                if (ndrain) {
+                if (staged) {
+#pragma unroll
+                    for (int j = 0; j < 16; j += 4) {
+                        const int u = (c + j) >> 2;
+                        const int4 v = *reinterpret_cast<const int4*>(srow + ((u ^ (lane & 7)) << 4));
+                        tot[j] += v.x;
+                        tot[j + 1] += v.y;
+                        tot[j + 2] += v.z;
+                        tot[j + 3] += v.w;
+                    }
+                } else if (ndrain) {
                     if (full) {
 #pragma unroll
                         for (int j = 0; j < 16; j += 4) {
