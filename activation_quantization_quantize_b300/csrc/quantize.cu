@@ -1378,10 +1378,10 @@ __global__ void k_dequant_vec(DequantArgs d) {
 }
 
 // Row-segment path (per-tensor / per-row / per-group with g % 16 == 0,
-// cols % 16 == 0): a CTA takes one unit of kDqUnroll * 256 chunks of 16 codes
-// (one segment of a long row, or several whole short rows) and issues all of
-// its loads, codes and scales, before converting, so each thread keeps
-// kDqUnroll loads in flight.  Same arithmetic as k_dequant_vec.
+// cols % 16 == 0): a CTA takes one segment of kDqUnroll * 256 chunks of 16
+// codes of one row and issues all of its loads before converting, so each
+// thread keeps kDqUnroll loads in flight; the row and segment come from one
+// division per CTA iteration.  Same arithmetic as k_dequant_vec.
 constexpr int kDqUnroll = 4;
 
 __device__ __forceinline__ void store16_y(const DequantArgs& d, int64_t base, const float (&o)[16]) {
@@ -1414,33 +1414,94 @@ __global__ void __launch_bounds__(256) k_dequant_rows(DequantArgs d) {
     const int tid = threadIdx.x, nt = blockDim.x;
     const int64_t nch = d.cols / 16;
     const int64_t seg_len = (int64_t)kDqUnroll * nt;
-    // Short rows whose chunk count divides a segment: a unit is seg_len / nch
-    // whole rows, and chunk u of this thread sits at a fixed (row offset,
-    // column) in every unit, so the thread keeps kDqUnroll loads in flight.
-    // Longer rows: a unit is one segment of one row.
-    const bool multi = nch > 0 && nch <= seg_len && seg_len % nch == 0;
-    const int64_t rows_per_unit = multi ? seg_len / nch : 1;
-    const int64_t nseg = multi ? 1 : (nch + seg_len - 1) / seg_len;
-    const int64_t units = multi ? (d.rows + rows_per_unit - 1) / rows_per_unit : d.rows * nseg;
+    const int64_t nseg = (nch + seg_len - 1) / seg_len;
+    const int64_t units = d.rows * nseg;
+    for (int64_t unit = blockIdx.x; unit < units; unit += gridDim.x) {
+        const int64_t r = unit / nseg, c0 = (unit - r * nseg) * seg_len + tid;
+        uint4 raw[kDqUnroll];
+#pragma unroll
+        for (int u = 0; u < kDqUnroll; ++u) {
+            const int64_t c = c0 + (int64_t)u * nt;
+            if (c < nch) {
+                if (d.code4) {
+                    const uint2 w = reinterpret_cast<const uint2*>(reinterpret_cast<const uint8_t*>(d.q) + r * (d.cols / 2))[c];
+                    raw[u] = make_uint4(w.x, w.y, 0, 0);
+                } else {
+                    raw[u] = reinterpret_cast<const uint4*>(reinterpret_cast<const uint8_t*>(d.q) + r * d.cols)[c];
+                }
+            }
+        }
+        const bool row_scope = d.gran != QLIN_PER_GROUP;
+        float s_row = 0.0f;
+        int z_row = 0;
+        if (row_scope) {
+            const int64_t sc = (d.gran == QLIN_PER_TENSOR) ? 0 : r;
+            s_row = load_scale(d.s, sc, d.scale_f16);
+            z_row = d.z ? d.z[sc] : 0;
+        }
+#pragma unroll
+        for (int u = 0; u < kDqUnroll; ++u) {
+            const int64_t c = c0 + (int64_t)u * nt;
+            if (c >= nch) break;
+            float s = s_row;
+            int z = z_row;
+            if (!row_scope) {
+                const int64_t sc = r * (d.cols / d.group) + (c * 16) / d.group;
+                s = load_scale(d.s, sc, d.scale_f16);
+                z = d.z ? d.z[sc] : 0;
+            }
+            int code[16];
+            if (d.code4) {
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    const int v = (((j < 8) ? raw[u].x : raw[u].y) >> (4 * (j & 7))) & 0xF;
+                    code[j] = (d.code_signed && v >= 8) ? v - 16 : v;
+                }
+            } else {
+                const uint32_t wv[4] = {raw[u].x, raw[u].y, raw[u].z, raw[u].w};
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    const uint32_t b = (wv[j >> 2] >> (8 * (j & 3))) & 0xFFu;
+                    code[j] = d.code_signed ? (int)(int8_t)b : (int)b;
+                }
+            }
+            float o[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) o[j] = s * (float)(code[j] - z);
+            store16_y(d, r * d.cols + c * 16, o);
+        }
+    }
+}
+
+// Short rows (row-segment conditions, and a row's chunk count divides
+// kDqUnroll * 256): a CTA takes a unit of several whole rows, so each thread
+// keeps kDqUnroll code and scale loads in flight where k_dequant_rows would
+// have one.  Same arithmetic as k_dequant_vec.
+__global__ void __launch_bounds__(256) k_dequant_short(DequantArgs d) {
+    const int tid = threadIdx.x, nt = blockDim.x;
+    const int64_t nch = d.cols / 16;
+    const int64_t rows_per_unit = (int64_t)kDqUnroll * nt / nch;
+    const int64_t units = (d.rows + rows_per_unit - 1) / rows_per_unit;
+    // chunk u of this thread: row offset roff[u], chunk column coff[u] of every unit
     int roff[kDqUnroll];
-    int64_t coff[kDqUnroll];
+    int coff[kDqUnroll];
 #pragma unroll
     for (int u = 0; u < kDqUnroll; ++u) {
-        const int64_t f = tid + (int64_t)u * nt;
-        roff[u] = multi ? (int)(f / nch) : 0;
-        coff[u] = multi ? f % nch : f;
+        const int f = tid + u * nt;
+        roff[u] = (int)(f / nch);
+        coff[u] = (int)(f % nch);
     }
     const bool row_scope = d.gran != QLIN_PER_GROUP;
     for (int64_t unit = blockIdx.x; unit < units; unit += gridDim.x) {
-        const int64_t r0 = multi ? unit * rows_per_unit : unit / nseg;
-        const int64_t cbase = multi ? 0 : (unit - r0 * nseg) * seg_len;
+        const int64_t r0 = unit * rows_per_unit;
         uint4 raw[kDqUnroll];
         float sv[kDqUnroll];
         int zv[kDqUnroll];
 #pragma unroll
         for (int u = 0; u < kDqUnroll; ++u) {
-            const int64_t r = r0 + roff[u], c = cbase + coff[u];
-            if (c < nch && r < d.rows) {
+            const int64_t r = r0 + roff[u];
+            const int64_t c = coff[u];
+            if (r < d.rows) {
                 if (d.code4) {
                     const uint2 w = reinterpret_cast<const uint2*>(reinterpret_cast<const uint8_t*>(d.q) + r * (d.cols / 2))[c];
                     raw[u] = make_uint4(w.x, w.y, 0, 0);
@@ -1455,8 +1516,9 @@ __global__ void __launch_bounds__(256) k_dequant_rows(DequantArgs d) {
         }
 #pragma unroll
         for (int u = 0; u < kDqUnroll; ++u) {
-            const int64_t r = r0 + roff[u], c = cbase + coff[u];
-            if (c >= nch || r >= d.rows) continue;
+            const int64_t r = r0 + roff[u];
+            const int64_t c = coff[u];
+            if (r >= d.rows) continue;
             const float s = sv[u];
             const int z = zv[u];
             int code[16];
@@ -1993,7 +2055,10 @@ cudaError_t run_dequantize(const void* q, const void* s, const int32_t* z, const
     const bool seg16 = (cols % 16 == 0) && (p->gran != QLIN_PER_COL) &&
                         (p->gran != QLIN_PER_GROUP || p->group % 16 == 0) &&
                         ((uintptr_t)q % (d.code4 ? 8 : 16) == 0) && ((uintptr_t)y % 16 == 0);
-    if (seg16)
+    const int64_t nch16 = cols / 16, seg = (int64_t)kDqUnroll * 256;
+    if (seg16 && nch16 > 0 && nch16 <= seg && seg % nch16 == 0)
+        k_dequant_short<<<blocks, 256, 0, st>>>(d);
+    else if (seg16)
         k_dequant_rows<<<blocks, 256, 0, st>>>(d);
     else if (vec)
         k_dequant_vec<<<blocks, 256, 0, st>>>(d);

@@ -76,7 +76,7 @@ W8A8_TRAFFIC_BYTES = 1099.9e6 + 61.1e6
 W8A8_TRAFFIC_SOURCES = ("activation_quantization_quantize_b300/csrc/gemm_w8a8.cu",
                         "activation_quantization_quantize_b300/csrc/tc_ptx.cuh",
                         "activation_quantization_quantize_b300/csrc/qlin_common.cuh")
-W8A8_TRAFFIC_DIGEST = "6a277da1499a7dba"
+W8A8_TRAFFIC_DIGEST = "3821cbb4ea6e29e4"
 
 
 def w8a8_traffic_bytes():
