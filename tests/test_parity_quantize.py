@@ -133,6 +133,27 @@ def test_quantize_unaligned_rows_generic_path():
         np.testing.assert_array_equal(scales_f32(s).view(np.uint32), so.view(np.uint32))
 
 
+@pytest.mark.parametrize("shape", [(37, 1024), (300, 4096)])
+def test_quantize_aligned_strided_rows(shape):
+    """A 16-byte-aligned view with ld > cols takes the vector kernels (strip,
+    row-streaming, percentile): every scope against the oracle on the
+    contiguous copy."""
+    rows, cols = shape
+    base = torch.from_numpy(inputs.normal((rows, cols + 64), 1.0, rows + 3)).to(torch.bfloat16).cuda()
+    xd = base[:, 32:32 + cols]                               # ld = cols + 64, 64-byte offset
+    xh = np.ascontiguousarray(host_f32(xd))
+    cases = [("s8", "tensor", 0, 0.0), ("u8", "tensor", 0, 0.0), ("s4", "tensor", 0, 0.0), ("s8", "col", 0, 0.0),
+             ("u8", "col", 0, 0.0), ("s8", "row", 0, 0.0), ("u4", "group", 64, 0.0), ("s8", "tensor", 0, 99.9)]
+    for code, gran, group, pct in cases:
+        p = qlin.make_params(code, gran, group=group, percentile=pct)
+        q, s, z = qlin.quantize(xd, p)
+        qo, so, zo = oracle_quantize(xh, p)
+        np.testing.assert_array_equal(codes_to_int(q, p, rows, cols), qo)
+        np.testing.assert_array_equal(scales_f32(s).view(np.uint32), so.view(np.uint32))
+        if not p.symmetric:
+            np.testing.assert_array_equal(z.cpu().numpy(), zo)
+
+
 def test_exhaustive_bf16_static_scales():
     """Every finite bf16 value against the oracle at a set of scales and zero
     points (the code decision near half-integers)."""
@@ -172,7 +193,7 @@ def test_near_ties_binary32():
         np.testing.assert_array_equal(codes_to_int(q, p, *x.shape), qo)
 
 
-@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("dtype", ["bf16", "f16", "f32"])
 def test_percentile_per_tensor(dtype):
     xd, xh = make_x(200, 1024, seed=51, dtype=dtype)
     run_case(xd, xh, qlin.make_params("s8", "tensor", percentile=99.9))
