@@ -576,6 +576,179 @@ __global__ void __launch_bounds__(NT) k_qrow_bulk(QuantArgs a, uint32_t buf_stri
     }
 }
 
+// k_qrow_bulk with the row held in registers: each thread copies its chunks
+// of the row (at most NC of them) out of the row buffer, so the buffer is free
+// -- and thread 0 starts the copy of a later row into it -- as soon as the
+// CTA has passed one barrier, which is also the barrier of the per-row
+// maximum.  One barrier per row; the reduction slots alternate between two
+// sets by row parity, so a fast thread writing the next row's slot never
+// overwrites one that a slow thread still reads.  Chunk c of a per-row scope
+// sits in slot (c - tid) / NT; per-group scopes (GL > 0) take the chunk
+// assignment of k_qrow_bulk, iteration `it` of its group loop in slots
+// it * CPT ... it * CPT + CPT - 1.  Rows of more than NC * NT chunks take
+// k_qrow_bulk.
+template <typename T, bool SYM, bool STATIC, bool CODE4, int NT, int GL, int NC>
+__global__ void __launch_bounds__(NT, NT >= 512 ? 2 : 1) k_qrow_reg(QuantArgs a, uint32_t buf_stride, int nbuf) {
+    constexpr int CPT = GL == 0 ? 1 : (GL < 4 ? GL : 4);
+    constexpr int LPG = GL == 0 ? 1 : GL / CPT;
+    constexpr int NI = NC / CPT;  // group-loop iterations held (GL > 0)
+    static_assert(NC % CPT == 0, "slots hold whole group iterations");
+    extern __shared__ __align__(128) uint8_t qb_smem[];
+    __shared__ float red_hi[2][NT / 32], red_lo[2][NT / 32];
+    __shared__ __align__(8) uint64_t bar[3];
+    __shared__ int abort_flag;
+    const int tid = threadIdx.x;
+    const uint32_t nchunks = (uint32_t)(a.cols / 8);
+    const uint32_t row_bytes = (uint32_t)(a.cols * 2);
+    const CodeRange cr = make_range(a.qmin, a.qmax);
+    const uint32_t bar0 = tc::smem_addr(&bar[0]);
+    const uint32_t buf0 = tc::smem_addr(qb_smem);
+    const uint8_t* xg = reinterpret_cast<const uint8_t*>(a.x);
+    if (tid == 0) {
+        for (int b = 0; b < nbuf; ++b) tc::mbar_init(bar0 + 8u * b, 1);
+        abort_flag = 0;
+        tc::mbar_init_fence();
+    }
+    __syncthreads();
+    auto issue = [&](int64_t r, int b) {
+        tc::fence_proxy_async_smem();
+        tc::mbar_arrive_expect_tx(bar0 + 8u * b, row_bytes);
+        tc::bulk_load(buf0 + (uint32_t)b * buf_stride, xg + r * a.ld * 2, row_bytes, bar0 + 8u * b);
+    };
+    const bool stalled = tc::producers_stalled();
+    if (tid == 0 && !stalled) {
+        for (int b = 0; b < nbuf; ++b)
+            if (blockIdx.x + (int64_t)b * gridDim.x < a.rows) issue(blockIdx.x + (int64_t)b * gridDim.x, b);
+    }
+    const int64_t qld = CODE4 ? a.cols / 2 : a.cols;
+    float s_t = 0.0f;
+    int z_t = 0;
+    if (STATIC && GL == 0 && a.gran == QLIN_PER_TENSOR) {
+        const ScopeOf o = scope_in(a, 0, blockIdx.x == 0 && tid == 0);
+        s_t = o.s;
+        z_t = o.z;
+    }
+    // chunk index of slot i (>= nchunks: no chunk)
+    auto chunk_of = [&](int i) -> uint32_t {
+        if constexpr (GL == 0) {
+            return (uint32_t)tid + (uint32_t)NT * (uint32_t)i;
+        } else {
+            const uint32_t gidx = (uint32_t)(i / CPT) * (uint32_t)(NT / LPG) + (uint32_t)tid / LPG;
+            return gidx * GL + (uint32_t)tid % LPG + (uint32_t)LPG * (uint32_t)(i % CPT);
+        }
+    };
+    int b = 0, par = 0;
+    uint32_t ph = 0;
+    for (int64_t r = blockIdx.x; r < a.rows; r += gridDim.x) {
+        const bool ok = tc::mbar_wait(bar0 + 8u * b, ph, &abort_flag);
+        const uint4* xs16 = reinterpret_cast<const uint4*>(qb_smem + (size_t)b * buf_stride);
+        uint4 raw[NC];
+#pragma unroll
+        for (int i = 0; i < NC; ++i) {
+            const uint32_t c = chunk_of(i);
+            raw[i] = (ok && c < nchunks) ? xs16[c] : make_uint4(0, 0, 0, 0);
+        }
+        if (GL == 0 && !STATIC) {
+            // zero padding: the range of a scope always includes 0
+            PairRange<T> pr;
+#pragma unroll
+            for (int i = 0; i < NC; ++i) pr.add(raw[i], SYM);
+            float hi, lo;
+            pr.result(SYM, hi, lo);
+            hi = warp_max(hi);
+            if (!SYM) lo = warp_min(lo);
+            if ((tid & 31) == 0) {
+                red_hi[par][tid >> 5] = hi;
+                red_lo[par][tid >> 5] = lo;
+            }
+        }
+        if (!__syncthreads_and(ok)) break;
+        // every thread holds its chunks: buffer b is free
+        if (tid == 0 && !stalled && r + (int64_t)nbuf * gridDim.x < a.rows) issue(r + (int64_t)nbuf * gridDim.x, b);
+        uint8_t* qrow = reinterpret_cast<uint8_t*>(a.q) + r * qld;
+        if constexpr (GL == 0) {
+            float s;
+            int z;
+            if (STATIC) {
+                if (a.gran == QLIN_PER_TENSOR) {
+                    s = s_t;
+                    z = z_t;
+                } else {
+                    s = load_scale(a.s, r, a.scale_f16);
+                    z = a.z ? a.z[r] : 0;
+                }
+            } else {
+                float hi = red_hi[par][0], lo = red_lo[par][0];
+#pragma unroll
+                for (int w = 1; w < NT / 32; ++w) {
+                    hi = fmaxf(hi, red_hi[par][w]);
+                    if (!SYM) lo = fminf(lo, red_lo[par][w]);
+                }
+                scale_zero(lo, hi, a.qmin, a.qmax, SYM, a.scale_f16, s, z);
+                if (tid == 0) {
+                    store_scale(a.s, r, a.scale_f16, s);
+                    if (!SYM) a.z[r] = z;
+                }
+            }
+            const ScopeParams sp = make_scope(s, z);
+#pragma unroll
+            for (int i = 0; i < NC; ++i) {
+                const uint32_t c = chunk_of(i);
+                if (c < nchunks) {
+                    uint32_t cb[8];
+                    codes_of_chunk<T, SYM, STATIC, false>(raw[i], sp, cr, cb);
+                    put_codes8<CODE4>(qrow, c, cb);
+                }
+            }
+        } else {
+            const uint32_t ngr = (uint32_t)(a.cols / a.group);
+#pragma unroll
+            for (int it = 0; it < NI; ++it) {
+                const uint32_t gidx = (uint32_t)it * (uint32_t)(NT / LPG) + (uint32_t)tid / LPG;
+                const bool live = gidx < ngr;  // a group's lanes are all live or all idle
+                if (it > 0 && (uint32_t)it * (uint32_t)(NT / LPG) >= ngr) break;  // CTA-uniform
+                const int64_t sc = r * ngr + gidx;
+                float s;
+                int z;
+                if (STATIC) {
+                    s = live ? load_scale(a.s, sc, a.scale_f16) : 1.0f;
+                    z = (a.z && live) ? a.z[sc] : 0;
+                } else {
+                    PairRange<T> pr;
+#pragma unroll
+                    for (int j = 0; j < CPT; ++j) pr.add(raw[it * CPT + j], SYM);
+                    float hi, lo;
+                    pr.result(SYM, hi, lo);
+#pragma unroll
+                    for (int o = 1; o < LPG; o <<= 1) {
+                        hi = fmaxf(hi, __shfl_xor_sync(0xffffffffu, hi, o));
+                        if (!SYM) lo = fminf(lo, __shfl_xor_sync(0xffffffffu, lo, o));
+                    }
+                    scale_zero(lo, hi, a.qmin, a.qmax, SYM, a.scale_f16, s, z);
+                    if (live && tid % LPG == 0) {
+                        store_scale(a.s, sc, a.scale_f16, s);
+                        if (!SYM) a.z[sc] = z;
+                    }
+                }
+                if (live) {
+                    const ScopeParams sp = make_scope(s, z);
+#pragma unroll
+                    for (int j = 0; j < CPT; ++j) {
+                        uint32_t cb[8];
+                        codes_of_chunk<T, SYM, STATIC, false>(raw[it * CPT + j], sp, cr, cb);
+                        put_codes8<CODE4>(qrow, chunk_of(it * CPT + j), cb);
+                    }
+                }
+            }
+        }
+        par ^= 1;
+        if (++b == nbuf) {
+            b = 0;
+            ph ^= 1u;
+        }
+    }
+}
+
 // Per-row scopes of 16-bit rows of at most 32 * NC eight-value chunks: one
 // warp per row, the row held in registers (lane l holds chunks l, l + 32,
 // ...), every reduction a register shuffle, many warps per SM in flight.
@@ -1666,9 +1839,20 @@ static cudaError_t launch_qrow_warp(const QuantArgs& a, cudaStream_t st) {
 // up to 28,672 16-bit values; longer rows take one CTA with three buffers.
 constexpr size_t kSmemPerSM = 233472;
 
+static int qrow_choice();
+
 template <typename T, bool SYM, bool STATIC, bool CODE4, int NT, int GL>
 static cudaError_t launch_qrow_bulk_k(const QuantArgs& a, uint32_t buf_stride, cudaStream_t st) {
+    // rows of up to NC * NT chunks are held in registers (k_qrow_reg), except
+    // per-group scopes at 512 threads: there the 64-register cap of two CTAs
+    // per SM spills, and the row-buffer kernel is faster (measured on
+    // 4096 x 28672 bf16 at g = 128: 78 us against 92 us)
+    constexpr int NC = NT >= 512 ? 8 : 4;
+    constexpr bool kReg = NT < 512 || GL == 0;
+    const bool reg = kReg && a.cols / 8 <= (int64_t)NC * NT && qrow_choice() != 2;
     const void* kern = (const void*)k_qrow_bulk<T, SYM, STATIC, CODE4, NT, GL>;
+    if constexpr (kReg)
+        if (reg) kern = (const void*)k_qrow_reg<T, SYM, STATIC, CODE4, NT, GL, NC>;
     int nbuf, smem;
     int64_t grid;
     if (NT == 512) {
@@ -1688,6 +1872,12 @@ static cudaError_t launch_qrow_bulk_k(const QuantArgs& a, uint32_t buf_stride, c
         grid = (int64_t)num_sms() * (per_sm > 0 ? per_sm : 1);
     }
     if (grid > a.rows) grid = a.rows;
+    if constexpr (kReg) {
+        if (reg) {
+            k_qrow_reg<T, SYM, STATIC, CODE4, NT, GL, NC><<<(unsigned)grid, NT, smem, st>>>(a, buf_stride, nbuf);
+            return cudaGetLastError();
+        }
+    }
     k_qrow_bulk<T, SYM, STATIC, CODE4, NT, GL><<<(unsigned)grid, NT, smem, st>>>(a, buf_stride, nbuf);
     return cudaGetLastError();
 }
@@ -1817,11 +2007,14 @@ static int blocks_per_sm(const void* kern, int nt, size_t smem) {
 }
 
 // QLIN_QROW: "warp" keeps the register-resident row kernels (per-row rows of
-// up to 4096 values, per-group slabs) for comparisons; read on every call,
-// same codes.
+// up to 4096 values, per-group slabs) and "smem" the row-streaming kernel
+// that reads its chunks from the row buffer (k_qrow_bulk) for comparisons;
+// read on every call, same codes.
 static int qrow_choice() {
     const char* e = getenv("QLIN_QROW");
-    return (e && strcmp(e, "warp") == 0) ? 1 : 0;
+    if (e && strcmp(e, "warp") == 0) return 1;
+    if (e && strcmp(e, "smem") == 0) return 2;
+    return 0;
 }
 
 static bool strip_ok(const QuantArgs& a, int xt) {

@@ -81,12 +81,22 @@ def test_w4a16_wait_times_out_then_recovers(M):
     assert rel_err_out(host_f32(y), yo) < GEMM_REL_TOL
 
 
-def test_streamed_quantize_wait_times_out_then_recovers():
-    """Per-token rows of 28672 bf16 values stream through shared memory by
-    bulk copies; with the copies held back every CTA's wait runs out."""
-    rows, cols = 300, 28672
-    x = inputs.downproj_activation(rows, outliers=True).cuda()
-    p = qlin.make_params("s8", "row")
+@pytest.mark.parametrize("kernel", ["reg", "smem"])
+@pytest.mark.parametrize("gran", ["row", "group"])
+def test_streamed_quantize_wait_times_out_then_recovers(kernel, gran, monkeypatch):
+    """Per-token rows of 28672 and per-group-128 rows of 4096 bf16 values
+    stream through shared memory by bulk copies (the chunks held in
+    registers, or read from the row buffer); with the copies held back every
+    CTA's wait runs out."""
+    if kernel == "smem":
+        monkeypatch.setenv("QLIN_QROW", "smem")
+    if gran == "row":
+        rows, cols = 300, 28672
+        x = inputs.downproj_activation(rows, outliers=True).cuda()
+    else:
+        rows, cols = 600, 4096
+        x = torch.from_numpy(inputs.normal((rows, cols), 1.0, 5)).to(torch.bfloat16).cuda()
+    p = qlin.make_params("s8", gran, group=128 if gran == "group" else 0)
     with stalled():
         qlin.quantize(x, p)
         assert qlin.qlin_device_error() == qlin.QLIN_ERR_TIMEOUT

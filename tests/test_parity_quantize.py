@@ -61,7 +61,7 @@ def test_quantize_dynamic(dtype, code, gran, shape):
 @pytest.mark.parametrize("dtype", ["bf16", "f16", "f32"])
 @pytest.mark.parametrize("code", CODES)
 @pytest.mark.parametrize("group", [8, 32, 64, 128])
-@pytest.mark.parametrize("shape", [(3, 128), (17, 384), (64, 4096), (2, 28672)])
+@pytest.mark.parametrize("shape", [(3, 128), (17, 384), (64, 4096), (5, 6144), (2, 28672), (3, 40960)])
 def test_quantize_groups(dtype, code, group, shape):
     rows, cols = shape
     if cols % group:
@@ -205,10 +205,12 @@ def test_percentile_per_tensor(dtype):
 
 @pytest.mark.parametrize("dtype", ["bf16", "f16"])
 @pytest.mark.parametrize("code", CODES)
-@pytest.mark.parametrize("shape", [(1, 4104), (300, 28672), (517, 8200)])
+@pytest.mark.parametrize("shape", [(1, 4104), (300, 28672), (517, 8200), (3, 40960)])
 def test_quantize_per_token_long_rows(dtype, code, shape):
     """Per-token scopes of rows longer than 4096 16-bit values: the rows are
-    streamed through shared memory (several rows per CTA when rows > SMs)."""
+    streamed through shared memory (several rows per CTA when rows > SMs),
+    held in registers up to 32,768 values and read from the row buffer
+    beyond."""
     rows, cols = shape
     xd, xh = make_x(rows, cols, seed=rows + cols, dtype=dtype)
     run_case(xd, xh, qlin.make_params(code, "row"))
