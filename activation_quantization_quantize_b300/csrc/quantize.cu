@@ -576,6 +576,43 @@ __global__ void __launch_bounds__(NT) k_qrow_bulk(QuantArgs a, uint32_t buf_stri
     }
 }
 
+// Maximum / minimum of NW per-warp slots in shared memory (16-byte aligned),
+// read four at a time when NW is a multiple of 4.
+template <int NW>
+__device__ __forceinline__ float slots_max(const float* p) {
+    if constexpr (NW % 4 == 0) {
+        float m = -INFINITY;
+#pragma unroll
+        for (int i = 0; i < NW / 4; ++i) {
+            const float4 q = reinterpret_cast<const float4*>(p)[i];
+            m = fmaxf(m, fmaxf(fmaxf(q.x, q.y), fmaxf(q.z, q.w)));
+        }
+        return m;
+    } else {
+        float m = p[0];
+#pragma unroll
+        for (int i = 1; i < NW; ++i) m = fmaxf(m, p[i]);
+        return m;
+    }
+}
+template <int NW>
+__device__ __forceinline__ float slots_min(const float* p) {
+    if constexpr (NW % 4 == 0) {
+        float m = INFINITY;
+#pragma unroll
+        for (int i = 0; i < NW / 4; ++i) {
+            const float4 q = reinterpret_cast<const float4*>(p)[i];
+            m = fminf(m, fminf(fminf(q.x, q.y), fminf(q.z, q.w)));
+        }
+        return m;
+    } else {
+        float m = p[0];
+#pragma unroll
+        for (int i = 1; i < NW; ++i) m = fminf(m, p[i]);
+        return m;
+    }
+}
+
 // k_qrow_bulk with the row held in registers: each thread copies its chunks
 // of the row (at most NC of them) out of the row buffer, so the buffer is free
 // -- and thread 0 starts the copy of a later row into it -- as soon as the
@@ -594,7 +631,8 @@ __global__ void __launch_bounds__(NT, NT >= 512 ? 2 : 1) k_qrow_reg(QuantArgs a,
     constexpr int NI = NC / CPT;  // group-loop iterations held (GL > 0)
     static_assert(NC % CPT == 0, "slots hold whole group iterations");
     extern __shared__ __align__(128) uint8_t qb_smem[];
-    __shared__ float red_hi[2][NT / 32], red_lo[2][NT / 32];
+    __shared__ __align__(16) float red_hi[2][NT / 32];
+    __shared__ __align__(16) float red_lo[2][NT / 32];
     __shared__ __align__(8) uint64_t bar[3];
     __shared__ int abort_flag;
     const int tid = threadIdx.x;
@@ -678,12 +716,8 @@ __global__ void __launch_bounds__(NT, NT >= 512 ? 2 : 1) k_qrow_reg(QuantArgs a,
                     z = a.z ? a.z[r] : 0;
                 }
             } else {
-                float hi = red_hi[par][0], lo = red_lo[par][0];
-#pragma unroll
-                for (int w = 1; w < NT / 32; ++w) {
-                    hi = fmaxf(hi, red_hi[par][w]);
-                    if (!SYM) lo = fminf(lo, red_lo[par][w]);
-                }
+                const float hi = slots_max<NT / 32>(red_hi[par]);
+                const float lo = SYM ? 0.0f : slots_min<NT / 32>(red_lo[par]);
                 scale_zero(lo, hi, a.qmin, a.qmax, SYM, a.scale_f16, s, z);
                 if (tid == 0) {
                     store_scale(a.s, r, a.scale_f16, s);
@@ -1843,12 +1877,16 @@ static int qrow_choice();
 
 template <typename T, bool SYM, bool STATIC, bool CODE4, int NT, int GL>
 static cudaError_t launch_qrow_bulk_k(const QuantArgs& a, uint32_t buf_stride, cudaStream_t st) {
-    // rows of up to NC * NT chunks are held in registers (k_qrow_reg), except
-    // per-group scopes at 512 threads: there the 64-register cap of two CTAs
-    // per SM spills, and the row-buffer kernel is faster (measured on
-    // 4096 x 28672 bf16 at g = 128: 78 us against 92 us)
+    // rows of up to NC * NT chunks are held in registers (k_qrow_reg) at 128
+    // threads and for per-row scopes at 512 threads; per-group scopes at 512
+    // threads take the row-buffer kernel: there the 64-register cap of two
+    // CTAs per SM spills, and the register-held kernel measured slower
+    // (4096 x 28672 bf16 at g = 128: 92 us against 78 us).  Eight chunks a
+    // thread at 64 threads measured slower too (16384 x 4096 per-token INT8
+    // 47.7 us against 41.5 us): its unrolled copies of the exact fallback
+    // fill the instruction cache, and out of line the call spills.
     constexpr int NC = NT >= 512 ? 8 : 4;
-    constexpr bool kReg = NT < 512 || GL == 0;
+    constexpr bool kReg = NT == 128 || (NT == 512 && GL == 0);
     const bool reg = kReg && a.cols / 8 <= (int64_t)NC * NT && qrow_choice() != 2;
     const void* kern = (const void*)k_qrow_bulk<T, SYM, STATIC, CODE4, NT, GL>;
     if constexpr (kReg)
@@ -1882,10 +1920,17 @@ static cudaError_t launch_qrow_bulk_k(const QuantArgs& a, uint32_t buf_stride, c
     return cudaGetLastError();
 }
 
-// NT = 512 threads for rows of more than 8192 values, 128 for shorter ones
-// (measured on 16384 x 4096 and 4096 x 28672 bf16).
+// NT = 512 threads for rows of more than 8192 values, 128 for shorter ones;
+// dynamic symmetric per-token INT8 codes of rows of up to 4096 values take
+// the row-buffer kernel at 64 threads, whose smaller CTAs keep more rows in
+// flight per SM (16384 x 4096 bf16: 39.8 us against 41.3 us; the other code
+// widths and scopes measured slower there).  Measured on 16384 x 4096 and
+// 4096 x 28672 bf16.
 template <typename T, bool SYM, bool STATIC, bool CODE4, int GL>
 static cudaError_t launch_qrow_bulk_g(const QuantArgs& a, uint32_t buf_stride, cudaStream_t st) {
+    if constexpr (GL == 0 && SYM && !STATIC && !CODE4) {
+        if (a.cols <= 4096) return launch_qrow_bulk_k<T, SYM, STATIC, CODE4, 64, GL>(a, buf_stride, st);
+    }
     if (a.cols <= 8192) return launch_qrow_bulk_k<T, SYM, STATIC, CODE4, 128, GL>(a, buf_stride, st);
     return launch_qrow_bulk_k<T, SYM, STATIC, CODE4, 512, GL>(a, buf_stride, st);
 }

@@ -82,19 +82,19 @@ def test_w4a16_wait_times_out_then_recovers(M):
 
 
 @pytest.mark.parametrize("kernel", ["reg", "smem"])
-@pytest.mark.parametrize("gran", ["row", "group"])
-def test_streamed_quantize_wait_times_out_then_recovers(kernel, gran, monkeypatch):
-    """Per-token rows of 28672 and per-group-128 rows of 4096 bf16 values
-    stream through shared memory by bulk copies (the chunks held in
-    registers, or read from the row buffer); with the copies held back every
-    CTA's wait runs out."""
+@pytest.mark.parametrize("gran,cols", [("row", 28672), ("row", 4096), ("group", 4096)])
+def test_streamed_quantize_wait_times_out_then_recovers(kernel, gran, cols, monkeypatch):
+    """Per-token rows of 28672 and 4096 and per-group-128 rows of 4096 bf16
+    values stream through shared memory by bulk copies (the chunks held in
+    registers, or read from the row buffer; 512, 64 and 128 threads); with
+    the copies held back every CTA's wait runs out."""
     if kernel == "smem":
         monkeypatch.setenv("QLIN_QROW", "smem")
-    if gran == "row":
-        rows, cols = 300, 28672
+    if cols == 28672:
+        rows = 300
         x = inputs.downproj_activation(rows, outliers=True).cuda()
     else:
-        rows, cols = 600, 4096
+        rows = 600
         x = torch.from_numpy(inputs.normal((rows, cols), 1.0, 5)).to(torch.bfloat16).cuda()
     p = qlin.make_params("s8", gran, group=128 if gran == "group" else 0)
     with stalled():
