@@ -339,6 +339,10 @@ __global__ void __launch_bounds__(512, 2) k_quant_longrows(QuantArgs a) {
 //                  asymmetric scopes (clamp), or static scales (clamp and
 //                  far-range test).
 //   CODE4        : two codes per byte.
+// Per-tensor scopes (GL = 0, gran = QLIN_PER_TENSOR) use one (s, z) for every
+// row: static, or derived from the statistics words of the pass before (the
+// first CTA's thread 0 writes it out); dynamic per-tensor scopes take the
+// dynamic arithmetic, since the tensor's own range bounds every |x / s|.
 
 // Running range of packed 16-bit pairs: |x| max (symmetric) or max and min.
 template <typename T>
@@ -451,10 +455,12 @@ __global__ void __launch_bounds__(NT) k_qrow_bulk(QuantArgs a, uint32_t buf_stri
             if (blockIdx.x + (int64_t)b * gridDim.x < a.rows) issue(blockIdx.x + (int64_t)b * gridDim.x, b);
     }
     const int64_t qld = CODE4 ? a.cols / 2 : a.cols;
-    // per-tensor static scopes (GL = 0): one (s, z) for every row
+    // per-tensor scopes (GL = 0), static or from the statistics pass: one
+    // (s, z) for every row
     float s_t = 0.0f;
     int z_t = 0;
-    if (STATIC && GL == 0 && a.gran == QLIN_PER_TENSOR) {
+    const bool one_scope = GL == 0 && a.gran == QLIN_PER_TENSOR;
+    if (one_scope) {
         const ScopeOf o = scope_in(a, 0, blockIdx.x == 0 && tid == 0);
         s_t = o.s;
         z_t = o.z;
@@ -525,14 +531,12 @@ __global__ void __launch_bounds__(NT) k_qrow_bulk(QuantArgs a, uint32_t buf_stri
         }
         float s;
         int z;
-        if (STATIC) {
-            if (a.gran == QLIN_PER_TENSOR) {
-                s = s_t;
-                z = z_t;
-            } else {
-                s = load_scale(a.s, r, a.scale_f16);
-                z = a.z ? a.z[r] : 0;
-            }
+        if (one_scope) {
+            s = s_t;
+            z = z_t;
+        } else if (STATIC) {
+            s = load_scale(a.s, r, a.scale_f16);
+            z = a.z ? a.z[r] : 0;
         } else {
             PairRange<T> pr;
 #pragma unroll 4
@@ -661,7 +665,8 @@ __global__ void __launch_bounds__(NT, NT >= 512 ? 2 : 1) k_qrow_reg(QuantArgs a,
     const int64_t qld = CODE4 ? a.cols / 2 : a.cols;
     float s_t = 0.0f;
     int z_t = 0;
-    if (STATIC && GL == 0 && a.gran == QLIN_PER_TENSOR) {
+    const bool one_scope = GL == 0 && a.gran == QLIN_PER_TENSOR;
+    if (one_scope) {
         const ScopeOf o = scope_in(a, 0, blockIdx.x == 0 && tid == 0);
         s_t = o.s;
         z_t = o.z;
@@ -686,7 +691,7 @@ __global__ void __launch_bounds__(NT, NT >= 512 ? 2 : 1) k_qrow_reg(QuantArgs a,
             const uint32_t c = chunk_of(i);
             raw[i] = (ok && c < nchunks) ? xs16[c] : make_uint4(0, 0, 0, 0);
         }
-        if (GL == 0 && !STATIC) {
+        if (GL == 0 && !STATIC && !one_scope) {
             // zero padding: the range of a scope always includes 0
             PairRange<T> pr;
 #pragma unroll
@@ -707,14 +712,12 @@ __global__ void __launch_bounds__(NT, NT >= 512 ? 2 : 1) k_qrow_reg(QuantArgs a,
         if constexpr (GL == 0) {
             float s;
             int z;
-            if (STATIC) {
-                if (a.gran == QLIN_PER_TENSOR) {
-                    s = s_t;
-                    z = z_t;
-                } else {
-                    s = load_scale(a.s, r, a.scale_f16);
-                    z = a.z ? a.z[r] : 0;
-                }
+            if (one_scope) {
+                s = s_t;
+                z = z_t;
+            } else if (STATIC) {
+                s = load_scale(a.s, r, a.scale_f16);
+                z = a.z ? a.z[r] : 0;
             } else {
                 const float hi = slots_max<NT / 32>(red_hi[par]);
                 const float lo = SYM ? 0.0f : slots_min<NT / 32>(red_lo[par]);
@@ -2052,13 +2055,15 @@ static int blocks_per_sm(const void* kern, int nt, size_t smem) {
 }
 
 // QLIN_QROW: "warp" keeps the register-resident row kernels (per-row rows of
-// up to 4096 values, per-group slabs) and "smem" the row-streaming kernel
-// that reads its chunks from the row buffer (k_qrow_bulk) for comparisons;
-// read on every call, same codes.
+// up to 4096 values, per-group slabs), "smem" the row-streaming kernel that
+// reads its chunks from the row buffer (k_qrow_bulk), and "strip" the strip
+// kernel for the codes of dynamic symmetric per-tensor scopes, for
+// comparisons; read on every call, same codes.
 static int qrow_choice() {
     const char* e = getenv("QLIN_QROW");
     if (e && strcmp(e, "warp") == 0) return 1;
     if (e && strcmp(e, "smem") == 0) return 2;
+    if (e && strcmp(e, "strip") == 0) return 3;
     return 0;
 }
 
@@ -2144,17 +2149,17 @@ static cudaError_t run_quantize_t(QuantArgs a, int xt, const qlin_qparams* p, vo
     // percentile scales clip values beyond the percentile, and binary16
     // scales can saturate: both take the fully checked codes
     const int mode = (a.static_scale || p->clip_percentile > 0.0 || a.scale_f16) ? 2 : (a.sym ? 0 : 1);
-    // per-tensor codes of unsmoothed 16-bit rows that need the clamp (an
-    // asymmetric, percentile, static or binary16 scale): the row-streaming
-    // kernel with one scope for all rows, which measured faster there
-    // (16384 x 4096 UINT8: 94 against 102 us); dynamic symmetric scopes
-    // (no clamp) measured faster in the strip kernel (INT4: 59 against 68 us)
+    // per-tensor codes of unsmoothed 16-bit rows: the row-streaming kernels
+    // with one scope for all rows.  Dynamic scopes (modes 0 and 1) take the
+    // per-row kernels' arithmetic -- no far-range test, and no clamp for
+    // symmetric codes, since the tensor's own max|x| (or range) bounds every
+    // |x / s| -- and the other scales the fully checked one.
     uint32_t buf_stride = 0;
     bool rowcodes = false;
     if constexpr (!std::is_same<T, float>::value) {
         buf_stride = (uint32_t)(((size_t)a.cols * 2 + 127) & ~(size_t)127);
-        rowcodes = !pc && !smoothed && strip && mode != 0 && a.cols / 8 <= 8 * 512 &&
-                   2 * (size_t)buf_stride <= 200 * 1024;
+        rowcodes = !pc && !smoothed && strip && a.cols / 8 <= 8 * 512 && 2 * (size_t)buf_stride <= 200 * 1024 &&
+                   !(mode == 0 && qrow_choice() == 3);
     }
     if (!a.static_scale) {
         uint32_t* stat = reinterpret_cast<uint32_t*>(ws);
@@ -2199,6 +2204,12 @@ static cudaError_t run_quantize_t(QuantArgs a, int xt, const qlin_qparams* p, vo
     if (a.absmax_out) return cudaGetLastError();
     if (rowcodes) {
         if constexpr (!std::is_same<T, float>::value) {
+            if (mode == 0)
+                return a.code4 ? launch_qrow_bulk_g<T, true, false, true, 0>(a, buf_stride, st)
+                               : launch_qrow_bulk_g<T, true, false, false, 0>(a, buf_stride, st);
+            if (mode == 1)
+                return a.code4 ? launch_qrow_bulk_g<T, false, false, true, 0>(a, buf_stride, st)
+                               : launch_qrow_bulk_g<T, false, false, false, 0>(a, buf_stride, st);
             return a.code4 ? launch_qrow_bulk_g<T, true, true, true, 0>(a, buf_stride, st)
                            : launch_qrow_bulk_g<T, true, true, false, 0>(a, buf_stride, st);
         }
