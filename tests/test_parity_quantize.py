@@ -380,3 +380,50 @@ def test_dequantize_asym_groups_long_rows():
     np.testing.assert_array_equal(codes_to_int(q, p, rows, cols), qo)
     for out in (torch.bfloat16, torch.float32):
         _dequant_check(q, s, z, p, rows, cols, out)
+
+
+@pytest.mark.parametrize("code", ["s8", "u8", "s4", "u4"])
+@pytest.mark.parametrize("cols", [256, 4096, 28672])
+def test_dequantize_every_code(code, cols):
+    """Every bit pattern of the code type (all 256 bytes, all 16 nibbles, the
+    ones outside [qmin, qmax] included) with zero points at both ends of the
+    code range, negative ones for signed codes, and scales from tiny to
+    binary16's largest, through the short-row and long-row dequantize
+    kernels: bit-exact against the oracle's s * (q - z)."""
+    bits = 4 if code in ("s4", "u4") else 8
+    signed = code.startswith("s")
+    allv = np.arange(-(1 << (bits - 1)), 1 << (bits - 1)) if signed else np.arange(0, 1 << bits)
+    zs = [0, int(allv[0]), int(allv[-1]), 3] + ([-5] if signed else [])
+    ss = np.array([0.37, 1e-3, 3.0, 65504.0, 2.0 ** -20], dtype=np.float32)
+    rows = 2 * len(zs) * len(ss)
+    rng = np.random.default_rng(cols + bits)
+    qi = np.empty((rows, cols), dtype=np.int32)
+    for r in range(rows):
+        qi[r] = np.resize(np.roll(allv, r), cols)
+        qi[r, rng.integers(0, cols, 16)] = allv[rng.integers(0, len(allv), 16)]
+    zi = np.array([zs[(r // len(ss)) % len(zs)] for r in range(rows)], dtype=np.int32)
+    sf = np.array([ss[r % len(ss)] for r in range(rows)], dtype=np.float32)
+    if bits == 4:
+        u = (qi & 0xF).astype(np.uint8)
+        packed = (u[:, 0::2] | (u[:, 1::2] << 4)).astype(np.uint8)
+        qd = torch.from_numpy(packed).cuda()
+    else:
+        qd = torch.from_numpy(qi.astype(np.int8 if signed else np.uint8)).cuda()
+    p = qlin.make_params(code, "row", symmetric=False)
+    y = qlin.dequantize(qd, torch.from_numpy(sf).cuda(), torch.from_numpy(zi).cuda(), p, rows, cols,
+                        out_dtype=torch.float32)
+    torch.cuda.synchronize()
+    yo = oracle.dequantize(qi, sf, zi, oracle.PER_ROW)
+    np.testing.assert_array_equal(host_f32(y).view(np.uint32), yo.view(np.uint32))
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+@pytest.mark.parametrize("code", CODES)
+@pytest.mark.parametrize("shape", [(9, 6144), (4, 8192), (17, 8200), (5, 12288)])
+def test_quantize_per_tensor_long_rows(dtype, code, shape):
+    """Dynamic per-tensor scopes on both sides of the routing boundary: rows
+    of up to 8192 values take the row-streaming kernels' one-scope mode,
+    longer rows the strip kernel."""
+    rows, cols = shape
+    xd, xh = make_x(rows, cols, seed=rows * 3 + cols, dtype=dtype)
+    run_case(xd, xh, qlin.make_params(code, "tensor"))
