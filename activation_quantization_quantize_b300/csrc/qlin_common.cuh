@@ -120,13 +120,17 @@ struct ScopeParams {
 };
 
 // Clamp bounds of code_bits() in the 1.5*2^23 + code domain.
+// lo2 / hi2: qmin / qmax in both 16-bit lanes, for clamp_pair16.
 struct CodeRange {
     float lo, hi;
+    uint32_t lo2, hi2;
 };
 __device__ __forceinline__ CodeRange make_range(int qmin, int qmax) {
     CodeRange c;
     c.lo = 12582912.0f + (float)qmin;
     c.hi = 12582912.0f + (float)qmax;
+    c.lo2 = (uint32_t)(uint16_t)qmin * 0x10001u;
+    c.hi2 = (uint32_t)(uint16_t)qmax * 0x10001u;
     return c;
 }
 
@@ -287,9 +291,38 @@ __device__ __noinline__ void code_bits8_exact(float v0, float v1, float v2, floa
 // the clamp to [qmin, qmax]; callers use it only for symmetric scopes whose
 // scale came from the scope's own absmax, where |rne(v/s)| <= qmax always
 // holds.  Same results as code_bits() / code_bits_inrange() per element.
-template <bool kInRange, bool kClamp = true, bool kOutline = false>
+// Two code candidates m0, m1 (bit patterns of 1.5*2^23 + z + n, |z + n| <
+// 2^15) as one word of two 16-bit lanes, each z + n in two's complement (the
+// low 16 bits of the pattern), clamped to [qmin, qmax] lane by lane: the same
+// integers as clamping the binary32 candidates, for one permute and two
+// instructions per pair.
+__device__ __forceinline__ uint32_t clamp_pair16(uint32_t m0, uint32_t m1, const CodeRange& cr) {
+    const uint32_t p = __byte_perm(m0, m1, 0x5410);
+    uint32_t d;
+    asm("max.s16x2 %0, %1, %2;" : "=r"(d) : "r"(p), "r"(cr.lo2));
+    asm("min.s16x2 %0, %1, %2;" : "=r"(d) : "r"(d), "r"(cr.hi2));
+    return d;
+}
+// Eight codes from four clamp_pair16 words: bytes (code j in byte j), or
+// nibbles (element 2i in the low nibble of byte i).
+__device__ __forceinline__ uint2 pack_pairs_bytes(const uint32_t p[4]) {
+    return make_uint2(__byte_perm(p[0], p[1], 0x6420), __byte_perm(p[2], p[3], 0x6420));
+}
+__device__ __forceinline__ uint32_t pack_pairs_nibbles(const uint32_t p[4]) {
+    uint32_t b0 = __byte_perm(p[0], p[1], 0x6420) & 0x0F0F0F0Fu;
+    uint32_t b1 = __byte_perm(p[2], p[3], 0x6420) & 0x0F0F0F0Fu;
+    b0 = b0 | (b0 >> 4);
+    b1 = b1 | (b1 >> 4);
+    return __byte_perm(b0, b1, 0x6420);
+}
+
+// kPairs (with kClamp): cb[0..3] receive the codes as clamp_pair16 words
+// (for pack_pairs_bytes / pack_pairs_nibbles) instead of eight clamped
+// candidates.
+template <bool kInRange, bool kClamp = true, bool kOutline = false, bool kPairs = false>
 __device__ __forceinline__ void code_bits8(const float v[8], const ScopeParams& p, const CodeRange& cr,
                                            uint32_t cb[8]) {
+    static_assert(!kPairs || kClamp, "pair words carry clamped codes");
     float m[8];
     uint32_t neg = 0xFFFFFFFFu;  // AND of the sign bits of the tests
     const float2 r2 = make_float2(p.r, p.r), cz2 = make_float2(p.cz, p.cz), ncz2 = make_float2(-p.cz, -p.cz);
@@ -314,17 +347,30 @@ __device__ __forceinline__ void code_bits8(const float v[8], const ScopeParams& 
         m[2 * j + 1] = m2.y;
     }
     if (neg & 0x80000000u) {
+        if constexpr (kPairs) {
 #pragma unroll
-        for (int j = 0; j < 8; ++j) cb[j] = __float_as_uint(kClamp ? fminf(fmaxf(m[j], cr.lo), cr.hi) : m[j]);
-    } else if (kOutline) {
-        // (code_bits equals code_bits_inrange wherever the latter applies)
-        uint32_t t8[8];
-        code_bits8_exact(v[0], v[1], v[2], v[3], v[4], v[5], v[6], v[7], p, cr, t8);
+            for (int k = 0; k < 4; ++k) cb[k] = clamp_pair16(__float_as_uint(m[2 * k]), __float_as_uint(m[2 * k + 1]), cr);
+        } else {
 #pragma unroll
-        for (int j = 0; j < 8; ++j) cb[j] = t8[j];
+            for (int j = 0; j < 8; ++j) cb[j] = __float_as_uint(kClamp ? fminf(fmaxf(m[j], cr.lo), cr.hi) : m[j]);
+        }
     } else {
+        uint32_t t8[8];
+        if (kOutline) {
+            // (code_bits equals code_bits_inrange wherever the latter applies)
+            code_bits8_exact(v[0], v[1], v[2], v[3], v[4], v[5], v[6], v[7], p, cr, t8);
+        } else {
 #pragma unroll
-        for (int j = 0; j < 8; ++j) cb[j] = kInRange ? code_bits_inrange(v[j], p, cr) : code_bits(v[j], p, cr);
+            for (int j = 0; j < 8; ++j) t8[j] = kInRange ? code_bits_inrange(v[j], p, cr) : code_bits(v[j], p, cr);
+        }
+        if constexpr (kPairs) {
+            // clamped candidates: their low 16 bits are the codes
+#pragma unroll
+            for (int k = 0; k < 4; ++k) cb[k] = __byte_perm(t8[2 * k], t8[2 * k + 1], 0x5410);
+        } else {
+#pragma unroll
+            for (int j = 0; j < 8; ++j) cb[j] = t8[j];
+        }
     }
 }
 

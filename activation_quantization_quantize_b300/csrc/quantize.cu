@@ -412,6 +412,27 @@ __device__ __forceinline__ void codes_of_chunk(const uint4 raw, const ScopeParam
         code_bits8<true, true, OUTLINE>(v, sp, cr, cb);
 }
 
+// Codes of one chunk stored at chunk index c of the code row.  Scopes with a
+// clamp clamp and pack the codes as 16-bit pairs (clamp_pair16); dynamic
+// symmetric scopes need no clamp and pack the candidates directly.
+template <typename T, bool SYM, bool STATIC, bool OUTLINE, bool CODE4>
+__device__ __forceinline__ void quant_chunk(const uint4 raw, const ScopeParams& sp, const CodeRange& cr,
+                                            uint8_t* __restrict__ qrow, uint32_t c) {
+    uint32_t cb[8];
+    if constexpr (STATIC || !SYM) {
+        float v[8];
+        unpack8<T>(raw, v);
+        code_bits8<!STATIC, true, OUTLINE, true>(v, sp, cr, cb);
+        if (CODE4)
+            reinterpret_cast<uint32_t*>(qrow)[c] = pack_pairs_nibbles(cb);
+        else
+            reinterpret_cast<uint2*>(qrow)[c] = pack_pairs_bytes(cb);
+    } else {
+        codes_of_chunk<T, SYM, STATIC, OUTLINE>(raw, sp, cr, cb);
+        put_codes8<CODE4>(qrow, c, cb);
+    }
+}
+
 // Row-local scopes of 16-bit rows streamed through shared memory by bulk
 // copies.  Each persistent CTA keeps `nbuf` row buffers: while it reduces and
 // quantizes one row, the copies of its next rows land in the others.  NT
@@ -517,9 +538,7 @@ __global__ void __launch_bounds__(NT) k_qrow_bulk(QuantArgs a, uint32_t buf_stri
                     const ScopeParams sp = make_scope(s, z);
 #pragma unroll
                     for (int j = 0; j < CPL; ++j) {
-                        uint32_t cb[8];
-                        codes_of_chunk<T, SYM, STATIC, false>(raw[j], sp, cr, cb);
-                        put_codes8<CODE4>(qrow, c0 + LPG * j, cb);
+                        quant_chunk<T, SYM, STATIC, false, CODE4>(raw[j], sp, cr, qrow, c0 + LPG * j);
                     }
                 }
             }
@@ -569,9 +588,7 @@ __global__ void __launch_bounds__(NT) k_qrow_bulk(QuantArgs a, uint32_t buf_stri
         uint8_t* qrow = reinterpret_cast<uint8_t*>(a.q) + r * qld;
 #pragma unroll 4
         for (uint32_t c = tid; c < nchunks; c += NT) {
-            uint32_t cb[8];
-            codes_of_chunk<T, SYM, STATIC, false>(xs16[c], sp, cr, cb);
-            put_codes8<CODE4>(qrow, c, cb);
+            quant_chunk<T, SYM, STATIC, false, CODE4>(xs16[c], sp, cr, qrow, c);
         }
         __syncthreads();  // buffer b and red_* are free
         if (tid == 0 && !stalled && r + (int64_t)nbuf * gridDim.x < a.rows) issue(r + (int64_t)nbuf * gridDim.x, b);
@@ -734,9 +751,7 @@ __global__ void __launch_bounds__(NT, NT >= 512 ? 2 : 1) k_qrow_reg(QuantArgs a,
             for (int i = 0; i < NC; ++i) {
                 const uint32_t c = chunk_of(i);
                 if (c < nchunks) {
-                    uint32_t cb[8];
-                    codes_of_chunk<T, SYM, STATIC, false>(raw[i], sp, cr, cb);
-                    put_codes8<CODE4>(qrow, c, cb);
+                    quant_chunk<T, SYM, STATIC, false, CODE4>(raw[i], sp, cr, qrow, c);
                 }
             }
         } else {
@@ -773,9 +788,8 @@ __global__ void __launch_bounds__(NT, NT >= 512 ? 2 : 1) k_qrow_reg(QuantArgs a,
                     const ScopeParams sp = make_scope(s, z);
 #pragma unroll
                     for (int j = 0; j < CPT; ++j) {
-                        uint32_t cb[8];
-                        codes_of_chunk<T, SYM, STATIC, false>(raw[it * CPT + j], sp, cr, cb);
-                        put_codes8<CODE4>(qrow, chunk_of(it * CPT + j), cb);
+                        quant_chunk<T, SYM, STATIC, false, CODE4>(raw[it * CPT + j], sp, cr, qrow,
+                                                                   chunk_of(it * CPT + j));
                     }
                 }
             }
