@@ -412,9 +412,10 @@ __device__ __noinline__ uint32_t code_bits_outline(float v, ScopeParams p, CodeR
 // code_bits8 with one scope per element (per-column scopes): the same packed
 // fast path with per-lane constants (m - cz is the same operation as
 // m + (-cz)); a chunk that fails takes the exact per-element path out of line.
-template <bool kInRange, bool kClamp>
+template <bool kInRange, bool kClamp, bool kPairs = false>
 __device__ __forceinline__ void code_bits8_cols(const float v[8], const ColPair cp[4], const CodeRange& cr,
                                                 uint32_t cb[8]) {
+    static_assert(!kPairs || kClamp, "pair words carry clamped codes");
     float m[8];
     uint32_t neg = 0xFFFFFFFFu;
     const float2 nlim2 = make_float2(-16777216.0f, -16777216.0f);
@@ -435,11 +436,24 @@ __device__ __forceinline__ void code_bits8_cols(const float v[8], const ColPair 
         m[2 * j + 1] = m2.y;
     }
     if (neg & 0x80000000u) {
+        if constexpr (kPairs) {
 #pragma unroll
-        for (int j = 0; j < 8; ++j) cb[j] = __float_as_uint(kClamp ? fminf(fmaxf(m[j], cr.lo), cr.hi) : m[j]);
+            for (int k = 0; k < 4; ++k) cb[k] = clamp_pair16(__float_as_uint(m[2 * k]), __float_as_uint(m[2 * k + 1]), cr);
+        } else {
+#pragma unroll
+            for (int j = 0; j < 8; ++j) cb[j] = __float_as_uint(kClamp ? fminf(fmaxf(m[j], cr.lo), cr.hi) : m[j]);
+        }
     } else {
+        uint32_t t8[8];
 #pragma unroll
-        for (int j = 0; j < 8; ++j) cb[j] = code_bits_outline(v[j], colpair_scope(cp[j / 2], j & 1), cr);
+        for (int j = 0; j < 8; ++j) t8[j] = code_bits_outline(v[j], colpair_scope(cp[j / 2], j & 1), cr);
+        if constexpr (kPairs) {
+#pragma unroll
+            for (int k = 0; k < 4; ++k) cb[k] = __byte_perm(t8[2 * k], t8[2 * k + 1], 0x5410);
+        } else {
+#pragma unroll
+            for (int j = 0; j < 8; ++j) cb[j] = t8[j];
+        }
     }
 }
 

@@ -1191,17 +1191,25 @@ __global__ void __launch_bounds__(kStripThreads, SMOOTHED ? 2 : (PER_COL ? 3 : 4
             float v[8];
             raw8_widen<T>(c, v);
             if constexpr (SMOOTHED) smooth8(v, a.smooth_mode, a.smooth, st.chunk * 8);
+            // clamped codes as 16-bit pairs (clamp_pair16), except static
+            // per-column scopes, whose far-range test already fills the
+            // registers (the pairs spill there)
+            constexpr bool kP = MODE == 1 || (MODE == 2 && !PER_COL);
             uint32_t cb[8];
             if constexpr (PER_COL)
-                code_bits8_cols<MODE != 2, MODE != 0>(v, cp, cr, cb);
+                code_bits8_cols<MODE != 2, MODE != 0, kP>(v, cp, cr, cb);
             else
-                code_bits8<MODE != 2, MODE != 0, true>(v, sp, cr, cb);
+                code_bits8<MODE != 2, MODE != 0, true, kP>(v, sp, cr, cb);
             if (a.code4) {
-                *reinterpret_cast<uint32_t*>(qp) = pack_nibbles8(cb);
+                *reinterpret_cast<uint32_t*>(qp) = kP ? pack_pairs_nibbles(cb) : pack_nibbles8(cb);
             } else {
                 uint2 w;
-                w.x = pack_bytes4(cb[0], cb[1], cb[2], cb[3]);
-                w.y = pack_bytes4(cb[4], cb[5], cb[6], cb[7]);
+                if constexpr (kP) {
+                    w = pack_pairs_bytes(cb);
+                } else {
+                    w.x = pack_bytes4(cb[0], cb[1], cb[2], cb[3]);
+                    w.y = pack_bytes4(cb[4], cb[5], cb[6], cb[7]);
+                }
                 *reinterpret_cast<uint2*>(qp) = w;
             }
             qp += qstep;
